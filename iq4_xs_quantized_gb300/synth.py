@@ -1,0 +1,98 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests/bench and the oracle.
+
+This module holds none of the method's arithmetic: it draws random bytes and
+random normals and names the workloads.  An IQ4_XS weight matrix is produced
+as raw super-block bytes -- the fp16 ``d`` field is drawn as |N(0,1)| * scale
+and stored at bytes 0-1 of each 136-byte block; every other byte (scales_h,
+scales_l, qs) is uniform, which makes each 6-bit ``ls`` uniform on 0..63 and
+each nibble uniform on 0..15 whatever the bit order inside the block.
+
+Stream order for one matrix: the block ``d`` normals (row-major block order),
+then the other 134 bytes of every block, then the activations.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+QK = 256
+BLOCK_BYTES = 136
+
+
+def iq4xs_weights(rng: np.random.Generator, N: int, K: int, d_scale: float) -> np.ndarray:
+    """Random IQ4_XS matrix [N][K/256] super-blocks as uint8 [N, K/256*136]."""
+    if K % QK:
+        raise ValueError("K must be a multiple of 256")
+    nb = N * (K // QK)
+    d = (np.abs(rng.standard_normal(nb)) * d_scale).astype(np.float16)
+    rest = rng.integers(0, 256, size=(nb, BLOCK_BYTES - 2), dtype=np.uint8)
+    blocks = np.empty((nb, BLOCK_BYTES), dtype=np.uint8)
+    blocks[:, 0:2] = d.view(np.uint8).reshape(nb, 2)  # little-endian fp16 bits
+    blocks[:, 2:] = rest
+    return blocks.reshape(N, (K // QK) * BLOCK_BYTES)
+
+
+def activations(rng: np.random.Generator, M: int, K: int, outlier_frac: float = 0.0,
+                outlier_scale: float = 20.0, bf16_round: bool = False) -> np.ndarray:
+    """x fp32 [M, K] ~ N(0,1).  ``outlier_frac`` of the channels (chosen without
+    replacement, the same for every row) are multiplied by ``outlier_scale``;
+    ``bf16_round`` rounds every value to bfloat16 (RNE) and widens it back."""
+    x = rng.standard_normal((M, K), dtype=np.float32)
+    n_out = int(np.floor(outlier_frac * K))
+    if n_out:
+        ch = rng.choice(K, size=n_out, replace=False)
+        x[:, ch] *= np.float32(outlier_scale)
+    if bf16_round:
+        import torch
+        x = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    return np.ascontiguousarray(x)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic workload: weight shapes, batch sizes and input recipe."""
+    name: str
+    seed: int
+    shapes: tuple          # ((N, K), ...)
+    ms: tuple              # batch sizes M
+    d_scale: float
+    outlier_frac: float = 0.0
+    bf16_round: bool = False
+    layers: int = 1        # >1: the shapes repeat per decoder layer
+
+    def rng(self, shape_index: int = 0, layer: int = 0) -> np.random.Generator:
+        return np.random.default_rng([self.seed, shape_index, layer])
+
+    def weights(self, shape_index: int = 0, layer: int = 0) -> np.ndarray:
+        N, K = self.shapes[shape_index]
+        return iq4xs_weights(self.rng(shape_index, layer), N, K, self.d_scale)
+
+    def inputs(self, shape_index: int = 0, M: int | None = None, layer: int = 0):
+        """(W bytes, x [M,K]) drawn from one stream: W first, then x.  Smaller
+        M are prefixes of the largest one when drawn with M=max(ms)."""
+        N, K = self.shapes[shape_index]
+        rng = self.rng(shape_index, layer)
+        w = iq4xs_weights(rng, N, K, self.d_scale)
+        M = max(self.ms) if M is None else M
+        x = activations(rng, M, K, self.outlier_frac, bf16_round=self.bf16_round)
+        return w, x
+
+
+# Workloads of the method's decode/verify batch range, named by what they are.
+TINY = Workload("tiny_256x1024", seed=0, shapes=((256, 1024),), ms=(1, 4, 8), d_scale=2e-3)
+SQUARE = Workload("square_4096x4096", seed=1, shapes=((4096, 4096),),
+                  ms=(1, 2, 4, 8, 12, 16, 32, 64, 96), d_scale=1e-3)
+DECODER_27B = Workload(
+    "decoder27b_9proj", seed=2,
+    shapes=((5120, 5120), (6144, 5120), (1024, 5120), (10240, 5120), (12288, 5120),
+            (5120, 6144), (17408, 5120), (34816, 5120), (5120, 17408)),
+    ms=(1, 4, 8, 16, 64), d_scale=2e-3, outlier_frac=0.01)
+PREFILL = Workload("prefill_sweep", seed=3, shapes=((17408, 5120), (5120, 17408)),
+                   ms=(96, 128, 192, 256, 512), d_scale=2e-3, bf16_round=True)
+DECODE_STREAM = Workload(
+    "decode_stream_64layers", seed=4,
+    shapes=((12288, 5120), (5120, 6144), (34816, 5120), (5120, 17408)),
+    ms=(1, 2, 8, 16, 32), d_scale=2e-3, layers=64)
+
+WORKLOADS = {w.name: w for w in (TINY, SQUARE, DECODER_27B, PREFILL, DECODE_STREAM)}
