@@ -1,0 +1,442 @@
+#!/usr/bin/env python
+"""IQ4_XS x Q8_1 batched-matmul benchmark on GB300.
+
+Workload (default): the 4096 x 4096 square projection swept over the decode /
+verify batch sizes M = 1, 2, 4, 8, 12, 16, 32, 64, 96.  One step is one pass
+of the hot path over that sweep: for every M, Q8_1-quantize a fresh resident
+activation batch x [M, 4096] and run the batched matmul (path chosen by the
+library's dispatcher) against one of 45 resident copies of W, rotating so the
+streamed weights (401 MB) exceed the 129 MB L2 several times over.  Each
+step is one CUDA-graph replay of those 18 launches.
+
+Metric: whole-job GB/s = algorithmic bytes of the step / step time, where a
+matmul moves 0.53125*N*K (IQ4_XS W) + 1.125*M*K (Q8_1 x) + 4*M*N (y) bytes and
+a quantization 4*M*K in + 1.125*M*K out.  TOPS (2*M*N*K per matmul) and a
+per-M breakdown come alongside.  ``e2e`` repeats the step through the public
+Python/C-ABI calls from pinned host buffers (x copied in, y copied out, every
+step).  ``--impl reference`` times the CPU oracle on a bounded sample of the
+same workload instead.
+
+Under torchrun (N > 1) every rank runs its own replica (the path shards into
+independent problems; no collective is on the data path) and rank 0 prints
+the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "IQ4_XS×Q8_1 matmul GB/s and TOPS vs GB300 roofline, M=1..96"
+UNIT = "GB/s"
+N_COPIES = 45
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "matmul_square4096_traffic.txt")
+KERNEL_SOURCES = ("iq4_xs_quantized_gb300/csrc/matmul_tc.cu",
+                  "iq4_xs_quantized_gb300/csrc/matmul_dp4a.cu",
+                  "iq4_xs_quantized_gb300/csrc/internal.cuh")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ms", default=None,
+                    help="comma-separated subset of the M sweep (profiling runs only)")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- bytes
+def matmul_bytes(M, N, K):
+    return N * (K // 256) * 136 + M * K + M * (K // 32) * 4 + 4 * M * N
+
+
+def quantize_bytes(M, K):
+    return 4 * M * K + M * K + M * (K // 32) * 4
+
+
+def step_bytes(ms, N, K):
+    return sum(matmul_bytes(M, N, K) + quantize_bytes(M, K) for M in ms)
+
+
+def step_ops(ms, N, K):
+    return sum(2 * M * N * K for M in ms)
+
+
+def hbm_peak_gbs():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per matmul launch of the sweep from the committed ncu summary,
+    or None if absent or taken on different kernel sources."""
+    try:
+        vals = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    vals[k.strip()] = v.strip()
+        if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
+        return float(vals["dram_bytes_per_matmul_launch_sweep_avg"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def oracle_sample(rows: int, threads: int):
+    """Time the CPU oracle (as it stands) on the square workload restricted to
+    the first `rows` weight rows, every M of the sweep.  Returns
+    (GB/s, seconds, sample description)."""
+    import oracle
+    from iq4_xs_quantized_gb300 import synth
+    W = synth.SQUARE
+    N, K = W.shapes[0]
+    w, x = W.inputs(0)
+    wr = np.ascontiguousarray(w[:rows])
+    orc = oracle.get()
+    t0 = time.perf_counter()
+    for M in W.ms:
+        qs, d_h, _ = orc.quantize_q8_1(x[:M])
+        orc.matmul(wr, rows, K, qs, d_h, nthreads=threads)
+    dt = time.perf_counter() - t0
+    nbytes = step_bytes(W.ms, rows, K)
+    desc = (f"weight rows 0..{rows - 1} of 4096 (K=4096), all M in {list(W.ms)}, "
+            f"quantize + matmul, {threads} threads")
+    return nbytes / dt / 1e9, dt, desc
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    threads = oracle.threads_available()
+    rows = 256
+    oracle_sample(16, threads)  # build, page in
+    for _ in range(min(args.warmup, 1)):
+        oracle_sample(rows, threads)
+    vals, secs = [], 0.0
+    for _ in range(args.steps):
+        v, dt, desc = oracle_sample(rows, threads)
+        vals.append(v)
+        secs += dt
+        if secs > 120:
+            break
+    value = len(vals) * step_bytes((1, 2, 4, 8, 12, 16, 32, 64, 96), rows, 4096) / secs / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": len(vals), "warmup": args.warmup,
+        "ms_per_step": secs / len(vals) * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32 dot / f64 accumulate (CPU oracle)",
+        "data": "synthetic",
+        "config": {"workload": "square_4096x4096, M=1..96 sweep (quantize + matmul per M)",
+                   "N": 4096, "K": 4096, "ms": [1, 2, 4, 8, 12, 16, 32, 64, 96],
+                   "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- our GPU leg
+def run_ours(args, world, rank, local):
+    import torch
+
+    from iq4_xs_quantized_gb300 import binding as B
+    from iq4_xs_quantized_gb300 import build, synth
+
+    build.build()
+    B.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    W = synth.SQUARE
+    N, K = W.shapes[0]
+    ms = list(W.ms) if not args.ms else [int(v) for v in args.ms.split(",")]
+    w_np, x_np = W.inputs(0, M=max(W.ms))  # W and x [96, K]; smaller M use prefixes
+    wd0 = torch.from_numpy(w_np).to(dev)
+    wcopies = [wd0] + [wd0.clone() for _ in range(N_COPIES - 1)]
+    xs = {M: torch.from_numpy(np.ascontiguousarray(x_np[:M])).to(dev) for M in ms}
+    acts = {M: B.alloc_activations(M, K, dev, tc=True) for M in ms}
+    ys = {M: torch.empty((M, N), dtype=torch.float32, device=dev) for M in ms}
+    paths = {M: B.iq4xs_select_path(M, N, K) for M in ms}
+    variants = N_COPIES // len(ms)
+    stream = torch.cuda.Stream(device=dev)
+
+    def launch_step(v, events=None):
+        for i, M in enumerate(ms):
+            qs, ds, op = acts[M]
+            B.iq4xs_quantize_q8_1(xs[M], qs, ds, op, stream)
+            if events is not None:
+                events[i][0].record(stream)
+            B.iq4xs_matmul(wcopies[v * len(ms) + i], N, K, qs, ds, op, M, ys[M], paths[M], stream)
+            if events is not None:
+                events[i][1].record(stream)
+
+    # Eager warm-up (also performs the library's one-time device set-up).
+    with torch.cuda.stream(stream):
+        for v in range(variants):
+            launch_step(v)
+    torch.cuda.synchronize(dev)
+
+    # One graph per weight-copy variant, with timing events around every matmul.
+    graphs, evs = [], []
+    for v in range(variants):
+        e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in ms]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            launch_step(v, e)
+        graphs.append(g)
+        evs.append(e)
+    torch.cuda.synchronize(dev)
+
+    with torch.cuda.stream(stream):
+        for s in range(max(3, args.warmup)):
+            graphs[s % variants].replay()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.2)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for s in range(args.steps):
+            graphs[s % variants].replay()
+        stop.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    ms_local = start.elapsed_time(stop)
+    ms_total = max_over_ranks(ms_local, world)
+
+    # Per-matmul device time from the in-graph events (last replay of each variant).
+    per_m = []
+    mm_us = {M: statistics.mean(evs[v][i][0].elapsed_time(evs[v][i][1]) * 1e3
+                                for v in range(variants)) for i, M in enumerate(ms)}
+    peak, peak_kind = hbm_peak_gbs()
+    for M in ms:
+        us = mm_us[M]
+        gbs = matmul_bytes(M, N, K) / (us * 1e-6) / 1e9
+        per_m.append({"M": M, "path": {1: "dp4a", 2: "tc"}[paths[M]], "matmul_us": round(us, 3),
+                      "GBps": round(gbs, 1), "TOPS": round(2 * M * N * K / (us * 1e-6) / 1e12, 3),
+                      "hbm_frac": round(gbs / peak, 4)})
+    mm_bytes = sum(matmul_bytes(M, N, K) for M in ms)
+    mm_us_total = sum(mm_us.values())
+    achieved = mm_bytes / (mm_us_total * 1e-6) / 1e9
+    traffic = recorded_traffic()
+
+    sbytes = step_bytes(ms, N, K)
+    ms_per_step = ms_total / args.steps
+    value = world * sbytes / (ms_per_step * 1e-3) / 1e9
+    tops = world * step_ops(ms, N, K) / (ms_per_step * 1e-3) / 1e12
+
+    e2e = run_e2e(args, dev, w_np, x_np, ms, N, K, world, wcopies, paths)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        threads = oracle.threads_available()
+        v, dt, desc = oracle_sample(256, threads)
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+               "seconds": round(dt, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8/fp16-exact integer dots, f32 scale-in",
+            "data": "synthetic",
+            "config": {"workload": "square_4096x4096, M=1..96 sweep (quantize + matmul per M)",
+                       "N": N, "K": K, "ms": ms, "weight_copies": N_COPIES,
+                       "l2": f"inputs larger than L2: {N_COPIES} rotating weight copies "
+                             f"({N_COPIES * N * K * 17 // 32 / 1e6:.0f} MB)",
+                       "graph": "one CUDA graph replay per step",
+                       "parallelism": f"replicas x{world}"},
+            "tops": tops,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "iq4xs matmul (dp4a for M<=crossover, tcgen05 above), "
+                                   "sweep aggregate", "peak_kind": peak_kind},
+            "per_m": per_m,
+            "e2e": e2e,
+            "gpu_launches": args.steps * 2 * len(ms),
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, dev, w_np, x_np, ms, N, K, world, wcopies, paths):
+    """Same step through the public calls: pinned host x -> device, quantize,
+    matmul, y -> pinned host, every step, synchronised at the end of each step."""
+    import torch
+
+    from iq4_xs_quantized_gb300 import binding as B
+    stream = torch.cuda.Stream(device=dev)
+    hx = {M: torch.from_numpy(np.ascontiguousarray(x_np[:M])).pin_memory() for M in ms}
+    hy = {M: torch.empty((M, N), dtype=torch.float32).pin_memory() for M in ms}
+    dx = {M: torch.empty((M, K), dtype=torch.float32, device=dev) for M in ms}
+    dy = {M: torch.empty((M, N), dtype=torch.float32, device=dev) for M in ms}
+    acts = {M: B.alloc_activations(M, K, dev, tc=True) for M in ms}
+    h2d = sum(M * K * 4 for M in ms)
+    d2h = sum(M * N * 4 for M in ms)
+    variants = len(wcopies) // len(ms)
+
+    def step(s):
+        v = s % variants
+        with torch.cuda.stream(stream):
+            for i, M in enumerate(ms):
+                dx[M].copy_(hx[M], non_blocking=True)
+                qs, ds, op = acts[M]
+                B.iq4xs_quantize_q8_1(dx[M], qs, ds, op, stream)
+                B.iq4xs_matmul(wcopies[v * len(ms) + i], N, K, qs, ds, op, M, dy[M], paths[M], stream)
+                hy[M].copy_(dy[M], non_blocking=True)
+        stream.synchronize()
+
+    for s in range(5):
+        step(s)
+    barrier(world)
+    t0 = time.perf_counter()
+    for s in range(args.e2e_steps):
+        step(s)
+    dt = max_over_ranks(time.perf_counter() - t0, world)
+    value = world * args.e2e_steps * step_bytes(ms, N, K) / dt / 1e9
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": args.e2e_steps, "ms_per_step": dt / args.e2e_steps * 1e3}
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,160 @@
+/*
+ * iq4xs.h -- C ABI of libiq4xs.so: IQ4_XS x Q8_1 batched matmul on GB300
+ * (sm_103a).
+ *
+ *   y[M,N] = x[M,K] . W[N,K]^T
+ *
+ * W is IQ4_XS-quantized (136-byte super-blocks of 256 weights, 4.25 bits per
+ * weight); x is quantized per 32 values to Q8_1 by iq4xs_quantize_q8_1 and the
+ * product is formed from exact int32 per-32-weight dot products scaled into
+ * fp32.  The method is the one described on the V100TPS engine page
+ * (agent-report.daedalus.work/V100TPS/engine.html): the kernel table at M=64
+ * (quantize_q8_1 feeding the batched matmul), the new-kernel table (batched
+ * IQ4_XS for 4 <= M <= 96) and the tile-geometry passage after it (sub-block
+ * scale d*(ls-32), nibbles through kvalues_iq4nl, low nibbles = elements
+ * 0-15 of a sub-block, high nibbles = 16-31).
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - All data pointers are DEVICE pointers owned by the caller.  The library
+ *    never allocates, frees or retains them, and allocates nothing per call.
+ *    A one-time per-device set-up (architecture check, the tensor-map encoder
+ *    entry point, kernel attributes) runs on the first call made on a device.
+ *  - `stream` is a cudaStream_t passed as an int64 (0 = legacy default
+ *    stream).  Every call is asynchronous on that stream and never
+ *    synchronizes; results are ready when the stream reaches that point.
+ *  - The current CUDA device (cudaSetDevice) is the one used; it must be an
+ *    sm_103 GPU (GB300) or the call returns IQ4XS_ERR_DEVICE.
+ *  - Argument errors are detected on the host BEFORE any launch and are
+ *    returned synchronously; nothing is launched and no output is touched.
+ *    Launch failures return IQ4XS_ERR_CUDA.  A device-side bounded wait that
+ *    ran out sets a device error word (see iq4xs_last_device_error) and the
+ *    kernel returns without hanging; the outputs of that call are undefined.
+ *  - Shapes: 1 <= M <= 32768; N >= 1; K a positive multiple of 256.
+ *
+ * Data layouts
+ * ------------
+ *  W (IQ4_XS): row-major [N][K/256] super-blocks, each 136 bytes:
+ *      bytes 0-1   d         fp16, little endian
+ *      bytes 2-3   scales_h  u16, little endian: bits 2j..2j+1 are the two
+ *                            high bits of ls_j
+ *      bytes 4-7   scales_l  u8[4]: low nibble of byte j/2 holds the four low
+ *                            bits of ls_j for even j, high nibble for odd j
+ *      bytes 8-135 qs        u8[128]: sub-block j uses bytes 16j..16j+15;
+ *                            element i (0..15) is the low nibble of byte
+ *                            16j+i, element 16+i the high nibble
+ *      weight = fp32(d) * (ls_j - 32) * kvalues_iq4nl[nibble].
+ *      Rows are K/256*136 bytes apart; W must be 16-byte aligned.
+ *  Q8_1 activations (structure of arrays):
+ *      qs  int8  [M][K]     q = round(x/d), ties away from zero
+ *      ds  half2 [M][K/32]  {d = amax/127, s = d*sum(q)} each rounded to fp16
+ *  Tensor-core operand (opaque, produced by iq4xs_quantize_q8_1 when asked):
+ *      the same q values as fp16 plus the block scales d as fp32, tiled for
+ *      the tcgen05 path; size iq4xs_tc_operand_bytes(M, K), 16-byte aligned.
+ *  y: fp32 [M][ldy] row-major, ldy >= N; columns N..ldy-1 are not written.
+ */
+#ifndef IQ4XS_H
+#define IQ4XS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    IQ4XS_OK = 0,
+    IQ4XS_ERR_ARG = 1,     /* null pointer, bad size, ldx/ldy too small, bad enum */
+    IQ4XS_ERR_ALIGN = 2,   /* a pointer lacks the alignment stated for it */
+    IQ4XS_ERR_SHAPE = 3,   /* K not a multiple of 256, M out of range, or a shape
+                              the requested path cannot take */
+    IQ4XS_ERR_DEVICE = 4,  /* no CUDA device, or the current device is not sm_103 */
+    IQ4XS_ERR_CUDA = 5,    /* a CUDA runtime/driver call or a launch failed */
+    IQ4XS_ERR_TIMEOUT = 6  /* a bounded device wait ran out (device error word) */
+} iq4xs_status;
+
+typedef enum {
+    IQ4XS_PATH_AUTO = 0, /* iq4xs_select_path decides from (M, N, K)            */
+    IQ4XS_PATH_DP4A = 1, /* CUDA-core int8 dot products (small M)               */
+    IQ4XS_PATH_TC = 2    /* tcgen05 tensor cores on exact small-integer fp16
+                            operands, per-sub-block fp32 scale-in (larger M)    */
+} iq4xs_path;
+
+/*
+ * Q8_1 activation quantization (engine page, kernel table at M=64: the
+ * activations enter the batched matmul through quantize_q8_1).
+ *   x           fp32 [M][ldx], ldx >= K, 4-byte aligned, ldx*4 % 16 == 0 and
+ *               x 16-byte aligned (rows are read as float4).
+ *   qs, ds      outputs, layouts above; qs 16-byte aligned, ds 4-byte aligned.
+ *   tc_operand  optional output (NULL to skip): the tensor-core operand for
+ *               IQ4XS_PATH_TC, iq4xs_tc_operand_bytes(M, K) bytes, 16-byte
+ *               aligned.  Padding rows inside it are written as zeros.
+ * Per block of 32: amax = max|x|, d = amax/127 (IEEE fp32 division),
+ * q = d == 0 ? 0 : roundf(x/d), s = d*sum(q); d and s stored as fp16 (RNE).
+ * Inputs must be finite (NaN/Inf give unspecified codes).
+ */
+int iq4xs_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx,
+                        int8_t* qs, void* ds, void* tc_operand, int64_t stream);
+
+/* Bytes of the tensor-core operand for (M, K); 0 if the shape is invalid. */
+int64_t iq4xs_tc_operand_bytes(int64_t M, int64_t K);
+
+/*
+ * Batched matmul y = x . W^T from IQ4_XS W and Q8_1 x (engine page,
+ * new-kernel table and tile-geometry passage: per-32 sub-block integer dot
+ * products scaled by d_w*(ls-32)*d_x into fp32).
+ *   w           IQ4_XS [N][K/256] blocks, 16-byte aligned.
+ *   qs, ds      Q8_1 activations from iq4xs_quantize_q8_1 (DP4A path).
+ *   tc_operand  tensor-core operand from iq4xs_quantize_q8_1 (TC path);
+ *               may be NULL when the chosen path is DP4A.
+ *   y           fp32 [M][ldy] output, fully overwritten for columns < N.
+ *   path        an iq4xs_path value.  AUTO asks iq4xs_select_path.
+ * The TC path needs K % 512 == 0 (super-blocks are staged in pairs so every
+ * tensor-memory copy starts on a 16-byte boundary) and a non-NULL
+ * tc_operand; otherwise it returns IQ4XS_ERR_SHAPE / IQ4XS_ERR_ARG.
+ * Result: fp32 accumulation of exact integer sub-block dots; it differs from
+ * the fp64 definition by fp32 rounding only.
+ */
+int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds,
+                 const void* tc_operand, int64_t M, float* y, int64_t ldy, int path,
+                 int64_t stream);
+
+/*
+ * Dequantize W to a dense [N][K] matrix (engine page, kernel table at M=64:
+ * dequantize_block_iq4_xs feeding a dense GEMM -- the baseline the batched
+ * kernel replaces).  out_dtype 0 = fp32 (exact), 1 = bfloat16 (RNE of the
+ * exact value).  out is 16-byte aligned, [N][K] row-major.
+ */
+int iq4xs_dequantize(const void* w, int64_t N, int64_t K, void* out, int out_dtype,
+                     int64_t stream);
+
+/*
+ * Path choice for (M, N, K) (engine page, mmvq vs dequantize table: the
+ * original dispatcher hard-coded its threshold at M=8 while the measured
+ * crossover was M~15).  Host only, no device access.  Returns DP4A when
+ * M <= the calibrated crossover for that shape class and the DP4A path
+ * applies, TC otherwise (TC requires K % 512 == 0).
+ */
+int iq4xs_select_path(int64_t M, int64_t N, int64_t K, int* path_out);
+
+/*
+ * Install the measured crossover: DP4A is chosen for M <= m_max_dp4a.
+ * Host only.  Defaults to 4 until a calibration sets it.  Thread-safe.
+ */
+int iq4xs_set_crossover(int64_t m_max_dp4a);
+
+/*
+ * Read and clear the current device's error word, written by kernels whose
+ * bounded waits ran out (IQ4XS_ERR_TIMEOUT) or that saw an impossible
+ * state.  Synchronizes the current device.  *code_out = 0 when clean.
+ */
+int iq4xs_last_device_error(int* code_out);
+
+/* Static string for a status code. */
+const char* iq4xs_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IQ4XS_H */

@@ -1,0 +1,162 @@
+"""Thin ctypes binding over libiq4xs.so (argument marshalling only).
+
+The names match the C ABI in include/iq4xs.h.  Tensors are torch CUDA tensors
+owned by the caller; streams default to torch's current stream.  Every step
+of the computation runs in the library's CUDA kernels: there is no CPU or
+PyTorch fallback, and a missing library raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libiq4xs.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "iq4xs.h")
+
+OK, ERR_ARG, ERR_ALIGN, ERR_SHAPE, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT = range(7)
+PATH_AUTO, PATH_DP4A, PATH_TC = 0, 1, 2
+PATHS = {"auto": PATH_AUTO, "dp4a": PATH_DP4A, "tc": PATH_TC}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class IQ4XSError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: status {status} ({msg})")
+        self.status = status
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/iq4xs.h."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+char\s*\*|int64_t|int)\s+(iq4xs_\w+)\s*\(", text, flags=re.M)
+
+
+def load(path: str | None = None):
+    """Load the CUDA library (built by ``iq4_xs_quantized_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with iq4_xs_quantized_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        lib.iq4xs_quantize_q8_1.argtypes = [vp, i64, i64, i64, vp, vp, vp, i64]
+        lib.iq4xs_tc_operand_bytes.argtypes = [i64, i64]
+        lib.iq4xs_tc_operand_bytes.restype = i64
+        lib.iq4xs_matmul.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, i64, ci, i64]
+        lib.iq4xs_dequantize.argtypes = [vp, i64, i64, vp, ci, i64]
+        lib.iq4xs_select_path.argtypes = [i64, i64, i64, ctypes.POINTER(ci)]
+        lib.iq4xs_set_crossover.argtypes = [i64]
+        lib.iq4xs_last_device_error.argtypes = [ctypes.POINTER(ci)]
+        lib.iq4xs_status_string.argtypes = [ci]
+        lib.iq4xs_status_string.restype = ctypes.c_char_p
+        for name in ("iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_dequantize",
+                     "iq4xs_select_path", "iq4xs_set_crossover", "iq4xs_last_device_error"):
+            getattr(lib, name).restype = ci
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(fn: str, rc: int):
+    if rc != OK:
+        raise IQ4XSError(fn, rc, load().iq4xs_status_string(rc).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+# --------------------------------------------------------------------------
+# Entry points (same names as the C ABI).
+# --------------------------------------------------------------------------
+def iq4xs_tc_operand_bytes(M: int, K: int) -> int:
+    return int(load().iq4xs_tc_operand_bytes(M, K))
+
+
+def iq4xs_quantize_q8_1(x, qs, ds, tc_operand=None, stream=None) -> None:
+    """x fp32 [M, K] (row stride x.stride(0)) -> qs int8 [M, K], ds fp16 [M, K/32, 2]
+    ({d, s}), optionally the tensor-core operand (uint8, iq4xs_tc_operand_bytes)."""
+    M, K = x.shape
+    rc = load().iq4xs_quantize_q8_1(_ptr(x), M, K, x.stride(0), _ptr(qs), _ptr(ds),
+                                    _ptr(tc_operand), _stream(stream))
+    _check("iq4xs_quantize_q8_1", rc)
+
+
+def iq4xs_matmul(w, N: int, K: int, qs, ds, tc_operand, M: int, y, path=PATH_AUTO,
+                 stream=None) -> None:
+    """y fp32 [M, ldy] = x . W^T from IQ4_XS bytes w and Q8_1 activations."""
+    if isinstance(path, str):
+        path = PATHS[path]
+    ldy = y.stride(0)
+    rc = load().iq4xs_matmul(_ptr(w), N, K, _ptr(qs), _ptr(ds), _ptr(tc_operand), M, _ptr(y),
+                             ldy, int(path), _stream(stream))
+    _check("iq4xs_matmul", rc)
+
+
+def iq4xs_dequantize(w, N: int, K: int, out, stream=None) -> None:
+    """IQ4_XS -> dense [N, K]; out dtype float32 (exact) or bfloat16 (RNE)."""
+    dt = {torch.float32: 0, torch.bfloat16: 1}[out.dtype]
+    rc = load().iq4xs_dequantize(_ptr(w), N, K, _ptr(out), dt, _stream(stream))
+    _check("iq4xs_dequantize", rc)
+
+
+def iq4xs_select_path(M: int, N: int, K: int) -> int:
+    out = ctypes.c_int(-1)
+    _check("iq4xs_select_path", load().iq4xs_select_path(M, N, K, ctypes.byref(out)))
+    return out.value
+
+
+def iq4xs_set_crossover(m_max_dp4a: int) -> None:
+    _check("iq4xs_set_crossover", load().iq4xs_set_crossover(int(m_max_dp4a)))
+
+
+def iq4xs_last_device_error() -> int:
+    out = ctypes.c_int(-1)
+    _check("iq4xs_last_device_error", load().iq4xs_last_device_error(ctypes.byref(out)))
+    return out.value
+
+
+def iq4xs_status_string(status: int) -> str:
+    return load().iq4xs_status_string(status).decode()
+
+
+# --------------------------------------------------------------------------
+# Buffer helpers (allocation by torch; the library allocates nothing).
+# --------------------------------------------------------------------------
+def alloc_activations(M: int, K: int, device="cuda", tc: bool = True):
+    """Q8_1 buffers for M x K activations: (qs, ds, tc_operand or None)."""
+    qs = torch.empty((M, K), dtype=torch.int8, device=device)
+    ds = torch.empty((M, K // 32, 2), dtype=torch.float16, device=device)
+    op = None
+    if tc:
+        op = torch.empty(iq4xs_tc_operand_bytes(M, K), dtype=torch.uint8, device=device)
+    return qs, ds, op
+
+
+def linear(w, N: int, K: int, x, path=PATH_AUTO, stream=None, out=None):
+    """Convenience: quantize x [M, K] and return y [M, N] fp32 (two launches)."""
+    M = x.shape[0]
+    qs, ds, op = alloc_activations(M, K, x.device, tc=True)
+    iq4xs_quantize_q8_1(x, qs, ds, op, stream)
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=x.device)
+    iq4xs_matmul(w, N, K, qs, ds, op, M, y, path, stream)
+    return y

@@ -1,0 +1,187 @@
+// api.cu -- the extern "C" boundary of libiq4xs.so (declared in
+// include/iq4xs.h): argument validation, per-device set-up, path dispatch.
+// All validation happens on the host before any launch.
+#include <cuda.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/iq4xs.h"
+#include "internal.cuh"
+
+namespace iq4xs {
+
+// Device error word: kernels whose bounded waits run out record a code here.
+__device__ int g_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxM = 32768;
+
+struct DevState {
+    bool ready = false;
+    int status = IQ4XS_OK;
+    int num_sms = 0;
+    int* err = nullptr;       // device address of g_device_error
+    void* encode = nullptr;   // cuTensorMapEncodeTiled
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+std::atomic<int64_t> g_crossover{4};
+
+// One-time per-device set-up, done with that device current.
+int device_state(DevState** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return IQ4XS_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevState& st = g_dev[dev];
+    if (!st.ready) {
+        st.ready = true;
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            st.status = IQ4XS_ERR_DEVICE;
+        } else if (major != 10 || minor != 3) {
+            st.status = IQ4XS_ERR_DEVICE;  // built for sm_103a only
+        } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err), g_device_error) !=
+                   cudaSuccess) {
+            cudaGetLastError();
+            st.status = IQ4XS_ERR_CUDA;
+        } else {
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &st.encode, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || st.encode == nullptr) {
+                cudaGetLastError();
+                st.status = IQ4XS_ERR_CUDA;
+            }
+        }
+    }
+    *out = &st;
+    return st.status;
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline int from_cuda(cudaError_t e) { return e == cudaSuccess ? IQ4XS_OK : IQ4XS_ERR_CUDA; }
+
+int select_path_impl(int64_t M, int64_t N, int64_t K) {
+    (void)N;
+    if (K % kPairK != 0) return IQ4XS_PATH_DP4A;  // TC stages super-blocks in pairs
+    return (M <= g_crossover.load()) ? IQ4XS_PATH_DP4A : IQ4XS_PATH_TC;
+}
+
+}  // namespace
+}  // namespace iq4xs
+
+using namespace iq4xs;
+
+extern "C" {
+
+int64_t iq4xs_tc_operand_bytes(int64_t M, int64_t K) {
+    if (M < 1 || M > kMaxM || K <= 0 || K % kQK) return 0;
+    return tc_qh_bytes(M, K) + tc_dx_bytes(M, K);
+}
+
+int iq4xs_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, void* ds,
+                        void* tc_operand, int64_t stream) {
+    if (!x || !qs || !ds) return IQ4XS_ERR_ARG;
+    if (M < 1 || M > kMaxM || K <= 0 || K % kQK) return IQ4XS_ERR_SHAPE;
+    if (ldx < K || (ldx * 4) % 16) return IQ4XS_ERR_ARG;
+    if (!aligned(x, 16) || !aligned(qs, 16) || !aligned(ds, 4) ||
+        (tc_operand && !aligned(tc_operand, 16)))
+        return IQ4XS_ERR_ALIGN;
+    DevState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    return from_cuda(launch_quantize_q8_1(x, M, K, ldx, qs, ds, tc_operand,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds,
+                 const void* tc_operand, int64_t M, float* y, int64_t ldy, int path,
+                 int64_t stream) {
+    if (!w || !y) return IQ4XS_ERR_ARG;
+    if (path < IQ4XS_PATH_AUTO || path > IQ4XS_PATH_TC) return IQ4XS_ERR_ARG;
+    if (M < 1 || M > kMaxM || N < 1 || N > (1 << 30) || K <= 0 || K % kQK || K > (1 << 30))
+        return IQ4XS_ERR_SHAPE;
+    if (ldy < N) return IQ4XS_ERR_ARG;
+    if (!aligned(w, 16) || !aligned(y, 4)) return IQ4XS_ERR_ALIGN;
+    if (path == IQ4XS_PATH_AUTO) path = select_path_impl(M, N, K);
+    if (path == IQ4XS_PATH_TC) {
+        if (K % kPairK) return IQ4XS_ERR_SHAPE;
+        if (!tc_operand) return IQ4XS_ERR_ARG;
+        if (!aligned(tc_operand, 16)) return IQ4XS_ERR_ALIGN;
+    } else {
+        if (!qs || !ds) return IQ4XS_ERR_ARG;
+        if (!aligned(qs, 16) || !aligned(ds, 4)) return IQ4XS_ERR_ALIGN;
+    }
+    DevState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (path == IQ4XS_PATH_TC)
+        return from_cuda(launch_matmul_tc(w, N, K, tc_operand, M, y, ldy, st->encode, st->err,
+                                          st->num_sms, s));
+    return from_cuda(launch_matmul_dp4a(w, N, K, qs, ds, M, y, ldy, s));
+}
+
+int iq4xs_dequantize(const void* w, int64_t N, int64_t K, void* out, int out_dtype,
+                     int64_t stream) {
+    if (!w || !out) return IQ4XS_ERR_ARG;
+    if (out_dtype != 0 && out_dtype != 1) return IQ4XS_ERR_ARG;
+    if (N < 1 || K <= 0 || K % kQK) return IQ4XS_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(out, 16)) return IQ4XS_ERR_ALIGN;
+    DevState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    return from_cuda(launch_dequantize(w, N, K, out, out_dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int iq4xs_select_path(int64_t M, int64_t N, int64_t K, int* path_out) {
+    if (!path_out) return IQ4XS_ERR_ARG;
+    if (M < 1 || M > kMaxM || N < 1 || K <= 0 || K % kQK) return IQ4XS_ERR_SHAPE;
+    *path_out = select_path_impl(M, N, K);
+    return IQ4XS_OK;
+}
+
+int iq4xs_set_crossover(int64_t m_max_dp4a) {
+    if (m_max_dp4a < 0 || m_max_dp4a > kMaxM) return IQ4XS_ERR_ARG;
+    g_crossover.store(m_max_dp4a);
+    return IQ4XS_OK;
+}
+
+int iq4xs_last_device_error(int* code_out) {
+    if (!code_out) return IQ4XS_ERR_ARG;
+    DevState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    if (cudaDeviceSynchronize() != cudaSuccess) return IQ4XS_ERR_CUDA;
+    int zero = 0;
+    if (cudaMemcpyFromSymbol(code_out, g_device_error, sizeof(int)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess)
+        return IQ4XS_ERR_CUDA;
+    return IQ4XS_OK;
+}
+
+const char* iq4xs_status_string(int status) {
+    switch (status) {
+        case IQ4XS_OK: return "ok";
+        case IQ4XS_ERR_ARG: return "invalid argument";
+        case IQ4XS_ERR_ALIGN: return "misaligned pointer";
+        case IQ4XS_ERR_SHAPE: return "unsupported shape";
+        case IQ4XS_ERR_DEVICE: return "no sm_103 device";
+        case IQ4XS_ERR_CUDA: return "CUDA error";
+        case IQ4XS_ERR_TIMEOUT: return "device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

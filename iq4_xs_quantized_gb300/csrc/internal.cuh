@@ -1,0 +1,337 @@
+// internal.cuh -- layout constants, decoders and PTX wrappers shared by the
+// kernels of libiq4xs.so.  Not part of the public ABI (include/iq4xs.h).
+//
+// Format facts (V100TPS engine page, agent-report.daedalus.work/V100TPS/
+// engine.html, tile-geometry passage after the new-kernel table): an IQ4_XS
+// sub-block of 32 weights is 4 ints of packed nibbles, low nibbles are
+// elements 0-15 and high nibbles 16-31; its scale is d*(ls-32); a nibble is
+// decoded through kvalues_iq4nl.  The same passage records that reusing
+// thread-mapping constants as tile geometry silently advanced four
+// super-blocks per step, so every tile size here is a named constant tied to
+// the format by static_assert.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace iq4xs {
+
+// ---------------------------------------------------------------------------
+// IQ4_XS super-block and Q8_1 block.
+// ---------------------------------------------------------------------------
+constexpr int kQK = 256;                      // weights per super-block
+constexpr int kSub = 32;                      // weights per sub-block == per Q8_1 block
+constexpr int kSubPerBlock = kQK / kSub;      // 8
+constexpr int kBlockBytes = 136;              // 2 + 2 + 4 + 128
+constexpr int kQsBytesPerSub = kSub / 2;      // 16 bytes of nibbles per sub-block
+
+struct BlockIQ4XS {
+    uint16_t d;            // fp16 super-block scale
+    uint16_t scales_h;     // 2 high bits of each ls_j at bits 2j..2j+1
+    uint8_t scales_l[4];   // 4 low bits of ls_j: low nibble for even j, high for odd j
+    uint8_t qs[kQK / 2];   // nibbles; sub-block j uses bytes 16j..16j+15
+};
+static_assert(sizeof(BlockIQ4XS) == kBlockBytes, "IQ4_XS super-block is 136 bytes");
+static_assert(offsetof(BlockIQ4XS, d) == 0, "d at byte 0");
+static_assert(offsetof(BlockIQ4XS, scales_h) == 2, "scales_h at byte 2");
+static_assert(offsetof(BlockIQ4XS, scales_l) == 4, "scales_l at byte 4");
+static_assert(offsetof(BlockIQ4XS, qs) == 8, "qs at byte 8");
+static_assert(kSubPerBlock * kQsBytesPerSub == sizeof(((BlockIQ4XS*)0)->qs), "8 sub-blocks of 16 bytes");
+
+constexpr int kQ8Max = 127;  // Q8_1 codes lie in [-127, 127]
+
+// kvalues_iq4nl packed four entries per word, little endian (entry 4w+k in
+// byte k of word w).  Two forms: the int8 values themselves, and u = kv + 128
+// (all of 1..241 fit one unsigned byte) for building exact fp16 operands.
+constexpr uint32_t kKvS8_0 = 0xBFAD9881u, kKvS8_1 = 0xF6EADDCFu, kKvS8_2 = 0x26190D01u,
+                   kKvS8_3 = 0x71594535u;
+constexpr uint32_t kKvU8_0 = 0x3F2D1801u, kKvU8_1 = 0x766A5D4Fu, kKvU8_2 = 0xA6998D81u,
+                   kKvU8_3 = 0xF1D9C5B5u;
+// fp16 with bit pattern 0x64XX is 1024 + XX; 1024 + u - 1152 = kv exactly.
+constexpr uint32_t kF16HiByte = 0x64646464u;
+constexpr uint32_t kF16Offset2 = 0x64806480u;  // half2(1152, 1152)
+
+// ---------------------------------------------------------------------------
+// Tensor-core path geometry.
+// ---------------------------------------------------------------------------
+constexpr int kTileN = 128;                       // W rows per CTA = TMEM lanes = UMMA M
+constexpr int kPairBlocks = 2;                    // super-blocks per W stage
+constexpr int kPairK = kPairBlocks * kQK;         // 512
+constexpr int kPairBytes = kPairBlocks * kBlockBytes;  // 272 = 17 x 16: TMA rows stay 16-byte aligned
+constexpr int kSubPerPair = kPairK / kSub;        // 16
+constexpr int kWStageBytes = kTileN * kPairBytes; // 34816
+static_assert(kPairBytes % 16 == 0, "a W stage row must be a whole number of 16-byte units");
+static_assert(kPairBytes / 4 <= 256, "TMA box inner extent (uint32 elements) <= 256");
+constexpr int kChunkElems = 8;                    // fp16 per 16-byte core-matrix row
+constexpr int kChunksPerSub = kSub / kChunkElems; // 4
+constexpr int kUmmaK = 16;                        // K per tcgen05.mma kind::f16
+constexpr int kMmaPerSub = kSub / kUmmaK;         // 2
+constexpr int kASubBytes = kTileN * kSub * 2;     // 8 KB of fp16 A per sub-block
+constexpr int kBStageSubs = 4;                    // sub-blocks per activation stage
+constexpr int kBStageChunks = kBStageSubs * kChunksPerSub;  // 16
+constexpr int kMaxMTile = 128;                    // activation rows per tcgen05 tile (UMMA N)
+static_assert(kSubPerPair % kBStageSubs == 0, "activation stages tile a W stage");
+
+// Activation tile height for a batch of M rows: round M up to 16 (UMMA N
+// granularity for M=128), capped at kMaxMTile.
+__host__ __device__ inline int tc_mtile(int64_t M) {
+    int64_t r = (M + 15) / 16 * 16;
+    return (int)(r < kMaxMTile ? r : kMaxMTile);
+}
+__host__ __device__ inline int64_t tc_num_mtiles(int64_t M) {
+    int mt = tc_mtile(M);
+    return (M + mt - 1) / mt;
+}
+// Tensor-core operand: qh (fp16 q, K-permuted, tiled) then dxT (fp32 d).
+//   qh:  [mtile][K/8 chunk][MT rows][8 fp16]    (16 B per (chunk,row))
+//   dxT: [mtile][K/32 sub-block][MT rows] fp32
+// Within every sub-block the K order is permuted to (0,16,1,17,...,15,31):
+// K position 2i+h holds element i+16h, matching the decoded weight order.
+__host__ __device__ inline int64_t tc_qh_bytes(int64_t M, int64_t K) {
+    return tc_num_mtiles(M) * (int64_t)tc_mtile(M) * K * 2;
+}
+__host__ __device__ inline int64_t tc_dx_bytes(int64_t M, int64_t K) {
+    return tc_num_mtiles(M) * (int64_t)tc_mtile(M) * (K / kSub) * 4;
+}
+
+// ---------------------------------------------------------------------------
+// Device error word (defined in api.cu); its address is passed to kernels.
+// ---------------------------------------------------------------------------
+enum DeviceError : int {
+    kDevErrNone = 0,
+    kDevErrTimeoutW = 0x101,
+    kDevErrTimeoutB = 0x102,
+    kDevErrTimeoutA = 0x103,
+    kDevErrTimeoutMma = 0x104,
+    kDevErrTimeoutFree = 0x105,
+    kDevErrTimeoutDrain = 0x106,
+};
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
+
+// ---------------------------------------------------------------------------
+// Nibble decoders (prmt.b32: 8 source bytes {b,a}; selector nibble bits 0-2
+// pick a byte, bit 3 replicates its sign -- kept clear here).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Look up the 8 nibbles of a qs word w through a 16-entry byte table T.
+// t0 = [T(L0), T(H0), T(L1), T(H1)], t1 = [T(L2), T(H2), T(L3), T(H3)],
+// where byte k of w is (Hk << 4) | Lk.
+__device__ __forceinline__ void lut16(uint32_t w, const uint32_t T0, const uint32_t T1,
+                                      const uint32_t T2, const uint32_t T3, uint32_t& t0,
+                                      uint32_t& t1) {
+    const uint32_t sel = w & 0x77777777u;
+    const uint32_t pick = ((w >> 1) & 0x44444444u) | 0x32103210u;
+    t0 = prmt(prmt(T0, T1, sel), prmt(T2, T3, sel), pick);
+    const uint32_t sel_hi = sel >> 16;
+    t1 = prmt(prmt(T0, T1, sel_hi), prmt(T2, T3, sel_hi), pick >> 16);
+}
+
+// qs word -> int8x4 codebook values of elements i..i+3 (low nibbles) and
+// 16+i..16+i+3 (high nibbles).
+__device__ __forceinline__ void decode_s8(uint32_t w, uint32_t& lo4, uint32_t& hi4) {
+    uint32_t t0, t1;
+    lut16(w, kKvS8_0, kKvS8_1, kKvS8_2, kKvS8_3, t0, t1);
+    lo4 = prmt(t0, t1, 0x6420u);
+    hi4 = prmt(t0, t1, 0x7531u);
+}
+
+// qs word (bytes k = 0..3 of sub-block element i = i0 + k) -> four fp16x2
+// words (kv[L_k], kv[H_k]): the K-permuted order (element i, element 16+i).
+__device__ __forceinline__ void decode_f16x2(uint32_t w, uint32_t out[4]) {
+    uint32_t t0, t1;
+    lut16(w, kKvU8_0, kKvU8_1, kKvU8_2, kKvU8_3, t0, t1);
+    const uint32_t h[4] = {prmt(t0, kF16HiByte, 0x4140u), prmt(t0, kF16HiByte, 0x4342u),
+                           prmt(t1, kF16HiByte, 0x4140u), prmt(t1, kF16HiByte, 0x4342u)};
+    const uint32_t off_bits = kF16Offset2;
+    const __half2 off = *reinterpret_cast<const __half2*>(&off_bits);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h[k]), off);
+        out[k] = *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+// 6-bit scale of sub-block j from the 8-byte header word pair
+// hdr0 = d | scales_h << 16, hdr1 = scales_l[0..3].
+__device__ __forceinline__ int iq4xs_ls(uint32_t hdr0, uint32_t hdr1, int j) {
+    const int lo = (hdr1 >> (4 * j)) & 0xF;  // byte j/2, nibble j&1 == bits 4j..4j+3
+    const int hi = (hdr0 >> (16 + 2 * j)) & 3;
+    return lo | (hi << 4);
+}
+__device__ __forceinline__ float iq4xs_scale(uint32_t hdr0, uint32_t hdr1, int j) {
+    const float d = __half2float(__ushort_as_half((unsigned short)(hdr0 & 0xFFFF)));
+    return d * (float)(iq4xs_ls(hdr0, hdr1, j) - 32);
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers: shared-memory addresses, mbarriers, bulk copies, tcgen05.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity to complete.  Returns
+// false (without waiting further) once the CTA's abort flag is set, or after
+// kWaitLimitNs, in which case it sets the abort flag and the device error word.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err, int code) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(a, parity)) return true;
+        if ((it & 63) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicExch(err, code);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 2D tiled TMA load into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, int x, int y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+// Contiguous bulk copy global -> this CTA's shared memory (16-byte aligned
+// addresses, size a multiple of 16), completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(smem_dst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// tcgen05 (5th-generation tensor core, tensor memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(smem_dst)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16, issued by one thread.
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on `bar` once every tcgen05 operation this thread issued so far is complete.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// Shared-memory matrix descriptor, K-major, no swizzle: core matrices of
+// 8 rows x 16 bytes stored contiguously; `lbo` = byte distance between
+// core matrices adjacent along K, `sbo` = along M/N.  Bits 46-48 = 0b001.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+// Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major,
+// N = n (multiple of 16 for M = 128), M = 128.
+__host__ __device__ constexpr uint32_t idesc_f16_m128(int n) {
+    return (1u << 4)                        // D format: F32
+           | (0u << 7) | (0u << 10)         // A, B format: F16
+           | ((uint32_t)(n >> 3) << 17)     // N >> 3
+           | ((uint32_t)(kTileN >> 4) << 24);  // M >> 4
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launchers (defined in the kernel translation units).
+// ---------------------------------------------------------------------------
+struct DevCtx;  // per-device state kept by api.cu
+
+cudaError_t launch_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs,
+                                 void* ds, void* tc_operand, cudaStream_t stream);
+cudaError_t launch_dequantize(const void* w, int64_t N, int64_t K, void* out, int out_dtype,
+                              cudaStream_t stream);
+cudaError_t launch_matmul_dp4a(const void* w, int64_t N, int64_t K, const int8_t* qs,
+                               const void* ds, int64_t M, float* y, int64_t ldy,
+                               cudaStream_t stream);
+// `encode` is the driver's cuTensorMapEncodeTiled; `err` the device error word.
+cudaError_t launch_matmul_tc(const void* w, int64_t N, int64_t K, const void* tc_operand,
+                             int64_t M, float* y, int64_t ldy, void* encode, int* err,
+                             int num_sms, cudaStream_t stream);
+
+}  // namespace iq4xs

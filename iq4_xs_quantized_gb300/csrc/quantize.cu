@@ -1,0 +1,106 @@
+// quantize.cu -- Q8_1 activation quantization (V100TPS engine page, kernel
+// table at M=64: the activations enter the batched matmul through
+// quantize_q8_1).  Per block of 32 values: amax = max|x|, d = amax/127,
+// q = round(x/d) (ties away from zero), s = d*sum(q); d and s stored as fp16.
+//
+// One thread owns 4 consecutive values (one float4 load), 8 threads own a
+// Q8_1 block, a warp owns 4 blocks.  The kernel optionally also writes the
+// tensor-core operand: the same q as exact fp16 in the K-permuted, tiled
+// order the tcgen05 path consumes, and each block's stored d widened to fp32.
+#include "internal.cuh"
+
+namespace iq4xs {
+namespace {
+
+constexpr int kQuantThreads = 256;
+constexpr int kElemsPerThread = 4;
+constexpr int kElemsPerCta = kQuantThreads * kElemsPerThread;  // 1024
+constexpr int kThreadsPerBlock = kSub / kElemsPerThread;        // 8
+static_assert(kThreadsPerBlock == 8, "8 lanes per Q8_1 block: xor-shuffles 1, 2, 4");
+
+// grid: x = ceil(K / 1024), y = rows (M, or the padded tile rows when the
+// tensor-core operand is requested).  K % 256 == 0, so a warp's 128 values
+// are either all inside K or all outside it.
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_q8_1_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
+                         int8_t* __restrict__ qs, __half2* __restrict__ ds,
+                         uint4* __restrict__ qh, float* __restrict__ dxT, int MT) {
+    const int64_t m = blockIdx.y;
+    const int64_t e0 = (int64_t)blockIdx.x * kElemsPerCta + threadIdx.x * kElemsPerThread;
+    if (e0 >= K) return;  // whole warps only (see above)
+    const int lane = threadIdx.x & 31;
+    const int l8 = lane & 7;  // position of this thread inside its Q8_1 block
+
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (m < M) v = __ldg(reinterpret_cast<const float4*>(x + m * ldx + e0));
+
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const float d = __fdiv_rn(amax, 127.0f);
+    int q[4] = {0, 0, 0, 0};
+    if (d != 0.0f) {
+        q[0] = (int)roundf(__fdiv_rn(v.x, d));
+        q[1] = (int)roundf(__fdiv_rn(v.y, d));
+        q[2] = (int)roundf(__fdiv_rn(v.z, d));
+        q[3] = (int)roundf(__fdiv_rn(v.w, d));
+    }
+    int sum = q[0] + q[1] + q[2] + q[3];
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+    const __half d_h = __float2half_rn(d);
+    const int64_t blk = e0 / kSub;  // global Q8_1 block (= sub-block) index
+
+    if (m < M) {
+        const uint32_t packed = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
+                                ((uint32_t)(q[2] & 0xFF) << 16) | ((uint32_t)(q[3] & 0xFF) << 24);
+        *reinterpret_cast<uint32_t*>(qs + m * K + e0) = packed;
+        if (l8 == 0) ds[m * (K / kSub) + blk] = __halves2half2(d_h, __float2half_rn(d * (float)sum));
+    }
+
+    if (qh != nullptr) {
+        // Element e of the block goes to K position 2*(e % 16) + e / 16.  The
+        // thread holding e = 4*l8 .. 4*l8+3 (l8 < 4) pairs with lane ^ 4,
+        // which holds e + 16, and writes one 16-byte chunk (8 positions).
+        int p[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) p[k] = __shfl_xor_sync(0xffffffffu, q[k], 4);
+        const int64_t mt = m / MT;
+        const int64_t r = m % MT;
+        if (l8 < 4) {
+            __half h[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                h[2 * k] = __int2half_rn(q[k]);
+                h[2 * k + 1] = __int2half_rn(p[k]);
+            }
+            const int64_t chunk = blk * kChunksPerSub + l8;
+            qh[(mt * (K / kChunkElems) + chunk) * MT + r] = *reinterpret_cast<const uint4*>(h);
+        }
+        if (l8 == 0) dxT[(mt * (K / kSub) + blk) * MT + r] = __half2float(d_h);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs,
+                                 void* ds, void* tc_operand, cudaStream_t stream) {
+    int64_t rows = M;
+    int MT = 0;
+    uint4* qh = nullptr;
+    float* dxT = nullptr;
+    if (tc_operand != nullptr) {
+        MT = tc_mtile(M);
+        rows = tc_num_mtiles(M) * MT;  // padding rows are written as zeros
+        qh = reinterpret_cast<uint4*>(tc_operand);
+        dxT = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tc_operand) + tc_qh_bytes(M, K));
+    }
+    dim3 grid((unsigned)((K + kElemsPerCta - 1) / kElemsPerCta), (unsigned)rows);
+    quantize_q8_1_kernel<<<grid, kQuantThreads, 0, stream>>>(
+        x, M, K, ldx, qs, reinterpret_cast<__half2*>(ds), qh, dxT, MT);
+    return cudaGetLastError();
+}
+
+}  // namespace iq4xs

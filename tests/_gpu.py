@@ -1,0 +1,78 @@
+"""Helpers for the GPU parity tests: move seeded inputs to the device, call the
+C ABI through the binding with NaN-poisoned outputs, and get oracle results
+(optionally on a sample of weight rows, for full-size shapes)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from iq4_xs_quantized_gb300 import binding as B
+
+BLOCK_BYTES = 136
+
+
+def dev(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def quantize_gpu(x: np.ndarray, tc: bool = True):
+    """Q8_1 on the GPU with every output poisoned first."""
+    M, K = x.shape
+    xd = dev(x)
+    qs, ds, op = B.alloc_activations(M, K, "cuda", tc=tc)
+    qs.fill_(0x55)
+    ds.view(torch.int16).fill_(0x7E00)  # fp16 NaN
+    if op is not None:
+        op.fill_(0xFF)  # fp16 NaN pattern / fp32 NaN in the scale part
+    B.iq4xs_quantize_q8_1(xd, qs, ds, op)
+    return qs, ds, op
+
+
+def matmul_gpu(wd: torch.Tensor, N: int, K: int, qs, ds, op, M: int, path, ldy: int | None = None):
+    ldy = N if ldy is None else ldy
+    y = torch.full((M, ldy), float("nan"), dtype=torch.float32, device="cuda")
+    B.iq4xs_matmul(wd, N, K, qs, ds, op, M, y, path)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def oracle_q8(x: np.ndarray):
+    return oracle.get().quantize_q8_1(x)
+
+
+def oracle_matmul(w: np.ndarray, N: int, K: int, qs: np.ndarray, d_h: np.ndarray, rows=None):
+    """Oracle y [M, N] (fp64), or y[:, rows] computed on those rows only."""
+    orc = oracle.get()
+    nt = max(1, min(16, oracle.threads_available()))
+    if rows is None:
+        return orc.matmul(w, N, K, qs, d_h, nthreads=nt)
+    wr = np.ascontiguousarray(w.reshape(N, -1)[rows])
+    return orc.matmul(wr, len(rows), K, qs, d_h, nthreads=nt)
+
+
+def sample_rows(N: int, count: int, seed: int = 0) -> np.ndarray:
+    """Rows spanning the first and last 128-row tiles plus random ones."""
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 127, 128, N // 2, N - 129, N - 2, N - 1]
+    fixed = [r for r in fixed if 0 <= r < N]
+    extra = rng.choice(N, size=min(N, max(0, count - len(fixed))), replace=False)
+    return np.unique(np.concatenate([np.array(fixed, dtype=np.int64), extra.astype(np.int64)]))
+
+
+def independent_fp32(w: np.ndarray, N: int, K: int, qs: np.ndarray, d_h: np.ndarray, rows=None):
+    """Independent check path: the oracle's exact fp32 dequantization of W and
+    the dequantized Q8_1 activations, multiplied by torch on the GPU in fp32
+    with TF32 disabled (different code, different summation order)."""
+    orc = oracle.get()
+    wr = w.reshape(N, -1) if rows is None else np.ascontiguousarray(w.reshape(N, -1)[rows])
+    n = wr.shape[0]
+    W = orc.dequantize(wr, n, K)
+    xhat = qs.astype(np.float32) * np.repeat(d_h.view(np.float16).astype(np.float32), 32, axis=1)
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        y = (dev(xhat) @ dev(W).T).cpu().numpy()
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    return y

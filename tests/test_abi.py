@@ -1,0 +1,93 @@
+"""The C ABI library on the host: it builds, loads, exports every function
+include/iq4xs.h declares, and its host-only entry points (path selection,
+argument validation) behave without touching a GPU."""
+import ctypes
+import os
+
+import pytest
+
+from iq4_xs_quantized_gb300 import binding as B
+from iq4_xs_quantized_gb300 import build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return B.load()
+
+
+def test_header_declares_the_entry_points():
+    names = set(B.header_functions())
+    assert {"iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_dequantize", "iq4xs_select_path",
+            "iq4xs_tc_operand_bytes", "iq4xs_set_crossover", "iq4xs_last_device_error",
+            "iq4xs_status_string"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in B.header_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_select_path_and_crossover(lib):
+    B.iq4xs_set_crossover(4)
+    assert B.iq4xs_select_path(1, 4096, 4096) == B.PATH_DP4A
+    assert B.iq4xs_select_path(4, 4096, 4096) == B.PATH_DP4A
+    assert B.iq4xs_select_path(5, 4096, 4096) == B.PATH_TC
+    assert B.iq4xs_select_path(96, 4096, 4096) == B.PATH_TC
+    # K % 512 != 0 cannot take the tensor-core path
+    assert B.iq4xs_select_path(96, 4096, 256 * 3) == B.PATH_DP4A
+    B.iq4xs_set_crossover(0)
+    assert B.iq4xs_select_path(1, 4096, 4096) == B.PATH_TC
+    B.iq4xs_set_crossover(4)
+    out = ctypes.c_int()
+    assert lib.iq4xs_select_path(0, 1, 256, ctypes.byref(out)) == B.ERR_SHAPE
+    assert lib.iq4xs_select_path(1, 1, 100, ctypes.byref(out)) == B.ERR_SHAPE
+    assert lib.iq4xs_select_path(1, 1, 256, None) == B.ERR_ARG
+    assert lib.iq4xs_set_crossover(-1) == B.ERR_ARG
+
+
+def test_tc_operand_bytes(lib):
+    # M rounds up to a multiple of 16 (max 128 per tile): fp16 q + fp32 scale per 32
+    assert B.iq4xs_tc_operand_bytes(1, 1024) == 16 * 1024 * 2 + 16 * 32 * 4
+    assert B.iq4xs_tc_operand_bytes(96, 4096) == 96 * 4096 * 2 + 96 * 128 * 4
+    assert B.iq4xs_tc_operand_bytes(129, 512) == 2 * 128 * 512 * 2 + 2 * 128 * 16 * 4
+    assert B.iq4xs_tc_operand_bytes(0, 1024) == 0
+    assert B.iq4xs_tc_operand_bytes(4, 1000) == 0
+
+
+def test_argument_errors_return_before_any_launch(lib):
+    p = ctypes.c_void_p(0x10000)      # never dereferenced: validation fails first
+    odd = ctypes.c_void_p(0x10008)
+    vp = ctypes.c_void_p
+    # null pointers
+    assert lib.iq4xs_matmul(None, 8, 256, p, p, p, 1, p, 8, 0, 0) == B.ERR_ARG
+    assert lib.iq4xs_quantize_q8_1(None, 1, 256, 256, p, p, None, 0) == B.ERR_ARG
+    assert lib.iq4xs_dequantize(p, 8, 256, None, 0, 0) == B.ERR_ARG
+    # shapes
+    assert lib.iq4xs_matmul(p, 8, 300, p, p, p, 1, p, 8, 0, 0) == B.ERR_SHAPE
+    assert lib.iq4xs_matmul(p, 8, 256, p, p, p, 0, p, 8, 0, 0) == B.ERR_SHAPE
+    assert lib.iq4xs_matmul(p, 0, 256, p, p, p, 1, p, 8, 0, 0) == B.ERR_SHAPE
+    assert lib.iq4xs_quantize_q8_1(p, 1, 100, 100, p, p, None, 0) == B.ERR_SHAPE
+    # bad ldy / ldx / path / dtype
+    assert lib.iq4xs_matmul(p, 8, 256, p, p, p, 1, p, 4, 0, 0) == B.ERR_ARG
+    assert lib.iq4xs_matmul(p, 8, 256, p, p, p, 1, p, 8, 7, 0) == B.ERR_ARG
+    assert lib.iq4xs_quantize_q8_1(p, 1, 256, 255, p, p, None, 0) == B.ERR_ARG
+    assert lib.iq4xs_dequantize(p, 8, 256, p, 5, 0) == B.ERR_ARG
+    # alignment
+    assert lib.iq4xs_matmul(odd, 8, 256, p, p, p, 1, p, 8, 1, 0) == B.ERR_ALIGN
+    assert lib.iq4xs_quantize_q8_1(odd, 1, 256, 256, p, p, None, 0) == B.ERR_ALIGN
+    # the tensor-core path needs K % 512 == 0 and its operand
+    assert lib.iq4xs_matmul(p, 8, 768, p, p, p, 1, p, 8, 2, 0) == B.ERR_SHAPE
+    assert lib.iq4xs_matmul(p, 8, 512, p, p, None, 1, p, 8, 2, 0) == B.ERR_ARG
+
+
+@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="host without a GPU only")
+def test_valid_call_without_gpu_reports_device_error(lib):
+    p = ctypes.c_void_p(0x10000)
+    assert lib.iq4xs_matmul(p, 8, 256, p, p, p, 1, p, 8, 1, 0) == B.ERR_DEVICE
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert B.iq4xs_status_string(s)

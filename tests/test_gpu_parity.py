@@ -1,0 +1,265 @@
+"""CUDA path vs the CPU oracle, through the C ABI (needs an sm_103 GPU).
+
+Q8_1 codes and scales are compared bit for bit; the matmul per output row
+within 1e-5 relative to the fp64 oracle; every output buffer is NaN-poisoned
+before the call and must come back fully written; an independent fp32
+dequantize + matmul must differ from the result by a nonzero amount within
+2e-3.  Full-size shapes are checked on sampled weight rows in the launch
+configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _gates import gate_independent, gate_parity, gate_written
+from _gpu import (dev, independent_fp32, matmul_gpu, oracle_matmul, oracle_q8, quantize_gpu,
+                  sample_rows)
+from _pins import make_block, parse_q8_cases
+from iq4_xs_quantized_gb300 import binding as B
+from iq4_xs_quantized_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+PATHS = ("dp4a", "tc")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from iq4_xs_quantized_gb300 import build
+    build.build()
+    B.load()
+    yield
+    assert B.iq4xs_last_device_error() == 0
+
+
+def check_q8(x, qs, ds):
+    qs_o, d_o, s_o = oracle_q8(x)
+    assert np.array_equal(qs.cpu().numpy(), qs_o)
+    dsn = ds.cpu().numpy().view(np.uint16)
+    assert np.array_equal(dsn[..., 0], d_o)
+    assert np.array_equal(dsn[..., 1], s_o)
+    return qs_o, d_o
+
+
+def run_and_gate(w, N, K, x, path, rows=None, ldy=None, independent=True):
+    qs, ds, op = quantize_gpu(x, tc=(path != "dp4a"))
+    qs_o, d_o = check_q8(x, qs, ds)
+    M = x.shape[0]
+    y = matmul_gpu(dev(w), N, K, qs, ds, op, M, path, ldy=ldy)
+    assert gate_written(y[:, :N]) is None, gate_written(y[:, :N])
+    if ldy is not None and ldy > N:
+        assert np.all(np.isnan(y[:, N:])), "columns beyond N must not be written"
+    y = y[:, :N]
+    ys = y if rows is None else y[:, rows]
+    yo = oracle_matmul(w, N, K, qs_o, d_o, rows)
+    r = gate_parity(ys, yo)
+    assert r is None, r
+    if independent:
+        yi = independent_fp32(w, N, K, qs_o, d_o, rows)
+        r = gate_independent(ys, yi)
+        assert r is None, r
+    return y, yo
+
+
+# --------------------------------------------------------------------------- Q8_1
+@pytest.mark.parametrize("wl,M", [("tiny_256x1024", 8), ("square_4096x4096", 96),
+                                  ("decoder27b_9proj", 64), ("prefill_sweep", 512)])
+def test_quantize_bit_exact(wl, M):
+    W = synth.WORKLOADS[wl]
+    idx = 0 if wl != "prefill_sweep" else 1
+    _, K = W.shapes[idx]
+    x = synth.activations(W.rng(idx, 99), M, K, W.outlier_frac, bf16_round=W.bf16_round)
+    qs, ds, _ = quantize_gpu(x)
+    check_q8(x, qs, ds)
+
+
+def test_quantize_closed_forms():
+    cases = parse_q8_cases()
+    x = np.zeros((len(cases), 256), np.float32)
+    for i, c in enumerate(cases):
+        x[i, :32] = c["x"]
+        x[i, 32:64] = -c["x"] * np.float32(0.125)
+    qs, ds, _ = quantize_gpu(x)
+    check_q8(x, qs, ds)
+    q = qs.cpu().numpy()
+    for i, c in enumerate(cases):
+        assert np.array_equal(q[i, :32], c["q"]), c["name"]
+
+
+# ------------------------------------------------------------------ matmul, tiny
+TINY_MS_TC = (1, 2, 3, 8, 16, 17, 31, 33, 48, 64, 80, 96, 112, 127, 128, 129, 200, 257)
+
+
+@pytest.mark.parametrize("M", (1, 2, 3, 4, 5, 8, 9, 16))
+def test_matmul_tiny_dp4a(M):
+    w, x = synth.TINY.inputs(0, M=M)
+    run_and_gate(w, 256, 1024, x, "dp4a")
+
+
+@pytest.mark.parametrize("M", TINY_MS_TC)
+def test_matmul_tiny_tc(M):
+    w, x = synth.TINY.inputs(0, M=M)
+    run_and_gate(w, 256, 1024, x, "tc")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("N", (1, 7, 130, 200, 383))
+def test_matmul_ragged_n(path, N):
+    rng = np.random.default_rng(N)
+    w = synth.iq4xs_weights(rng, N, 1024, 2e-3)
+    for M in (1, 5, 40):
+        x = synth.activations(rng, M, 1024)
+        run_and_gate(w, N, 1024, x, path)
+
+
+@pytest.mark.parametrize("K", (512, 1536, 2560, 5120, 7168))
+@pytest.mark.parametrize("path", PATHS)
+def test_matmul_k_variants(K, path):
+    rng = np.random.default_rng(K)
+    w = synth.iq4xs_weights(rng, 384, K, 1e-3)
+    for M in (3, 24):
+        x = synth.activations(rng, M, K, outlier_frac=0.01)
+        run_and_gate(w, 384, K, x, path)
+
+
+def test_matmul_k256_dp4a_only():
+    rng = np.random.default_rng(5)
+    w = synth.iq4xs_weights(rng, 64, 256, 2e-3)
+    x = synth.activations(rng, 4, 256)
+    run_and_gate(w, 64, 256, x, "dp4a")
+    qs, ds, op = quantize_gpu(x)
+    y = torch.empty((4, 64), dtype=torch.float32, device="cuda")
+    with pytest.raises(B.IQ4XSError) as e:
+        B.iq4xs_matmul(dev(w), 64, 256, qs, ds, op, 4, y, "tc")
+    assert e.value.status == B.ERR_SHAPE
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_matmul_ldy_padding(path):
+    w, x = synth.TINY.inputs(0, M=6)
+    run_and_gate(w, 256, 1024, x, path, ldy=300)
+
+
+# ---------------------------------------------------------- exactness, degenerate
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M", (1, 16, 96))
+def test_matmul_integer_exact(path, M):
+    """d = 1, ls = 33 and integer activations with a +-127 in every block make
+    every scale 1: y is an integer below 2^24 and must match exactly."""
+    rng = np.random.default_rng(M)
+    N, K = 256, 1024
+    w = np.stack([np.concatenate([make_block(1.0, [33] * 8, rng.integers(0, 256, 128))
+                                  for _ in range(K // 256)]) for _ in range(N)])
+    x = rng.integers(-126, 127, (M, K)).astype(np.float32)
+    x[:, ::32] = 127 * rng.choice([-1, 1], (M, K // 32))
+    y, yo = run_and_gate(w, N, K, x, path, independent=False)
+    assert np.array_equal(y.astype(np.float64), yo)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_matmul_zero_scales_and_zero_activations(path):
+    rng = np.random.default_rng(3)
+    N, K, M = 256, 1024, 20
+    w = np.stack([np.concatenate([make_block(0.5, [32] * 8, rng.integers(0, 256, 128))
+                                  for _ in range(K // 256)]) for _ in range(N)])
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    y, _ = run_and_gate(w, N, K, x, path, independent=False)
+    assert np.all(y == 0)
+    w2, _ = synth.TINY.inputs(0, M=1)
+    y2, _ = run_and_gate(w2, N, K, np.zeros((M, K), np.float32), path, independent=False)
+    assert np.all(y2 == 0)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_matmul_extreme_magnitudes(path):
+    """Largest fp16 d with the largest |ls-32| and |kv|; activations near the
+    top of the fp16 scale range and down in its subnormal range."""
+    rng = np.random.default_rng(4)
+    N, K, M = 128, 512, 4
+    w = np.stack([np.concatenate([make_block(65504.0, rng.choice([0, 63], 8), rng.integers(0, 256, 128))
+                                  for _ in range(K // 256)]) for _ in range(N)])
+    x = (rng.standard_normal((M, K)) * 1e5).astype(np.float32)
+    run_and_gate(w, N, K, x, path)
+    # activation scales in the fp16 subnormal range
+    run_and_gate(w, N, K, (x * np.float32(1e-10)).astype(np.float32), path)
+
+
+# ------------------------------------------------ full-size shapes, sampled rows
+def _full_case(wl, shape_index, M, path, nrows=48):
+    W = synth.WORKLOADS[wl]
+    N, K = W.shapes[shape_index]
+    w, x = W.inputs(shape_index, M=M)
+    run_and_gate(w, N, K, x, path, rows=sample_rows(N, nrows, seed=M))
+
+
+@pytest.mark.parametrize("M", synth.SQUARE.ms)
+def test_full_square(M):
+    B.iq4xs_set_crossover(4)
+    path = "dp4a" if B.iq4xs_select_path(M, 4096, 4096) == B.PATH_DP4A else "tc"
+    _full_case("square_4096x4096", 0, M, path)
+    if M <= 16:
+        _full_case("square_4096x4096", 0, M, "tc" if path == "dp4a" else "dp4a")
+
+
+@pytest.mark.parametrize("shape_index", range(9))
+def test_full_decoder_shapes(shape_index):
+    for M, path in ((1, "dp4a"), (16, "tc"), (64, "tc")):
+        _full_case("decoder27b_9proj", shape_index, M, path, nrows=24)
+
+
+@pytest.mark.parametrize("M", (96, 256, 512))
+@pytest.mark.parametrize("shape_index", (0, 1))
+def test_full_prefill(shape_index, M):
+    _full_case("prefill_sweep", shape_index, M, "tc", nrows=16)
+
+
+# ------------------------------------------------------------------- dequantize
+def test_dequantize_bit_exact():
+    rng = np.random.default_rng(21)
+    N, K = 300, 2048
+    w = synth.iq4xs_weights(rng, N, K, 2e-3)
+    f32_o, b16_o = oracle.get().dequantize(w, N, K, bf16=True)
+    wd = dev(w)
+    out = torch.full((N, K), float("nan"), dtype=torch.float32, device="cuda")
+    B.iq4xs_dequantize(wd, N, K, out)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), f32_o.view(np.uint32))
+    outb = torch.full((N, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    B.iq4xs_dequantize(wd, N, K, outb)
+    assert np.array_equal(outb.view(torch.int16).cpu().numpy().view(np.uint16), b16_o)
+
+
+# --------------------------------------------------------------------- dispatch
+def test_auto_matches_explicit_path():
+    w, x = synth.TINY.inputs(0, M=8)
+    qs, ds, op = quantize_gpu(x)
+    wd = dev(w)
+    for cross in (2, 8):
+        B.iq4xs_set_crossover(cross)
+        expect = "dp4a" if 8 <= cross else "tc"
+        ya = matmul_gpu(wd, 256, 1024, qs, ds, op, 8, "auto")
+        ye = matmul_gpu(wd, 256, 1024, qs, ds, op, 8, expect)
+        assert np.array_equal(ya, ye)
+    B.iq4xs_set_crossover(4)
+
+
+# ------------------------------------------------------------ negative controls
+def test_gate_fires_when_no_kernel_runs():
+    y = torch.full((4, 256), float("nan"), device="cuda").cpu().numpy()
+    assert gate_written(y) is not None
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_gate_fires_on_one_corrupted_weight_byte(path):
+    """Plant one flipped qs byte in the oracle's copy of W: the parity gate
+    must fail for the row that holds it."""
+    w, x = synth.TINY.inputs(0, M=4)
+    qs, ds, op = quantize_gpu(x, tc=True)
+    qs_o, d_o, _ = oracle_q8(x)
+    y = matmul_gpu(dev(w), 256, 1024, qs, ds, op, 4, path)
+    bad = w.copy()
+    bad[17, 136 * 2 + 8 + 40] ^= 0x5A
+    assert gate_parity(y, oracle_matmul(w, 256, 1024, qs_o, d_o)) is None
+    assert gate_parity(y, oracle_matmul(bad, 256, 1024, qs_o, d_o)) is not None
