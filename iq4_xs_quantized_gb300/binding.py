@@ -65,7 +65,16 @@ def load(path: str | None = None):
             getattr(lib, name).restype = ci
         if path is None:
             _lib = lib
+            _install_calibration(lib)
         return lib
+
+
+def _install_calibration(lib):
+    """Apply the measured dp4a/tcgen05 crossover, if one has been calibrated."""
+    from . import calibrate
+    table = calibrate.load_table()
+    if table and "crossover_m_max_dp4a" in table:
+        lib.iq4xs_set_crossover(int(table["crossover_m_max_dp4a"]))
 
 
 def _check(fn: str, rc: int):

@@ -1,0 +1,109 @@
+"""Measure the dp4a <-> tcgen05 crossover and store it for the dispatcher.
+
+The engine page's dispatcher hard-coded its mmvq -> dequantize threshold at
+M=8 while the measured crossover sat near M=15 (V100TPS engine page, mmvq vs
+dequantize table).  Here the crossover is measured: for every M in 1..16 and
+every calibration shape, both kernel paths are timed from CUDA-graph replays
+over rotating weight copies (inputs larger than L2); the dispatcher's
+threshold becomes the largest M at which the dp4a path is faster summed over
+the shapes.  The result is written to ``dispatch_table.json`` beside this file
+and installed with ``iq4xs_set_crossover`` whenever the binding loads.
+
+Run on the GPU:  python -m iq4_xs_quantized_gb300.calibrate
+"""
+from __future__ import annotations
+
+import json
+import os
+import sys
+
+import numpy as np
+
+TABLE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "dispatch_table.json")
+SHAPES = ((4096, 4096), (5120, 5120), (12288, 5120), (5120, 17408))
+MS = tuple(range(1, 17))
+L2_MULTIPLE = 3
+L2_BYTES = 129 * 2**20
+
+
+def time_path(B, torch, wcopies, N, K, M, path, reps=20):
+    qs, ds, op = B.alloc_activations(M, K, "cuda", tc=True)
+    x = torch.randn(M, K, device="cuda")
+    y = torch.empty(M, N, device="cuda")
+    B.iq4xs_quantize_q8_1(x, qs, ds, op)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for w in wcopies:
+            B.iq4xs_matmul(w, N, K, qs, ds, op, M, y, path, s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for w in wcopies:
+            B.iq4xs_matmul(w, N, K, qs, ds, op, M, y, path, s)
+    with torch.cuda.stream(s):
+        g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        t0.record(s)
+        for _ in range(reps):
+            g.replay()
+        t1.record(s)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) * 1e3 / (reps * len(wcopies))  # us per call
+
+
+def calibrate(shapes=SHAPES, ms=MS, verbose=True):
+    import torch
+
+    from . import binding as B
+    from . import synth
+    rng = np.random.default_rng(123)
+    per_shape = {}
+    total = {M: {"dp4a": 0.0, "tc": 0.0} for M in ms}
+    for N, K in shapes:
+        w = torch.from_numpy(synth.iq4xs_weights(rng, N, K, 1e-3)).cuda()
+        ncopy = max(2, int(np.ceil(L2_MULTIPLE * L2_BYTES / w.numel())))
+        wcopies = [w] + [w.clone() for _ in range(ncopy - 1)]
+        rows = {}
+        for M in ms:
+            t_dp = time_path(B, torch, wcopies, N, K, M, B.PATH_DP4A)
+            t_tc = time_path(B, torch, wcopies, N, K, M, B.PATH_TC)
+            rows[M] = {"dp4a_us": round(t_dp, 3), "tc_us": round(t_tc, 3)}
+            total[M]["dp4a"] += t_dp
+            total[M]["tc"] += t_tc
+            if verbose:
+                print(f"N={N} K={K} M={M}: dp4a {t_dp:.2f} us  tc {t_tc:.2f} us", flush=True)
+        per_shape[f"{N}x{K}"] = rows
+        del wcopies, w
+        torch.cuda.empty_cache()
+    crossover = 0
+    for M in ms:
+        if total[M]["dp4a"] < total[M]["tc"]:
+            crossover = M
+        else:
+            break
+    table = {"crossover_m_max_dp4a": crossover, "gpu": torch.cuda.get_device_name(),
+             "shapes": per_shape,
+             "rule": "largest M (scanning up from 1) at which the dp4a path is faster "
+                     "summed over the calibration shapes"}
+    return table
+
+
+def load_table():
+    try:
+        with open(TABLE) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def main():
+    table = calibrate()
+    with open(TABLE, "w") as f:
+        json.dump(table, f, indent=1)
+    print(json.dumps({"crossover_m_max_dp4a": table["crossover_m_max_dp4a"]}))
+
+
+if __name__ == "__main__":
+    sys.exit(main())

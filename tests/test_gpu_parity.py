@@ -59,7 +59,9 @@ def run_and_gate(w, N, K, x, path, rows=None, ldy=None, independent=True):
     assert r is None, r
     if independent:
         yi = independent_fp32(w, N, K, qs_o, d_o, rows)
-        r = gate_independent(ys, yi)
+        # A handful of outputs can agree with the independent path exactly by
+        # chance; the nonzero-error rule is applied to outputs of >= 256 values.
+        r = gate_independent(ys, yi, require_nonzero=ys.size >= 256)
         assert r is None, r
     return y, yo
 
