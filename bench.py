@@ -59,6 +59,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ms", default=None,
                     help="comma-separated subset of the M sweep (profiling runs only)")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="launch without programmatic dependent launch (for serialised profilers)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the dequantize+GEMM baseline and the decode-stream workload")
     return ap.parse_args()
 
 
@@ -198,10 +202,10 @@ def max_over_ranks(value: float, world: int) -> float:
 
 
 # ---------------------------------------------------------------- CPU oracle leg
-def oracle_sample(rows: int, threads: int):
+def oracle_sample(rows: int, threads: int, min_seconds: float = 0.0):
     """Time the CPU oracle (as it stands) on the square workload restricted to
-    the first `rows` weight rows, every M of the sweep.  Returns
-    (GB/s, seconds, sample description)."""
+    the first `rows` weight rows, every M of the sweep, repeating the sweep
+    until `min_seconds` have passed.  Returns (GB/s, seconds, description)."""
     import oracle
     from iq4_xs_quantized_gb300 import synth
     W = synth.SQUARE
@@ -209,14 +213,19 @@ def oracle_sample(rows: int, threads: int):
     w, x = W.inputs(0)
     wr = np.ascontiguousarray(w[:rows])
     orc = oracle.get()
+    passes = 0
     t0 = time.perf_counter()
-    for M in W.ms:
-        qs, d_h, _ = orc.quantize_q8_1(x[:M])
-        orc.matmul(wr, rows, K, qs, d_h, nthreads=threads)
-    dt = time.perf_counter() - t0
-    nbytes = step_bytes(W.ms, rows, K)
+    while True:
+        for M in W.ms:
+            qs, d_h, _ = orc.quantize_q8_1(x[:M])
+            orc.matmul(wr, rows, K, qs, d_h, nthreads=threads)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    nbytes = passes * step_bytes(W.ms, rows, K)
     desc = (f"weight rows 0..{rows - 1} of 4096 (K=4096), all M in {list(W.ms)}, "
-            f"quantize + matmul, {threads} threads")
+            f"quantize + matmul, {passes} pass(es), {threads} threads")
     return nbytes / dt / 1e9, dt, desc
 
 
@@ -262,6 +271,7 @@ def run_ours(args, world, rank, local):
 
     build.build()
     B.load()
+    B.iq4xs_set_pdl(not args.no_pdl)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     W = synth.SQUARE
@@ -354,12 +364,19 @@ def run_ours(args, world, rank, local):
     tops = world * step_ops(ms, N, K) / (ms_per_step * 1e-3) / 1e12
 
     e2e = run_e2e(args, dev, w_np, x_np, ms, N, K, world, wcopies, paths)
+    extras = {}
+    if not args.no_extras and not args.ms:
+        extras["baseline_dequant_gemm"] = baseline_times(torch, B, stream, ms, N, K, wcopies,
+                                                         xs, mm_us)
+        del wcopies, acts, ys, graphs
+        torch.cuda.empty_cache()
+        extras["decode_stream"] = decode_stream(torch, B, dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         threads = oracle.threads_available()
-        v, dt, desc = oracle_sample(256, threads)
+        v, dt, desc = oracle_sample(4096, threads, min_seconds=10.0)
         cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
                "seconds": round(dt, 2)}
 
@@ -375,6 +392,7 @@ def run_ours(args, world, rank, local):
                        "l2": f"inputs larger than L2: {N_COPIES} rotating weight copies "
                              f"({N_COPIES * N * K * 17 // 32 / 1e6:.0f} MB)",
                        "graph": "one CUDA graph replay per step",
+                       "pdl": not args.no_pdl,
                        "parallelism": f"replicas x{world}"},
             "tops": tops,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -384,6 +402,7 @@ def run_ours(args, world, rank, local):
                          "timing": mm_timing},
             "per_m": per_m,
             "e2e": e2e,
+            **extras,
             "gpu_launches": args.steps * 2 * len(ms),
             "clocks": clk,
             "cpu_baseline": cpu,
@@ -420,6 +439,89 @@ def matmul_only_times(torch, B, stream, ms, N, K, wcopies, acts, ys, paths, reps
         torch.cuda.synchronize()
         out[M] = t0.elapsed_time(t1) * 1e3 / (reps * len(wcopies))
     return out
+
+
+def baseline_times(torch, B, stream, ms, N, K, wcopies, xs, mm_us, reps=10):
+    """The path the batched kernel replaces (engine page, kernel table at M=64):
+    dequantize the whole weight to bf16 (this library's kernel), then a dense
+    bf16 GEMM (torch/cuBLAS) on bf16 activations.  Same rotating weight
+    copies, per-call device time from graph replays."""
+    wbf = torch.empty((N, K), dtype=torch.bfloat16, device=wcopies[0].device)
+    out = []
+    for M in ms:
+        xb = xs[M].to(torch.bfloat16)
+        with torch.cuda.stream(stream):  # eager first: cuBLAS sets up outside capture
+            B.iq4xs_dequantize(wcopies[0], N, K, wbf, stream)
+            torch.matmul(xb, wbf.t())
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for w in wcopies:
+                B.iq4xs_dequantize(w, N, K, wbf, stream)
+                torch.matmul(xb, wbf.t())
+        with torch.cuda.stream(stream):
+            g.replay()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+        us = t0.elapsed_time(t1) * 1e3 / (reps * len(wcopies))
+        out.append({"M": M, "us": round(us, 3), "speedup_of_iq4xs_matmul": round(us / mm_us[M], 2)})
+        del g
+    return out
+
+
+def decode_stream(torch, B, dev, reps=5):
+    """Decode-step weight streaming: 64 decoder layers x 4 projections
+    (12288x5120, 5120x6144, 34816x5120, 5120x17408; 12.3 GB of IQ4_XS resident),
+    a fresh activation batch per call, each call = quantize + matmul, all 256
+    calls of a step captured in one CUDA graph.  One layer's matrices are drawn
+    from the seeded generator and replicated to 64 distinct device copies."""
+    from iq4_xs_quantized_gb300 import synth
+    W = synth.DECODE_STREAM
+    layer0 = [torch.from_numpy(W.weights(i, 0)).to(dev) for i in range(len(W.shapes))]
+    layers = [layer0] + [[w.clone() for w in layer0] for _ in range(W.layers - 1)]
+    wbytes = sum(w.numel() for w in layer0) * W.layers
+    stream = torch.cuda.Stream(device=dev)
+    res = []
+    for M in W.ms:
+        g = torch.Generator(device=dev)
+        g.manual_seed(W.seed * 1000 + M)
+        calls = []
+        for l in range(W.layers):
+            for i, (N, K) in enumerate(W.shapes):
+                x = torch.randn((M, K), device=dev, generator=g)
+                qs, ds, op = B.alloc_activations(M, K, dev, tc=True)
+                y = torch.empty((M, N), dtype=torch.float32, device=dev)
+                calls.append((layers[l][i], N, K, x, qs, ds, op, y, B.iq4xs_select_path(M, N, K)))
+
+        def step():
+            for (w, N, K, x, qs, ds, op, y, path) in calls:
+                B.iq4xs_quantize_q8_1(x, qs, ds, op, stream)
+                B.iq4xs_matmul(w, N, K, qs, ds, op, M, y, path, stream)
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        with torch.cuda.stream(stream):
+            graph.replay()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+        ms_step = t0.elapsed_time(t1) / reps
+        nbytes = sum(matmul_bytes(M, N, K) + quantize_bytes(M, K) for (_, N, K, *_r) in calls)
+        res.append({"M": M, "ms_per_step": round(ms_step, 4), "GBps": round(nbytes / (ms_step * 1e-3) / 1e9, 1),
+                    "weight_GB": round(wbytes / 1e9, 2), "calls": len(calls)})
+        del graph, calls
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_e2e(args, dev, w_np, x_np, ms, N, K, world, wcopies, paths):

@@ -120,6 +120,28 @@ int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const vo
                  int64_t stream);
 
 /*
+ * The projection as one call: y = Q8_1(x) . W^T from fp32 activations
+ * (engine page, kernel table at M=64: the projection op quantizes its
+ * activations with quantize_q8_1 and runs the batched matmul).  Launches the
+ * quantizer into `workspace` and then the matmul on the path
+ * iq4xs_select_path picks; the second launch overlaps the first's tail
+ * (programmatic dependent launch).
+ *   x          fp32 [M][ldx], as for iq4xs_quantize_q8_1.
+ *   workspace  device scratch owned by the caller, 16-byte aligned, at least
+ *              iq4xs_linear_workspace_bytes(M, N, K) bytes; its contents on
+ *              return are the Q8_1 activations (qs, then ds, then the
+ *              tensor-core operand when that path is taken).
+ * Errors as for the two calls it makes; IQ4XS_ERR_ARG if the workspace is
+ * too small.
+ */
+int iq4xs_linear(const void* w, int64_t N, int64_t K, const float* x, int64_t M, int64_t ldx,
+                 float* y, int64_t ldy, void* workspace, int64_t workspace_bytes,
+                 int64_t stream);
+
+/* Workspace bytes iq4xs_linear needs for (M, N, K); 0 if the shape is invalid. */
+int64_t iq4xs_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
  * Dequantize W to a dense [N][K] matrix (engine page, kernel table at M=64:
  * dequantize_block_iq4_xs feeding a dense GEMM -- the baseline the batched
  * kernel replaces).  out_dtype 0 = fp32 (exact), 1 = bfloat16 (RNE of the
@@ -142,6 +164,16 @@ int iq4xs_select_path(int64_t M, int64_t N, int64_t K, int* path_out);
  * Host only.  Defaults to 4 until a calibration sets it.  Thread-safe.
  */
 int iq4xs_set_crossover(int64_t m_max_dp4a);
+
+/*
+ * Programmatic dependent launch (default on): each kernel lets the next one
+ * in the stream start launching early, and a matmul begins streaming W before
+ * the preceding kernel has finished (W is read before that wait, so W must
+ * not be produced by a kernel that triggers its dependents early -- none of
+ * this library's kernels writes W).  Off: every launch waits for the
+ * preceding one in the usual way.  Host only; applies to later launches.
+ */
+int iq4xs_set_pdl(int enable);
 
 /*
  * Read and clear the current device's error word, written by kernels whose

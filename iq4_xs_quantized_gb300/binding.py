@@ -55,12 +55,17 @@ def load(path: str | None = None):
         lib.iq4xs_tc_operand_bytes.restype = i64
         lib.iq4xs_matmul.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, i64, ci, i64]
         lib.iq4xs_dequantize.argtypes = [vp, i64, i64, vp, ci, i64]
+        lib.iq4xs_linear.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, i64]
+        lib.iq4xs_linear_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.iq4xs_linear_workspace_bytes.restype = i64
         lib.iq4xs_select_path.argtypes = [i64, i64, i64, ctypes.POINTER(ci)]
         lib.iq4xs_set_crossover.argtypes = [i64]
+        lib.iq4xs_set_pdl.argtypes = [ci]
+        lib.iq4xs_set_pdl.restype = ci
         lib.iq4xs_last_device_error.argtypes = [ctypes.POINTER(ci)]
         lib.iq4xs_status_string.argtypes = [ci]
         lib.iq4xs_status_string.restype = ctypes.c_char_p
-        for name in ("iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_dequantize",
+        for name in ("iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_dequantize", "iq4xs_linear",
                      "iq4xs_select_path", "iq4xs_set_crossover", "iq4xs_last_device_error"):
             getattr(lib, name).restype = ci
         if path is None:
@@ -121,6 +126,20 @@ def iq4xs_matmul(w, N: int, K: int, qs, ds, tc_operand, M: int, y, path=PATH_AUT
     _check("iq4xs_matmul", rc)
 
 
+def iq4xs_linear_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().iq4xs_linear_workspace_bytes(M, N, K))
+
+
+def iq4xs_linear(w, N: int, K: int, x, y, workspace, stream=None) -> None:
+    """y fp32 [M, ldy] = Q8_1(x) . W^T in one call; workspace: uint8 device
+    tensor of at least iq4xs_linear_workspace_bytes(M, N, K) bytes."""
+    M = x.shape[0]
+    rc = load().iq4xs_linear(_ptr(w), N, K, _ptr(x), M, x.stride(0), _ptr(y), y.stride(0),
+                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             _stream(stream))
+    _check("iq4xs_linear", rc)
+
+
 def iq4xs_dequantize(w, N: int, K: int, out, stream=None) -> None:
     """IQ4_XS -> dense [N, K]; out dtype float32 (exact) or bfloat16 (RNE)."""
     dt = {torch.float32: 0, torch.bfloat16: 1}[out.dtype]
@@ -136,6 +155,10 @@ def iq4xs_select_path(M: int, N: int, K: int) -> int:
 
 def iq4xs_set_crossover(m_max_dp4a: int) -> None:
     _check("iq4xs_set_crossover", load().iq4xs_set_crossover(int(m_max_dp4a)))
+
+
+def iq4xs_set_pdl(enable: bool) -> None:
+    _check("iq4xs_set_pdl", load().iq4xs_set_pdl(1 if enable else 0))
 
 
 def iq4xs_last_device_error() -> int:

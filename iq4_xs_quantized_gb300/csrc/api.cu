@@ -30,6 +30,7 @@ struct DevState {
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 std::atomic<int64_t> g_crossover{4};
+std::atomic<int> g_pdl{1};
 
 // One-time per-device set-up, done with that device current.
 int device_state(DevState** out) {
@@ -79,6 +80,9 @@ int select_path_impl(int64_t M, int64_t N, int64_t K) {
 }
 
 }  // namespace
+
+bool pdl_enabled() { return g_pdl.load() != 0; }
+
 }  // namespace iq4xs
 
 using namespace iq4xs;
@@ -133,6 +137,46 @@ int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const vo
     return from_cuda(launch_matmul_dp4a(w, N, K, qs, ds, M, y, ldy, s));
 }
 
+namespace {
+inline int64_t align16(int64_t v) { return (v + 15) / 16 * 16; }
+struct LinearLayout {
+    int64_t qs, ds, op, total;
+    int path;
+};
+bool linear_layout(int64_t M, int64_t N, int64_t K, LinearLayout* L) {
+    if (M < 1 || M > kMaxM || N < 1 || N > (1 << 30) || K <= 0 || K % kQK || K > (1 << 30))
+        return false;
+    L->path = select_path_impl(M, N, K);
+    L->qs = 0;
+    L->ds = align16(M * K);
+    L->op = L->ds + align16(M * (K / kSub) * 4);
+    L->total = L->op + (L->path == IQ4XS_PATH_TC ? tc_qh_bytes(M, K) + tc_dx_bytes(M, K) : 0);
+    return true;
+}
+}  // namespace
+
+int64_t iq4xs_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    LinearLayout L;
+    return linear_layout(M, N, K, &L) ? L.total : 0;
+}
+
+int iq4xs_linear(const void* w, int64_t N, int64_t K, const float* x, int64_t M, int64_t ldx,
+                 float* y, int64_t ldy, void* workspace, int64_t workspace_bytes,
+                 int64_t stream) {
+    if (!w || !x || !y || !workspace) return IQ4XS_ERR_ARG;
+    LinearLayout L;
+    if (!linear_layout(M, N, K, &L)) return IQ4XS_ERR_SHAPE;
+    if (workspace_bytes < L.total) return IQ4XS_ERR_ARG;
+    if (!aligned(workspace, 16)) return IQ4XS_ERR_ALIGN;
+    uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+    int8_t* qs = reinterpret_cast<int8_t*>(ws + L.qs);
+    void* ds = ws + L.ds;
+    void* op = (L.path == IQ4XS_PATH_TC) ? ws + L.op : nullptr;
+    int rc = iq4xs_quantize_q8_1(x, M, K, ldx, qs, ds, op, stream);
+    if (rc) return rc;
+    return iq4xs_matmul(w, N, K, qs, ds, op, M, y, ldy, L.path, stream);
+}
+
 int iq4xs_dequantize(const void* w, int64_t N, int64_t K, void* out, int out_dtype,
                      int64_t stream) {
     if (!w || !out) return IQ4XS_ERR_ARG;
@@ -155,6 +199,11 @@ int iq4xs_select_path(int64_t M, int64_t N, int64_t K, int* path_out) {
 int iq4xs_set_crossover(int64_t m_max_dp4a) {
     if (m_max_dp4a < 0 || m_max_dp4a > kMaxM) return IQ4XS_ERR_ARG;
     g_crossover.store(m_max_dp4a);
+    return IQ4XS_OK;
+}
+
+int iq4xs_set_pdl(int enable) {
+    g_pdl.store(enable ? 1 : 0);
     return IQ4XS_OK;
 }
 

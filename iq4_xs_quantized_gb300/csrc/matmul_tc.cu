@@ -11,18 +11,21 @@
 // and an activation tile of MT rows (= UMMA N); K is split over a cluster
 // whose CTAs reduce their partial tiles through distributed shared memory.
 //
-//   warp 8 (producer)  TMA: W stages of 2 super-blocks (128 x 272 B, 2D tensor
-//                      map) and activation stages of 4 sub-blocks (bulk copy
-//                      of the pre-tiled fp16 operand).
-//   warp 9 (issuer)    allocates TMEM; one thread issues tcgen05.mma
-//                      128 x MT x 16 twice per sub-block into a fresh TMEM
-//                      accumulator, commits to mbarriers.
-//   warps 0-7          two groups of 4 warps; group g takes the sub-blocks of
-//                      parity g.  Thread t decodes row t's sub-block from the
-//                      staged bytes to exact fp16 in the canonical K-major
-//                      layout, then scales the previous sub-block's TMEM result
-//                      into its fp32 register accumulators.
-//
+// Warp-specialized roles, each a loop over the CTA's sub-blocks, decoupled by
+// mbarrier rings so that no round trip sits on the critical path:
+//   warpgroups 0, 1 (decoders)  sub-blocks of parity g: thread t decodes row
+//                               t's sub-block from the staged W bytes to exact
+//                               fp16 in the canonical K-major layout (A ring)
+//   warp 12 (producer)          TMA: W stages of 2 super-blocks (128 x 272 B,
+//                               2D tensor map); activation stages of 4
+//                               sub-blocks (bulk copies of the pre-tiled fp16
+//                               codes and their fp32 block scales)
+//   warp 13 (issuer)            allocates TMEM; one thread issues two
+//                               tcgen05.mma 128 x MT x 16 per sub-block into a
+//                               fresh TMEM accumulator (kND slots)
+//   warpgroup 2 (epilogue)      thread t loads row t's int-valued fp32 results
+//                               (all columns, then one wait) and scales them by
+//                               d_w*(ls-32)*d_x into fp32 register accumulators
 // Every mbarrier wait is bounded (2 s); a timeout sets the device error word
 // and an abort flag that releases every other wait, the CTA drains its copies
 // and frees its TMEM, and the call's output is undefined.
@@ -33,39 +36,64 @@
 namespace iq4xs {
 namespace {
 
-constexpr int kTcWorkerWarps = 8;
-constexpr int kTcProducerWarp = 8;
-constexpr int kTcIssuerWarp = 9;
-constexpr int kTcThreads = 32 * 10;
-constexpr int kGroups = 2;        // worker groups (sub-block parity)
-constexpr int kSlots = 2;         // A buffers / TMEM accumulators per group
-constexpr int kTmemCols = 512;    // whole TMEM; one CTA per SM (see kMinSmem)
+constexpr int kTcThreads = 32 * 16;   // 4 warpgroups
+constexpr int kDecGroups = 2;         // decoder warpgroups 0, 1 (sub-block parity)
+constexpr int kEpiWarp0 = 8;          // epilogue: warps 8-11
+constexpr int kProducerWarp = 12;
+constexpr int kIssuerWarp = 13;       // warps 14, 15 idle
+constexpr int kTmemCols = 512;        // whole TMEM; one CTA per SM (see kMinSmem)
 constexpr int kMaxCluster = 8;
 constexpr int kMinSmem = 120 * 1024;  // > half of the SM's shared memory: one CTA per SM
+constexpr int kNA = 4;                // A (decoded fp16) slots; decoder g uses slots of parity g
 constexpr int kALbo = kTileN * 16;    // A: byte distance between K-adjacent core matrices
 constexpr int kCoreSbo = 128;         // 8 rows x 16 B core matrices, contiguous along M/N
+// Per-warpgroup register budgets (setmaxnreg).  The block launches with
+// 65536 / 512 = 128 registers per thread; the budgets sum to
+// 128 * (2 * 80 + 248 + 56) = 59392, within the 65536 it holds.
+constexpr int kRegsDecode = 80;
+constexpr int kRegsEpilogue = 248;
+constexpr int kRegsControl = 56;
+static_assert(128 * (kDecGroups * kRegsDecode + kRegsEpilogue + kRegsControl) <= kTcThreads * 128,
+              "register split fits the launch allocation");
+
+template <int R>
+__device__ __forceinline__ void reg_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void reg_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
 
 template <int MT>
 struct TcCfg {
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= kMaxMTile, "UMMA N for M=128");
-    static_assert(kGroups * kSlots * MT <= kTmemCols, "TMEM accumulators fit");
-    static constexpr int kNW = (MT <= 64) ? 3 : 2;            // W stages
-    static constexpr int kNB = 3;                             // activation stages
-    static constexpr int kBStageBytes = kBStageChunks * MT * 16;
+    static constexpr int kND = (kTmemCols / MT) < 8 ? (kTmemCols / MT) : 8;  // TMEM accumulators
+    static_assert(kND >= 4, "at least four accumulators in flight");
+    static constexpr int kNW = (MT <= 64) ? 3 : 2;             // W stages
+    static constexpr int kNB = (MT <= 96) ? 4 : 3;             // activation stages
+    static constexpr int kBQhBytes = kBStageChunks * MT * 16;  // fp16 codes of 4 sub-blocks
+    static constexpr int kBDxBytes = kBStageSubs * MT * 4;     // their fp32 block scales
+    // slot stride, padded to 1 KB; the copies into a slot fill kBQhBytes + kBDxBytes
+    static constexpr int kBStageBytes = (kBQhBytes + kBDxBytes + 1023) / 1024 * 1024;
+    static constexpr int kPartCols = (MT > 64) ? 64 : MT;      // TMEM columns read per wait
     static constexpr int kOffW = 0;
     static constexpr int kOffB = kOffW + kNW * kWStageBytes;
     static constexpr int kOffA = kOffB + kNB * kBStageBytes;
-    static constexpr int kOffBar = kOffA + kGroups * kSlots * kASubBytes;
-    // barriers: W full/empty, B full/empty, per (group, slot): a_full, mma_done, d_free; drain
-    static constexpr int kNumBars = 2 * kNW + 2 * kNB + 3 * kGroups * kSlots + 1;
+    static constexpr int kOffBar = kOffA + kNA * kASubBytes;
+    // W full/empty, B full/empty, A full/free, D full/free, drain
+    static constexpr int kNumBars = 2 * kNW + 2 * kNB + 2 * kNA + 2 * kND + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;   // tmem base, abort flag
     static constexpr int kUsed = kOffMisc + 16;
     static constexpr int kSmem = (kUsed + 1024 > kMinSmem) ? kUsed + 1024 : kMinSmem;
     static constexpr int kRedStride = MT + 1;                  // fp32 words per row
     static_assert(kTileN * kRedStride * 4 <= kNW * kWStageBytes, "reduction tile fits the W ring");
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-    static_assert(kOffB % 1024 == 0 && kOffA % 1024 == 0, "stage alignment");
+    static_assert(kOffB % 1024 == 0 && kOffA % 1024 == 0 && kBStageBytes % 16 == 0, "alignment");
+    static_assert(kPartCols % 16 == 0, "TMEM read granularity");
 };
+
+constexpr int kEpilogueBarrier = 1;  // named barrier id for the 4 epilogue warps
 
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -101,10 +129,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* w_empty = w_full + C::kNW;
     uint64_t* b_full = w_empty + C::kNW;
     uint64_t* b_empty = b_full + C::kNB;
-    uint64_t* a_full = b_empty + C::kNB;          // [g][s]
-    uint64_t* mma_done = a_full + kGroups * kSlots;
-    uint64_t* d_free = mma_done + kGroups * kSlots;
-    uint64_t* drain = d_free + kGroups * kSlots;
+    uint64_t* a_full = b_empty + C::kNB;
+    uint64_t* a_free = a_full + kNA;
+    uint64_t* d_full = a_free + kNA;
+    uint64_t* d_free = d_full + C::kND;
+    uint64_t* drain = d_free + C::kND;
     uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -117,59 +146,78 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int pairs = K / kPairK;
     const int p0 = (int)((int64_t)pairs * rank / S);
     const int p1 = (int)((int64_t)pairs * (rank + 1) / S);
-    const int npairs = p1 - p0;
-    const int nsub = npairs * kSubPerPair;
+    const int nsub = (p1 - p0) * kSubPerPair;
     const int nbst = nsub / kBStageSubs;
     const int64_t K8 = K / kChunkElems, K32 = K / kSub;
     const uint8_t* qh_tile = tc_op + (int64_t)z * K8 * MT * 16;
-    const float* dx_tile =
-        reinterpret_cast<const float*>(tc_op + tc_qh_bytes(M, K)) + (int64_t)z * K32 * MT;
+    const uint8_t* dx_tile = tc_op + tc_qh_bytes(M, K) + (int64_t)z * K32 * MT * 4;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kNW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], kTcWorkerWarps * 32); }
-        for (int i = 0; i < C::kNB; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], 1); }
-        for (int i = 0; i < kGroups * kSlots; ++i) {
-            mbar_init(&a_full[i], 4 * 32);
-            mbar_init(&mma_done[i], 1);
-            mbar_init(&d_free[i], 4 * 32);
+        for (int i = 0; i < C::kNW; ++i) {
+            mbar_init(&w_full[i], 1);
+            mbar_init(&w_empty[i], (kDecGroups + 1) * kTileN);  // both decoders + epilogue
         }
+        for (int i = 0; i < C::kNB; ++i) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_empty[i], 1 + kTileN);  // MMA commit + epilogue (block scales)
+        }
+        for (int i = 0; i < kNA; ++i) { mbar_init(&a_full[i], kTileN); mbar_init(&a_free[i], 1); }
+        for (int i = 0; i < C::kND; ++i) { mbar_init(&d_full[i], 1); mbar_init(&d_free[i], kTileN); }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
     }
-    if (warp == kTcProducerWarp && lane == 0) prefetch_tmap(&tmap_w);
-    if (warp == kTcIssuerWarp) tmem_alloc(tmem_base_ptr, kTmemCols);
+    if (warp == kProducerWarp && lane == 0) prefetch_tmap(&tmap_w);
+    if (warp == kIssuerWarp) tmem_alloc(tmem_base_ptr, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_base_ptr;
+    // Let the next kernel in the stream begin its launch; it waits for this
+    // grid's completion before touching anything this grid reads or writes.
+    griddep_launch_dependents();
 
-    if (warp == kTcProducerWarp) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
+    if (warp >= kProducerWarp) {
+        reg_dealloc<kRegsControl>();
+        if (warp == kProducerWarp && lane == 0) {
+            // ------------------------------------------------------- producer
             int issued_w = 0, issued_b = 0;
             bool ok = true;
+            // W is read-only model state: its first stages stream before the
+            // preceding kernel (which produces the activations) has finished.
+            const int pre = (C::kNW < (p1 - p0)) ? C::kNW : (p1 - p0);
+            for (int ps = 0; ps < pre; ++ps) {
+                mbar_arrive_expect_tx(&w_full[ps], kWStageBytes);
+                tma_load_2d(smem + C::kOffW + ps * kWStageBytes, &tmap_w,
+                            (p0 + ps) * (kPairBytes / 4), n0, &w_full[ps]);
+                ++issued_w;
+            }
+            griddep_wait();
             for (int bs = 0; bs < nbst && ok; ++bs) {
                 if (bs % (kSubPerPair / kBStageSubs) == 0) {
                     const int ps = bs / (kSubPerPair / kBStageSubs);
-                    const int slot = ps % C::kNW;
-                    if (ps >= C::kNW)
-                        ok = mbar_wait(&w_empty[slot], ((ps / C::kNW) - 1) & 1, abort_flag, err, kDevErrTimeoutW);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(&w_full[slot], kWStageBytes);
-                    tma_load_2d(smem + C::kOffW + slot * kWStageBytes, &tmap_w,
-                                (p0 + ps) * (kPairBytes / 4), n0, &w_full[slot]);
-                    ++issued_w;
+                    if (ps >= pre) {
+                        const int slot = ps % C::kNW;
+                        ok = mbar_wait(&w_empty[slot], ((ps / C::kNW) - 1) & 1, abort_flag, err,
+                                       kDevErrTimeoutW);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(&w_full[slot], kWStageBytes);
+                        tma_load_2d(smem + C::kOffW + slot * kWStageBytes, &tmap_w,
+                                    (p0 + ps) * (kPairBytes / 4), n0, &w_full[slot]);
+                        ++issued_w;
+                    }
                 }
                 const int slot = bs % C::kNB;
                 if (bs >= C::kNB)
-                    ok = mbar_wait(&b_empty[slot], ((bs / C::kNB) - 1) & 1, abort_flag, err, kDevErrTimeoutB);
+                    ok = mbar_wait(&b_empty[slot], ((bs / C::kNB) - 1) & 1, abort_flag, err,
+                                   kDevErrTimeoutB);
                 if (!ok) break;
-                mbar_arrive_expect_tx(&b_full[slot], C::kBStageBytes);
-                const int64_t chunk0 = ((int64_t)p0 * kSubPerPair + (int64_t)bs * kBStageSubs) * kChunksPerSub;
-                bulk_load(smem + C::kOffB + slot * C::kBStageBytes, qh_tile + chunk0 * MT * 16,
-                          C::kBStageBytes, &b_full[slot]);
+                uint8_t* dst = smem + C::kOffB + slot * C::kBStageBytes;
+                const int64_t sub0 = (int64_t)p0 * kSubPerPair + (int64_t)bs * kBStageSubs;
+                mbar_arrive_expect_tx(&b_full[slot], C::kBQhBytes + C::kBDxBytes);
+                bulk_load(dst, qh_tile + sub0 * kChunksPerSub * MT * 16, C::kBQhBytes, &b_full[slot]);
+                bulk_load(dst + C::kBQhBytes, dx_tile + sub0 * MT * 4, C::kBDxBytes, &b_full[slot]);
                 ++issued_b;
             }
             // Drain: the last copies issued into each ring slot have landed.
@@ -177,25 +225,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_wait(&w_full[ps % C::kNW], (ps / C::kNW) & 1, abort_flag, err, kDevErrTimeoutDrain);
             for (int bs = (issued_b > C::kNB ? issued_b - C::kNB : 0); bs < issued_b; ++bs)
                 mbar_wait(&b_full[bs % C::kNB], (bs / C::kNB) & 1, abort_flag, err, kDevErrTimeoutDrain);
-        }
-    } else if (warp == kTcIssuerWarp) {
-        // -------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        } else if (warp == kIssuerWarp && lane == 0) {
+            // ----------------------------------------------------- MMA issuer
             constexpr uint32_t idesc = idesc_f16_m128(MT);
             const uint32_t a_base = smem_u32(smem + C::kOffA);
             const uint32_t b_base = smem_u32(smem + C::kOffB);
             bool ok = true;
             for (int li = 0; li < nsub && ok; ++li) {
-                const int g = li & 1, u = li >> 1, s = u & 1, gs = g * kSlots + s;
-                ok = mbar_wait(&a_full[gs], (u >> 1) & 1, abort_flag, err, kDevErrTimeoutA);
-                if (ok && u >= 2) ok = mbar_wait(&d_free[gs], ((u - 2) >> 1) & 1, abort_flag, err, kDevErrTimeoutFree);
+                const int sa = li % kNA, sd = li % C::kND;
+                ok = mbar_wait(&a_full[sa], (li / kNA) & 1, abort_flag, err, kDevErrTimeoutA);
+                if (ok && li >= C::kND)
+                    ok = mbar_wait(&d_free[sd], ((li / C::kND) - 1) & 1, abort_flag, err,
+                                   kDevErrTimeoutFree);
                 const int bs = li / kBStageSubs, bslot = bs % C::kNB;
                 if (ok && li % kBStageSubs == 0)
                     ok = mbar_wait(&b_full[bslot], (bs / C::kNB) & 1, abort_flag, err, kDevErrTimeoutB);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + (uint32_t)(gs * MT);
-                const uint32_t a_addr = a_base + gs * kASubBytes;
+                const uint32_t d_tmem = tmem + (uint32_t)(sd * MT);
+                const uint32_t a_addr = a_base + sa * kASubBytes;
                 const uint32_t b_addr =
                     b_base + bslot * C::kBStageBytes + (li % kBStageSubs) * kChunksPerSub * MT * 16;
 #pragma unroll
@@ -204,112 +252,126 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint64_t bdesc = smem_desc(b_addr + i * 2 * MT * 16, MT * 16, kCoreSbo);
                     tc_mma_f16(d_tmem, adesc, bdesc, idesc, i);
                 }
-                tc_commit(&mma_done[gs]);
+                tc_commit(&a_free[sa]);
+                tc_commit(&d_full[sd]);
                 if (li % kBStageSubs == kBStageSubs - 1) tc_commit(&b_empty[bslot]);
             }
             // Every MMA issued so far has completed before TMEM is released.
             tc_commit(drain);
             mbar_wait(drain, 0, abort_flag, err, kDevErrTimeoutDrain);
         }
-    } else {
-        // ------------------------------------------------------------ workers
-        const int g = warp / 4;
-        const int t = threadIdx.x & (kTileN - 1);  // row within the tile == TMEM lane
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        uint8_t* a_base = smem + C::kOffA;
-        float acc[MT];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------------------ decoders
+        reg_dealloc<kRegsDecode>();
+        const int g = warp >> 2;                   // sub-block parity of this warpgroup
+        const int t = threadIdx.x & (kTileN - 1);  // row within the tile
+        uint8_t* a_row = smem + C::kOffA + t * 16;
         bool ok = true;
-        float S_prev = 0.f;
-        int nu = 0;  // uses issued by this group
-
-        auto epilogue = [&](int v, float Sv) {
-            const int s = v & 1, gs = g * kSlots + s;
-            const int li = g + 2 * v;
-            if (ok) ok = mbar_wait(&mma_done[gs], (v >> 1) & 1, abort_flag, err, kDevErrTimeoutMma);
-            tc_fence_after();
-            const float* dxp = dx_tile + ((int64_t)p0 * kSubPerPair + li) * MT;
-#pragma unroll
-            for (int c = 0; c < MT / 16; ++c) {
-                uint32_t r[16];
-                tmem_ld16(tmem + lane_base + (uint32_t)(gs * MT + 16 * c), r);
-                tc_wait_ld();
-                if (c == MT / 16 - 1) {
-                    tc_fence_before();
-                    mbar_arrive(&d_free[gs]);
-                }
-#pragma unroll
-                for (int k = 0; k < 16; k += 4) {
-                    const float4 d4 = __ldg(reinterpret_cast<const float4*>(dxp + 16 * c + k));
-                    const float2 s01 = __fmul2_rn(make_float2(Sv, Sv), make_float2(d4.x, d4.y));
-                    const float2 s23 = __fmul2_rn(make_float2(Sv, Sv), make_float2(d4.z, d4.w));
-                    float2 a01 = make_float2(acc[16 * c + k], acc[16 * c + k + 1]);
-                    float2 a23 = make_float2(acc[16 * c + k + 2], acc[16 * c + k + 3]);
-                    a01 = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), s01, a01);
-                    a23 = __ffma2_rn(make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])), s23, a23);
-                    acc[16 * c + k] = a01.x;
-                    acc[16 * c + k + 1] = a01.y;
-                    acc[16 * c + k + 2] = a23.x;
-                    acc[16 * c + k + 3] = a23.y;
-                }
-            }
-        };
-
-        for (int li = g; li < nsub; li += kGroups) {
-            const int u = li >> 1, s = u & 1, gs = g * kSlots + s;
+        for (int li = g; li < nsub; li += kDecGroups) {
             const int ps = li / kSubPerPair, jj = li % kSubPerPair, wslot = ps % C::kNW;
-            if (ok && jj < kGroups)
+            if (ok && jj < kDecGroups)
                 ok = mbar_wait(&w_full[wslot], (ps / C::kNW) & 1, abort_flag, err, kDevErrTimeoutW);
-            // Row t's bytes of super-block jj/8 in the staged pair.
             const uint8_t* rowp = smem + C::kOffW + wslot * kWStageBytes + t * kPairBytes +
                                   (jj / kSubPerBlock) * kBlockBytes;
             const int j = jj % kSubPerBlock;
-            const uint2 hdr = *reinterpret_cast<const uint2*>(rowp);
             const uint2 q01 = *reinterpret_cast<const uint2*>(rowp + 8 + 16 * j);
             const uint2 q23 = *reinterpret_cast<const uint2*>(rowp + 16 + 16 * j);
-            if (jj >= kSubPerPair - kGroups) mbar_arrive(&w_empty[wslot]);
-            const float S = iq4xs_scale(hdr.x, hdr.y, j);
+            if (jj >= kSubPerPair - kDecGroups) mbar_arrive(&w_empty[wslot]);
             uint32_t h[16];
             decode_f16x2(q01.x, h + 0);
             decode_f16x2(q01.y, h + 4);
             decode_f16x2(q23.x, h + 8);
             decode_f16x2(q23.y, h + 12);
-            // A[g][s] was last read by the MMA of use u-2, whose completion the
-            // epilogue of use u-2 (run in the previous iteration) waited for.
-            uint8_t* ap = a_base + gs * kASubBytes + t * 16;
+            const int sa = li % kNA;
+            if (ok && li >= kNA)
+                ok = mbar_wait(&a_free[sa], ((li / kNA) - 1) & 1, abort_flag, err, kDevErrTimeoutA);
+            uint8_t* ap = a_row + sa * kASubBytes;
 #pragma unroll
             for (int c = 0; c < kChunksPerSub; ++c)
                 *reinterpret_cast<uint4*>(ap + c * kALbo) =
                     make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
             fence_proxy_async_smem();
-            mbar_arrive(&a_full[gs]);
-            if (u >= 1) epilogue(u - 1, S_prev);
-            S_prev = S;
-            nu = u + 1;
+            mbar_arrive(&a_full[sa]);
         }
-        if (nu >= 1) epilogue(nu - 1, S_prev);
-
-        // Combine the two groups' partial sums in shared memory (the W ring
-        // is idle once every worker has passed the first barrier).
-        float* red = reinterpret_cast<float*>(smem + C::kOffW);
-        named_barrier_sync(1, kTcWorkerWarps * 32);
-        if (g == 1) {
+    } else {
+        // ------------------------------------------------------------ epilogue
+        reg_alloc<kRegsEpilogue>();
+        const int t = threadIdx.x - kEpiWarp0 * 32;  // row within the tile == TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        float acc[MT];
 #pragma unroll
-            for (int m = 0; m < MT; ++m) red[t * C::kRedStride + m] = acc[m];
-        }
-        named_barrier_sync(1, kTcWorkerWarps * 32);
-        if (g == 0) {
-            const int64_t mrows = M - (int64_t)z * MT;
+        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+        bool ok = true;
+        for (int li = 0; li < nsub; ++li) {
+            const int ps = li / kSubPerPair, jj = li % kSubPerPair, wslot = ps % C::kNW;
+            const int bs = li / kBStageSubs, bslot = bs % C::kNB;
+            if (ok && jj == 0)
+                ok = mbar_wait(&w_full[wslot], (ps / C::kNW) & 1, abort_flag, err, kDevErrTimeoutW);
+            const uint8_t* rowp = smem + C::kOffW + wslot * kWStageBytes + t * kPairBytes +
+                                  (jj / kSubPerBlock) * kBlockBytes;
+            const uint2 hdr = *reinterpret_cast<const uint2*>(rowp);
+            if (jj == kSubPerPair - 1) mbar_arrive(&w_empty[wslot]);
+            const float Sw = iq4xs_scale(hdr.x, hdr.y, jj % kSubPerBlock);
+            const float2 Sw2 = make_float2(Sw, Sw);
+            if (ok && li % kBStageSubs == 0)
+                ok = mbar_wait(&b_full[bslot], (bs / C::kNB) & 1, abort_flag, err, kDevErrTimeoutB);
+            const float4* dx4 = reinterpret_cast<const float4*>(
+                smem + C::kOffB + bslot * C::kBStageBytes + C::kBQhBytes + (li % kBStageSubs) * MT * 4);
+            const int sd = li % C::kND;
+            if (ok) ok = mbar_wait(&d_full[sd], (li / C::kND) & 1, abort_flag, err, kDevErrTimeoutMma);
+            tc_fence_after();
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                const float v = acc[m] + red[t * C::kRedStride + m];
-                if (S == 1) {
-                    if (m < mrows && n0 + t < N) y[((int64_t)z * MT + m) * ldy + n0 + t] = v;
-                } else {
-                    red[t * C::kRedStride + m] = v;
+            for (int part = 0; part < MT; part += C::kPartCols) {
+                constexpr int kW = C::kPartCols;  // columns of this part (the last may be narrower)
+                const int cols = (MT - part < kW) ? MT - part : kW;
+                uint32_t r[kW];
+                const uint32_t taddr = tmem + lane_base + (uint32_t)(sd * MT + part);
+                if (cols == 64) tmem_ld64_wait(taddr, r);
+                else if (cols == 48) tmem_ld48_wait(taddr, r);
+                else if (cols == 32) tmem_ld32_wait(taddr, r);
+                else tmem_ld16_wait(taddr, r);
+                if (part + C::kPartCols >= MT) {
+                    tc_fence_before();
+                    mbar_arrive(&d_free[sd]);
+                }
+#pragma unroll
+                for (int k = 0; k < kW; k += 4) {
+                    if (k >= cols) break;
+                    const int m = part + k;
+                    const float4 d = dx4[m / 4];
+                    const float2 s01 = __fmul2_rn(Sw2, make_float2(d.x, d.y));
+                    const float2 s23 = __fmul2_rn(Sw2, make_float2(d.z, d.w));
+                    const float2 a01 =
+                        __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), s01,
+                                   make_float2(acc[m], acc[m + 1]));
+                    const float2 a23 =
+                        __ffma2_rn(make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
+                                   s23, make_float2(acc[m + 2], acc[m + 3]));
+                    acc[m] = a01.x;
+                    acc[m + 1] = a01.y;
+                    acc[m + 2] = a23.x;
+                    acc[m + 3] = a23.y;
                 }
             }
+            if (li % kBStageSubs == kBStageSubs - 1) mbar_arrive(&b_empty[bslot]);
+        }
+        // Partial tile -> y (one CTA) or -> shared memory for the cluster
+        // reduction, which reuses the W ring.  Before any epilogue thread
+        // writes there, all four epilogue warps must have read their last
+        // block headers from it (named barrier); the decoders' last reads of
+        // it preceded the last accumulator these threads waited for, and
+        // every W copy issued has been consumed.
+        const int64_t mrows = M - (int64_t)z * MT;
+        if (S == 1) {
+            griddep_wait();
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (m < mrows && n0 + t < N) y[((int64_t)z * MT + m) * ldy + n0 + t] = acc[m];
+        } else {
+            named_barrier_sync(kEpilogueBarrier, kTileN);
+            float* red = reinterpret_cast<float*>(smem + C::kOffW);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) red[t * C::kRedStride + m] = acc[m];
         }
     }
 
@@ -317,13 +379,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // Split-K reduction over the cluster through distributed shared memory:
         // CTA `rank` sums rows [rank*128/S, (rank+1)*128/S) over all CTAs in
         // rank order (deterministic) and writes them.
+        __syncwarp();
         cluster_sync_all();
-        if (warp < kTcWorkerWarps) {
+        if (warp < kProducerWarp) {
+            griddep_wait();
+            const int64_t mrows = M - (int64_t)z * MT;
             const uint32_t red_s = smem_u32(smem + C::kOffW);
             const int r0 = (int)(kTileN * rank / S), r1 = (int)(kTileN * (rank + 1) / S);
-            const int64_t mrows = M - (int64_t)z * MT;
             const int rows = r1 - r0;
-            for (int e = threadIdx.x; e < rows * MT; e += kTcWorkerWarps * 32) {
+            for (int e = threadIdx.x; e < rows * MT; e += kProducerWarp * 32) {
                 const int row = r0 + e % rows, m = e / rows;
                 float v = 0.f;
                 for (int q = 0; q < S; ++q)
@@ -331,12 +395,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (m < mrows && n0 + row < N) y[((int64_t)z * MT + m) * ldy + n0 + row] = v;
             }
         }
+        __syncwarp();
         cluster_sync_all();
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kTcIssuerWarp) {
+    if (warp == kIssuerWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -366,13 +431,15 @@ cudaError_t launch_mt(const CUtensorMap& tmap, const uint8_t* tc_op, int64_t M, 
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = (unsigned)S;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, matmul_tc_kernel<MT>, tmap, tc_op, M, N, K, y, ldy, err);
 }
 

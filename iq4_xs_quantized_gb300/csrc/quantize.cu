@@ -25,6 +25,10 @@ __global__ void __launch_bounds__(kQuantThreads)
     quantize_q8_1_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
                          int8_t* __restrict__ qs, __half2* __restrict__ ds,
                          uint4* __restrict__ qh, float* __restrict__ dxT, int MT) {
+    // x may come from the preceding grid, and qs/ds/the operand may still be
+    // read by it: wait for it, then let the next grid start launching.
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t m = blockIdx.y;
     const int64_t e0 = (int64_t)blockIdx.x * kElemsPerCta + threadIdx.x * kElemsPerThread;
     if (e0 >= K) return;  // whole warps only (see above)
@@ -97,10 +101,17 @@ cudaError_t launch_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t l
         qh = reinterpret_cast<uint4*>(tc_operand);
         dxT = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tc_operand) + tc_qh_bytes(M, K));
     }
-    dim3 grid((unsigned)((K + kElemsPerCta - 1) / kElemsPerCta), (unsigned)rows);
-    quantize_q8_1_kernel<<<grid, kQuantThreads, 0, stream>>>(
-        x, M, K, ldx, qs, reinterpret_cast<__half2*>(ds), qh, dxT, MT);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((K + kElemsPerCta - 1) / kElemsPerCta), (unsigned)rows);
+    cfg.blockDim = dim3(kQuantThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel, x, M, K, ldx, qs,
+                              reinterpret_cast<__half2*>(ds), qh, dxT, MT);
 }
 
 }  // namespace iq4xs

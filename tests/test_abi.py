@@ -20,7 +20,7 @@ def test_header_declares_the_entry_points():
     names = set(B.header_functions())
     assert {"iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_dequantize", "iq4xs_select_path",
             "iq4xs_tc_operand_bytes", "iq4xs_set_crossover", "iq4xs_last_device_error",
-            "iq4xs_status_string"} <= names
+            "iq4xs_status_string", "iq4xs_linear", "iq4xs_linear_workspace_bytes"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -91,3 +91,17 @@ def test_valid_call_without_gpu_reports_device_error(lib):
 def test_status_strings(lib):
     for s in range(7):
         assert B.iq4xs_status_string(s)
+
+
+def test_linear_workspace_and_validation(lib):
+    B.iq4xs_set_crossover(4)
+    # dp4a path: qs + ds only; tensor-core path adds the operand
+    assert B.iq4xs_linear_workspace_bytes(2, 4096, 4096) == 2 * 4096 + 2 * 128 * 4
+    assert (B.iq4xs_linear_workspace_bytes(96, 4096, 4096) ==
+            96 * 4096 + 96 * 128 * 4 + B.iq4xs_tc_operand_bytes(96, 4096))
+    assert B.iq4xs_linear_workspace_bytes(0, 8, 256) == 0
+    p = ctypes.c_void_p(0x10000)
+    need = B.iq4xs_linear_workspace_bytes(96, 4096, 4096)
+    assert lib.iq4xs_linear(p, 4096, 4096, p, 96, 4096, p, 4096, p, need - 1, 0) == B.ERR_ARG
+    assert lib.iq4xs_linear(p, 4096, 4096, p, 96, 4096, p, 4096, None, need, 0) == B.ERR_ARG
+    assert lib.iq4xs_linear(p, 4096, 300, p, 96, 4096, p, 4096, p, need, 0) == B.ERR_SHAPE

@@ -1,0 +1,58 @@
+"""iq4xs_linear (quantize + matmul through a caller workspace) on the GPU:
+same result as the two separate calls, within 1e-5 per row of the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from _gates import gate_parity, gate_written
+from _gpu import dev, matmul_gpu, oracle_matmul, oracle_q8, quantize_gpu, sample_rows
+from iq4_xs_quantized_gb300 import binding as B
+from iq4_xs_quantized_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from iq4_xs_quantized_gb300 import build
+    build.build()
+    B.load()
+    yield
+    assert B.iq4xs_last_device_error() == 0
+
+
+@pytest.mark.parametrize("M", (1, 3, 8, 33, 96, 200))
+def test_linear_matches_two_calls_and_oracle(M):
+    B.iq4xs_set_crossover(4)
+    W = synth.SQUARE
+    N, K = W.shapes[0]
+    w, x = W.inputs(0, M=M)
+    wd, xd = dev(w), dev(x)
+    ws = torch.full((B.iq4xs_linear_workspace_bytes(M, N, K),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    y = torch.full((M, N), float("nan"), device="cuda")
+    B.iq4xs_linear(wd, N, K, xd, y, ws)
+    torch.cuda.synchronize()
+    yl = y.cpu().numpy()
+    assert gate_written(yl) is None
+    path = "dp4a" if B.iq4xs_select_path(M, N, K) == B.PATH_DP4A else "tc"
+    qs, ds, op = quantize_gpu(x, tc=(path == "tc"))
+    y2 = matmul_gpu(wd, N, K, qs, ds, op, M, path)
+    assert np.array_equal(yl, y2)
+    qs_o, d_o, _ = oracle_q8(x)
+    rows = sample_rows(N, 40, seed=M)
+    r = gate_parity(yl[:, rows], oracle_matmul(w, N, K, qs_o, d_o, rows))
+    assert r is None, r
+
+
+def test_linear_rejects_small_workspace():
+    N, K, M = 256, 1024, 4
+    w, x = synth.TINY.inputs(0, M=M)
+    need = B.iq4xs_linear_workspace_bytes(M, N, K)
+    ws = torch.empty((need - 16,), dtype=torch.uint8, device="cuda")
+    y = torch.empty((M, N), device="cuda")
+    with pytest.raises(B.IQ4XSError) as e:
+        B.iq4xs_linear(dev(w), N, K, dev(x), y, ws)
+    assert e.value.status == B.ERR_ARG
