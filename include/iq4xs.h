@@ -142,6 +142,35 @@ int iq4xs_linear(const void* w, int64_t N, int64_t K, const float* x, int64_t M,
 int64_t iq4xs_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
+ * iq4xs_linear without a caller workspace: the same projection, with its
+ * scratch held in a fixed 8 MiB device array inside this library.  (The
+ * source pages have no counterpart; this entry point serves callers that
+ * cannot allocate device memory themselves -- a plugin inside a framework
+ * that owns every device allocation, or a serving loop that must not
+ * allocate once running, since cudaMalloc can synchronize the device, fail
+ * under memory pressure, and is not allowed during stream capture.)
+ *   - Allocates nothing and calls no allocating routine.  The array is
+ *     created when the library is loaded and every GPU that loads it holds
+ *     it until the process exits.
+ *   - Size limit: iq4xs_linear_workspace_bytes(M, N, K) must not exceed
+ *     iq4xs_linear_static_max_bytes() (8 MiB: e.g. M <= 128 at K = 17408);
+ *     larger requests return IQ4XS_ERR_SHAPE and launch nothing.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - Every call shares the one array and leaves its contents behind; calls
+ *     that can overlap on the GPU (different streams, or different host
+ *     threads without ordering) race on it.  Serialize them, e.g. on one
+ *     stream.
+ * Arguments and errors otherwise as for iq4xs_linear.
+ */
+int iq4xs_linear_static(const void* w, int64_t N, int64_t K, const float* x, int64_t M,
+                        int64_t ldx, float* y, int64_t ldy, int64_t stream);
+
+/* Bytes of the fixed scratch behind iq4xs_linear_static. */
+int64_t iq4xs_linear_static_max_bytes(void);
+
+/*
  * Dequantize W to a dense [N][K] matrix (engine page, kernel table at M=64:
  * dequantize_block_iq4_xs feeding a dense GEMM -- the baseline the batched
  * kernel replaces).  out_dtype 0 = fp32 (exact), 1 = bfloat16 (RNE of the

@@ -58,6 +58,10 @@ def load(path: str | None = None):
         lib.iq4xs_linear.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, i64]
         lib.iq4xs_linear_workspace_bytes.argtypes = [i64, i64, i64]
         lib.iq4xs_linear_workspace_bytes.restype = i64
+        lib.iq4xs_linear_static.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, i64]
+        lib.iq4xs_linear_static.restype = ci
+        lib.iq4xs_linear_static_max_bytes.argtypes = []
+        lib.iq4xs_linear_static_max_bytes.restype = i64
         lib.iq4xs_select_path.argtypes = [i64, i64, i64, ctypes.POINTER(ci)]
         lib.iq4xs_set_crossover.argtypes = [i64]
         lib.iq4xs_set_pdl.argtypes = [ci]
@@ -138,6 +142,19 @@ def iq4xs_linear(w, N: int, K: int, x, y, workspace, stream=None) -> None:
                              _ptr(workspace), workspace.numel() * workspace.element_size(),
                              _stream(stream))
     _check("iq4xs_linear", rc)
+
+
+def iq4xs_linear_static(w, N: int, K: int, x, y, stream=None) -> None:
+    """iq4xs_linear with the library's fixed device scratch: nothing is
+    allocated (for callers that cannot allocate device memory)."""
+    M = x.shape[0]
+    rc = load().iq4xs_linear_static(_ptr(w), N, K, _ptr(x), M, x.stride(0), _ptr(y), y.stride(0),
+                                    _stream(stream))
+    _check("iq4xs_linear_static", rc)
+
+
+def iq4xs_linear_static_max_bytes() -> int:
+    return int(load().iq4xs_linear_static_max_bytes())
 
 
 def iq4xs_dequantize(w, N: int, K: int, out, stream=None) -> None:
