@@ -15,14 +15,19 @@
 // mbarrier rings so that no round trip sits on the critical path:
 //   warpgroups 0, 1 (decoders)  sub-blocks of parity g: thread t decodes row
 //                               t's sub-block from the staged W bytes to exact
-//                               fp16 in the canonical K-major layout (A ring)
+//                               fp16 in the canonical K-major layout (A ring);
+//                               after a barrier over the warpgroup, its first
+//                               thread issues two tcgen05.mma 128 x MT x 16 for
+//                               that sub-block into a fresh TMEM accumulator
+//                               (kND slots).  Issuing from the decoders keeps
+//                               the MMA issue off a separate warp whose
+//                               integer work would queue behind the decoders'
+//                               on the shared ALU pipes.
 //   warp 12 (producer)          TMA: W stages of 2 super-blocks (128 x 272 B,
 //                               2D tensor map); activation stages of 4
 //                               sub-blocks (bulk copies of the pre-tiled fp16
 //                               codes and their fp32 block scales)
-//   warp 13 (issuer)            allocates TMEM; one thread issues two
-//                               tcgen05.mma 128 x MT x 16 per sub-block into a
-//                               fresh TMEM accumulator (kND slots)
+//   warp 13                     allocates and frees TMEM
 //   warpgroup 2 (epilogue)      thread t loads row t's int-valued fp32 results
 //                               (all columns, then one wait) and scales them by
 //                               d_w*(ls-32)*d_x into fp32 register accumulators
@@ -40,17 +45,19 @@ constexpr int kTcThreads = 32 * 16;   // 4 warpgroups
 constexpr int kDecGroups = 2;         // decoder warpgroups 0, 1 (sub-block parity)
 constexpr int kEpiWarp0 = 8;          // epilogue: warps 8-11
 constexpr int kProducerWarp = 12;
-constexpr int kIssuerWarp = 13;       // warps 14, 15 idle
+constexpr int kTmemWarp = 13;         // TMEM owner; warps 14, 15 idle
 constexpr int kTmemCols = 512;        // whole TMEM; one CTA per SM (see kMinSmem)
 constexpr int kMaxCluster = 8;
 constexpr int kMinSmem = 120 * 1024;  // > half of the SM's shared memory: one CTA per SM
-constexpr int kNA = 4;                // A (decoded fp16) slots; decoder g uses slots of parity g
+constexpr int kNA = 4;                // A (decoded fp16) slots = TMEM accumulators
+constexpr int kDecUnit = 2;           // sub-blocks a decoder warpgroup takes per step
+static_assert(kNA == kDecGroups * kDecUnit, "decoder g owns slots kDecUnit*g ..");
 constexpr int kALbo = kTileN * 16;    // A: byte distance between K-adjacent core matrices
 constexpr int kCoreSbo = 128;         // 8 rows x 16 B core matrices, contiguous along M/N
 // Per-warpgroup register budgets (setmaxnreg).  The block launches with
 // 65536 / 512 = 128 registers per thread; the budgets sum to
-// 128 * (2 * 80 + 248 + 56) = 59392, within the 65536 it holds.
-constexpr int kRegsDecode = 80;
+// 128 * (2 * 96 + 248 + 56) = 63488, within the 65536 it holds.
+constexpr int kRegsDecode = 96;
 constexpr int kRegsEpilogue = 248;
 constexpr int kRegsControl = 56;
 static_assert(128 * (kDecGroups * kRegsDecode + kRegsEpilogue + kRegsControl) <= kTcThreads * 128,
@@ -68,8 +75,8 @@ __device__ __forceinline__ void reg_dealloc() {
 template <int MT>
 struct TcCfg {
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= kMaxMTile, "UMMA N for M=128");
-    static constexpr int kND = (kTmemCols / MT) < 8 ? (kTmemCols / MT) : 8;  // TMEM accumulators
-    static_assert(kND >= 4, "at least four accumulators in flight");
+    static constexpr int kND = kNA;  // TMEM accumulators, one per A slot
+    static_assert(kND * MT <= kTmemCols, "accumulators fit TMEM");
     static constexpr int kNW = (MT <= 64) ? 3 : 2;             // W stages
     static constexpr int kNB = (MT <= 96) ? 4 : 3;             // activation stages
     static constexpr int kBQhBytes = kBStageChunks * MT * 16;  // fp16 codes of 4 sub-blocks
@@ -81,8 +88,8 @@ struct TcCfg {
     static constexpr int kOffB = kOffW + kNW * kWStageBytes;
     static constexpr int kOffA = kOffB + kNB * kBStageBytes;
     static constexpr int kOffBar = kOffA + kNA * kASubBytes;
-    // W full/empty, B full/empty, A full/free, D full/free, drain
-    static constexpr int kNumBars = 2 * kNW + 2 * kNB + 2 * kNA + 2 * kND + 1;
+    // W full/empty, B full/empty, MMA done / accumulator free per slot, drain
+    static constexpr int kNumBars = 2 * kNW + 2 * kNB + 2 * kND + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;   // tmem base, abort flag
     static constexpr int kUsed = kOffMisc + 16;
     static constexpr int kSmem = (kUsed + 1024 > kMinSmem) ? kUsed + 1024 : kMinSmem;
@@ -94,6 +101,7 @@ struct TcCfg {
 };
 
 constexpr int kEpilogueBarrier = 1;  // named barrier id for the 4 epilogue warps
+constexpr int kDecodeBarrier0 = 2;   // named barrier ids 2, 3: decoder warpgroups 0, 1
 
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -129,10 +137,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* w_empty = w_full + C::kNW;
     uint64_t* b_full = w_empty + C::kNW;
     uint64_t* b_empty = b_full + C::kNB;
-    uint64_t* a_full = b_empty + C::kNB;
-    uint64_t* a_free = a_full + kNA;
-    uint64_t* d_full = a_free + kNA;
-    uint64_t* d_free = d_full + C::kND;
+    // mma_done[s]: the MMAs of the sub-block in slot s are complete (its A
+    // slot may be rewritten, its accumulator read); d_free[s]: the epilogue
+    // has read accumulator s.  Since an MMA into slot s waits for d_free[s],
+    // mma_done[s] never runs two phases ahead of either waiter.
+    uint64_t* mma_done = b_empty + C::kNB;
+    uint64_t* d_free = mma_done + C::kND;
     uint64_t* drain = d_free + C::kND;
     uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -159,17 +169,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int i = 0; i < C::kNB; ++i) {
             mbar_init(&b_full[i], 1);
-            mbar_init(&b_empty[i], 1 + kTileN);  // MMA commit + epilogue (block scales)
+            // one MMA commit per decoder warpgroup + the epilogue (block scales)
+            mbar_init(&b_empty[i], kDecGroups + kTileN);
         }
-        for (int i = 0; i < kNA; ++i) { mbar_init(&a_full[i], kTileN); mbar_init(&a_free[i], 1); }
-        for (int i = 0; i < C::kND; ++i) { mbar_init(&d_full[i], 1); mbar_init(&d_free[i], kTileN); }
-        mbar_init(drain, 1);
+        for (int i = 0; i < C::kND; ++i) { mbar_init(&mma_done[i], 1); mbar_init(&d_free[i], kTileN); }
+        mbar_init(drain, kDecGroups);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
     }
     if (warp == kProducerWarp && lane == 0) prefetch_tmap(&tmap_w);
-    if (warp == kIssuerWarp) tmem_alloc(tmem_base_ptr, kTmemCols);
+    if (warp == kTmemWarp) tmem_alloc(tmem_base_ptr, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -225,39 +235,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_wait(&w_full[ps % C::kNW], (ps / C::kNW) & 1, abort_flag, err, kDevErrTimeoutDrain);
             for (int bs = (issued_b > C::kNB ? issued_b - C::kNB : 0); bs < issued_b; ++bs)
                 mbar_wait(&b_full[bs % C::kNB], (bs / C::kNB) & 1, abort_flag, err, kDevErrTimeoutDrain);
-        } else if (warp == kIssuerWarp && lane == 0) {
-            // ----------------------------------------------------- MMA issuer
-            constexpr uint32_t idesc = idesc_f16_m128(MT);
-            const uint32_t a_base = smem_u32(smem + C::kOffA);
-            const uint32_t b_base = smem_u32(smem + C::kOffB);
-            bool ok = true;
-            for (int li = 0; li < nsub && ok; ++li) {
-                const int sa = li % kNA, sd = li % C::kND;
-                ok = mbar_wait(&a_full[sa], (li / kNA) & 1, abort_flag, err, kDevErrTimeoutA);
-                if (ok && li >= C::kND)
-                    ok = mbar_wait(&d_free[sd], ((li / C::kND) - 1) & 1, abort_flag, err,
-                                   kDevErrTimeoutFree);
-                const int bs = li / kBStageSubs, bslot = bs % C::kNB;
-                if (ok && li % kBStageSubs == 0)
-                    ok = mbar_wait(&b_full[bslot], (bs / C::kNB) & 1, abort_flag, err, kDevErrTimeoutB);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + (uint32_t)(sd * MT);
-                const uint32_t a_addr = a_base + sa * kASubBytes;
-                const uint32_t b_addr =
-                    b_base + bslot * C::kBStageBytes + (li % kBStageSubs) * kChunksPerSub * MT * 16;
-#pragma unroll
-                for (int i = 0; i < kMmaPerSub; ++i) {
-                    const uint64_t adesc = smem_desc(a_addr + i * 2 * kALbo, kALbo, kCoreSbo);
-                    const uint64_t bdesc = smem_desc(b_addr + i * 2 * MT * 16, MT * 16, kCoreSbo);
-                    tc_mma_f16(d_tmem, adesc, bdesc, idesc, i);
-                }
-                tc_commit(&a_free[sa]);
-                tc_commit(&d_full[sd]);
-                if (li % kBStageSubs == kBStageSubs - 1) tc_commit(&b_empty[bslot]);
-            }
-            // Every MMA issued so far has completed before TMEM is released.
-            tc_commit(drain);
+        } else if (warp == kTmemWarp) {
+            // Every MMA issued by both decoder warpgroups has completed before
+            // TMEM is released (one commit from each).
             mbar_wait(drain, 0, abort_flag, err, kDevErrTimeoutDrain);
         }
     } else if (warp < kEpiWarp0) {
@@ -266,33 +246,88 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int g = warp >> 2;                   // sub-block parity of this warpgroup
         const int t = threadIdx.x & (kTileN - 1);  // row within the tile
         uint8_t* a_row = smem + C::kOffA + t * 16;
+        constexpr uint32_t idesc = idesc_f16_m128(MT);
+        const uint32_t a_base = smem_u32(smem + C::kOffA);
+        const uint32_t b_base = smem_u32(smem + C::kOffB);
         bool ok = true;
-        for (int li = g; li < nsub; li += kDecGroups) {
-            const int ps = li / kSubPerPair, jj = li % kSubPerPair, wslot = ps % C::kNW;
-            if (ok && jj < kDecGroups)
+        // Step: sub-blocks l0, l0+1 (l0 = 4k + 2g), always in slots 2g, 2g+1,
+        // always in one super-block and one activation stage.
+        for (int l0 = kDecUnit * g; l0 < nsub; l0 += kDecUnit * kDecGroups) {
+            const int ps = l0 / kSubPerPair, jj = l0 % kSubPerPair, wslot = ps % C::kNW;
+            if (ok && jj < kDecUnit * kDecGroups)
                 ok = mbar_wait(&w_full[wslot], (ps / C::kNW) & 1, abort_flag, err, kDevErrTimeoutW);
             const uint8_t* rowp = smem + C::kOffW + wslot * kWStageBytes + t * kPairBytes +
                                   (jj / kSubPerBlock) * kBlockBytes;
             const int j = jj % kSubPerBlock;
-            const uint2 q01 = *reinterpret_cast<const uint2*>(rowp + 8 + 16 * j);
-            const uint2 q23 = *reinterpret_cast<const uint2*>(rowp + 16 + 16 * j);
-            if (jj >= kSubPerPair - kDecGroups) mbar_arrive(&w_empty[wslot]);
-            uint32_t h[16];
-            decode_f16x2(q01.x, h + 0);
-            decode_f16x2(q01.y, h + 4);
-            decode_f16x2(q23.x, h + 8);
-            decode_f16x2(q23.y, h + 12);
-            const int sa = li % kNA;
-            if (ok && li >= kNA)
-                ok = mbar_wait(&a_free[sa], ((li / kNA) - 1) & 1, abort_flag, err, kDevErrTimeoutA);
-            uint8_t* ap = a_row + sa * kASubBytes;
+            uint2 q[2 * kDecUnit];
 #pragma unroll
-            for (int c = 0; c < kChunksPerSub; ++c)
-                *reinterpret_cast<uint4*>(ap + c * kALbo) =
-                    make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+            for (int u = 0; u < kDecUnit; ++u) {
+                q[2 * u] = *reinterpret_cast<const uint2*>(rowp + 8 + 16 * (j + u));
+                q[2 * u + 1] = *reinterpret_cast<const uint2*>(rowp + 16 + 16 * (j + u));
+            }
+            if (jj >= kSubPerPair - kDecUnit * kDecGroups) mbar_arrive(&w_empty[wslot]);
+            uint32_t h[16 * kDecUnit];
+#pragma unroll
+            for (int u = 0; u < 2 * kDecUnit; ++u) {
+                decode_f16x2(q[u].x, h + 8 * u);
+                decode_f16x2(q[u].y, h + 8 * u + 4);
+            }
+            const int s0 = l0 % kNA;  // == kDecUnit * g
+            if (ok && l0 >= kNA) {
+#pragma unroll
+                for (int u = 0; u < kDecUnit; ++u)
+                    if (ok) ok = mbar_wait(&mma_done[s0 + u], ((l0 / kNA) - 1) & 1, abort_flag, err,
+                                           kDevErrTimeoutA);
+            }
+#pragma unroll
+            for (int u = 0; u < kDecUnit; ++u) {
+                uint8_t* ap = a_row + (s0 + u) * kASubBytes;
+#pragma unroll
+                for (int c = 0; c < kChunksPerSub; ++c)
+                    *reinterpret_cast<uint4*>(ap + c * kALbo) =
+                        make_uint4(h[16 * u + 4 * c], h[16 * u + 4 * c + 1], h[16 * u + 4 * c + 2],
+                                   h[16 * u + 4 * c + 3]);
+            }
             fence_proxy_async_smem();
-            mbar_arrive(&a_full[sa]);
+            // All 128 rows of both slots are written (and fenced for the async
+            // proxy); the warpgroup's first thread issues their MMAs.
+            named_barrier_sync(kDecodeBarrier0 + g, kTileN);
+            if (t == 0) {
+                const int bs = l0 / kBStageSubs, bslot = bs % C::kNB;
+                if (ok && l0 >= kNA) {
+#pragma unroll
+                    for (int u = 0; u < kDecUnit; ++u)
+                        if (ok) ok = mbar_wait(&d_free[s0 + u], ((l0 / kNA) - 1) & 1, abort_flag, err,
+                                               kDevErrTimeoutFree);
+                }
+                if (ok)
+                    ok = mbar_wait(&b_full[bslot], (bs / C::kNB) & 1, abort_flag, err, kDevErrTimeoutB);
+                tc_fence_after();
+#pragma unroll
+                for (int u = 0; u < kDecUnit; ++u) {
+                    const int li = l0 + u, sa = s0 + u;
+                    if (ok) {
+                        const uint32_t d_tmem = tmem + (uint32_t)(sa * MT);
+                        const uint32_t a_addr = a_base + sa * kASubBytes;
+                        const uint32_t b_addr = b_base + bslot * C::kBStageBytes +
+                                                (li % kBStageSubs) * kChunksPerSub * MT * 16;
+#pragma unroll
+                        for (int i = 0; i < kMmaPerSub; ++i) {
+                            const uint64_t adesc = smem_desc(a_addr + i * 2 * kALbo, kALbo, kCoreSbo);
+                            const uint64_t bdesc =
+                                smem_desc(b_addr + i * 2 * MT * 16, MT * 16, kCoreSbo);
+                            tc_mma_f16(d_tmem, adesc, bdesc, idesc, i);
+                        }
+                    }
+                    // Commits are made even after an abort so that every
+                    // waiter's barrier still completes.
+                    tc_commit(&mma_done[sa]);
+                }
+                // this warpgroup's sub-blocks of the activation stage are issued
+                tc_commit(&b_empty[bslot]);
+            }
         }
+        if (t == 0) tc_commit(drain);
     } else {
         // ------------------------------------------------------------ epilogue
         reg_alloc<kRegsEpilogue>();
@@ -318,7 +353,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float4* dx4 = reinterpret_cast<const float4*>(
                 smem + C::kOffB + bslot * C::kBStageBytes + C::kBQhBytes + (li % kBStageSubs) * MT * 4);
             const int sd = li % C::kND;
-            if (ok) ok = mbar_wait(&d_full[sd], (li / C::kND) & 1, abort_flag, err, kDevErrTimeoutMma);
+            if (ok) ok = mbar_wait(&mma_done[sd], (li / C::kND) & 1, abort_flag, err, kDevErrTimeoutMma);
             tc_fence_after();
 #pragma unroll
             for (int part = 0; part < MT; part += C::kPartCols) {
@@ -401,7 +436,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kIssuerWarp) {
+    if (warp == kTmemWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
