@@ -287,15 +287,11 @@ def run_ours(args, world, rank, local):
     variants = N_COPIES // len(ms)
     stream = torch.cuda.Stream(device=dev)
 
-    def launch_step(v, events=None):
+    def launch_step(v):
         for i, M in enumerate(ms):
             qs, ds, op = acts[M]
             B.iq4xs_quantize_q8_1(xs[M], qs, ds, op, stream)
-            if events is not None:
-                events[i][0].record(stream)
             B.iq4xs_matmul(wcopies[v * len(ms) + i], N, K, qs, ds, op, M, ys[M], paths[M], stream)
-            if events is not None:
-                events[i][1].record(stream)
 
     # Eager warm-up (also performs the library's one-time device set-up).
     with torch.cuda.stream(stream):
@@ -303,15 +299,15 @@ def run_ours(args, world, rank, local):
             launch_step(v)
     torch.cuda.synchronize(dev)
 
-    # One graph per weight-copy variant, with timing events around every matmul.
-    graphs, evs = [], []
+    # One graph per weight-copy variant.  No event nodes inside the graphs:
+    # an event-record node between two kernels costs microseconds and breaks
+    # programmatic dependent launch.
+    graphs = []
     for v in range(variants):
-        e = [(timing_event(torch), timing_event(torch)) for _ in ms]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            launch_step(v, e)
+            launch_step(v)
         graphs.append(g)
-        evs.append(e)
     torch.cuda.synchronize(dev)
 
     with torch.cuda.stream(stream):
@@ -336,16 +332,12 @@ def run_ours(args, world, rank, local):
     ms_local = start.elapsed_time(stop)
     ms_total = max_over_ranks(ms_local, world)
 
-    # Per-matmul device time from the events recorded inside the step graphs
-    # (last replay of each variant); a matmul-only graph pass if unavailable.
+    # Per-matmul device time: graphs of back-to-back matmul launches over the
+    # rotating weight copies, CUDA events on the launching stream.
     per_m = []
-    try:
-        mm_us = {M: statistics.mean(evs[v][i][0].elapsed_time(evs[v][i][1]) * 1e3
-                                    for v in range(variants)) for i, M in enumerate(ms)}
-        mm_timing = "events around each matmul inside the timed step graphs"
-    except Exception:
-        mm_us = matmul_only_times(torch, B, stream, ms, N, K, wcopies, acts, ys, paths)
-        mm_timing = "matmul-only graph replays over the rotating weight copies"
+    mm_us = matmul_only_times(torch, B, stream, ms, N, K, wcopies, acts, ys, paths)
+    mm_timing = ("CUDA events around graph replays of 45 back-to-back matmul launches "
+                 "(rotating weight copies) on the launching stream, per M")
     peak, peak_kind = hbm_peak_gbs()
     for M in ms:
         us = mm_us[M]
@@ -408,15 +400,6 @@ def run_ours(args, world, rank, local):
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
-
-
-def timing_event(torch):
-    """A timing event that becomes a real event-record node when captured in
-    a CUDA graph (torch >= 2.7); a plain timing event otherwise."""
-    try:
-        return torch.cuda.Event(enable_timing=True, external=True)
-    except TypeError:
-        return torch.cuda.Event(enable_timing=True)
 
 
 def matmul_only_times(torch, B, stream, ms, N, K, wcopies, acts, ys, paths, reps=20):

@@ -49,9 +49,7 @@ constexpr int kTmemWarp = 13;         // TMEM owner; warps 14, 15 idle
 constexpr int kTmemCols = 512;        // whole TMEM; one CTA per SM (see kMinSmem)
 constexpr int kMaxCluster = 8;
 constexpr int kMinSmem = 120 * 1024;  // > half of the SM's shared memory: one CTA per SM
-constexpr int kNA = 4;                // A (decoded fp16) slots = TMEM accumulators
 constexpr int kDecUnit = 2;           // sub-blocks a decoder warpgroup takes per step
-static_assert(kNA == kDecGroups * kDecUnit, "decoder g owns slots kDecUnit*g ..");
 constexpr int kALbo = kTileN * 16;    // A: byte distance between K-adjacent core matrices
 constexpr int kCoreSbo = 128;         // 8 rows x 16 B core matrices, contiguous along M/N
 // Per-warpgroup register budgets (setmaxnreg).  The block launches with
@@ -75,9 +73,16 @@ __device__ __forceinline__ void reg_dealloc() {
 template <int MT>
 struct TcCfg {
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= kMaxMTile, "UMMA N for M=128");
-    static constexpr int kND = kNA;  // TMEM accumulators, one per A slot
+    // A (decoded fp16) slots = TMEM accumulators.  The slots in flight set
+    // the throughput of the decode -> MMA -> epilogue ring (each slot's round
+    // trip is a few thousand cycles), so use as many as TMEM and shared
+    // memory allow.  Decoder g's steps use slots whose index / kDecUnit has
+    // parity g.
+    static constexpr int kNA = (MT <= 64) ? 8 : 4;
+    static constexpr int kND = kNA;
+    static_assert(kNA % (kDecGroups * kDecUnit) == 0, "slots split evenly between decoders");
     static_assert(kND * MT <= kTmemCols, "accumulators fit TMEM");
-    static constexpr int kNW = (MT <= 64) ? 3 : 2;             // W stages
+    static constexpr int kNW = (MT <= 48) ? 3 : 2;             // W stages
     static constexpr int kNB = (MT <= 96) ? 4 : 3;             // activation stages
     static constexpr int kBQhBytes = kBStageChunks * MT * 16;  // fp16 codes of 4 sub-blocks
     static constexpr int kBDxBytes = kBStageSubs * MT * 4;     // their fp32 block scales
@@ -88,6 +93,7 @@ struct TcCfg {
     static constexpr int kOffB = kOffW + kNW * kWStageBytes;
     static constexpr int kOffA = kOffB + kNB * kBStageBytes;
     static constexpr int kOffBar = kOffA + kNA * kASubBytes;
+    static_assert(kOffBar <= 226 * 1024, "stages and slots fit shared memory");
     // W full/empty, B full/empty, MMA done / accumulator free per slot, drain
     static constexpr int kNumBars = 2 * kNW + 2 * kNB + 2 * kND + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;   // tmem base, abort flag
@@ -272,11 +278,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 decode_f16x2(q[u].x, h + 8 * u);
                 decode_f16x2(q[u].y, h + 8 * u + 4);
             }
-            const int s0 = l0 % kNA;  // == kDecUnit * g
-            if (ok && l0 >= kNA) {
+            const int s0 = l0 % C::kNA;
+            if (ok && l0 >= C::kNA) {
 #pragma unroll
                 for (int u = 0; u < kDecUnit; ++u)
-                    if (ok) ok = mbar_wait(&mma_done[s0 + u], ((l0 / kNA) - 1) & 1, abort_flag, err,
+                    if (ok) ok = mbar_wait(&mma_done[s0 + u], ((l0 / C::kNA) - 1) & 1, abort_flag, err,
                                            kDevErrTimeoutA);
             }
 #pragma unroll
@@ -294,10 +300,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             named_barrier_sync(kDecodeBarrier0 + g, kTileN);
             if (t == 0) {
                 const int bs = l0 / kBStageSubs, bslot = bs % C::kNB;
-                if (ok && l0 >= kNA) {
+                if (ok && l0 >= C::kNA) {
 #pragma unroll
                     for (int u = 0; u < kDecUnit; ++u)
-                        if (ok) ok = mbar_wait(&d_free[s0 + u], ((l0 / kNA) - 1) & 1, abort_flag, err,
+                        if (ok) ok = mbar_wait(&d_free[s0 + u], ((l0 / C::kNA) - 1) & 1, abort_flag, err,
                                                kDevErrTimeoutFree);
                 }
                 if (ok)
