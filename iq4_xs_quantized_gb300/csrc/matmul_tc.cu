@@ -12,28 +12,29 @@
 // whose CTAs reduce their partial tiles through distributed shared memory.
 //
 // Warp-specialized roles, each a loop over the CTA's sub-blocks, decoupled by
-// mbarrier rings so that no round trip sits on the critical path:
-//   warpgroups 0, 1 (decoders)  sub-blocks of parity g: thread t decodes row
-//                               t's sub-block from the staged W bytes to exact
-//                               fp16 in the canonical K-major layout (A ring);
-//                               after a barrier over the warpgroup, its first
-//                               thread issues two tcgen05.mma 128 x MT x 16 for
-//                               that sub-block into a fresh TMEM accumulator
-//                               (kND slots).  Issuing from the decoders keeps
-//                               the MMA issue off a separate warp whose
-//                               integer work would queue behind the decoders'
-//                               on the shared ALU pipes.
-//   warp 12 (producer)          TMA: W stages of 2 super-blocks (128 x 272 B,
-//                               2D tensor map); activation stages of 4
-//                               sub-blocks (bulk copies of the pre-tiled fp16
-//                               codes and their fp32 block scales)
-//   warp 13                     allocates and frees TMEM
-//   warpgroup 2 (epilogue)      thread t loads row t's int-valued fp32 results
-//                               (all columns, then one wait) and scales them by
-//                               d_w*(ls-32)*d_x into fp32 register accumulators
+// mbarrier rings (kNS slots of tensor memory per ring position: the decoded
+// A operand, 16 columns; the integer accumulator, MT columns; the row scale,
+// one column):
+//   warps 0-7 (decoders)   two groups of four; group g takes sub-blocks
+//                          4k+2g and 4k+2g+1.  Warp w decodes rows 32(w%4)..+31 from
+//                          the staged W bytes to exact fp16 and stores them
+//                          with tcgen05.st straight into the A slot (row i in
+//                          TMEM lane i), plus d_w*(ls-32) into the scale
+//                          column, then arrives on the slot's a_full.
+//   warp 8 (MMA)           warp-uniform loop; one elected lane issues two
+//                          tcgen05.mma 128 x MT x 16 (A from tensor memory, B
+//                          from shared memory) per sub-block and commits.
+//   warp 9 (producer)      TMA: W stages of 2 super-blocks (128 x 272 B, 2D
+//                          tensor map); activation stages of 4 sub-blocks
+//                          (bulk copies of the pre-tiled fp16 codes and their
+//                          fp32 block scales).
+//   warp 10                allocates and frees tensor memory.
+//   warps 12-15 (epilogue) thread t reads row t's integer results and scale,
+//                          releases the slot, and accumulates
+//                          d_w*(ls-32)*d_x*dot in fp32 registers.
 // Every mbarrier wait is bounded (2 s); a timeout sets the device error word
 // and an abort flag that releases every other wait, the CTA drains its copies
-// and frees its TMEM, and the call's output is undefined.
+// and frees its tensor memory, and the call's output is undefined.
 #include <cuda.h>
 
 #include "internal.cuh"
@@ -42,23 +43,25 @@ namespace iq4xs {
 namespace {
 
 constexpr int kTcThreads = 32 * 16;   // 4 warpgroups
-constexpr int kDecGroups = 2;         // decoder warpgroups 0, 1 (sub-block parity)
-constexpr int kEpiWarp0 = 8;          // epilogue: warps 8-11
-constexpr int kProducerWarp = 12;
-constexpr int kTmemWarp = 13;         // TMEM owner; warps 14, 15 idle
+constexpr int kDecWarps = 8;          // warps 0-7
+constexpr int kDecGroups = 2;         // groups of 4 warps, alternating sub-block pairs
+constexpr int kDecUnit = 2;           // consecutive sub-blocks a group decodes per iteration
+constexpr int kMmaWarp = 8;
+constexpr int kProducerWarp = 9;
+constexpr int kTmemWarp = 10;         // warp 11 idle
+constexpr int kEpiWarp0 = 12;         // epilogue: warps 12-15
 constexpr int kTmemCols = 512;        // whole TMEM; one CTA per SM (see kMinSmem)
 constexpr int kMaxCluster = 8;
 constexpr int kMinSmem = 120 * 1024;  // > half of the SM's shared memory: one CTA per SM
-constexpr int kDecUnit = 2;           // sub-blocks a decoder warpgroup takes per step
-constexpr int kALbo = kTileN * 16;    // A: byte distance between K-adjacent core matrices
-constexpr int kCoreSbo = 128;         // 8 rows x 16 B core matrices, contiguous along M/N
+constexpr int kACols = kSub / 2;      // 16 TMEM columns of fp16 pairs per sub-block
+constexpr int kCoreSbo = 128;         // 8 rows x 16 B core matrices, contiguous along N
 // Per-warpgroup register budgets (setmaxnreg).  The block launches with
 // 65536 / 512 = 128 registers per thread; the budgets sum to
-// 128 * (2 * 96 + 248 + 56) = 63488, within the 65536 it holds.
+// 128 * (2 * 96 + 56 + 248) = 63488, within the 65536 it holds.
 constexpr int kRegsDecode = 96;
-constexpr int kRegsEpilogue = 248;
 constexpr int kRegsControl = 56;
-static_assert(128 * (kDecGroups * kRegsDecode + kRegsEpilogue + kRegsControl) <= kTcThreads * 128,
+constexpr int kRegsEpilogue = 248;
+static_assert(128 * (kDecGroups * kRegsDecode + kRegsControl + kRegsEpilogue) <= kTcThreads * 128,
               "register split fits the launch allocation");
 
 template <int R>
@@ -73,45 +76,40 @@ __device__ __forceinline__ void reg_dealloc() {
 template <int MT>
 struct TcCfg {
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= kMaxMTile, "UMMA N for M=128");
-    // A (decoded fp16) slots = TMEM accumulators.  The slots in flight set
-    // the throughput of the decode -> MMA -> epilogue ring (each slot's round
-    // trip is a few thousand cycles), so use as many as TMEM and shared
-    // memory allow.  Decoder g's steps use slots whose index / kDecUnit has
-    // parity g.
-    static constexpr int kNA = (MT <= 64) ? 8 : 4;
-    static constexpr int kND = kNA;
-    static_assert(kNA % (kDecGroups * kDecUnit) == 0, "slots split evenly between decoders");
-    static_assert(kND * MT <= kTmemCols, "accumulators fit TMEM");
-    static constexpr int kNW = (MT <= 48) ? 3 : 2;             // W stages
-    static constexpr int kNB = (MT <= 96) ? 4 : 3;             // activation stages
+    // Work unit: kU consecutive sub-blocks, decoded, multiplied and scaled
+    // together (one barrier handshake per unit between the roles).
+    static constexpr int kU = (MT <= 96) ? 2 : 1;
+    // Tensor-memory slots per unit: accumulators (kU*MT columns), A (kU*16),
+    // scales (kU).  kNP units are in flight.
+    static constexpr int kUnitCols = kU * (MT + kACols + 1);
+    static constexpr int kNP = (kTmemCols / kUnitCols < 8) ? kTmemCols / kUnitCols : 8;
+    static constexpr int kColD = 0;
+    static constexpr int kColA = kNP * kU * MT;
+    static constexpr int kColS = kColA + kNP * kU * kACols;
+    static_assert(kColS + kNP * kU <= kTmemCols, "slots fit tensor memory");
+    static_assert(kNP >= 2, "at least two units in flight");
+    static_assert(kBStageSubs % kU == 0 && kSubPerBlock % kU == 0, "units tile stages and super-blocks");
+    static constexpr int kNW = (MT <= 32) ? 5 : (MT <= 64) ? 4 : 3;  // W stages
+    static constexpr int kNB = (MT <= 96) ? 4 : 3;                    // activation stages
     static constexpr int kBQhBytes = kBStageChunks * MT * 16;  // fp16 codes of 4 sub-blocks
     static constexpr int kBDxBytes = kBStageSubs * MT * 4;     // their fp32 block scales
     // slot stride, padded to 1 KB; the copies into a slot fill kBQhBytes + kBDxBytes
     static constexpr int kBStageBytes = (kBQhBytes + kBDxBytes + 1023) / 1024 * 1024;
-    static constexpr int kPartCols = (MT > 64) ? 64 : MT;      // TMEM columns read per wait
     static constexpr int kOffW = 0;
     static constexpr int kOffB = kOffW + kNW * kWStageBytes;
-    static constexpr int kOffA = kOffB + kNB * kBStageBytes;
-    static constexpr int kOffBar = kOffA + kNA * kASubBytes;
-    static_assert(kOffBar <= 226 * 1024, "stages and slots fit shared memory");
-    // W full/empty, B full/empty, MMA done / accumulator free per slot, drain
-    static constexpr int kNumBars = 2 * kNW + 2 * kNB + 2 * kND + 1;
+    static constexpr int kOffBar = kOffB + kNB * kBStageBytes;
+    // W full/empty, B full/empty, A full / MMA done / accumulator free per unit slot, drain
+    static constexpr int kNumBars = 2 * kNW + 2 * kNB + 3 * kNP + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;   // tmem base, abort flag
     static constexpr int kUsed = kOffMisc + 16;
+    static_assert(kUsed <= 226 * 1024, "stages fit shared memory");
     static constexpr int kSmem = (kUsed + 1024 > kMinSmem) ? kUsed + 1024 : kMinSmem;
-    static constexpr int kRedStride = MT + 1;                  // fp32 words per row
+    static constexpr int kRedStride = MT + 4;                  // fp32 words per row (16-byte rows)
     static_assert(kTileN * kRedStride * 4 <= kNW * kWStageBytes, "reduction tile fits the W ring");
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-    static_assert(kOffB % 1024 == 0 && kOffA % 1024 == 0 && kBStageBytes % 16 == 0, "alignment");
-    static_assert(kPartCols % 16 == 0, "TMEM read granularity");
+    static_assert(kOffB % 1024 == 0 && kBStageBytes % 16 == 0, "alignment");
 };
 
-constexpr int kEpilogueBarrier = 1;  // named barrier id for the 4 epilogue warps
-constexpr int kDecodeBarrier0 = 2;   // named barrier ids 2, 3: decoder warpgroups 0, 1
-
-__device__ __forceinline__ void named_barrier_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
@@ -121,11 +119,16 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
 }
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t local_saddr, uint32_t rank) {
+// 16 bytes of CTA `rank`'s shared memory at this CTA's offset `local_saddr`.
+// No memory clobber: the loads of all ranks issue back to back (they stay
+// between the two cluster barriers, which are volatile with a clobber).
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_saddr, uint32_t rank) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_saddr), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(remote));
     return v;
 }
 
@@ -143,13 +146,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* w_empty = w_full + C::kNW;
     uint64_t* b_full = w_empty + C::kNW;
     uint64_t* b_empty = b_full + C::kNB;
-    // mma_done[s]: the MMAs of the sub-block in slot s are complete (its A
-    // slot may be rewritten, its accumulator read); d_free[s]: the epilogue
-    // has read accumulator s.  Since an MMA into slot s waits for d_free[s],
-    // mma_done[s] never runs two phases ahead of either waiter.
-    uint64_t* mma_done = b_empty + C::kNB;
-    uint64_t* d_free = mma_done + C::kND;
-    uint64_t* drain = d_free + C::kND;
+    // a_full[p]: unit slot p holds a decoded unit (A and scale columns);
+    // mma_done[p]: its MMAs are complete (accumulators readable);
+    // d_free[p]: the epilogue has read the accumulators and scales, so the
+    // whole slot may be reused.  Every use of slot p waits, directly or
+    // through this chain, for the previous use's d_free, so none of the
+    // three barriers ever runs two phases ahead of a waiter.
+    uint64_t* a_full = b_empty + C::kNB;
+    uint64_t* mma_done = a_full + C::kNP;
+    uint64_t* d_free = mma_done + C::kNP;
+    uint64_t* drain = d_free + C::kNP;
     uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -163,6 +169,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int p0 = (int)((int64_t)pairs * rank / S);
     const int p1 = (int)((int64_t)pairs * (rank + 1) / S);
     const int nsub = (p1 - p0) * kSubPerPair;
+    const int nunits = nsub / C::kU;
     const int nbst = nsub / kBStageSubs;
     const int64_t K8 = K / kChunkElems, K32 = K / kSub;
     const uint8_t* qh_tile = tc_op + (int64_t)z * K8 * MT * 16;
@@ -171,15 +178,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNW; ++i) {
             mbar_init(&w_full[i], 1);
-            mbar_init(&w_empty[i], (kDecGroups + 1) * kTileN);  // both decoders + epilogue
+            mbar_init(&w_empty[i], kDecWarps);  // one arrive per decoder warp
         }
         for (int i = 0; i < C::kNB; ++i) {
             mbar_init(&b_full[i], 1);
-            // one MMA commit per decoder warpgroup + the epilogue (block scales)
-            mbar_init(&b_empty[i], kDecGroups + kTileN);
+            mbar_init(&b_empty[i], 1 + 4);  // MMA commit + the 4 epilogue warps (block scales)
         }
-        for (int i = 0; i < C::kND; ++i) { mbar_init(&mma_done[i], 1); mbar_init(&d_free[i], kTileN); }
-        mbar_init(drain, kDecGroups);
+        for (int i = 0; i < C::kNP; ++i) {
+            mbar_init(&a_full[i], 4);  // the 4 warps of the unit's decoder group
+            mbar_init(&mma_done[i], 1);
+            mbar_init(&d_free[i], 4);  // the 4 epilogue warps
+        }
+        mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -194,10 +204,103 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // grid's completion before touching anything this grid reads or writes.
     griddep_launch_dependents();
 
-    if (warp >= kProducerWarp) {
+    if (warp < kDecWarps) {
+        // ------------------------------------------------------------ decoders
+        reg_dealloc<kRegsDecode>();
+        const int g = warp >> 2;                // decoder group: units g, g+2, ...
+        const int t = (warp & 3) * 32 + lane;   // row within the tile == TMEM lane
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        bool ok = true;
+        // A unit is kU consecutive sub-blocks of one super-block of one W stage.
+        for (int v = g; v < nunits; v += kDecGroups) {
+            const int l0 = v * C::kU;
+            const int ps = l0 / kSubPerPair, jj = l0 % kSubPerPair, wslot = ps % C::kNW;
+            if (ok && jj < C::kU * kDecGroups)
+                ok = mbar_wait(&w_full[wslot], (ps / C::kNW) & 1, abort_flag, err, kDevErrTimeoutW);
+            const uint8_t* blk = smem + C::kOffW + wslot * kWStageBytes + t * kPairBytes +
+                                 (jj / kSubPerBlock) * kBlockBytes;
+            const int j = jj % kSubPerBlock;
+            const uint2 hdr = *reinterpret_cast<const uint2*>(blk);
+            uint2 q[2 * C::kU];
+#pragma unroll
+            for (int u = 0; u < C::kU; ++u) {
+                q[2 * u] = *reinterpret_cast<const uint2*>(blk + 8 + 16 * (j + u));
+                q[2 * u + 1] = *reinterpret_cast<const uint2*>(blk + 16 + 16 * (j + u));
+            }
+            uint32_t h[C::kU][kACols];
+#pragma unroll
+            for (int u = 0; u < C::kU; ++u) {
+                decode_f16x2(q[2 * u].x, h[u]);
+                decode_f16x2(q[2 * u].y, h[u] + 4);
+                decode_f16x2(q[2 * u + 1].x, h[u] + 8);
+                decode_f16x2(q[2 * u + 1].y, h[u] + 12);
+            }
+            float Sw[C::kU];
+#pragma unroll
+            for (int u = 0; u < C::kU; ++u) Sw[u] = iq4xs_scale(hdr.x, hdr.y, j + u);
+            // The stage's bytes are consumed (in registers) once this warp's
+            // last unit of it is decoded.
+            if (jj >= kSubPerPair - C::kU * kDecGroups) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&w_empty[wslot]);
+            }
+            const int sp = v % C::kNP;
+            if (ok && v >= C::kNP)
+                ok = mbar_wait(&d_free[sp], ((v / C::kNP) - 1) & 1, abort_flag, err, kDevErrTimeoutFree);
+            tc_fence_after();
+#pragma unroll
+            for (int u = 0; u < C::kU; ++u) {
+                tmem_st16(tmem + lane_off + (uint32_t)(C::kColA + (sp * C::kU + u) * kACols), h[u]);
+                tmem_st1(tmem + lane_off + (uint32_t)(C::kColS + sp * C::kU + u), __float_as_uint(Sw[u]));
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[sp]);
+        }
+    } else if (warp < kEpiWarp0) {
         reg_dealloc<kRegsControl>();
-        if (warp == kProducerWarp && lane == 0) {
-            // ------------------------------------------------------- producer
+        if (warp == kMmaWarp) {
+            // ---------------------------------------------------------- MMA
+            // Warp-uniform loop with incremental indices (the warp shares its
+            // SM sub-partition's integer pipe with decoders); one elected
+            // lane issues.
+            constexpr uint32_t idesc = idesc_f16_m128(MT);
+            const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffB), MT * 16, kCoreSbo);
+            bool ok = true;
+            int sp = 0, sphase = 0, bslot = 0, bphase = 0;
+            for (int v = 0, l0 = 0; v < nunits; ++v, l0 += C::kU) {
+                const int lb = l0 % kBStageSubs;  // first sub-block's position in its B stage
+                if (ok && lb == 0)
+                    ok = mbar_wait(&b_full[bslot], bphase, abort_flag, err, kDevErrTimeoutB);
+                if (ok) ok = mbar_wait(&a_full[sp], sphase, abort_flag, err, kDevErrTimeoutA);
+                ok = __all_sync(0xffffffffu, ok);
+                tc_fence_after();
+                if (elect_one()) {
+                    if (ok) {
+                        const uint32_t boff = (uint32_t)(bslot * C::kBStageBytes + lb * kChunksPerSub * MT * 16);
+#pragma unroll
+                        for (int u = 0; u < C::kU; ++u)
+#pragma unroll
+                            for (int i = 0; i < kMmaPerSub; ++i)
+                                tc_mma_f16_ta(
+                                    tmem + (uint32_t)(C::kColD + (sp * C::kU + u) * MT),
+                                    tmem + (uint32_t)(C::kColA + (sp * C::kU + u) * kACols + i * (kUmmaK / 2)),
+                                    bdesc0 + ((boff + (u * kChunksPerSub + 2 * i) * MT * 16) >> 4), idesc, i);
+                    }
+                    // Commits are made even after an abort so that every
+                    // waiter's barrier still completes.
+                    tc_commit(&mma_done[sp]);
+                    if (lb + C::kU == kBStageSubs) tc_commit(&b_empty[bslot]);
+                }
+                __syncwarp();
+                if (++sp == C::kNP) { sp = 0; sphase ^= 1; }
+                if (lb + C::kU == kBStageSubs && ++bslot == C::kNB) { bslot = 0; bphase ^= 1; }
+            }
+            if (elect_one()) tc_commit(drain);
+            __syncwarp();
+        } else if (warp == kProducerWarp && lane == 0) {
+            // ----------------------------------------------------- producer
             int issued_w = 0, issued_b = 0;
             bool ok = true;
             // W is read-only model state: its first stages stream before the
@@ -242,166 +345,89 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int bs = (issued_b > C::kNB ? issued_b - C::kNB : 0); bs < issued_b; ++bs)
                 mbar_wait(&b_full[bs % C::kNB], (bs / C::kNB) & 1, abort_flag, err, kDevErrTimeoutDrain);
         } else if (warp == kTmemWarp) {
-            // Every MMA issued by both decoder warpgroups has completed before
-            // TMEM is released (one commit from each).
+            // Every MMA issued has completed before tensor memory is freed.
             mbar_wait(drain, 0, abort_flag, err, kDevErrTimeoutDrain);
         }
-    } else if (warp < kEpiWarp0) {
-        // ------------------------------------------------------------ decoders
-        reg_dealloc<kRegsDecode>();
-        const int g = warp >> 2;                   // sub-block parity of this warpgroup
-        const int t = threadIdx.x & (kTileN - 1);  // row within the tile
-        uint8_t* a_row = smem + C::kOffA + t * 16;
-        constexpr uint32_t idesc = idesc_f16_m128(MT);
-        const uint32_t a_base = smem_u32(smem + C::kOffA);
-        const uint32_t b_base = smem_u32(smem + C::kOffB);
-        bool ok = true;
-        // Step: sub-blocks l0, l0+1 (l0 = 4k + 2g), always in slots 2g, 2g+1,
-        // always in one super-block and one activation stage.
-        for (int l0 = kDecUnit * g; l0 < nsub; l0 += kDecUnit * kDecGroups) {
-            const int ps = l0 / kSubPerPair, jj = l0 % kSubPerPair, wslot = ps % C::kNW;
-            if (ok && jj < kDecUnit * kDecGroups)
-                ok = mbar_wait(&w_full[wslot], (ps / C::kNW) & 1, abort_flag, err, kDevErrTimeoutW);
-            const uint8_t* rowp = smem + C::kOffW + wslot * kWStageBytes + t * kPairBytes +
-                                  (jj / kSubPerBlock) * kBlockBytes;
-            const int j = jj % kSubPerBlock;
-            uint2 q[2 * kDecUnit];
-#pragma unroll
-            for (int u = 0; u < kDecUnit; ++u) {
-                q[2 * u] = *reinterpret_cast<const uint2*>(rowp + 8 + 16 * (j + u));
-                q[2 * u + 1] = *reinterpret_cast<const uint2*>(rowp + 16 + 16 * (j + u));
-            }
-            if (jj >= kSubPerPair - kDecUnit * kDecGroups) mbar_arrive(&w_empty[wslot]);
-            uint32_t h[16 * kDecUnit];
-#pragma unroll
-            for (int u = 0; u < 2 * kDecUnit; ++u) {
-                decode_f16x2(q[u].x, h + 8 * u);
-                decode_f16x2(q[u].y, h + 8 * u + 4);
-            }
-            const int s0 = l0 % C::kNA;
-            if (ok && l0 >= C::kNA) {
-#pragma unroll
-                for (int u = 0; u < kDecUnit; ++u)
-                    if (ok) ok = mbar_wait(&mma_done[s0 + u], ((l0 / C::kNA) - 1) & 1, abort_flag, err,
-                                           kDevErrTimeoutA);
-            }
-#pragma unroll
-            for (int u = 0; u < kDecUnit; ++u) {
-                uint8_t* ap = a_row + (s0 + u) * kASubBytes;
-#pragma unroll
-                for (int c = 0; c < kChunksPerSub; ++c)
-                    *reinterpret_cast<uint4*>(ap + c * kALbo) =
-                        make_uint4(h[16 * u + 4 * c], h[16 * u + 4 * c + 1], h[16 * u + 4 * c + 2],
-                                   h[16 * u + 4 * c + 3]);
-            }
-            fence_proxy_async_smem();
-            // All 128 rows of both slots are written (and fenced for the async
-            // proxy); the warpgroup's first thread issues their MMAs.
-            named_barrier_sync(kDecodeBarrier0 + g, kTileN);
-            if (t == 0) {
-                const int bs = l0 / kBStageSubs, bslot = bs % C::kNB;
-                if (ok && l0 >= C::kNA) {
-#pragma unroll
-                    for (int u = 0; u < kDecUnit; ++u)
-                        if (ok) ok = mbar_wait(&d_free[s0 + u], ((l0 / C::kNA) - 1) & 1, abort_flag, err,
-                                               kDevErrTimeoutFree);
-                }
-                if (ok)
-                    ok = mbar_wait(&b_full[bslot], (bs / C::kNB) & 1, abort_flag, err, kDevErrTimeoutB);
-                tc_fence_after();
-#pragma unroll
-                for (int u = 0; u < kDecUnit; ++u) {
-                    const int li = l0 + u, sa = s0 + u;
-                    if (ok) {
-                        const uint32_t d_tmem = tmem + (uint32_t)(sa * MT);
-                        const uint32_t a_addr = a_base + sa * kASubBytes;
-                        const uint32_t b_addr = b_base + bslot * C::kBStageBytes +
-                                                (li % kBStageSubs) * kChunksPerSub * MT * 16;
-#pragma unroll
-                        for (int i = 0; i < kMmaPerSub; ++i) {
-                            const uint64_t adesc = smem_desc(a_addr + i * 2 * kALbo, kALbo, kCoreSbo);
-                            const uint64_t bdesc =
-                                smem_desc(b_addr + i * 2 * MT * 16, MT * 16, kCoreSbo);
-                            tc_mma_f16(d_tmem, adesc, bdesc, idesc, i);
-                        }
-                    }
-                    // Commits are made even after an abort so that every
-                    // waiter's barrier still completes.
-                    tc_commit(&mma_done[sa]);
-                }
-                // this warpgroup's sub-blocks of the activation stage are issued
-                tc_commit(&b_empty[bslot]);
-            }
-        }
-        if (t == 0) tc_commit(drain);
     } else {
         // ------------------------------------------------------------ epilogue
         reg_alloc<kRegsEpilogue>();
-        const int t = threadIdx.x - kEpiWarp0 * 32;  // row within the tile == TMEM lane
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int t = (warp & 3) * 32 + lane;  // row within the tile == TMEM lane
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        constexpr int kCols = C::kU * MT;      // accumulator columns of a unit
         float acc[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[m] = 0.f;
         bool ok = true;
-        for (int li = 0; li < nsub; ++li) {
-            const int ps = li / kSubPerPair, jj = li % kSubPerPair, wslot = ps % C::kNW;
-            const int bs = li / kBStageSubs, bslot = bs % C::kNB;
-            if (ok && jj == 0)
-                ok = mbar_wait(&w_full[wslot], (ps / C::kNW) & 1, abort_flag, err, kDevErrTimeoutW);
-            const uint8_t* rowp = smem + C::kOffW + wslot * kWStageBytes + t * kPairBytes +
-                                  (jj / kSubPerBlock) * kBlockBytes;
-            const uint2 hdr = *reinterpret_cast<const uint2*>(rowp);
-            if (jj == kSubPerPair - 1) mbar_arrive(&w_empty[wslot]);
-            const float Sw = iq4xs_scale(hdr.x, hdr.y, jj % kSubPerBlock);
-            const float2 Sw2 = make_float2(Sw, Sw);
-            if (ok && li % kBStageSubs == 0)
-                ok = mbar_wait(&b_full[bslot], (bs / C::kNB) & 1, abort_flag, err, kDevErrTimeoutB);
-            const float4* dx4 = reinterpret_cast<const float4*>(
-                smem + C::kOffB + bslot * C::kBStageBytes + C::kBQhBytes + (li % kBStageSubs) * MT * 4);
-            const int sd = li % C::kND;
-            if (ok) ok = mbar_wait(&mma_done[sd], (li / C::kND) & 1, abort_flag, err, kDevErrTimeoutMma);
+        int sp = 0, sphase = 0, bslot = 0, bphase = 0;
+        for (int v = 0, l0 = 0; v < nunits; ++v, l0 += C::kU) {
+            const int lb = l0 % kBStageSubs;
+            if (ok && lb == 0) ok = mbar_wait(&b_full[bslot], bphase, abort_flag, err, kDevErrTimeoutB);
+            const float* dxs = reinterpret_cast<const float*>(smem + C::kOffB + bslot * C::kBStageBytes +
+                                                              C::kBQhBytes + lb * MT * 4);
+            if (ok) ok = mbar_wait(&mma_done[sp], sphase, abort_flag, err, kDevErrTimeoutMma);
             tc_fence_after();
+            const uint32_t dcol = tmem + lane_off + (uint32_t)(C::kColD + sp * kCols);
+            const uint32_t scol = tmem + lane_off + (uint32_t)(C::kColS + sp * C::kU);
+            uint32_t swb[C::kU];
 #pragma unroll
-            for (int part = 0; part < MT; part += C::kPartCols) {
-                constexpr int kW = C::kPartCols;  // columns of this part (the last may be narrower)
-                const int cols = (MT - part < kW) ? MT - part : kW;
-                uint32_t r[kW];
-                const uint32_t taddr = tmem + lane_base + (uint32_t)(sd * MT + part);
-                if (cols == 64) tmem_ld64_wait(taddr, r);
-                else if (cols == 48) tmem_ld48_wait(taddr, r);
-                else if (cols == 32) tmem_ld32_wait(taddr, r);
-                else tmem_ld16_wait(taddr, r);
-                if (part + C::kPartCols >= MT) {
-                    tc_fence_before();
-                    mbar_arrive(&d_free[sd]);
+            for (int part = 0; part < kCols; part += 64) {
+                const int w = (kCols - part < 64) ? kCols - part : 64;
+                uint32_t r[64];
+                if (part == 0) {
+                    if (C::kU == 2) {
+                        if (w == 64) tmem_ld64_s2_wait(dcol, scol, r, swb);
+                        else if (w == 48) tmem_ld48_s2_wait(dcol, scol, r, swb);
+                        else if (w == 32) tmem_ld32_s2_wait(dcol, scol, r, swb);
+                        else tmem_ld16_s2_wait(dcol, scol, r, swb);
+                    } else {
+                        if (w == 64) tmem_ld64_s1_wait(dcol, scol, r, swb);
+                        else if (w == 48) tmem_ld48_s1_wait(dcol, scol, r, swb);
+                        else if (w == 32) tmem_ld32_s1_wait(dcol, scol, r, swb);
+                        else tmem_ld16_s1_wait(dcol, scol, r, swb);
+                    }
+                } else {
+                    if (w == 64) tmem_ld64_wait(dcol + part, r);
+                    else if (w == 48) tmem_ld48_wait(dcol + part, r);
+                    else if (w == 32) tmem_ld32_wait(dcol + part, r);
+                    else tmem_ld16_wait(dcol + part, r);
                 }
+                if (part + 64 >= kCols) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&d_free[sp]);
+                }
+                // acc[m] += P * (Sw * dx), two columns per instruction; a
+                // group of four columns never straddles two sub-blocks.
 #pragma unroll
-                for (int k = 0; k < kW; k += 4) {
-                    if (k >= cols) break;
-                    const int m = part + k;
-                    const float4 d = dx4[m / 4];
+                for (int k = 0; k < 64; k += 4) {
+                    if (k >= w) break;
+                    const int c = part + k, u = c / MT, m = c % MT;
+                    const float sw = __uint_as_float(swb[u]);
+                    const float2 Sw2 = make_float2(sw, sw);
+                    const float4 d = *reinterpret_cast<const float4*>(dxs + u * MT + m);
                     const float2 s01 = __fmul2_rn(Sw2, make_float2(d.x, d.y));
                     const float2 s23 = __fmul2_rn(Sw2, make_float2(d.z, d.w));
-                    const float2 a01 =
-                        __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), s01,
-                                   make_float2(acc[m], acc[m + 1]));
-                    const float2 a23 =
-                        __ffma2_rn(make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
-                                   s23, make_float2(acc[m + 2], acc[m + 3]));
+                    const float2 a01 = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
+                                                  s01, make_float2(acc[m], acc[m + 1]));
+                    const float2 a23 = __ffma2_rn(make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
+                                                  s23, make_float2(acc[m + 2], acc[m + 3]));
                     acc[m] = a01.x;
                     acc[m + 1] = a01.y;
                     acc[m + 2] = a23.x;
                     acc[m + 3] = a23.y;
                 }
             }
-            if (li % kBStageSubs == kBStageSubs - 1) mbar_arrive(&b_empty[bslot]);
+            if (lb + C::kU == kBStageSubs) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&b_empty[bslot]);
+                if (++bslot == C::kNB) { bslot = 0; bphase ^= 1; }
+            }
+            if (++sp == C::kNP) { sp = 0; sphase ^= 1; }
         }
         // Partial tile -> y (one CTA) or -> shared memory for the cluster
-        // reduction, which reuses the W ring.  Before any epilogue thread
-        // writes there, all four epilogue warps must have read their last
-        // block headers from it (named barrier); the decoders' last reads of
-        // it preceded the last accumulator these threads waited for, and
-        // every W copy issued has been consumed.
+        // reduction, which reuses the W ring: every decoder read of it
+        // preceded an accumulator these threads have consumed, and every W
+        // copy issued has been consumed.
         const int64_t mrows = M - (int64_t)z * MT;
         if (S == 1) {
             griddep_wait();
@@ -409,31 +435,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int m = 0; m < MT; ++m)
                 if (m < mrows && n0 + t < N) y[((int64_t)z * MT + m) * ldy + n0 + t] = acc[m];
         } else {
-            named_barrier_sync(kEpilogueBarrier, kTileN);
-            float* red = reinterpret_cast<float*>(smem + C::kOffW);
+            float4* red = reinterpret_cast<float4*>(smem + C::kOffW + t * C::kRedStride * 4);
 #pragma unroll
-            for (int m = 0; m < MT; ++m) red[t * C::kRedStride + m] = acc[m];
+            for (int m = 0; m < MT; m += 4) red[m / 4] = make_float4(acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
         }
     }
 
     if (S > 1) {
         // Split-K reduction over the cluster through distributed shared memory:
         // CTA `rank` sums rows [rank*128/S, (rank+1)*128/S) over all CTAs in
-        // rank order (deterministic) and writes them.
+        // rank order (deterministic) and writes them.  Decoder and epilogue
+        // warps (384 threads) share the work.
         __syncwarp();
         cluster_sync_all();
-        if (warp < kProducerWarp) {
+        if (warp < kDecWarps || warp >= kEpiWarp0) {
             griddep_wait();
+            const int idx = (warp < kDecWarps) ? threadIdx.x : threadIdx.x - 4 * 32 * 1;
             const int64_t mrows = M - (int64_t)z * MT;
             const uint32_t red_s = smem_u32(smem + C::kOffW);
+            static_assert(C::kOffW % 16 == 0 && C::kRedStride % 4 == 0, "16-byte reduction rows");
             const int r0 = (int)(kTileN * rank / S), r1 = (int)(kTileN * (rank + 1) / S);
             const int rows = r1 - r0;
-            for (int e = threadIdx.x; e < rows * MT; e += kProducerWarp * 32) {
-                const int row = r0 + e % rows, m = e / rows;
-                float v = 0.f;
-                for (int q = 0; q < S; ++q)
-                    v += ld_dsmem_f32(red_s + (uint32_t)((row * C::kRedStride + m) * 4), (uint32_t)q);
-                if (m < mrows && n0 + row < N) y[((int64_t)z * MT + m) * ldy + n0 + row] = v;
+            // element e = (row, 4 columns); consecutive threads take
+            // consecutive rows, so the stores to y coalesce
+            for (int e = idx; e < rows * (MT / 4); e += 12 * 32) {
+                const int row = r0 + e % rows, m = 4 * (e / rows);
+                const uint32_t a = red_s + (uint32_t)((row * C::kRedStride + m) * 4);
+                float4 v[kMaxCluster];
+#pragma unroll
+                for (int q = 0; q < kMaxCluster; ++q)
+                    if (q < S) v[q] = ld_dsmem_v4(a, (uint32_t)q);
+                float4 sum = v[0];
+#pragma unroll
+                for (int q = 1; q < kMaxCluster; ++q)
+                    if (q < S) {
+                        sum.x += v[q].x;
+                        sum.y += v[q].y;
+                        sum.z += v[q].z;
+                        sum.w += v[q].w;
+                    }
+                if (n0 + row < N) {
+                    float* yp = y + ((int64_t)z * MT + m) * ldy + n0 + row;
+                    if (m < mrows) yp[0] = sum.x;
+                    if (m + 1 < mrows) yp[ldy] = sum.y;
+                    if (m + 2 < mrows) yp[2 * ldy] = sum.z;
+                    if (m + 3 < mrows) yp[3 * ldy] = sum.w;
+                }
             }
         }
         __syncwarp();
