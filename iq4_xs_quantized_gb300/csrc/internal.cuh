@@ -203,23 +203,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// try_wait that may suspend the thread (up to `ns` nanoseconds) until the
+// phase completes, instead of returning at once: a waiting warp then takes
+// no issue slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (without waiting further) once the CTA's abort flag is set, or after
 // kWaitLimitNs, in which case it sets the abort flag and the device error word.
+// The first probe returns at once; later ones suspend for up to 0.1 ms.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* err, int code) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const unsigned long long t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(a, parity)) return true;
-        if ((it & 63) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
-                *abort_flag = 1;
-                atomicExch(err, code);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_sleep(a, parity, 100000u)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicExch(err, code);
+            return false;
         }
     }
 }

@@ -17,15 +17,19 @@ namespace {
 
 constexpr int kDp4aThreads = 256;
 constexpr int kRows = 2;   // weight rows per warp
-constexpr int kIters = 4;  // sub-block steps whose loads are in flight together
 constexpr int kWarpsPerCta = kDp4aThreads / 32;
+// Sub-block steps whose loads are in flight together: as many as fit in the
+// 128 registers that keep two CTAs (16 warps) resident per SM, so that a
+// 4096-row matrix runs in one wave.
+template <int MC>
+constexpr int iters_for() { return MC == 1 ? 4 : (MC <= 4 ? 2 : 1); }
 
 __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
     return __dp4a((int)a, (int)b, c);
 }
 
 template <int MC>  // activation rows per pass
-__global__ void __launch_bounds__(kDp4aThreads)
+__global__ void __launch_bounds__(kDp4aThreads, 2)
     matmul_dp4a_kernel(const uint8_t* __restrict__ w, int64_t N, int64_t K,
                        const int8_t* __restrict__ qs, const __half2* __restrict__ ds, int64_t M,
                        float* __restrict__ y, int64_t ldy) {
@@ -36,6 +40,7 @@ __global__ void __launch_bounds__(kDp4aThreads)
     if (n0 >= N) return;  // whole warp
     const int64_t nsub = K / kSub;
     const int64_t row_bytes = (K / kQK) * kBlockBytes;
+    constexpr int kIters = iters_for<MC>();
     bool waited = false;
 
     for (int64_t m0 = 0; m0 < M; m0 += MC) {

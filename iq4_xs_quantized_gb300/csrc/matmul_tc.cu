@@ -21,9 +21,11 @@
 //                          with tcgen05.st straight into the A slot (row i in
 //                          TMEM lane i), plus d_w*(ls-32) into the scale
 //                          column, then arrives on the slot's a_full.
-//   warp 8 (MMA)           warp-uniform loop; one elected lane issues two
-//                          tcgen05.mma 128 x MT x 16 (A from tensor memory, B
-//                          from shared memory) per sub-block and commits.
+//   warps 8, 11 (MMA)      warp-uniform loops over even / odd units; one
+//                          elected lane issues two tcgen05.mma 128 x MT x 16
+//                          (A from tensor memory, B from shared memory) per
+//                          sub-block and commits.  Two issuers keep the
+//                          tensor pipe fed between their own handshakes.
 //   warp 9 (producer)      TMA: W stages of 2 super-blocks (128 x 272 B, 2D
 //                          tensor map); activation stages of 4 sub-blocks
 //                          (bulk copies of the pre-tiled fp16 codes and their
@@ -45,10 +47,10 @@ namespace {
 constexpr int kTcThreads = 32 * 16;   // 4 warpgroups
 constexpr int kDecWarps = 8;          // warps 0-7
 constexpr int kDecGroups = 2;         // groups of 4 warps, alternating sub-block pairs
-constexpr int kDecUnit = 2;           // consecutive sub-blocks a group decodes per iteration
-constexpr int kMmaWarp = 8;
+constexpr int kMmaWarp0 = 8;          // MMA issuers: warps 8 and 11 (even / odd units)
+constexpr int kMmaWarp1 = 11;
 constexpr int kProducerWarp = 9;
-constexpr int kTmemWarp = 10;         // warp 11 idle
+constexpr int kTmemWarp = 10;
 constexpr int kEpiWarp0 = 12;         // epilogue: warps 12-15
 constexpr int kTmemCols = 512;        // whole TMEM; one CTA per SM (see kMinSmem)
 constexpr int kMaxCluster = 8;
@@ -175,26 +177,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint8_t* qh_tile = tc_op + (int64_t)z * K8 * MT * 16;
     const uint8_t* dx_tile = tc_op + tc_qh_bytes(M, K) + (int64_t)z * K32 * MT * 4;
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kNW; ++i) {
-            mbar_init(&w_full[i], 1);
-            mbar_init(&w_empty[i], kDecWarps);  // one arrive per decoder warp
+    static_assert(C::kNumBars <= 64, "barriers initialised two per producer lane");
+    if (warp == kProducerWarp) {
+        // Lane i initialises barriers i and i + 32; lane 0 then starts the
+        // first W copy at once (W is read-only model state).
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = lane + 32 * h;
+            uint32_t count = 0;
+            if (i < C::kNW) count = 1;                                           // w_full
+            else if (i < 2 * C::kNW) count = kDecWarps;                          // w_empty
+            else if (i < 2 * C::kNW + C::kNB) count = 1;                         // b_full
+            else if (i < 2 * C::kNW + 2 * C::kNB) count = 2 + 4;                 // b_empty: MMA warps + epilogue warps
+            else if (i < 2 * C::kNW + 2 * C::kNB + C::kNP) count = 4;            // a_full: a decoder group
+            else if (i < 2 * C::kNW + 2 * C::kNB + 2 * C::kNP) count = 1;        // mma_done
+            else if (i < 2 * C::kNW + 2 * C::kNB + 3 * C::kNP) count = 4;        // d_free: epilogue warps
+            else if (i < C::kNumBars) count = 2;                                 // drain: MMA warps
+            if (count) mbar_init(&bars[i], count);
         }
-        for (int i = 0; i < C::kNB; ++i) {
-            mbar_init(&b_full[i], 1);
-            mbar_init(&b_empty[i], 1 + 4);  // MMA commit + the 4 epilogue warps (block scales)
-        }
-        for (int i = 0; i < C::kNP; ++i) {
-            mbar_init(&a_full[i], 4);  // the 4 warps of the unit's decoder group
-            mbar_init(&mma_done[i], 1);
-            mbar_init(&d_free[i], 4);  // the 4 epilogue warps
-        }
-        mbar_init(drain, 1);
-        *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            *abort_flag = 0;
+            prefetch_tmap(&tmap_w);
+            mbar_arrive_expect_tx(&w_full[0], kWStageBytes);
+            tma_load_2d(smem + C::kOffW, &tmap_w, p0 * (kPairBytes / 4), n0, &w_full[0]);
+        }
     }
-    if (warp == kProducerWarp && lane == 0) prefetch_tmap(&tmap_w);
     if (warp == kTmemWarp) tmem_alloc(tmem_base_ptr, kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -211,12 +221,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int t = (warp & 3) * 32 + lane;   // row within the tile == TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         bool ok = true;
-        // A unit is kU consecutive sub-blocks of one super-block of one W stage.
+        // A unit is kU consecutive sub-blocks of one super-block of one W
+        // stage.  Software pipeline: unit v's tensor-memory stores are
+        // issued, and completed and signalled only after unit v+2 has been
+        // decoded, so their latency hides behind that decode.
+        int jj = C::kU * g, wslot = 0, wphase = 0;  // position in the W ring
+        int sp = g, sphase = 0;                     // unit slot of v (v % kNP, v / kNP)
+        int pend_sp = -1;                           // slot stored but not yet signalled
         for (int v = g; v < nunits; v += kDecGroups) {
-            const int l0 = v * C::kU;
-            const int ps = l0 / kSubPerPair, jj = l0 % kSubPerPair, wslot = ps % C::kNW;
             if (ok && jj < C::kU * kDecGroups)
-                ok = mbar_wait(&w_full[wslot], (ps / C::kNW) & 1, abort_flag, err, kDevErrTimeoutW);
+                ok = mbar_wait(&w_full[wslot], wphase, abort_flag, err, kDevErrTimeoutW);
             const uint8_t* blk = smem + C::kOffW + wslot * kWStageBytes + t * kPairBytes +
                                  (jj / kSubPerBlock) * kBlockBytes;
             const int j = jj % kSubPerBlock;
@@ -240,38 +254,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int u = 0; u < C::kU; ++u) Sw[u] = iq4xs_scale(hdr.x, hdr.y, j + u);
             // The stage's bytes are consumed (in registers) once this warp's
             // last unit of it is decoded.
-            if (jj >= kSubPerPair - C::kU * kDecGroups) {
+            jj += C::kU * kDecGroups;
+            if (jj >= kSubPerPair) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&w_empty[wslot]);
+                jj -= kSubPerPair;
+                if (++wslot == C::kNW) { wslot = 0; wphase ^= 1; }
             }
-            const int sp = v % C::kNP;
+            // Signal the previous unit (its stores have had a decode to land).
+            if (pend_sp >= 0) {
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[pend_sp]);
+            }
             if (ok && v >= C::kNP)
-                ok = mbar_wait(&d_free[sp], ((v / C::kNP) - 1) & 1, abort_flag, err, kDevErrTimeoutFree);
+                ok = mbar_wait(&d_free[sp], sphase ^ 1, abort_flag, err, kDevErrTimeoutFree);
             tc_fence_after();
 #pragma unroll
             for (int u = 0; u < C::kU; ++u) {
                 tmem_st16(tmem + lane_off + (uint32_t)(C::kColA + (sp * C::kU + u) * kACols), h[u]);
                 tmem_st1(tmem + lane_off + (uint32_t)(C::kColS + sp * C::kU + u), __float_as_uint(Sw[u]));
             }
+            pend_sp = sp;
+            sp += kDecGroups;
+            if (sp >= C::kNP) { sp -= C::kNP; sphase ^= 1; }
+        }
+        if (pend_sp >= 0) {
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&a_full[sp]);
+            if (lane == 0) mbar_arrive(&a_full[pend_sp]);
         }
     } else if (warp < kEpiWarp0) {
         reg_dealloc<kRegsControl>();
-        if (warp == kMmaWarp) {
+        if (warp == kMmaWarp0 || warp == kMmaWarp1) {
             // ---------------------------------------------------------- MMA
             // Warp-uniform loop with incremental indices (the warp shares its
             // SM sub-partition's integer pipe with decoders); one elected
-            // lane issues.
+            // lane issues.  Warp k takes units k, k+2, ... (those of decoder
+            // group k).
             constexpr uint32_t idesc = idesc_f16_m128(MT);
             const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffB), MT * 16, kCoreSbo);
+            const int k = (warp == kMmaWarp0) ? 0 : 1;
             bool ok = true;
-            int sp = 0, sphase = 0, bslot = 0, bphase = 0;
-            for (int v = 0, l0 = 0; v < nunits; ++v, l0 += C::kU) {
+            int sp = k, sphase = 0;
+            for (int v = k, l0 = k * C::kU; v < nunits; v += 2, l0 += 2 * C::kU) {
                 const int lb = l0 % kBStageSubs;  // first sub-block's position in its B stage
-                if (ok && lb == 0)
+                const int bs = l0 / kBStageSubs, bslot = bs % C::kNB, bphase = (bs / C::kNB) & 1;
+                if (ok && lb < 2 * C::kU)  // this warp's first unit of the B stage
                     ok = mbar_wait(&b_full[bslot], bphase, abort_flag, err, kDevErrTimeoutB);
                 if (ok) ok = mbar_wait(&a_full[sp], sphase, abort_flag, err, kDevErrTimeoutA);
                 ok = __all_sync(0xffffffffu, ok);
@@ -291,29 +322,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // Commits are made even after an abort so that every
                     // waiter's barrier still completes.
                     tc_commit(&mma_done[sp]);
-                    if (lb + C::kU == kBStageSubs) tc_commit(&b_empty[bslot]);
+                    // this warp's last unit of the B stage
+                    if (lb + 2 * C::kU >= kBStageSubs) tc_commit(&b_empty[bslot]);
                 }
                 __syncwarp();
-                if (++sp == C::kNP) { sp = 0; sphase ^= 1; }
-                if (lb + C::kU == kBStageSubs && ++bslot == C::kNB) { bslot = 0; bphase ^= 1; }
+                sp += 2;
+                if (sp >= C::kNP) { sp -= C::kNP; sphase ^= 1; }
             }
             if (elect_one()) tc_commit(drain);
             __syncwarp();
         } else if (warp == kProducerWarp && lane == 0) {
             // ----------------------------------------------------- producer
-            int issued_w = 0, issued_b = 0;
-            bool ok = true;
-            // W is read-only model state: its first stages stream before the
+            // The first W stage was started during set-up, before the
             // preceding kernel (which produces the activations) has finished.
+            // The other stages follow once it has landed, so that at launch,
+            // when every CTA requests at once, first stages are served first.
+            int issued_w = 1, issued_b = 0;
+            bool ok = true;
             const int pre = (C::kNW < (p1 - p0)) ? C::kNW : (p1 - p0);
-            for (int ps = 0; ps < pre; ++ps) {
+            griddep_wait();
+            for (int bs = 0; bs < C::kNB && bs < nbst; ++bs) {
+                uint8_t* dst = smem + C::kOffB + bs * C::kBStageBytes;
+                const int64_t sub0 = (int64_t)p0 * kSubPerPair + (int64_t)bs * kBStageSubs;
+                mbar_arrive_expect_tx(&b_full[bs], C::kBQhBytes + C::kBDxBytes);
+                bulk_load(dst, qh_tile + sub0 * kChunksPerSub * MT * 16, C::kBQhBytes, &b_full[bs]);
+                bulk_load(dst + C::kBQhBytes, dx_tile + sub0 * MT * 4, C::kBDxBytes, &b_full[bs]);
+                ++issued_b;
+            }
+            if (pre > 1) ok = mbar_wait(&w_full[0], 0, abort_flag, err, kDevErrTimeoutW);
+            for (int ps = 1; ps < pre && ok; ++ps) {
                 mbar_arrive_expect_tx(&w_full[ps], kWStageBytes);
                 tma_load_2d(smem + C::kOffW + ps * kWStageBytes, &tmap_w,
                             (p0 + ps) * (kPairBytes / 4), n0, &w_full[ps]);
                 ++issued_w;
             }
-            griddep_wait();
-            for (int bs = 0; bs < nbst && ok; ++bs) {
+            for (int bs = issued_b; bs < nbst && ok; ++bs) {
                 if (bs % (kSubPerPair / kBStageSubs) == 0) {
                     const int ps = bs / (kSubPerPair / kBStageSubs);
                     if (ps >= pre) {
