@@ -44,27 +44,11 @@
 namespace iq4xs {
 namespace {
 
-constexpr int kTcThreads = 32 * 16;   // 4 warpgroups
-constexpr int kDecWarps = 8;          // warps 0-7
-constexpr int kDecGroups = 2;         // groups of 4 warps, alternating sub-block pairs
-constexpr int kMmaWarp0 = 8;          // MMA issuers: warps 8 and 11 (even / odd units)
-constexpr int kMmaWarp1 = 11;
-constexpr int kProducerWarp = 9;
-constexpr int kTmemWarp = 10;
-constexpr int kEpiWarp0 = 12;         // epilogue: warps 12-15
 constexpr int kTmemCols = 512;        // whole TMEM; one CTA per SM (see kMinSmem)
 constexpr int kMaxCluster = 8;
 constexpr int kMinSmem = 120 * 1024;  // > half of the SM's shared memory: one CTA per SM
 constexpr int kACols = kSub / 2;      // 16 TMEM columns of fp16 pairs per sub-block
 constexpr int kCoreSbo = 128;         // 8 rows x 16 B core matrices, contiguous along N
-// Per-warpgroup register budgets (setmaxnreg).  The block launches with
-// 65536 / 512 = 128 registers per thread; the budgets sum to
-// 128 * (2 * 96 + 56 + 248) = 63488, within the 65536 it holds.
-constexpr int kRegsDecode = 96;
-constexpr int kRegsControl = 56;
-constexpr int kRegsEpilogue = 248;
-static_assert(128 * (kDecGroups * kRegsDecode + kRegsControl + kRegsEpilogue) <= kTcThreads * 128,
-              "register split fits the launch allocation");
 
 template <int R>
 __device__ __forceinline__ void reg_alloc() {
@@ -78,6 +62,27 @@ __device__ __forceinline__ void reg_dealloc() {
 template <int MT>
 struct TcCfg {
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= kMaxMTile, "UMMA N for M=128");
+    // Warp roles.  Decoders: kDecGroups groups of four warps (warpgroups
+    // 0..G-1); more groups hide more of the decode's latency where the
+    // epilogue is light (small tiles).  Then one control warpgroup (MMA
+    // issuers, TMA producer, tensor-memory owner) and the epilogue warpgroup.
+    static constexpr int kDecGroups = 2;  // three groups measured slower: the epilogue then starves
+    static constexpr int kDecWarps = 4 * kDecGroups;
+    static constexpr int kMmaWarp0 = kDecWarps;       // MMA issuers (even / odd units)
+    static constexpr int kProducerWarp = kDecWarps + 1;
+    static constexpr int kTmemWarp = kDecWarps + 2;
+    static constexpr int kMmaWarp1 = kDecWarps + 3;
+    static constexpr int kEpiWarp0 = kDecWarps + 4;
+    static constexpr int kThreads = 32 * (kDecWarps + 8);
+    // Per-warpgroup register budgets (setmaxnreg).  The block launches with
+    // the registers of 65536 / kThreads per thread (rounded down to 8); the
+    // budgets, 128 threads each, must sum within that.
+    static constexpr int kRegsLaunch = (65536 / kThreads) / 8 * 8;
+    static constexpr int kRegsDecode = (kDecGroups == 3) ? 88 : 96;
+    static constexpr int kRegsControl = 56;
+    static constexpr int kRegsEpilogue = (kDecGroups == 3) ? 160 : 248;
+    static_assert(kDecGroups * kRegsDecode + kRegsControl + kRegsEpilogue <= (kThreads / 128) * kRegsLaunch,
+                  "register split fits the launch allocation");
     // Work unit: kU consecutive sub-blocks, decoded, multiplied and scaled
     // together (one barrier handshake per unit between the roles).
     static constexpr int kU = (MT <= 96) ? 2 : 1;
@@ -135,11 +140,14 @@ __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_saddr, uint32_t ran
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
     matmul_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                      const uint8_t* __restrict__ tc_op, int64_t M, int N, int K,
                      float* __restrict__ y, int64_t ldy, int* err) {
     using C = TcCfg<MT>;
+    constexpr int kDecGroups = C::kDecGroups, kDecWarps = C::kDecWarps;
+    constexpr int kMmaWarp0 = C::kMmaWarp0, kMmaWarp1 = C::kMmaWarp1;
+    constexpr int kProducerWarp = C::kProducerWarp, kTmemWarp = C::kTmemWarp, kEpiWarp0 = C::kEpiWarp0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -216,21 +224,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp < kDecWarps) {
         // ------------------------------------------------------------ decoders
-        reg_dealloc<kRegsDecode>();
-        const int g = warp >> 2;                // decoder group: units g, g+2, ...
+        reg_dealloc<C::kRegsDecode>();
+        const int g = warp >> 2;                // decoder group: units g, g+G, ...
         const int t = (warp & 3) * 32 + lane;   // row within the tile == TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         bool ok = true;
         // A unit is kU consecutive sub-blocks of one super-block of one W
         // stage.  Software pipeline: unit v's tensor-memory stores are
-        // issued, and completed and signalled only after unit v+2 has been
+        // issued, and completed and signalled only after the group's next unit has been
         // decoded, so their latency hides behind that decode.
-        int jj = C::kU * g, wslot = 0, wphase = 0;  // position in the W ring
         int sp = g, sphase = 0;                     // unit slot of v (v % kNP, v / kNP)
         int pend_sp = -1;                           // slot stored but not yet signalled
+        int prev_ps = -1;                           // W stage of this group's previous unit
         for (int v = g; v < nunits; v += kDecGroups) {
-            if (ok && jj < C::kU * kDecGroups)
-                ok = mbar_wait(&w_full[wslot], wphase, abort_flag, err, kDevErrTimeoutW);
+            const int l0 = v * C::kU;
+            const int ps = l0 / kSubPerPair, jj = l0 % kSubPerPair;
+            const int wslot = ps % C::kNW;
+            if (ok && ps != prev_ps)  // this group's first unit of the stage
+                ok = mbar_wait(&w_full[wslot], (ps / C::kNW) & 1, abort_flag, err, kDevErrTimeoutW);
+            prev_ps = ps;
             const uint8_t* blk = smem + C::kOffW + wslot * kWStageBytes + t * kPairBytes +
                                  (jj / kSubPerBlock) * kBlockBytes;
             const int j = jj % kSubPerBlock;
@@ -254,12 +266,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int u = 0; u < C::kU; ++u) Sw[u] = iq4xs_scale(hdr.x, hdr.y, j + u);
             // The stage's bytes are consumed (in registers) once this warp's
             // last unit of it is decoded.
-            jj += C::kU * kDecGroups;
-            if (jj >= kSubPerPair) {
+            if (v + kDecGroups >= nunits || (l0 + kDecGroups * C::kU) / kSubPerPair != ps) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&w_empty[wslot]);
-                jj -= kSubPerPair;
-                if (++wslot == C::kNW) { wslot = 0; wphase ^= 1; }
             }
             // Signal the previous unit (its stores have had a decode to land).
             if (pend_sp >= 0) {
@@ -278,7 +287,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             pend_sp = sp;
             sp += kDecGroups;
-            if (sp >= C::kNP) { sp -= C::kNP; sphase ^= 1; }
+            while (sp >= C::kNP) { sp -= C::kNP; sphase ^= 1; }
         }
         if (pend_sp >= 0) {
             tmem_wait_st();
@@ -287,7 +296,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) mbar_arrive(&a_full[pend_sp]);
         }
     } else if (warp < kEpiWarp0) {
-        reg_dealloc<kRegsControl>();
+        reg_dealloc<C::kRegsControl>();
         if (warp == kMmaWarp0 || warp == kMmaWarp1) {
             // ---------------------------------------------------------- MMA
             // Warp-uniform loop with incremental indices (the warp shares its
@@ -393,7 +402,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        reg_alloc<kRegsEpilogue>();
+        reg_alloc<C::kRegsEpilogue>();
         const int t = (warp & 3) * 32 + lane;  // row within the tile == TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         constexpr int kCols = C::kU * MT;      // accumulator columns of a unit
@@ -493,7 +502,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         cluster_sync_all();
         if (warp < kDecWarps || warp >= kEpiWarp0) {
             griddep_wait();
-            const int idx = (warp < kDecWarps) ? threadIdx.x : threadIdx.x - 4 * 32 * 1;
+            const int idx = (warp < kDecWarps) ? threadIdx.x : threadIdx.x - 4 * 32;
             const int64_t mrows = M - (int64_t)z * MT;
             const uint32_t red_s = smem_u32(smem + C::kOffW);
             static_assert(C::kOffW % 16 == 0 && C::kRedStride % 4 == 0, "16-byte reduction rows");
@@ -501,7 +510,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int rows = r1 - r0;
             // element e = (row, 4 columns); consecutive threads take
             // consecutive rows, so the stores to y coalesce
-            for (int e = idx; e < rows * (MT / 4); e += 12 * 32) {
+            for (int e = idx; e < rows * (MT / 4); e += (kDecWarps + 4) * 32) {
                 const int row = r0 + e % rows, m = 4 * (e / rows);
                 const uint32_t a = red_s + (uint32_t)((row * C::kRedStride + m) * 4);
                 float4 v[kMaxCluster];
@@ -559,7 +568,7 @@ cudaError_t launch_mt(const CUtensorMap& tmap, const uint8_t* tc_op, int64_t M, 
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ntiles, (unsigned)S, (unsigned)mtiles);
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];

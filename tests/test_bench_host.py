@@ -73,9 +73,9 @@ def test_clock_parser(tmp_path):
 def test_traffic_record_is_ignored_when_kernels_change(tmp_path, monkeypatch):
     p = tmp_path / "t.txt"
     p.write_text("kernel_source_sha256_16: deadbeefdeadbeef\n"
-                 "dram_bytes_per_matmul_launch_sweep_avg: 123\n")
+                 "dram_bytes_per_tc_launch_mean: 123\n")
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(p))
     assert bench.recorded_traffic() is None
     p.write_text(f"kernel_source_sha256_16: {bench.kernel_source_hash()}\n"
-                 "dram_bytes_per_matmul_launch_sweep_avg: 123\n")
+                 "dram_bytes_per_tc_launch_mean: 123\n")
     assert bench.recorded_traffic() == 123.0
