@@ -291,7 +291,8 @@ def run_ours(args, world, rank, local):
     def launch_step(v):
         for i, M in enumerate(ms):
             qs, ds, op = acts[M]
-            B.iq4xs_quantize_q8_1(xs[M], qs, ds, op, stream)
+            # the tensor-core operand is written only for the path that reads it
+            B.iq4xs_quantize_q8_1(xs[M], qs, ds, op if paths[M] == B.PATH_TC else None, stream)
             B.iq4xs_matmul(wcopies[v * len(ms) + i], N, K, qs, ds, op, M, ys[M], paths[M], stream)
 
     # Eager warm-up (also performs the library's one-time device set-up).
@@ -491,7 +492,7 @@ def decode_stream(torch, B, dev, reps=5):
 
         def step():
             for (w, N, K, x, qs, ds, op, y, path) in calls:
-                B.iq4xs_quantize_q8_1(x, qs, ds, op, stream)
+                B.iq4xs_quantize_q8_1(x, qs, ds, op if path == B.PATH_TC else None, stream)
                 B.iq4xs_matmul(w, N, K, qs, ds, op, M, y, path, stream)
         with torch.cuda.stream(stream):
             step()
@@ -538,7 +539,7 @@ def run_e2e(args, dev, w_np, x_np, ms, N, K, world, wcopies, paths):
             for i, M in enumerate(ms):
                 dx[M].copy_(hx[M], non_blocking=True)
                 qs, ds, op = acts[M]
-                B.iq4xs_quantize_q8_1(dx[M], qs, ds, op, stream)
+                B.iq4xs_quantize_q8_1(dx[M], qs, ds, op if paths[M] == B.PATH_TC else None, stream)
                 B.iq4xs_matmul(wcopies[v * len(ms) + i], N, K, qs, ds, op, M, dy[M], paths[M], stream)
                 hy[M].copy_(dy[M], non_blocking=True)
         stream.synchronize()

@@ -49,8 +49,10 @@
  *      qs  int8  [M][K]     q = round(x/d), ties away from zero
  *      ds  half2 [M][K/32]  {d = amax/127, s = d*sum(q)} each rounded to fp16
  *  Tensor-core operand (opaque, produced by iq4xs_quantize_q8_1 when asked):
- *      the same q values as fp16 plus the block scales d as fp32, tiled for
- *      the tcgen05 path; size iq4xs_tc_operand_bytes(M, K), 16-byte aligned.
+ *      each value q*d (d the block's stored fp16 scale) held exactly as a
+ *      pair of fp16 values, tiled for the tcgen05 path; size
+ *      iq4xs_tc_operand_bytes(M, K) = 4 * Mpad * K bytes (Mpad = M rounded up
+ *      to the tile height), 16-byte aligned.
  *  y: fp32 [M][ldy] row-major, ldy >= N; columns N..ldy-1 are not written.
  */
 #ifndef IQ4XS_H

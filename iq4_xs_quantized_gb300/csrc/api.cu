@@ -91,7 +91,7 @@ extern "C" {
 
 int64_t iq4xs_tc_operand_bytes(int64_t M, int64_t K) {
     if (M < 1 || M > kMaxM || K <= 0 || K % kQK) return 0;
-    return tc_qh_bytes(M, K) + tc_dx_bytes(M, K);
+    return tc_operand_total_bytes(M, K);
 }
 
 int iq4xs_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, void* ds,
@@ -150,7 +150,7 @@ bool linear_layout(int64_t M, int64_t N, int64_t K, LinearLayout* L) {
     L->qs = 0;
     L->ds = align16(M * K);
     L->op = L->ds + align16(M * (K / kSub) * 4);
-    L->total = L->op + (L->path == IQ4XS_PATH_TC ? tc_qh_bytes(M, K) + tc_dx_bytes(M, K) : 0);
+    L->total = L->op + (L->path == IQ4XS_PATH_TC ? tc_operand_total_bytes(M, K) : 0);
     return true;
 }
 }  // namespace

@@ -84,16 +84,30 @@ __host__ __device__ inline int64_t tc_num_mtiles(int64_t M) {
     int mt = tc_mtile(M);
     return (M + mt - 1) / mt;
 }
-// Tensor-core operand: qh (fp16 q, K-permuted, tiled) then dxT (fp32 d).
-//   qh:  [mtile][K/8 chunk][MT rows][8 fp16]    (16 B per (chunk,row))
-//   dxT: [mtile][K/32 sub-block][MT rows] fp32
+// Tensor-core operand: the dequantized activations v = q*d_h (d_h the
+// block's stored fp16 scale), times a power of two 2^-e per row and span of
+// kScaleSpan values, as a pair of fp16 values hi + lo: hi = fp16(v*2^-e),
+// lo = fp16(v*2^-e - hi).  q has 8 significant bits and d_h 11, so v has at
+// most 19 and the pair holds it exactly (lo keeps the low 8 bits) whenever
+// v*2^-e is a multiple of 2^-24.  e is the smallest e >= 0 with
+// 127 * max_span(d_h) * 2^-e < 65504: hi never overflows, e = 0 (every value
+// exact) unless the span's values reach the fp16 range, and otherwise only
+// blocks 2^14 times smaller than the span's largest lose low bits.  The
+// matmul scales its fp32 partial sums by 2^e (exact) per span.
+//   planes: [mtile][K/32 sub-block][plane hi, lo][4 chunks of 8 K][MT rows][8 fp16]
+//           (16 B per (chunk, row); a sub-block is 8*MT*16 bytes)
+//   then:   [mtile][ceil(K/kScaleSpan) span][MT rows] fp32 2^e
 // Within every sub-block the K order is permuted to (0,16,1,17,...,15,31):
 // K position 2i+h holds element i+16h, matching the decoded weight order.
+constexpr int kPlanes = 2;  // hi, lo
 __host__ __device__ inline int64_t tc_qh_bytes(int64_t M, int64_t K) {
-    return tc_num_mtiles(M) * (int64_t)tc_mtile(M) * K * 2;
+    return tc_num_mtiles(M) * (int64_t)tc_mtile(M) * K * 2 * kPlanes;
 }
-__host__ __device__ inline int64_t tc_dx_bytes(int64_t M, int64_t K) {
-    return tc_num_mtiles(M) * (int64_t)tc_mtile(M) * (K / kSub) * 4;
+constexpr int kScaleSpan = 1024;                  // values per activation scale span
+constexpr int kSubPerSpan = kScaleSpan / kSub;     // 32 sub-blocks
+__host__ __device__ inline int64_t tc_num_spans(int64_t K) { return (K + kScaleSpan - 1) / kScaleSpan; }
+__host__ __device__ inline int64_t tc_operand_total_bytes(int64_t M, int64_t K) {
+    return tc_qh_bytes(M, K) + tc_num_mtiles(M) * tc_num_spans(K) * (int64_t)tc_mtile(M) * 4;
 }
 
 // ---------------------------------------------------------------------------
@@ -272,6 +286,36 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// Thread-block clusters: a barrier over all threads of the cluster, this
+// CTA's rank, and loads from another CTA's shared memory at the same offset.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// No memory clobber: loads of several ranks issue back to back; callers keep
+// them between two cluster barriers (volatile, with a clobber).
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_saddr, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_saddr), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(remote));
+    return v;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t local_saddr, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_saddr), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
+    return v;
 }
 
 // tcgen05 (5th-generation tensor core, tensor memory).

@@ -1,15 +1,20 @@
 // matmul_tc.cu -- IQ4_XS x Q8_1 matmul on the 5th-generation tensor cores.
 //
 // Method (V100TPS engine page, new-kernel table and the tile-geometry passage
-// after it): per 32-weight sub-block, an exact integer dot product of decoded
-// codebook values with Q8_1 codes, scaled by d_w*(ls-32)*d_x into fp32.
+// after it): per 32-weight sub-block, a dot product of decoded codebook
+// values with Q8_1 codes, scaled by d_w*(ls-32)*d_x into fp32.
 //
-// GB300 design.  sm_103a has no integer tcgen05 kind, so the exact small
-// integers travel as fp16 (kv in [-127, 113], q in [-127, 127]: every product
-// and every 32-term sum is an integer below 2^24, exact in the fp32 TMEM
-// accumulator).  One CTA owns 128 weight rows (= 128 TMEM lanes = UMMA M)
-// and an activation tile of MT rows (= UMMA N); K is split over a cluster
-// whose CTAs reduce their partial tiles through distributed shared memory.
+// GB300 design.  sm_103a has no integer tcgen05 kind, so the operands travel
+// as fp16: the codebook values kv (exact), and each activation's q*d_x as an
+// exact pair of fp16 values hi + lo (written by the quantizer).  Per K step
+// of 16 two MMAs accumulate kv*hi and kv*lo into the fp32 TMEM accumulator:
+// every product is exact (at most 8 + 11 significant bits), so a sub-block's
+// result d_x*sum(kv*q) differs from the exact one only by fp32 accumulation
+// rounding, and the epilogue needs no activation scale (one fp32 FMA per
+// element with d_w*(ls-32)).  One CTA owns 128 weight rows (= 128 TMEM lanes
+// = UMMA M) and an activation tile of MT rows (= UMMA N); K is split over a
+// cluster whose CTAs reduce their partial tiles through distributed shared
+// memory.
 //
 // Warp-specialized roles, each a loop over the CTA's sub-blocks, decoupled by
 // mbarrier rings (kNS slots of tensor memory per ring position: the decoded
@@ -22,18 +27,18 @@
 //                          TMEM lane i), plus d_w*(ls-32) into the scale
 //                          column, then arrives on the slot's a_full.
 //   warps 8, 11 (MMA)      warp-uniform loops over even / odd units; one
-//                          elected lane issues two tcgen05.mma 128 x MT x 16
-//                          (A from tensor memory, B from shared memory) per
-//                          sub-block and commits.  Two issuers keep the
-//                          tensor pipe fed between their own handshakes.
+//                          elected lane issues four tcgen05.mma 128 x MT x 16
+//                          (A from tensor memory, B hi / lo planes from
+//                          shared memory) per sub-block and commits.  Two
+//                          issuers keep the tensor pipe fed between their
+//                          own handshakes.
 //   warp 9 (producer)      TMA: W stages of 2 super-blocks (128 x 272 B, 2D
 //                          tensor map); activation stages of 4 sub-blocks
-//                          (bulk copies of the pre-tiled fp16 codes and their
-//                          fp32 block scales).
+//                          (one bulk copy of the pre-tiled fp16 hi / lo pairs).
 //   warp 10                allocates and frees tensor memory.
 //   warps 12-15 (epilogue) thread t reads row t's integer results and scale,
 //                          releases the slot, and accumulates
-//                          d_w*(ls-32)*d_x*dot in fp32 registers.
+//                          d_w*(ls-32)*(d_x*dot) in fp32 registers.
 // Every mbarrier wait is bounded (2 s); a timeout sets the device error word
 // and an abort flag that releases every other wait, the CTA drains its copies
 // and frees its tensor memory, and the call's output is undefined.
@@ -96,19 +101,20 @@ struct TcCfg {
     static_assert(kColS + kNP * kU <= kTmemCols, "slots fit tensor memory");
     static_assert(kNP >= 2, "at least two units in flight");
     static_assert(kBStageSubs % kU == 0 && kSubPerBlock % kU == 0, "units tile stages and super-blocks");
-    static constexpr int kNW = (MT <= 32) ? 5 : (MT <= 64) ? 4 : 3;  // W stages
-    static constexpr int kNB = (MT <= 96) ? 4 : 3;                    // activation stages
-    static constexpr int kBQhBytes = kBStageChunks * MT * 16;  // fp16 codes of 4 sub-blocks
-    static constexpr int kBDxBytes = kBStageSubs * MT * 4;     // their fp32 block scales
-    // slot stride, padded to 1 KB; the copies into a slot fill kBQhBytes + kBDxBytes
-    static constexpr int kBStageBytes = (kBQhBytes + kBDxBytes + 1023) / 1024 * 1024;
+    static constexpr int kNW = (MT <= 16) ? 5 : (MT <= 48) ? 4 : (MT <= 96) ? 3 : 2;  // W stages
+    static constexpr int kNB = (MT <= 32) ? 4 : (MT <= 64) ? 3 : 2;                   // activation stages
+    static constexpr int kBSubBytes = kPlanes * kChunksPerSub * MT * 16;  // hi + lo of one sub-block
+    static constexpr int kBQhBytes = kBStageSubs * kBSubBytes;            // one bulk copy per stage
+    static constexpr int kBStageBytes = kBQhBytes;
     static constexpr int kOffW = 0;
     static constexpr int kOffB = kOffW + kNW * kWStageBytes;
     static constexpr int kOffBar = kOffB + kNB * kBStageBytes;
     // W full/empty, B full/empty, A full / MMA done / accumulator free per unit slot, drain
     static constexpr int kNumBars = 2 * kNW + 2 * kNB + 3 * kNP + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;   // tmem base, abort flag
-    static constexpr int kUsed = kOffMisc + 16;
+    static constexpr int kOffSpan = (kOffMisc + 16 + 15) / 16 * 16;  // current span's scales (MT fp32)
+    static_assert(kOffSpan % 16 == 0, "span scales are read as 16-byte vectors");
+    static constexpr int kUsed = kOffSpan + MT * 4;
     static_assert(kUsed <= 226 * 1024, "stages fit shared memory");
     static constexpr int kSmem = (kUsed + 1024 > kMinSmem) ? kUsed + 1024 : kMinSmem;
     static constexpr int kRedStride = MT + 4;                  // fp32 words per row (16-byte rows)
@@ -117,26 +123,9 @@ struct TcCfg {
     static_assert(kOffB % 1024 == 0 && kBStageBytes % 16 == 0, "alignment");
 };
 
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// 16 bytes of CTA `rank`'s shared memory at this CTA's offset `local_saddr`.
-// No memory clobber: the loads of all ranks issue back to back (they stay
-// between the two cluster barriers, which are volatile with a clobber).
-__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_saddr, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_saddr), "r"(rank));
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(remote));
-    return v;
+constexpr int kEpilogueBarrier = 1;  // named barrier: the 4 epilogue warps
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 template <int MT>
@@ -181,9 +170,8 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
     const int nsub = (p1 - p0) * kSubPerPair;
     const int nunits = nsub / C::kU;
     const int nbst = nsub / kBStageSubs;
-    const int64_t K8 = K / kChunkElems, K32 = K / kSub;
-    const uint8_t* qh_tile = tc_op + (int64_t)z * K8 * MT * 16;
-    const uint8_t* dx_tile = tc_op + tc_qh_bytes(M, K) + (int64_t)z * K32 * MT * 4;
+    const int64_t K32 = K / kSub;
+    const uint8_t* qh_tile = tc_op + (int64_t)z * K32 * C::kBSubBytes;
 
     static_assert(C::kNumBars <= 64, "barriers initialised two per producer lane");
     if (warp == kProducerWarp) {
@@ -196,7 +184,7 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
             if (i < C::kNW) count = 1;                                           // w_full
             else if (i < 2 * C::kNW) count = kDecWarps;                          // w_empty
             else if (i < 2 * C::kNW + C::kNB) count = 1;                         // b_full
-            else if (i < 2 * C::kNW + 2 * C::kNB) count = 2 + 4;                 // b_empty: MMA warps + epilogue warps
+            else if (i < 2 * C::kNW + 2 * C::kNB) count = 2;                     // b_empty: the MMA warps' commits
             else if (i < 2 * C::kNW + 2 * C::kNB + C::kNP) count = 4;            // a_full: a decoder group
             else if (i < 2 * C::kNW + 2 * C::kNB + 2 * C::kNP) count = 1;        // mma_done
             else if (i < 2 * C::kNW + 2 * C::kNB + 3 * C::kNP) count = 4;        // d_free: epilogue warps
@@ -318,15 +306,18 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
                 tc_fence_after();
                 if (elect_one()) {
                     if (ok) {
-                        const uint32_t boff = (uint32_t)(bslot * C::kBStageBytes + lb * kChunksPerSub * MT * 16);
+                        const uint32_t boff = (uint32_t)(bslot * C::kBStageBytes + lb * C::kBSubBytes);
 #pragma unroll
                         for (int u = 0; u < C::kU; ++u)
 #pragma unroll
                             for (int i = 0; i < kMmaPerSub; ++i)
-                                tc_mma_f16_ta(
-                                    tmem + (uint32_t)(C::kColD + (sp * C::kU + u) * MT),
-                                    tmem + (uint32_t)(C::kColA + (sp * C::kU + u) * kACols + i * (kUmmaK / 2)),
-                                    bdesc0 + ((boff + (u * kChunksPerSub + 2 * i) * MT * 16) >> 4), idesc, i);
+#pragma unroll
+                                for (int pl = 0; pl < kPlanes; ++pl)
+                                    tc_mma_f16_ta(
+                                        tmem + (uint32_t)(C::kColD + (sp * C::kU + u) * MT),
+                                        tmem + (uint32_t)(C::kColA + (sp * C::kU + u) * kACols + i * (kUmmaK / 2)),
+                                        bdesc0 + ((boff + u * C::kBSubBytes + (pl * kChunksPerSub + 2 * i) * MT * 16) >> 4),
+                                        idesc, (i | pl) != 0);
                     }
                     // Commits are made even after an abort so that every
                     // waiter's barrier still completes.
@@ -353,9 +344,8 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
             for (int bs = 0; bs < C::kNB && bs < nbst; ++bs) {
                 uint8_t* dst = smem + C::kOffB + bs * C::kBStageBytes;
                 const int64_t sub0 = (int64_t)p0 * kSubPerPair + (int64_t)bs * kBStageSubs;
-                mbar_arrive_expect_tx(&b_full[bs], C::kBQhBytes + C::kBDxBytes);
-                bulk_load(dst, qh_tile + sub0 * kChunksPerSub * MT * 16, C::kBQhBytes, &b_full[bs]);
-                bulk_load(dst + C::kBQhBytes, dx_tile + sub0 * MT * 4, C::kBDxBytes, &b_full[bs]);
+                mbar_arrive_expect_tx(&b_full[bs], C::kBQhBytes);
+                bulk_load(dst, qh_tile + sub0 * C::kBSubBytes, C::kBQhBytes, &b_full[bs]);
                 ++issued_b;
             }
             if (pre > 1) ok = mbar_wait(&w_full[0], 0, abort_flag, err, kDevErrTimeoutW);
@@ -386,9 +376,8 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
                 if (!ok) break;
                 uint8_t* dst = smem + C::kOffB + slot * C::kBStageBytes;
                 const int64_t sub0 = (int64_t)p0 * kSubPerPair + (int64_t)bs * kBStageSubs;
-                mbar_arrive_expect_tx(&b_full[slot], C::kBQhBytes + C::kBDxBytes);
-                bulk_load(dst, qh_tile + sub0 * kChunksPerSub * MT * 16, C::kBQhBytes, &b_full[slot]);
-                bulk_load(dst + C::kBQhBytes, dx_tile + sub0 * MT * 4, C::kBDxBytes, &b_full[slot]);
+                mbar_arrive_expect_tx(&b_full[slot], C::kBQhBytes);
+                bulk_load(dst, qh_tile + sub0 * C::kBSubBytes, C::kBQhBytes, &b_full[slot]);
                 ++issued_b;
             }
             // Drain: the last copies issued into each ring slot have landed.
@@ -409,13 +398,37 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
         float acc[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+        // Activation span scales (from the preceding grid): the partial sums
+        // are kept in units of the current span's 2^-e and rescaled by exact
+        // powers of two where the span changes (every 32 sub-blocks).  The
+        // current span's scales are staged in shared memory.
+        griddep_wait();
+        const float* span_scale = reinterpret_cast<const float*>(tc_op + tc_qh_bytes(M, K)) +
+                                  (int64_t)z * tc_num_spans(K) * MT;
+        float* s_span = reinterpret_cast<float*>(smem + C::kOffSpan);
+        int cur_span = (p0 * kSubPerPair) / kSubPerSpan;
+        if (t < MT) s_span[t] = span_scale[(int64_t)cur_span * MT + t];
+        named_barrier_sync(kEpilogueBarrier, kTileN);
         bool ok = true;
-        int sp = 0, sphase = 0, bslot = 0, bphase = 0;
-        for (int v = 0, l0 = 0; v < nunits; ++v, l0 += C::kU) {
-            const int lb = l0 % kBStageSubs;
-            if (ok && lb == 0) ok = mbar_wait(&b_full[bslot], bphase, abort_flag, err, kDevErrTimeoutB);
-            const float* dxs = reinterpret_cast<const float*>(smem + C::kOffB + bslot * C::kBStageBytes +
-                                                              C::kBQhBytes + lb * MT * 4);
+        int sp = 0, sphase = 0;
+        for (int v = 0; v < nunits; ++v) {
+            const int span = (p0 * kSubPerPair + v * C::kU) / kSubPerSpan;
+            if (span != cur_span) {
+                const float4* fo = reinterpret_cast<const float4*>(s_span);
+                const float4* fn = reinterpret_cast<const float4*>(span_scale + (int64_t)span * MT);
+#pragma unroll
+                for (int m = 0; m < MT; m += 4) {
+                    const float4 a = fo[m / 4], b = fn[m / 4];
+                    acc[m] *= a.x / b.x;
+                    acc[m + 1] *= a.y / b.y;
+                    acc[m + 2] *= a.z / b.z;
+                    acc[m + 3] *= a.w / b.w;
+                }
+                named_barrier_sync(kEpilogueBarrier, kTileN);  // every thread has read the old scales
+                if (t < MT) s_span[t] = span_scale[(int64_t)span * MT + t];
+                named_barrier_sync(kEpilogueBarrier, kTileN);
+                cur_span = span;
+            }
             if (ok) ok = mbar_wait(&mma_done[sp], sphase, abort_flag, err, kDevErrTimeoutMma);
             tc_fence_after();
             const uint32_t dcol = tmem + lane_off + (uint32_t)(C::kColD + sp * kCols);
@@ -448,33 +461,32 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&d_free[sp]);
                 }
-                // acc[m] += P * (Sw * dx), two columns per instruction; a
-                // group of four columns never straddles two sub-blocks.
+                // acc[m] += (d_x * dot) * Sw, two columns per instruction; a
+                // pair of columns never straddles two sub-blocks.
 #pragma unroll
-                for (int k = 0; k < 64; k += 4) {
+                for (int k = 0; k < 64; k += 2) {
                     if (k >= w) break;
                     const int c = part + k, u = c / MT, m = c % MT;
                     const float sw = __uint_as_float(swb[u]);
-                    const float2 Sw2 = make_float2(sw, sw);
-                    const float4 d = *reinterpret_cast<const float4*>(dxs + u * MT + m);
-                    const float2 s01 = __fmul2_rn(Sw2, make_float2(d.x, d.y));
-                    const float2 s23 = __fmul2_rn(Sw2, make_float2(d.z, d.w));
-                    const float2 a01 = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
-                                                  s01, make_float2(acc[m], acc[m + 1]));
-                    const float2 a23 = __ffma2_rn(make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
-                                                  s23, make_float2(acc[m + 2], acc[m + 3]));
-                    acc[m] = a01.x;
-                    acc[m + 1] = a01.y;
-                    acc[m + 2] = a23.x;
-                    acc[m + 3] = a23.y;
+                    const float2 a = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
+                                                make_float2(sw, sw), make_float2(acc[m], acc[m + 1]));
+                    acc[m] = a.x;
+                    acc[m + 1] = a.y;
                 }
             }
-            if (lb + C::kU == kBStageSubs) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&b_empty[bslot]);
-                if (++bslot == C::kNB) { bslot = 0; bphase ^= 1; }
-            }
             if (++sp == C::kNP) { sp = 0; sphase ^= 1; }
+        }
+        // Back to true units: times the last span's 2^e (exact).
+        {
+            const float4* f = reinterpret_cast<const float4*>(s_span);
+#pragma unroll
+            for (int m = 0; m < MT; m += 4) {
+                const float4 a = f[m / 4];
+                acc[m] *= a.x;
+                acc[m + 1] *= a.y;
+                acc[m + 2] *= a.z;
+                acc[m + 3] *= a.w;
+            }
         }
         // Partial tile -> y (one CTA) or -> shared memory for the cluster
         // reduction, which reuses the W ring: every decoder read of it

@@ -48,10 +48,12 @@ def test_select_path_and_crossover(lib):
 
 
 def test_tc_operand_bytes(lib):
-    # M rounds up to a multiple of 16 (max 128 per tile): fp16 q + fp32 scale per 32
-    assert B.iq4xs_tc_operand_bytes(1, 1024) == 16 * 1024 * 2 + 16 * 32 * 4
-    assert B.iq4xs_tc_operand_bytes(96, 4096) == 96 * 4096 * 2 + 96 * 128 * 4
-    assert B.iq4xs_tc_operand_bytes(129, 512) == 2 * 128 * 512 * 2 + 2 * 128 * 16 * 4
+    # M rounds up to a multiple of 16 (max 128 per tile); q*d as an exact
+    # fp16 pair (4 bytes) per padded activation element, plus one fp32 power
+    # of two per padded row and span of 1024 values
+    assert B.iq4xs_tc_operand_bytes(1, 1024) == 16 * 1024 * 4 + 16 * 1 * 4
+    assert B.iq4xs_tc_operand_bytes(96, 4096) == 96 * 4096 * 4 + 96 * 4 * 4
+    assert B.iq4xs_tc_operand_bytes(129, 512) == 2 * 128 * 512 * 4 + 2 * 128 * 1 * 4
     assert B.iq4xs_tc_operand_bytes(0, 1024) == 0
     assert B.iq4xs_tc_operand_bytes(4, 1000) == 0
 
