@@ -76,10 +76,16 @@ typedef enum {
 } iq4xs_status;
 
 typedef enum {
-    IQ4XS_PATH_AUTO = 0, /* iq4xs_select_path decides from (M, N, K)            */
-    IQ4XS_PATH_DP4A = 1, /* CUDA-core int8 dot products (small M)               */
-    IQ4XS_PATH_TC = 2    /* tcgen05 tensor cores on exact small-integer fp16
-                            operands, per-sub-block fp32 scale-in (larger M)    */
+    IQ4XS_PATH_AUTO = 0,    /* iq4xs_select_path decides from (M, N, K)          */
+    IQ4XS_PATH_DP4A = 1,    /* CUDA-core int8 dot products (small M)             */
+    IQ4XS_PATH_TC = 2,      /* tcgen05 tensor cores, exact fp16 operand products,
+                               per-sub-block fp32 scale-in (larger M)            */
+    IQ4XS_PATH_BASELINE = 3 /* advice from iq4xs_select_path only: above a
+                               measured M, dequantizing W (iq4xs_dequantize) and
+                               a dense bf16 GEMM in the caller's BLAS is faster,
+                               at bf16 precision.  The library's own calls never
+                               take it: iq4xs_matmul / iq4xs_linear run TC
+                               there, and reject it as an explicit path.        */
 } iq4xs_path;
 
 /*
@@ -184,9 +190,10 @@ int iq4xs_dequantize(const void* w, int64_t N, int64_t K, void* out, int out_dty
 /*
  * Path choice for (M, N, K) (engine page, mmvq vs dequantize table: the
  * original dispatcher hard-coded its threshold at M=8 while the measured
- * crossover was M~15).  Host only, no device access.  Returns DP4A when
- * M <= the calibrated crossover for that shape class and the DP4A path
- * applies, TC otherwise (TC requires K % 512 == 0).
+ * crossover was M~15; the dequantize + GEMM route was the choice above it).
+ * Host only, no device access.  Returns DP4A when M <= the calibrated
+ * crossover and the DP4A path applies; BASELINE when M >= the calibrated
+ * baseline threshold (0 = never); TC otherwise (TC requires K % 512 == 0).
  */
 int iq4xs_select_path(int64_t M, int64_t N, int64_t K, int* path_out);
 
@@ -195,6 +202,13 @@ int iq4xs_select_path(int64_t M, int64_t N, int64_t K, int* path_out);
  * Host only.  Defaults to 4 until a calibration sets it.  Thread-safe.
  */
 int iq4xs_set_crossover(int64_t m_max_dp4a);
+
+/*
+ * Install the measured upper threshold: iq4xs_select_path answers BASELINE
+ * for M >= m_min_baseline (0 = never, the default until a calibration sets
+ * it).  Host only.  Thread-safe.
+ */
+int iq4xs_set_baseline_threshold(int64_t m_min_baseline);
 
 /*
  * Programmatic dependent launch (default on): each kernel lets the next one

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libiq4xs.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "iq4xs.h")
 
 OK, ERR_ARG, ERR_ALIGN, ERR_SHAPE, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT = range(7)
-PATH_AUTO, PATH_DP4A, PATH_TC = 0, 1, 2
+PATH_AUTO, PATH_DP4A, PATH_TC, PATH_BASELINE = 0, 1, 2, 3
 PATHS = {"auto": PATH_AUTO, "dp4a": PATH_DP4A, "tc": PATH_TC}
 
 _lock = threading.Lock()
@@ -64,13 +64,15 @@ def load(path: str | None = None):
         lib.iq4xs_linear_static_max_bytes.restype = i64
         lib.iq4xs_select_path.argtypes = [i64, i64, i64, ctypes.POINTER(ci)]
         lib.iq4xs_set_crossover.argtypes = [i64]
+        lib.iq4xs_set_baseline_threshold.argtypes = [i64]
         lib.iq4xs_set_pdl.argtypes = [ci]
         lib.iq4xs_set_pdl.restype = ci
         lib.iq4xs_last_device_error.argtypes = [ctypes.POINTER(ci)]
         lib.iq4xs_status_string.argtypes = [ci]
         lib.iq4xs_status_string.restype = ctypes.c_char_p
         for name in ("iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_dequantize", "iq4xs_linear",
-                     "iq4xs_select_path", "iq4xs_set_crossover", "iq4xs_last_device_error"):
+                     "iq4xs_select_path", "iq4xs_set_crossover", "iq4xs_set_baseline_threshold",
+                     "iq4xs_last_device_error"):
             getattr(lib, name).restype = ci
         if path is None:
             _lib = lib
@@ -79,11 +81,14 @@ def load(path: str | None = None):
 
 
 def _install_calibration(lib):
-    """Apply the measured dp4a/tcgen05 crossover, if one has been calibrated."""
+    """Apply the measured crossovers (dp4a/tcgen05, and the M from which the
+    dequantize + GEMM route is advised), if they have been calibrated."""
     from . import calibrate
     table = calibrate.load_table()
     if table and "crossover_m_max_dp4a" in table:
         lib.iq4xs_set_crossover(int(table["crossover_m_max_dp4a"]))
+    if table and "baseline_m_min" in table:
+        lib.iq4xs_set_baseline_threshold(int(table["baseline_m_min"]))
 
 
 def _check(fn: str, rc: int):
@@ -174,6 +179,10 @@ def iq4xs_set_crossover(m_max_dp4a: int) -> None:
     _check("iq4xs_set_crossover", load().iq4xs_set_crossover(int(m_max_dp4a)))
 
 
+def iq4xs_set_baseline_threshold(m_min_baseline: int) -> None:
+    _check("iq4xs_set_baseline_threshold", load().iq4xs_set_baseline_threshold(int(m_min_baseline)))
+
+
 def iq4xs_set_pdl(enable: bool) -> None:
     _check("iq4xs_set_pdl", load().iq4xs_set_pdl(1 if enable else 0))
 
@@ -201,11 +210,27 @@ def alloc_activations(M: int, K: int, device="cuda", tc: bool = True):
     return qs, ds, op
 
 
-def linear(w, N: int, K: int, x, path=PATH_AUTO, stream=None, out=None):
-    """Convenience: quantize x [M, K] and return y [M, N] fp32 (two launches)."""
+def linear(w, N: int, K: int, x, path=PATH_AUTO, stream=None, out=None, allow_baseline=False):
+    """Convenience: quantize x [M, K] and return y [M, N] fp32 (two launches).
+
+    With allow_baseline and the dispatcher advising BASELINE (M at or above
+    the measured threshold), W is dequantized to bf16 by this library and the
+    product is a dense bf16 GEMM (torch / cuBLAS): faster there, at bf16
+    precision rather than the exact-product Q8_1 paths' fp32 rounding."""
     M = x.shape[0]
-    qs, ds, op = alloc_activations(M, K, x.device, tc=True)
-    iq4xs_quantize_q8_1(x, qs, ds, op, stream)
     y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=x.device)
-    iq4xs_matmul(w, N, K, qs, ds, op, M, y, path, stream)
+    if allow_baseline and path == PATH_AUTO and iq4xs_select_path(M, N, K) == PATH_BASELINE:
+        wbf = torch.empty((N, K), dtype=torch.bfloat16, device=x.device)
+        iq4xs_dequantize(w, N, K, wbf, stream)
+        s = torch.cuda.current_stream() if stream is None else stream
+        with torch.cuda.stream(s):
+            y.copy_(torch.matmul(x.to(torch.bfloat16), wbf.t()).float())
+        return y
+    kpath = path
+    if path == PATH_AUTO:
+        sel = iq4xs_select_path(M, N, K)
+        kpath = PATH_TC if sel == PATH_BASELINE else sel
+    qs, ds, op = alloc_activations(M, K, x.device, tc=(kpath == PATH_TC))
+    iq4xs_quantize_q8_1(x, qs, ds, op, stream)
+    iq4xs_matmul(w, N, K, qs, ds, op, M, y, kpath, stream)
     return y

@@ -22,6 +22,10 @@ import numpy as np
 TABLE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "dispatch_table.json")
 SHAPES = ((4096, 4096), (5120, 5120), (12288, 5120), (5120, 17408))
 MS = tuple(range(1, 17))
+# Upper threshold: the tcgen05 route (quantize + matmul) against dequantize
+# to bf16 + a dense bf16 GEMM, on the square and the two prefill shapes.
+BASE_SHAPES = ((4096, 4096), (17408, 5120), (5120, 17408))
+BASE_MS = (32, 48, 64, 80, 96, 128, 192, 256, 512)
 L2_MULTIPLE = 3
 L2_BYTES = 129 * 2**20
 
@@ -90,6 +94,77 @@ def calibrate(shapes=SHAPES, ms=MS, verbose=True):
     return table
 
 
+def _graph_time(torch, fn, reps=10):
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fn(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn(s)
+    with torch.cuda.stream(s):
+        g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        t0.record(s)
+        for _ in range(reps):
+            g.replay()
+        t1.record(s)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) * 1e3 / reps
+
+
+def calibrate_baseline(shapes=BASE_SHAPES, ms=BASE_MS, verbose=True):
+    """Smallest M from which dequantize + bf16 GEMM beats quantize + tcgen05
+    matmul at that M and every larger one (summed over the shapes); 0 if
+    never.  Returns (threshold, per-shape times)."""
+    import torch
+
+    from . import binding as B
+    from . import synth
+    rng = np.random.default_rng(321)
+    per_shape, total = {}, {M: [0.0, 0.0] for M in ms}
+    for N, K in shapes:
+        w = torch.from_numpy(synth.iq4xs_weights(rng, N, K, 1e-3)).cuda()
+        ncopy = max(2, int(np.ceil(L2_MULTIPLE * L2_BYTES / w.numel())))
+        wcopies = [w] + [w.clone() for _ in range(ncopy - 1)]
+        wbf = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+        rows = {}
+        for M in ms:
+            x = torch.randn(M, K, device="cuda")
+            qs, ds, op = B.alloc_activations(M, K, "cuda", tc=True)
+            y = torch.empty(M, N, device="cuda")
+
+            def tc(s):
+                for ww in wcopies:
+                    B.iq4xs_quantize_q8_1(x, qs, ds, op, s)
+                    B.iq4xs_matmul(ww, N, K, qs, ds, op, M, y, B.PATH_TC, s)
+
+            def base(s):
+                for ww in wcopies:
+                    B.iq4xs_dequantize(ww, N, K, wbf, s)
+                    torch.matmul(x.to(torch.bfloat16), wbf.t())
+
+            t_tc = _graph_time(torch, tc) / len(wcopies)
+            t_b = _graph_time(torch, base) / len(wcopies)
+            rows[M] = {"tc_us": round(t_tc, 3), "dequant_gemm_us": round(t_b, 3)}
+            total[M][0] += t_tc
+            total[M][1] += t_b
+            if verbose:
+                print(f"N={N} K={K} M={M}: tc {t_tc:.2f} us  dequant+gemm {t_b:.2f} us", flush=True)
+        per_shape[f"{N}x{K}"] = rows
+        del wcopies, w, wbf
+        torch.cuda.empty_cache()
+    threshold = 0
+    for M in sorted(ms, reverse=True):
+        if total[M][1] < total[M][0]:
+            threshold = M
+        else:
+            break
+    return threshold, per_shape
+
+
 def load_table():
     try:
         with open(TABLE) as f:
@@ -100,9 +175,16 @@ def load_table():
 
 def main():
     table = calibrate()
+    thr, per_shape = calibrate_baseline()
+    table["baseline_m_min"] = thr
+    table["baseline_shapes"] = per_shape
+    table["baseline_rule"] = ("smallest M from which dequantize to bf16 + a dense bf16 GEMM beats "
+                              "quantize + tcgen05 matmul at that M and every larger one, summed "
+                              "over the shapes (0 = never)")
     with open(TABLE, "w") as f:
         json.dump(table, f, indent=1)
-    print(json.dumps({"crossover_m_max_dp4a": table["crossover_m_max_dp4a"]}))
+    print(json.dumps({"crossover_m_max_dp4a": table["crossover_m_max_dp4a"],
+                      "baseline_m_min": table["baseline_m_min"]}))
 
 
 if __name__ == "__main__":

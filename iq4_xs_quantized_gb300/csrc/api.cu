@@ -30,6 +30,7 @@ struct DevState {
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 std::atomic<int64_t> g_crossover{4};
+std::atomic<int64_t> g_baseline_min{0};  // 0 = never advise the dequantize + GEMM route
 std::atomic<int> g_pdl{1};
 
 // One-time per-device set-up, done with that device current.
@@ -73,10 +74,17 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 
 inline int from_cuda(cudaError_t e) { return e == cudaSuccess ? IQ4XS_OK : IQ4XS_ERR_CUDA; }
 
-int select_path_impl(int64_t M, int64_t N, int64_t K) {
+// The path this library's own kernels take (DP4A or TC).
+int kernel_path_impl(int64_t M, int64_t N, int64_t K) {
     (void)N;
     if (K % kPairK != 0) return IQ4XS_PATH_DP4A;  // TC stages super-blocks in pairs
     return (M <= g_crossover.load()) ? IQ4XS_PATH_DP4A : IQ4XS_PATH_TC;
+}
+// The advised path: the kernel path, or BASELINE above the measured threshold.
+int select_path_impl(int64_t M, int64_t N, int64_t K) {
+    const int p = kernel_path_impl(M, N, K);
+    const int64_t b = g_baseline_min.load();
+    return (p == IQ4XS_PATH_TC && b > 0 && M >= b) ? IQ4XS_PATH_BASELINE : p;
 }
 
 }  // namespace
@@ -118,7 +126,7 @@ int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const vo
         return IQ4XS_ERR_SHAPE;
     if (ldy < N) return IQ4XS_ERR_ARG;
     if (!aligned(w, 16) || !aligned(y, 4)) return IQ4XS_ERR_ALIGN;
-    if (path == IQ4XS_PATH_AUTO) path = select_path_impl(M, N, K);
+    if (path == IQ4XS_PATH_AUTO) path = kernel_path_impl(M, N, K);
     if (path == IQ4XS_PATH_TC) {
         if (K % kPairK) return IQ4XS_ERR_SHAPE;
         if (!tc_operand) return IQ4XS_ERR_ARG;
@@ -146,7 +154,7 @@ struct LinearLayout {
 bool linear_layout(int64_t M, int64_t N, int64_t K, LinearLayout* L) {
     if (M < 1 || M > kMaxM || N < 1 || N > (1 << 30) || K <= 0 || K % kQK || K > (1 << 30))
         return false;
-    L->path = select_path_impl(M, N, K);
+    L->path = kernel_path_impl(M, N, K);
     L->qs = 0;
     L->ds = align16(M * K);
     L->op = L->ds + align16(M * (K / kSub) * 4);
@@ -199,6 +207,12 @@ int iq4xs_select_path(int64_t M, int64_t N, int64_t K, int* path_out) {
 int iq4xs_set_crossover(int64_t m_max_dp4a) {
     if (m_max_dp4a < 0 || m_max_dp4a > kMaxM) return IQ4XS_ERR_ARG;
     g_crossover.store(m_max_dp4a);
+    return IQ4XS_OK;
+}
+
+int iq4xs_set_baseline_threshold(int64_t m_min_baseline) {
+    if (m_min_baseline < 0 || m_min_baseline > kMaxM + 1) return IQ4XS_ERR_ARG;
+    g_baseline_min.store(m_min_baseline);
     return IQ4XS_OK;
 }
 

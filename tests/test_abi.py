@@ -19,7 +19,8 @@ def lib():
 def test_header_declares_the_entry_points():
     names = set(B.header_functions())
     assert {"iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_dequantize", "iq4xs_select_path",
-            "iq4xs_tc_operand_bytes", "iq4xs_set_crossover", "iq4xs_last_device_error",
+            "iq4xs_tc_operand_bytes", "iq4xs_set_crossover", "iq4xs_set_baseline_threshold",
+            "iq4xs_last_device_error",
             "iq4xs_status_string", "iq4xs_linear", "iq4xs_linear_workspace_bytes"} <= names
 
 
@@ -45,6 +46,29 @@ def test_select_path_and_crossover(lib):
     assert lib.iq4xs_select_path(1, 1, 100, ctypes.byref(out)) == B.ERR_SHAPE
     assert lib.iq4xs_select_path(1, 1, 256, None) == B.ERR_ARG
     assert lib.iq4xs_set_crossover(-1) == B.ERR_ARG
+
+
+def test_baseline_threshold_is_advice_above_the_tc_range(lib):
+    B.iq4xs_set_crossover(4)
+    B.iq4xs_set_baseline_threshold(0)  # never
+    assert B.iq4xs_select_path(512, 5120, 17408) == B.PATH_TC
+    B.iq4xs_set_baseline_threshold(128)
+    assert B.iq4xs_select_path(96, 5120, 17408) == B.PATH_TC
+    assert B.iq4xs_select_path(128, 5120, 17408) == B.PATH_BASELINE
+    assert B.iq4xs_select_path(512, 5120, 17408) == B.PATH_BASELINE
+    # below the dp4a crossover the dp4a path stays
+    B.iq4xs_set_baseline_threshold(1)
+    assert B.iq4xs_select_path(2, 4096, 4096) == B.PATH_DP4A
+    assert B.iq4xs_select_path(8, 4096, 4096) == B.PATH_BASELINE
+    # shapes the tensor-core path cannot take keep dp4a
+    assert B.iq4xs_select_path(256, 4096, 256 * 3) == B.PATH_DP4A
+    assert lib.iq4xs_set_baseline_threshold(-1) == B.ERR_ARG
+    B.iq4xs_set_baseline_threshold(0)
+    # the library's own calls never take the advice as an explicit path
+    out = ctypes.c_int()
+    rc = lib.iq4xs_matmul(ctypes.c_void_p(16), 256, 512, ctypes.c_void_p(16), ctypes.c_void_p(16),
+                          ctypes.c_void_p(16), 8, ctypes.c_void_p(16), 256, B.PATH_BASELINE, 0)
+    assert rc == B.ERR_ARG, rc
 
 
 def test_tc_operand_bytes(lib):

@@ -56,3 +56,31 @@ def test_linear_rejects_small_workspace():
     with pytest.raises(B.IQ4XSError) as e:
         B.iq4xs_linear(dev(w), N, K, dev(x), y, ws)
     assert e.value.status == B.ERR_ARG
+
+
+def test_linear_baseline_route_only_when_asked():
+    """Above the advised threshold, linear(allow_baseline=True) takes the
+    dequantize + bf16 GEMM route (bf16 precision: within a few 1e-2 of the
+    oracle's row maximum, which also carries the Q8_1 rounding the route
+    skips); without the opt-in the exact tensor-core path runs."""
+    N, K, M = 256, 1024, 128
+    w, x = synth.TINY.inputs(0, M=M)
+    wd, xd = dev(w), dev(x)
+    qs_o, d_o, _ = oracle_q8(x)
+    rows = sample_rows(N, 32, seed=5)
+    ref = oracle_matmul(w, N, K, qs_o, d_o, rows)
+    B.iq4xs_set_crossover(4)
+    B.iq4xs_set_baseline_threshold(64)
+    try:
+        assert B.iq4xs_select_path(M, N, K) == B.PATH_BASELINE
+        yb = B.linear(wd, N, K, xd, allow_baseline=True)
+        ye = B.linear(wd, N, K, xd)
+        torch.cuda.synchronize()
+    finally:
+        B.iq4xs_set_baseline_threshold(0)
+    yb, ye = yb.cpu().numpy(), ye.cpu().numpy()
+    assert gate_written(yb) is None and gate_written(ye) is None
+    assert gate_parity(ye[:, rows], ref) is None
+    scale = np.abs(ref).max(axis=1, keepdims=True)
+    err = np.abs(yb[:, rows] - ref) / scale
+    assert 0 < err.max() < 5e-2, err.max()
