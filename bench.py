@@ -369,6 +369,7 @@ def run_ours(args, world, rank, local):
         del wcopies, acts, ys, graphs
         torch.cuda.empty_cache()
         extras["decode_stream"] = decode_stream(torch, B, dev)
+        extras["moe_grouped"] = moe_grouped(torch, B, dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -523,6 +524,71 @@ def decode_stream(torch, B, dev, reps=5):
                     "weight_GB": round(wbytes / 1e9, 2), "calls": len(calls)})
         del graph, calls
         torch.cuda.empty_cache()
+    return res
+
+
+def moe_grouped(torch, B, dev, layers=12, reps=5):
+    """Routed-expert layer (128 experts of 1536 x 2048, top-8): per token
+    count T, one layer call = quantize the T*8 routed rows + the grouped
+    matmul in one launch, against the same layer with one dp4a launch per
+    routed expert.  `layers` copies of the expert set (2.6 GB) rotate so the
+    touched experts' bytes exceed L2.  GB/s counts the touched experts'
+    weights plus activations and outputs."""
+    from iq4_xs_quantized_gb300 import synth
+    W = synth.MOE_DECODE
+    w0 = torch.from_numpy(W.weights().reshape(W.G, -1)).to(dev)
+    stride = w0.shape[1]
+    ws = [w0] + [w0.clone() for _ in range(layers - 1)]
+    stream = torch.cuda.Stream(device=dev)
+    res = []
+    for T in W.tokens:
+        _, rows, offsets = W.inputs(T)
+        M = rows.shape[0]
+        xr = torch.from_numpy(rows).to(dev)
+        off = torch.from_numpy(offsets).to(dev)
+        qs, ds, _ = B.alloc_activations(M, W.K, dev, tc=False)
+        y = torch.empty((M, W.N), dtype=torch.float32, device=dev)
+        touched = [g for g in range(W.G) if offsets[g + 1] > offsets[g]]
+
+        def grouped(s):
+            for w in ws:
+                B.iq4xs_quantize_q8_1(xr, qs, ds, None, s)
+                B.iq4xs_matmul_grouped(w, stride, W.G, W.N, W.K, qs, ds, off, y, s)
+
+        def per_expert(s):
+            for w in ws:
+                B.iq4xs_quantize_q8_1(xr, qs, ds, None, s)
+                for g in touched:
+                    r0, r1 = int(offsets[g]), int(offsets[g + 1])
+                    B.iq4xs_matmul(w[g], W.N, W.K, qs[r0:r1], ds[r0:r1], None, r1 - r0, y[r0:r1],
+                                   B.PATH_DP4A, s)
+
+        times = {}
+        for name, fn in (("grouped", grouped), ("per_expert", per_expert)):
+            with torch.cuda.stream(stream):
+                fn(stream)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn(stream)
+            with torch.cuda.stream(stream):
+                g.replay()
+                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                t1.record(stream)
+            torch.cuda.synchronize()
+            times[name] = t0.elapsed_time(t1) * 1e3 / (reps * layers)
+            del g
+        nbytes = (len(touched) * W.N * (W.K // 256) * 136 + M * W.K + M * (W.K // 32) * 4
+                  + 4 * M * W.N + quantize_bytes(M, W.K))
+        res.append({"tokens": T, "rows": M, "experts_touched": len(touched),
+                    "grouped_us_per_layer": round(times["grouped"], 3),
+                    "per_expert_launches_us_per_layer": round(times["per_expert"], 3),
+                    "grouped_GBps": round(nbytes / (times["grouped"] * 1e-6) / 1e9, 1)})
+    del ws
+    torch.cuda.empty_cache()
     return res
 
 

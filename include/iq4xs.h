@@ -128,6 +128,34 @@ int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const vo
                  int64_t stream);
 
 /*
+ * Grouped (mixture-of-experts) matmul in one launch: G experts, each with its
+ * own IQ4_XS matrix and its own Q8_1 activation rows (forum page lcz.me post
+ * 31556, the decode measurement of the grouped expert kernel: one call per
+ * layer over the routed experts, because per-expert launches cost more than
+ * the experts' bytes).  CUDA-core (DP4A) path: per-expert batches are small.
+ *   w             G matrices, each [N][K/256] blocks as for iq4xs_matmul;
+ *                 expert g starts at byte g * expert_stride (expert_stride
+ *                 >= N*(K/256)*136 and a multiple of 16; w 16-byte aligned).
+ *   qs, ds        Q8_1 rows of all experts (iq4xs_quantize_q8_1 over the
+ *                 concatenated rows, grouped by expert).
+ *   row_offsets   DEVICE int32 [G+1]: expert g owns rows
+ *                 [row_offsets[g], row_offsets[g+1]); non-decreasing, read
+ *                 by the kernel after the preceding grid completes (so it may
+ *                 come from a routing kernel).
+ *   total_rows    the number of rows (row_offsets[G] <= total_rows); at most
+ *                 min(G, total_rows) experts have rows, and the launch has
+ *                 that many expert slots, each taking the next non-empty
+ *                 expert, so empty experts cost nothing.
+ *   y             fp32 [rows][ldy]; the rows of every expert are written.
+ * Each expert is computed with the batch width its own row count selects,
+ * so the result per expert is bit-identical to iq4xs_matmul on the DP4A
+ * path over the same rows.
+ */
+int iq4xs_matmul_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
+                         const int8_t* qs, const void* ds, const int32_t* row_offsets,
+                         int64_t total_rows, float* y, int64_t ldy, int64_t stream);
+
+/*
  * The projection as one call: y = Q8_1(x) . W^T from fp32 activations
  * (engine page, kernel table at M=64: the projection op quantizes its
  * activations with quantize_q8_1 and runs the batched matmul).  Launches the

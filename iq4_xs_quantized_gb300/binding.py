@@ -55,6 +55,7 @@ def load(path: str | None = None):
         lib.iq4xs_tc_operand_bytes.restype = i64
         lib.iq4xs_matmul.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, i64, ci, i64]
         lib.iq4xs_dequantize.argtypes = [vp, i64, i64, vp, ci, i64]
+        lib.iq4xs_matmul_grouped.argtypes = [vp, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, i64]
         lib.iq4xs_linear.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, i64]
         lib.iq4xs_linear_workspace_bytes.argtypes = [i64, i64, i64]
         lib.iq4xs_linear_workspace_bytes.restype = i64
@@ -70,7 +71,8 @@ def load(path: str | None = None):
         lib.iq4xs_last_device_error.argtypes = [ctypes.POINTER(ci)]
         lib.iq4xs_status_string.argtypes = [ci]
         lib.iq4xs_status_string.restype = ctypes.c_char_p
-        for name in ("iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_dequantize", "iq4xs_linear",
+        for name in ("iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_matmul_grouped",
+                     "iq4xs_dequantize", "iq4xs_linear",
                      "iq4xs_select_path", "iq4xs_set_crossover", "iq4xs_set_baseline_threshold",
                      "iq4xs_last_device_error"):
             getattr(lib, name).restype = ci
@@ -160,6 +162,20 @@ def iq4xs_linear_static(w, N: int, K: int, x, y, stream=None) -> None:
 
 def iq4xs_linear_static_max_bytes() -> int:
     return int(load().iq4xs_linear_static_max_bytes())
+
+
+def iq4xs_matmul_grouped(w, expert_stride: int, G: int, N: int, K: int, qs, ds, row_offsets, y,
+                         stream=None) -> None:
+    """Mixture-of-experts matmul in one launch: expert g (W at byte
+    g * expert_stride of w) over the Q8_1 rows [row_offsets[g],
+    row_offsets[g+1]) (row_offsets: int32 device tensor [G+1]); y holds
+    every row (its row count bounds the number of non-empty experts)."""
+    if row_offsets.dtype != torch.int32:
+        raise TypeError("row_offsets must be int32")
+    rc = load().iq4xs_matmul_grouped(_ptr(w), int(expert_stride), G, N, K, _ptr(qs), _ptr(ds),
+                                     _ptr(row_offsets), y.shape[0], _ptr(y), y.stride(0),
+                                     _stream(stream))
+    _check("iq4xs_matmul_grouped", rc)
 
 
 def iq4xs_dequantize(w, N: int, K: int, out, stream=None) -> None:

@@ -185,6 +185,25 @@ int iq4xs_linear(const void* w, int64_t N, int64_t K, const float* x, int64_t M,
     return iq4xs_matmul(w, N, K, qs, ds, op, M, y, ldy, L.path, stream);
 }
 
+int iq4xs_matmul_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
+                         const int8_t* qs, const void* ds, const int32_t* row_offsets,
+                         int64_t total_rows, float* y, int64_t ldy, int64_t stream) {
+    if (!w || !qs || !ds || !row_offsets || !y) return IQ4XS_ERR_ARG;
+    if (G < 1 || G > 65535 || N < 1 || N > (1 << 30) || K <= 0 || K % kQK || K > (1 << 30))
+        return IQ4XS_ERR_SHAPE;
+    if (ldy < N || total_rows < 1) return IQ4XS_ERR_ARG;
+    if (expert_stride < N * (K / kQK) * kBlockBytes || expert_stride % 16) return IQ4XS_ERR_ARG;
+    if (!aligned(w, 16) || !aligned(qs, 16) || !aligned(ds, 4) || !aligned(row_offsets, 4) ||
+        !aligned(y, 4))
+        return IQ4XS_ERR_ALIGN;
+    DevState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    return from_cuda(launch_matmul_dp4a_grouped(w, expert_stride, G, N, K, qs, ds, row_offsets,
+                                                total_rows, y, ldy,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int iq4xs_dequantize(const void* w, int64_t N, int64_t K, void* out, int out_dtype,
                      int64_t stream) {
     if (!w || !out) return IQ4XS_ERR_ARG;

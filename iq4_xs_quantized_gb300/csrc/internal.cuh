@@ -573,6 +573,12 @@ cudaError_t launch_dequantize(const void* w, int64_t N, int64_t K, void* out, in
 cudaError_t launch_matmul_dp4a(const void* w, int64_t N, int64_t K, const int8_t* qs,
                                const void* ds, int64_t M, float* y, int64_t ldy,
                                cudaStream_t stream);
+// G experts in one launch: expert g has W at w + g * expert_stride and the
+// Q8_1 / output rows [row_offsets[g], row_offsets[g+1]) (device array).
+cudaError_t launch_matmul_dp4a_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N,
+                                       int64_t K, const int8_t* qs, const void* ds,
+                                       const int32_t* row_offsets, int64_t total_rows, float* y,
+                                       int64_t ldy, cudaStream_t stream);
 // Programmatic dependent launch on (default) or off for every launch.
 bool pdl_enabled();
 // `encode` is the driver's cuTensorMapEncodeTiled; `err` the device error word.

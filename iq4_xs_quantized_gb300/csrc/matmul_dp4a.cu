@@ -28,21 +28,18 @@ __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
     return __dp4a((int)a, (int)b, c);
 }
 
-template <int MC>  // activation rows per pass
-__global__ void __launch_bounds__(kDp4aThreads, 2)
-    matmul_dp4a_kernel(const uint8_t* __restrict__ w, int64_t N, int64_t K,
-                       const int8_t* __restrict__ qs, const __half2* __restrict__ ds, int64_t M,
-                       float* __restrict__ y, int64_t ldy) {
-    griddep_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-    const int64_t n0 = warp * kRows;
-    if (n0 >= N) return;  // whole warp
+// Rows [0, M) of x against the warp's kRows weight rows n0.. of W, MC
+// activation rows per pass.  `waited`: the wait for the preceding grid (which
+// wrote the activations) has been done already.
+template <int MC>
+__device__ __forceinline__ void dp4a_rows(const uint8_t* __restrict__ w, int64_t N, int64_t K,
+                                          const int8_t* __restrict__ qs,
+                                          const __half2* __restrict__ ds, int64_t M,
+                                          float* __restrict__ y, int64_t ldy, int64_t n0, int lane,
+                                          bool waited) {
     const int64_t nsub = K / kSub;
     const int64_t row_bytes = (K / kQK) * kBlockBytes;
     constexpr int kIters = iters_for<MC>();
-    bool waited = false;
-
     for (int64_t m0 = 0; m0 < M; m0 += MC) {
         float acc[kRows][MC];
 #pragma unroll
@@ -150,20 +147,90 @@ __global__ void __launch_bounds__(kDp4aThreads, 2)
     }
 }
 
-template <int MC>
-cudaError_t launch_mc(const uint8_t* w, int64_t N, int64_t K, const int8_t* qs, const __half2* ds,
-                      int64_t M, float* y, int64_t ldy, cudaStream_t stream) {
-    static_assert(kRows * MC <= 32, "one output per lane");
+template <int MC>  // activation rows per pass
+__global__ void __launch_bounds__(kDp4aThreads, 2)
+    matmul_dp4a_kernel(const uint8_t* __restrict__ w, int64_t N, int64_t K,
+                       const int8_t* __restrict__ qs, const __half2* __restrict__ ds, int64_t M,
+                       float* __restrict__ y, int64_t ldy) {
+    griddep_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t n0 = ((int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)) * kRows;
+    if (n0 >= N) return;  // whole warp
+    dp4a_rows<MC>(w, N, K, qs, ds, M, y, ldy, n0, lane, false);
+}
+
+// Grouped (mixture-of-experts) form: G experts, expert g with its own W at
+// w + g * expert_stride and the activation / output rows
+// [row_offsets[g], row_offsets[g+1]) (a device array, read after the wait for
+// the preceding grid, which may have produced it).  blockIdx.y = k takes the
+// k-th expert that has rows; the host sizes the grid from the total row
+// count, so slots past the last non-empty expert exit at once.  The batch
+// width follows each expert's own row count, so an expert with one row costs
+// what a one-row matmul costs.
+__global__ void __launch_bounds__(kDp4aThreads, 2)
+    matmul_dp4a_grouped_kernel(const uint8_t* __restrict__ w, int64_t expert_stride, int64_t G,
+                               int64_t N, int64_t K, const int8_t* __restrict__ qs,
+                               const __half2* __restrict__ ds, const int32_t* __restrict__ row_offsets,
+                               float* __restrict__ y, int64_t ldy) {
+    griddep_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t n0 = ((int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)) * kRows;
+    if (n0 >= N) return;  // whole warp
+    griddep_wait();
+    // The k-th non-empty expert: the offsets of 128 experts are loaded at
+    // once (independent loads), then a ballot per 32 of them.
+    int64_t g = -1;
+    uint32_t k = blockIdx.y;
+    for (int64_t base = 0; base < G && g < 0; base += 4 * 32) {
+        int32_t lo[4], hi[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t e = base + 32 * j + lane;
+            lo[j] = e < G ? __ldg(row_offsets + e) : 0;
+            hi[j] = e < G ? __ldg(row_offsets + e + 1) : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t mask = __ballot_sync(0xffffffffu, hi[j] > lo[j]);
+            const uint32_t cnt = __popc(mask);
+            if (g < 0) {
+                if (k < cnt) g = base + 32 * j + (int64_t)__fns(mask, 0, (int)k + 1);
+                else k -= cnt;
+            }
+        }
+    }
+    if (g < 0) return;  // fewer non-empty experts than slots (whole warp)
+    const int64_t r0 = row_offsets[g], M = row_offsets[g + 1] - r0;
+    w += g * expert_stride;
+    qs += r0 * K;
+    ds += r0 * (K / kSub);
+    y += r0 * ldy;
+    if (M == 1) dp4a_rows<1>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+    else if (M == 2) dp4a_rows<2>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+    else if (M <= 4) dp4a_rows<4>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+    else dp4a_rows<8>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+}
+
+cudaLaunchConfig_t dp4a_config(int64_t N, unsigned slots, cudaStream_t stream,
+                               cudaLaunchAttribute* attr) {
     const int64_t warps = (N + kRows - 1) / kRows;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((warps + kWarpsPerCta - 1) / kWarpsPerCta));
+    cfg.gridDim = dim3((unsigned)((warps + kWarpsPerCta - 1) / kWarpsPerCta), slots);
     cfg.blockDim = dim3(kDp4aThreads);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <int MC>
+cudaError_t launch_mc(const uint8_t* w, int64_t N, int64_t K, const int8_t* qs, const __half2* ds,
+                      int64_t M, float* y, int64_t ldy, cudaStream_t stream) {
+    static_assert(kRows * MC <= 32, "one output per lane");
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = dp4a_config(N, 1, stream, attr);
     return cudaLaunchKernelEx(&cfg, matmul_dp4a_kernel<MC>, w, N, K, qs, ds, M, y, ldy);
 }
 
@@ -178,6 +245,19 @@ cudaError_t launch_matmul_dp4a(const void* w, int64_t N, int64_t K, const int8_t
     if (M == 2) return launch_mc<2>(wb, N, K, qs, d2, M, y, ldy, stream);
     if (M <= 4) return launch_mc<4>(wb, N, K, qs, d2, M, y, ldy, stream);
     return launch_mc<8>(wb, N, K, qs, d2, M, y, ldy, stream);
+}
+
+cudaError_t launch_matmul_dp4a_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N,
+                                       int64_t K, const int8_t* qs, const void* ds,
+                                       const int32_t* row_offsets, int64_t total_rows, float* y,
+                                       int64_t ldy, cudaStream_t stream) {
+    // at most min(G, total rows) experts have rows
+    const unsigned slots = (unsigned)(G < total_rows ? G : total_rows);
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = dp4a_config(N, slots, stream, attr);
+    return cudaLaunchKernelEx(&cfg, matmul_dp4a_grouped_kernel, reinterpret_cast<const uint8_t*>(w),
+                              expert_stride, G, N, K, qs, reinterpret_cast<const __half2*>(ds),
+                              row_offsets, y, ldy);
 }
 
 }  // namespace iq4xs

@@ -96,3 +96,49 @@ DECODE_STREAM = Workload(
     ms=(1, 2, 8, 16, 32), d_scale=2e-3, layers=64)
 
 WORKLOADS = {w.name: w for w in (TINY, SQUARE, DECODER_27B, PREFILL, DECODE_STREAM)}
+
+
+@dataclasses.dataclass(frozen=True)
+class MoEWorkload:
+    """Routed experts of one layer: G experts of shape (N, K); each of T
+    tokens is routed to ``topk`` distinct experts drawn uniformly; the
+    activation rows are grouped by expert (expert g owns rows
+    [row_offsets[g], row_offsets[g+1]), tokens in increasing order)."""
+    name: str
+    seed: int
+    G: int
+    N: int
+    K: int
+    topk: int
+    tokens: tuple
+    d_scale: float
+
+    def weights(self) -> np.ndarray:
+        """uint8 [G, N, K/256*136]; expert g from its own stream."""
+        return np.stack([iq4xs_weights(np.random.default_rng([self.seed, g]), self.N, self.K,
+                                       self.d_scale) for g in range(self.G)])
+
+    def routing(self, T: int):
+        """(row_offsets int32 [G+1], token of each row int64 [T*topk])."""
+        rng = np.random.default_rng([self.seed, 100000 + T])
+        choice = np.stack([rng.choice(self.G, size=self.topk, replace=False) for _ in range(T)])
+        tok = np.repeat(np.arange(T), self.topk)
+        exp = choice.reshape(-1)
+        order = np.lexsort((tok, exp))  # by expert, then token
+        counts = np.bincount(exp, minlength=self.G)
+        offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+        return offsets, tok[order]
+
+    def inputs(self, T: int):
+        """(x [T, K] token activations, rows [T*topk, K] grouped by expert,
+        row_offsets int32 [G+1])."""
+        rng = np.random.default_rng([self.seed, 200000 + T])
+        x = activations(rng, T, self.K)
+        offsets, tok = self.routing(T)
+        return x, np.ascontiguousarray(x[tok]), offsets
+
+
+# A routed-expert layer for the grouped matmul (decode: a few tokens, top-8 of
+# 128 experts; 214 MB of expert weights, larger than L2).
+MOE_DECODE = MoEWorkload("moe_decode_128x1536x2048", seed=5, G=128, N=1536, K=2048, topk=8,
+                         tokens=(1, 4, 16), d_scale=2e-3)

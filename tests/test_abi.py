@@ -32,6 +32,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_select_path_and_crossover(lib):
     B.iq4xs_set_crossover(4)
+    B.iq4xs_set_baseline_threshold(0)  # the dp4a/tcgen05 choice alone
     assert B.iq4xs_select_path(1, 4096, 4096) == B.PATH_DP4A
     assert B.iq4xs_select_path(4, 4096, 4096) == B.PATH_DP4A
     assert B.iq4xs_select_path(5, 4096, 4096) == B.PATH_TC
@@ -46,6 +47,7 @@ def test_select_path_and_crossover(lib):
     assert lib.iq4xs_select_path(1, 1, 100, ctypes.byref(out)) == B.ERR_SHAPE
     assert lib.iq4xs_select_path(1, 1, 256, None) == B.ERR_ARG
     assert lib.iq4xs_set_crossover(-1) == B.ERR_ARG
+    B._install_calibration(lib)
 
 
 def test_baseline_threshold_is_advice_above_the_tc_range(lib):
@@ -63,12 +65,12 @@ def test_baseline_threshold_is_advice_above_the_tc_range(lib):
     # shapes the tensor-core path cannot take keep dp4a
     assert B.iq4xs_select_path(256, 4096, 256 * 3) == B.PATH_DP4A
     assert lib.iq4xs_set_baseline_threshold(-1) == B.ERR_ARG
-    B.iq4xs_set_baseline_threshold(0)
     # the library's own calls never take the advice as an explicit path
     out = ctypes.c_int()
     rc = lib.iq4xs_matmul(ctypes.c_void_p(16), 256, 512, ctypes.c_void_p(16), ctypes.c_void_p(16),
                           ctypes.c_void_p(16), 8, ctypes.c_void_p(16), 256, B.PATH_BASELINE, 0)
     assert rc == B.ERR_ARG, rc
+    B._install_calibration(lib)
 
 
 def test_tc_operand_bytes(lib):
@@ -131,3 +133,19 @@ def test_linear_workspace_and_validation(lib):
     assert lib.iq4xs_linear(p, 4096, 4096, p, 96, 4096, p, 4096, p, need - 1, 0) == B.ERR_ARG
     assert lib.iq4xs_linear(p, 4096, 4096, p, 96, 4096, p, 4096, None, need, 0) == B.ERR_ARG
     assert lib.iq4xs_linear(p, 4096, 300, p, 96, 4096, p, 4096, p, need, 0) == B.ERR_SHAPE
+
+
+def test_grouped_argument_errors_return_before_any_launch(lib):
+    p = ctypes.c_void_p(256)  # never dereferenced: validation fails first
+    f = lib.iq4xs_matmul_grouped
+    N, K, stride = 128, 512, 128 * 2 * 136
+    assert f(None, stride, 2, N, K, p, p, p, 1, p, N, 0) == B.ERR_ARG
+    assert f(p, stride, 2, N, K, p, p, None, 1, p, N, 0) == B.ERR_ARG
+    assert f(p, stride, 0, N, K, p, p, p, 1, p, N, 0) == B.ERR_SHAPE
+    assert f(p, stride, 70000, N, K, p, p, p, 1, p, N, 0) == B.ERR_SHAPE
+    assert f(p, stride, 2, N, 500, p, p, p, 1, p, N, 0) == B.ERR_SHAPE
+    assert f(p, stride - 16, 2, N, K, p, p, p, 1, p, N, 0) == B.ERR_ARG   # overlapping experts
+    assert f(p, stride + 8, 2, N, K, p, p, p, 1, p, N, 0) == B.ERR_ARG    # stride not 16-byte
+    assert f(p, stride, 2, N, K, p, p, p, 0, p, N, 0) == B.ERR_ARG        # no rows
+    assert f(p, stride, 2, N, K, p, p, p, 1, p, N - 1, 0) == B.ERR_ARG    # ldy < N
+    assert f(ctypes.c_void_p(264), stride, 2, N, K, p, p, p, 1, p, N, 0) == B.ERR_ALIGN

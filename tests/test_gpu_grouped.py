@@ -1,0 +1,111 @@
+"""Grouped (mixture-of-experts) matmul on the GPU: one launch over G experts
+with per-expert rows read from a device array.  Each expert's rows match the
+oracle (within 1e-5 per row) and, bit for bit, the single-expert dp4a call
+on the same rows; empty experts, an expert holding every row and experts
+with more rows than the kernel's batch width are covered."""
+import numpy as np
+import pytest
+import torch
+
+from _gates import gate_independent, gate_parity, gate_written
+from _gpu import dev, independent_fp32, oracle_matmul, oracle_q8, quantize_gpu
+from iq4_xs_quantized_gb300 import binding as B
+from iq4_xs_quantized_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from iq4_xs_quantized_gb300 import build
+    build.build()
+    B.load()
+    yield
+    assert B.iq4xs_last_device_error() == 0
+
+
+def _run_grouped(W, rows_x, offsets):
+    G, N, K = W.G, W.N, W.K
+    w = W.weights()
+    stride = w.shape[1] * w.shape[2]
+    wd = dev(w.reshape(G, -1))
+    qs, ds, _ = quantize_gpu(rows_x, tc=False)
+    off_d = dev(offsets.astype(np.int32))
+    M = rows_x.shape[0]
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    B.iq4xs_matmul_grouped(wd, stride, G, N, K, qs, ds, off_d, y)
+    torch.cuda.synchronize()
+    return w, wd, qs, ds, y.cpu().numpy()
+
+
+@pytest.mark.parametrize("T,topk", [(20, 4), (40, 6), (3, 2), (9, 3)])
+def test_grouped_matches_oracle_and_single_expert_calls(T, topk):
+    W = synth.MoEWorkload("moe_small", seed=7, G=8, N=256, K=1024, topk=topk, tokens=(T,),
+                          d_scale=2e-3)
+    x, rows_x, offsets = W.inputs(T)
+    w, wd, qs, ds, y = _run_grouped(W, rows_x, offsets)
+    assert gate_written(y) is None
+    qs_o, d_o, _ = oracle_q8(rows_x)
+    for g in range(W.G):
+        r0, r1 = int(offsets[g]), int(offsets[g + 1])
+        if r1 == r0:
+            continue
+        ref = oracle_matmul(w[g], W.N, W.K, qs_o[r0:r1], d_o[r0:r1])
+        r = gate_parity(y[r0:r1], ref)
+        assert r is None, (g, r)
+        # the single-expert call on the same rows gives the same bits
+        ys = torch.full((r1 - r0, W.N), float("nan"), device="cuda")
+        B.iq4xs_matmul(wd[g], W.N, W.K, qs[r0:r1], ds[r0:r1], None, r1 - r0, ys, B.PATH_DP4A)
+        torch.cuda.synchronize()
+        assert np.array_equal(ys.cpu().numpy(), y[r0:r1]), g
+    ind = independent_fp32(np.concatenate([w[g] for g in range(W.G)]), W.G * W.N, W.K, qs_o, d_o)
+    ind_own = np.full_like(y, np.nan)
+    for g in range(W.G):
+        r0, r1 = int(offsets[g]), int(offsets[g + 1])
+        ind_own[r0:r1] = ind[r0:r1, g * W.N:(g + 1) * W.N]
+    assert gate_independent(y, ind_own) is None
+
+
+@pytest.mark.parametrize("G,T,topk", [(70, 5, 2), (100, 40, 3)])
+def test_grouped_many_experts_compacted_slots(G, T, topk):
+    # more experts than a warp's ballot covers; fewer (and more) rows than experts
+    W = synth.MoEWorkload("moe_wide", seed=13, G=G, N=128, K=512, topk=topk, tokens=(T,),
+                          d_scale=2e-3)
+    _, rows_x, offsets = W.inputs(T)
+    w, wd, qs, ds, y = _run_grouped(W, rows_x, offsets)
+    assert gate_written(y) is None
+    qs_o, d_o, _ = oracle_q8(rows_x)
+    for g in range(W.G):
+        r0, r1 = int(offsets[g]), int(offsets[g + 1])
+        if r1 > r0:
+            r = gate_parity(y[r0:r1], oracle_matmul(w[g], W.N, W.K, qs_o[r0:r1], d_o[r0:r1]))
+            assert r is None, (g, r)
+
+
+def test_grouped_empty_experts_and_one_expert_with_every_row():
+    W = synth.MoEWorkload("moe_edge", seed=9, G=6, N=128, K=512, topk=1, tokens=(11,),
+                          d_scale=2e-3)
+    rng = np.random.default_rng(11)
+    rows_x = synth.activations(rng, 11, W.K)
+    offsets = np.array([0, 0, 0, 11, 11, 11, 11], dtype=np.int32)  # all rows on expert 2
+    w, wd, qs, ds, y = _run_grouped(W, rows_x, offsets)
+    assert gate_written(y) is None
+    qs_o, d_o, _ = oracle_q8(rows_x)
+    assert gate_parity(y, oracle_matmul(w[2], W.N, W.K, qs_o, d_o)) is None
+
+
+def test_grouped_rejects_bad_arguments():
+    W = synth.MoEWorkload("moe_arg", seed=1, G=2, N=128, K=512, topk=1, tokens=(2,), d_scale=2e-3)
+    w = dev(W.weights().reshape(2, -1))
+    qs, ds, _ = B.alloc_activations(2, W.K, "cuda", tc=False)
+    off = torch.tensor([0, 1, 2], dtype=torch.int32, device="cuda")
+    y = torch.empty((2, W.N), device="cuda")
+    stride = w.shape[1]
+    with pytest.raises(B.IQ4XSError) as e:
+        B.iq4xs_matmul_grouped(w, stride - 16, 2, W.N, W.K, qs, ds, off, y)
+    assert e.value.status == B.ERR_ARG
+    with pytest.raises(B.IQ4XSError) as e:
+        B.iq4xs_matmul_grouped(w, stride, 0, W.N, W.K, qs, ds, off, y)
+    assert e.value.status == B.ERR_SHAPE
