@@ -33,6 +33,39 @@ def iq4xs_weights(rng: np.random.Generator, N: int, K: int, d_scale: float) -> n
     return blocks.reshape(N, (K // QK) * BLOCK_BYTES)
 
 
+SUB = 32
+B18_BYTES = 18
+
+
+def block32_weights(rng: np.random.Generator, N: int, K: int, d_scale: float) -> np.ndarray:
+    """Random matrix of 18-byte, 32-weight blocks (the Q4_0 and IQ4_NL byte
+    shape: fp16 ``d`` at bytes 0-1 drawn as |N(0,1)| * scale, then 16 uniform
+    bytes of nibbles) as uint8 [N, K/32*18].  Stream order: the ``d`` normals,
+    then the nibble bytes, both in row-major block order."""
+    if K % SUB:
+        raise ValueError("K must be a multiple of 32")
+    nb = N * (K // SUB)
+    d = (np.abs(rng.standard_normal(nb)) * d_scale).astype(np.float16)
+    qs = rng.integers(0, 256, size=(nb, B18_BYTES - 2), dtype=np.uint8)
+    blocks = np.empty((nb, B18_BYTES), dtype=np.uint8)
+    blocks[:, 0:2] = d.view(np.uint8).reshape(nb, 2)
+    blocks[:, 2:] = qs
+    return blocks.reshape(N, (K // SUB) * B18_BYTES)
+
+
+# Weight formats by name: IQ4_XS (256-weight super-blocks of 136 bytes), Q4_0
+# and IQ4_NL (32-weight blocks of 18 bytes; the same bytes decode either way).
+WTYPES = {"iq4_xs": 0, "q4_0": 1, "iq4_nl": 2}
+
+
+def weights_for(wtype: int, rng: np.random.Generator, N: int, K: int,
+                d_scale: float) -> np.ndarray:
+    """Random weights in the byte shape of format ``wtype``."""
+    if wtype == 0:
+        return iq4xs_weights(rng, N, K, d_scale)
+    return block32_weights(rng, N, K, d_scale)
+
+
 def activations(rng: np.random.Generator, M: int, K: int, outlier_frac: float = 0.0,
                 outlier_scale: float = 20.0, bf16_round: bool = False) -> np.ndarray:
     """x fp32 [M, K] ~ N(0,1).  ``outlier_frac`` of the channels (chosen without

@@ -28,6 +28,11 @@ _lib = None
 QK = 256          # weights per IQ4_XS super-block
 BLOCK_BYTES = 136  # bytes per super-block
 SUB = 32          # weights per sub-block / per Q8_1 block
+B18_BYTES = 18    # bytes per 32-weight Q4_0 / IQ4_NL block
+
+# Weight formats: IQ4_XS (256-weight super-blocks), Q4_0 and IQ4_NL (32-weight
+# blocks of 18 bytes).
+WT_IQ4_XS, WT_Q4_0, WT_IQ4_NL = 0, 1, 2
 
 
 def compile_oracle(src: str = _SRC, out: str = _LIB, extra_flags=()) -> str:
@@ -73,6 +78,18 @@ def _bind(lib):
     lib.oracle_matmul.restype = c.c_int
     lib.oracle_subblock_dot.argtypes = [p, i64, p, i64, i64, i64, c.c_int]
     lib.oracle_subblock_dot.restype = c.c_int64
+    lib.oracle_b18_code.argtypes = [c.c_int, p, c.c_int]
+    lib.oracle_b18_code.restype = c.c_int
+    lib.oracle_b18_scale.argtypes = [p]
+    lib.oracle_b18_scale.restype = c.c_float
+    lib.oracle_row_bytes.argtypes = [c.c_int, i64]
+    lib.oracle_row_bytes.restype = c.c_int64
+    lib.oracle_decode_wt.argtypes = [c.c_int, p, i64, i64, p]
+    lib.oracle_decode_wt.restype = c.c_int
+    lib.oracle_dequantize_wt.argtypes = [c.c_int, p, i64, i64, p, p]
+    lib.oracle_dequantize_wt.restype = c.c_int
+    lib.oracle_matmul_wt.argtypes = [c.c_int, p, i64, i64, p, p, i64, p, c.c_int]
+    lib.oracle_matmul_wt.restype = c.c_int
     return lib
 
 
@@ -169,6 +186,54 @@ class Oracle:
         y = np.empty((M, N), dtype=np.float64)
         rc = self.lib.oracle_matmul(_ptr(w), N, K, _ptr(qs), _ptr(d_h), M, _ptr(y),
                                     int(nthreads))
+        if rc:
+            raise ValueError(f"oracle matmul failed: {rc}")
+        return y
+
+    # -- any weight format -------------------------------------------------
+    def row_bytes(self, wtype: int, K: int) -> int:
+        return self.lib.oracle_row_bytes(wtype, K)
+
+    def b18_code(self, wtype: int, block: np.ndarray, i: int) -> int:
+        block = np.ascontiguousarray(block, dtype=np.uint8)
+        return self.lib.oracle_b18_code(wtype, _ptr(block), i)
+
+    def b18_scale(self, block: np.ndarray) -> float:
+        block = np.ascontiguousarray(block, dtype=np.uint8)
+        return self.lib.oracle_b18_scale(_ptr(block))
+
+    def decode_wt(self, wtype: int, w: np.ndarray, N: int, K: int) -> np.ndarray:
+        w = np.ascontiguousarray(w, dtype=np.uint8)
+        assert w.size == N * self.row_bytes(wtype, K)
+        out = np.empty((N, K), dtype=np.float64)
+        rc = self.lib.oracle_decode_wt(wtype, _ptr(w), N, K, _ptr(out))
+        if rc:
+            raise ValueError(f"oracle decode failed: {rc}")
+        return out
+
+    def dequantize_wt(self, wtype: int, w: np.ndarray, N: int, K: int, bf16: bool = False):
+        w = np.ascontiguousarray(w, dtype=np.uint8)
+        assert w.size == N * self.row_bytes(wtype, K)
+        f32 = np.empty((N, K), dtype=np.float32)
+        b16 = np.empty((N, K), dtype=np.uint16) if bf16 else None
+        rc = self.lib.oracle_dequantize_wt(wtype, _ptr(w), N, K, _ptr(f32),
+                                           _ptr(b16) if bf16 else None)
+        if rc:
+            raise ValueError(f"oracle dequantize failed: {rc}")
+        return (f32, b16) if bf16 else f32
+
+    def matmul_wt(self, wtype: int, w: np.ndarray, N: int, K: int, qs: np.ndarray,
+                  d_h: np.ndarray, nthreads: int = 1) -> np.ndarray:
+        """y [M,N] fp64 for weights in format ``wtype``."""
+        w = np.ascontiguousarray(w, dtype=np.uint8)
+        assert w.size == N * self.row_bytes(wtype, K)
+        qs = np.ascontiguousarray(qs, dtype=np.int8)
+        d_h = np.ascontiguousarray(d_h, dtype=np.uint16)
+        M = qs.shape[0]
+        assert qs.shape == (M, K) and d_h.shape == (M, K // SUB)
+        y = np.empty((M, N), dtype=np.float64)
+        rc = self.lib.oracle_matmul_wt(wtype, _ptr(w), N, K, _ptr(qs), _ptr(d_h), M, _ptr(y),
+                                       int(nthreads))
         if rc:
             raise ValueError(f"oracle matmul failed: {rc}")
         return y

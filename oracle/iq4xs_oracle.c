@@ -337,3 +337,159 @@ int64_t oracle_subblock_dot(const uint8_t* w, int64_t K, const int8_t* qs, int64
     }
     return P;
 }
+
+/* ------------------------------------------------------------------------ */
+/* The 32-weight formats Q4_0 and IQ4_NL.                                    */
+/*                                                                           */
+/* V100TPS engine page, tile-geometry passage: one IQ4_XS sub-block is      */
+/* exactly one Q4_0 block -- 4 ints of packed nibbles, low nibbles are       */
+/* elements 0-15 and high nibbles 16-31 -- and the two formats differ only   */
+/* in the scale (one d per 32 weights for Q4_0, d*(ls-32) per sub-block for  */
+/* IQ4_XS) and in the value of a nibble (q-8 for Q4_0, kvalues_iq4nl for     */
+/* IQ4_XS).  IQ4_NL is the kvalues_iq4nl codebook on blocks of 32 weights    */
+/* in 18 bytes (forum page on the Qwen3.5 engine, the retracted TP claim:    */
+/* the (32, 18) block shape of IQ4_NL).  Both blocks are 18 bytes: d (fp16)  */
+/* at byte 0, then 16 bytes of nibbles (a reading: the pages give the sizes, */
+/* not the offsets).                                                          */
+/*   Q4_0:   w[i] = float(d) * (nib_i - 8)                                   */
+/*   IQ4_NL: w[i] = float(d) * kv[nib_i]                                      */
+/* with nib_i the low nibble of byte 2+i for i < 16, the high nibble of byte */
+/* 2+(i-16) otherwise.                                                       */
+/* ------------------------------------------------------------------------ */
+#define OR_WT_IQ4XS 0
+#define OR_WT_Q4_0  1
+#define OR_WT_IQ4NL 2
+#define OR_B18_BYTES 18
+#define OR_B18_OFF_QS 2
+
+/* Integer value of element i (0..31) of one 18-byte block. */
+int oracle_b18_code(int wtype, const uint8_t* block, int i) {
+    uint8_t byte = block[OR_B18_OFF_QS + (i % 16)];
+    int nib = (i < 16) ? (byte & 0x0F) : (byte >> 4);
+    return (wtype == OR_WT_Q4_0) ? nib - 8 : or_kvalues[nib];
+}
+
+/* fp32 scale of one 18-byte block: float(d). */
+float oracle_b18_scale(const uint8_t* block) {
+    return oracle_f16_to_f32((uint16_t)(block[0] | (block[1] << 8)));
+}
+
+/* Bytes of one weight row of K values in format wtype, or -1 if K does not
+ * fit the format's block (256 for IQ4_XS, 32 for the others). */
+int64_t oracle_row_bytes(int wtype, int64_t K) {
+    if (wtype == OR_WT_IQ4XS) return (K % OR_QK) ? -1 : (K / OR_QK) * OR_BLOCK_BYTES;
+    if (wtype == OR_WT_Q4_0 || wtype == OR_WT_IQ4NL)
+        return (K % OR_SUB) ? -1 : (K / OR_SUB) * OR_B18_BYTES;
+    return -1;
+}
+
+/* Code of element i and fp32 scale of 32-weight block c of row n. */
+static int or_wt_code(int wtype, const uint8_t* w, int64_t row_bytes, int64_t n, int64_t c,
+                      int i) {
+    if (wtype == OR_WT_IQ4XS) {
+        const uint8_t* blk = w + n * row_bytes + (c / OR_NSUB) * OR_BLOCK_BYTES;
+        return oracle_iq4xs_code(blk, (int)(c % OR_NSUB) * OR_SUB + i);
+    }
+    return oracle_b18_code(wtype, w + n * row_bytes + c * OR_B18_BYTES, i);
+}
+static float or_wt_scale(int wtype, const uint8_t* w, int64_t row_bytes, int64_t n, int64_t c) {
+    if (wtype == OR_WT_IQ4XS) {
+        const uint8_t* blk = w + n * row_bytes + (c / OR_NSUB) * OR_BLOCK_BYTES;
+        return oracle_iq4xs_subblock_scale(blk, (int)(c % OR_NSUB));
+    }
+    return oracle_b18_scale(w + n * row_bytes + c * OR_B18_BYTES);
+}
+
+/* Decode any format to doubles, out[n*K + k]. */
+int oracle_decode_wt(int wtype, const uint8_t* w, int64_t N, int64_t K, double* out) {
+    int64_t rb = oracle_row_bytes(wtype, K);
+    if (rb < 0) return -1;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t c = k / OR_SUB;
+            out[n * K + k] = (double)or_wt_scale(wtype, w, rb, n, c) *
+                             (double)or_wt_code(wtype, w, rb, n, c, (int)(k % OR_SUB));
+        }
+    return 0;
+}
+
+/* Dequantize any format to fp32 (exact) and, if out_bf16, to bfloat16 (RNE). */
+int oracle_dequantize_wt(int wtype, const uint8_t* w, int64_t N, int64_t K, float* out_f32,
+                         uint16_t* out_bf16) {
+    int64_t rb = oracle_row_bytes(wtype, K);
+    if (rb < 0) return -1;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t c = k / OR_SUB;
+            float v = or_wt_scale(wtype, w, rb, n, c) *
+                      (float)or_wt_code(wtype, w, rb, n, c, (int)(k % OR_SUB));
+            if (out_f32) out_f32[n * K + k] = v;
+            if (out_bf16) out_bf16[n * K + k] = oracle_f32_to_bf16(v);
+        }
+    return 0;
+}
+
+typedef struct {
+    int wtype;
+    const uint8_t* w;
+    int64_t row_bytes, N, K;
+    const int8_t* qs;
+    const uint16_t* d_h;
+    int64_t M;
+    double* y;
+    int64_t n0, n1;
+    int status;
+} or_wt_job;
+
+/* The same product as oracle_matmul, for any format: per 32-weight block an
+ * exact integer dot P, then S_w * d_x * P accumulated in fp64 in block order. */
+static void* or_matmul_wt_rows(void* arg) {
+    or_wt_job* job = (or_wt_job*)arg;
+    int64_t nblk = job->K / OR_SUB;
+    for (int64_t n = job->n0; n < job->n1; ++n) {
+        for (int64_t m = 0; m < job->M; ++m) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < nblk; ++c) {
+                int64_t P = 0;
+                for (int i = 0; i < OR_SUB; ++i)
+                    P += (int64_t)or_wt_code(job->wtype, job->w, job->row_bytes, n, c, i) *
+                         (int64_t)job->qs[m * job->K + c * OR_SUB + i];
+                if (P > 516128 || P < -516128) { job->status = -3; return NULL; }
+                double sw = (double)or_wt_scale(job->wtype, job->w, job->row_bytes, n, c);
+                double dx = (double)oracle_f16_to_f32(job->d_h[m * nblk + c]);
+                acc += sw * dx * (double)P;
+            }
+            job->y[m * job->N + n] = acc;
+        }
+    }
+    return NULL;
+}
+
+/* y[M][N] (double) for weights in format wtype; threads as oracle_matmul. */
+int oracle_matmul_wt(int wtype, const uint8_t* w, int64_t N, int64_t K, const int8_t* qs,
+                     const uint16_t* d_h, int64_t M, double* y, int nthreads) {
+    int64_t rb = oracle_row_bytes(wtype, K);
+    if (rb < 0 || N < 0 || M < 0) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > N && N > 0) nthreads = (int)N;
+    or_wt_job* jobs = (or_wt_job*)calloc((size_t)nthreads, sizeof(or_wt_job));
+    pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) { free(jobs); free(th); return -4; }
+    int status = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        or_wt_job j = {wtype, w, rb, N, K, qs, d_h, M, y,
+                       N * t / nthreads, N * (t + 1) / nthreads, 0};
+        jobs[t] = j;
+        if (nthreads == 1 || pthread_create(&th[t], NULL, or_matmul_wt_rows, &jobs[t]) != 0) {
+            or_matmul_wt_rows(&jobs[t]);
+            th[t] = 0;
+        }
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        if (th[t]) pthread_join(th[t], NULL);
+        if (jobs[t].status) status = jobs[t].status;
+    }
+    free(jobs);
+    free(th);
+    return status;
+}

@@ -325,4 +325,176 @@ def pin_int32_extreme(orc, kv):
     assert y[0, 0] == 8 * 516128 * dh
 
 
+# ---------------------------------------------------------------------------
+# The 32-weight formats Q4_0 (value (q-8)*d) and IQ4_NL (value kv[q]*d), in
+# 18-byte blocks (the layout reading: fp16 d at bytes 0-1, nibbles at 2-17;
+# element i < 16 is the low nibble of byte 2+i, element 16+i the high one).
+# ---------------------------------------------------------------------------
+WT_Q4_0, WT_IQ4_NL = 1, 2
+
+
+def make_b18(d: float, qs) -> np.ndarray:
+    b = np.zeros(18, np.uint8)
+    b[0:2] = np.frombuffer(np.float16(d).tobytes(), np.uint8)
+    b[2:] = np.asarray(qs, np.uint8)
+    return b
+
+
+def _nib_value(wtype, kv, nib):
+    return nib - 8 if wtype == WT_Q4_0 else kv[nib]
+
+
+def pin_b18_row_bytes(orc, kv):
+    assert orc.row_bytes(WT_Q4_0, 4096) == 4096 // 32 * 18
+    assert orc.row_bytes(WT_IQ4_NL, 96) == 3 * 18
+    assert orc.row_bytes(WT_Q4_0, 48) == -1
+    assert orc.row_bytes(0, 512) == 2 * 136 and orc.row_bytes(0, 96) == -1
+
+
+def pin_b18_nibble_positions(orc, kv):
+    """d = 1; one qs byte (b<<4)|a at position i and a fill byte elsewhere:
+    element i decodes to value(a), element 16+i to value(b), every other
+    element to the fill nibble's value; Q4_0's value is q-8 (nibble 8 is 0)."""
+    for wtype in (WT_Q4_0, WT_IQ4_NL):
+        for i in (0, 3, 15):
+            a, b = (5 + i) % 16, (12 + 3 * i) % 16
+            if a == b:
+                b = (b + 1) % 16
+            qs = np.full(16, 0x88, np.uint8)
+            qs[i] = (b << 4) | a
+            blk = make_b18(1.0, qs)
+            w = orc.decode_wt(wtype, blk.reshape(1, 18), 1, 32)[0]
+            exp = np.full(32, float(_nib_value(wtype, kv, 8)))
+            exp[i] = _nib_value(wtype, kv, a)
+            exp[16 + i] = _nib_value(wtype, kv, b)
+            assert np.array_equal(w, exp), (wtype, i)
+            for e in range(32):
+                assert orc.b18_code(wtype, blk, e) == exp[e]
+
+
+def pin_q4_0_values_span_minus8_to_7(orc, kv):
+    """Q4_0 nibbles 0..15 decode to -8..7 (the q-8 rule): the sixteen values
+    of one block hold each nibble once in the low and once in the high half."""
+    qs = (np.arange(16, dtype=np.uint8) | (np.arange(15, -1, -1, dtype=np.uint8) << 4))
+    w = orc.decode_wt(WT_Q4_0, make_b18(1.0, qs).reshape(1, 18), 1, 32)[0]
+    assert np.array_equal(w[:16], np.arange(-8, 8))
+    assert np.array_equal(w[16:], np.arange(7, -9, -1))
+
+
+def pin_b18_scale_is_d(orc, kv):
+    """The block scale is float(d) itself: subnormal, largest and ordinary d."""
+    for d in (2.0**-24, 65504.0, 0.375, 1e-3):
+        blk = make_b18(d, np.full(16, 0x99, np.uint8))  # nibble 9: Q4_0 1, IQ4_NL 13
+        assert orc.b18_scale(blk) == np.float32(np.float16(d))
+        w = orc.decode_wt(WT_Q4_0, blk.reshape(1, 18), 1, 32)[0]
+        assert np.all(w == float(np.float16(d)) * 1)
+        w = orc.decode_wt(WT_IQ4_NL, blk.reshape(1, 18), 1, 32)[0]
+        assert np.all(w == float(np.float32(np.float16(d)) * np.float32(kv[9])))
+
+
+def pin_iq4nl_equals_iq4xs_with_uniform_scale(orc, kv):
+    """An IQ4_XS super-block whose eight ls are all L holds the same weights
+    as eight IQ4_NL blocks with d' = d*(L-32) (chosen exact in fp16) and the
+    same 16 nibble bytes per sub-block: decode and product agree exactly."""
+    rng = np.random.default_rng(31)
+    N, K, M = 3, 512, 2
+    d, L = 0.0078125, 45              # d' = 2^-7 * 13, exact in fp16
+    xs_rows, nl_rows = [], []
+    for _ in range(N):
+        xs_blocks, nl_blocks = [], []
+        for _b in range(K // 256):
+            qs = rng.integers(0, 256, 128).astype(np.uint8)
+            xs_blocks.append(make_block(d, [L] * 8, qs))
+            nl_blocks += [make_b18(d * (L - 32), qs[16 * j:16 * j + 16]) for j in range(8)]
+        xs_rows.append(np.concatenate(xs_blocks))
+        nl_rows.append(np.concatenate(nl_blocks))
+    w_xs, w_nl = np.stack(xs_rows), np.stack(nl_rows)
+    assert np.array_equal(orc.decode_wt(WT_IQ4_NL, w_nl, N, K), orc.decode(w_xs, N, K))
+    x = synth_acts(rng, M, K)
+    qs_x, d_h, _ = orc.quantize_q8_1(x)
+    assert np.array_equal(orc.matmul_wt(WT_IQ4_NL, w_nl, N, K, qs_x, d_h),
+                          orc.matmul(w_xs, N, K, qs_x, d_h))
+    assert np.array_equal(orc.matmul_wt(0, w_xs, N, K, qs_x, d_h), orc.matmul(w_xs, N, K, qs_x, d_h))
+
+
+def synth_acts(rng, M, K):
+    return rng.standard_normal((M, K)).astype(np.float32)
+
+
+def pin_q4_0_integer_exact(orc, kv):
+    """d = 1 blocks and integer activations with a +-127 in every block of 32
+    (so every Q8_1 scale is 1): y is the exact integer product of the q-8
+    values and x (numpy int64 matmul)."""
+    rng = np.random.default_rng(32)
+    N, K, M = 4, 256, 3
+    nib = rng.integers(0, 16, (N, K // 32, 32))
+    rows = []
+    for n in range(N):
+        blocks = []
+        for c in range(K // 32):
+            qs = (nib[n, c, :16] | (nib[n, c, 16:] << 4)).astype(np.uint8)
+            blocks.append(make_b18(1.0, qs))
+        rows.append(np.concatenate(blocks))
+    w = np.stack(rows)
+    codes = (nib.reshape(N, K) - 8).astype(np.int64)
+    x = rng.integers(-126, 127, (M, K)).astype(np.int64)
+    x[:, 7::32] = 127 * rng.choice([-1, 1], (M, K // 32))
+    qs_x, d_h, _ = orc.quantize_q8_1(x.astype(np.float32))
+    assert np.array_equal(qs_x.astype(np.int64), x)
+    y = orc.matmul_wt(WT_Q4_0, w, N, K, qs_x, d_h)
+    assert np.array_equal(y, (x @ codes.T).astype(np.float64))
+
+
+def pin_q4_0_nibble8_is_zero(orc, kv):
+    """Every nibble 8 decodes to 0 under q-8, so the product is exactly 0."""
+    rng = np.random.default_rng(33)
+    w = np.stack([np.concatenate([make_b18(float(rng.uniform(0.01, 2)), np.full(16, 0x88))
+                                  for _ in range(8)]) for _ in range(2)])
+    x = synth_acts(rng, 2, 256)
+    qs_x, d_h, _ = orc.quantize_q8_1(x)
+    assert np.all(orc.matmul_wt(WT_Q4_0, w, 2, 256, qs_x, d_h) == 0.0)
+
+
+def pin_b18_bruteforce_fp64(orc, kv):
+    """Per-block integer dots scaled in fp64 equal the plain fp64
+    dequantize-then-matmul of the same W and dequantized activations; the
+    fp32 dequantization is exact and its bf16 form is torch's RNE of it."""
+    import torch
+    from iq4_xs_quantized_gb300 import synth
+    rng = np.random.default_rng(34)
+    N, K, M = 9, 512, 3
+    for wtype in (WT_Q4_0, WT_IQ4_NL):
+        w = synth.block32_weights(rng, N, K, 2e-3)
+        x = synth.activations(rng, M, K, outlier_frac=0.02)
+        qs_x, d_h, _ = orc.quantize_q8_1(x)
+        W = orc.decode_wt(wtype, w, N, K)
+        xhat = qs_x.astype(np.float64) * np.repeat(d_h.view(np.float16).astype(np.float64), 32, 1)
+        ref = xhat @ W.T
+        y = orc.matmul_wt(wtype, w, N, K, qs_x, d_h)
+        assert np.max(np.abs(y - ref)) <= 1e-12 * np.max(np.abs(ref))
+        assert np.array_equal(y, orc.matmul_wt(wtype, w, N, K, qs_x, d_h, nthreads=3))
+        f32, b16 = orc.dequantize_wt(wtype, w, N, K, bf16=True)
+        assert np.array_equal(f32.astype(np.float64), W)
+        ref16 = torch.from_numpy(f32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(b16, ref16)
+
+
+def pin_b18_single_activation(orc, kv):
+    """x with one nonzero v at column k: y[n] = half(|v|/127) * sign(v) * 127
+    * w[n, k], for both 32-weight formats."""
+    from iq4_xs_quantized_gb300 import synth
+    rng = np.random.default_rng(35)
+    for wtype in (WT_Q4_0, WT_IQ4_NL):
+        w = synth.block32_weights(rng, 5, 256, 2e-3)
+        W = orc.decode_wt(wtype, w, 5, 256)
+        for k in (0, 15, 16, 31, 32, 255):
+            v = np.float32(-3.5 if k % 2 else 0.75)
+            x = np.zeros((1, 256), np.float32)
+            x[0, k] = v
+            qs_x, d_h, _ = orc.quantize_q8_1(x)
+            dh = float(np.float16(np.float32(abs(v)) / np.float32(127)))
+            y = orc.matmul_wt(wtype, w, 5, 256, qs_x, d_h)
+            assert np.array_equal(y[0], dh * np.sign(v) * 127 * W[:, k]), (wtype, k)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
