@@ -89,6 +89,30 @@ typedef enum {
 } iq4xs_path;
 
 /*
+ * Weight formats (engine page, tile-geometry passage: an IQ4_XS 32-weight
+ * sub-block is exactly one Q4_0 block -- 16 bytes of nibbles, low nibbles =
+ * elements 0-15, high = 16-31 -- and the two differ only in the scale and in
+ * the nibble's value; forum page on the Qwen3.5 engine: IQ4_NL is the
+ * kvalues_iq4nl codebook on (32, 18) blocks).  Q4_0 and IQ4_NL share one
+ * byte shape, row-major [N][K/32] blocks of 18 bytes:
+ *      bytes 0-1   d    fp16, little endian
+ *      bytes 2-17  qs   u8[16]: element i (0..15) is the low nibble of byte
+ *                       2+i, element 16+i the high nibble
+ *      Q4_0:   weight = fp32(d) * (nibble - 8)
+ *      IQ4_NL: weight = fp32(d) * kvalues_iq4nl[nibble]
+ * Rows are K/32*18 bytes apart; K must be a multiple of 256 here as for
+ * IQ4_XS (rows are then 16-byte aligned), and W 16-byte aligned.
+ */
+typedef enum {
+    IQ4XS_WTYPE_IQ4_XS = 0,
+    IQ4XS_WTYPE_Q4_0 = 1,
+    IQ4XS_WTYPE_IQ4_NL = 2
+} iq4xs_wtype;
+
+/* Bytes of an [N][K] weight matrix in format wtype; 0 if invalid. */
+int64_t iq4xs_weight_bytes(int wtype, int64_t N, int64_t K);
+
+/*
  * Q8_1 activation quantization (engine page, kernel table at M=64: the
  * activations enter the batched matmul through quantize_q8_1).
  *   x           fp32 [M][ldx], ldx >= K, 4-byte aligned, ldx*4 % 16 == 0 and
@@ -126,6 +150,19 @@ int64_t iq4xs_tc_operand_bytes(int64_t M, int64_t K);
 int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds,
                  const void* tc_operand, int64_t M, float* y, int64_t ldy, int path,
                  int64_t stream);
+
+/*
+ * iq4xs_matmul for a weight in any iq4xs_wtype (IQ4XS_WTYPE_IQ4_XS is
+ * iq4xs_matmul itself).  Both paths run the same tiles for every format; only
+ * the decode differs (scale d per 18-byte block, nibble value q-8 or
+ * kvalues_iq4nl[q]), so the result is, as for IQ4_XS, fp32 accumulation of
+ * exact per-32-weight integer dots scaled by d_w * d_x.  The path choice
+ * (AUTO) is the one iq4xs_select_path makes for IQ4_XS.  IQ4XS_ERR_ARG for
+ * an unknown wtype.
+ */
+int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t* qs,
+                    const void* ds, const void* tc_operand, int64_t M, float* y, int64_t ldy,
+                    int path, int64_t stream);
 
 /*
  * Grouped (mixture-of-experts) matmul in one launch: G experts, each with its
@@ -214,6 +251,10 @@ int64_t iq4xs_linear_static_max_bytes(void);
  */
 int iq4xs_dequantize(const void* w, int64_t N, int64_t K, void* out, int out_dtype,
                      int64_t stream);
+
+/* iq4xs_dequantize for a weight in any iq4xs_wtype (exact fp32, or bf16 RNE). */
+int iq4xs_dequantize_wt(const void* w, int wtype, int64_t N, int64_t K, void* out,
+                        int out_dtype, int64_t stream);
 
 /*
  * Path choice for (M, N, K) (engine page, mmvq vs dequantize table: the

@@ -21,6 +21,8 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "iq4xs.h")
 OK, ERR_ARG, ERR_ALIGN, ERR_SHAPE, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT = range(7)
 PATH_AUTO, PATH_DP4A, PATH_TC, PATH_BASELINE = 0, 1, 2, 3
 PATHS = {"auto": PATH_AUTO, "dp4a": PATH_DP4A, "tc": PATH_TC}
+WTYPE_IQ4_XS, WTYPE_Q4_0, WTYPE_IQ4_NL = 0, 1, 2
+WTYPES = {"iq4_xs": WTYPE_IQ4_XS, "q4_0": WTYPE_Q4_0, "iq4_nl": WTYPE_IQ4_NL}
 
 _lock = threading.Lock()
 _lib = None
@@ -55,6 +57,10 @@ def load(path: str | None = None):
         lib.iq4xs_tc_operand_bytes.restype = i64
         lib.iq4xs_matmul.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, i64, ci, i64]
         lib.iq4xs_dequantize.argtypes = [vp, i64, i64, vp, ci, i64]
+        lib.iq4xs_matmul_wt.argtypes = [vp, ci, i64, i64, vp, vp, vp, i64, vp, i64, ci, i64]
+        lib.iq4xs_dequantize_wt.argtypes = [vp, ci, i64, i64, vp, ci, i64]
+        lib.iq4xs_weight_bytes.argtypes = [ci, i64, i64]
+        lib.iq4xs_weight_bytes.restype = i64
         lib.iq4xs_matmul_grouped.argtypes = [vp, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, i64]
         lib.iq4xs_linear.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, i64]
         lib.iq4xs_linear_workspace_bytes.argtypes = [i64, i64, i64]
@@ -72,7 +78,7 @@ def load(path: str | None = None):
         lib.iq4xs_status_string.argtypes = [ci]
         lib.iq4xs_status_string.restype = ctypes.c_char_p
         for name in ("iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_matmul_grouped",
-                     "iq4xs_dequantize", "iq4xs_linear",
+                     "iq4xs_dequantize", "iq4xs_linear", "iq4xs_matmul_wt", "iq4xs_dequantize_wt",
                      "iq4xs_select_path", "iq4xs_set_crossover", "iq4xs_set_baseline_threshold",
                      "iq4xs_last_device_error"):
             getattr(lib, name).restype = ci
@@ -137,6 +143,25 @@ def iq4xs_matmul(w, N: int, K: int, qs, ds, tc_operand, M: int, y, path=PATH_AUT
     _check("iq4xs_matmul", rc)
 
 
+def _wtype(wtype) -> int:
+    return WTYPES[wtype] if isinstance(wtype, str) else int(wtype)
+
+
+def iq4xs_weight_bytes(wtype, N: int, K: int) -> int:
+    return int(load().iq4xs_weight_bytes(_wtype(wtype), N, K))
+
+
+def iq4xs_matmul_wt(w, wtype, N: int, K: int, qs, ds, tc_operand, M: int, y, path=PATH_AUTO,
+                    stream=None) -> None:
+    """iq4xs_matmul for weights in format ``wtype`` (WTYPE_* or its name)."""
+    if isinstance(path, str):
+        path = PATHS[path]
+    rc = load().iq4xs_matmul_wt(_ptr(w), _wtype(wtype), N, K, _ptr(qs), _ptr(ds),
+                                _ptr(tc_operand), M, _ptr(y), y.stride(0), int(path),
+                                _stream(stream))
+    _check("iq4xs_matmul_wt", rc)
+
+
 def iq4xs_linear_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(load().iq4xs_linear_workspace_bytes(M, N, K))
 
@@ -183,6 +208,13 @@ def iq4xs_dequantize(w, N: int, K: int, out, stream=None) -> None:
     dt = {torch.float32: 0, torch.bfloat16: 1}[out.dtype]
     rc = load().iq4xs_dequantize(_ptr(w), N, K, _ptr(out), dt, _stream(stream))
     _check("iq4xs_dequantize", rc)
+
+
+def iq4xs_dequantize_wt(w, wtype, N: int, K: int, out, stream=None) -> None:
+    """Weights in format ``wtype`` -> dense [N, K] (float32 exact, or bfloat16 RNE)."""
+    dt = {torch.float32: 0, torch.bfloat16: 1}[out.dtype]
+    rc = load().iq4xs_dequantize_wt(_ptr(w), _wtype(wtype), N, K, _ptr(out), dt, _stream(stream))
+    _check("iq4xs_dequantize_wt", rc)
 
 
 def iq4xs_select_path(M: int, N: int, K: int) -> int:

@@ -117,10 +117,24 @@ int iq4xs_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx, int8_
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int64_t iq4xs_weight_bytes(int wtype, int64_t N, int64_t K) {
+    if (wtype < IQ4XS_WTYPE_IQ4_XS || wtype > IQ4XS_WTYPE_IQ4_NL) return 0;
+    if (N < 1 || N > (1 << 30) || K <= 0 || K % kQK || K > (1 << 30)) return 0;
+    return N * wt_row_bytes(wtype, K);
+}
+
 int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds,
                  const void* tc_operand, int64_t M, float* y, int64_t ldy, int path,
                  int64_t stream) {
+    return iq4xs_matmul_wt(w, IQ4XS_WTYPE_IQ4_XS, N, K, qs, ds, tc_operand, M, y, ldy, path,
+                           stream);
+}
+
+int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t* qs,
+                    const void* ds, const void* tc_operand, int64_t M, float* y, int64_t ldy,
+                    int path, int64_t stream) {
     if (!w || !y) return IQ4XS_ERR_ARG;
+    if (wtype < IQ4XS_WTYPE_IQ4_XS || wtype > IQ4XS_WTYPE_IQ4_NL) return IQ4XS_ERR_ARG;
     if (path < IQ4XS_PATH_AUTO || path > IQ4XS_PATH_TC) return IQ4XS_ERR_ARG;
     if (M < 1 || M > kMaxM || N < 1 || N > (1 << 30) || K <= 0 || K % kQK || K > (1 << 30))
         return IQ4XS_ERR_SHAPE;
@@ -140,9 +154,9 @@ int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const vo
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (path == IQ4XS_PATH_TC)
-        return from_cuda(launch_matmul_tc(w, N, K, tc_operand, M, y, ldy, st->encode, st->err,
-                                          st->num_sms, s));
-    return from_cuda(launch_matmul_dp4a(w, N, K, qs, ds, M, y, ldy, s));
+        return from_cuda(launch_matmul_tc(w, wtype, N, K, tc_operand, M, y, ldy, st->encode,
+                                          st->err, st->num_sms, s));
+    return from_cuda(launch_matmul_dp4a(w, wtype, N, K, qs, ds, M, y, ldy, s));
 }
 
 namespace {
@@ -206,14 +220,21 @@ int iq4xs_matmul_grouped(const void* w, int64_t expert_stride, int64_t G, int64_
 
 int iq4xs_dequantize(const void* w, int64_t N, int64_t K, void* out, int out_dtype,
                      int64_t stream) {
+    return iq4xs_dequantize_wt(w, IQ4XS_WTYPE_IQ4_XS, N, K, out, out_dtype, stream);
+}
+
+int iq4xs_dequantize_wt(const void* w, int wtype, int64_t N, int64_t K, void* out,
+                        int out_dtype, int64_t stream) {
     if (!w || !out) return IQ4XS_ERR_ARG;
+    if (wtype < IQ4XS_WTYPE_IQ4_XS || wtype > IQ4XS_WTYPE_IQ4_NL) return IQ4XS_ERR_ARG;
     if (out_dtype != 0 && out_dtype != 1) return IQ4XS_ERR_ARG;
     if (N < 1 || K <= 0 || K % kQK) return IQ4XS_ERR_SHAPE;
     if (!aligned(w, 16) || !aligned(out, 16)) return IQ4XS_ERR_ALIGN;
     DevState* st;
     int rc = device_state(&st);
     if (rc) return rc;
-    return from_cuda(launch_dequantize(w, N, K, out, out_dtype, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_dequantize(w, wtype, N, K, out, out_dtype,
+                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int iq4xs_select_path(int64_t M, int64_t N, int64_t K, int* path_out) {

@@ -1,7 +1,9 @@
-// dequantize.cu -- IQ4_XS -> dense fp32 / bfloat16 (V100TPS engine page,
-// kernel table at M=64: dequantize_block_iq4_xs writing the whole weight
-// before a dense GEMM -- the baseline path the batched kernel replaces).
-// weight = fp32(d) * (ls - 32) * kvalues_iq4nl[nibble], exact in fp32.
+// dequantize.cu -- IQ4_XS / Q4_0 / IQ4_NL -> dense fp32 / bfloat16
+// (V100TPS engine page, kernel table at M=64: dequantize_block_iq4_xs
+// writing the whole weight before a dense GEMM -- the baseline path the
+// batched kernel replaces).  weight = sub-block scale * nibble value, exact
+// in fp32: IQ4_XS fp32(d) * (ls - 32) * kvalues_iq4nl[q]; Q4_0 fp32(d) * (q - 8);
+// IQ4_NL fp32(d) * kvalues_iq4nl[q].
 #include <cuda_bf16.h>
 
 #include "internal.cuh"
@@ -12,7 +14,7 @@ namespace {
 constexpr int kDqThreads = 256;
 
 // One thread per (row n, sub-block s): 32 outputs, written contiguously.
-template <bool kBf16>
+template <bool kBf16, int WT>
 __global__ void __launch_bounds__(kDqThreads)
     dequantize_kernel(const uint8_t* __restrict__ w, int64_t N, int64_t K, void* __restrict__ out) {
     const int64_t nsub = K / kSub;
@@ -20,18 +22,14 @@ __global__ void __launch_bounds__(kDqThreads)
     if (idx >= N * nsub) return;
     const int64_t n = idx / nsub;
     const int64_t s = idx % nsub;
-    const int j = (int)(s % kSubPerBlock);
-    const uint8_t* blk = w + (n * (K / kQK) + s / kSubPerBlock) * kBlockBytes;
-    const uint2 hdr = __ldg(reinterpret_cast<const uint2*>(blk));  // 8-byte aligned
-    const uint2 q01 = __ldg(reinterpret_cast<const uint2*>(blk + 8 + 16 * j));
-    const uint2 q23 = __ldg(reinterpret_cast<const uint2*>(blk + 16 + 16 * j));
-    const float S = iq4xs_scale(hdr.x, hdr.y, j);
-    const uint32_t words[4] = {q01.x, q01.y, q23.x, q23.y};
+    uint32_t raw[6], words[4];
+    wt_load_sub<WT>(w + n * wt_row_bytes(WT, K), s, raw);
+    const float S = wt_unpack_sub<WT>(raw, s, words);
     float v[32];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         uint32_t lo4, hi4;
-        decode_s8(words[c], lo4, hi4);
+        decode_s8<WT>(words[c], lo4, hi4);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             v[4 * c + k] = S * (float)(int8_t)(lo4 >> (8 * k));
@@ -55,18 +53,28 @@ __global__ void __launch_bounds__(kDqThreads)
     }
 }
 
+template <int WT>
+void launch_dq(const uint8_t* w, int64_t N, int64_t K, void* out, int out_dtype, unsigned grid,
+               cudaStream_t stream) {
+    if (out_dtype == 1)
+        dequantize_kernel<true, WT><<<grid, kDqThreads, 0, stream>>>(w, N, K, out);
+    else
+        dequantize_kernel<false, WT><<<grid, kDqThreads, 0, stream>>>(w, N, K, out);
+}
+
 }  // namespace
 
-cudaError_t launch_dequantize(const void* w, int64_t N, int64_t K, void* out, int out_dtype,
-                              cudaStream_t stream) {
+cudaError_t launch_dequantize(const void* w, int wt, int64_t N, int64_t K, void* out,
+                              int out_dtype, cudaStream_t stream) {
     const int64_t total = N * (K / kSub);
     const unsigned grid = (unsigned)((total + kDqThreads - 1) / kDqThreads);
-    if (out_dtype == 1)
-        dequantize_kernel<true><<<grid, kDqThreads, 0, stream>>>(
-            reinterpret_cast<const uint8_t*>(w), N, K, out);
-    else
-        dequantize_kernel<false><<<grid, kDqThreads, 0, stream>>>(
-            reinterpret_cast<const uint8_t*>(w), N, K, out);
+    const uint8_t* wb = reinterpret_cast<const uint8_t*>(w);
+    switch (wt) {
+        case kWtIQ4XS: launch_dq<kWtIQ4XS>(wb, N, K, out, out_dtype, grid, stream); break;
+        case kWtQ4_0: launch_dq<kWtQ4_0>(wb, N, K, out, out_dtype, grid, stream); break;
+        case kWtIQ4NL: launch_dq<kWtIQ4NL>(wb, N, K, out, out_dtype, grid, stream); break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

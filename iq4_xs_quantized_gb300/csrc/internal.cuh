@@ -42,6 +42,30 @@ static_assert(kSubPerBlock * kQsBytesPerSub == sizeof(((BlockIQ4XS*)0)->qs), "8 
 
 constexpr int kQ8Max = 127;  // Q8_1 codes lie in [-127, 127]
 
+// ---------------------------------------------------------------------------
+// Weight formats.  The same engine page's tile-geometry passage: an IQ4_XS
+// sub-block is exactly one Q4_0 block (16 bytes of nibbles, low nibbles
+// elements 0-15, high nibbles 16-31); only the scale (one fp16 d per 32
+// weights for Q4_0, d*(ls-32) for IQ4_XS) and the nibble's value (q-8 for
+// Q4_0, kvalues_iq4nl for IQ4_XS) differ.  IQ4_NL is kvalues_iq4nl on
+// 32-weight blocks of 18 bytes (forum page on the Qwen3.5 engine: the
+// (32, 18) block shape).  Q4_0 and IQ4_NL share one byte shape: fp16 d at
+// byte 0, nibbles at bytes 2..17.  Every format's row is a whole number of
+// 256-weight groups here (136 or 8 x 18 = 144 bytes), so rows stay 16-byte
+// aligned and a 32-weight block starts 2 bytes past a 4-byte boundary
+// exactly when its index is odd.
+// ---------------------------------------------------------------------------
+enum WType : int { kWtIQ4XS = 0, kWtQ4_0 = 1, kWtIQ4NL = 2 };
+constexpr int kB18Bytes = 18;                      // one Q4_0 / IQ4_NL block
+constexpr int kB18GroupBytes = kSubPerBlock * kB18Bytes;  // 144 per 256 weights
+static_assert(kB18GroupBytes % 16 == 0, "256-weight groups of 18-byte blocks keep rows 16-byte aligned");
+__host__ __device__ constexpr int wt_group_bytes(int wt) {
+    return wt == kWtIQ4XS ? kBlockBytes : kB18GroupBytes;
+}
+__host__ __device__ inline int64_t wt_row_bytes(int wt, int64_t K) {
+    return (K / kQK) * wt_group_bytes(wt);
+}
+
 // kvalues_iq4nl packed four entries per word, little endian (entry 4w+k in
 // byte k of word w).  Two forms: the int8 values themselves, and u = kv + 128
 // (all of 1..241 fit one unsigned byte) for building exact fp16 operands.
@@ -49,9 +73,32 @@ constexpr uint32_t kKvS8_0 = 0xBFAD9881u, kKvS8_1 = 0xF6EADDCFu, kKvS8_2 = 0x261
                    kKvS8_3 = 0x71594535u;
 constexpr uint32_t kKvU8_0 = 0x3F2D1801u, kKvU8_1 = 0x766A5D4Fu, kKvU8_2 = 0xA6998D81u,
                    kKvU8_3 = 0xF1D9C5B5u;
-// fp16 with bit pattern 0x64XX is 1024 + XX; 1024 + u - 1152 = kv exactly.
+// Q4_0's nibble values q-8, in the same two forms (int8; u = q-8+128).
+__host__ __device__ constexpr uint32_t q4_0_word(int w, int bias) {
+    return (uint32_t)((4 * w + 0 - 8 + bias) & 0xFF) | ((uint32_t)((4 * w + 1 - 8 + bias) & 0xFF) << 8) |
+           ((uint32_t)((4 * w + 2 - 8 + bias) & 0xFF) << 16) | ((uint32_t)((4 * w + 3 - 8 + bias) & 0xFF) << 24);
+}
+// fp16 with bit pattern 0x64XX is 1024 + XX; 1024 + u - 1152 = value exactly.
 constexpr uint32_t kF16HiByte = 0x64646464u;
 constexpr uint32_t kF16Offset2 = 0x64806480u;  // half2(1152, 1152)
+
+// Nibble-value tables of a format: T8 the int8 values, TU the u = value+128 bytes.
+template <int WT>
+struct WTables {
+    static constexpr uint32_t S0 = kKvS8_0, S1 = kKvS8_1, S2 = kKvS8_2, S3 = kKvS8_3;
+    static constexpr uint32_t U0 = kKvU8_0, U1 = kKvU8_1, U2 = kKvU8_2, U3 = kKvU8_3;
+};
+template <>
+struct WTables<kWtQ4_0> {
+    static constexpr uint32_t S0 = q4_0_word(0, 0), S1 = q4_0_word(1, 0), S2 = q4_0_word(2, 0),
+                              S3 = q4_0_word(3, 0);
+    static constexpr uint32_t U0 = q4_0_word(0, 128), U1 = q4_0_word(1, 128),
+                              U2 = q4_0_word(2, 128), U3 = q4_0_word(3, 128);
+};
+static_assert(WTables<kWtQ4_0>::S0 == 0xFBFAF9F8u && WTables<kWtQ4_0>::S3 == 0x07060504u,
+              "Q4_0 values -8..7 as int8");
+static_assert(WTables<kWtQ4_0>::U0 == 0x7B7A7978u && WTables<kWtQ4_0>::U3 == 0x87868584u,
+              "Q4_0 values + 128");
 
 // ---------------------------------------------------------------------------
 // Tensor-core path geometry.
@@ -61,7 +108,6 @@ constexpr int kPairBlocks = 2;                    // super-blocks per W stage
 constexpr int kPairK = kPairBlocks * kQK;         // 512
 constexpr int kPairBytes = kPairBlocks * kBlockBytes;  // 272 = 17 x 16: TMA rows stay 16-byte aligned
 constexpr int kSubPerPair = kPairK / kSub;        // 16
-constexpr int kWStageBytes = kTileN * kPairBytes; // 34816
 static_assert(kPairBytes % 16 == 0, "a W stage row must be a whole number of 16-byte units");
 static_assert(kPairBytes / 4 <= 256, "TMA box inner extent (uint32 elements) <= 256");
 constexpr int kChunkElems = 8;                    // fp16 per 16-byte core-matrix row
@@ -147,20 +193,24 @@ __device__ __forceinline__ void lut16(uint32_t w, const uint32_t T0, const uint3
     t1 = prmt(prmt(T0, T1, sel_hi), prmt(T2, T3, sel_hi), pick >> 16);
 }
 
-// qs word -> int8x4 codebook values of elements i..i+3 (low nibbles) and
-// 16+i..16+i+3 (high nibbles).
+// qs word -> int8x4 nibble values of elements i..i+3 (low nibbles) and
+// 16+i..16+i+3 (high nibbles), through format WT's table.
+template <int WT = kWtIQ4XS>
 __device__ __forceinline__ void decode_s8(uint32_t w, uint32_t& lo4, uint32_t& hi4) {
+    using T = WTables<WT>;
     uint32_t t0, t1;
-    lut16(w, kKvS8_0, kKvS8_1, kKvS8_2, kKvS8_3, t0, t1);
+    lut16(w, T::S0, T::S1, T::S2, T::S3, t0, t1);
     lo4 = prmt(t0, t1, 0x6420u);
     hi4 = prmt(t0, t1, 0x7531u);
 }
 
 // qs word (bytes k = 0..3 of sub-block element i = i0 + k) -> four fp16x2
-// words (kv[L_k], kv[H_k]): the K-permuted order (element i, element 16+i).
+// words (value[L_k], value[H_k]): the K-permuted order (element i, 16+i).
+template <int WT = kWtIQ4XS>
 __device__ __forceinline__ void decode_f16x2(uint32_t w, uint32_t out[4]) {
+    using T = WTables<WT>;
     uint32_t t0, t1;
-    lut16(w, kKvU8_0, kKvU8_1, kKvU8_2, kKvU8_3, t0, t1);
+    lut16(w, T::U0, T::U1, T::U2, T::U3, t0, t1);
     const uint32_t h[4] = {prmt(t0, kF16HiByte, 0x4140u), prmt(t0, kF16HiByte, 0x4342u),
                            prmt(t1, kF16HiByte, 0x4140u), prmt(t1, kF16HiByte, 0x4342u)};
     const uint32_t off_bits = kF16Offset2;
@@ -182,6 +232,50 @@ __device__ __forceinline__ int iq4xs_ls(uint32_t hdr0, uint32_t hdr1, int j) {
 __device__ __forceinline__ float iq4xs_scale(uint32_t hdr0, uint32_t hdr1, int j) {
     const float d = __half2float(__ushort_as_half((unsigned short)(hdr0 & 0xFFFF)));
     return d * (float)(iq4xs_ls(hdr0, hdr1, j) - 32);
+}
+
+// One 18-byte block from the five 4-byte words starting at the block's
+// address rounded down to 4 (raw[0..4]); `odd` = the block starts 2 bytes
+// past that boundary.  Out: float(d) and the four words of nibbles.
+__device__ __forceinline__ float b18_unpack(const uint32_t raw[5], bool odd, uint32_t q[4]) {
+    const uint32_t sh = odd ? 16u : 0u;
+    const uint32_t d16 = __funnelshift_rc(raw[0], raw[1], sh) & 0xFFFFu;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) q[k] = __funnelshift_rc(raw[k], raw[k + 1], 16u + sh);
+    return __half2float(__ushort_as_half((unsigned short)d16));
+}
+
+// Sub-block s (32 weights) of a weight row in format WT, loaded from global
+// memory into six raw words (all loads in flight before any use), then
+// unpacked into its fp32 scale and its four words of nibbles.
+template <int WT>
+__device__ __forceinline__ void wt_load_sub(const uint8_t* row, int64_t s, uint32_t raw[6]) {
+    if constexpr (WT == kWtIQ4XS) {
+        const uint8_t* blk = row + (s / kSubPerBlock) * kBlockBytes;
+        const int j = (int)(s % kSubPerBlock);
+        const uint2 hdr = __ldg(reinterpret_cast<const uint2*>(blk));
+        const uint2 q01 = __ldg(reinterpret_cast<const uint2*>(blk + 8 + 16 * j));
+        const uint2 q23 = __ldg(reinterpret_cast<const uint2*>(blk + 16 + 16 * j));
+        raw[0] = hdr.x; raw[1] = hdr.y; raw[2] = q01.x; raw[3] = q01.y; raw[4] = q23.x; raw[5] = q23.y;
+    } else {
+        // block s at 18*s; its 4-byte-aligned start is 18*s - 2*(s & 1).  The
+        // five words end at most 2 bytes past the block, inside the next
+        // block of the row (the row's last block, s odd, ends exactly).
+        const uint32_t* a = reinterpret_cast<const uint32_t*>(row + kB18Bytes * s - 2 * (s & 1));
+#pragma unroll
+        for (int k = 0; k < 5; ++k) raw[k] = __ldg(a + k);
+        raw[5] = 0;
+    }
+}
+template <int WT>
+__device__ __forceinline__ float wt_unpack_sub(const uint32_t raw[6], int64_t s, uint32_t q[4]) {
+    if constexpr (WT == kWtIQ4XS) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) q[k] = raw[2 + k];
+        return iq4xs_scale(raw[0], raw[1], (int)(s % kSubPerBlock));
+    } else {
+        return b18_unpack(raw, (s & 1) != 0, q);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -568,9 +662,9 @@ struct DevCtx;  // per-device state kept by api.cu
 
 cudaError_t launch_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs,
                                  void* ds, void* tc_operand, cudaStream_t stream);
-cudaError_t launch_dequantize(const void* w, int64_t N, int64_t K, void* out, int out_dtype,
-                              cudaStream_t stream);
-cudaError_t launch_matmul_dp4a(const void* w, int64_t N, int64_t K, const int8_t* qs,
+cudaError_t launch_dequantize(const void* w, int wt, int64_t N, int64_t K, void* out,
+                              int out_dtype, cudaStream_t stream);
+cudaError_t launch_matmul_dp4a(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,
                                const void* ds, int64_t M, float* y, int64_t ldy,
                                cudaStream_t stream);
 // G experts in one launch: expert g has W at w + g * expert_stride and the
@@ -582,7 +676,7 @@ cudaError_t launch_matmul_dp4a_grouped(const void* w, int64_t expert_stride, int
 // Programmatic dependent launch on (default) or off for every launch.
 bool pdl_enabled();
 // `encode` is the driver's cuTensorMapEncodeTiled; `err` the device error word.
-cudaError_t launch_matmul_tc(const void* w, int64_t N, int64_t K, const void* tc_operand,
+cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const void* tc_operand,
                              int64_t M, float* y, int64_t ldy, void* encode, int* err,
                              int num_sms, cudaStream_t stream);
 

@@ -28,17 +28,17 @@ __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
     return __dp4a((int)a, (int)b, c);
 }
 
-// Rows [0, M) of x against the warp's kRows weight rows n0.. of W, MC
-// activation rows per pass.  `waited`: the wait for the preceding grid (which
-// wrote the activations) has been done already.
-template <int MC>
+// Rows [0, M) of x against the warp's kRows weight rows n0.. of W (format
+// WT), MC activation rows per pass.  `waited`: the wait for the preceding
+// grid (which wrote the activations) has been done already.
+template <int MC, int WT>
 __device__ __forceinline__ void dp4a_rows(const uint8_t* __restrict__ w, int64_t N, int64_t K,
                                           const int8_t* __restrict__ qs,
                                           const __half2* __restrict__ ds, int64_t M,
                                           float* __restrict__ y, int64_t ldy, int64_t n0, int lane,
                                           bool waited) {
     const int64_t nsub = K / kSub;
-    const int64_t row_bytes = (K / kQK) * kBlockBytes;
+    const int64_t row_bytes = wt_row_bytes(WT, K);
     constexpr int kIters = iters_for<MC>();
     for (int64_t m0 = 0; m0 < M; m0 += MC) {
         float acc[kRows][MC];
@@ -49,20 +49,17 @@ __device__ __forceinline__ void dp4a_rows(const uint8_t* __restrict__ w, int64_t
 
         for (int64_t sb = 0; sb < nsub; sb += 32 * kIters) {
             // Weight bytes (read-only model state) for kIters steps, all in flight.
-            uint2 hdr[kIters][kRows], q01[kIters][kRows], q23[kIters][kRows];
+            uint32_t raw[kIters][kRows][6];
 #pragma unroll
             for (int it = 0; it < kIters; ++it) {
                 const int64_t s = sb + lane + 32 * it;
-                const int j = (int)(s % kSubPerBlock);
 #pragma unroll
                 for (int r = 0; r < kRows; ++r) {
                     if (s < nsub && n0 + r < N) {
-                        const uint8_t* blk = w + (n0 + r) * row_bytes + (s / kSubPerBlock) * kBlockBytes;
-                        hdr[it][r] = __ldg(reinterpret_cast<const uint2*>(blk));
-                        q01[it][r] = __ldg(reinterpret_cast<const uint2*>(blk + 8 + 16 * j));
-                        q23[it][r] = __ldg(reinterpret_cast<const uint2*>(blk + 16 + 16 * j));
+                        wt_load_sub<WT>(w + (n0 + r) * row_bytes, s, raw[it][r]);
                     } else {
-                        hdr[it][r] = q01[it][r] = q23[it][r] = make_uint2(0, 0);
+#pragma unroll
+                        for (int k = 0; k < 6; ++k) raw[it][r][k] = 0;
                     }
                 }
             }
@@ -103,15 +100,13 @@ __device__ __forceinline__ void dp4a_rows(const uint8_t* __restrict__ w, int64_t
                 if (kPre != kIters) load_act(it, qpre[0], dpre[0]);
                 const uint4 (&qa)[MC][2] = qpre[pi];
                 const float (&dx)[MC] = dpre[pi];
-                const int j = (int)(s % kSubPerBlock);
 #pragma unroll
                 for (int r = 0; r < kRows; ++r) {
-                    const float S = iq4xs_scale(hdr[it][r].x, hdr[it][r].y, j);
+                    uint32_t q[4];
+                    const float S = wt_unpack_sub<WT>(raw[it][r], s, q);
                     uint32_t lo[4], hi[4];
-                    decode_s8(q01[it][r].x, lo[0], hi[0]);
-                    decode_s8(q01[it][r].y, lo[1], hi[1]);
-                    decode_s8(q23[it][r].x, lo[2], hi[2]);
-                    decode_s8(q23[it][r].y, lo[3], hi[3]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) decode_s8<WT>(q[c], lo[c], hi[c]);
 #pragma unroll
                     for (int mi = 0; mi < MC; ++mi) {
                         // elements 4c..4c+3 <-> code word c; elements 16+4c.. <-> word 4+c
@@ -147,7 +142,7 @@ __device__ __forceinline__ void dp4a_rows(const uint8_t* __restrict__ w, int64_t
     }
 }
 
-template <int MC>  // activation rows per pass
+template <int MC, int WT>  // activation rows per pass, weight format
 __global__ void __launch_bounds__(kDp4aThreads, 2)
     matmul_dp4a_kernel(const uint8_t* __restrict__ w, int64_t N, int64_t K,
                        const int8_t* __restrict__ qs, const __half2* __restrict__ ds, int64_t M,
@@ -156,7 +151,7 @@ __global__ void __launch_bounds__(kDp4aThreads, 2)
     const int lane = threadIdx.x & 31;
     const int64_t n0 = ((int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)) * kRows;
     if (n0 >= N) return;  // whole warp
-    dp4a_rows<MC>(w, N, K, qs, ds, M, y, ldy, n0, lane, false);
+    dp4a_rows<MC, WT>(w, N, K, qs, ds, M, y, ldy, n0, lane, false);
 }
 
 // Grouped (mixture-of-experts) form: G experts, expert g with its own W at
@@ -205,10 +200,10 @@ __global__ void __launch_bounds__(kDp4aThreads, 2)
     qs += r0 * K;
     ds += r0 * (K / kSub);
     y += r0 * ldy;
-    if (M == 1) dp4a_rows<1>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
-    else if (M == 2) dp4a_rows<2>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
-    else if (M <= 4) dp4a_rows<4>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
-    else dp4a_rows<8>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+    if (M == 1) dp4a_rows<1, kWtIQ4XS>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+    else if (M == 2) dp4a_rows<2, kWtIQ4XS>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+    else if (M <= 4) dp4a_rows<4, kWtIQ4XS>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+    else dp4a_rows<8, kWtIQ4XS>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
 }
 
 cudaLaunchConfig_t dp4a_config(int64_t N, unsigned slots, cudaStream_t stream,
@@ -225,26 +220,37 @@ cudaLaunchConfig_t dp4a_config(int64_t N, unsigned slots, cudaStream_t stream,
     return cfg;
 }
 
-template <int MC>
+template <int MC, int WT>
 cudaError_t launch_mc(const uint8_t* w, int64_t N, int64_t K, const int8_t* qs, const __half2* ds,
                       int64_t M, float* y, int64_t ldy, cudaStream_t stream) {
     static_assert(kRows * MC <= 32, "one output per lane");
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = dp4a_config(N, 1, stream, attr);
-    return cudaLaunchKernelEx(&cfg, matmul_dp4a_kernel<MC>, w, N, K, qs, ds, M, y, ldy);
+    return cudaLaunchKernelEx(&cfg, matmul_dp4a_kernel<MC, WT>, w, N, K, qs, ds, M, y, ldy);
+}
+
+template <int WT>
+cudaError_t launch_wt(const uint8_t* w, int64_t N, int64_t K, const int8_t* qs, const __half2* ds,
+                      int64_t M, float* y, int64_t ldy, cudaStream_t stream) {
+    if (M == 1) return launch_mc<1, WT>(w, N, K, qs, ds, M, y, ldy, stream);
+    if (M == 2) return launch_mc<2, WT>(w, N, K, qs, ds, M, y, ldy, stream);
+    if (M <= 4) return launch_mc<4, WT>(w, N, K, qs, ds, M, y, ldy, stream);
+    return launch_mc<8, WT>(w, N, K, qs, ds, M, y, ldy, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_matmul_dp4a(const void* w, int64_t N, int64_t K, const int8_t* qs,
+cudaError_t launch_matmul_dp4a(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,
                                const void* ds, int64_t M, float* y, int64_t ldy,
                                cudaStream_t stream) {
     const uint8_t* wb = reinterpret_cast<const uint8_t*>(w);
     const __half2* d2 = reinterpret_cast<const __half2*>(ds);
-    if (M == 1) return launch_mc<1>(wb, N, K, qs, d2, M, y, ldy, stream);
-    if (M == 2) return launch_mc<2>(wb, N, K, qs, d2, M, y, ldy, stream);
-    if (M <= 4) return launch_mc<4>(wb, N, K, qs, d2, M, y, ldy, stream);
-    return launch_mc<8>(wb, N, K, qs, d2, M, y, ldy, stream);
+    switch (wt) {
+        case kWtIQ4XS: return launch_wt<kWtIQ4XS>(wb, N, K, qs, d2, M, y, ldy, stream);
+        case kWtQ4_0: return launch_wt<kWtQ4_0>(wb, N, K, qs, d2, M, y, ldy, stream);
+        case kWtIQ4NL: return launch_wt<kWtIQ4NL>(wb, N, K, qs, d2, M, y, ldy, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_matmul_dp4a_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N,

@@ -32,9 +32,14 @@
 //                          shared memory) per sub-block and commits.  Two
 //                          issuers keep the tensor pipe fed between their
 //                          own handshakes.
-//   warp 9 (producer)      TMA: W stages of 2 super-blocks (128 x 272 B, 2D
-//                          tensor map); activation stages of 4 sub-blocks
-//                          (one bulk copy of the pre-tiled fp16 hi / lo pairs).
+//   warp 9 (producer)      TMA: W stages of 512 weights per row (2D tensor
+//                          map: one 128 x 272 B box of two IQ4_XS
+//                          super-blocks, or two 128 x 144 B boxes of eight
+//                          18-byte Q4_0 / IQ4_NL blocks each -- 144-byte rows
+//                          keep the decoders' shared-memory reads at 4-way
+//                          bank conflicts where 288-byte rows would be
+//                          8-way); activation stages of 4 sub-blocks (one
+//                          bulk copy of the pre-tiled fp16 hi / lo pairs).
 //   warp 10                allocates and frees tensor memory.
 //   warps 12-15 (epilogue) thread t reads row t's integer results and scale,
 //                          releases the slot, and accumulates
@@ -64,9 +69,16 @@ __device__ __forceinline__ void reg_dealloc() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
 }
 
-template <int MT>
+template <int MT, int WT>
 struct TcCfg {
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= kMaxMTile, "UMMA N for M=128");
+    // W stage: 512 weights of each of the 128 rows, as kWBoxes TMA boxes of
+    // kTileN rows x kWBoxBytes (each box a dense block of shared memory).
+    static constexpr int kWBoxes = (WT == kWtIQ4XS) ? 1 : 2;
+    static constexpr int kWBoxBytes = (WT == kWtIQ4XS) ? kPairBytes : kB18GroupBytes;
+    static constexpr int kWRowBytes = kWBoxes * kWBoxBytes;  // bytes of one row per stage
+    static constexpr int kWStage = kTileN * kWRowBytes;
+    static_assert(kWBoxBytes % 16 == 0 && kWBoxBytes / 4 <= 256, "TMA box inner extent");
     // Warp roles.  Decoders: kDecGroups groups of four warps (warpgroups
     // 0..G-1); more groups hide more of the decode's latency where the
     // epilogue is light (small tiles).  Then one control warpgroup (MMA
@@ -107,7 +119,7 @@ struct TcCfg {
     static constexpr int kBQhBytes = kBStageSubs * kBSubBytes;            // one bulk copy per stage
     static constexpr int kBStageBytes = kBQhBytes;
     static constexpr int kOffW = 0;
-    static constexpr int kOffB = kOffW + kNW * kWStageBytes;
+    static constexpr int kOffB = kOffW + kNW * kWStage;
     static constexpr int kOffBar = kOffB + kNB * kBStageBytes;
     // W full/empty, B full/empty, A full / MMA done / accumulator free per unit slot, drain
     static constexpr int kNumBars = 2 * kNW + 2 * kNB + 3 * kNP + 1;
@@ -118,7 +130,7 @@ struct TcCfg {
     static_assert(kUsed <= 226 * 1024, "stages fit shared memory");
     static constexpr int kSmem = (kUsed + 1024 > kMinSmem) ? kUsed + 1024 : kMinSmem;
     static constexpr int kRedStride = MT + 4;                  // fp32 words per row (16-byte rows)
-    static_assert(kTileN * kRedStride * 4 <= kNW * kWStageBytes, "reduction tile fits the W ring");
+    static_assert(kTileN * kRedStride * 4 <= kNW * kWStage, "reduction tile fits the W ring");
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
     static_assert(kOffB % 1024 == 0 && kBStageBytes % 16 == 0, "alignment");
 };
@@ -128,12 +140,12 @@ __device__ __forceinline__ void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-template <int MT>
-__global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
+template <int MT, int WT>
+__global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
     matmul_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                      const uint8_t* __restrict__ tc_op, int64_t M, int N, int K,
                      float* __restrict__ y, int64_t ldy, int* err) {
-    using C = TcCfg<MT>;
+    using C = TcCfg<MT, WT>;
     constexpr int kDecGroups = C::kDecGroups, kDecWarps = C::kDecWarps;
     constexpr int kMmaWarp0 = C::kMmaWarp0, kMmaWarp1 = C::kMmaWarp1;
     constexpr int kProducerWarp = C::kProducerWarp, kTmemWarp = C::kTmemWarp, kEpiWarp0 = C::kEpiWarp0;
@@ -174,6 +186,15 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
     const uint8_t* qh_tile = tc_op + (int64_t)z * K32 * C::kBSubBytes;
 
     static_assert(C::kNumBars <= 64, "barriers initialised two per producer lane");
+    // W stage ps (pair index within this CTA's K range) into ring slot `slot`.
+    auto load_w_stage = [&](int slot, int ps) {
+        mbar_arrive_expect_tx(&w_full[slot], C::kWStage);
+#pragma unroll
+        for (int b = 0; b < C::kWBoxes; ++b)
+            tma_load_2d(smem + C::kOffW + slot * C::kWStage + b * (kTileN * C::kWBoxBytes), &tmap_w,
+                        (p0 + ps) * (C::kWRowBytes / 4) + b * (C::kWBoxBytes / 4), n0,
+                        &w_full[slot]);
+    };
     if (warp == kProducerWarp) {
         // Lane i initialises barriers i and i + 32; lane 0 then starts the
         // first W copy at once (W is read-only model state).
@@ -197,8 +218,7 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
         if (lane == 0) {
             *abort_flag = 0;
             prefetch_tmap(&tmap_w);
-            mbar_arrive_expect_tx(&w_full[0], kWStageBytes);
-            tma_load_2d(smem + C::kOffW, &tmap_w, p0 * (kPairBytes / 4), n0, &w_full[0]);
+            load_w_stage(0, 0);
         }
     }
     if (warp == kTmemWarp) tmem_alloc(tmem_base_ptr, kTmemCols);
@@ -231,27 +251,45 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
             if (ok && ps != prev_ps)  // this group's first unit of the stage
                 ok = mbar_wait(&w_full[wslot], (ps / C::kNW) & 1, abort_flag, err, kDevErrTimeoutW);
             prev_ps = ps;
-            const uint8_t* blk = smem + C::kOffW + wslot * kWStageBytes + t * kPairBytes +
-                                 (jj / kSubPerBlock) * kBlockBytes;
-            const int j = jj % kSubPerBlock;
-            const uint2 hdr = *reinterpret_cast<const uint2*>(blk);
-            uint2 q[2 * C::kU];
+            const uint8_t* stage = smem + C::kOffW + wslot * C::kWStage;
+            uint32_t q[C::kU][4];
+            float Sw[C::kU];
+            if constexpr (WT == kWtIQ4XS) {
+                const uint8_t* blk = stage + t * kPairBytes + (jj / kSubPerBlock) * kBlockBytes;
+                const int j = jj % kSubPerBlock;
+                const uint2 hdr = *reinterpret_cast<const uint2*>(blk);
 #pragma unroll
-            for (int u = 0; u < C::kU; ++u) {
-                q[2 * u] = *reinterpret_cast<const uint2*>(blk + 8 + 16 * (j + u));
-                q[2 * u + 1] = *reinterpret_cast<const uint2*>(blk + 16 + 16 * (j + u));
+                for (int u = 0; u < C::kU; ++u) {
+                    const uint2 a = *reinterpret_cast<const uint2*>(blk + 8 + 16 * (j + u));
+                    const uint2 b = *reinterpret_cast<const uint2*>(blk + 16 + 16 * (j + u));
+                    q[u][0] = a.x; q[u][1] = a.y; q[u][2] = b.x; q[u][3] = b.y;
+                }
+#pragma unroll
+                for (int u = 0; u < C::kU; ++u) Sw[u] = iq4xs_scale(hdr.x, hdr.y, j + u);
+            } else {
+                // 18-byte block jq of the stage: box jq / 8, row t (144 bytes,
+                // 16-byte aligned), block jq % 8 at byte 18 * (jq % 8); its
+                // five aligned words stay inside the row.
+#pragma unroll
+                for (int u = 0; u < C::kU; ++u) {
+                    const int jq = jj + u, b = jq % kSubPerBlock;
+                    const uint32_t* a = reinterpret_cast<const uint32_t*>(
+                        stage + (jq / kSubPerBlock) * (kTileN * kB18GroupBytes) + t * kB18GroupBytes +
+                        kB18Bytes * b - 2 * (b & 1));
+                    uint32_t raw[5];
+#pragma unroll
+                    for (int k = 0; k < 5; ++k) raw[k] = a[k];
+                    Sw[u] = b18_unpack(raw, (b & 1) != 0, q[u]);
+                }
             }
             uint32_t h[C::kU][kACols];
 #pragma unroll
             for (int u = 0; u < C::kU; ++u) {
-                decode_f16x2(q[2 * u].x, h[u]);
-                decode_f16x2(q[2 * u].y, h[u] + 4);
-                decode_f16x2(q[2 * u + 1].x, h[u] + 8);
-                decode_f16x2(q[2 * u + 1].y, h[u] + 12);
+                decode_f16x2<WT>(q[u][0], h[u]);
+                decode_f16x2<WT>(q[u][1], h[u] + 4);
+                decode_f16x2<WT>(q[u][2], h[u] + 8);
+                decode_f16x2<WT>(q[u][3], h[u] + 12);
             }
-            float Sw[C::kU];
-#pragma unroll
-            for (int u = 0; u < C::kU; ++u) Sw[u] = iq4xs_scale(hdr.x, hdr.y, j + u);
             // The stage's bytes are consumed (in registers) once this warp's
             // last unit of it is decoded.
             if (v + kDecGroups >= nunits || (l0 + kDecGroups * C::kU) / kSubPerPair != ps) {
@@ -350,9 +388,7 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
             }
             if (pre > 1) ok = mbar_wait(&w_full[0], 0, abort_flag, err, kDevErrTimeoutW);
             for (int ps = 1; ps < pre && ok; ++ps) {
-                mbar_arrive_expect_tx(&w_full[ps], kWStageBytes);
-                tma_load_2d(smem + C::kOffW + ps * kWStageBytes, &tmap_w,
-                            (p0 + ps) * (kPairBytes / 4), n0, &w_full[ps]);
+                load_w_stage(ps, ps);
                 ++issued_w;
             }
             for (int bs = issued_b; bs < nbst && ok; ++bs) {
@@ -363,9 +399,7 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
                         ok = mbar_wait(&w_empty[slot], ((ps / C::kNW) - 1) & 1, abort_flag, err,
                                        kDevErrTimeoutW);
                         if (!ok) break;
-                        mbar_arrive_expect_tx(&w_full[slot], kWStageBytes);
-                        tma_load_2d(smem + C::kOffW + slot * kWStageBytes, &tmap_w,
-                                    (p0 + ps) * (kPairBytes / 4), n0, &w_full[slot]);
+                        load_w_stage(slot, ps);
                         ++issued_w;
                     }
                 }
@@ -564,16 +598,16 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-template <int MT>
+template <int MT, int WT>
 cudaError_t launch_mt(const CUtensorMap& tmap, const uint8_t* tc_op, int64_t M, int N, int K,
                       float* y, int64_t ldy, int* err, int S, int ntiles, int mtiles,
                       cudaStream_t stream) {
-    using C = TcCfg<MT>;
+    using C = TcCfg<MT, WT>;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(matmul_tc_kernel<MT>,
+        cudaError_t e = cudaFuncSetAttribute(matmul_tc_kernel<MT, WT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
@@ -592,19 +626,39 @@ cudaError_t launch_mt(const CUtensorMap& tmap, const uint8_t* tc_op, int64_t M, 
     attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, matmul_tc_kernel<MT>, tmap, tc_op, M, N, K, y, ldy, err);
+    return cudaLaunchKernelEx(&cfg, matmul_tc_kernel<MT, WT>, tmap, tc_op, M, N, K, y, ldy, err);
+}
+
+template <int WT>
+cudaError_t launch_wt(const CUtensorMap& tmap, const uint8_t* op, int64_t M, int N, int K,
+                      float* y, int64_t ldy, int* err, int S, int ntiles, int mtiles,
+                      cudaStream_t stream) {
+    switch (tc_mtile(M)) {
+        case 16: return launch_mt<16, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
+        case 32: return launch_mt<32, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
+        case 48: return launch_mt<48, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
+        case 64: return launch_mt<64, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
+        case 80: return launch_mt<80, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
+        case 96: return launch_mt<96, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
+        case 112: return launch_mt<112, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
+        case 128: return launch_mt<128, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
 
-cudaError_t launch_matmul_tc(const void* w, int64_t N, int64_t K, const void* tc_operand,
+cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const void* tc_operand,
                              int64_t M, float* y, int64_t ldy, void* encode, int* err,
                              int num_sms, cudaStream_t stream) {
-    const int64_t row_bytes = (K / kQK) * kBlockBytes;
+    if (wt != kWtIQ4XS && wt != kWtQ4_0 && wt != kWtIQ4NL) return cudaErrorInvalidValue;
+    const int64_t row_bytes = wt_row_bytes(wt, K);
+    // one TMA box: 128 rows x (two super-blocks, or eight 18-byte blocks)
+    const int box_bytes = (wt == kWtIQ4XS) ? kPairBytes : kB18GroupBytes;
     CUtensorMap tmap;
     const cuuint64_t gdim[2] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)N};
     const cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
-    const cuuint32_t box[2] = {(cuuint32_t)(kPairBytes / 4), (cuuint32_t)kTileN};
+    const cuuint32_t box[2] = {(cuuint32_t)(box_bytes / 4), (cuuint32_t)kTileN};
     const cuuint32_t estride[2] = {1, 1};
     CUresult cr = reinterpret_cast<EncodeTiledFn>(encode)(
         &tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(w), gdim, gstride, box,
@@ -612,7 +666,6 @@ cudaError_t launch_matmul_tc(const void* w, int64_t N, int64_t K, const void* tc
         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
-    const int MT = tc_mtile(M);
     const int mtiles = (int)tc_num_mtiles(M);
     const int ntiles = (int)((N + kTileN - 1) / kTileN);
     const int pairs = (int)(K / kPairK);
@@ -622,17 +675,9 @@ cudaError_t launch_matmul_tc(const void* w, int64_t N, int64_t K, const void* tc
     if (S < 1) S = 1;
     const uint8_t* op = reinterpret_cast<const uint8_t*>(tc_operand);
     const int Ni = (int)N, Ki = (int)K;
-    switch (MT) {
-        case 16: return launch_mt<16>(tmap, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, stream);
-        case 32: return launch_mt<32>(tmap, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, stream);
-        case 48: return launch_mt<48>(tmap, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, stream);
-        case 64: return launch_mt<64>(tmap, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, stream);
-        case 80: return launch_mt<80>(tmap, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, stream);
-        case 96: return launch_mt<96>(tmap, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, stream);
-        case 112: return launch_mt<112>(tmap, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, stream);
-        case 128: return launch_mt<128>(tmap, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    if (wt == kWtQ4_0) return launch_wt<kWtQ4_0>(tmap, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, stream);
+    if (wt == kWtIQ4NL) return launch_wt<kWtIQ4NL>(tmap, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, stream);
+    return launch_wt<kWtIQ4XS>(tmap, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, stream);
 }
 
 }  // namespace iq4xs

@@ -21,7 +21,8 @@ def test_header_declares_the_entry_points():
     assert {"iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_dequantize", "iq4xs_select_path",
             "iq4xs_tc_operand_bytes", "iq4xs_set_crossover", "iq4xs_set_baseline_threshold",
             "iq4xs_last_device_error",
-            "iq4xs_status_string", "iq4xs_linear", "iq4xs_linear_workspace_bytes"} <= names
+            "iq4xs_status_string", "iq4xs_linear", "iq4xs_linear_workspace_bytes",
+            "iq4xs_matmul_wt", "iq4xs_dequantize_wt", "iq4xs_weight_bytes"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -108,6 +109,25 @@ def test_argument_errors_return_before_any_launch(lib):
     # the tensor-core path needs K % 512 == 0 and its operand
     assert lib.iq4xs_matmul(p, 8, 768, p, p, p, 1, p, 8, 2, 0) == B.ERR_SHAPE
     assert lib.iq4xs_matmul(p, 8, 512, p, p, None, 1, p, 8, 2, 0) == B.ERR_ARG
+
+
+def test_weight_formats_sizes_and_argument_errors(lib):
+    # bytes per [N][K]: IQ4_XS 136 per 256 weights, Q4_0 / IQ4_NL 18 per 32
+    assert B.iq4xs_weight_bytes("iq4_xs", 3, 512) == 3 * 2 * 136
+    assert B.iq4xs_weight_bytes("q4_0", 3, 512) == 3 * 16 * 18
+    assert B.iq4xs_weight_bytes("iq4_nl", 5, 4096) == 5 * 128 * 18
+    assert B.iq4xs_weight_bytes(3, 3, 512) == 0 and B.iq4xs_weight_bytes(1, 3, 96) == 0
+    p = ctypes.c_void_p(0x10000)
+    for wt in (0, 1, 2):
+        assert lib.iq4xs_matmul_wt(None, wt, 8, 256, p, p, p, 1, p, 8, 0, 0) == B.ERR_ARG
+        assert lib.iq4xs_matmul_wt(p, wt, 8, 288, p, p, p, 1, p, 8, 0, 0) == B.ERR_SHAPE
+        assert lib.iq4xs_matmul_wt(p, wt, 8, 768, p, p, p, 1, p, 8, 2, 0) == B.ERR_SHAPE
+        assert lib.iq4xs_matmul_wt(ctypes.c_void_p(0x10004), wt, 8, 256, p, p, p, 1, p, 8, 1,
+                                   0) == B.ERR_ALIGN
+        assert lib.iq4xs_dequantize_wt(p, wt, 8, 256, p, 2, 0) == B.ERR_ARG
+    for bad in (-1, 3, 99):
+        assert lib.iq4xs_matmul_wt(p, bad, 8, 256, p, p, p, 1, p, 8, 0, 0) == B.ERR_ARG
+        assert lib.iq4xs_dequantize_wt(p, bad, 8, 256, p, 0, 0) == B.ERR_ARG
 
 
 @pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="host without a GPU only")

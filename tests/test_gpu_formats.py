@@ -1,0 +1,138 @@
+"""Q4_0 and IQ4_NL weights (32-weight blocks of 18 bytes) on the GPU through
+the C ABI, against the oracle: both paths, ragged N tails, several M tiles,
+split K, full-size sampled rows; dequantization bit-exact; and the
+IQ4_NL / IQ4_XS identity (uniform sub-block scale) bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _gates import gate_independent, gate_parity, gate_written
+from _gpu import dev, oracle_q8, quantize_gpu, sample_rows
+from iq4_xs_quantized_gb300 import binding as B
+from iq4_xs_quantized_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+FORMATS = [("q4_0", B.WTYPE_Q4_0), ("iq4_nl", B.WTYPE_IQ4_NL)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from iq4_xs_quantized_gb300 import build
+    build.build()
+    B.load()
+    yield
+    assert B.iq4xs_last_device_error() == 0
+
+
+def _oracle_wt(wt, w, N, K, qs, d_h, rows=None):
+    orc = oracle.get()
+    nt = max(1, min(16, oracle.threads_available()))
+    if rows is not None:
+        w = np.ascontiguousarray(w.reshape(N, -1)[rows])
+        N = len(rows)
+    return orc.matmul_wt(wt, w, N, K, qs, d_h, nthreads=nt)
+
+
+def _matmul_wt(wd, wt, N, K, qs, ds, op, M, path):
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    B.iq4xs_matmul_wt(wd, wt, N, K, qs, ds, op, M, y, path)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def _independent(wt, w, N, K, qs, d_h):
+    W = oracle.get().dequantize_wt(wt, w, N, K)
+    xhat = qs.astype(np.float32) * np.repeat(d_h.view(np.float16).astype(np.float32), 32, axis=1)
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        return (dev(xhat) @ dev(W).T).cpu().numpy()
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+@pytest.mark.parametrize("name,wt", FORMATS)
+@pytest.mark.parametrize("N,K", [(300, 2048), (128, 1024), (200, 768)])
+def test_formats_match_oracle_on_every_path(name, wt, N, K):
+    rng = np.random.default_rng([41, wt, N, K])
+    w = synth.block32_weights(rng, N, K, 2e-3)
+    wd = dev(w)
+    Ms = (1, 2, 3, 4, 5, 8, 16, 33, 96, 130)
+    x = synth.activations(rng, max(Ms), K, outlier_frac=0.01)
+    for M in Ms:
+        qs, ds, op = quantize_gpu(x[:M], tc=True)
+        qs_o, d_o, _ = oracle_q8(x[:M])
+        ref = _oracle_wt(wt, w, N, K, qs_o, d_o)
+        paths = [B.PATH_AUTO, B.PATH_DP4A] + ([B.PATH_TC] if K % 512 == 0 else [])
+        for path in paths:
+            y = _matmul_wt(wd, wt, N, K, qs, ds, op, M, path)
+            assert gate_written(y) is None, (name, M, path)
+            r = gate_parity(y, ref)
+            assert r is None, (name, N, K, M, path, r)
+        assert gate_independent(y, _independent(wt, w, N, K, qs_o, d_o)) is None
+
+
+@pytest.mark.parametrize("name,wt", FORMATS)
+def test_formats_full_size_sampled_rows(name, wt):
+    N = K = 4096
+    rng = np.random.default_rng([42, wt])
+    w = synth.block32_weights(rng, N, K, 1e-3)
+    wd = dev(w)
+    rows = sample_rows(N, 48, seed=wt)
+    for M in (1, 4, 16, 64, 96):
+        x = synth.activations(rng, M, K)
+        qs, ds, op = quantize_gpu(x, tc=True)
+        qs_o, d_o, _ = oracle_q8(x)
+        y = _matmul_wt(wd, wt, N, K, qs, ds, op, M, B.PATH_AUTO)
+        assert gate_written(y) is None
+        assert gate_parity(y[:, rows], _oracle_wt(wt, w, N, K, qs_o, d_o, rows)) is None, (name, M)
+
+
+@pytest.mark.parametrize("name,wt", FORMATS + [("iq4_xs", B.WTYPE_IQ4_XS)])
+def test_formats_dequantize_bit_exact(name, wt):
+    N, K = 70, 1536
+    rng = np.random.default_rng([43, wt])
+    w = synth.weights_for(wt, rng, N, K, 2e-3)
+    f32, b16 = oracle.get().dequantize_wt(wt, w, N, K, bf16=True)
+    out = torch.full((N, K), float("nan"), dtype=torch.float32, device="cuda")
+    B.iq4xs_dequantize_wt(dev(w), wt, N, K, out)
+    ob = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
+    B.iq4xs_dequantize_wt(dev(w), name, N, K, ob)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), f32.view(np.uint32))
+    assert np.array_equal(ob.view(torch.int16).cpu().numpy().view(np.uint16), b16)
+
+
+def test_iq4nl_equals_iq4xs_with_uniform_scale_bitwise():
+    """IQ4_XS blocks whose eight ls are all L equal IQ4_NL blocks with
+    d' = d*(L-32) (exact in fp16): same weights, same integer dots and the
+    same fp32 scales, so both kernels give the same bits on both paths."""
+    N, K = 256, 1024
+    rng = np.random.default_rng(44)
+    d, L = np.float16(0.0078125), 45
+    qs_bytes = rng.integers(0, 256, (N, K // 256, 128), dtype=np.uint8)
+    xs = np.zeros((N, K // 256, 136), np.uint8)
+    xs[:, :, 0:2] = np.frombuffer(d.tobytes(), np.uint8)
+    ls = [L] * 8
+    sh = sum(((v >> 4) & 3) << (2 * j) for j, v in enumerate(ls))
+    xs[:, :, 2] = sh & 0xFF
+    xs[:, :, 3] = sh >> 8
+    for j, v in enumerate(ls):
+        xs[:, :, 4 + j // 2] |= np.uint8((v & 0xF) << (4 * (j % 2)))
+    xs[:, :, 8:] = qs_bytes
+    nl = np.zeros((N, K // 32, 18), np.uint8)
+    nl[:, :, 0:2] = np.frombuffer(np.float16(float(d) * (L - 32)).tobytes(), np.uint8)
+    nl[:, :, 2:] = qs_bytes.reshape(N, K // 256, 8, 16).reshape(N, K // 32, 16)
+    w_xs, w_nl = dev(xs.reshape(N, -1)), dev(nl.reshape(N, -1))
+    x = synth.activations(rng, 40, K)
+    for M in (1, 3, 40):
+        qs, ds, op = quantize_gpu(x[:M], tc=True)
+        for path in (B.PATH_DP4A, B.PATH_TC):
+            a = _matmul_wt(w_xs, B.WTYPE_IQ4_XS, N, K, qs, ds, op, M, path)
+            b = _matmul_wt(w_nl, B.WTYPE_IQ4_NL, N, K, qs, ds, op, M, path)
+            assert gate_written(a) is None
+            assert np.array_equal(a, b), (M, path)
