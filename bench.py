@@ -370,6 +370,7 @@ def run_ours(args, world, rank, local):
         torch.cuda.empty_cache()
         extras["decode_stream"] = decode_stream(torch, B, dev)
         extras["moe_grouped"] = moe_grouped(torch, B, dev)
+        extras["weight_formats"] = weight_formats(torch, B, dev, stream, mm_us)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -589,6 +590,51 @@ def moe_grouped(torch, B, dev, layers=12, reps=5):
                     "grouped_GBps": round(nbytes / (times["grouped"] * 1e-6) / 1e9, 1)})
     del ws
     torch.cuda.empty_cache()
+    return res
+
+
+def weight_formats(torch, B, dev, stream, iq4xs_us, N=4096, K=4096, copies=48, reps=10,
+                   ms=(1, 4, 16, 64, 96)):
+    """The same square 4096 x 4096 matmul with Q4_0 and IQ4_NL weights
+    (18-byte blocks of 32, 0.5625 B/weight) on the dispatcher's path:
+    device time per launch from graphs of back-to-back launches over
+    `copies` rotating weight copies (452 MB, larger than L2), beside the
+    IQ4_XS time of the main sweep.  GB/s counts the format's weight bytes
+    plus the Q8_1 activations and fp32 outputs."""
+    from iq4_xs_quantized_gb300 import synth
+    res = []
+    for name in ("q4_0", "iq4_nl"):
+        wt = B.WTYPES[name]
+        w0 = torch.from_numpy(synth.block32_weights(np.random.default_rng([7, wt]), N, K,
+                                                    1e-3)).to(dev)
+        ws = [w0] + [w0.clone() for _ in range(copies - 1)]
+        wbytes = B.iq4xs_weight_bytes(wt, N, K)
+        rng = np.random.default_rng(8)
+        for M in ms:
+            x = torch.from_numpy(synth.activations(rng, M, K)).to(dev)
+            qs, ds, op = B.alloc_activations(M, K, dev, tc=True)
+            B.iq4xs_quantize_q8_1(x, qs, ds, op, stream)
+            y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for w in ws:
+                    B.iq4xs_matmul_wt(w, wt, N, K, qs, ds, op, M, y, B.PATH_AUTO, stream)
+            with torch.cuda.stream(stream):
+                g.replay()
+                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                t1.record(stream)
+            torch.cuda.synchronize()
+            us = t0.elapsed_time(t1) * 1e3 / (reps * copies)
+            nbytes = wbytes + M * K + M * (K // 32) * 4 + 4 * M * N
+            res.append({"format": name, "M": M, "us": round(us, 3),
+                        "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                        "iq4_xs_us": round(iq4xs_us[M], 3) if M in iq4xs_us else None})
+            del g
+        del ws, w0
+        torch.cuda.empty_cache()
     return res
 
 
