@@ -156,7 +156,7 @@ int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t
     if (path == IQ4XS_PATH_TC)
         return from_cuda(launch_matmul_tc(w, wtype, N, K, tc_operand, M, y, ldy, st->encode,
                                           st->err, st->num_sms, s));
-    return from_cuda(launch_matmul_dp4a(w, wtype, N, K, qs, ds, M, y, ldy, s));
+    return from_cuda(launch_matmul_dp4a(w, wtype, N, K, qs, ds, M, y, ldy, st->num_sms, s));
 }
 
 namespace {

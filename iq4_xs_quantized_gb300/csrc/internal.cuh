@@ -664,8 +664,10 @@ cudaError_t launch_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t l
                                  void* ds, void* tc_operand, cudaStream_t stream);
 cudaError_t launch_dequantize(const void* w, int wt, int64_t N, int64_t K, void* out,
                               int out_dtype, cudaStream_t stream);
+// num_sms picks the launch shape (grids of more than two CTAs per SM run
+// with more resident CTAs).
 cudaError_t launch_matmul_dp4a(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,
-                               const void* ds, int64_t M, float* y, int64_t ldy,
+                               const void* ds, int64_t M, float* y, int64_t ldy, int num_sms,
                                cudaStream_t stream);
 // G experts in one launch: expert g has W at w + g * expert_stride and the
 // Q8_1 / output rows [row_offsets[g], row_offsets[g+1]) (device array).

@@ -18,11 +18,27 @@ namespace {
 constexpr int kDp4aThreads = 256;
 constexpr int kRows = 2;   // weight rows per warp
 constexpr int kWarpsPerCta = kDp4aThreads / 32;
-// Sub-block steps whose loads are in flight together: as many as fit in the
-// 128 registers that keep two CTAs (16 warps) resident per SM, so that a
-// 4096-row matrix runs in one wave.
+// Launch shapes, chosen from the grid size G (CTAs) against the SM count:
+// resident CTAs per SM x sub-block steps whose loads each warp keeps in
+// flight (registers bound their product).
+//   shape 0, G <= 2 SMs (one wave, e.g. 4096 rows): 2 CTAs, 4 steps at M=1.
+//   shape 1, G <= 3 SMs (5120-6144 rows): 3 CTAs x 2 steps at M=1, so that
+//            every CTA is resident at once, spread over the SMs.
+//   shape 2, more (several waves): 4 CTAs x 1 step at M=1, so that CTAs of
+//            the next wave are already streaming while the current ones
+//            decode and reduce.
+// M=2 takes 3 CTAs x 1 step from shape 1 on; M >= 3 (ALU-bound) keeps
+// shape 0.  Measured on GB300 (us, shape 0 -> chosen shape): M=1 5120x5120
+// 8.8 -> 6.8 (shape 1), 5120x17408 26.6 -> 20.5 (1), 34816x5120 35.4 ->
+// 29.1 (2); M=2 34816x5120 40.0 -> 36.2.
 template <int MC>
-constexpr int iters_for() { return MC == 1 ? 4 : (MC <= 4 ? 2 : 1); }
+constexpr int max_shape() { return MC == 1 ? 2 : (MC == 2 ? 1 : 0); }
+template <int MC, int S>
+constexpr int ctas_per_sm() { return S == 0 ? 2 : (MC == 1 ? (S == 1 ? 3 : 4) : 3); }
+template <int MC, int S>
+constexpr int iters_for() {
+    return S == 0 ? (MC == 1 ? 4 : (MC <= 4 ? 2 : 1)) : (MC == 1 ? (S == 1 ? 2 : 1) : 1);
+}
 
 __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
     return __dp4a((int)a, (int)b, c);
@@ -31,7 +47,7 @@ __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
 // Rows [0, M) of x against the warp's kRows weight rows n0.. of W (format
 // WT), MC activation rows per pass.  `waited`: the wait for the preceding
 // grid (which wrote the activations) has been done already.
-template <int MC, int WT>
+template <int MC, int WT, int kIters>
 __device__ __forceinline__ void dp4a_rows(const uint8_t* __restrict__ w, int64_t N, int64_t K,
                                           const int8_t* __restrict__ qs,
                                           const __half2* __restrict__ ds, int64_t M,
@@ -39,7 +55,6 @@ __device__ __forceinline__ void dp4a_rows(const uint8_t* __restrict__ w, int64_t
                                           bool waited) {
     const int64_t nsub = K / kSub;
     const int64_t row_bytes = wt_row_bytes(WT, K);
-    constexpr int kIters = iters_for<MC>();
     for (int64_t m0 = 0; m0 < M; m0 += MC) {
         float acc[kRows][MC];
 #pragma unroll
@@ -142,8 +157,8 @@ __device__ __forceinline__ void dp4a_rows(const uint8_t* __restrict__ w, int64_t
     }
 }
 
-template <int MC, int WT>  // activation rows per pass, weight format
-__global__ void __launch_bounds__(kDp4aThreads, 2)
+template <int MC, int WT, int S>  // activation rows per pass, weight format, launch shape
+__global__ void __launch_bounds__(kDp4aThreads, ctas_per_sm<MC, S>())
     matmul_dp4a_kernel(const uint8_t* __restrict__ w, int64_t N, int64_t K,
                        const int8_t* __restrict__ qs, const __half2* __restrict__ ds, int64_t M,
                        float* __restrict__ y, int64_t ldy) {
@@ -151,7 +166,7 @@ __global__ void __launch_bounds__(kDp4aThreads, 2)
     const int lane = threadIdx.x & 31;
     const int64_t n0 = ((int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)) * kRows;
     if (n0 >= N) return;  // whole warp
-    dp4a_rows<MC, WT>(w, N, K, qs, ds, M, y, ldy, n0, lane, false);
+    dp4a_rows<MC, WT, iters_for<MC, S>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, false);
 }
 
 // Grouped (mixture-of-experts) form: G experts, expert g with its own W at
@@ -200,10 +215,11 @@ __global__ void __launch_bounds__(kDp4aThreads, 2)
     qs += r0 * K;
     ds += r0 * (K / kSub);
     y += r0 * ldy;
-    if (M == 1) dp4a_rows<1, kWtIQ4XS>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
-    else if (M == 2) dp4a_rows<2, kWtIQ4XS>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
-    else if (M <= 4) dp4a_rows<4, kWtIQ4XS>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
-    else dp4a_rows<8, kWtIQ4XS>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+    constexpr int X = kWtIQ4XS;
+    if (M == 1) dp4a_rows<1, X, iters_for<1, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+    else if (M == 2) dp4a_rows<2, X, iters_for<2, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+    else if (M <= 4) dp4a_rows<4, X, iters_for<4, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+    else dp4a_rows<8, X, iters_for<8, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
 }
 
 cudaLaunchConfig_t dp4a_config(int64_t N, unsigned slots, cudaStream_t stream,
@@ -222,33 +238,41 @@ cudaLaunchConfig_t dp4a_config(int64_t N, unsigned slots, cudaStream_t stream,
 
 template <int MC, int WT>
 cudaError_t launch_mc(const uint8_t* w, int64_t N, int64_t K, const int8_t* qs, const __half2* ds,
-                      int64_t M, float* y, int64_t ldy, cudaStream_t stream) {
+                      int64_t M, float* y, int64_t ldy, int num_sms, cudaStream_t stream) {
     static_assert(kRows * MC <= 32, "one output per lane");
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = dp4a_config(N, 1, stream, attr);
-    return cudaLaunchKernelEx(&cfg, matmul_dp4a_kernel<MC, WT>, w, N, K, qs, ds, M, y, ldy);
+    const int64_t G = cfg.gridDim.x, sms = num_sms > 0 ? num_sms : 1;
+    const int shape = G <= 2 * sms ? 0 : (G <= 3 * sms ? 1 : 2);
+    if constexpr (max_shape<MC>() >= 2)
+        if (shape >= 2)
+            return cudaLaunchKernelEx(&cfg, matmul_dp4a_kernel<MC, WT, 2>, w, N, K, qs, ds, M, y, ldy);
+    if constexpr (max_shape<MC>() >= 1)
+        if (shape >= 1)
+            return cudaLaunchKernelEx(&cfg, matmul_dp4a_kernel<MC, WT, 1>, w, N, K, qs, ds, M, y, ldy);
+    return cudaLaunchKernelEx(&cfg, matmul_dp4a_kernel<MC, WT, 0>, w, N, K, qs, ds, M, y, ldy);
 }
 
 template <int WT>
 cudaError_t launch_wt(const uint8_t* w, int64_t N, int64_t K, const int8_t* qs, const __half2* ds,
-                      int64_t M, float* y, int64_t ldy, cudaStream_t stream) {
-    if (M == 1) return launch_mc<1, WT>(w, N, K, qs, ds, M, y, ldy, stream);
-    if (M == 2) return launch_mc<2, WT>(w, N, K, qs, ds, M, y, ldy, stream);
-    if (M <= 4) return launch_mc<4, WT>(w, N, K, qs, ds, M, y, ldy, stream);
-    return launch_mc<8, WT>(w, N, K, qs, ds, M, y, ldy, stream);
+                      int64_t M, float* y, int64_t ldy, int num_sms, cudaStream_t stream) {
+    if (M == 1) return launch_mc<1, WT>(w, N, K, qs, ds, M, y, ldy, num_sms, stream);
+    if (M == 2) return launch_mc<2, WT>(w, N, K, qs, ds, M, y, ldy, num_sms, stream);
+    if (M <= 4) return launch_mc<4, WT>(w, N, K, qs, ds, M, y, ldy, num_sms, stream);
+    return launch_mc<8, WT>(w, N, K, qs, ds, M, y, ldy, num_sms, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_matmul_dp4a(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,
-                               const void* ds, int64_t M, float* y, int64_t ldy,
+                               const void* ds, int64_t M, float* y, int64_t ldy, int num_sms,
                                cudaStream_t stream) {
     const uint8_t* wb = reinterpret_cast<const uint8_t*>(w);
     const __half2* d2 = reinterpret_cast<const __half2*>(ds);
     switch (wt) {
-        case kWtIQ4XS: return launch_wt<kWtIQ4XS>(wb, N, K, qs, d2, M, y, ldy, stream);
-        case kWtQ4_0: return launch_wt<kWtQ4_0>(wb, N, K, qs, d2, M, y, ldy, stream);
-        case kWtIQ4NL: return launch_wt<kWtIQ4NL>(wb, N, K, qs, d2, M, y, ldy, stream);
+        case kWtIQ4XS: return launch_wt<kWtIQ4XS>(wb, N, K, qs, d2, M, y, ldy, num_sms, stream);
+        case kWtQ4_0: return launch_wt<kWtQ4_0>(wb, N, K, qs, d2, M, y, ldy, num_sms, stream);
+        case kWtIQ4NL: return launch_wt<kWtIQ4NL>(wb, N, K, qs, d2, M, y, ldy, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }

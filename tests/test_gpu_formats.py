@@ -77,13 +77,13 @@ def test_formats_match_oracle_on_every_path(name, wt, N, K):
 
 
 @pytest.mark.parametrize("name,wt", FORMATS)
-def test_formats_full_size_sampled_rows(name, wt):
-    N = K = 4096
-    rng = np.random.default_rng([42, wt])
+@pytest.mark.parametrize("N,K", [(4096, 4096), (5120, 5120), (12288, 5120)])
+def test_formats_full_size_sampled_rows(name, wt, N, K):
+    rng = np.random.default_rng([42, wt, N])
     w = synth.block32_weights(rng, N, K, 1e-3)
     wd = dev(w)
     rows = sample_rows(N, 48, seed=wt)
-    for M in (1, 4, 16, 64, 96):
+    for M in ((1, 2, 4, 16, 64, 96) if N == 4096 else (1, 2, 16)):
         x = synth.activations(rng, M, K)
         qs, ds, op = quantize_gpu(x, tc=True)
         qs_o, d_o, _ = oracle_q8(x)

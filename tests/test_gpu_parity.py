@@ -208,7 +208,9 @@ def test_full_square(M):
 
 @pytest.mark.parametrize("shape_index", range(9))
 def test_full_decoder_shapes(shape_index):
-    for M, path in ((1, "dp4a"), (16, "tc"), (64, "tc")):
+    # dp4a at M = 1 and 2 meets all three launch shapes across these grids
+    # (1024 rows: 64 CTAs; 5120-6144: 320-384; 10240-34816: 640-2176)
+    for M, path in ((1, "dp4a"), (2, "dp4a"), (16, "tc"), (64, "tc")):
         _full_case("decoder27b_9proj", shape_index, M, path, nrows=24)
 
 
