@@ -598,6 +598,62 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// K splits per tile (= cluster size): the S in 1..kMaxCluster (and at most
+// the K pairs) with the least modelled time
+//     waves(S) x (F + ceil(pairs / S)),
+// in units of one K pair's streaming time per CTA.  A wave is as many
+// clusters as the device runs at once for this kernel and cluster size
+// (cudaOccupancyMaxActiveClusters, queried once per device and S; clusters
+// stay inside one GPC, so on GB300 at most 152 / 76 / 46 / 36 / 28 / 23 /
+// 15 / 15 clusters of 1..8 run at once -- the query agrees with a probe of
+// CTA start times).  F is a CTA's fixed cost (launch ramp, first W stage,
+// reduction), ~4.5 us on GB300 against 2.4 / 4.6 / 6.7 us per pair at
+// MT = 16 / 64 / 96.  Ties keep the smaller split.  Examples: 48 row tiles
+// take S = 2 (one wave) instead of S = 3 (48 clusters of 3 need two waves):
+// 27.2 -> 18.4 us at 6144 x 5120, M = 16; 96 tiles stay at S = 1.
+// `fallback` (the largest split that fits one wave on the SM count) stands
+// if a query fails.
+template <int MT, int WT>
+int choose_split(int dev, int fallback, int units, int pairs) {
+    using C = TcCfg<MT, WT>;
+    constexpr double kFixed = MT <= 32 ? 1.9 : (MT <= 64 ? 1.1 : 0.66);
+    static int max_clusters[64][kMaxCluster + 1] = {};
+    if (dev < 0 || dev >= 64) return fallback;
+    int best = fallback;
+    double best_t = 0.0;
+    for (int s = 1; s <= kMaxCluster && s <= pairs; ++s) {
+        int& mc = max_clusters[dev][s];
+        if (mc == 0) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(1, (unsigned)s, 1);
+            q.blockDim = dim3(C::kThreads);
+            q.dynamicSmemBytes = C::kSmem;
+            cudaLaunchAttribute a[1];
+            a[0].id = cudaLaunchAttributeClusterDimension;
+            a[0].val.clusterDim.x = 1;
+            a[0].val.clusterDim.y = (unsigned)s;
+            a[0].val.clusterDim.z = 1;
+            q.attrs = a;
+            q.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, matmul_tc_kernel<MT, WT>, &q) != cudaSuccess ||
+                n < 1) {
+                cudaGetLastError();
+                n = -1;
+            }
+            mc = n;
+        }
+        if (mc < 1) return fallback;
+        const int waves = (units + mc - 1) / mc;
+        const double t = waves * (kFixed + (double)((pairs + s - 1) / s));
+        if (s == 1 || t < best_t * 0.999) {
+            best = s;
+            best_t = t;
+        }
+    }
+    return best;
+}
+
 template <int MT, int WT>
 cudaError_t launch_mt(const CUtensorMap& tmap, const uint8_t* tc_op, int64_t M, int N, int K,
                       float* y, int64_t ldy, int* err, int S, int ntiles, int mtiles,
@@ -612,6 +668,7 @@ cudaError_t launch_mt(const CUtensorMap& tmap, const uint8_t* tc_op, int64_t M, 
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
+    S = choose_split<MT, WT>(dev, S, ntiles * mtiles, K / kPairK);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ntiles, (unsigned)S, (unsigned)mtiles);
     cfg.blockDim = dim3(C::kThreads);
