@@ -16,12 +16,14 @@
 // cluster whose CTAs reduce their partial tiles through distributed shared
 // memory.
 //
-// Warp-specialized roles, each a loop over the CTA's sub-blocks, decoupled by
-// mbarrier rings (kNS slots of tensor memory per ring position: the decoded
-// A operand, 16 columns; the integer accumulator, MT columns; the row scale,
-// one column):
-//   warps 0-7 (decoders)   two groups of four; group g takes sub-blocks
-//                          4k+2g and 4k+2g+1.  Warp w decodes rows 32(w%4)..+31 from
+// Warp-specialized roles, each a loop over the CTA's units of kU sub-blocks,
+// decoupled by mbarrier rings (kNP slots of tensor memory: the decoded A
+// operand, 16 columns per sub-block; the accumulators, MT columns per
+// sub-block; the row scales, one column per sub-block).  Warp numbers below
+// are for two decoder groups (MT > 16); at MT = 16 a third group takes warps
+// 8-11 and the others move up by four:
+//   warps 0-7 (decoders)   G groups of four; group g takes units g, g+G,
+//                          ....  Warp w decodes rows 32(w%4)..+31 from
 //                          the staged W bytes to exact fp16 and stores them
 //                          with tcgen05.st straight into the A slot (row i in
 //                          TMEM lane i), plus d_w*(ls-32) into the scale
@@ -83,7 +85,10 @@ struct TcCfg {
     // 0..G-1); more groups hide more of the decode's latency where the
     // epilogue is light (small tiles).  Then one control warpgroup (MMA
     // issuers, TMA producer, tensor-memory owner) and the epilogue warpgroup.
-    static constexpr int kDecGroups = 2;  // three groups measured slower: the epilogue then starves
+    // Three groups at MT = 16 (more independent decode streams per SM
+    // sub-partition: the decoders are latency-bound there; measured 4-11%
+    // faster); at MT >= 32 a third group measured 5-17% slower.
+    static constexpr int kDecGroups = (MT <= 16) ? 3 : 2;
     static constexpr int kDecWarps = 4 * kDecGroups;
     static constexpr int kMmaWarp0 = kDecWarps;       // MMA issuers (even / odd units)
     static constexpr int kProducerWarp = kDecWarps + 1;
