@@ -371,6 +371,8 @@ def run_ours(args, world, rank, local):
         extras["decode_stream"] = decode_stream(torch, B, dev)
         extras["moe_grouped"] = moe_grouped(torch, B, dev)
         extras["weight_formats"] = weight_formats(torch, B, dev, stream, mm_us)
+        extras["decoder_shapes"] = decoder_shapes(torch, B, dev, stream)
+        extras["prefill_sweep"] = prefill_sweep(torch, B, dev, stream)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -634,6 +636,101 @@ def weight_formats(torch, B, dev, stream, iq4xs_us, N=4096, K=4096, copies=48, r
                         "iq4_xs_us": round(iq4xs_us[M], 3) if M in iq4xs_us else None})
             del g
         del ws, w0
+        torch.cuda.empty_cache()
+    return res
+
+
+def _graph_us(torch, stream, fn, calls, reps):
+    """Device time per call of `fn` (which issues `calls` launches) from
+    graph replays timed with CUDA events on the launching stream."""
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    with torch.cuda.stream(stream):
+        g.replay()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return t0.elapsed_time(t1) * 1e3 / (reps * calls)
+
+
+def _copies_over_l2(torch, w0, target=4 * 129 * 2**20):
+    n = max(4, -(-target // w0.numel()))
+    return [w0] + [w0.clone() for _ in range(n - 1)]
+
+
+def decoder_shapes(torch, B, dev, stream, reps=10):
+    """The nine projection shapes of a ~27B-class decoder layer (1% of the
+    activation channels x20), M = 1, 4, 8, 16, 64: the matmul on the
+    dispatcher's kernel path, device time per launch from graphs of
+    back-to-back launches over rotating weight copies (more than 4x L2 per
+    shape); GB/s counts W, the Q8_1 activations and y."""
+    from iq4_xs_quantized_gb300 import synth
+    W = synth.DECODER_27B
+    res = []
+    for si, (N, K) in enumerate(W.shapes):
+        w_np, x_np = W.inputs(si, M=max(W.ms))
+        ws = _copies_over_l2(torch, torch.from_numpy(w_np).to(dev))
+        y = torch.empty((max(W.ms), N), dtype=torch.float32, device=dev)
+        for M in W.ms:
+            path = kernel_path(B, M, N, K)
+            x = torch.from_numpy(np.ascontiguousarray(x_np[:M])).to(dev)
+            qs, ds, op = B.alloc_activations(M, K, dev, tc=(path == B.PATH_TC))
+            B.iq4xs_quantize_q8_1(x, qs, ds, op, stream)
+
+            def mm():
+                for w in ws:
+                    B.iq4xs_matmul(w, N, K, qs, ds, op, M, y, path, stream)
+            us = _graph_us(torch, stream, mm, len(ws), reps)
+            gbs = matmul_bytes(M, N, K) / (us * 1e-6) / 1e9
+            res.append({"N": N, "K": K, "M": M, "path": "dp4a" if path == B.PATH_DP4A else "tc",
+                        "us": round(us, 3), "GBps": round(gbs, 1),
+                        "TOPS": round(2 * M * N * K / (us * 1e-6) / 1e12, 2)})
+        del ws
+        torch.cuda.empty_cache()
+    return res
+
+
+def prefill_sweep(torch, B, dev, stream, reps=3):
+    """Prefill range: (17408, 5120) and (5120, 17408), M = 96..512, x rounded
+    to bf16.  The tcgen05 matmul (quantize included) against the dequantize to
+    bf16 + dense bf16 GEMM route, same rotating weight copies, device time
+    per call; `advised` is the route iq4xs_select_path names."""
+    from iq4_xs_quantized_gb300 import synth
+    W = synth.PREFILL
+    res = []
+    for si, (N, K) in enumerate(W.shapes):
+        w_np, x_np = W.inputs(si, M=max(W.ms))
+        ws = _copies_over_l2(torch, torch.from_numpy(w_np).to(dev))
+        wbf = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+        for M in W.ms:
+            x = torch.from_numpy(np.ascontiguousarray(x_np[:M])).to(dev)
+            xb = x.to(torch.bfloat16)
+            qs, ds, op = B.alloc_activations(M, K, dev, tc=True)
+            y = torch.empty((M, N), dtype=torch.float32, device=dev)
+
+            def tc():
+                for w in ws:
+                    B.iq4xs_quantize_q8_1(x, qs, ds, op, stream)
+                    B.iq4xs_matmul(w, N, K, qs, ds, op, M, y, B.PATH_TC, stream)
+
+            def base():
+                for w in ws:
+                    B.iq4xs_dequantize(w, N, K, wbf, stream)
+                    torch.matmul(xb, wbf.t())
+            t_tc = _graph_us(torch, stream, tc, len(ws), reps)
+            t_b = _graph_us(torch, stream, base, len(ws), reps)
+            adv = B.iq4xs_select_path(M, N, K)
+            res.append({"N": N, "K": K, "M": M, "tc_us": round(t_tc, 2), "dequant_gemm_us": round(t_b, 2),
+                        "advised": "baseline" if adv == B.PATH_BASELINE else "tc"})
+        del ws, wbf
         torch.cuda.empty_cache()
     return res
 
