@@ -388,28 +388,27 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
 }
+// Split phases of the cluster barrier: arrive without waiting (no ordering),
+// and the matching wait (acquire).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
 }
-// No memory clobber: loads of several ranks issue back to back; callers keep
-// them between two cluster barriers (volatile, with a clobber).
-__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_saddr, uint32_t rank) {
+// Store to the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ void st_dsmem_v4(uint32_t local_saddr, uint32_t rank, float a, float b,
+                                            float c, float d) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_saddr), "r"(rank));
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(remote));
-    return v;
-}
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t local_saddr, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_saddr), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
-    return v;
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
 }
 
 // tcgen05 (5th-generation tensor core, tensor memory).

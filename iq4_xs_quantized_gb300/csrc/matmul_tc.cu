@@ -131,11 +131,21 @@ struct TcCfg {
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;   // tmem base, abort flag
     static constexpr int kOffSpan = (kOffMisc + 16 + 15) / 16 * 16;  // current span's scales (MT fp32)
     static_assert(kOffSpan % 16 == 0, "span scales are read as 16-byte vectors");
-    static constexpr int kUsed = kOffSpan + MT * 4;
+    static constexpr int kRedStride = MT + 4;                  // fp32 words per row (16-byte rows)
+    // Split-K reduction by push: the receive region holds every cluster
+    // rank's partial rows for this CTA's share of the tile (S slices of
+    // ceil(128 / S) rows, at most 128 + 7 rows).  Where it fits, a region
+    // that nothing else uses (pushes need not wait for the owner to finish);
+    // otherwise the W and B rings, free once every role is done (every W and
+    // B copy issued has been consumed, every MMA has completed).
+    static constexpr int kRedBytes = (kTileN + kMaxCluster) * kRedStride * 4;
+    static constexpr int kOffRed = (kOffSpan + MT * 4 + 15) / 16 * 16;
+    static constexpr bool kRedPush = kOffRed + kRedBytes <= 226 * 1024;
+    static constexpr int kOffRecv = kRedPush ? kOffRed : kOffW;
+    static_assert(kRedPush || kRedBytes <= kOffBar - kOffW, "receive region fits the W and B rings");
+    static constexpr int kUsed = kRedPush ? kOffRed + kRedBytes : kOffSpan + MT * 4;
     static_assert(kUsed <= 226 * 1024, "stages fit shared memory");
     static constexpr int kSmem = (kUsed + 1024 > kMinSmem) ? kUsed + 1024 : kMinSmem;
-    static constexpr int kRedStride = MT + 4;                  // fp32 words per row (16-byte rows)
-    static_assert(kTileN * kRedStride * 4 <= kNW * kWStage, "reduction tile fits the W ring");
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
     static_assert(kOffB % 1024 == 0 && kBStageBytes % 16 == 0, "alignment");
 };
@@ -231,6 +241,10 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_base_ptr;
+    // Reduction into a dedicated region: every thread arrives on the cluster
+    // barrier now; waiting on this phase before the first remote store
+    // guarantees that every rank of the cluster has started.
+    if (C::kRedPush && S > 1) cluster_arrive_relaxed();
     // Let the next kernel in the stream begin its launch; it waits for this
     // grid's completion before touching anything this grid reads or writes.
     griddep_launch_dependents();
@@ -518,10 +532,8 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                 acc[m + 3] *= a.w;
             }
         }
-        // Partial tile -> y (one CTA) or -> shared memory for the cluster
-        // reduction, which reuses the W ring: every decoder read of it
-        // preceded an accumulator these threads have consumed, and every W
-        // copy issued has been consumed.
+        // Partial tile -> y (one CTA), or pushed (posted remote stores) into
+        // the shared memory of the cluster rank that owns row t.
         const int64_t mrows = M - (int64_t)z * MT;
         if (S == 1) {
             griddep_wait();
@@ -529,45 +541,58 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
             for (int m = 0; m < MT; ++m)
                 if (m < mrows && n0 + t < N) y[((int64_t)z * MT + m) * ldy + n0 + t] = acc[m];
         } else {
-            float4* red = reinterpret_cast<float4*>(smem + C::kOffW + t * C::kRedStride * 4);
+            // Push row t into the shared memory of the rank that owns it:
+            // where a dedicated receive region fits, as soon as every rank
+            // has started; otherwise into the owner's W and B rings, once
+            // every rank is done with them (this barrier).
+            if constexpr (C::kRedPush) cluster_wait();
+            else cluster_sync_all();
+            // owner: the rank r with 128 r / S <= t < 128 (r + 1) / S
+            const uint32_t owner = (uint32_t)((t * S + S - 1) / kTileN);
+            const int lr = t - (int)((kTileN * owner) / S);
+            const int cap = (kTileN + S - 1) / S;
+            const uint32_t dst =
+                smem_u32(smem + C::kOffRecv) + (uint32_t)(((int)rank * cap + lr) * C::kRedStride * 4);
 #pragma unroll
-            for (int m = 0; m < MT; m += 4) red[m / 4] = make_float4(acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
+            for (int m = 0; m < MT; m += 4)
+                st_dsmem_v4(dst + (uint32_t)(m * 4), owner, acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
         }
     }
 
     if (S > 1) {
-        // Split-K reduction over the cluster through distributed shared memory:
-        // CTA `rank` sums rows [rank*128/S, (rank+1)*128/S) over all CTAs in
-        // rank order (deterministic) and writes them.  Decoder and epilogue
-        // warps (384 threads) share the work.
+        // Split-K reduction: after the cluster barrier that follows the
+        // pushes (its release / acquire orders every rank's remote stores
+        // before the reads), CTA `rank` sums rows [rank*128/S,
+        // (rank+1)*128/S) over the S slices in rank order (deterministic)
+        // from its own shared memory and writes them.  No rank touches
+        // another's shared memory after that barrier, so none waits for the
+        // others before exiting.  Decoder and epilogue warps share the work.
         __syncwarp();
+        if (warp < kEpiWarp0) {  // the phase the epilogue warps completed before pushing
+            if constexpr (C::kRedPush) cluster_wait();
+            else cluster_sync_all();
+        }
         cluster_sync_all();
         if (warp < kDecWarps || warp >= kEpiWarp0) {
             griddep_wait();
             const int idx = (warp < kDecWarps) ? threadIdx.x : threadIdx.x - 4 * 32;
             const int64_t mrows = M - (int64_t)z * MT;
-            const uint32_t red_s = smem_u32(smem + C::kOffW);
-            static_assert(C::kOffW % 16 == 0 && C::kRedStride % 4 == 0, "16-byte reduction rows");
+            const float* red = reinterpret_cast<const float*>(smem + C::kOffRecv);
             const int r0 = (int)(kTileN * rank / S), r1 = (int)(kTileN * (rank + 1) / S);
-            const int rows = r1 - r0;
+            const int rows = r1 - r0, cap = (kTileN + S - 1) / S;
             // element e = (row, 4 columns); consecutive threads take
             // consecutive rows, so the stores to y coalesce
             for (int e = idx; e < rows * (MT / 4); e += (kDecWarps + 4) * 32) {
-                const int row = r0 + e % rows, m = 4 * (e / rows);
-                const uint32_t a = red_s + (uint32_t)((row * C::kRedStride + m) * 4);
-                float4 v[kMaxCluster];
-#pragma unroll
-                for (int q = 0; q < kMaxCluster; ++q)
-                    if (q < S) v[q] = ld_dsmem_v4(a, (uint32_t)q);
-                float4 sum = v[0];
-#pragma unroll
-                for (int q = 1; q < kMaxCluster; ++q)
-                    if (q < S) {
-                        sum.x += v[q].x;
-                        sum.y += v[q].y;
-                        sum.z += v[q].z;
-                        sum.w += v[q].w;
-                    }
+                const int lr = e % rows, m = 4 * (e / rows);
+                float4 sum = *reinterpret_cast<const float4*>(red + lr * C::kRedStride + m);
+                for (int q = 1; q < S; ++q) {
+                    const float4 v = *reinterpret_cast<const float4*>(red + (q * cap + lr) * C::kRedStride + m);
+                    sum.x += v.x;
+                    sum.y += v.y;
+                    sum.z += v.z;
+                    sum.w += v.w;
+                }
+                const int row = r0 + lr;
                 if (n0 + row < N) {
                     float* yp = y + ((int64_t)z * MT + m) * ldy + n0 + row;
                     if (m < mrows) yp[0] = sum.x;
@@ -577,8 +602,6 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                 }
             }
         }
-        __syncwarp();
-        cluster_sync_all();
     }
 
     tc_fence_before();
