@@ -1,5 +1,6 @@
 """iq4xs_linear (quantize + matmul through a caller workspace) on the GPU:
-same result as the two separate calls, within 1e-5 per row of the oracle."""
+same result as the two separate calls, within 1e-5 per row of the oracle,
+and the workspace holds the Q8_1 codes and {d, s}, bit-exact."""
 import numpy as np
 import pytest
 import torch
@@ -45,6 +46,35 @@ def test_linear_matches_two_calls_and_oracle(M):
     rows = sample_rows(N, 40, seed=M)
     r = gate_parity(yl[:, rows], oracle_matmul(w, N, K, qs_o, d_o, rows))
     assert r is None, r
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 5120, 5120), (2, 12288, 5120), (3, 300, 1536),
+                                   (4, 1024, 17408), (4, 256, 25600), (1, 34816, 5120)])
+def test_linear_small_m_bitwise_and_workspace_q8(M, N, K):
+    """CUDA-core path across its launch shapes (two, three, four CTAs per
+    SM), a ragged N and a long K."""
+    B.iq4xs_set_crossover(4)
+    rng = np.random.default_rng([51, M, N, K])
+    w = synth.iq4xs_weights(rng, N, K, 1e-3)
+    x = synth.activations(rng, M, K, outlier_frac=0.01)
+    wd, xd = dev(w), dev(x)
+    ws = torch.full((B.iq4xs_linear_workspace_bytes(M, N, K),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    y = torch.full((M, N), float("nan"), device="cuda")
+    B.iq4xs_linear(wd, N, K, xd, y, ws)
+    torch.cuda.synchronize()
+    yl = y.cpu().numpy()
+    assert gate_written(yl) is None
+    qs, ds, op = quantize_gpu(x, tc=False)
+    assert np.array_equal(yl, matmul_gpu(wd, N, K, qs, ds, None, M, "dp4a"))
+    qs_o, d_o, s_o = oracle_q8(x)
+    wsh = ws.cpu().numpy()
+    assert np.array_equal(wsh[:M * K].view(np.int8).reshape(M, K), qs_o)
+    off = (M * K + 15) // 16 * 16
+    dsw = wsh[off:off + M * (K // 32) * 4].view(np.uint16).reshape(M, K // 32, 2)
+    assert np.array_equal(dsw[:, :, 0], d_o) and np.array_equal(dsw[:, :, 1], s_o)
+    rows = sample_rows(N, 24, seed=M)
+    assert gate_parity(yl[:, rows], oracle_matmul(w, N, K, qs_o, d_o, rows)) is None
 
 
 def test_linear_rejects_small_workspace():
