@@ -59,6 +59,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ms", default=None,
                     help="comma-separated subset of the M sweep (profiling runs only)")
+    ap.add_argument("--shape", default=None,
+                    help="N,K: another weight shape instead of the square 4096 one (profiling runs "
+                         "only; the weights and activations come from the same seeded generators)")
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch without programmatic dependent launch (for serialised profilers)")
     ap.add_argument("--no-extras", action="store_true",
@@ -279,6 +282,13 @@ def run_ours(args, world, rank, local):
     N, K = W.shapes[0]
     ms = list(W.ms) if not args.ms else [int(v) for v in args.ms.split(",")]
     w_np, x_np = W.inputs(0, M=max(W.ms))  # W and x [96, K]; smaller M use prefixes
+    workload = "square_4096x4096, M=1..96 sweep (quantize + matmul per M)"
+    if args.shape:
+        N, K = (int(v) for v in args.shape.split(","))
+        rng = np.random.default_rng([W.seed, N, K])
+        w_np = synth.iq4xs_weights(rng, N, K, W.d_scale)
+        x_np = synth.activations(rng, max(max(ms), max(W.ms)), K)
+        workload = f"shape_{N}x{K}, M sweep (quantize + matmul per M)"
     wd0 = torch.from_numpy(w_np).to(dev)
     wcopies = [wd0] + [wd0.clone() for _ in range(N_COPIES - 1)]
     xs = {M: torch.from_numpy(np.ascontiguousarray(x_np[:M])).to(dev) for M in ms}
@@ -352,7 +362,7 @@ def run_ours(args, world, rank, local):
     tc_bytes = sum(matmul_bytes(M, N, K) for M in tc_ms)
     tc_us = sum(mm_us[M] for M in tc_ms)
     achieved = tc_bytes / (tc_us * 1e-6) / 1e9
-    traffic = recorded_traffic()
+    traffic = recorded_traffic() if not args.shape else None  # recorded for the square shape
     mm_bytes = sum(matmul_bytes(M, N, K) for M in ms)
     mm_us_total = sum(mm_us.values())
 
@@ -389,7 +399,7 @@ def run_ours(args, world, rank, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "int8/fp16-exact integer dots, f32 scale-in",
             "data": "synthetic",
-            "config": {"workload": "square_4096x4096, M=1..96 sweep (quantize + matmul per M)",
+            "config": {"workload": workload,
                        "N": N, "K": K, "ms": ms, "weight_copies": N_COPIES,
                        "l2": f"inputs larger than L2: {N_COPIES} rotating weight copies "
                              f"({N_COPIES * N * K * 17 // 32 / 1e6:.0f} MB)",
