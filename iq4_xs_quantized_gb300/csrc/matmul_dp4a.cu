@@ -176,8 +176,14 @@ __global__ void __launch_bounds__(kDp4aThreads, ctas_per_sm<MC, S>())
 // k-th expert that has rows; the host sizes the grid from the total row
 // count, so slots past the last non-empty expert exit at once.  The batch
 // width follows each expert's own row count, so an expert with one row costs
-// what a one-row matmul costs.
-__global__ void __launch_bounds__(kDp4aThreads, 2)
+// what a one-row matmul costs.  kNarrow (decode batches: at most two rows per
+// routed expert on average): batch widths of one and two rows only (larger
+// experts take several passes), which fit three CTAs per SM -- the launch
+// shape that keeps the next wave streaming on these many-wave grids.  A row's
+// result does not depend on the batch width (each lane sums its sub-blocks
+// in the same order), so both forms give the same bits.
+template <bool kNarrow>
+__global__ void __launch_bounds__(kDp4aThreads, kNarrow ? 3 : 2)
     matmul_dp4a_grouped_kernel(const uint8_t* __restrict__ w, int64_t expert_stride, int64_t G,
                                int64_t N, int64_t K, const int8_t* __restrict__ qs,
                                const __half2* __restrict__ ds, const int32_t* __restrict__ row_offsets,
@@ -216,10 +222,15 @@ __global__ void __launch_bounds__(kDp4aThreads, 2)
     ds += r0 * (K / kSub);
     y += r0 * ldy;
     constexpr int X = kWtIQ4XS;
-    if (M == 1) dp4a_rows<1, X, iters_for<1, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
-    else if (M == 2) dp4a_rows<2, X, iters_for<2, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
-    else if (M <= 4) dp4a_rows<4, X, iters_for<4, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
-    else dp4a_rows<8, X, iters_for<8, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+    if constexpr (kNarrow) {
+        if (M == 1) dp4a_rows<1, X, iters_for<1, 1>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+        else dp4a_rows<2, X, iters_for<2, 1>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+    } else {
+        if (M == 1) dp4a_rows<1, X, iters_for<1, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+        else if (M == 2) dp4a_rows<2, X, iters_for<2, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+        else if (M <= 4) dp4a_rows<4, X, iters_for<4, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+        else dp4a_rows<8, X, iters_for<8, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+    }
 }
 
 cudaLaunchConfig_t dp4a_config(int64_t N, unsigned slots, cudaStream_t stream,
@@ -285,9 +296,13 @@ cudaError_t launch_matmul_dp4a_grouped(const void* w, int64_t expert_stride, int
     const unsigned slots = (unsigned)(G < total_rows ? G : total_rows);
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = dp4a_config(N, slots, stream, attr);
-    return cudaLaunchKernelEx(&cfg, matmul_dp4a_grouped_kernel, reinterpret_cast<const uint8_t*>(w),
-                              expert_stride, G, N, K, qs, reinterpret_cast<const __half2*>(ds),
-                              row_offsets, y, ldy);
+    const uint8_t* wb = reinterpret_cast<const uint8_t*>(w);
+    const __half2* d2 = reinterpret_cast<const __half2*>(ds);
+    if (total_rows <= 2 * (int64_t)slots)  // at most two rows per routed expert on average
+        return cudaLaunchKernelEx(&cfg, matmul_dp4a_grouped_kernel<true>, wb, expert_stride, G, N, K,
+                                  qs, d2, row_offsets, y, ldy);
+    return cudaLaunchKernelEx(&cfg, matmul_dp4a_grouped_kernel<false>, wb, expert_stride, G, N, K, qs,
+                              d2, row_offsets, y, ldy);
 }
 
 }  // namespace iq4xs
