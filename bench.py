@@ -44,8 +44,8 @@ UNIT = "GB/s"
 N_COPIES = 45
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "matmul_square4096_traffic.txt")
+# Sources of the kernel whose DRAM traffic is recorded (the tcgen05 matmul).
 KERNEL_SOURCES = ("iq4_xs_quantized_gb300/csrc/matmul_tc.cu",
-                  "iq4_xs_quantized_gb300/csrc/matmul_dp4a.cu",
                   "iq4_xs_quantized_gb300/csrc/internal.cuh")
 
 
