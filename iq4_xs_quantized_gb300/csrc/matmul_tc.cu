@@ -95,15 +95,26 @@ struct TcCfg {
     static constexpr int kTmemWarp = kDecWarps + 2;
     static constexpr int kMmaWarp1 = kDecWarps + 3;
     static constexpr int kEpiWarp0 = kDecWarps + 4;
-    static constexpr int kThreads = 32 * (kDecWarps + 8);
+    // Epilogue warpgroups: from MT = 48 on two, each owning half of the
+    // activation rows (columns of every accumulator): the per-unit read and
+    // scale-in of 128 x MT results then takes half as long, which matters
+    // because only two to four units fit in tensor memory at once.
+    // Measured on GB300: 10-25% faster at MT = 48..128; at MT = 32 mixed
+    // (3% slower on 4096 x 4096, 3-5% faster on larger shapes), so one group.
+    static constexpr int kEpiGroups = (MT >= 48) ? 2 : 1;
+    static constexpr int kMH = MT / kEpiGroups;  // activation rows of one epilogue group
+    static constexpr int kThreads = 32 * (kDecWarps + 4 + 4 * kEpiGroups);
     // Per-warpgroup register budgets (setmaxnreg).  The block launches with
     // the registers of 65536 / kThreads per thread (rounded down to 8); the
     // budgets, 128 threads each, must sum within that.
     static constexpr int kRegsLaunch = (65536 / kThreads) / 8 * 8;
-    static constexpr int kRegsDecode = (kDecGroups == 3) ? 88 : 96;
+    static constexpr int kRegsDecode = (kEpiGroups == 2) ? (MT >= 80 ? 72 : 80) : (kDecGroups == 3) ? 88 : 96;
     static constexpr int kRegsControl = 56;
-    static constexpr int kRegsEpilogue = (kDecGroups == 3) ? 160 : 248;
-    static_assert(kDecGroups * kRegsDecode + kRegsControl + kRegsEpilogue <= (kThreads / 128) * kRegsLaunch,
+    static constexpr int kRegsEpiFree =
+        ((kThreads / 128) * kRegsLaunch - kDecGroups * kRegsDecode - kRegsControl) / kEpiGroups / 8 * 8;
+    static constexpr int kRegsEpilogue = kRegsEpiFree < 248 ? kRegsEpiFree : 248;
+    static_assert(kDecGroups * kRegsDecode + kRegsControl + kEpiGroups * kRegsEpilogue <=
+                      (kThreads / 128) * kRegsLaunch,
                   "register split fits the launch allocation");
     // Work unit: kU consecutive sub-blocks, decoded, multiplied and scaled
     // together (one barrier handshake per unit between the roles).
@@ -150,7 +161,7 @@ struct TcCfg {
     static_assert(kOffB % 1024 == 0 && kBStageBytes % 16 == 0, "alignment");
 };
 
-constexpr int kEpilogueBarrier = 1;  // named barrier: the 4 epilogue warps
+constexpr int kEpilogueBarrier = 1;  // named barriers 1, 2: the 4 warps of epilogue group 0, 1
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -223,7 +234,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
             else if (i < 2 * C::kNW + 2 * C::kNB) count = 2;                     // b_empty: the MMA warps' commits
             else if (i < 2 * C::kNW + 2 * C::kNB + C::kNP) count = 4;            // a_full: a decoder group
             else if (i < 2 * C::kNW + 2 * C::kNB + 2 * C::kNP) count = 1;        // mma_done
-            else if (i < 2 * C::kNW + 2 * C::kNB + 3 * C::kNP) count = 4;        // d_free: epilogue warps
+            else if (i < 2 * C::kNW + 2 * C::kNB + 3 * C::kNP) count = 4 * C::kEpiGroups;  // d_free: epilogue warps
             else if (i < C::kNumBars) count = 2;                                 // drain: MMA warps
             if (count) mbar_init(&bars[i], count);
         }
@@ -438,21 +449,24 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
         reg_alloc<C::kRegsEpilogue>();
         const int t = (warp & 3) * 32 + lane;  // row within the tile == TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        constexpr int kCols = C::kU * MT;      // accumulator columns of a unit
-        float acc[MT];
+        constexpr int kMH = C::kMH;            // activation rows of this epilogue group
+        const int eg = (warp - kEpiWarp0) / 4;  // epilogue group
+        const int c0 = eg * kMH;                // its first activation row (accumulator column)
+        float acc[kMH];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+        for (int m = 0; m < kMH; ++m) acc[m] = 0.f;
         // Activation span scales (from the preceding grid): the partial sums
         // are kept in units of the current span's 2^-e and rescaled by exact
         // powers of two where the span changes (every 32 sub-blocks).  The
-        // current span's scales are staged in shared memory.
+        // current span's scales are staged in shared memory, each group's
+        // own entries by that group (named barrier 1 + group).
         griddep_wait();
         const float* span_scale = reinterpret_cast<const float*>(tc_op + tc_qh_bytes(M, K)) +
-                                  (int64_t)z * tc_num_spans(K) * MT;
-        float* s_span = reinterpret_cast<float*>(smem + C::kOffSpan);
+                                  (int64_t)z * tc_num_spans(K) * MT + c0;
+        float* s_span = reinterpret_cast<float*>(smem + C::kOffSpan) + c0;
         int cur_span = (p0 * kSubPerPair) / kSubPerSpan;
-        if (t < MT) s_span[t] = span_scale[(int64_t)cur_span * MT + t];
-        named_barrier_sync(kEpilogueBarrier, kTileN);
+        if (t < kMH) s_span[t] = span_scale[(int64_t)cur_span * MT + t];
+        named_barrier_sync(kEpilogueBarrier + eg, kTileN);
         bool ok = true;
         int sp = 0, sphase = 0;
         for (int v = 0; v < nunits; ++v) {
@@ -461,61 +475,110 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                 const float4* fo = reinterpret_cast<const float4*>(s_span);
                 const float4* fn = reinterpret_cast<const float4*>(span_scale + (int64_t)span * MT);
 #pragma unroll
-                for (int m = 0; m < MT; m += 4) {
+                for (int m = 0; m < kMH; m += 4) {
                     const float4 a = fo[m / 4], b = fn[m / 4];
                     acc[m] *= a.x / b.x;
                     acc[m + 1] *= a.y / b.y;
                     acc[m + 2] *= a.z / b.z;
                     acc[m + 3] *= a.w / b.w;
                 }
-                named_barrier_sync(kEpilogueBarrier, kTileN);  // every thread has read the old scales
-                if (t < MT) s_span[t] = span_scale[(int64_t)span * MT + t];
-                named_barrier_sync(kEpilogueBarrier, kTileN);
+                named_barrier_sync(kEpilogueBarrier + eg, kTileN);  // every thread has read the old scales
+                if (t < kMH) s_span[t] = span_scale[(int64_t)span * MT + t];
+                named_barrier_sync(kEpilogueBarrier + eg, kTileN);
                 cur_span = span;
             }
             if (ok) ok = mbar_wait(&mma_done[sp], sphase, abort_flag, err, kDevErrTimeoutMma);
             tc_fence_after();
-            const uint32_t dcol = tmem + lane_off + (uint32_t)(C::kColD + sp * kCols);
+            const uint32_t dcol = tmem + lane_off + (uint32_t)(C::kColD + sp * C::kU * MT + c0);
             const uint32_t scol = tmem + lane_off + (uint32_t)(C::kColS + sp * C::kU);
             uint32_t swb[C::kU];
+            if constexpr (C::kEpiGroups == 1) {
+                // this group's columns of both sub-blocks are contiguous
+                constexpr int kCols = C::kU * MT;
 #pragma unroll
-            for (int part = 0; part < kCols; part += 64) {
-                const int w = (kCols - part < 64) ? kCols - part : 64;
-                uint32_t r[64];
-                if (part == 0) {
-                    if (C::kU == 2) {
-                        if (w == 64) tmem_ld64_s2_wait(dcol, scol, r, swb);
-                        else if (w == 48) tmem_ld48_s2_wait(dcol, scol, r, swb);
-                        else if (w == 32) tmem_ld32_s2_wait(dcol, scol, r, swb);
-                        else tmem_ld16_s2_wait(dcol, scol, r, swb);
+                for (int part = 0; part < kCols; part += 64) {
+                    const int w = (kCols - part < 64) ? kCols - part : 64;
+                    uint32_t r[64];
+                    if (part == 0) {
+                        if (C::kU == 2) {
+                            if (w == 64) tmem_ld64_s2_wait(dcol, scol, r, swb);
+                            else if (w == 48) tmem_ld48_s2_wait(dcol, scol, r, swb);
+                            else if (w == 32) tmem_ld32_s2_wait(dcol, scol, r, swb);
+                            else tmem_ld16_s2_wait(dcol, scol, r, swb);
+                        } else {
+                            if (w == 64) tmem_ld64_s1_wait(dcol, scol, r, swb);
+                            else if (w == 48) tmem_ld48_s1_wait(dcol, scol, r, swb);
+                            else if (w == 32) tmem_ld32_s1_wait(dcol, scol, r, swb);
+                            else tmem_ld16_s1_wait(dcol, scol, r, swb);
+                        }
                     } else {
-                        if (w == 64) tmem_ld64_s1_wait(dcol, scol, r, swb);
-                        else if (w == 48) tmem_ld48_s1_wait(dcol, scol, r, swb);
-                        else if (w == 32) tmem_ld32_s1_wait(dcol, scol, r, swb);
-                        else tmem_ld16_s1_wait(dcol, scol, r, swb);
+                        if (w == 64) tmem_ld64_wait(dcol + part, r);
+                        else if (w == 48) tmem_ld48_wait(dcol + part, r);
+                        else if (w == 32) tmem_ld32_wait(dcol + part, r);
+                        else tmem_ld16_wait(dcol + part, r);
                     }
-                } else {
-                    if (w == 64) tmem_ld64_wait(dcol + part, r);
-                    else if (w == 48) tmem_ld48_wait(dcol + part, r);
-                    else if (w == 32) tmem_ld32_wait(dcol + part, r);
-                    else tmem_ld16_wait(dcol + part, r);
-                }
-                if (part + 64 >= kCols) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&d_free[sp]);
-                }
-                // acc[m] += (d_x * dot) * Sw, two columns per instruction; a
-                // pair of columns never straddles two sub-blocks.
+                    if (part + 64 >= kCols) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&d_free[sp]);
+                    }
+                    // acc[m] += (d_x * dot) * Sw, two columns per instruction; a
+                    // pair of columns never straddles two sub-blocks.
 #pragma unroll
-                for (int k = 0; k < 64; k += 2) {
-                    if (k >= w) break;
-                    const int c = part + k, u = c / MT, m = c % MT;
-                    const float sw = __uint_as_float(swb[u]);
-                    const float2 a = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
-                                                make_float2(sw, sw), make_float2(acc[m], acc[m + 1]));
-                    acc[m] = a.x;
-                    acc[m + 1] = a.y;
+                    for (int k = 0; k < 64; k += 2) {
+                        if (k >= w) break;
+                        const int c = part + k, u = c / MT, m = c % MT;
+                        const float sw = __uint_as_float(swb[u]);
+                        const float2 a = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
+                                                    make_float2(sw, sw), make_float2(acc[m], acc[m + 1]));
+                        acc[m] = a.x;
+                        acc[m + 1] = a.y;
+                    }
+                }
+            } else {
+                // kMH columns of each sub-block u, at u * MT + c0, in at most
+                // two loads (the first with the scale columns)
+                constexpr int kP0 = (kMH <= 48) ? kMH : 32;
+                constexpr int kP1 = kMH - kP0;
+#pragma unroll
+                for (int u = 0; u < C::kU; ++u) {
+                    const uint32_t col = dcol + (uint32_t)(u * MT);
+                    {
+                        uint32_t r[kP0];
+                        if (u == 0) tmem_ld_cols_wait<kP0, C::kU>(col, scol, r, swb);
+                        else tmem_ld_cols_wait<kP0, 0>(col, scol, r, swb);
+                        if (kP1 == 0 && u == C::kU - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&d_free[sp]);
+                        }
+                        const float sw = __uint_as_float(swb[u]);
+#pragma unroll
+                        for (int k = 0; k < kP0; k += 2) {
+                            const float2 a = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
+                                                        make_float2(sw, sw), make_float2(acc[k], acc[k + 1]));
+                            acc[k] = a.x;
+                            acc[k + 1] = a.y;
+                        }
+                    }
+                    if constexpr (kP1 > 0) {
+                        uint32_t r[kP1];
+                        tmem_ld_cols_wait<kP1, 0>(col + kP0, scol, r, swb);
+                        if (u == C::kU - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&d_free[sp]);
+                        }
+                        const float sw = __uint_as_float(swb[u]);
+#pragma unroll
+                        for (int k = 0; k < kP1; k += 2) {
+                            const float2 a = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
+                                                        make_float2(sw, sw),
+                                                        make_float2(acc[kP0 + k], acc[kP0 + k + 1]));
+                            acc[kP0 + k] = a.x;
+                            acc[kP0 + k + 1] = a.y;
+                        }
+                    }
                 }
             }
             if (++sp == C::kNP) { sp = 0; sphase ^= 1; }
@@ -524,7 +587,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
         {
             const float4* f = reinterpret_cast<const float4*>(s_span);
 #pragma unroll
-            for (int m = 0; m < MT; m += 4) {
+            for (int m = 0; m < kMH; m += 4) {
                 const float4 a = f[m / 4];
                 acc[m] *= a.x;
                 acc[m + 1] *= a.y;
@@ -538,8 +601,8 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
         if (S == 1) {
             griddep_wait();
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
-                if (m < mrows && n0 + t < N) y[((int64_t)z * MT + m) * ldy + n0 + t] = acc[m];
+            for (int m = 0; m < kMH; ++m)
+                if (c0 + m < mrows && n0 + t < N) y[((int64_t)z * MT + c0 + m) * ldy + n0 + t] = acc[m];
         } else {
             // Push row t into the shared memory of the rank that owns it:
             // where a dedicated receive region fits, as soon as every rank
@@ -554,8 +617,8 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
             const uint32_t dst =
                 smem_u32(smem + C::kOffRecv) + (uint32_t)(((int)rank * cap + lr) * C::kRedStride * 4);
 #pragma unroll
-            for (int m = 0; m < MT; m += 4)
-                st_dsmem_v4(dst + (uint32_t)(m * 4), owner, acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
+            for (int m = 0; m < kMH; m += 4)
+                st_dsmem_v4(dst + (uint32_t)((c0 + m) * 4), owner, acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
         }
     }
 
@@ -582,7 +645,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
             const int rows = r1 - r0, cap = (kTileN + S - 1) / S;
             // element e = (row, 4 columns); consecutive threads take
             // consecutive rows, so the stores to y coalesce
-            for (int e = idx; e < rows * (MT / 4); e += (kDecWarps + 4) * 32) {
+            for (int e = idx; e < rows * (MT / 4); e += (kDecWarps + 4 * C::kEpiGroups) * 32) {
                 const int lr = e % rows, m = 4 * (e / rows);
                 float4 sum = *reinterpret_cast<const float4*>(red + lr * C::kRedStride + m);
                 for (int q = 1; q < S; ++q) {
