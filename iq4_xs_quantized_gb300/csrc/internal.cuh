@@ -222,6 +222,28 @@ __device__ __forceinline__ void decode_f16x2(uint32_t w, uint32_t out[4]) {
     }
 }
 
+// Nibble c (0..15) of format WT as its integer value.
+template <int WT = kWtIQ4XS>
+__device__ __forceinline__ int wt_nibble_value(int c) {
+    using T = WTables<WT>;
+    const uint32_t word = (c < 4) ? T::S0 : (c < 8) ? T::S1 : (c < 12) ? T::S2 : T::S3;
+    return (int)(int8_t)(uint8_t)(word >> (8 * (c & 3)));
+}
+// Byte-table entry for a qs byte j (low nibble L = element i, high nibble
+// H = element 16+i): the fp16x2 word (value[L], value[H]) that decode_f16x2
+// produces for that byte, exact (|value| <= 128).
+template <int WT = kWtIQ4XS>
+__device__ __forceinline__ uint32_t f16x2_byte_entry(int j) {
+    const uint32_t lo = __half_as_ushort(__int2half_rn(wt_nibble_value<WT>(j & 15)));
+    const uint32_t hi = __half_as_ushort(__int2half_rn(wt_nibble_value<WT>(j >> 4)));
+    return lo | (hi << 16);
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 // 6-bit scale of sub-block j from the 8-byte header word pair
 // hdr0 = d | scales_h << 16, hdr1 = scales_l[0..3].
 __device__ __forceinline__ int iq4xs_ls(uint32_t hdr0, uint32_t hdr1, int j) {

@@ -24,10 +24,12 @@
 // 8-11 and the others move up by four:
 //   warps 0-7 (decoders)   G groups of four; group g takes units g, g+G,
 //                          ....  Warp w decodes rows 32(w%4)..+31 from
-//                          the staged W bytes to exact fp16 and stores them
-//                          with tcgen05.st straight into the A slot (row i in
-//                          TMEM lane i), plus d_w*(ls-32) into the scale
-//                          column, then arrives on the slot's a_full.
+//                          the staged W bytes to exact fp16 (one shared-
+//                          memory table lookup per qs byte for MT <= 96)
+//                          and stores them with tcgen05.st straight into
+//                          the A slot (row i in TMEM lane i), plus
+//                          d_w*(ls-32) into the scale column, then arrives
+//                          on the slot's a_full.
 //   warps 8, 11 (MMA)      warp-uniform loops over even / odd units; one
 //                          elected lane issues four tcgen05.mma 128 x MT x 16
 //                          (A from tensor memory, B hi / lo planes from
@@ -129,14 +131,25 @@ struct TcCfg {
     static_assert(kColS + kNP * kU <= kTmemCols, "slots fit tensor memory");
     static_assert(kNP >= 2, "at least two units in flight");
     static_assert(kBStageSubs % kU == 0 && kSubPerBlock % kU == 0, "units tile stages and super-blocks");
-    static constexpr int kNW = (MT <= 16) ? 5 : (MT <= 48) ? 4 : (MT <= 96) ? 3 : 2;  // W stages
-    static constexpr int kNB = (MT <= 32) ? 4 : (MT <= 64) ? 3 : 2;                   // activation stages
+    // Byte-table decode (MT <= 96): each qs byte (two nibbles) is looked up
+    // in shared memory as the fp16x2 word of the A operand, one load in
+    // place of the register-table decode's integer instructions.  32
+    // copies of the 256-entry table, copy l in bank l: entry j for lane l
+    // at 4 * (32 * j + l), so a warp's 32 lookups never conflict.  Larger
+    // tiles keep the register tables (their activation stages leave no
+    // room).
+    static constexpr bool kLut = MT <= 96;
+    static constexpr int kLutBytes = kLut ? 256 * 32 * 4 : 0;
+    static constexpr int kNW = kLut ? ((MT <= 16) ? 4 : (MT <= 48) ? 3 : (MT <= 64) ? 2 : (MT <= 80) ? 3 : 2)
+                                    : ((MT <= 16) ? 5 : (MT <= 48) ? 4 : (MT <= 96) ? 3 : 2);  // W stages
+    static constexpr int kNB = (MT <= 32) ? 4 : (MT <= 64) ? 3 : 2;                               // activation stages
     static constexpr int kBSubBytes = kPlanes * kChunksPerSub * MT * 16;  // hi + lo of one sub-block
     static constexpr int kBQhBytes = kBStageSubs * kBSubBytes;            // one bulk copy per stage
     static constexpr int kBStageBytes = kBQhBytes;
     static constexpr int kOffW = 0;
     static constexpr int kOffB = kOffW + kNW * kWStage;
-    static constexpr int kOffBar = kOffB + kNB * kBStageBytes;
+    static constexpr int kOffLut = kOffB + kNB * kBStageBytes;
+    static constexpr int kOffBar = kOffLut + kLutBytes;
     // W full/empty, B full/empty, A full / MMA done / accumulator free per unit slot, drain
     static constexpr int kNumBars = 2 * kNW + 2 * kNB + 3 * kNP + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;   // tmem base, abort flag
@@ -153,12 +166,12 @@ struct TcCfg {
     static constexpr int kOffRed = (kOffSpan + MT * 4 + 15) / 16 * 16;
     static constexpr bool kRedPush = kOffRed + kRedBytes <= 226 * 1024;
     static constexpr int kOffRecv = kRedPush ? kOffRed : kOffW;
-    static_assert(kRedPush || kRedBytes <= kOffBar - kOffW, "receive region fits the W and B rings");
+    static_assert(kRedPush || kRedBytes <= kOffLut - kOffW, "receive region fits the W and B rings");
     static constexpr int kUsed = kRedPush ? kOffRed + kRedBytes : kOffSpan + MT * 4;
     static_assert(kUsed <= 226 * 1024, "stages fit shared memory");
     static constexpr int kSmem = (kUsed + 1024 > kMinSmem) ? kUsed + 1024 : kMinSmem;
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-    static_assert(kOffB % 1024 == 0 && kBStageBytes % 16 == 0, "alignment");
+    static_assert(kOffB % 1024 == 0 && kBStageBytes % 16 == 0 && kOffLut % 128 == 0, "alignment");
 };
 
 constexpr int kEpilogueBarrier = 1;  // named barriers 1, 2: the 4 warps of epilogue group 0, 1
@@ -247,6 +260,14 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
             load_w_stage(0, 0);
         }
     }
+    if constexpr (C::kLut) {
+        // Row j of the byte table: 32 copies of entry j (one per bank).
+        uint4* lut = reinterpret_cast<uint4*>(smem + C::kOffLut);
+        for (int i = threadIdx.x; i < 256 * 8; i += C::kThreads) {
+            const uint32_t e = f16x2_byte_entry<WT>(i >> 3);
+            lut[i] = make_uint4(e, e, e, e);
+        }
+    }
     if (warp == kTmemWarp) tmem_alloc(tmem_base_ptr, kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -310,12 +331,25 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                 }
             }
             uint32_t h[C::kU][kACols];
+            if constexpr (C::kLut) {
+                // Byte k of word c holds elements 4c+k (low nibble) and
+                // 16+4c+k (high nibble): table row = the byte.
+                const uint32_t lut = smem_u32(smem + C::kOffLut) + (uint32_t)lane * 4u;
 #pragma unroll
-            for (int u = 0; u < C::kU; ++u) {
-                decode_f16x2<WT>(q[u][0], h[u]);
-                decode_f16x2<WT>(q[u][1], h[u] + 4);
-                decode_f16x2<WT>(q[u][2], h[u] + 8);
-                decode_f16x2<WT>(q[u][3], h[u] + 12);
+                for (int u = 0; u < C::kU; ++u)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            h[u][4 * c + k] = lds_u32(lut + (((q[u][c] >> (8 * k)) & 0xFFu) << 7));
+            } else {
+#pragma unroll
+                for (int u = 0; u < C::kU; ++u) {
+                    decode_f16x2<WT>(q[u][0], h[u]);
+                    decode_f16x2<WT>(q[u][1], h[u] + 4);
+                    decode_f16x2<WT>(q[u][2], h[u] + 8);
+                    decode_f16x2<WT>(q[u][3], h[u] + 12);
+                }
             }
             // The stage's bytes are consumed (in registers) once this warp's
             // last unit of it is decoded.
