@@ -167,6 +167,7 @@ enum DeviceError : int {
     kDevErrTimeoutMma = 0x104,
     kDevErrTimeoutFree = 0x105,
     kDevErrTimeoutDrain = 0x106,
+    kDevErrTimeoutRecv = 0x107,
 };
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
 
@@ -404,16 +405,16 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
-// Thread-block clusters: a barrier over all threads of the cluster, this
-// CTA's rank, and loads from another CTA's shared memory at the same offset.
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-}
-// Split phases of the cluster barrier: arrive without waiting (no ordering),
-// and the matching wait (acquire).
+// Thread-block clusters: the cluster barrier, this CTA's rank, and bulk
+// copies into another CTA's shared memory.
+// Split phases of the cluster barrier: arrive without waiting (no ordering,
+// or releasing this thread's earlier memory accesses), and the matching wait
+// (acquire).
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
@@ -423,14 +424,19 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
 }
-// Store to the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ void st_dsmem_v4(uint32_t local_saddr, uint32_t rank, float a, float b,
-                                            float c, float d) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_saddr), "r"(rank));
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(a), "f"(b),
-                 "f"(c), "f"(d)
-                 : "memory");
+// Bulk copy from this CTA's shared memory (src) to the same-offset address
+// dst_local in CTA `rank` of the cluster, completing `bytes` on that CTA's
+// mbarrier at offset bar_local (16-byte aligned addresses, size a multiple
+// of 16).
+__device__ __forceinline__ void bulk_copy_to_rank(uint32_t dst_local, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar_local, uint32_t rank) {
+    uint32_t dst, bar;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dst) : "r"(dst_local), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(bar) : "r"(bar_local), "r"(rank));
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "r"(src), "r"(bytes), "r"(bar)
+        : "memory");
 }
 
 // tcgen05 (5th-generation tensor core, tensor memory).

@@ -73,6 +73,17 @@ __device__ __forceinline__ void reg_dealloc() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
 }
 
+// Rows of other ranks' slices a rank receives in the split-K reduction, at
+// most: max over S = 2..kMaxCluster of (S - 1) * ceil(128 / S).
+constexpr int recv_rows_max() {
+    int r = 0;
+    for (int s = 2; s <= kMaxCluster; ++s) {
+        const int v = (s - 1) * ((kTileN + s - 1) / s);
+        r = v > r ? v : r;
+    }
+    return r;
+}
+
 template <int MT, int WT>
 struct TcCfg {
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= kMaxMTile, "UMMA N for M=128");
@@ -147,27 +158,28 @@ struct TcCfg {
     static constexpr int kBQhBytes = kBStageSubs * kBSubBytes;            // one bulk copy per stage
     static constexpr int kBStageBytes = kBQhBytes;
     static constexpr int kOffW = 0;
-    static constexpr int kOffB = kOffW + kNW * kWStage;
-    static constexpr int kOffLut = kOffB + kNB * kBStageBytes;
-    static constexpr int kOffBar = kOffLut + kLutBytes;
-    // W full/empty, B full/empty, A full / MMA done / accumulator free per unit slot, drain
-    static constexpr int kNumBars = 2 * kNW + 2 * kNB + 3 * kNP + 1;
+    static constexpr int kOffLut = kOffW + kNW * kWStage;
+    static constexpr int kOffB = kOffLut + kLutBytes;
+    static constexpr int kOffBar = kOffB + kNB * kBStageBytes;
+    // W full/empty, B full/empty, A full / MMA done / accumulator free per
+    // unit slot, drain, split-K rows received
+    static constexpr int kNumBars = 2 * kNW + 2 * kNB + 3 * kNP + 2;
+    static constexpr int kBarDrain = 2 * kNW + 2 * kNB + 3 * kNP;
+    static constexpr int kBarRecv = kBarDrain + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;   // tmem base, abort flag
     static constexpr int kOffSpan = (kOffMisc + 16 + 15) / 16 * 16;  // current span's scales (MT fp32)
     static_assert(kOffSpan % 16 == 0, "span scales are read as 16-byte vectors");
-    static constexpr int kRedStride = MT + 4;                  // fp32 words per row (16-byte rows)
-    // Split-K reduction by push: the receive region holds every cluster
-    // rank's partial rows for this CTA's share of the tile (S slices of
-    // ceil(128 / S) rows, at most 128 + 7 rows).  Where it fits, a region
-    // that nothing else uses (pushes need not wait for the owner to finish);
-    // otherwise the W and B rings, free once every role is done (every W and
-    // B copy issued has been consumed, every MMA has completed).
-    static constexpr int kRedBytes = (kTileN + kMaxCluster) * kRedStride * 4;
-    static constexpr int kOffRed = (kOffSpan + MT * 4 + 15) / 16 * 16;
-    static constexpr bool kRedPush = kOffRed + kRedBytes <= 226 * 1024;
-    static constexpr int kOffRecv = kRedPush ? kOffRed : kOffW;
-    static_assert(kRedPush || kRedBytes <= kOffLut - kOffW, "receive region fits the W and B rings");
-    static constexpr int kUsed = kRedPush ? kOffRed + kRedBytes : kOffSpan + MT * 4;
+    // Split-K reduction.  Each rank stages its partial tile (128 rows of
+    // MT fp32, kRedStride apart) in its own activation ring, which is free
+    // once its last MMA has completed, and bulk-copies the rows every other
+    // rank owns into that rank's W ring and byte table, which are free once
+    // that rank's decoders are done: S - 1 slices of ceil(128 / S) rows.
+    static constexpr int kRedStride = MT + 4;  // fp32 words per row (16-byte rows, no bank conflicts)
+    static constexpr int kOffStage = kOffB;
+    static constexpr int kOffRecv = kOffW;
+    static_assert(kTileN * kRedStride * 4 <= kNB * kBStageBytes, "staged partial tile fits the activation ring");
+    static_assert(recv_rows_max() * kRedStride * 4 <= kOffB - kOffW, "received slices fit the W ring and table");
+    static constexpr int kUsed = kOffSpan + MT * 4;
     static_assert(kUsed <= 226 * 1024, "stages fit shared memory");
     static constexpr int kSmem = (kUsed + 1024 > kMinSmem) ? kUsed + 1024 : kMinSmem;
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
@@ -206,6 +218,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
     uint64_t* mma_done = a_full + C::kNP;
     uint64_t* d_free = mma_done + C::kNP;
     uint64_t* drain = d_free + C::kNP;
+    uint64_t* recv_bar = bars + C::kBarRecv;  // split-K: the other ranks' slices have landed
     uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -248,7 +261,8 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
             else if (i < 2 * C::kNW + 2 * C::kNB + C::kNP) count = 4;            // a_full: a decoder group
             else if (i < 2 * C::kNW + 2 * C::kNB + 2 * C::kNP) count = 1;        // mma_done
             else if (i < 2 * C::kNW + 2 * C::kNB + 3 * C::kNP) count = 4 * C::kEpiGroups;  // d_free: epilogue warps
-            else if (i < C::kNumBars) count = 2;                                 // drain: MMA warps
+            else if (i == C::kBarDrain) count = 2;                               // drain: MMA warps
+            else if (i == C::kBarRecv) count = 1;                                // recv: expect_tx below
             if (count) mbar_init(&bars[i], count);
         }
         fence_barrier_init();
@@ -258,6 +272,13 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
             *abort_flag = 0;
             prefetch_tmap(&tmap_w);
             load_w_stage(0, 0);
+            // Split-K: this rank's rows arrive from the S - 1 other ranks.
+            // Posted now, before any rank can send (sends wait for a cluster
+            // barrier phase that needs this CTA's threads past set-up).
+            if (S > 1) {
+                const int rows = (int)(kTileN * (rank + 1) / S) - (int)(kTileN * rank / S);
+                mbar_arrive_expect_tx(recv_bar, (uint32_t)((S - 1) * rows * C::kRedStride * 4));
+            }
         }
     }
     if constexpr (C::kLut) {
@@ -273,10 +294,12 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_base_ptr;
-    // Reduction into a dedicated region: every thread arrives on the cluster
-    // barrier now; waiting on this phase before the first remote store
-    // guarantees that every rank of the cluster has started.
-    if (C::kRedPush && S > 1) cluster_arrive_relaxed();
+    // Split-K clusters use three phases of the cluster barrier, each thread
+    // arriving and waiting once per phase: 0 (now) -- every rank has started;
+    // 1 -- every rank's decoders are done with their W ring and byte table
+    // (the other roles arrive at once); 2 -- every rank has received its
+    // slices, so no copy still reads a rank's staged rows when it exits.
+    if (S > 1) cluster_arrive_relaxed();
     // Let the next kernel in the stream begin its launch; it waits for this
     // grid's completion before touching anything this grid reads or writes.
     griddep_launch_dependents();
@@ -333,7 +356,9 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
             uint32_t h[C::kU][kACols];
             if constexpr (C::kLut) {
                 // Byte k of word c holds elements 4c+k (low nibble) and
-                // 16+4c+k (high nibble): table row = the byte.
+                // 16+4c+k (high nibble): table row = the byte (moved to the
+                // low byte by one byte permute, measured faster than a
+                // shift and mask).
                 const uint32_t lut = smem_u32(smem + C::kOffLut) + (uint32_t)lane * 4u;
 #pragma unroll
                 for (int u = 0; u < C::kU; ++u)
@@ -341,7 +366,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            h[u][4 * c + k] = lds_u32(lut + (((q[u][c] >> (8 * k)) & 0xFFu) << 7));
+                            h[u][4 * c + k] = lds_u32(lut + (__byte_perm(q[u][c], 0u, 0x4440u + k) << 7));
             } else {
 #pragma unroll
                 for (int u = 0; u < C::kU; ++u) {
@@ -376,8 +401,17 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
             sp += kDecGroups;
             while (sp >= C::kNP) { sp -= C::kNP; sphase ^= 1; }
         }
+        if (S > 1) {  // phase 1: this warp's reads of the W ring and table are done
+            __syncwarp();
+            cluster_wait();
+            cluster_arrive_release();
+        }
     } else if (warp < kEpiWarp0) {
         reg_dealloc<C::kRegsControl>();
+        if (S > 1) {
+            cluster_wait();
+            cluster_arrive_relaxed();
+        }
         if (warp == kMmaWarp0 || warp == kMmaWarp1) {
             // ---------------------------------------------------------- MMA
             // Warp-uniform loop with incremental indices (the warp shares its
@@ -481,6 +515,10 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         reg_alloc<C::kRegsEpilogue>();
+        if (S > 1) {
+            cluster_wait();
+            cluster_arrive_relaxed();
+        }
         const int t = (warp & 3) * 32 + lane;  // row within the tile == TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         constexpr int kMH = C::kMH;            // activation rows of this epilogue group
@@ -629,8 +667,8 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                 acc[m + 3] *= a.w;
             }
         }
-        // Partial tile -> y (one CTA), or pushed (posted remote stores) into
-        // the shared memory of the cluster rank that owns row t.
+        // Partial tile -> y (one CTA), or staged in this CTA's activation
+        // ring (free: every MMA has completed) for the split-K reduction.
         const int64_t mrows = M - (int64_t)z * MT;
         if (S == 1) {
             griddep_wait();
@@ -638,56 +676,68 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
             for (int m = 0; m < kMH; ++m)
                 if (c0 + m < mrows && n0 + t < N) y[((int64_t)z * MT + c0 + m) * ldy + n0 + t] = acc[m];
         } else {
-            // Push row t into the shared memory of the rank that owns it:
-            // where a dedicated receive region fits, as soon as every rank
-            // has started; otherwise into the owner's W and B rings, once
-            // every rank is done with them (this barrier).
-            if constexpr (C::kRedPush) cluster_wait();
-            else cluster_sync_all();
-            // owner: the rank r with 128 r / S <= t < 128 (r + 1) / S
-            const uint32_t owner = (uint32_t)((t * S + S - 1) / kTileN);
-            const int lr = t - (int)((kTileN * owner) / S);
-            const int cap = (kTileN + S - 1) / S;
-            const uint32_t dst =
-                smem_u32(smem + C::kOffRecv) + (uint32_t)(((int)rank * cap + lr) * C::kRedStride * 4);
+            float* st = reinterpret_cast<float*>(smem + C::kOffStage) + t * C::kRedStride + c0;
 #pragma unroll
             for (int m = 0; m < kMH; m += 4)
-                st_dsmem_v4(dst + (uint32_t)((c0 + m) * 4), owner, acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
+                *reinterpret_cast<float4*>(st + m) = make_float4(acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
+            fence_proxy_async_smem();  // the staged rows are read by bulk copies
         }
     }
 
     if (S > 1) {
-        // Split-K reduction: after the cluster barrier that follows the
-        // pushes (its release / acquire orders every rank's remote stores
-        // before the reads), CTA `rank` sums rows [rank*128/S,
-        // (rank+1)*128/S) over the S slices in rank order (deterministic)
-        // from its own shared memory and writes them.  No rank touches
-        // another's shared memory after that barrier, so none waits for the
-        // others before exiting.  Decoder and epilogue warps share the work.
+        // Split-K reduction.  Rank r owns rows [128 r / S, 128 (r + 1) / S)
+        // of the tile.  Once every rank's decoders are done (phase 1), one
+        // thread of each rank bulk-copies the staged rows every other rank
+        // owns into that rank's W ring (slot of sender q: q, or q - 1 past
+        // the owner), completing on the owner's recv barrier.  The owner
+        // then sums its rows over the S slices in rank order (deterministic)
+        // and writes them; decoder and epilogue warps share the sums.
+        __syncthreads();  // staged rows written
         __syncwarp();
-        if (warp < kEpiWarp0) {  // the phase the epilogue warps completed before pushing
-            if constexpr (C::kRedPush) cluster_wait();
-            else cluster_sync_all();
+        cluster_wait();   // phase 1
+        const int cap = (kTileN + S - 1) / S;
+        if (warp == kEpiWarp0 && lane == 0) {
+            const uint32_t stage0 = smem_u32(smem + C::kOffStage);
+            const uint32_t recv0 = smem_u32(smem + C::kOffRecv);
+            const int slot_base = (int)rank;
+            for (int q = 0; q < S; ++q) {
+                if (q == (int)rank) continue;
+                const int q0 = kTileN * q / S, q1 = kTileN * (q + 1) / S;
+                const int slot = slot_base < q ? slot_base : slot_base - 1;
+                bulk_copy_to_rank(recv0 + (uint32_t)(slot * cap * C::kRedStride * 4),
+                                  stage0 + (uint32_t)(q0 * C::kRedStride * 4),
+                                  (uint32_t)((q1 - q0) * C::kRedStride * 4), smem_u32(recv_bar), (uint32_t)q);
+            }
         }
-        cluster_sync_all();
+        mbar_wait(recv_bar, 0, abort_flag, err, kDevErrTimeoutRecv);
+        __syncwarp();
+        cluster_arrive_relaxed();  // phase 2: this rank's slices have landed
         if (warp < kDecWarps || warp >= kEpiWarp0) {
             griddep_wait();
             const int idx = (warp < kDecWarps) ? threadIdx.x : threadIdx.x - 4 * 32;
             const int64_t mrows = M - (int64_t)z * MT;
-            const float* red = reinterpret_cast<const float*>(smem + C::kOffRecv);
+            const float* stg = reinterpret_cast<const float*>(smem + C::kOffStage);
+            const float* recv = reinterpret_cast<const float*>(smem + C::kOffRecv);
             const int r0 = (int)(kTileN * rank / S), r1 = (int)(kTileN * (rank + 1) / S);
-            const int rows = r1 - r0, cap = (kTileN + S - 1) / S;
+            const int rows = r1 - r0;
             // element e = (row, 4 columns); consecutive threads take
             // consecutive rows, so the stores to y coalesce
             for (int e = idx; e < rows * (MT / 4); e += (kDecWarps + 4 * C::kEpiGroups) * 32) {
                 const int lr = e % rows, m = 4 * (e / rows);
-                float4 sum = *reinterpret_cast<const float4*>(red + lr * C::kRedStride + m);
-                for (int q = 1; q < S; ++q) {
-                    const float4 v = *reinterpret_cast<const float4*>(red + (q * cap + lr) * C::kRedStride + m);
-                    sum.x += v.x;
-                    sum.y += v.y;
-                    sum.z += v.z;
-                    sum.w += v.w;
+                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int q = 0; q < S; ++q) {
+                    const float* src = (q == (int)rank)
+                                           ? stg + (r0 + lr) * C::kRedStride
+                                           : recv + ((q < (int)rank ? q : q - 1) * cap + lr) * C::kRedStride;
+                    const float4 v = *reinterpret_cast<const float4*>(src + m);
+                    if (q == 0) {
+                        sum = v;
+                    } else {
+                        sum.x += v.x;
+                        sum.y += v.y;
+                        sum.z += v.z;
+                        sum.w += v.w;
+                    }
                 }
                 const int row = r0 + lr;
                 if (n0 + row < N) {
@@ -699,6 +749,8 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                 }
             }
         }
+        __syncwarp();
+        cluster_wait();  // phase 2: no copy still reads this CTA's staged rows
     }
 
     tc_fence_before();
