@@ -121,7 +121,7 @@ struct TcCfg {
     // the registers of 65536 / kThreads per thread (rounded down to 8); the
     // budgets, 128 threads each, must sum within that.
     static constexpr int kRegsLaunch = (65536 / kThreads) / 8 * 8;
-    static constexpr int kRegsDecode = (kEpiGroups == 2) ? (MT >= 80 ? 72 : 80) : (kDecGroups == 3) ? 88 : 96;
+    static constexpr int kRegsDecode = (kEpiGroups == 2) ? (MT >= 64 ? 72 : 80) : (kDecGroups == 3) ? 88 : 96;
     static constexpr int kRegsControl = 56;
     static constexpr int kRegsEpiFree =
         ((kThreads / 128) * kRegsLaunch - kDecGroups * kRegsDecode - kRegsControl) / kEpiGroups / 8 * 8;
@@ -329,11 +329,24 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                 const uint8_t* blk = stage + t * kPairBytes + (jj / kSubPerBlock) * kBlockBytes;
                 const int j = jj % kSubPerBlock;
                 const uint2 hdr = *reinterpret_cast<const uint2*>(blk);
+                if (C::kLut && MT >= 80 && jj >= kSubPerBlock) {
+                    // Second super-block of the stage row: its qs start at
+                    // byte 144, 16-byte aligned, so one 16-byte load per
+                    // sub-block (half the shared-memory wavefronts of two
+                    // 8-byte loads at this row stride; measured 1-4% faster
+                    // at MT = 80 and 96, no gain at smaller tiles).
 #pragma unroll
-                for (int u = 0; u < C::kU; ++u) {
-                    const uint2 a = *reinterpret_cast<const uint2*>(blk + 8 + 16 * (j + u));
-                    const uint2 b = *reinterpret_cast<const uint2*>(blk + 16 + 16 * (j + u));
-                    q[u][0] = a.x; q[u][1] = a.y; q[u][2] = b.x; q[u][3] = b.y;
+                    for (int u = 0; u < C::kU; ++u) {
+                        const uint4 a = *reinterpret_cast<const uint4*>(blk + 8 + 16 * (j + u));
+                        q[u][0] = a.x; q[u][1] = a.y; q[u][2] = a.z; q[u][3] = a.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < C::kU; ++u) {
+                        const uint2 a = *reinterpret_cast<const uint2*>(blk + 8 + 16 * (j + u));
+                        const uint2 b = *reinterpret_cast<const uint2*>(blk + 16 + 16 * (j + u));
+                        q[u][0] = a.x; q[u][1] = a.y; q[u][2] = b.x; q[u][3] = b.y;
+                    }
                 }
 #pragma unroll
                 for (int u = 0; u < C::kU; ++u) Sw[u] = iq4xs_scale(hdr.x, hdr.y, j + u);
