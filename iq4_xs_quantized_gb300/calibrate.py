@@ -5,8 +5,9 @@ M=8 while the measured crossover sat near M=15 (V100TPS engine page, mmvq vs
 dequantize table).  Here the crossover is measured: for every M in 1..16 and
 every calibration shape, both kernel paths are timed from CUDA-graph replays
 over rotating weight copies (inputs larger than L2); the dispatcher's
-threshold becomes the largest M at which the dp4a path is faster summed over
-the shapes.  The result is written to ``dispatch_table.json`` beside this file
+threshold becomes the largest M at which the dp4a path costs less summed over
+the shapes, each shape's times taken relative to the faster path there (so
+that every shape counts alike, not the one with the most bytes).  The result is written to ``dispatch_table.json`` beside this file
 and installed with ``iq4xs_set_crossover`` whenever the binding loads.
 
 Run on the GPU:  python -m iq4_xs_quantized_gb300.calibrate
@@ -64,7 +65,6 @@ def calibrate(shapes=SHAPES, ms=MS, verbose=True):
     from . import synth
     rng = np.random.default_rng(123)
     per_shape = {}
-    total = {M: {"dp4a": 0.0, "tc": 0.0} for M in ms}
     for N, K in shapes:
         w = torch.from_numpy(synth.iq4xs_weights(rng, N, K, 1e-3)).cuda()
         ncopy = max(2, int(np.ceil(L2_MULTIPLE * L2_BYTES / w.numel())))
@@ -74,24 +74,36 @@ def calibrate(shapes=SHAPES, ms=MS, verbose=True):
             t_dp = time_path(B, torch, wcopies, N, K, M, B.PATH_DP4A)
             t_tc = time_path(B, torch, wcopies, N, K, M, B.PATH_TC)
             rows[M] = {"dp4a_us": round(t_dp, 3), "tc_us": round(t_tc, 3)}
-            total[M]["dp4a"] += t_dp
-            total[M]["tc"] += t_tc
             if verbose:
                 print(f"N={N} K={K} M={M}: dp4a {t_dp:.2f} us  tc {t_tc:.2f} us", flush=True)
         per_shape[f"{N}x{K}"] = rows
         del wcopies, w
         torch.cuda.empty_cache()
+    table = {"crossover_m_max_dp4a": crossover_from(per_shape, ms), "gpu": torch.cuda.get_device_name(),
+             "shapes": per_shape, "rule": CROSSOVER_RULE}
+    return table
+
+
+CROSSOVER_RULE = ("largest M (scanning up from 1) at which the dp4a path costs less than the "
+                  "tcgen05 path summed over the calibration shapes, each shape's time relative "
+                  "to the faster path at that shape and M")
+
+
+def crossover_from(per_shape, ms):
+    """The dispatcher threshold from per-shape timings {shape: {M: {"dp4a_us", "tc_us"}}}."""
     crossover = 0
     for M in ms:
-        if total[M]["dp4a"] < total[M]["tc"]:
+        rel = {"dp4a": 0.0, "tc": 0.0}
+        for rows in per_shape.values():
+            r = rows.get(M, rows.get(str(M)))
+            best = min(r["dp4a_us"], r["tc_us"])
+            rel["dp4a"] += r["dp4a_us"] / best
+            rel["tc"] += r["tc_us"] / best
+        if rel["dp4a"] < rel["tc"]:
             crossover = M
         else:
             break
-    table = {"crossover_m_max_dp4a": crossover, "gpu": torch.cuda.get_device_name(),
-             "shapes": per_shape,
-             "rule": "largest M (scanning up from 1) at which the dp4a path is faster "
-                     "summed over the calibration shapes"}
-    return table
+    return crossover
 
 
 def _graph_time(torch, fn, reps=10):

@@ -100,8 +100,9 @@ struct TcCfg {
     // issuers, TMA producer, tensor-memory owner) and the epilogue warpgroup.
     // Three groups at MT = 16 (more independent decode streams per SM
     // sub-partition: the decoders are latency-bound there; measured 4-11%
-    // faster); at MT >= 32 a third group measured 5-17% slower.
-    static constexpr int kDecGroups = (MT <= 16) ? 3 : 2;
+    // faster) and at MT = 48 (1-3% faster); at MT = 32 and MT >= 64 a third
+    // group measured 9-15% slower, and a fourth at MT = 16 2% slower.
+    static constexpr int kDecGroups = (MT <= 16 || MT == 48) ? 3 : 2;
     static constexpr int kDecWarps = 4 * kDecGroups;
     static constexpr int kMmaWarp0 = kDecWarps;       // MMA issuers (even / odd units)
     static constexpr int kProducerWarp = kDecWarps + 1;
@@ -121,7 +122,7 @@ struct TcCfg {
     // the registers of 65536 / kThreads per thread (rounded down to 8); the
     // budgets, 128 threads each, must sum within that.
     static constexpr int kRegsLaunch = (65536 / kThreads) / 8 * 8;
-    static constexpr int kRegsDecode = (kEpiGroups == 2) ? (MT >= 64 ? 72 : 80) : (kDecGroups == 3) ? 88 : 96;
+    static constexpr int kRegsDecode = (kEpiGroups == 2) ? ((MT >= 64 || kDecGroups == 3) ? 72 : 80) : (kDecGroups == 3) ? 88 : 96;
     static constexpr int kRegsControl = 56;
     static constexpr int kRegsEpiFree =
         ((kThreads / 128) * kRegsLaunch - kDecGroups * kRegsDecode - kRegsControl) / kEpiGroups / 8 * 8;
