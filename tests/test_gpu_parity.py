@@ -117,7 +117,11 @@ def test_matmul_ragged_n(path, N):
         run_and_gate(w, N, 1024, x, path)
 
 
-@pytest.mark.parametrize("K", (512, 1536, 2560, 5120, 7168))
+# With 3 row tiles every split fits one wave, so the tcgen05 path takes the
+# largest useful split: K = 512 / 1536 / 2560 / 3072 / 3584 / 4096 give
+# clusters of 1 / 3 / 5 / 6 / 7 / 8 (uneven row shares of the split-K
+# reduction at 3, 5, 6, 7), 5120 and 7168 clusters of 5 and 7.
+@pytest.mark.parametrize("K", (512, 1536, 2560, 3072, 3584, 4096, 5120, 7168))
 @pytest.mark.parametrize("path", PATHS)
 def test_matmul_k_variants(K, path):
     rng = np.random.default_rng(K)
