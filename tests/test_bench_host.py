@@ -79,3 +79,32 @@ def test_traffic_record_is_ignored_when_kernels_change(tmp_path, monkeypatch):
     p.write_text(f"kernel_source_sha256_16: {bench.kernel_source_hash()}\n"
                  "dram_bytes_per_tc_launch_mean: 123\n")
     assert bench.recorded_traffic() == 123.0
+
+
+def test_crossover_rule_weighs_shapes_alike():
+    """The dispatcher threshold: the largest M (scanning up from 1) at which
+    dp4a costs less summed over shapes, each shape's time relative to the
+    faster path there.  A shape with many bytes must not outvote the others
+    by its absolute microseconds."""
+    from iq4_xs_quantized_gb300 import calibrate
+    def row(dp, tc):
+        return {"dp4a_us": dp, "tc_us": tc}
+    per_shape = {
+        # small shape: dp4a clearly faster through M = 4
+        "small": {1: row(3.5, 7.4), 2: row(4.4, 7.4), 3: row(5.7, 7.4), 4: row(5.8, 7.4), 5: row(12.0, 7.4)},
+        # large shape: tcgen05 ahead from M = 3 by more absolute microseconds
+        # than dp4a gains on the small one
+        "large": {1: row(20.8, 27.5), 2: row(25.4, 27.5), 3: row(30.2, 27.5), 4: row(30.9, 27.5),
+                  5: row(71.4, 27.5)},
+        "mid": {1: row(12.6, 21.9), 2: row(15.4, 21.9), 3: row(19.7, 22.0), 4: row(20.3, 22.0),
+                5: row(35.0, 22.0)},
+    }
+    assert calibrate.crossover_from(per_shape, range(1, 6)) == 4
+    # absolute sums would have stopped at M = 3 (dp4a 55.6 vs tcgen05 56.9 us; at M = 4 57.0 vs 56.9)
+    total = {M: [sum(v[M][k] for v in per_shape.values()) for k in ("dp4a_us", "tc_us")] for M in range(1, 6)}
+    assert total[4][0] > total[4][1] and total[3][0] < total[3][1]
+    # string keys (as read back from the JSON table) work the same way
+    as_json = {k: {str(m): r for m, r in v.items()} for k, v in per_shape.items()}
+    assert calibrate.crossover_from(as_json, range(1, 6)) == 4
+    # dp4a never faster -> 0
+    assert calibrate.crossover_from({"s": {1: row(9.0, 7.0)}}, range(1, 2)) == 0
