@@ -188,6 +188,7 @@ struct TcCfg {
 };
 
 constexpr int kEpilogueBarrier = 1;  // named barriers 1, 2: the 4 warps of epilogue group 0, 1
+__device__ volatile int g_never_abort = 0;  // an abort flag that is never set
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -723,7 +724,10 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                                   (uint32_t)((q1 - q0) * C::kRedStride * 4), smem_u32(recv_bar), (uint32_t)q);
             }
         }
-        mbar_wait(recv_bar, 0, abort_flag, err, kDevErrTimeoutRecv);
+        // Every rank sends its slices whatever its state, so this wait does
+        // not stop early on an abort (bounded all the same): no copy may
+        // land in this CTA's shared memory after it exits.
+        mbar_wait(recv_bar, 0, &g_never_abort, err, kDevErrTimeoutRecv);
         __syncwarp();
         cluster_arrive_relaxed();  // phase 2: this rank's slices have landed
         if (warp < kDecWarps || warp >= kEpiWarp0) {
