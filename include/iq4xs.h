@@ -18,6 +18,14 @@
  * ----------------------------------------
  *  - All data pointers are DEVICE pointers owned by the caller.  The library
  *    never allocates, frees or retains them, and allocates nothing per call.
+ *    Exception: the activations x (iq4xs_quantize_q8_1, iq4xs_linear) and
+ *    the result y (iq4xs_matmul, iq4xs_linear) may instead be HOST memory
+ *    the device can address -- page-locked host memory under unified
+ *    addressing (cudaHostAlloc, cudaHostRegister), whose pointer is the
+ *    device pointer -- in which case the quantizer reads x and the matmul
+ *    writes y over the host-device link (NVLink-C2C on Grace-Blackwell)
+ *    with no staging copy; results are bit-identical to device buffers.
+ *    The library does not check which kind of memory it was given.
  *    A one-time per-device set-up (architecture check, the tensor-map encoder
  *    entry point, kernel attributes) runs on the first call made on a device.
  *  - `stream` is a cudaStream_t passed as an int64 (0 = legacy default

@@ -114,3 +114,24 @@ def test_linear_baseline_route_only_when_asked():
     scale = np.abs(ref).max(axis=1, keepdims=True)
     err = np.abs(yb[:, rows] - ref) / scale
     assert 0 < err.max() < 5e-2, err.max()
+
+
+@pytest.mark.parametrize("M", (1, 4, 16, 96))
+def test_linear_on_pinned_host_buffers_is_bitwise_device(M):
+    """x read from and y written to page-locked host memory by the kernels
+    (the e2e form of the benchmark): bit-identical to device buffers, on
+    both paths, with a ragged N tail and split K."""
+    B.iq4xs_set_crossover(4)
+    N, K = 1000, 4096
+    rng = np.random.default_rng([77, M])
+    w = dev(synth.iq4xs_weights(rng, N, K, 1e-3))
+    x = synth.activations(rng, M, K, outlier_frac=0.01)
+    ws = torch.empty((B.iq4xs_linear_workspace_bytes(M, N, K),), dtype=torch.uint8, device="cuda")
+    yd = torch.full((M, N), float("nan"), device="cuda")
+    B.iq4xs_linear(w, N, K, dev(x), yd, ws)
+    hx = torch.from_numpy(x).pin_memory()
+    hy = torch.full((M, N), float("nan")).pin_memory()
+    B.iq4xs_linear(w, N, K, hx, hy, ws)
+    torch.cuda.synchronize()
+    assert gate_written(hy.numpy()) is None
+    assert np.array_equal(hy.numpy().view(np.uint32), yd.cpu().numpy().view(np.uint32))
