@@ -299,8 +299,12 @@ int iq4xs_set_pdl(int enable);
 
 /*
  * Read and clear the current device's error word, written by kernels whose
- * bounded waits ran out (IQ4XS_ERR_TIMEOUT) or that saw an impossible
- * state.  Synchronizes the current device.  *code_out = 0 when clean.
+ * bounded waits (2 s each) ran out or that saw an impossible state.
+ * Synchronizes the current device.  *code_out = 0 when clean, else the code
+ * of the last wait that ran out, in the tensor-core matmul:
+ *   0x101 a W stage      0x102 an activation stage   0x103 a decoded unit
+ *   0x104 a unit's MMAs  0x105 a free unit slot      0x106 the final drain
+ *   0x107 the split-K slices of the other cluster ranks.
  */
 int iq4xs_last_device_error(int* code_out);
 
