@@ -292,7 +292,7 @@ def run_ours(args, world, rank, local):
     wd0 = torch.from_numpy(w_np).to(dev)
     wcopies = [wd0] + [wd0.clone() for _ in range(N_COPIES - 1)]
     xs = {M: torch.from_numpy(np.ascontiguousarray(x_np[:M])).to(dev) for M in ms}
-    acts = {M: B.alloc_activations(M, K, dev, tc=True) for M in ms}
+    acts = {M: B.alloc_activations(M, K, dev) for M in ms}
     ys = {M: torch.empty((M, N), dtype=torch.float32, device=dev) for M in ms}
     paths = {M: kernel_path(B, M, N, K) for M in ms}
     variants = N_COPIES // len(ms)
@@ -300,10 +300,9 @@ def run_ours(args, world, rank, local):
 
     def launch_step(v):
         for i, M in enumerate(ms):
-            qs, ds, op = acts[M]
-            # the tensor-core operand is written only for the path that reads it
-            B.iq4xs_quantize_q8_1(xs[M], qs, ds, op if paths[M] == B.PATH_TC else None, stream)
-            B.iq4xs_matmul(wcopies[v * len(ms) + i], N, K, qs, ds, op, M, ys[M], paths[M], stream)
+            qs, ds = acts[M]
+            B.iq4xs_quantize_q8_1(xs[M], qs, ds, stream)
+            B.iq4xs_matmul(wcopies[v * len(ms) + i], N, K, qs, ds, M, ys[M], paths[M], stream)
 
     # Eager warm-up (also performs the library's one-time device set-up).
     with torch.cuda.stream(stream):
@@ -440,11 +439,11 @@ def matmul_only_times(torch, B, stream, ms, N, K, wcopies, acts, ys, paths, reps
     matmuls over the rotating weight copies."""
     out = {}
     for M in ms:
-        qs, ds, op = acts[M]
+        qs, ds = acts[M]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for w in wcopies:
-                B.iq4xs_matmul(w, N, K, qs, ds, op, M, ys[M], paths[M], stream)
+                B.iq4xs_matmul(w, N, K, qs, ds, M, ys[M], paths[M], stream)
         with torch.cuda.stream(stream):
             g.replay()
             t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -509,14 +508,14 @@ def decode_stream(torch, B, dev, reps=5):
         for l in range(W.layers):
             for i, (N, K) in enumerate(W.shapes):
                 x = torch.randn((M, K), device=dev, generator=g)
-                qs, ds, op = B.alloc_activations(M, K, dev, tc=True)
+                qs, ds = B.alloc_activations(M, K, dev)
                 y = torch.empty((M, N), dtype=torch.float32, device=dev)
-                calls.append((layers[l][i], N, K, x, qs, ds, op, y, kernel_path(B, M, N, K)))
+                calls.append((layers[l][i], N, K, x, qs, ds, y, kernel_path(B, M, N, K)))
 
         def step():
-            for (w, N, K, x, qs, ds, op, y, path) in calls:
-                B.iq4xs_quantize_q8_1(x, qs, ds, op if path == B.PATH_TC else None, stream)
-                B.iq4xs_matmul(w, N, K, qs, ds, op, M, y, path, stream)
+            for (w, N, K, x, qs, ds, y, path) in calls:
+                B.iq4xs_quantize_q8_1(x, qs, ds, stream)
+                B.iq4xs_matmul(w, N, K, qs, ds, M, y, path, stream)
         with torch.cuda.stream(stream):
             step()
         torch.cuda.synchronize()
@@ -559,21 +558,21 @@ def moe_grouped(torch, B, dev, layers=12, reps=5):
         M = rows.shape[0]
         xr = torch.from_numpy(rows).to(dev)
         off = torch.from_numpy(offsets).to(dev)
-        qs, ds, _ = B.alloc_activations(M, W.K, dev, tc=False)
+        qs, ds = B.alloc_activations(M, W.K, dev)
         y = torch.empty((M, W.N), dtype=torch.float32, device=dev)
         touched = [g for g in range(W.G) if offsets[g + 1] > offsets[g]]
 
         def grouped(s):
             for w in ws:
-                B.iq4xs_quantize_q8_1(xr, qs, ds, None, s)
+                B.iq4xs_quantize_q8_1(xr, qs, ds, s)
                 B.iq4xs_matmul_grouped(w, stride, W.G, W.N, W.K, qs, ds, off, y, s)
 
         def per_expert(s):
             for w in ws:
-                B.iq4xs_quantize_q8_1(xr, qs, ds, None, s)
+                B.iq4xs_quantize_q8_1(xr, qs, ds, s)
                 for g in touched:
                     r0, r1 = int(offsets[g]), int(offsets[g + 1])
-                    B.iq4xs_matmul(w[g], W.N, W.K, qs[r0:r1], ds[r0:r1], None, r1 - r0, y[r0:r1],
+                    B.iq4xs_matmul(w[g], W.N, W.K, qs[r0:r1], ds[r0:r1], r1 - r0, y[r0:r1],
                                    B.PATH_DP4A, s)
 
         times = {}
@@ -624,13 +623,13 @@ def weight_formats(torch, B, dev, stream, iq4xs_us, N=4096, K=4096, copies=48, r
         rng = np.random.default_rng(8)
         for M in ms:
             x = torch.from_numpy(synth.activations(rng, M, K)).to(dev)
-            qs, ds, op = B.alloc_activations(M, K, dev, tc=True)
-            B.iq4xs_quantize_q8_1(x, qs, ds, op, stream)
+            qs, ds = B.alloc_activations(M, K, dev)
+            B.iq4xs_quantize_q8_1(x, qs, ds, stream)
             y = torch.empty((M, N), dtype=torch.float32, device=dev)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for w in ws:
-                    B.iq4xs_matmul_wt(w, wt, N, K, qs, ds, op, M, y, B.PATH_AUTO, stream)
+                    B.iq4xs_matmul_wt(w, wt, N, K, qs, ds, M, y, B.PATH_AUTO, stream)
             with torch.cuda.stream(stream):
                 g.replay()
                 t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -692,12 +691,12 @@ def decoder_shapes(torch, B, dev, stream, reps=10):
         for M in W.ms:
             path = kernel_path(B, M, N, K)
             x = torch.from_numpy(np.ascontiguousarray(x_np[:M])).to(dev)
-            qs, ds, op = B.alloc_activations(M, K, dev, tc=(path == B.PATH_TC))
-            B.iq4xs_quantize_q8_1(x, qs, ds, op, stream)
+            qs, ds = B.alloc_activations(M, K, dev)
+            B.iq4xs_quantize_q8_1(x, qs, ds, stream)
 
             def mm():
                 for w in ws:
-                    B.iq4xs_matmul(w, N, K, qs, ds, op, M, y, path, stream)
+                    B.iq4xs_matmul(w, N, K, qs, ds, M, y, path, stream)
             us = _graph_us(torch, stream, mm, len(ws), reps)
             gbs = matmul_bytes(M, N, K) / (us * 1e-6) / 1e9
             res.append({"N": N, "K": K, "M": M, "path": "dp4a" if path == B.PATH_DP4A else "tc",
@@ -723,13 +722,13 @@ def prefill_sweep(torch, B, dev, stream, reps=3):
         for M in W.ms:
             x = torch.from_numpy(np.ascontiguousarray(x_np[:M])).to(dev)
             xb = x.to(torch.bfloat16)
-            qs, ds, op = B.alloc_activations(M, K, dev, tc=True)
+            qs, ds = B.alloc_activations(M, K, dev)
             y = torch.empty((M, N), dtype=torch.float32, device=dev)
 
             def tc():
                 for w in ws:
-                    B.iq4xs_quantize_q8_1(x, qs, ds, op, stream)
-                    B.iq4xs_matmul(w, N, K, qs, ds, op, M, y, B.PATH_TC, stream)
+                    B.iq4xs_quantize_q8_1(x, qs, ds, stream)
+                    B.iq4xs_matmul(w, N, K, qs, ds, M, y, B.PATH_TC, stream)
 
             def base():
                 for w in ws:

@@ -6,8 +6,8 @@
  *
  * W is IQ4_XS-quantized (136-byte super-blocks of 256 weights, 4.25 bits per
  * weight); x is quantized per 32 values to Q8_1 by iq4xs_quantize_q8_1 and the
- * product is formed from exact int32 per-32-weight dot products scaled into
- * fp32.  The method is the one described on the V100TPS engine page
+ * product is formed from exact integer per-32-weight dot products, each
+ * scaled by d_w*(ls-32)*d_x and accumulated in fp32.  The method is the one described on the V100TPS engine page
  * (agent-report.daedalus.work/V100TPS/engine.html): the kernel table at M=64
  * (quantize_q8_1 feeding the batched matmul), the new-kernel table (batched
  * IQ4_XS for 4 <= M <= 96) and the tile-geometry passage after it (sub-block
@@ -56,11 +56,8 @@
  *  Q8_1 activations (structure of arrays):
  *      qs  int8  [M][K]     q = round(x/d), ties away from zero
  *      ds  half2 [M][K/32]  {d = amax/127, s = d*sum(q)} each rounded to fp16
- *  Tensor-core operand (opaque, produced by iq4xs_quantize_q8_1 when asked):
- *      each value q*d (d the block's stored fp16 scale) held exactly as a
- *      pair of fp16 values, tiled for the tcgen05 path; size
- *      iq4xs_tc_operand_bytes(M, K) = 4 * Mpad * K bytes (Mpad = M rounded up
- *      to the tile height), 16-byte aligned.
+ *      Both matmul paths read these two arrays as they are (1.125 bytes per
+ *      activation); qs must be 16-byte aligned, ds 4-byte aligned.
  *  y: fp32 [M][ldy] row-major, ldy >= N; columns N..ldy-1 are not written.
  */
 #ifndef IQ4XS_H
@@ -86,8 +83,8 @@ typedef enum {
 typedef enum {
     IQ4XS_PATH_AUTO = 0,    /* iq4xs_select_path decides from (M, N, K)          */
     IQ4XS_PATH_DP4A = 1,    /* CUDA-core int8 dot products (small M)             */
-    IQ4XS_PATH_TC = 2,      /* tcgen05 tensor cores, exact fp16 operand products,
-                               per-sub-block fp32 scale-in (larger M)            */
+    IQ4XS_PATH_TC = 2,      /* tcgen05 tensor cores: exact integer sub-block dots
+                               in fp32 tensor memory, fp32 scale-in (larger M)   */
     IQ4XS_PATH_BASELINE = 3 /* advice from iq4xs_select_path only: above a
                                measured M, dequantizing W (iq4xs_dequantize) and
                                a dense bf16 GEMM in the caller's BLAS is faster,
@@ -126,38 +123,34 @@ int64_t iq4xs_weight_bytes(int wtype, int64_t N, int64_t K);
  *   x           fp32 [M][ldx], ldx >= K, 4-byte aligned, ldx*4 % 16 == 0 and
  *               x 16-byte aligned (rows are read as float4).
  *   qs, ds      outputs, layouts above; qs 16-byte aligned, ds 4-byte aligned.
- *   tc_operand  optional output (NULL to skip): the tensor-core operand for
- *               IQ4XS_PATH_TC, iq4xs_tc_operand_bytes(M, K) bytes, 16-byte
- *               aligned.  Padding rows inside it are written as zeros.
  * Per block of 32: amax = max|x|, d = amax/127 (IEEE fp32 division),
  * q = d == 0 ? 0 : roundf(x/d), s = d*sum(q); d and s stored as fp16 (RNE).
  * Inputs must be finite (NaN/Inf give unspecified codes).
  */
 int iq4xs_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx,
-                        int8_t* qs, void* ds, void* tc_operand, int64_t stream);
-
-/* Bytes of the tensor-core operand for (M, K); 0 if the shape is invalid. */
-int64_t iq4xs_tc_operand_bytes(int64_t M, int64_t K);
+                        int8_t* qs, void* ds, int64_t stream);
 
 /*
  * Batched matmul y = x . W^T from IQ4_XS W and Q8_1 x (engine page,
  * new-kernel table and tile-geometry passage: per-32 sub-block integer dot
  * products scaled by d_w*(ls-32)*d_x into fp32).
- *   w           IQ4_XS [N][K/256] blocks, 16-byte aligned.
- *   qs, ds      Q8_1 activations from iq4xs_quantize_q8_1 (DP4A path).
- *   tc_operand  tensor-core operand from iq4xs_quantize_q8_1 (TC path);
- *               may be NULL when the chosen path is DP4A.
- *   y           fp32 [M][ldy] output, fully overwritten for columns < N.
- *   path        an iq4xs_path value.  AUTO asks iq4xs_select_path.
+ *   w       IQ4_XS [N][K/256] blocks, 16-byte aligned.
+ *   qs, ds  Q8_1 activations as iq4xs_quantize_q8_1 writes them (qs 16-byte,
+ *           ds 4-byte aligned), read on either path.
+ *   M       activation rows; y fp32 [M][ldy] output, fully overwritten for
+ *           columns < N.
+ *   path    an iq4xs_path value: AUTO (the choice iq4xs_select_path makes),
+ *           DP4A or TC; BASELINE is advice only and returns IQ4XS_ERR_ARG.
  * The TC path needs K % 512 == 0 (super-blocks are staged in pairs so every
- * tensor-memory copy starts on a 16-byte boundary) and a non-NULL
- * tc_operand; otherwise it returns IQ4XS_ERR_SHAPE / IQ4XS_ERR_ARG.
- * Result: fp32 accumulation of exact integer sub-block dots; it differs from
- * the fp64 definition by fp32 rounding only.
+ * copy starts on a 16-byte boundary), else IQ4XS_ERR_SHAPE.
+ * Result: each sub-block's dot sum_i kv*q is an exact integer on both paths
+ * (int32 on DP4A; on TC exact in the tensor core's fp32 accumulator, every
+ * partial sum being an integer below 2^24); the scaled sub-block terms are
+ * accumulated in fp32, so y differs from the fp64 definition by fp32
+ * rounding and summation order only.
  */
 int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds,
-                 const void* tc_operand, int64_t M, float* y, int64_t ldy, int path,
-                 int64_t stream);
+                 int64_t M, float* y, int64_t ldy, int path, int64_t stream);
 
 /*
  * iq4xs_matmul for a weight in any iq4xs_wtype (IQ4XS_WTYPE_IQ4_XS is
@@ -169,8 +162,7 @@ int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const vo
  * an unknown wtype.
  */
 int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t* qs,
-                    const void* ds, const void* tc_operand, int64_t M, float* y, int64_t ldy,
-                    int path, int64_t stream);
+                    const void* ds, int64_t M, float* y, int64_t ldy, int path, int64_t stream);
 
 /*
  * Grouped (mixture-of-experts) matmul in one launch: G experts, each with its
@@ -209,9 +201,9 @@ int iq4xs_matmul_grouped(const void* w, int64_t expert_stride, int64_t G, int64_
  * (programmatic dependent launch).
  *   x          fp32 [M][ldx], as for iq4xs_quantize_q8_1.
  *   workspace  device scratch owned by the caller, 16-byte aligned, at least
- *              iq4xs_linear_workspace_bytes(M, N, K) bytes; its contents on
- *              return are the Q8_1 activations (qs, then ds, then the
- *              tensor-core operand when that path is taken).
+ *              iq4xs_linear_workspace_bytes(M, N, K) bytes (M*K bytes of qs
+ *              rounded up to 16, then M*K/32*4 bytes of ds rounded up to 16);
+ *              its contents on return are those Q8_1 activations.
  * Errors as for the two calls it makes; IQ4XS_ERR_ARG if the workspace is
  * too small.
  */
@@ -233,9 +225,10 @@ int64_t iq4xs_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *   - Allocates nothing and calls no allocating routine.  The array is
  *     created when the library is loaded and every GPU that loads it holds
  *     it until the process exits.
- *   - Size limit: iq4xs_linear_workspace_bytes(M, N, K) must not exceed
- *     iq4xs_linear_static_max_bytes() (8 MiB: e.g. M <= 128 at K = 17408);
- *     larger requests return IQ4XS_ERR_SHAPE and launch nothing.
+ *   - Size limit: iq4xs_linear_workspace_bytes(M, N, K), about 1.125*M*K
+ *     bytes on either path, must not exceed iq4xs_linear_static_max_bytes()
+ *     (8 MiB: M <= 428 at K = 17408, M <= 1456 at K = 5120); larger
+ *     requests return IQ4XS_ERR_SHAPE and launch nothing.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before
  *     any stream capture.
@@ -269,7 +262,8 @@ int iq4xs_dequantize_wt(const void* w, int wtype, int64_t N, int64_t K, void* ou
  * original dispatcher hard-coded its threshold at M=8 while the measured
  * crossover was M~15; the dequantize + GEMM route was the choice above it).
  * Host only, no device access.  Returns DP4A when M <= the calibrated
- * crossover and the DP4A path applies; BASELINE when M >= the calibrated
+ * crossover for the matrix's size class (iq4xs_set_crossover_classes) and the
+ * DP4A path applies; BASELINE when M >= the calibrated
  * baseline threshold (0 = never); TC otherwise (TC requires K % 512 == 0).
  */
 int iq4xs_select_path(int64_t M, int64_t N, int64_t K, int* path_out);
@@ -279,6 +273,16 @@ int iq4xs_select_path(int64_t M, int64_t N, int64_t K, int* path_out);
  * Host only.  Defaults to 4 until a calibration sets it.  Thread-safe.
  */
 int iq4xs_set_crossover(int64_t m_max_dp4a);
+
+/*
+ * Install measured crossovers per weight-size class: for a matrix of N*K
+ * weights, the entry with the largest min_weights[i] <= N*K applies, and DP4A
+ * is chosen for M <= m_max_dp4a[i]; matrices below every entry use the value
+ * of iq4xs_set_crossover.  count = 0 clears the classes.  At most 16 entries,
+ * min_weights[i] >= 1, 0 <= m_max_dp4a[i] <= 32768, else IQ4XS_ERR_ARG and
+ * nothing changes.  Host only; the arrays are copied.  Thread-safe.
+ */
+int iq4xs_set_crossover_classes(const int64_t* min_weights, const int64_t* m_max_dp4a, int count);
 
 /*
  * Install the measured upper threshold: iq4xs_select_path answers BASELINE
@@ -299,14 +303,28 @@ int iq4xs_set_pdl(int enable);
 
 /*
  * Read and clear the current device's error word, written by kernels whose
- * bounded waits (2 s each) ran out or that saw an impossible state.
- * Synchronizes the current device.  *code_out = 0 when clean, else the code
- * of the last wait that ran out, in the tensor-core matmul:
+ * bounded waits (2 s each) ran out.  Synchronizes the current device.
+ * Returns IQ4XS_OK with *code_out = 0 when clean, IQ4XS_ERR_TIMEOUT with
+ * *code_out = the code of the last wait that ran out, in the tensor-core
+ * matmul:
  *   0x101 a W stage      0x102 an activation stage   0x103 a decoded unit
  *   0x104 a unit's MMAs  0x105 a free unit slot      0x106 the final drain
- *   0x107 the split-K slices of the other cluster ranks.
+ *   0x107 the split-K slices of the other cluster ranks
+ *   0x108 a stage of Q8_1 codes  0x109 a stage of activation scales.
+ * (0x102 is a code stage's MMAs completing, which frees its slot.)
  */
 int iq4xs_last_device_error(int* code_out);
+
+/*
+ * Test hook for the bounded waits (no counterpart on the source pages): the
+ * next tensor-core matmul launched after this call (on any thread) leaves W
+ * stage `stage` (0-based, in units of 512 weights of each CTA's K range) of
+ * every CTA unissued, so that the decoders' wait for it runs out after its
+ * 2 s limit.  That call's output is then undefined, every CTA still drains
+ * its copies and frees its tensor memory, and iq4xs_last_device_error
+ * reports IQ4XS_ERR_TIMEOUT with code 0x101.  -1 disarms.  Host only.
+ */
+int iq4xs_test_skip_w_stage(int64_t stage);
 
 /* Static string for a status code. */
 const char* iq4xs_status_string(int status);

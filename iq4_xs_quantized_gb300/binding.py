@@ -52,12 +52,10 @@ def load(path: str | None = None):
             raise RuntimeError(f"{p} is missing: build it with iq4_xs_quantized_gb300.build.build()")
         lib = ctypes.CDLL(p)
         i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
-        lib.iq4xs_quantize_q8_1.argtypes = [vp, i64, i64, i64, vp, vp, vp, i64]
-        lib.iq4xs_tc_operand_bytes.argtypes = [i64, i64]
-        lib.iq4xs_tc_operand_bytes.restype = i64
-        lib.iq4xs_matmul.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, i64, ci, i64]
+        lib.iq4xs_quantize_q8_1.argtypes = [vp, i64, i64, i64, vp, vp, i64]
+        lib.iq4xs_matmul.argtypes = [vp, i64, i64, vp, vp, i64, vp, i64, ci, i64]
         lib.iq4xs_dequantize.argtypes = [vp, i64, i64, vp, ci, i64]
-        lib.iq4xs_matmul_wt.argtypes = [vp, ci, i64, i64, vp, vp, vp, i64, vp, i64, ci, i64]
+        lib.iq4xs_matmul_wt.argtypes = [vp, ci, i64, i64, vp, vp, i64, vp, i64, ci, i64]
         lib.iq4xs_dequantize_wt.argtypes = [vp, ci, i64, i64, vp, ci, i64]
         lib.iq4xs_weight_bytes.argtypes = [ci, i64, i64]
         lib.iq4xs_weight_bytes.restype = i64
@@ -72,14 +70,17 @@ def load(path: str | None = None):
         lib.iq4xs_select_path.argtypes = [i64, i64, i64, ctypes.POINTER(ci)]
         lib.iq4xs_set_crossover.argtypes = [i64]
         lib.iq4xs_set_baseline_threshold.argtypes = [i64]
+        lib.iq4xs_set_crossover_classes.argtypes = [ctypes.POINTER(i64), ctypes.POINTER(i64), ci]
         lib.iq4xs_set_pdl.argtypes = [ci]
         lib.iq4xs_set_pdl.restype = ci
         lib.iq4xs_last_device_error.argtypes = [ctypes.POINTER(ci)]
+        lib.iq4xs_test_skip_w_stage.argtypes = [i64]
         lib.iq4xs_status_string.argtypes = [ci]
         lib.iq4xs_status_string.restype = ctypes.c_char_p
         for name in ("iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_matmul_grouped",
                      "iq4xs_dequantize", "iq4xs_linear", "iq4xs_matmul_wt", "iq4xs_dequantize_wt",
                      "iq4xs_select_path", "iq4xs_set_crossover", "iq4xs_set_baseline_threshold",
+                     "iq4xs_set_crossover_classes", "iq4xs_test_skip_w_stage",
                      "iq4xs_last_device_error"):
             getattr(lib, name).restype = ci
         if path is None:
@@ -95,8 +96,17 @@ def _install_calibration(lib):
     table = calibrate.load_table()
     if table and "crossover_m_max_dp4a" in table:
         lib.iq4xs_set_crossover(int(table["crossover_m_max_dp4a"]))
+    if table and "crossover_classes" in table:
+        _set_classes(lib, table["crossover_classes"])
     if table and "baseline_m_min" in table:
         lib.iq4xs_set_baseline_threshold(int(table["baseline_m_min"]))
+
+
+def _set_classes(lib, classes):
+    n = len(classes)
+    mins = (ctypes.c_int64 * max(n, 1))(*[int(c[0]) for c in classes])
+    ms = (ctypes.c_int64 * max(n, 1))(*[int(c[1]) for c in classes])
+    return lib.iq4xs_set_crossover_classes(mins, ms, n)
 
 
 def _check(fn: str, rc: int):
@@ -119,27 +129,21 @@ def _stream(stream) -> int:
 # --------------------------------------------------------------------------
 # Entry points (same names as the C ABI).
 # --------------------------------------------------------------------------
-def iq4xs_tc_operand_bytes(M: int, K: int) -> int:
-    return int(load().iq4xs_tc_operand_bytes(M, K))
-
-
-def iq4xs_quantize_q8_1(x, qs, ds, tc_operand=None, stream=None) -> None:
+def iq4xs_quantize_q8_1(x, qs, ds, stream=None) -> None:
     """x fp32 [M, K] (row stride x.stride(0)) -> qs int8 [M, K], ds fp16 [M, K/32, 2]
-    ({d, s}), optionally the tensor-core operand (uint8, iq4xs_tc_operand_bytes)."""
+    ({d, s})."""
     M, K = x.shape
-    rc = load().iq4xs_quantize_q8_1(_ptr(x), M, K, x.stride(0), _ptr(qs), _ptr(ds),
-                                    _ptr(tc_operand), _stream(stream))
+    rc = load().iq4xs_quantize_q8_1(_ptr(x), M, K, x.stride(0), _ptr(qs), _ptr(ds), _stream(stream))
     _check("iq4xs_quantize_q8_1", rc)
 
 
-def iq4xs_matmul(w, N: int, K: int, qs, ds, tc_operand, M: int, y, path=PATH_AUTO,
-                 stream=None) -> None:
+def iq4xs_matmul(w, N: int, K: int, qs, ds, M: int, y, path=PATH_AUTO, stream=None) -> None:
     """y fp32 [M, ldy] = x . W^T from IQ4_XS bytes w and Q8_1 activations."""
     if isinstance(path, str):
         path = PATHS[path]
     ldy = y.stride(0)
-    rc = load().iq4xs_matmul(_ptr(w), N, K, _ptr(qs), _ptr(ds), _ptr(tc_operand), M, _ptr(y),
-                             ldy, int(path), _stream(stream))
+    rc = load().iq4xs_matmul(_ptr(w), N, K, _ptr(qs), _ptr(ds), M, _ptr(y), ldy, int(path),
+                             _stream(stream))
     _check("iq4xs_matmul", rc)
 
 
@@ -151,14 +155,13 @@ def iq4xs_weight_bytes(wtype, N: int, K: int) -> int:
     return int(load().iq4xs_weight_bytes(_wtype(wtype), N, K))
 
 
-def iq4xs_matmul_wt(w, wtype, N: int, K: int, qs, ds, tc_operand, M: int, y, path=PATH_AUTO,
+def iq4xs_matmul_wt(w, wtype, N: int, K: int, qs, ds, M: int, y, path=PATH_AUTO,
                     stream=None) -> None:
     """iq4xs_matmul for weights in format ``wtype`` (WTYPE_* or its name)."""
     if isinstance(path, str):
         path = PATHS[path]
-    rc = load().iq4xs_matmul_wt(_ptr(w), _wtype(wtype), N, K, _ptr(qs), _ptr(ds),
-                                _ptr(tc_operand), M, _ptr(y), y.stride(0), int(path),
-                                _stream(stream))
+    rc = load().iq4xs_matmul_wt(_ptr(w), _wtype(wtype), N, K, _ptr(qs), _ptr(ds), M, _ptr(y),
+                                y.stride(0), int(path), _stream(stream))
     _check("iq4xs_matmul_wt", rc)
 
 
@@ -227,6 +230,11 @@ def iq4xs_set_crossover(m_max_dp4a: int) -> None:
     _check("iq4xs_set_crossover", load().iq4xs_set_crossover(int(m_max_dp4a)))
 
 
+def iq4xs_set_crossover_classes(classes) -> None:
+    """[(min_weights, m_max_dp4a), ...]: the crossover per weight-size class."""
+    _check("iq4xs_set_crossover_classes", _set_classes(load(), list(classes)))
+
+
 def iq4xs_set_baseline_threshold(m_min_baseline: int) -> None:
     _check("iq4xs_set_baseline_threshold", load().iq4xs_set_baseline_threshold(int(m_min_baseline)))
 
@@ -236,9 +244,17 @@ def iq4xs_set_pdl(enable: bool) -> None:
 
 
 def iq4xs_last_device_error() -> int:
+    """The device error word (0 = clean), read and cleared; a timeout code
+    (status IQ4XS_ERR_TIMEOUT) is returned, not raised."""
     out = ctypes.c_int(-1)
-    _check("iq4xs_last_device_error", load().iq4xs_last_device_error(ctypes.byref(out)))
+    rc = load().iq4xs_last_device_error(ctypes.byref(out))
+    if rc != ERR_TIMEOUT:
+        _check("iq4xs_last_device_error", rc)
     return out.value
+
+
+def iq4xs_test_skip_w_stage(stage: int) -> None:
+    _check("iq4xs_test_skip_w_stage", load().iq4xs_test_skip_w_stage(int(stage)))
 
 
 def iq4xs_status_string(status: int) -> str:
@@ -248,14 +264,11 @@ def iq4xs_status_string(status: int) -> str:
 # --------------------------------------------------------------------------
 # Buffer helpers (allocation by torch; the library allocates nothing).
 # --------------------------------------------------------------------------
-def alloc_activations(M: int, K: int, device="cuda", tc: bool = True):
-    """Q8_1 buffers for M x K activations: (qs, ds, tc_operand or None)."""
+def alloc_activations(M: int, K: int, device="cuda"):
+    """Q8_1 buffers for M x K activations: (qs int8 [M, K], ds fp16 [M, K/32, 2])."""
     qs = torch.empty((M, K), dtype=torch.int8, device=device)
     ds = torch.empty((M, K // 32, 2), dtype=torch.float16, device=device)
-    op = None
-    if tc:
-        op = torch.empty(iq4xs_tc_operand_bytes(M, K), dtype=torch.uint8, device=device)
-    return qs, ds, op
+    return qs, ds
 
 
 def linear(w, N: int, K: int, x, path=PATH_AUTO, stream=None, out=None, allow_baseline=False):
@@ -264,7 +277,7 @@ def linear(w, N: int, K: int, x, path=PATH_AUTO, stream=None, out=None, allow_ba
     With allow_baseline and the dispatcher advising BASELINE (M at or above
     the measured threshold), W is dequantized to bf16 by this library and the
     product is a dense bf16 GEMM (torch / cuBLAS): faster there, at bf16
-    precision rather than the exact-product Q8_1 paths' fp32 rounding."""
+    precision rather than the Q8_1 paths' exact sub-block dots."""
     M = x.shape[0]
     y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=x.device)
     if allow_baseline and path == PATH_AUTO and iq4xs_select_path(M, N, K) == PATH_BASELINE:
@@ -278,7 +291,7 @@ def linear(w, N: int, K: int, x, path=PATH_AUTO, stream=None, out=None, allow_ba
     if path == PATH_AUTO:
         sel = iq4xs_select_path(M, N, K)
         kpath = PATH_TC if sel == PATH_BASELINE else sel
-    qs, ds, op = alloc_activations(M, K, x.device, tc=(kpath == PATH_TC))
-    iq4xs_quantize_q8_1(x, qs, ds, op, stream)
-    iq4xs_matmul(w, N, K, qs, ds, op, M, y, kpath, stream)
+    qs, ds = alloc_activations(M, K, x.device)
+    iq4xs_quantize_q8_1(x, qs, ds, stream)
+    iq4xs_matmul(w, N, K, qs, ds, M, y, kpath, stream)
     return y

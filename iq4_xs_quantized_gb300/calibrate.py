@@ -21,7 +21,7 @@ import sys
 import numpy as np
 
 TABLE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "dispatch_table.json")
-SHAPES = ((4096, 4096), (5120, 5120), (12288, 5120), (5120, 17408))
+SHAPES = ((4096, 4096), (5120, 5120), (12288, 5120), (5120, 17408), (34816, 5120))
 MS = tuple(range(1, 17))
 # Upper threshold: the tcgen05 route (quantize + matmul) against dequantize
 # to bf16 + a dense bf16 GEMM, on the square and the two prefill shapes.
@@ -32,19 +32,19 @@ L2_BYTES = 129 * 2**20
 
 
 def time_path(B, torch, wcopies, N, K, M, path, reps=20):
-    qs, ds, op = B.alloc_activations(M, K, "cuda", tc=True)
+    qs, ds = B.alloc_activations(M, K, "cuda")
     x = torch.randn(M, K, device="cuda")
     y = torch.empty(M, N, device="cuda")
-    B.iq4xs_quantize_q8_1(x, qs, ds, op)
+    B.iq4xs_quantize_q8_1(x, qs, ds)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         for w in wcopies:
-            B.iq4xs_matmul(w, N, K, qs, ds, op, M, y, path, s)
+            B.iq4xs_matmul(w, N, K, qs, ds, M, y, path, s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         for w in wcopies:
-            B.iq4xs_matmul(w, N, K, qs, ds, op, M, y, path, s)
+            B.iq4xs_matmul(w, N, K, qs, ds, M, y, path, s)
     with torch.cuda.stream(s):
         g.replay()
     torch.cuda.synchronize()
@@ -80,7 +80,8 @@ def calibrate(shapes=SHAPES, ms=MS, verbose=True):
         del wcopies, w
         torch.cuda.empty_cache()
     table = {"crossover_m_max_dp4a": crossover_from(per_shape, ms), "gpu": torch.cuda.get_device_name(),
-             "shapes": per_shape, "rule": CROSSOVER_RULE}
+             "crossover_classes": class_crossovers(per_shape, ms),
+             "shapes": per_shape, "rule": CROSSOVER_RULE, "class_rule": CLASS_RULE}
     return table
 
 
@@ -104,6 +105,35 @@ def crossover_from(per_shape, ms):
         else:
             break
     return crossover
+
+
+CLASS_RULE = ("per weight-size class: each calibration shape's own crossover (largest M, "
+              "scanning up from 1, at which dp4a is faster on that shape); a shape's class "
+              "starts at the geometric mean of its weight count and the next smaller shape's")
+
+
+def shape_crossover(rows, ms):
+    """Largest M (scanning up from 1) at which dp4a beats tcgen05 on one shape."""
+    crossover = 0
+    for M in ms:
+        r = rows.get(M, rows.get(str(M)))
+        if r["dp4a_us"] < r["tc_us"]:
+            crossover = M
+        else:
+            break
+    return crossover
+
+
+def class_crossovers(per_shape, ms):
+    """[[min_weights, m_max_dp4a], ...] ascending, one class per calibration
+    shape above the smallest (the smallest shape's crossover is the default
+    for everything below the first class)."""
+    sizes = sorted((int(k.split("x")[0]) * int(k.split("x")[1]), k) for k in per_shape)
+    out = []
+    for i in range(1, len(sizes)):
+        lo = int(round((sizes[i - 1][0] * sizes[i][0]) ** 0.5))
+        out.append([lo, shape_crossover(per_shape[sizes[i][1]], ms)])
+    return out
 
 
 def _graph_time(torch, fn, reps=10):
@@ -145,13 +175,13 @@ def calibrate_baseline(shapes=BASE_SHAPES, ms=BASE_MS, verbose=True):
         rows = {}
         for M in ms:
             x = torch.randn(M, K, device="cuda")
-            qs, ds, op = B.alloc_activations(M, K, "cuda", tc=True)
+            qs, ds = B.alloc_activations(M, K, "cuda")
             y = torch.empty(M, N, device="cuda")
 
             def tc(s):
                 for ww in wcopies:
-                    B.iq4xs_quantize_q8_1(x, qs, ds, op, s)
-                    B.iq4xs_matmul(ww, N, K, qs, ds, op, M, y, B.PATH_TC, s)
+                    B.iq4xs_quantize_q8_1(x, qs, ds, s)
+                    B.iq4xs_matmul(ww, N, K, qs, ds, M, y, B.PATH_TC, s)
 
             def base(s):
                 for ww in wcopies:

@@ -32,6 +32,29 @@ DevState g_dev[kMaxDevices];
 std::atomic<int64_t> g_crossover{4};
 std::atomic<int64_t> g_baseline_min{0};  // 0 = never advise the dequantize + GEMM route
 std::atomic<int> g_pdl{1};
+std::atomic<int> g_skip_w_stage{-1};  // armed by iq4xs_test_skip_w_stage, one launch
+
+// Measured crossover per weight-size class: entry i applies to matrices of
+// at least g_class_min[i] weights (N*K), the largest such entry winning;
+// matrices below every entry use g_crossover.
+constexpr int kMaxClasses = 16;
+std::mutex g_class_mu;
+int g_nclass = 0;
+int64_t g_class_min[kMaxClasses];
+int64_t g_class_m[kMaxClasses];
+
+int64_t crossover_for(int64_t N, int64_t K) {
+    const int64_t nk = N * K;
+    std::lock_guard<std::mutex> lock(g_class_mu);
+    int64_t m = g_crossover.load();
+    int64_t best = -1;
+    for (int i = 0; i < g_nclass; ++i)
+        if (g_class_min[i] <= nk && g_class_min[i] > best) {
+            best = g_class_min[i];
+            m = g_class_m[i];
+        }
+    return m;
+}
 
 // One-time per-device set-up, done with that device current.
 int device_state(DevState** out) {
@@ -76,9 +99,8 @@ inline int from_cuda(cudaError_t e) { return e == cudaSuccess ? IQ4XS_OK : IQ4XS
 
 // The path this library's own kernels take (DP4A or TC).
 int kernel_path_impl(int64_t M, int64_t N, int64_t K) {
-    (void)N;
     if (K % kPairK != 0) return IQ4XS_PATH_DP4A;  // TC stages super-blocks in pairs
-    return (M <= g_crossover.load()) ? IQ4XS_PATH_DP4A : IQ4XS_PATH_TC;
+    return (M <= crossover_for(N, K)) ? IQ4XS_PATH_DP4A : IQ4XS_PATH_TC;
 }
 // The advised path: the kernel path, or BASELINE above the measured threshold.
 int select_path_impl(int64_t M, int64_t N, int64_t K) {
@@ -97,24 +119,16 @@ using namespace iq4xs;
 
 extern "C" {
 
-int64_t iq4xs_tc_operand_bytes(int64_t M, int64_t K) {
-    if (M < 1 || M > kMaxM || K <= 0 || K % kQK) return 0;
-    return tc_operand_total_bytes(M, K);
-}
-
 int iq4xs_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, void* ds,
-                        void* tc_operand, int64_t stream) {
+                        int64_t stream) {
     if (!x || !qs || !ds) return IQ4XS_ERR_ARG;
     if (M < 1 || M > kMaxM || K <= 0 || K % kQK) return IQ4XS_ERR_SHAPE;
     if (ldx < K || (ldx * 4) % 16) return IQ4XS_ERR_ARG;
-    if (!aligned(x, 16) || !aligned(qs, 16) || !aligned(ds, 4) ||
-        (tc_operand && !aligned(tc_operand, 16)))
-        return IQ4XS_ERR_ALIGN;
+    if (!aligned(x, 16) || !aligned(qs, 16) || !aligned(ds, 4)) return IQ4XS_ERR_ALIGN;
     DevState* st;
     int rc = device_state(&st);
     if (rc) return rc;
-    return from_cuda(launch_quantize_q8_1(x, M, K, ldx, qs, ds, tc_operand,
-                                          reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_quantize_q8_1(x, M, K, ldx, qs, ds, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int64_t iq4xs_weight_bytes(int wtype, int64_t N, int64_t K) {
@@ -123,46 +137,38 @@ int64_t iq4xs_weight_bytes(int wtype, int64_t N, int64_t K) {
     return N * wt_row_bytes(wtype, K);
 }
 
-int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds,
-                 const void* tc_operand, int64_t M, float* y, int64_t ldy, int path,
-                 int64_t stream) {
-    return iq4xs_matmul_wt(w, IQ4XS_WTYPE_IQ4_XS, N, K, qs, ds, tc_operand, M, y, ldy, path,
-                           stream);
+int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds, int64_t M,
+                 float* y, int64_t ldy, int path, int64_t stream) {
+    return iq4xs_matmul_wt(w, IQ4XS_WTYPE_IQ4_XS, N, K, qs, ds, M, y, ldy, path, stream);
 }
 
 int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t* qs,
-                    const void* ds, const void* tc_operand, int64_t M, float* y, int64_t ldy,
-                    int path, int64_t stream) {
-    if (!w || !y) return IQ4XS_ERR_ARG;
+                    const void* ds, int64_t M, float* y, int64_t ldy, int path, int64_t stream) {
+    if (!w || !qs || !ds || !y) return IQ4XS_ERR_ARG;
     if (wtype < IQ4XS_WTYPE_IQ4_XS || wtype > IQ4XS_WTYPE_IQ4_NL) return IQ4XS_ERR_ARG;
     if (path < IQ4XS_PATH_AUTO || path > IQ4XS_PATH_TC) return IQ4XS_ERR_ARG;
     if (M < 1 || M > kMaxM || N < 1 || N > (1 << 30) || K <= 0 || K % kQK || K > (1 << 30))
         return IQ4XS_ERR_SHAPE;
     if (ldy < N) return IQ4XS_ERR_ARG;
-    if (!aligned(w, 16) || !aligned(y, 4)) return IQ4XS_ERR_ALIGN;
+    if (!aligned(w, 16) || !aligned(qs, 16) || !aligned(ds, 4) || !aligned(y, 4)) return IQ4XS_ERR_ALIGN;
     if (path == IQ4XS_PATH_AUTO) path = kernel_path_impl(M, N, K);
-    if (path == IQ4XS_PATH_TC) {
-        if (K % kPairK) return IQ4XS_ERR_SHAPE;
-        if (!tc_operand) return IQ4XS_ERR_ARG;
-        if (!aligned(tc_operand, 16)) return IQ4XS_ERR_ALIGN;
-    } else {
-        if (!qs || !ds) return IQ4XS_ERR_ARG;
-        if (!aligned(qs, 16) || !aligned(ds, 4)) return IQ4XS_ERR_ALIGN;
-    }
+    if (path == IQ4XS_PATH_TC && K % kPairK) return IQ4XS_ERR_SHAPE;
     DevState* st;
     int rc = device_state(&st);
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (path == IQ4XS_PATH_TC)
-        return from_cuda(launch_matmul_tc(w, wtype, N, K, tc_operand, M, y, ldy, st->encode,
-                                          st->err, st->num_sms, s));
+        return from_cuda(launch_matmul_tc(w, wtype, N, K, qs, ds, M, y, ldy, st->encode, st->err,
+                                          st->num_sms, g_skip_w_stage.exchange(-1), s));
     return from_cuda(launch_matmul_dp4a(w, wtype, N, K, qs, ds, M, y, ldy, st->num_sms, s));
 }
 
 namespace {
 inline int64_t align16(int64_t v) { return (v + 15) / 16 * 16; }
+// Workspace of iq4xs_linear: the Q8_1 codes, then (16-byte aligned) the
+// {d, s} pairs -- 1.125 bytes per activation on either path.
 struct LinearLayout {
-    int64_t qs, ds, op, total;
+    int64_t qs, ds, total;
     int path;
 };
 bool linear_layout(int64_t M, int64_t N, int64_t K, LinearLayout* L) {
@@ -171,8 +177,7 @@ bool linear_layout(int64_t M, int64_t N, int64_t K, LinearLayout* L) {
     L->path = kernel_path_impl(M, N, K);
     L->qs = 0;
     L->ds = align16(M * K);
-    L->op = L->ds + align16(M * (K / kSub) * 4);
-    L->total = L->op + (L->path == IQ4XS_PATH_TC ? tc_operand_total_bytes(M, K) : 0);
+    L->total = L->ds + align16(M * (K / kSub) * 4);
     return true;
 }
 }  // namespace
@@ -193,10 +198,9 @@ int iq4xs_linear(const void* w, int64_t N, int64_t K, const float* x, int64_t M,
     uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
     int8_t* qs = reinterpret_cast<int8_t*>(ws + L.qs);
     void* ds = ws + L.ds;
-    void* op = (L.path == IQ4XS_PATH_TC) ? ws + L.op : nullptr;
-    int rc = iq4xs_quantize_q8_1(x, M, K, ldx, qs, ds, op, stream);
+    int rc = iq4xs_quantize_q8_1(x, M, K, ldx, qs, ds, stream);
     if (rc) return rc;
-    return iq4xs_matmul(w, N, K, qs, ds, op, M, y, ldy, L.path, stream);
+    return iq4xs_matmul(w, N, K, qs, ds, M, y, ldy, L.path, stream);
 }
 
 int iq4xs_matmul_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
@@ -250,6 +254,20 @@ int iq4xs_set_crossover(int64_t m_max_dp4a) {
     return IQ4XS_OK;
 }
 
+int iq4xs_set_crossover_classes(const int64_t* min_weights, const int64_t* m_max_dp4a, int count) {
+    if (count < 0 || count > kMaxClasses) return IQ4XS_ERR_ARG;
+    if (count > 0 && (!min_weights || !m_max_dp4a)) return IQ4XS_ERR_ARG;
+    for (int i = 0; i < count; ++i)
+        if (min_weights[i] < 1 || m_max_dp4a[i] < 0 || m_max_dp4a[i] > kMaxM) return IQ4XS_ERR_ARG;
+    std::lock_guard<std::mutex> lock(g_class_mu);
+    for (int i = 0; i < count; ++i) {
+        g_class_min[i] = min_weights[i];
+        g_class_m[i] = m_max_dp4a[i];
+    }
+    g_nclass = count;
+    return IQ4XS_OK;
+}
+
 int iq4xs_set_baseline_threshold(int64_t m_min_baseline) {
     if (m_min_baseline < 0 || m_min_baseline > kMaxM + 1) return IQ4XS_ERR_ARG;
     g_baseline_min.store(m_min_baseline);
@@ -271,6 +289,13 @@ int iq4xs_last_device_error(int* code_out) {
     if (cudaMemcpyFromSymbol(code_out, g_device_error, sizeof(int)) != cudaSuccess ||
         cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess)
         return IQ4XS_ERR_CUDA;
+    return (*code_out >= kDevErrTimeoutW && *code_out <= kDevErrTimeoutX) ? IQ4XS_ERR_TIMEOUT
+                                                                           : IQ4XS_OK;
+}
+
+int iq4xs_test_skip_w_stage(int64_t stage) {
+    if (stage < -1 || stage > (1 << 20)) return IQ4XS_ERR_ARG;
+    g_skip_w_stage.store((int)stage);
     return IQ4XS_OK;
 }
 

@@ -130,30 +130,38 @@ __host__ __device__ inline int64_t tc_num_mtiles(int64_t M) {
     int mt = tc_mtile(M);
     return (M + mt - 1) / mt;
 }
-// Tensor-core operand: the dequantized activations v = q*d_h (d_h the
-// block's stored fp16 scale), times a power of two 2^-e per row and span of
-// kScaleSpan values, as a pair of fp16 values hi + lo: hi = fp16(v*2^-e),
-// lo = fp16(v*2^-e - hi).  q has 8 significant bits and d_h 11, so v has at
-// most 19 and the pair holds it exactly (lo keeps the low 8 bits) whenever
-// v*2^-e is a multiple of 2^-24.  e is the smallest e >= 0 with
-// 127 * max_span(d_h) * 2^-e < 65504: hi never overflows, e = 0 (every value
-// exact) unless the span's values reach the fp16 range, and otherwise only
-// blocks 2^14 times smaller than the span's largest lose low bits.  The
-// matmul scales its fp32 partial sums by 2^e (exact) per span.
-//   planes: [mtile][K/32 sub-block][plane hi, lo][4 chunks of 8 K][MT rows][8 fp16]
-//           (16 B per (chunk, row); a sub-block is 8*MT*16 bytes)
-//   then:   [mtile][ceil(K/kScaleSpan) span][MT rows] fp32 2^e
-// Within every sub-block the K order is permuted to (0,16,1,17,...,15,31):
-// K position 2i+h holds element i+16h, matching the decoded weight order.
-constexpr int kPlanes = 2;  // hi, lo
-__host__ __device__ inline int64_t tc_qh_bytes(int64_t M, int64_t K) {
-    return tc_num_mtiles(M) * (int64_t)tc_mtile(M) * K * 2 * kPlanes;
-}
-constexpr int kScaleSpan = 1024;                  // values per activation scale span
-constexpr int kSubPerSpan = kScaleSpan / kSub;     // 32 sub-blocks
-__host__ __device__ inline int64_t tc_num_spans(int64_t K) { return (K + kScaleSpan - 1) / kScaleSpan; }
-__host__ __device__ inline int64_t tc_operand_total_bytes(int64_t M, int64_t K) {
-    return tc_qh_bytes(M, K) + tc_num_mtiles(M) * tc_num_spans(K) * (int64_t)tc_mtile(M) * 4;
+// Activation operand of the tensor-core path, built inside the matmul from
+// the Q8_1 codes: each code q (|q| <= 127) as an exact fp16 integer, in the
+// K order of the decoded weights.  Within every sub-block K position 2i+h
+// holds element i+16h (one qs byte decodes to elements i and 16+i), so a
+// 16-byte chunk c (K positions 8c..8c+7) holds elements
+// (4c, 16+4c, 4c+1, 16+4c+1, ..., 4c+3, 16+4c+3).
+//   per sub-block: [4 chunks of 8 K][MT rows][8 fp16]  (16 B per (chunk, row))
+// The products kv*q are integers of magnitude <= 127*127 and a sub-block's
+// sum of 32 is at most 516,128 < 2^24, so the fp32 accumulator holds the
+// exact integer dot of the sub-block, whatever the summation order.
+constexpr int kQRowBytes = kBStageSubs * kSub;  // Q8_1 codes of one row per activation stage
+static_assert(kQRowBytes == 128, "one 128-byte swizzle row per activation row and stage");
+
+// Eight Q8_1 codes -> the 16-byte fp16 chunk above.  lo4 holds elements
+// 4c..4c+3 (one byte each), hi4 elements 16+4c..16+4c+3.  fp16 with bit
+// pattern 0x64XX is 1024 + XX, and q ^ 0x80 is q + 128 as an unsigned byte,
+// so each half is (1152 + q) - 1152 = q exactly.
+__device__ __forceinline__ uint4 q8x8_to_f16(uint32_t lo4, uint32_t hi4) {
+    const uint32_t ua = lo4 ^ 0x80808080u, ub = hi4 ^ 0x80808080u;
+    const uint32_t p01 = __byte_perm(ua, ub, 0x5140u);  // [a0, b0, a1, b1]
+    const uint32_t p23 = __byte_perm(ua, ub, 0x7362u);  // [a2, b2, a3, b3]
+    const uint32_t w[4] = {__byte_perm(p01, 0x64646464u, 0x4140u), __byte_perm(p01, 0x64646464u, 0x4342u),
+                           __byte_perm(p23, 0x64646464u, 0x4140u), __byte_perm(p23, 0x64646464u, 0x4342u)};
+    const uint32_t off_bits = 0x64806480u;  // half2(1152, 1152)
+    const __half2 off = *reinterpret_cast<const __half2*>(&off_bits);
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&w[k]), off);
+        o[k] = *reinterpret_cast<uint32_t*>(&v);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // ---------------------------------------------------------------------------
@@ -168,6 +176,8 @@ enum DeviceError : int {
     kDevErrTimeoutFree = 0x105,
     kDevErrTimeoutDrain = 0x106,
     kDevErrTimeoutRecv = 0x107,
+    kDevErrTimeoutQ = 0x108,
+    kDevErrTimeoutX = 0x109,
 };
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
 
@@ -239,9 +249,22 @@ __device__ __forceinline__ uint32_t f16x2_byte_entry(int j) {
     const uint32_t hi = __half_as_ushort(__int2half_rn(wt_nibble_value<WT>(j >> 4)));
     return lo | (hi << 16);
 }
+__device__ __forceinline__ void sts_u128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
     uint32_t v;
     asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+// As lds_u32, but ordered after earlier barrier waits (for data that a copy
+// or another warp writes while this kernel runs; lds_u32 is only for data
+// fixed since the block-wide barrier of set-up).
+__device__ __forceinline__ uint32_t lds_u32_ordered(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
 
@@ -815,7 +838,7 @@ __host__ __device__ constexpr uint32_t idesc_f16_m128(int n) {
 struct DevCtx;  // per-device state kept by api.cu
 
 cudaError_t launch_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs,
-                                 void* ds, void* tc_operand, cudaStream_t stream);
+                                 void* ds, cudaStream_t stream);
 cudaError_t launch_dequantize(const void* w, int wt, int64_t N, int64_t K, void* out,
                               int out_dtype, cudaStream_t stream);
 // num_sms picks the launch shape (grids of more than two CTAs per SM run
@@ -832,8 +855,11 @@ cudaError_t launch_matmul_dp4a_grouped(const void* w, int64_t expert_stride, int
 // Programmatic dependent launch on (default) or off for every launch.
 bool pdl_enabled();
 // `encode` is the driver's cuTensorMapEncodeTiled; `err` the device error word.
-cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const void* tc_operand,
-                             int64_t M, float* y, int64_t ldy, void* encode, int* err,
-                             int num_sms, cudaStream_t stream);
+// qs must be 16-byte aligned (its rows are staged by TMA).  skip_w_stage >= 0
+// leaves that W stage of every CTA unissued (tests of the bounded waits); -1
+// in every ordinary call.
+cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,
+                             const void* ds, int64_t M, float* y, int64_t ldy, void* encode,
+                             int* err, int num_sms, int skip_w_stage, cudaStream_t stream);
 
 }  // namespace iq4xs

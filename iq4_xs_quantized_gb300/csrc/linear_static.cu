@@ -64,8 +64,9 @@ int iq4xs_linear_static(const void* w, int64_t N, int64_t K, const float* x, int
     void* scratch = nullptr;
     const int rc = iq4xs::scratch_address(&scratch);
     if (rc) return rc;
-    // Every byte of the scratch that the matmul reads is written by the
-    // quantizer first (padding rows included), so nothing needs clearing.
+    // Every byte of the scratch that the matmul reads (the Q8_1 codes and
+    // scales of rows 0..M-1) is written by the quantizer first, so nothing
+    // needs clearing.
     return iq4xs_linear(w, N, K, x, M, ldx, y, ldy, scratch, iq4xs::kStaticScratchBytes, stream);
 }
 

@@ -1,53 +1,54 @@
 // matmul_tc.cu -- IQ4_XS x Q8_1 matmul on the 5th-generation tensor cores.
 //
 // Method (V100TPS engine page, new-kernel table and the tile-geometry passage
-// after it): per 32-weight sub-block, a dot product of decoded codebook
-// values with Q8_1 codes, scaled by d_w*(ls-32)*d_x into fp32.
+// after it): per 32-weight sub-block, an integer dot product of decoded
+// codebook values with Q8_1 codes, scaled by d_w*(ls-32)*d_x into fp32.
 //
-// GB300 design.  sm_103a has no integer tcgen05 kind, so the operands travel
-// as fp16: the codebook values kv (exact), and each activation's q*d_x as an
-// exact pair of fp16 values hi + lo (written by the quantizer).  Per K step
-// of 16 two MMAs accumulate kv*hi and kv*lo into the fp32 TMEM accumulator:
-// every product is exact (at most 8 + 11 significant bits), so a sub-block's
-// result d_x*sum(kv*q) differs from the exact one only by fp32 accumulation
-// rounding, and the epilogue needs no activation scale (one fp32 FMA per
-// element with d_w*(ls-32)).  One CTA owns 128 weight rows (= 128 TMEM lanes
-// = UMMA M) and an activation tile of MT rows (= UMMA N); K is split over a
-// cluster whose CTAs reduce their partial tiles through distributed shared
-// memory.
+// GB300 design.  sm_103a has no integer tcgen05 kind, so both operands
+// travel as fp16 holding small integers exactly: the codebook values kv and
+// the Q8_1 codes q.  Two MMAs (K = 16 each) per sub-block accumulate into
+// the sub-block's own fp32 TMEM accumulator; every product and every partial
+// sum is an integer below 2^24, so the accumulator holds the exact integer
+// dot P of the sub-block.  The epilogue scales it in: acc += (P*d_x)*Sw with
+// Sw = d_w*(ls-32).  One CTA owns 128 weight rows (= 128 TMEM lanes = UMMA M)
+// and an activation tile of MT rows (= UMMA N); K is split over a cluster
+// whose CTAs reduce their partial tiles through distributed shared memory.
+// The kernel reads the Q8_1 arrays (qs, ds) as the quantizer wrote them.
 //
-// Warp-specialized roles, each a loop over the CTA's units of kU sub-blocks,
-// decoupled by mbarrier rings (kNP slots of tensor memory: the decoded A
-// operand, 16 columns per sub-block; the accumulators, MT columns per
-// sub-block; the row scales, one column per sub-block).  Warp numbers below
-// are for two decoder groups (MT > 16); at MT = 16 a third group takes warps
-// 8-11 and the others move up by four:
+// Warp-specialized roles, each a loop over the CTA's work, decoupled by
+// mbarrier rings (kNP slots of tensor memory: the decoded A operand, 16
+// columns per sub-block; the accumulators, MT columns per sub-block; the row
+// scales, one column per sub-block).  Warp numbers are for two decoder
+// groups; at MT = 16 a third group takes warps 8-11 and the others move up:
 //   warps 0-7 (decoders)   G groups of four; group g takes units g, g+G,
-//                          ....  Warp w decodes rows 32(w%4)..+31 from
-//                          the staged W bytes to exact fp16 (one shared-
-//                          memory table lookup per qs byte for MT <= 96)
-//                          and stores them with tcgen05.st straight into
-//                          the A slot (row i in TMEM lane i), plus
-//                          d_w*(ls-32) into the scale column, then arrives
-//                          on the slot's a_full.
-//   warps 8, 11 (MMA)      warp-uniform loops over even / odd units; one
-//                          elected lane issues four tcgen05.mma 128 x MT x 16
-//                          (A from tensor memory, B hi / lo planes from
-//                          shared memory) per sub-block and commits.  Two
-//                          issuers keep the tensor pipe fed between their
-//                          own handshakes.
+//                          ....  Warp w decodes rows 32(w%4)..+31 from the
+//                          staged W bytes to exact fp16 (one shared-memory
+//                          table lookup per qs byte) and stores them with
+//                          tcgen05.st straight into the A slot (row i in
+//                          TMEM lane i), plus d_w*(ls-32) into the scale
+//                          column, then arrives on the slot's a_full.
+//   warps 8, 11 (MMA)      warp-uniform loops over even / odd units: the
+//                          warp builds its unit's B operand from the staged
+//                          Q8_1 codes (exact fp16, canonical K-major layout,
+//                          K-permuted like the decoded weights), then one
+//                          elected lane issues two tcgen05.mma 128 x MT x 16
+//                          (A from tensor memory, B from shared memory) per
+//                          sub-block and commits.
 //   warp 9 (producer)      TMA: W stages of 512 weights per row (2D tensor
 //                          map: one 128 x 272 B box of two IQ4_XS
 //                          super-blocks, or two 128 x 144 B boxes of eight
 //                          18-byte Q4_0 / IQ4_NL blocks each -- 144-byte rows
 //                          keep the decoders' shared-memory reads at 4-way
 //                          bank conflicts where 288-byte rows would be
-//                          8-way); activation stages of 4 sub-blocks (one
-//                          bulk copy of the pre-tiled fp16 hi / lo pairs).
-//   warp 10                allocates and frees tensor memory.
-//   warps 12-15 (epilogue) thread t reads row t's integer results and scale,
+//                          8-way); Q8_1 code stages of 4 sub-blocks (2D
+//                          tensor map over qs, MT rows x 128 B, 128-byte
+//                          swizzle, rows past M read as zeros).
+//   warp 10                allocates and frees tensor memory, and turns each
+//                          stage's activation scales d_x (fp16 in ds) into
+//                          fp32 for the epilogue.
+//   warps 12- (epilogue)   thread t reads row t's integer dots and scale,
 //                          releases the slot, and accumulates
-//                          d_w*(ls-32)*(d_x*dot) in fp32 registers.
+//                          (P*d_x)*d_w*(ls-32) in fp32 registers.
 // Every mbarrier wait is bounded (2 s); a timeout sets the device error word
 // and an abort flag that releases every other wait, the CTA drains its copies
 // and frees its tensor memory, and the call's output is undefined.
@@ -63,6 +64,7 @@ constexpr int kMaxCluster = 8;
 constexpr int kMinSmem = 120 * 1024;  // > half of the SM's shared memory: one CTA per SM
 constexpr int kACols = kSub / 2;      // 16 TMEM columns of fp16 pairs per sub-block
 constexpr int kCoreSbo = 128;         // 8 rows x 16 B core matrices, contiguous along N
+constexpr int kBStagesPerW = kSubPerPair / kBStageSubs;  // activation stages per W stage
 
 template <int R>
 __device__ __forceinline__ void reg_alloc() {
@@ -96,13 +98,10 @@ struct TcCfg {
     static_assert(kWBoxBytes % 16 == 0 && kWBoxBytes / 4 <= 256, "TMA box inner extent");
     // Warp roles.  Decoders: kDecGroups groups of four warps (warpgroups
     // 0..G-1); more groups hide more of the decode's latency where the
-    // epilogue is light (small tiles).  Then one control warpgroup (MMA
-    // issuers, TMA producer, tensor-memory owner) and the epilogue warpgroup.
-    // Three groups at MT = 16 (more independent decode streams per SM
-    // sub-partition: the decoders are latency-bound there; measured 4-11%
-    // faster) and at MT = 48 (1-3% faster); at MT = 32 and MT >= 64 a third
-    // group measured 9-15% slower, and a fourth at MT = 16 2% slower.
-    static constexpr int kDecGroups = (MT <= 16 || MT == 48) ? 3 : 2;
+    // epilogue is light (three at MT = 16).  Then one control warpgroup
+    // (MMA issuers, TMA producer, tensor-memory owner) and the epilogue
+    // warpgroups.
+    static constexpr int kDecGroups = (MT <= 16) ? 3 : 2;
     static constexpr int kDecWarps = 4 * kDecGroups;
     static constexpr int kMmaWarp0 = kDecWarps;       // MMA issuers (even / odd units)
     static constexpr int kProducerWarp = kDecWarps + 1;
@@ -113,22 +112,21 @@ struct TcCfg {
     // activation rows (columns of every accumulator): the per-unit read and
     // scale-in of 128 x MT results then takes half as long, which matters
     // because only two to four units fit in tensor memory at once.
-    // Measured on GB300: 10-25% faster at MT = 48..128; at MT = 32 mixed
-    // (3% slower on 4096 x 4096, 3-5% faster on larger shapes), so one group.
     static constexpr int kEpiGroups = (MT >= 48) ? 2 : 1;
     static constexpr int kMH = MT / kEpiGroups;  // activation rows of one epilogue group
-    static constexpr int kThreads = 32 * (kDecWarps + 4 + 4 * kEpiGroups);
+    static constexpr int kWarps = kEpiWarp0 + 4 * kEpiGroups;
+    static constexpr int kThreads = 32 * kWarps;
     // Per-warpgroup register budgets (setmaxnreg).  The block launches with
     // the registers of 65536 / kThreads per thread (rounded down to 8); the
     // budgets, 128 threads each, must sum within that.
     static constexpr int kRegsLaunch = (65536 / kThreads) / 8 * 8;
-    static constexpr int kRegsDecode = (kEpiGroups == 2) ? ((MT >= 64 || kDecGroups == 3) ? 72 : 80) : (kDecGroups == 3) ? 88 : 96;
-    static constexpr int kRegsControl = 56;
+    static constexpr int kRegsDecode = (kEpiGroups == 2) ? 72 : (kDecGroups == 3) ? 88 : 96;
+    static constexpr int kRegsControl = 64;
     static constexpr int kRegsEpiFree =
-        ((kThreads / 128) * kRegsLaunch - kDecGroups * kRegsDecode - kRegsControl) / kEpiGroups / 8 * 8;
+        ((kWarps / 4) * kRegsLaunch - kDecGroups * kRegsDecode - kRegsControl) / kEpiGroups / 8 * 8;
     static constexpr int kRegsEpilogue = kRegsEpiFree < 248 ? kRegsEpiFree : 248;
     static_assert(kDecGroups * kRegsDecode + kRegsControl + kEpiGroups * kRegsEpilogue <=
-                      (kThreads / 128) * kRegsLaunch,
+                      (kWarps / 4) * kRegsLaunch,
                   "register split fits the launch allocation");
     // Work unit: kU consecutive sub-blocks, decoded, multiplied and scaled
     // together (one barrier handshake per unit between the roles).
@@ -143,33 +141,50 @@ struct TcCfg {
     static_assert(kColS + kNP * kU <= kTmemCols, "slots fit tensor memory");
     static_assert(kNP >= 2, "at least two units in flight");
     static_assert(kBStageSubs % kU == 0 && kSubPerBlock % kU == 0, "units tile stages and super-blocks");
-    // Byte-table decode (MT <= 96): each qs byte (two nibbles) is looked up
-    // in shared memory as the fp16x2 word of the A operand, one load in
-    // place of the register-table decode's integer instructions.  32
-    // copies of the 256-entry table, copy l in bank l: entry j for lane l
-    // at 4 * (32 * j + l), so a warp's 32 lookups never conflict.  Larger
-    // tiles keep the register tables (their activation stages leave no
-    // room).
-    static constexpr bool kLut = MT <= 96;
-    static constexpr int kLutBytes = kLut ? 256 * 32 * 4 : 0;
-    static constexpr int kNW = kLut ? ((MT <= 16) ? 4 : (MT <= 48) ? 3 : (MT <= 64) ? 2 : (MT <= 80) ? 3 : 2)
-                                    : ((MT <= 16) ? 5 : (MT <= 48) ? 4 : (MT <= 96) ? 3 : 2);  // W stages
-    static constexpr int kNB = (MT <= 32) ? 4 : (MT <= 64) ? 3 : 2;                               // activation stages
-    static constexpr int kBSubBytes = kPlanes * kChunksPerSub * MT * 16;  // hi + lo of one sub-block
-    static constexpr int kBQhBytes = kBStageSubs * kBSubBytes;            // one bulk copy per stage
-    static constexpr int kBStageBytes = kBQhBytes;
+    // Byte-table decode: each qs byte (two nibbles) is looked up in shared
+    // memory as the fp16x2 word of the A operand.  32 copies of the
+    // 256-entry table, copy l in bank l: entry j for lane l at
+    // 4 * (32 * j + l), so a warp's 32 lookups never conflict.
+    static constexpr int kLutBytes = 256 * 32 * 4;
+    static constexpr int kNW = (MT <= 16) ? 4 : (MT <= 48) ? 3 : (MT <= 64) ? 2 : (MT <= 80) ? 3 : 2;  // W stages
+    static constexpr int kNB = (MT <= 32) ? 4 : (MT <= 64) ? 3 : 2;  // activation stages
+    // Activation stage slot: the staged codes (MT rows x 128 B, swizzled)
+    // and the fp16 B operand built from them (4 sub-blocks of kBSubBytes).
+    static constexpr int kQRawBytes = kQRowBytes * MT;
+    static constexpr int kBSubBytes = kChunksPerSub * MT * 16;
+    static constexpr int kBSlotBytes = kQRawBytes + kBStageSubs * kBSubBytes;
+    // Activation scales: fp32 [4 sub-blocks][MT] per stage, in a ring the
+    // epilogue releases (it runs behind the MMAs by up to kNP units).
+    static constexpr int kNX0 = kNB + (kNP * kU + kBStageSubs - 1) / kBStageSubs + 1;
+    static constexpr int kNX = kNX0 < 8 ? kNX0 : 8;
+    static constexpr int kXStageBytes = kBStageSubs * MT * 4;
+    static constexpr int kXItems = (kBStageSubs * MT + 31) / 32;  // scales per lane and stage
     static constexpr int kOffW = 0;
     static constexpr int kOffLut = kOffW + kNW * kWStage;
     static constexpr int kOffB = kOffLut + kLutBytes;
-    static constexpr int kOffBar = kOffB + kNB * kBStageBytes;
-    // W full/empty, B full/empty, A full / MMA done / accumulator free per
-    // unit slot, drain, split-K rows received
-    static constexpr int kNumBars = 2 * kNW + 2 * kNB + 3 * kNP + 2;
-    static constexpr int kBarDrain = 2 * kNW + 2 * kNB + 3 * kNP;
-    static constexpr int kBarRecv = kBarDrain + 1;
-    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;   // tmem base, abort flag
-    static constexpr int kOffSpan = (kOffMisc + 16 + 15) / 16 * 16;  // current span's scales (MT fp32)
-    static_assert(kOffSpan % 16 == 0, "span scales are read as 16-byte vectors");
+    static constexpr int kOffX = kOffB + kNB * kBSlotBytes;
+    static constexpr int kOffBar = kOffX + kNX * kXStageBytes;
+    // Barriers, in this order: W full / empty, code stage landed, code
+    // stage consumed (its MMAs complete), scales built / consumed, and per
+    // unit slot A full / MMA done / accumulators free; then drain and
+    // split-K rows received.
+    static constexpr int kNumBars = 2 * kNW + 2 * kNB + 2 * kNX + 3 * kNP + 2;
+    static constexpr int kBarDrain = kNumBars - 2;
+    static constexpr int kBarRecv = kNumBars - 1;
+    __host__ __device__ static constexpr uint32_t bar_count(int i) {
+        if (i < kNW) return 1;                       // w_full: producer, + tx
+        if ((i -= kNW) < kNW) return kDecWarps;      // w_empty
+        if ((i -= kNW) < kNB) return 1;              // q_full: producer, + tx
+        if ((i -= kNB) < kNB) return 2;              // b_empty: the MMA warps' commits
+        if ((i -= kNB) < kNX) return 1;              // x_full: the scale warp
+        if ((i -= kNX) < kNX) return 4 * kEpiGroups; // x_empty
+        if ((i -= kNX) < kNP) return 4;              // a_full: a decoder group
+        if ((i -= kNP) < kNP) return 1;              // mma_done: commit
+        if ((i -= kNP) < kNP) return 4 * kEpiGroups; // d_free: epilogue warps
+        if ((i -= kNP) == 0) return 2;               // drain: MMA warps
+        return 1;                                    // recv: expect_tx
+    }
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base, abort flag
     // Split-K reduction.  Each rank stages its partial tile (128 rows of
     // MT fp32, kRedStride apart) in its own activation ring, which is free
     // once its last MMA has completed, and bulk-copies the rows every other
@@ -178,26 +193,27 @@ struct TcCfg {
     static constexpr int kRedStride = MT + 4;  // fp32 words per row (16-byte rows, no bank conflicts)
     static constexpr int kOffStage = kOffB;
     static constexpr int kOffRecv = kOffW;
-    static_assert(kTileN * kRedStride * 4 <= kNB * kBStageBytes, "staged partial tile fits the activation ring");
+    static_assert(kTileN * kRedStride * 4 <= kNB * kBSlotBytes, "staged partial tile fits the activation ring");
     static_assert(recv_rows_max() * kRedStride * 4 <= kOffB - kOffW, "received slices fit the W ring and table");
-    static constexpr int kUsed = kOffSpan + MT * 4;
+    static constexpr int kUsed = kOffMisc + 16;
     static_assert(kUsed <= 226 * 1024, "stages fit shared memory");
     static constexpr int kSmem = (kUsed + 1024 > kMinSmem) ? kUsed + 1024 : kMinSmem;
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-    static_assert(kOffB % 1024 == 0 && kBStageBytes % 16 == 0 && kOffLut % 128 == 0, "alignment");
+    static_assert(kOffB % 1024 == 0 && kBSlotBytes % 1024 == 0 && kQRawBytes % 1024 == 0,
+                  "128-byte-swizzled code stages start on 1024-byte boundaries");
+    static_assert(kOffLut % 128 == 0 && kOffX % 16 == 0 && kOffBar % 8 == 0, "alignment");
+    static_assert(kNumBars <= 96, "barriers initialised three per producer lane");
+    static_assert(kRegsControl >= 56, "the MMA warps also build the B operand");
 };
 
-constexpr int kEpilogueBarrier = 1;  // named barriers 1, 2: the 4 warps of epilogue group 0, 1
 __device__ volatile int g_never_abort = 0;  // an abort flag that is never set
-__device__ __forceinline__ void named_barrier_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
 
 template <int MT, int WT>
 __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
     matmul_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                     const uint8_t* __restrict__ tc_op, int64_t M, int N, int K,
-                     float* __restrict__ y, int64_t ldy, int* err) {
+                     const __grid_constant__ CUtensorMap tmap_q, const __half* __restrict__ ds,
+                     int64_t M, int N, int K, float* __restrict__ y, int64_t ldy, int* err,
+                     int skip_w_stage) {
     using C = TcCfg<MT, WT>;
     constexpr int kDecGroups = C::kDecGroups, kDecWarps = C::kDecWarps;
     constexpr int kMmaWarp0 = C::kMmaWarp0, kMmaWarp1 = C::kMmaWarp1;
@@ -208,18 +224,20 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint64_t* w_full = bars;
     uint64_t* w_empty = w_full + C::kNW;
-    uint64_t* b_full = w_empty + C::kNW;
-    uint64_t* b_empty = b_full + C::kNB;
+    uint64_t* q_full = w_empty + C::kNW;   // a code stage has landed (TMA)
+    uint64_t* b_empty = q_full + C::kNB;   // its MMAs are complete (slot reusable)
+    uint64_t* x_full = b_empty + C::kNB;   // a stage's activation scales are built
+    uint64_t* x_empty = x_full + C::kNX;   // ... and read by the epilogue
     // a_full[p]: unit slot p holds a decoded unit (A and scale columns);
     // mma_done[p]: its MMAs are complete (accumulators readable);
     // d_free[p]: the epilogue has read the accumulators and scales, so the
     // whole slot may be reused.  Every use of slot p waits, directly or
     // through this chain, for the previous use's d_free, so none of the
     // three barriers ever runs two phases ahead of a waiter.
-    uint64_t* a_full = b_empty + C::kNB;
+    uint64_t* a_full = x_empty + C::kNX;
     uint64_t* mma_done = a_full + C::kNP;
     uint64_t* d_free = mma_done + C::kNP;
-    uint64_t* drain = d_free + C::kNP;
+    uint64_t* drain = bars + C::kBarDrain;
     uint64_t* recv_bar = bars + C::kBarRecv;  // split-K: the other ranks' slices have landed
     uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -236,12 +254,12 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
     const int nsub = (p1 - p0) * kSubPerPair;
     const int nunits = nsub / C::kU;
     const int nbst = nsub / kBStageSubs;
-    const int64_t K32 = K / kSub;
-    const uint8_t* qh_tile = tc_op + (int64_t)z * K32 * C::kBSubBytes;
 
-    static_assert(C::kNumBars <= 64, "barriers initialised two per producer lane");
     // W stage ps (pair index within this CTA's K range) into ring slot `slot`.
+    // Stage skip_w_stage is not issued at all (a test of the bounded waits:
+    // its consumers' wait runs out; -1 in every ordinary launch).
     auto load_w_stage = [&](int slot, int ps) {
+        if (ps == skip_w_stage) return;
         mbar_arrive_expect_tx(&w_full[slot], C::kWStage);
 #pragma unroll
         for (int b = 0; b < C::kWBoxes; ++b)
@@ -250,22 +268,12 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                         &w_full[slot]);
     };
     if (warp == kProducerWarp) {
-        // Lane i initialises barriers i and i + 32; lane 0 then starts the
-        // first W copy at once (W is read-only model state).
+        // Lane i initialises barriers i, i + 32, i + 64; lane 0 then starts
+        // the first W copy at once (W is read-only model state).
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 3; ++h) {
             const int i = lane + 32 * h;
-            uint32_t count = 0;
-            if (i < C::kNW) count = 1;                                           // w_full
-            else if (i < 2 * C::kNW) count = kDecWarps;                          // w_empty
-            else if (i < 2 * C::kNW + C::kNB) count = 1;                         // b_full
-            else if (i < 2 * C::kNW + 2 * C::kNB) count = 2;                     // b_empty: the MMA warps' commits
-            else if (i < 2 * C::kNW + 2 * C::kNB + C::kNP) count = 4;            // a_full: a decoder group
-            else if (i < 2 * C::kNW + 2 * C::kNB + 2 * C::kNP) count = 1;        // mma_done
-            else if (i < 2 * C::kNW + 2 * C::kNB + 3 * C::kNP) count = 4 * C::kEpiGroups;  // d_free: epilogue warps
-            else if (i == C::kBarDrain) count = 2;                               // drain: MMA warps
-            else if (i == C::kBarRecv) count = 1;                                // recv: expect_tx below
-            if (count) mbar_init(&bars[i], count);
+            if (i < C::kNumBars) mbar_init(&bars[i], C::bar_count(i));
         }
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -273,6 +281,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
         if (lane == 0) {
             *abort_flag = 0;
             prefetch_tmap(&tmap_w);
+            prefetch_tmap(&tmap_q);
             load_w_stage(0, 0);
             // Split-K: this rank's rows arrive from the S - 1 other ranks.
             // Posted now, before any rank can send (sends wait for a cluster
@@ -283,7 +292,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
             }
         }
     }
-    if constexpr (C::kLut) {
+    {
         // Row j of the byte table: 32 copies of entry j (one per bank).
         uint4* lut = reinterpret_cast<uint4*>(smem + C::kOffLut);
         for (int i = threadIdx.x; i < 256 * 8; i += C::kThreads) {
@@ -305,6 +314,42 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
     // Let the next kernel in the stream begin its launch; it waits for this
     // grid's completion before touching anything this grid reads or writes.
     griddep_launch_dependents();
+
+    // Activation scales (tensor-memory warp, running ahead of the epilogue
+    // by up to kNX stages): d_x of each stage's four sub-blocks, fp16 in
+    // ds, to fp32 [sub-block][row] for the epilogue; rows past M get 0.
+    auto build_scales = [&]() {
+        bool ok = true;
+        const int64_t K32 = K / kSub;
+        const uint32_t* ds32 = reinterpret_cast<const uint32_t*>(ds);  // {d, s} pairs
+        griddep_wait();  // ds comes from the preceding grid
+        for (int bs = 0; bs < nbst; ++bs) {
+            const int xs = bs % C::kNX;
+            const int64_t sub0 = (int64_t)p0 * kSubPerPair + (int64_t)bs * kBStageSubs;
+            // Item e = 4 * row + sub-block: four consecutive lanes read one
+            // row's 16 contiguous bytes.
+            uint32_t dsv[C::kXItems];
+#pragma unroll
+            for (int k = 0; k < C::kXItems; ++k) {
+                const int e = lane + 32 * k;
+                const int64_t row = (int64_t)z * MT + e / kBStageSubs;
+                dsv[k] = (e < kBStageSubs * MT && row < M) ? __ldg(ds32 + row * K32 + sub0 + e % kBStageSubs) : 0u;
+            }
+            if (ok && bs >= C::kNX)
+                ok = mbar_wait(&x_empty[xs], ((bs / C::kNX) - 1) & 1, abort_flag, err, kDevErrTimeoutX);
+            if (!ok) break;
+            float* xr = reinterpret_cast<float*>(smem + C::kOffX + xs * C::kXStageBytes);
+#pragma unroll
+            for (int k = 0; k < C::kXItems; ++k) {
+                const int e = lane + 32 * k;
+                if (e < kBStageSubs * MT)
+                    xr[(e % kBStageSubs) * MT + e / kBStageSubs] =
+                        __half2float(__ushort_as_half((unsigned short)(dsv[k] & 0xFFFFu)));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&x_full[xs]);
+        }
+    };
 
     if (warp < kDecWarps) {
         // ------------------------------------------------------------ decoders
@@ -331,7 +376,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                 const uint8_t* blk = stage + t * kPairBytes + (jj / kSubPerBlock) * kBlockBytes;
                 const int j = jj % kSubPerBlock;
                 const uint2 hdr = *reinterpret_cast<const uint2*>(blk);
-                if (C::kLut && MT >= 80 && jj >= kSubPerBlock) {
+                if (MT >= 80 && jj >= kSubPerBlock) {
                     // Second super-block of the stage row: its qs start at
                     // byte 144, 16-byte aligned, so one 16-byte load per
                     // sub-block (half the shared-memory wavefronts of two
@@ -369,7 +414,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                 }
             }
             uint32_t h[C::kU][kACols];
-            if constexpr (C::kLut) {
+            {
                 // Byte k of word c holds elements 4c+k (low nibble) and
                 // 16+4c+k (high nibble): table row = the byte (moved to the
                 // low byte by one byte permute, measured faster than a
@@ -382,14 +427,6 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             h[u][4 * c + k] = lds_u32(lut + (__byte_perm(q[u][c], 0u, 0x4440u + k) << 7));
-            } else {
-#pragma unroll
-                for (int u = 0; u < C::kU; ++u) {
-                    decode_f16x2<WT>(q[u][0], h[u]);
-                    decode_f16x2<WT>(q[u][1], h[u] + 4);
-                    decode_f16x2<WT>(q[u][2], h[u] + 8);
-                    decode_f16x2<WT>(q[u][3], h[u] + 12);
-                }
             }
             // The stage's bytes are consumed (in registers) once this warp's
             // last unit of it is decoded.
@@ -434,32 +471,50 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
             // lane issues.  Warp k takes units k, k+2, ... (those of decoder
             // group k).
             constexpr uint32_t idesc = idesc_f16_m128(MT);
-            const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffB), MT * 16, kCoreSbo);
+            const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffB + C::kQRawBytes), MT * 16, kCoreSbo);
             const int k = (warp == kMmaWarp0) ? 0 : 1;
+            const int r8 = lane & 7, c = lane >> 3;
             bool ok = true;
             int sp = k, sphase = 0;
             for (int v = k, l0 = k * C::kU; v < nunits; v += 2, l0 += 2 * C::kU) {
                 const int lb = l0 % kBStageSubs;  // first sub-block's position in its B stage
                 const int bs = l0 / kBStageSubs, bslot = bs % C::kNB, bphase = (bs / C::kNB) & 1;
-                if (ok && lb < 2 * C::kU)  // this warp's first unit of the B stage
-                    ok = mbar_wait(&b_full[bslot], bphase, abort_flag, err, kDevErrTimeoutB);
+                // B operand of this unit's sub-blocks, built from the staged
+                // codes (MT rows x 128 B, 128-byte swizzled: 16-byte unit u
+                // of row r sits at unit u ^ (r % 8)).  Lane (r8, c) of
+                // item (sub-block s, rows 8rb..8rb+7) builds chunk c of row
+                // 8rb + r8 from code words c and 4 + c: the 32 lanes read 32
+                // distinct banks and store 4 x 128 contiguous bytes.
+                if (ok) ok = mbar_wait(&q_full[bslot], bphase, abort_flag, err, kDevErrTimeoutQ);
+                if (ok) {
+                    const uint8_t* raw = smem + C::kOffB + bslot * C::kBSlotBytes;
+                    uint8_t* bop = smem + C::kOffB + bslot * C::kBSlotBytes + C::kQRawBytes;
+#pragma unroll 4
+                    for (int wi = 0; wi < C::kU * (MT / 8); ++wi) {
+                        const int s = lb + wi / (MT / 8), r = (wi % (MT / 8)) * 8 + r8;
+                        const uint8_t* row = raw + r * kQRowBytes + 4 * c;
+                        const uint32_t lo4 = *reinterpret_cast<const uint32_t*>(row + (((2 * s) ^ r8) << 4));
+                        const uint32_t hi4 = *reinterpret_cast<const uint32_t*>(row + (((2 * s + 1) ^ r8) << 4));
+                        *reinterpret_cast<uint4*>(bop + s * C::kBSubBytes + c * MT * 16 + r * 16) =
+                            q8x8_to_f16(lo4, hi4);
+                    }
+                    fence_proxy_async_smem();  // the tensor core reads what was stored
+                }
+                __syncwarp();
                 if (ok) ok = mbar_wait(&a_full[sp], sphase, abort_flag, err, kDevErrTimeoutA);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
                 if (elect_one()) {
                     if (ok) {
-                        const uint32_t boff = (uint32_t)(bslot * C::kBStageBytes + lb * C::kBSubBytes);
+                        const uint32_t boff = (uint32_t)(bslot * C::kBSlotBytes + lb * C::kBSubBytes);
 #pragma unroll
                         for (int u = 0; u < C::kU; ++u)
 #pragma unroll
                             for (int i = 0; i < kMmaPerSub; ++i)
-#pragma unroll
-                                for (int pl = 0; pl < kPlanes; ++pl)
-                                    tc_mma_f16_ta(
-                                        tmem + (uint32_t)(C::kColD + (sp * C::kU + u) * MT),
-                                        tmem + (uint32_t)(C::kColA + (sp * C::kU + u) * kACols + i * (kUmmaK / 2)),
-                                        bdesc0 + ((boff + u * C::kBSubBytes + (pl * kChunksPerSub + 2 * i) * MT * 16) >> 4),
-                                        idesc, (i | pl) != 0);
+                                tc_mma_f16_ta(
+                                    tmem + (uint32_t)(C::kColD + (sp * C::kU + u) * MT),
+                                    tmem + (uint32_t)(C::kColA + (sp * C::kU + u) * kACols + i * (kUmmaK / 2)),
+                                    bdesc0 + ((boff + u * C::kBSubBytes + 2 * i * MT * 16) >> 4), idesc, i != 0);
                     }
                     // Commits are made even after an abort so that every
                     // waiter's barrier still completes.
@@ -473,59 +528,69 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
             }
             if (elect_one()) tc_commit(drain);
             __syncwarp();
-        } else if (warp == kProducerWarp && lane == 0) {
-            // ----------------------------------------------------- producer
-            // The first W stage was started during set-up, before the
-            // preceding kernel (which produces the activations) has finished.
-            // The other stages follow once it has landed, so that at launch,
-            // when every CTA requests at once, first stages are served first.
-            int issued_w = 1, issued_b = 0;
-            bool ok = true;
-            const int pre = (C::kNW < (p1 - p0)) ? C::kNW : (p1 - p0);
-            griddep_wait();
-            for (int bs = 0; bs < C::kNB && bs < nbst; ++bs) {
-                uint8_t* dst = smem + C::kOffB + bs * C::kBStageBytes;
-                const int64_t sub0 = (int64_t)p0 * kSubPerPair + (int64_t)bs * kBStageSubs;
-                mbar_arrive_expect_tx(&b_full[bs], C::kBQhBytes);
-                bulk_load(dst, qh_tile + sub0 * C::kBSubBytes, C::kBQhBytes, &b_full[bs]);
-                ++issued_b;
-            }
-            if (pre > 1) ok = mbar_wait(&w_full[0], 0, abort_flag, err, kDevErrTimeoutW);
-            for (int ps = 1; ps < pre && ok; ++ps) {
-                load_w_stage(ps, ps);
-                ++issued_w;
-            }
-            for (int bs = issued_b; bs < nbst && ok; ++bs) {
-                if (bs % (kSubPerPair / kBStageSubs) == 0) {
-                    const int ps = bs / (kSubPerPair / kBStageSubs);
-                    if (ps >= pre) {
-                        const int slot = ps % C::kNW;
-                        ok = mbar_wait(&w_empty[slot], ((ps / C::kNW) - 1) & 1, abort_flag, err,
-                                       kDevErrTimeoutW);
-                        if (!ok) break;
-                        load_w_stage(slot, ps);
-                        ++issued_w;
-                    }
+        } else if (warp == kProducerWarp) {
+            if (lane == 0) {
+                // ------------------------------------------------- producer
+                // The first W stage was started during set-up, before the
+                // preceding kernel (which produces the activations) has
+                // finished.  The other stages follow once it has landed, so
+                // that at launch, when every CTA requests at once, first
+                // stages are served first.
+                auto load_q_stage = [&](int slot, int bs) {
+                    mbar_arrive_expect_tx(&q_full[slot], C::kQRawBytes);
+                    tma_load_2d(smem + C::kOffB + slot * C::kBSlotBytes, &tmap_q,
+                                (p0 * kSubPerPair + bs * kBStageSubs) * kSub, z * MT, &q_full[slot]);
+                };
+                int issued_w = 1, issued_q = 0;
+                bool ok = true;
+                const int pre = (C::kNW < (p1 - p0)) ? C::kNW : (p1 - p0);
+                griddep_wait();  // the codes come from the preceding grid
+                for (int bs = 0; bs < C::kNB && bs < nbst; ++bs) {
+                    load_q_stage(bs, bs);
+                    ++issued_q;
                 }
-                const int slot = bs % C::kNB;
-                if (bs >= C::kNB)
-                    ok = mbar_wait(&b_empty[slot], ((bs / C::kNB) - 1) & 1, abort_flag, err,
-                                   kDevErrTimeoutB);
-                if (!ok) break;
-                uint8_t* dst = smem + C::kOffB + slot * C::kBStageBytes;
-                const int64_t sub0 = (int64_t)p0 * kSubPerPair + (int64_t)bs * kBStageSubs;
-                mbar_arrive_expect_tx(&b_full[slot], C::kBQhBytes);
-                bulk_load(dst, qh_tile + sub0 * C::kBSubBytes, C::kBQhBytes, &b_full[slot]);
-                ++issued_b;
+                if (pre > 1) ok = mbar_wait(&w_full[0], 0, abort_flag, err, kDevErrTimeoutW);
+                for (int ps = 1; ps < pre && ok; ++ps) {
+                    load_w_stage(ps, ps);
+                    ++issued_w;
+                }
+                for (int bs = issued_q; bs < nbst && ok; ++bs) {
+                    if (bs % kBStagesPerW == 0) {
+                        const int ps = bs / kBStagesPerW;
+                        if (ps >= pre) {
+                            const int slot = ps % C::kNW;
+                            ok = mbar_wait(&w_empty[slot], ((ps / C::kNW) - 1) & 1, abort_flag, err,
+                                           kDevErrTimeoutW);
+                            if (!ok) break;
+                            load_w_stage(slot, ps);
+                            ++issued_w;
+                        }
+                    }
+                    // The slot's previous stage is consumed: its MMAs are
+                    // complete, so its codes have been read too.
+                    const int slot = bs % C::kNB;
+                    ok = mbar_wait(&b_empty[slot], ((bs / C::kNB) - 1) & 1, abort_flag, err, kDevErrTimeoutB);
+                    if (!ok) break;
+                    load_q_stage(slot, bs);
+                    ++issued_q;
+                }
+                // Drain: the last copies issued into each ring slot have
+                // landed (earlier ones were consumed before their slot was
+                // reused).  These waits do not stop on an abort (bounded all
+                // the same): no copy may land after the CTA exits.
+                for (int ps = (issued_w > C::kNW ? issued_w - C::kNW : 0); ps < issued_w; ++ps)
+                    if (ps != skip_w_stage)
+                        mbar_wait(&w_full[ps % C::kNW], (ps / C::kNW) & 1, &g_never_abort, err,
+                                  kDevErrTimeoutDrain);
+                for (int bs = (issued_q > C::kNB ? issued_q - C::kNB : 0); bs < issued_q; ++bs)
+                    mbar_wait(&q_full[bs % C::kNB], (bs / C::kNB) & 1, &g_never_abort, err,
+                              kDevErrTimeoutDrain);
             }
-            // Drain: the last copies issued into each ring slot have landed.
-            for (int ps = (issued_w > C::kNW ? issued_w - C::kNW : 0); ps < issued_w; ++ps)
-                mbar_wait(&w_full[ps % C::kNW], (ps / C::kNW) & 1, abort_flag, err, kDevErrTimeoutDrain);
-            for (int bs = (issued_b > C::kNB ? issued_b - C::kNB : 0); bs < issued_b; ++bs)
-                mbar_wait(&b_full[bs % C::kNB], (bs / C::kNB) & 1, abort_flag, err, kDevErrTimeoutDrain);
         } else if (warp == kTmemWarp) {
-            // Every MMA issued has completed before tensor memory is freed.
-            mbar_wait(drain, 0, abort_flag, err, kDevErrTimeoutDrain);
+            build_scales();
+            // Every MMA issued has completed before tensor memory is freed
+            // (the MMA warps commit this after their loops, abort or not).
+            mbar_wait(drain, 0, &g_never_abort, err, kDevErrTimeoutDrain);
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -542,94 +607,66 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
         float acc[kMH];
 #pragma unroll
         for (int m = 0; m < kMH; ++m) acc[m] = 0.f;
-        // Activation span scales (from the preceding grid): the partial sums
-        // are kept in units of the current span's 2^-e and rescaled by exact
-        // powers of two where the span changes (every 32 sub-blocks).  The
-        // current span's scales are staged in shared memory, each group's
-        // own entries by that group (named barrier 1 + group).
-        griddep_wait();
-        const float* span_scale = reinterpret_cast<const float*>(tc_op + tc_qh_bytes(M, K)) +
-                                  (int64_t)z * tc_num_spans(K) * MT + c0;
-        float* s_span = reinterpret_cast<float*>(smem + C::kOffSpan) + c0;
-        int cur_span = (p0 * kSubPerPair) / kSubPerSpan;
-        if (t < kMH) s_span[t] = span_scale[(int64_t)cur_span * MT + t];
-        named_barrier_sync(kEpilogueBarrier + eg, kTileN);
+        // acc[m0 + i] += (P[i] * d_x[m0 + i]) * sw for i < n, two columns per
+        // instruction; the scales of four columns per shared-memory load
+        // (the same address across the warp: a broadcast).
+        auto scale_in = [&](const uint32_t* r, int n, int m0, float sw, const float* xrow) {
+#pragma unroll
+            for (int i = 0; i < n; i += 4) {
+                const float4 d = *reinterpret_cast<const float4*>(xrow + m0 + i);
+                const float2 p0 = __fmul2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                             make_float2(d.x, d.y));
+                const float2 p1 = __fmul2_rn(make_float2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
+                                             make_float2(d.z, d.w));
+                const float2 a0 = __ffma2_rn(p0, make_float2(sw, sw), make_float2(acc[m0 + i], acc[m0 + i + 1]));
+                const float2 a1 = __ffma2_rn(p1, make_float2(sw, sw), make_float2(acc[m0 + i + 2], acc[m0 + i + 3]));
+                acc[m0 + i] = a0.x;
+                acc[m0 + i + 1] = a0.y;
+                acc[m0 + i + 2] = a1.x;
+                acc[m0 + i + 3] = a1.y;
+            }
+        };
         bool ok = true;
         int sp = 0, sphase = 0;
         for (int v = 0; v < nunits; ++v) {
-            const int span = (p0 * kSubPerPair + v * C::kU) / kSubPerSpan;
-            if (span != cur_span) {
-                const float4* fo = reinterpret_cast<const float4*>(s_span);
-                const float4* fn = reinterpret_cast<const float4*>(span_scale + (int64_t)span * MT);
-#pragma unroll
-                for (int m = 0; m < kMH; m += 4) {
-                    const float4 a = fo[m / 4], b = fn[m / 4];
-                    acc[m] *= a.x / b.x;
-                    acc[m + 1] *= a.y / b.y;
-                    acc[m + 2] *= a.z / b.z;
-                    acc[m + 3] *= a.w / b.w;
-                }
-                named_barrier_sync(kEpilogueBarrier + eg, kTileN);  // every thread has read the old scales
-                if (t < kMH) s_span[t] = span_scale[(int64_t)span * MT + t];
-                named_barrier_sync(kEpilogueBarrier + eg, kTileN);
-                cur_span = span;
-            }
+            const int l0 = v * C::kU, bs = l0 / kBStageSubs, jj = l0 % kBStageSubs, xs = bs % C::kNX;
+            if (ok && jj == 0)  // the stage's scales
+                ok = mbar_wait(&x_full[xs], (bs / C::kNX) & 1, abort_flag, err, kDevErrTimeoutX);
             if (ok) ok = mbar_wait(&mma_done[sp], sphase, abort_flag, err, kDevErrTimeoutMma);
             tc_fence_after();
             const uint32_t dcol = tmem + lane_off + (uint32_t)(C::kColD + sp * C::kU * MT + c0);
             const uint32_t scol = tmem + lane_off + (uint32_t)(C::kColS + sp * C::kU);
+            const float* xst = reinterpret_cast<const float*>(smem + C::kOffX + xs * C::kXStageBytes) + c0;
             uint32_t swb[C::kU];
             if constexpr (C::kEpiGroups == 1) {
                 // this group's columns of both sub-blocks are contiguous
                 constexpr int kCols = C::kU * MT;
-#pragma unroll
-                for (int part = 0; part < kCols; part += 64) {
-                    const int w = (kCols - part < 64) ? kCols - part : 64;
-                    uint32_t r[64];
-                    if (part == 0) {
-                        if (C::kU == 2) {
-                            if (w == 64) tmem_ld64_s2_wait(dcol, scol, r, swb);
-                            else if (w == 48) tmem_ld48_s2_wait(dcol, scol, r, swb);
-                            else if (w == 32) tmem_ld32_s2_wait(dcol, scol, r, swb);
-                            else tmem_ld16_s2_wait(dcol, scol, r, swb);
-                        } else {
-                            if (w == 64) tmem_ld64_s1_wait(dcol, scol, r, swb);
-                            else if (w == 48) tmem_ld48_s1_wait(dcol, scol, r, swb);
-                            else if (w == 32) tmem_ld32_s1_wait(dcol, scol, r, swb);
-                            else tmem_ld16_s1_wait(dcol, scol, r, swb);
-                        }
-                    } else {
-                        if (w == 64) tmem_ld64_wait(dcol + part, r);
-                        else if (w == 48) tmem_ld48_wait(dcol + part, r);
-                        else if (w == 32) tmem_ld32_wait(dcol + part, r);
-                        else tmem_ld16_wait(dcol + part, r);
-                    }
-                    if (part + 64 >= kCols) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&d_free[sp]);
-                    }
-                    // acc[m] += (d_x * dot) * Sw, two columns per instruction; a
-                    // pair of columns never straddles two sub-blocks.
-#pragma unroll
-                    for (int k = 0; k < 64; k += 2) {
-                        if (k >= w) break;
-                        const int c = part + k, u = c / MT, m = c % MT;
-                        const float sw = __uint_as_float(swb[u]);
-                        const float2 a = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
-                                                    make_float2(sw, sw), make_float2(acc[m], acc[m + 1]));
-                        acc[m] = a.x;
-                        acc[m + 1] = a.y;
-                    }
+                static_assert(kCols <= 64, "one load per unit");
+                uint32_t r[kCols];
+                if constexpr (C::kU == 2) {
+                    if constexpr (kCols == 64) tmem_ld64_s2_wait(dcol, scol, r, swb);
+                    else tmem_ld32_s2_wait(dcol, scol, r, swb);
+                } else {
+                    if constexpr (kCols == 64) tmem_ld64_s1_wait(dcol, scol, r, swb);
+                    else if constexpr (kCols == 32) tmem_ld32_s1_wait(dcol, scol, r, swb);
+                    else tmem_ld16_s1_wait(dcol, scol, r, swb);
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&d_free[sp]);
+#pragma unroll
+                for (int u = 0; u < C::kU; ++u)
+                    scale_in(r + u * MT, MT, 0, __uint_as_float(swb[u]), xst + (jj + u) * MT);
             } else {
                 // kMH columns of each sub-block u, at u * MT + c0, in at most
                 // two loads (the first with the scale columns)
-                constexpr int kP0 = (kMH <= 48) ? kMH : 32;
+                constexpr int kP0 = (kMH <= 40) ? kMH : 32;
                 constexpr int kP1 = kMH - kP0;
+                static_assert(kP1 == 0 || kP1 == 16 || kP1 == 24 || kP1 == 32, "load widths");
 #pragma unroll
                 for (int u = 0; u < C::kU; ++u) {
                     const uint32_t col = dcol + (uint32_t)(u * MT);
+                    const float* xrow = xst + (jj + u) * MT;
                     {
                         uint32_t r[kP0];
                         if (u == 0) tmem_ld_cols_wait<kP0, C::kU>(col, scol, r, swb);
@@ -639,48 +676,25 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                             __syncwarp();
                             if (lane == 0) mbar_arrive(&d_free[sp]);
                         }
-                        const float sw = __uint_as_float(swb[u]);
-#pragma unroll
-                        for (int k = 0; k < kP0; k += 2) {
-                            const float2 a = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
-                                                        make_float2(sw, sw), make_float2(acc[k], acc[k + 1]));
-                            acc[k] = a.x;
-                            acc[k + 1] = a.y;
-                        }
+                        scale_in(r, kP0, 0, __uint_as_float(swb[u]), xrow);
                     }
                     if constexpr (kP1 > 0) {
-                        uint32_t r[kP1];
+                        uint32_t r[kP1 > 0 ? kP1 : 1];
                         tmem_ld_cols_wait<kP1, 0>(col + kP0, scol, r, swb);
                         if (u == C::kU - 1) {
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) mbar_arrive(&d_free[sp]);
                         }
-                        const float sw = __uint_as_float(swb[u]);
-#pragma unroll
-                        for (int k = 0; k < kP1; k += 2) {
-                            const float2 a = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
-                                                        make_float2(sw, sw),
-                                                        make_float2(acc[kP0 + k], acc[kP0 + k + 1]));
-                            acc[kP0 + k] = a.x;
-                            acc[kP0 + k + 1] = a.y;
-                        }
+                        scale_in(r, kP1, kP0, __uint_as_float(swb[u]), xrow);
                     }
                 }
             }
-            if (++sp == C::kNP) { sp = 0; sphase ^= 1; }
-        }
-        // Back to true units: times the last span's 2^e (exact).
-        {
-            const float4* f = reinterpret_cast<const float4*>(s_span);
-#pragma unroll
-            for (int m = 0; m < kMH; m += 4) {
-                const float4 a = f[m / 4];
-                acc[m] *= a.x;
-                acc[m + 1] *= a.y;
-                acc[m + 2] *= a.z;
-                acc[m + 3] *= a.w;
+            if (jj + C::kU >= kBStageSubs) {  // the stage's last unit: its scales are read
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&x_empty[xs]);
             }
+            if (++sp == C::kNP) { sp = 0; sphase ^= 1; }
         }
         // Partial tile -> y (one CTA), or staged in this CTA's activation
         // ring (free: every MMA has completed) for the split-K reduction.
@@ -732,7 +746,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
         cluster_arrive_relaxed();  // phase 2: this rank's slices have landed
         if (warp < kDecWarps || warp >= kEpiWarp0) {
             griddep_wait();
-            const int idx = (warp < kDecWarps) ? threadIdx.x : threadIdx.x - 4 * 32;
+            const int idx = (warp < kDecWarps) ? threadIdx.x : threadIdx.x - (kEpiWarp0 - kDecWarps) * 32;
             const int64_t mrows = M - (int64_t)z * MT;
             const float* stg = reinterpret_cast<const float*>(smem + C::kOffStage);
             const float* recv = reinterpret_cast<const float*>(smem + C::kOffRecv);
@@ -841,9 +855,9 @@ int choose_split(int dev, int fallback, int units, int pairs) {
 }
 
 template <int MT, int WT>
-cudaError_t launch_mt(const CUtensorMap& tmap, const uint8_t* tc_op, int64_t M, int N, int K,
-                      float* y, int64_t ldy, int* err, int S, int ntiles, int mtiles,
-                      cudaStream_t stream) {
+cudaError_t launch_mt(const CUtensorMap& tmap_w, const CUtensorMap& tmap_q, const __half* ds, int64_t M,
+                      int N, int K, float* y, int64_t ldy, int* err, int S, int ntiles, int mtiles,
+                      int skip, cudaStream_t stream) {
     using C = TcCfg<MT, WT>;
     static bool attr_done[64] = {};
     int dev = 0;
@@ -869,45 +883,63 @@ cudaError_t launch_mt(const CUtensorMap& tmap, const uint8_t* tc_op, int64_t M, 
     attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, matmul_tc_kernel<MT, WT>, tmap, tc_op, M, N, K, y, ldy, err);
+    return cudaLaunchKernelEx(&cfg, matmul_tc_kernel<MT, WT>, tmap_w, tmap_q, ds, M, N, K, y, ldy, err,
+                              skip);
 }
 
 template <int WT>
-cudaError_t launch_wt(const CUtensorMap& tmap, const uint8_t* op, int64_t M, int N, int K,
-                      float* y, int64_t ldy, int* err, int S, int ntiles, int mtiles,
+cudaError_t launch_wt(const CUtensorMap& tw, const CUtensorMap& tq, const __half* ds, int64_t M, int N,
+                      int K, float* y, int64_t ldy, int* err, int S, int ntiles, int mtiles, int skip,
                       cudaStream_t stream) {
     switch (tc_mtile(M)) {
-        case 16: return launch_mt<16, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
-        case 32: return launch_mt<32, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
-        case 48: return launch_mt<48, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
-        case 64: return launch_mt<64, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
-        case 80: return launch_mt<80, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
-        case 96: return launch_mt<96, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
-        case 112: return launch_mt<112, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
-        case 128: return launch_mt<128, WT>(tmap, op, M, N, K, y, ldy, err, S, ntiles, mtiles, stream);
+        case 16: return launch_mt<16, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
+        case 32: return launch_mt<32, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
+        case 48: return launch_mt<48, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
+        case 64: return launch_mt<64, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
+        case 80: return launch_mt<80, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
+        case 96: return launch_mt<96, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
+        case 112: return launch_mt<112, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
+        case 128: return launch_mt<128, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const void* tc_operand,
-                             int64_t M, float* y, int64_t ldy, void* encode, int* err,
-                             int num_sms, cudaStream_t stream) {
+cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,
+                             const void* ds, int64_t M, float* y, int64_t ldy, void* encode,
+                             int* err, int num_sms, int skip_w_stage, cudaStream_t stream) {
     if (wt != kWtIQ4XS && wt != kWtQ4_0 && wt != kWtIQ4NL) return cudaErrorInvalidValue;
+    const EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(encode);
     const int64_t row_bytes = wt_row_bytes(wt, K);
-    // one TMA box: 128 rows x (two super-blocks, or eight 18-byte blocks)
+    // W: one TMA box = 128 rows x (two super-blocks, or eight 18-byte blocks)
     const int box_bytes = (wt == kWtIQ4XS) ? kPairBytes : kB18GroupBytes;
-    CUtensorMap tmap;
-    const cuuint64_t gdim[2] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)N};
-    const cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
-    const cuuint32_t box[2] = {(cuuint32_t)(box_bytes / 4), (cuuint32_t)kTileN};
-    const cuuint32_t estride[2] = {1, 1};
-    CUresult cr = reinterpret_cast<EncodeTiledFn>(encode)(
-        &tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(w), gdim, gstride, box,
-        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    CUtensorMap tmap_w;
+    {
+        const cuuint64_t gdim[2] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)N};
+        const cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
+        const cuuint32_t box[2] = {(cuuint32_t)(box_bytes / 4), (cuuint32_t)kTileN};
+        const cuuint32_t estride[2] = {1, 1};
+        if (enc(&tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(w), gdim, gstride, box,
+                estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    // Q8_1 codes: one TMA box = MT rows x 128 codes (4 sub-blocks), 128-byte
+    // swizzle (conflict-free reads when the B operand is built); rows past M
+    // read as 0.
+    const int MT = tc_mtile(M);
+    CUtensorMap tmap_q;
+    {
+        const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
+        const cuuint64_t gstride[1] = {(cuuint64_t)K};
+        const cuuint32_t box[2] = {(cuuint32_t)kQRowBytes, (cuuint32_t)MT};
+        const cuuint32_t estride[2] = {1, 1};
+        if (enc(&tmap_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qs), gdim, gstride, box,
+                estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
 
     const int mtiles = (int)tc_num_mtiles(M);
     const int ntiles = (int)((N + kTileN - 1) / kTileN);
@@ -916,11 +948,14 @@ cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const 
     if (S > kMaxCluster) S = kMaxCluster;
     if (S > pairs) S = pairs;
     if (S < 1) S = 1;
-    const uint8_t* op = reinterpret_cast<const uint8_t*>(tc_operand);
+    const __half* dsh = reinterpret_cast<const __half*>(ds);
     const int Ni = (int)N, Ki = (int)K;
-    if (wt == kWtQ4_0) return launch_wt<kWtQ4_0>(tmap, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, stream);
-    if (wt == kWtIQ4NL) return launch_wt<kWtIQ4NL>(tmap, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, stream);
-    return launch_wt<kWtIQ4XS>(tmap, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, stream);
+    const int skip = skip_w_stage;
+    if (wt == kWtQ4_0)
+        return launch_wt<kWtQ4_0>(tmap_w, tmap_q, dsh, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, skip, stream);
+    if (wt == kWtIQ4NL)
+        return launch_wt<kWtIQ4NL>(tmap_w, tmap_q, dsh, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, skip, stream);
+    return launch_wt<kWtIQ4XS>(tmap_w, tmap_q, dsh, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, skip, stream);
 }
 
 }  // namespace iq4xs

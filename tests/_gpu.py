@@ -16,23 +16,21 @@ def dev(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def quantize_gpu(x: np.ndarray, tc: bool = True):
+def quantize_gpu(x: np.ndarray):
     """Q8_1 on the GPU with every output poisoned first."""
     M, K = x.shape
     xd = dev(x)
-    qs, ds, op = B.alloc_activations(M, K, "cuda", tc=tc)
+    qs, ds = B.alloc_activations(M, K, "cuda")
     qs.fill_(0x55)
     ds.view(torch.int16).fill_(0x7E00)  # fp16 NaN
-    if op is not None:
-        op.fill_(0xFF)  # fp16 NaN pattern / fp32 NaN in the scale part
-    B.iq4xs_quantize_q8_1(xd, qs, ds, op)
-    return qs, ds, op
+    B.iq4xs_quantize_q8_1(xd, qs, ds)
+    return qs, ds
 
 
-def matmul_gpu(wd: torch.Tensor, N: int, K: int, qs, ds, op, M: int, path, ldy: int | None = None):
+def matmul_gpu(wd: torch.Tensor, N: int, K: int, qs, ds, M: int, path, ldy: int | None = None):
     ldy = N if ldy is None else ldy
     y = torch.full((M, ldy), float("nan"), dtype=torch.float32, device="cuda")
-    B.iq4xs_matmul(wd, N, K, qs, ds, op, M, y, path)
+    B.iq4xs_matmul(wd, N, K, qs, ds, M, y, path)
     torch.cuda.synchronize()
     return y.cpu().numpy()
 

@@ -19,10 +19,41 @@ def lib():
 def test_header_declares_the_entry_points():
     names = set(B.header_functions())
     assert {"iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_dequantize", "iq4xs_select_path",
-            "iq4xs_tc_operand_bytes", "iq4xs_set_crossover", "iq4xs_set_baseline_threshold",
+            "iq4xs_set_crossover", "iq4xs_set_baseline_threshold",
             "iq4xs_last_device_error",
             "iq4xs_status_string", "iq4xs_linear", "iq4xs_linear_workspace_bytes",
             "iq4xs_matmul_wt", "iq4xs_dequantize_wt", "iq4xs_weight_bytes"} <= names
+
+
+def _prototype(name):
+    """Parameter list of `name` in include/iq4xs.h, as (type, name) pairs."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", open(B.HEADER).read(), flags=re.S)
+    m = re.search(r"\b" + name + r"\s*\(([^)]*)\)\s*;", text)
+    assert m, name
+    out = []
+    for p in m.group(1).split(","):
+        p = " ".join(p.replace("*", " * ").split())
+        typ, _, pname = p.rpartition(" ")
+        out.append((typ.replace(" *", "*"), pname))
+    return out
+
+
+def test_boundary_prototypes():
+    """The four calls of the boundary, with exactly these parameters (plain
+    pointers and sizes, stream as int64)."""
+    assert _prototype("iq4xs_quantize_q8_1") == [
+        ("const float*", "x"), ("int64_t", "M"), ("int64_t", "K"), ("int64_t", "ldx"),
+        ("int8_t*", "qs"), ("void*", "ds"), ("int64_t", "stream")]
+    assert _prototype("iq4xs_matmul") == [
+        ("const void*", "w"), ("int64_t", "N"), ("int64_t", "K"), ("const int8_t*", "qs"),
+        ("const void*", "ds"), ("int64_t", "M"), ("float*", "y"), ("int64_t", "ldy"),
+        ("int", "path"), ("int64_t", "stream")]
+    assert _prototype("iq4xs_dequantize") == [
+        ("const void*", "w"), ("int64_t", "N"), ("int64_t", "K"), ("void*", "out"),
+        ("int", "out_dtype"), ("int64_t", "stream")]
+    assert _prototype("iq4xs_select_path") == [
+        ("int64_t", "M"), ("int64_t", "N"), ("int64_t", "K"), ("int*", "path_out")]
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -69,20 +100,9 @@ def test_baseline_threshold_is_advice_above_the_tc_range(lib):
     # the library's own calls never take the advice as an explicit path
     out = ctypes.c_int()
     rc = lib.iq4xs_matmul(ctypes.c_void_p(16), 256, 512, ctypes.c_void_p(16), ctypes.c_void_p(16),
-                          ctypes.c_void_p(16), 8, ctypes.c_void_p(16), 256, B.PATH_BASELINE, 0)
+                          8, ctypes.c_void_p(16), 256, B.PATH_BASELINE, 0)
     assert rc == B.ERR_ARG, rc
     B._install_calibration(lib)
-
-
-def test_tc_operand_bytes(lib):
-    # M rounds up to a multiple of 16 (max 128 per tile); q*d as an exact
-    # fp16 pair (4 bytes) per padded activation element, plus one fp32 power
-    # of two per padded row and span of 1024 values
-    assert B.iq4xs_tc_operand_bytes(1, 1024) == 16 * 1024 * 4 + 16 * 1 * 4
-    assert B.iq4xs_tc_operand_bytes(96, 4096) == 96 * 4096 * 4 + 96 * 4 * 4
-    assert B.iq4xs_tc_operand_bytes(129, 512) == 2 * 128 * 512 * 4 + 2 * 128 * 1 * 4
-    assert B.iq4xs_tc_operand_bytes(0, 1024) == 0
-    assert B.iq4xs_tc_operand_bytes(4, 1000) == 0
 
 
 def test_argument_errors_return_before_any_launch(lib):
@@ -90,25 +110,30 @@ def test_argument_errors_return_before_any_launch(lib):
     odd = ctypes.c_void_p(0x10008)
     vp = ctypes.c_void_p
     # null pointers
-    assert lib.iq4xs_matmul(None, 8, 256, p, p, p, 1, p, 8, 0, 0) == B.ERR_ARG
-    assert lib.iq4xs_quantize_q8_1(None, 1, 256, 256, p, p, None, 0) == B.ERR_ARG
+    assert lib.iq4xs_matmul(None, 8, 256, p, p, 1, p, 8, 0, 0) == B.ERR_ARG
+    assert lib.iq4xs_matmul(p, 8, 256, None, p, 1, p, 8, 0, 0) == B.ERR_ARG
+    assert lib.iq4xs_matmul(p, 8, 256, p, None, 1, p, 8, 0, 0) == B.ERR_ARG
+    assert lib.iq4xs_matmul(p, 8, 256, p, p, 1, None, 8, 0, 0) == B.ERR_ARG
+    assert lib.iq4xs_quantize_q8_1(None, 1, 256, 256, p, p, 0) == B.ERR_ARG
+    assert lib.iq4xs_quantize_q8_1(p, 1, 256, 256, p, None, 0) == B.ERR_ARG
     assert lib.iq4xs_dequantize(p, 8, 256, None, 0, 0) == B.ERR_ARG
     # shapes
-    assert lib.iq4xs_matmul(p, 8, 300, p, p, p, 1, p, 8, 0, 0) == B.ERR_SHAPE
-    assert lib.iq4xs_matmul(p, 8, 256, p, p, p, 0, p, 8, 0, 0) == B.ERR_SHAPE
-    assert lib.iq4xs_matmul(p, 0, 256, p, p, p, 1, p, 8, 0, 0) == B.ERR_SHAPE
-    assert lib.iq4xs_quantize_q8_1(p, 1, 100, 100, p, p, None, 0) == B.ERR_SHAPE
+    assert lib.iq4xs_matmul(p, 8, 300, p, p, 1, p, 8, 0, 0) == B.ERR_SHAPE
+    assert lib.iq4xs_matmul(p, 8, 256, p, p, 0, p, 8, 0, 0) == B.ERR_SHAPE
+    assert lib.iq4xs_matmul(p, 0, 256, p, p, 1, p, 8, 0, 0) == B.ERR_SHAPE
+    assert lib.iq4xs_quantize_q8_1(p, 1, 100, 100, p, p, 0) == B.ERR_SHAPE
     # bad ldy / ldx / path / dtype
-    assert lib.iq4xs_matmul(p, 8, 256, p, p, p, 1, p, 4, 0, 0) == B.ERR_ARG
-    assert lib.iq4xs_matmul(p, 8, 256, p, p, p, 1, p, 8, 7, 0) == B.ERR_ARG
-    assert lib.iq4xs_quantize_q8_1(p, 1, 256, 255, p, p, None, 0) == B.ERR_ARG
+    assert lib.iq4xs_matmul(p, 8, 256, p, p, 1, p, 4, 0, 0) == B.ERR_ARG
+    assert lib.iq4xs_matmul(p, 8, 256, p, p, 1, p, 8, 7, 0) == B.ERR_ARG
+    assert lib.iq4xs_quantize_q8_1(p, 1, 256, 255, p, p, 0) == B.ERR_ARG
     assert lib.iq4xs_dequantize(p, 8, 256, p, 5, 0) == B.ERR_ARG
-    # alignment
-    assert lib.iq4xs_matmul(odd, 8, 256, p, p, p, 1, p, 8, 1, 0) == B.ERR_ALIGN
-    assert lib.iq4xs_quantize_q8_1(odd, 1, 256, 256, p, p, None, 0) == B.ERR_ALIGN
-    # the tensor-core path needs K % 512 == 0 and its operand
-    assert lib.iq4xs_matmul(p, 8, 768, p, p, p, 1, p, 8, 2, 0) == B.ERR_SHAPE
-    assert lib.iq4xs_matmul(p, 8, 512, p, p, None, 1, p, 8, 2, 0) == B.ERR_ARG
+    # alignment: W, qs (16 bytes), ds (4 bytes)
+    assert lib.iq4xs_matmul(odd, 8, 256, p, p, 1, p, 8, 1, 0) == B.ERR_ALIGN
+    assert lib.iq4xs_matmul(p, 8, 256, odd, p, 1, p, 8, 1, 0) == B.ERR_ALIGN
+    assert lib.iq4xs_matmul(p, 8, 256, p, ctypes.c_void_p(0x10002), 1, p, 8, 1, 0) == B.ERR_ALIGN
+    assert lib.iq4xs_quantize_q8_1(odd, 1, 256, 256, p, p, 0) == B.ERR_ALIGN
+    # the tensor-core path needs K % 512 == 0
+    assert lib.iq4xs_matmul(p, 8, 768, p, p, 1, p, 8, 2, 0) == B.ERR_SHAPE
 
 
 def test_weight_formats_sizes_and_argument_errors(lib):
@@ -119,21 +144,21 @@ def test_weight_formats_sizes_and_argument_errors(lib):
     assert B.iq4xs_weight_bytes(3, 3, 512) == 0 and B.iq4xs_weight_bytes(1, 3, 96) == 0
     p = ctypes.c_void_p(0x10000)
     for wt in (0, 1, 2):
-        assert lib.iq4xs_matmul_wt(None, wt, 8, 256, p, p, p, 1, p, 8, 0, 0) == B.ERR_ARG
-        assert lib.iq4xs_matmul_wt(p, wt, 8, 288, p, p, p, 1, p, 8, 0, 0) == B.ERR_SHAPE
-        assert lib.iq4xs_matmul_wt(p, wt, 8, 768, p, p, p, 1, p, 8, 2, 0) == B.ERR_SHAPE
-        assert lib.iq4xs_matmul_wt(ctypes.c_void_p(0x10004), wt, 8, 256, p, p, p, 1, p, 8, 1,
+        assert lib.iq4xs_matmul_wt(None, wt, 8, 256, p, p, 1, p, 8, 0, 0) == B.ERR_ARG
+        assert lib.iq4xs_matmul_wt(p, wt, 8, 288, p, p, 1, p, 8, 0, 0) == B.ERR_SHAPE
+        assert lib.iq4xs_matmul_wt(p, wt, 8, 768, p, p, 1, p, 8, 2, 0) == B.ERR_SHAPE
+        assert lib.iq4xs_matmul_wt(ctypes.c_void_p(0x10004), wt, 8, 256, p, p, 1, p, 8, 1,
                                    0) == B.ERR_ALIGN
         assert lib.iq4xs_dequantize_wt(p, wt, 8, 256, p, 2, 0) == B.ERR_ARG
     for bad in (-1, 3, 99):
-        assert lib.iq4xs_matmul_wt(p, bad, 8, 256, p, p, p, 1, p, 8, 0, 0) == B.ERR_ARG
+        assert lib.iq4xs_matmul_wt(p, bad, 8, 256, p, p, 1, p, 8, 0, 0) == B.ERR_ARG
         assert lib.iq4xs_dequantize_wt(p, bad, 8, 256, p, 0, 0) == B.ERR_ARG
 
 
 @pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="host without a GPU only")
 def test_valid_call_without_gpu_reports_device_error(lib):
     p = ctypes.c_void_p(0x10000)
-    assert lib.iq4xs_matmul(p, 8, 256, p, p, p, 1, p, 8, 1, 0) == B.ERR_DEVICE
+    assert lib.iq4xs_matmul(p, 8, 256, p, p, 1, p, 8, 1, 0) == B.ERR_DEVICE
 
 
 def test_status_strings(lib):
@@ -143,10 +168,10 @@ def test_status_strings(lib):
 
 def test_linear_workspace_and_validation(lib):
     B.iq4xs_set_crossover(4)
-    # dp4a path: qs + ds only; tensor-core path adds the operand
+    # qs, then ds 16-byte aligned, on either path: 1.125 bytes per activation
     assert B.iq4xs_linear_workspace_bytes(2, 4096, 4096) == 2 * 4096 + 2 * 128 * 4
-    assert (B.iq4xs_linear_workspace_bytes(96, 4096, 4096) ==
-            96 * 4096 + 96 * 128 * 4 + B.iq4xs_tc_operand_bytes(96, 4096))
+    assert B.iq4xs_linear_workspace_bytes(96, 4096, 4096) == 96 * 4096 + 96 * 128 * 4
+    assert B.iq4xs_linear_workspace_bytes(3, 8, 256) == 3 * 256 + 3 * 8 * 4
     assert B.iq4xs_linear_workspace_bytes(0, 8, 256) == 0
     p = ctypes.c_void_p(0x10000)
     need = B.iq4xs_linear_workspace_bytes(96, 4096, 4096)
@@ -169,3 +194,25 @@ def test_grouped_argument_errors_return_before_any_launch(lib):
     assert f(p, stride, 2, N, K, p, p, p, 0, p, N, 0) == B.ERR_ARG        # no rows
     assert f(p, stride, 2, N, K, p, p, p, 1, p, N - 1, 0) == B.ERR_ARG    # ldy < N
     assert f(ctypes.c_void_p(264), stride, 2, N, K, p, p, p, 1, p, N, 0) == B.ERR_ALIGN
+
+
+def test_crossover_classes(lib):
+    B.iq4xs_set_crossover(4)
+    B.iq4xs_set_baseline_threshold(0)
+    try:
+        B.iq4xs_set_crossover_classes([(50_000_000, 2), (150_000_000, 6)])
+        assert B.iq4xs_select_path(4, 4096, 4096) == B.PATH_DP4A      # below every class: 4
+        assert B.iq4xs_select_path(5, 4096, 4096) == B.PATH_TC
+        assert B.iq4xs_select_path(2, 12288, 5120) == B.PATH_DP4A     # 63M weights: 2
+        assert B.iq4xs_select_path(3, 12288, 5120) == B.PATH_TC
+        assert B.iq4xs_select_path(6, 34816, 5120) == B.PATH_DP4A     # 178M weights: 6
+        assert B.iq4xs_select_path(7, 34816, 5120) == B.PATH_TC
+        i64 = ctypes.c_int64
+        assert lib.iq4xs_set_crossover_classes((i64 * 1)(0), (i64 * 1)(3), 1) == B.ERR_ARG
+        assert lib.iq4xs_set_crossover_classes((i64 * 1)(5), (i64 * 1)(-1), 1) == B.ERR_ARG
+        assert lib.iq4xs_set_crossover_classes(None, None, 17) == B.ERR_ARG
+        assert B.iq4xs_select_path(2, 12288, 5120) == B.PATH_DP4A     # unchanged after errors
+        B.iq4xs_set_crossover_classes([])
+        assert B.iq4xs_select_path(4, 12288, 5120) == B.PATH_DP4A
+    finally:
+        B._install_calibration(lib)

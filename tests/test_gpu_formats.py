@@ -37,9 +37,9 @@ def _oracle_wt(wt, w, N, K, qs, d_h, rows=None):
     return orc.matmul_wt(wt, w, N, K, qs, d_h, nthreads=nt)
 
 
-def _matmul_wt(wd, wt, N, K, qs, ds, op, M, path):
+def _matmul_wt(wd, wt, N, K, qs, ds, M, path):
     y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
-    B.iq4xs_matmul_wt(wd, wt, N, K, qs, ds, op, M, y, path)
+    B.iq4xs_matmul_wt(wd, wt, N, K, qs, ds, M, y, path)
     torch.cuda.synchronize()
     return y.cpu().numpy()
 
@@ -64,12 +64,12 @@ def test_formats_match_oracle_on_every_path(name, wt, N, K):
     Ms = (1, 2, 3, 4, 5, 8, 16, 33, 96, 130)
     x = synth.activations(rng, max(Ms), K, outlier_frac=0.01)
     for M in Ms:
-        qs, ds, op = quantize_gpu(x[:M], tc=True)
+        qs, ds = quantize_gpu(x[:M])
         qs_o, d_o, _ = oracle_q8(x[:M])
         ref = _oracle_wt(wt, w, N, K, qs_o, d_o)
         paths = [B.PATH_AUTO, B.PATH_DP4A] + ([B.PATH_TC] if K % 512 == 0 else [])
         for path in paths:
-            y = _matmul_wt(wd, wt, N, K, qs, ds, op, M, path)
+            y = _matmul_wt(wd, wt, N, K, qs, ds, M, path)
             assert gate_written(y) is None, (name, M, path)
             r = gate_parity(y, ref)
             assert r is None, (name, N, K, M, path, r)
@@ -85,9 +85,9 @@ def test_formats_full_size_sampled_rows(name, wt, N, K):
     rows = sample_rows(N, 48, seed=wt)
     for M in ((1, 2, 4, 16, 64, 96) if N == 4096 else (1, 2, 16)):
         x = synth.activations(rng, M, K)
-        qs, ds, op = quantize_gpu(x, tc=True)
+        qs, ds = quantize_gpu(x)
         qs_o, d_o, _ = oracle_q8(x)
-        y = _matmul_wt(wd, wt, N, K, qs, ds, op, M, B.PATH_AUTO)
+        y = _matmul_wt(wd, wt, N, K, qs, ds, M, B.PATH_AUTO)
         assert gate_written(y) is None
         assert gate_parity(y[:, rows], _oracle_wt(wt, w, N, K, qs_o, d_o, rows)) is None, (name, M)
 
@@ -130,9 +130,9 @@ def test_iq4nl_equals_iq4xs_with_uniform_scale_bitwise():
     w_xs, w_nl = dev(xs.reshape(N, -1)), dev(nl.reshape(N, -1))
     x = synth.activations(rng, 40, K)
     for M in (1, 3, 40):
-        qs, ds, op = quantize_gpu(x[:M], tc=True)
+        qs, ds = quantize_gpu(x[:M])
         for path in (B.PATH_DP4A, B.PATH_TC):
-            a = _matmul_wt(w_xs, B.WTYPE_IQ4_XS, N, K, qs, ds, op, M, path)
-            b = _matmul_wt(w_nl, B.WTYPE_IQ4_NL, N, K, qs, ds, op, M, path)
+            a = _matmul_wt(w_xs, B.WTYPE_IQ4_XS, N, K, qs, ds, M, path)
+            b = _matmul_wt(w_nl, B.WTYPE_IQ4_NL, N, K, qs, ds, M, path)
             assert gate_written(a) is None
             assert np.array_equal(a, b), (M, path)

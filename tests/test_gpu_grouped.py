@@ -31,7 +31,7 @@ def _run_grouped(W, rows_x, offsets):
     w = W.weights()
     stride = w.shape[1] * w.shape[2]
     wd = dev(w.reshape(G, -1))
-    qs, ds, _ = quantize_gpu(rows_x, tc=False)
+    qs, ds = quantize_gpu(rows_x)
     off_d = dev(offsets.astype(np.int32))
     M = rows_x.shape[0]
     y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
@@ -57,7 +57,7 @@ def test_grouped_matches_oracle_and_single_expert_calls(T, topk):
         assert r is None, (g, r)
         # the single-expert call on the same rows gives the same bits
         ys = torch.full((r1 - r0, W.N), float("nan"), device="cuda")
-        B.iq4xs_matmul(wd[g], W.N, W.K, qs[r0:r1], ds[r0:r1], None, r1 - r0, ys, B.PATH_DP4A)
+        B.iq4xs_matmul(wd[g], W.N, W.K, qs[r0:r1], ds[r0:r1], r1 - r0, ys, B.PATH_DP4A)
         torch.cuda.synchronize()
         assert np.array_equal(ys.cpu().numpy(), y[r0:r1]), g
     ind = independent_fp32(np.concatenate([w[g] for g in range(W.G)]), W.G * W.N, W.K, qs_o, d_o)
@@ -99,7 +99,7 @@ def test_grouped_empty_experts_and_one_expert_with_every_row():
 def test_grouped_rejects_bad_arguments():
     W = synth.MoEWorkload("moe_arg", seed=1, G=2, N=128, K=512, topk=1, tokens=(2,), d_scale=2e-3)
     w = dev(W.weights().reshape(2, -1))
-    qs, ds, _ = B.alloc_activations(2, W.K, "cuda", tc=False)
+    qs, ds = B.alloc_activations(2, W.K, "cuda")
     off = torch.tensor([0, 1, 2], dtype=torch.int32, device="cuda")
     y = torch.empty((2, W.N), device="cuda")
     stride = w.shape[1]

@@ -39,8 +39,8 @@ def test_linear_matches_two_calls_and_oracle(M):
     yl = y.cpu().numpy()
     assert gate_written(yl) is None
     path = "dp4a" if B.iq4xs_select_path(M, N, K) == B.PATH_DP4A else "tc"
-    qs, ds, op = quantize_gpu(x, tc=(path == "tc"))
-    y2 = matmul_gpu(wd, N, K, qs, ds, op, M, path)
+    qs, ds = quantize_gpu(x)
+    y2 = matmul_gpu(wd, N, K, qs, ds, M, path)
     assert np.array_equal(yl, y2)
     qs_o, d_o, _ = oracle_q8(x)
     rows = sample_rows(N, 40, seed=M)
@@ -65,8 +65,8 @@ def test_linear_small_m_bitwise_and_workspace_q8(M, N, K):
     torch.cuda.synchronize()
     yl = y.cpu().numpy()
     assert gate_written(yl) is None
-    qs, ds, op = quantize_gpu(x, tc=False)
-    assert np.array_equal(yl, matmul_gpu(wd, N, K, qs, ds, None, M, "dp4a"))
+    qs, ds = quantize_gpu(x)
+    assert np.array_equal(yl, matmul_gpu(wd, N, K, qs, ds, M, "dp4a"))
     qs_o, d_o, s_o = oracle_q8(x)
     wsh = ws.cpu().numpy()
     assert np.array_equal(wsh[:M * K].view(np.int8).reshape(M, K), qs_o)

@@ -45,10 +45,10 @@ def check_q8(x, qs, ds):
 
 
 def run_and_gate(w, N, K, x, path, rows=None, ldy=None, independent=True):
-    qs, ds, op = quantize_gpu(x, tc=(path != "dp4a"))
+    qs, ds = quantize_gpu(x)
     qs_o, d_o = check_q8(x, qs, ds)
     M = x.shape[0]
-    y = matmul_gpu(dev(w), N, K, qs, ds, op, M, path, ldy=ldy)
+    y = matmul_gpu(dev(w), N, K, qs, ds, M, path, ldy=ldy)
     assert gate_written(y[:, :N]) is None, gate_written(y[:, :N])
     if ldy is not None and ldy > N:
         assert np.all(np.isnan(y[:, N:])), "columns beyond N must not be written"
@@ -74,7 +74,7 @@ def test_quantize_bit_exact(wl, M):
     idx = 0 if wl != "prefill_sweep" else 1
     _, K = W.shapes[idx]
     x = synth.activations(W.rng(idx, 99), M, K, W.outlier_frac, bf16_round=W.bf16_round)
-    qs, ds, _ = quantize_gpu(x)
+    qs, ds = quantize_gpu(x)
     check_q8(x, qs, ds)
 
 
@@ -84,7 +84,7 @@ def test_quantize_closed_forms():
     for i, c in enumerate(cases):
         x[i, :32] = c["x"]
         x[i, 32:64] = -c["x"] * np.float32(0.125)
-    qs, ds, _ = quantize_gpu(x)
+    qs, ds = quantize_gpu(x)
     check_q8(x, qs, ds)
     q = qs.cpu().numpy()
     for i, c in enumerate(cases):
@@ -136,10 +136,10 @@ def test_matmul_k256_dp4a_only():
     w = synth.iq4xs_weights(rng, 64, 256, 2e-3)
     x = synth.activations(rng, 4, 256)
     run_and_gate(w, 64, 256, x, "dp4a")
-    qs, ds, op = quantize_gpu(x)
+    qs, ds = quantize_gpu(x)
     y = torch.empty((4, 64), dtype=torch.float32, device="cuda")
     with pytest.raises(B.IQ4XSError) as e:
-        B.iq4xs_matmul(dev(w), 64, 256, qs, ds, op, 4, y, "tc")
+        B.iq4xs_matmul(dev(w), 64, 256, qs, ds, 4, y, "tc")
     assert e.value.status == B.ERR_SHAPE
 
 
@@ -242,13 +242,13 @@ def test_dequantize_bit_exact():
 # --------------------------------------------------------------------- dispatch
 def test_auto_matches_explicit_path():
     w, x = synth.TINY.inputs(0, M=8)
-    qs, ds, op = quantize_gpu(x)
+    qs, ds = quantize_gpu(x)
     wd = dev(w)
     for cross in (2, 8):
         B.iq4xs_set_crossover(cross)
         expect = "dp4a" if 8 <= cross else "tc"
-        ya = matmul_gpu(wd, 256, 1024, qs, ds, op, 8, "auto")
-        ye = matmul_gpu(wd, 256, 1024, qs, ds, op, 8, expect)
+        ya = matmul_gpu(wd, 256, 1024, qs, ds, 8, "auto")
+        ye = matmul_gpu(wd, 256, 1024, qs, ds, 8, expect)
         assert np.array_equal(ya, ye)
     B.iq4xs_set_crossover(4)
 
@@ -264,9 +264,9 @@ def test_gate_fires_on_one_corrupted_weight_byte(path):
     """Plant one flipped qs byte in the oracle's copy of W: the parity gate
     must fail for the row that holds it."""
     w, x = synth.TINY.inputs(0, M=4)
-    qs, ds, op = quantize_gpu(x, tc=True)
+    qs, ds = quantize_gpu(x)
     qs_o, d_o, _ = oracle_q8(x)
-    y = matmul_gpu(dev(w), 256, 1024, qs, ds, op, 4, path)
+    y = matmul_gpu(dev(w), 256, 1024, qs, ds, 4, path)
     bad = w.copy()
     bad[17, 136 * 2 + 8 + 40] ^= 0x5A
     assert gate_parity(y, oracle_matmul(w, 256, 1024, qs_o, d_o)) is None
