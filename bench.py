@@ -95,6 +95,45 @@ def hbm_peak_gbs():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def tensor_peak_tflops():
+    """Dense fp16/bf16 tensor peak (TFLOP/s), burst: the tcgen05 kernel runs
+    kind::f16 MMAs on fp16 operands, whose dense rate is the bf16 rate."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16 burst = fp16 dense rate)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def tc_executed_flops(M, N, K):
+    """Floating-point work the tensor cores execute for one tcgen05 launch:
+    128-row tiles x activation tiles padded to 16 rows (at most 128), two
+    128 x MT x 16 MMAs per 32-weight sub-block (exact fp16 integers)."""
+    mt = min(128, (M + 15) // 16 * 16)
+    mtiles = -(-M // mt)
+    return 2 * (-(-N // 128) * 128) * (mtiles * mt) * K
+
+
+ROOFLINE_SLACK = 1.10
+
+
+def roofline_gate(items, peak_gbs, slack=ROOFLINE_SLACK):
+    """items: (name, algorithmic bytes, seconds).  A call reported faster
+    than its bytes allow (more than `slack` x the measured HBM rate) did not
+    do its work; every such call is listed."""
+    bad = []
+    for name, nbytes, sec in items:
+        gbs = nbytes / sec / 1e9 if sec > 0 else float("inf")
+        if gbs > slack * peak_gbs:
+            bad.append({"call": name, "GBps": round(gbs, 1)})
+    return {"slack": slack, "peak_gbs": peak_gbs, "checked": len(items), "violations": bad,
+            "ok": not bad}
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -103,10 +142,10 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per tcgen05 matmul launch (mean over M = 8..96 of the sweep)
-    from the committed ncu summary, or None if absent or taken on different
-    kernel sources."""
+def recorded_counters():
+    """Per tcgen05 matmul launch (mean over the sweep's tcgen05 M) from the
+    committed ncu summary: DRAM bytes and warp instructions executed.  Empty
+    if absent or taken on different kernel sources."""
     try:
         vals = {}
         with open(TRAFFIC_FILE) as f:
@@ -115,10 +154,17 @@ def recorded_traffic():
                     k, v = line.split(":", 1)
                     vals[k.strip()] = v.strip()
         if vals.get("kernel_source_sha256_16") != kernel_source_hash():
-            return None
-        return float(vals["dram_bytes_per_tc_launch_mean"])
+            return {}
+        out = {"dram_bytes": float(vals["dram_bytes_per_tc_launch_mean"])}
+        if "inst_executed_per_tc_launch_mean" in vals:
+            out["inst"] = float(vals["inst_executed_per_tc_launch_mean"])
+        return out
     except Exception:
-        return None
+        return {}
+
+
+def recorded_traffic():
+    return recorded_counters().get("dram_bytes")
 
 
 # ------------------------------------------------------------------------ clocks
@@ -365,6 +411,33 @@ def run_ours(args, world, rank, local):
     mm_bytes = sum(matmul_bytes(M, N, K) for M in ms)
     mm_us_total = sum(mm_us.values())
 
+    # Tensor roofline of the same kernel: the method's 2*M*N*K and the fp16
+    # MMA work the tensor cores execute (padded tiles), against the dense
+    # fp16 peak.  Issue roofline: warp instructions per launch (ncu, same
+    # sources) against 4 per SM and cycle at the sampled SM clock.
+    tpeak, tpeak_kind = tensor_peak_tflops()
+    tc_method = sum(2 * M * N * K for M in tc_ms) / (tc_us * 1e-6) / 1e12
+    tc_exec = sum(tc_executed_flops(M, N, K) for M in tc_ms) / (tc_us * 1e-6) / 1e12
+    tensor = {"achieved": tc_exec, "peak": tpeak, "unit": "TFLOP/s", "frac": tc_exec / tpeak,
+              "method_tops": tc_method, "method_frac": tc_method / tpeak,
+              "peak_kind": tpeak_kind,
+              "counts": "achieved = executed fp16 MMA flops (two 128 x MT x 16 MMAs per "
+                        "sub-block, padded tiles); method_tops = 2*M*N*K"}
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    inst = recorded_counters().get("inst") if not args.shape else None
+    issue = None
+    if inst and clk.get("sm_mhz"):
+        ipeak = nsm * 4 * clk["sm_mhz"] * 1e6 / 1e12  # T warp-instructions / s
+        ach = inst / (tc_us / len(tc_ms) * 1e-6) / 1e12
+        issue = {"achieved": ach, "peak": ipeak, "unit": "Twarp-inst/s", "frac": ach / ipeak,
+                 "inst_per_launch": inst,
+                 "peak_kind": f"{nsm} SMs x 4 issue slots x sampled SM clock"}
+    fracs = {"hbm": achieved / peak, "tensor": tensor["frac"]}
+    if issue:
+        fracs["alu"] = issue["frac"]
+    binding = max(fracs, key=fracs.get)
+    gate_items = [(f"matmul M={M} {N}x{K}", matmul_bytes(M, N, K), mm_us[M] * 1e-6) for M in ms]
+
     sbytes = step_bytes(ms, N, K)
     ms_per_step = ms_total / args.steps
     value = world * sbytes / (ms_per_step * 1e-3) / 1e9
@@ -382,6 +455,12 @@ def run_ours(args, world, rank, local):
         extras["weight_formats"] = weight_formats(torch, B, dev, stream, mm_us)
         extras["decoder_shapes"] = decoder_shapes(torch, B, dev, stream)
         extras["prefill_sweep"] = prefill_sweep(torch, B, dev, stream)
+        for r in extras["decoder_shapes"]:
+            gate_items.append((f"matmul M={r['M']} {r['N']}x{r['K']}", matmul_bytes(r["M"], r["N"], r["K"]),
+                               r["us"] * 1e-6))
+        for r in extras["weight_formats"]:
+            gate_items.append((f"{r['format']} M={r['M']}", r["GBps"] * 1e9 * r["us"] * 1e-6,
+                               r["us"] * 1e-6))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -411,7 +490,10 @@ def run_ours(args, world, rank, local):
                          "traffic_algorithmic": tc_bytes / len(tc_ms),
                          "kernel": f"matmul_tc_kernel (tcgen05), M in {tc_ms}: algorithmic "
                                    "bytes per launch / mean launch time",
-                         "peak_kind": peak_kind, "timing": mm_timing},
+                         "peak_kind": peak_kind, "timing": mm_timing,
+                         "tensor": tensor, "alu": issue, "binding": binding,
+                         "binding_rule": "the roofline with the largest fraction"},
+            "roofline_gate": roofline_gate(gate_items, peak),
             "matmul_all": {"achieved_gbs": mm_bytes / (mm_us_total * 1e-6) / 1e9,
                            "frac": mm_bytes / (mm_us_total * 1e-6) / 1e9 / peak,
                            "kernels": "dp4a for M <= crossover, tcgen05 above, whole sweep"},

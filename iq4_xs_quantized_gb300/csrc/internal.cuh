@@ -178,6 +178,7 @@ enum DeviceError : int {
     kDevErrTimeoutRecv = 0x107,
     kDevErrTimeoutQ = 0x108,
     kDevErrTimeoutX = 0x109,
+    kDevErrLayout = 0x10A,  // dynamic shared memory not 1024-byte aligned
 };
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
 

@@ -108,3 +108,15 @@ def test_crossover_rule_weighs_shapes_alike():
     assert calibrate.crossover_from(as_json, range(1, 6)) == 4
     # dp4a never faster -> 0
     assert calibrate.crossover_from({"s": {1: row(9.0, 7.0)}}, range(1, 2)) == 0
+
+
+def test_tensor_work_and_roofline_gate():
+    # padded tiles: M = 8 runs a 16-row tile (twice the method's work); M = 129
+    # two 128-row tiles; N = 130 two 128-row weight tiles
+    assert bench.tc_executed_flops(16, 4096, 4096) == 2 * 16 * 4096 * 4096
+    assert bench.tc_executed_flops(8, 4096, 4096) == 2 * 16 * 4096 * 4096
+    assert bench.tc_executed_flops(129, 256, 512) == 2 * 256 * 256 * 512
+    assert bench.tc_executed_flops(1, 130, 512) == 2 * 256 * 16 * 512
+    g = bench.roofline_gate([("fast", 9.25e6, 0.5e-6), ("ok", 9.25e6, 2.0e-6)], 6800.0)
+    assert not g["ok"] and [v["call"] for v in g["violations"]] == ["fast"]
+    assert bench.roofline_gate([("ok", 9.25e6, 2.0e-6)], 6800.0)["ok"]
