@@ -58,6 +58,14 @@
  *      ds  half2 [M][K/32]  {d = amax/127, s = d*sum(q)} each rounded to fp16
  *      Both matmul paths read these two arrays as they are (1.125 bytes per
  *      activation); qs must be 16-byte aligned, ds 4-byte aligned.
+ *  Prepared tensor-core operand (opaque; iq4xs_quantize_q8_1_tc writes it
+ *      beside qs and ds, iq4xs_matmul_tc_operand reads it): each value q*d
+ *      (d the block's stored fp16 scale) held exactly as a pair of fp16
+ *      values, tiled for the tcgen05 kernel; iq4xs_tc_operand_bytes(M, K) =
+ *      4 * Mpad * K + 4 * Mpad * ceil(K/1024) bytes (Mpad = M rounded up to
+ *      the tile height), 16-byte aligned.  It costs the quantizer one more
+ *      write of 4 bytes per activation and spares every CTA of the matmul
+ *      the conversion of the codes and the activation scaling.
  *  y: fp32 [M][ldy] row-major, ldy >= N; columns N..ldy-1 are not written.
  */
 #ifndef IQ4XS_H
@@ -131,6 +139,18 @@ int iq4xs_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx,
                         int8_t* qs, void* ds, int64_t stream);
 
 /*
+ * iq4xs_quantize_q8_1 that also writes the prepared tensor-core operand
+ * (layout above; padding rows written as zeros) for iq4xs_matmul_tc_operand.
+ * tc_operand: iq4xs_tc_operand_bytes(M, K) bytes, 16-byte aligned, non-NULL.
+ * qs and ds are written exactly as iq4xs_quantize_q8_1 writes them.
+ */
+int iq4xs_quantize_q8_1_tc(const float* x, int64_t M, int64_t K, int64_t ldx,
+                           int8_t* qs, void* ds, void* tc_operand, int64_t stream);
+
+/* Bytes of the prepared tensor-core operand for (M, K); 0 if invalid. */
+int64_t iq4xs_tc_operand_bytes(int64_t M, int64_t K);
+
+/*
  * Batched matmul y = x . W^T from IQ4_XS W and Q8_1 x (engine page,
  * new-kernel table and tile-geometry passage: per-32 sub-block integer dot
  * products scaled by d_w*(ls-32)*d_x into fp32).
@@ -151,6 +171,21 @@ int iq4xs_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx,
  */
 int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds,
                  int64_t M, float* y, int64_t ldy, int path, int64_t stream);
+
+/*
+ * The tensor-core matmul from the prepared operand (the faster form of the
+ * TC path: the same kernel with d_x folded into exact fp16 hi / lo operand
+ * pairs, four MMAs per 32-weight sub-block instead of two, no conversion in
+ * the kernel and one FMA per result in its epilogue).  Each sub-block's
+ * d_x*sum(kv*q) then carries the tensor core's fp32 accumulation rounding
+ * (every product is exact); the bar is the same as iq4xs_matmul's.
+ *   w           weights in format wtype (iq4xs_wtype), 16-byte aligned.
+ *   tc_operand  from iq4xs_quantize_q8_1_tc for the same M and K.
+ * K % 512 == 0, else IQ4XS_ERR_SHAPE; other errors as for iq4xs_matmul.
+ */
+int iq4xs_matmul_tc_operand(const void* w, int wtype, int64_t N, int64_t K,
+                            const void* tc_operand, int64_t M, float* y, int64_t ldy,
+                            int64_t stream);
 
 /*
  * iq4xs_matmul for a weight in any iq4xs_wtype (IQ4XS_WTYPE_IQ4_XS is
@@ -200,10 +235,15 @@ int iq4xs_matmul_grouped(const void* w, int64_t expert_stride, int64_t G, int64_
  * iq4xs_select_path picks; the second launch overlaps the first's tail
  * (programmatic dependent launch).
  *   x          fp32 [M][ldx], as for iq4xs_quantize_q8_1.
- *   workspace  device scratch owned by the caller, 16-byte aligned, at least
- *              iq4xs_linear_workspace_bytes(M, N, K) bytes (M*K bytes of qs
- *              rounded up to 16, then M*K/32*4 bytes of ds rounded up to 16);
- *              its contents on return are those Q8_1 activations.
+ *   workspace  device scratch owned by the caller, 16-byte aligned, of
+ *              workspace_bytes >= iq4xs_linear_workspace_min_bytes(M, N, K)
+ *              (M*K bytes of qs rounded up to 16, then M*K/32*4 bytes of ds
+ *              rounded up to 16): its contents on return are those Q8_1
+ *              activations.  On the TC path, with workspace_bytes >=
+ *              iq4xs_linear_workspace_bytes(M, N, K) (the prepared operand
+ *              after them), the faster prepared form runs
+ *              (iq4xs_quantize_q8_1_tc + iq4xs_matmul_tc_operand); with less,
+ *              the Q8_1 form (iq4xs_quantize_q8_1 + iq4xs_matmul).
  * Errors as for the two calls it makes; IQ4XS_ERR_ARG if the workspace is
  * too small.
  */
@@ -211,8 +251,10 @@ int iq4xs_linear(const void* w, int64_t N, int64_t K, const float* x, int64_t M,
                  float* y, int64_t ldy, void* workspace, int64_t workspace_bytes,
                  int64_t stream);
 
-/* Workspace bytes iq4xs_linear needs for (M, N, K); 0 if the shape is invalid. */
+/* Workspace bytes for iq4xs_linear's fastest form at (M, N, K), and the
+ * least it accepts (the Q8_1 codes and scales); 0 if the shape is invalid. */
 int64_t iq4xs_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int64_t iq4xs_linear_workspace_min_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
  * iq4xs_linear without a caller workspace: the same projection, with its
@@ -225,10 +267,11 @@ int64_t iq4xs_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *   - Allocates nothing and calls no allocating routine.  The array is
  *     created when the library is loaded and every GPU that loads it holds
  *     it until the process exits.
- *   - Size limit: iq4xs_linear_workspace_bytes(M, N, K), about 1.125*M*K
- *     bytes on either path, must not exceed iq4xs_linear_static_max_bytes()
+ *   - Size limit: iq4xs_linear_workspace_min_bytes(M, N, K), about
+ *     1.125*M*K bytes, must not exceed iq4xs_linear_static_max_bytes()
  *     (8 MiB: M <= 428 at K = 17408, M <= 1456 at K = 5120); larger
- *     requests return IQ4XS_ERR_SHAPE and launch nothing.
+ *     requests return IQ4XS_ERR_SHAPE and launch nothing.  Where the
+ *     prepared tensor-core operand fits as well, the faster form runs.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before
  *     any stream capture.

@@ -53,6 +53,12 @@ def load(path: str | None = None):
         lib = ctypes.CDLL(p)
         i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
         lib.iq4xs_quantize_q8_1.argtypes = [vp, i64, i64, i64, vp, vp, i64]
+        lib.iq4xs_quantize_q8_1_tc.argtypes = [vp, i64, i64, i64, vp, vp, vp, i64]
+        lib.iq4xs_tc_operand_bytes.argtypes = [i64, i64]
+        lib.iq4xs_tc_operand_bytes.restype = i64
+        lib.iq4xs_matmul_tc_operand.argtypes = [vp, ci, i64, i64, vp, i64, vp, i64, i64]
+        lib.iq4xs_linear_workspace_min_bytes.argtypes = [i64, i64, i64]
+        lib.iq4xs_linear_workspace_min_bytes.restype = i64
         lib.iq4xs_matmul.argtypes = [vp, i64, i64, vp, vp, i64, vp, i64, ci, i64]
         lib.iq4xs_dequantize.argtypes = [vp, i64, i64, vp, ci, i64]
         lib.iq4xs_matmul_wt.argtypes = [vp, ci, i64, i64, vp, vp, i64, vp, i64, ci, i64]
@@ -81,6 +87,7 @@ def load(path: str | None = None):
                      "iq4xs_dequantize", "iq4xs_linear", "iq4xs_matmul_wt", "iq4xs_dequantize_wt",
                      "iq4xs_select_path", "iq4xs_set_crossover", "iq4xs_set_baseline_threshold",
                      "iq4xs_set_crossover_classes", "iq4xs_test_skip_w_stage",
+                     "iq4xs_quantize_q8_1_tc", "iq4xs_matmul_tc_operand",
                      "iq4xs_last_device_error"):
             getattr(lib, name).restype = ci
         if path is None:
@@ -137,6 +144,27 @@ def iq4xs_quantize_q8_1(x, qs, ds, stream=None) -> None:
     _check("iq4xs_quantize_q8_1", rc)
 
 
+def iq4xs_tc_operand_bytes(M: int, K: int) -> int:
+    return int(load().iq4xs_tc_operand_bytes(M, K))
+
+
+def iq4xs_quantize_q8_1_tc(x, qs, ds, tc_operand, stream=None) -> None:
+    """iq4xs_quantize_q8_1 that also writes the prepared tensor-core operand
+    (uint8 device tensor of iq4xs_tc_operand_bytes(M, K) bytes)."""
+    M, K = x.shape
+    rc = load().iq4xs_quantize_q8_1_tc(_ptr(x), M, K, x.stride(0), _ptr(qs), _ptr(ds),
+                                       _ptr(tc_operand), _stream(stream))
+    _check("iq4xs_quantize_q8_1_tc", rc)
+
+
+def iq4xs_matmul_tc_operand(w, N: int, K: int, tc_operand, M: int, y, wtype=WTYPE_IQ4_XS,
+                            stream=None) -> None:
+    """The tensor-core matmul from the prepared operand."""
+    rc = load().iq4xs_matmul_tc_operand(_ptr(w), _wtype(wtype), N, K, _ptr(tc_operand), M, _ptr(y),
+                                        y.stride(0), _stream(stream))
+    _check("iq4xs_matmul_tc_operand", rc)
+
+
 def iq4xs_matmul(w, N: int, K: int, qs, ds, M: int, y, path=PATH_AUTO, stream=None) -> None:
     """y fp32 [M, ldy] = x . W^T from IQ4_XS bytes w and Q8_1 activations."""
     if isinstance(path, str):
@@ -167,6 +195,10 @@ def iq4xs_matmul_wt(w, wtype, N: int, K: int, qs, ds, M: int, y, path=PATH_AUTO,
 
 def iq4xs_linear_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(load().iq4xs_linear_workspace_bytes(M, N, K))
+
+
+def iq4xs_linear_workspace_min_bytes(M: int, N: int, K: int) -> int:
+    return int(load().iq4xs_linear_workspace_min_bytes(M, N, K))
 
 
 def iq4xs_linear(w, N: int, K: int, x, y, workspace, stream=None) -> None:
@@ -269,6 +301,11 @@ def alloc_activations(M: int, K: int, device="cuda"):
     qs = torch.empty((M, K), dtype=torch.int8, device=device)
     ds = torch.empty((M, K // 32, 2), dtype=torch.float16, device=device)
     return qs, ds
+
+
+def alloc_tc_operand(M: int, K: int, device="cuda"):
+    """A uint8 device buffer for the prepared tensor-core operand."""
+    return torch.empty(iq4xs_tc_operand_bytes(M, K), dtype=torch.uint8, device=device)
 
 
 def linear(w, N: int, K: int, x, path=PATH_AUTO, stream=None, out=None, allow_baseline=False):

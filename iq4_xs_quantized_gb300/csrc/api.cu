@@ -128,7 +128,27 @@ int iq4xs_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx, int8_
     DevState* st;
     int rc = device_state(&st);
     if (rc) return rc;
-    return from_cuda(launch_quantize_q8_1(x, M, K, ldx, qs, ds, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(
+        launch_quantize_q8_1(x, M, K, ldx, qs, ds, nullptr, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int64_t iq4xs_tc_operand_bytes(int64_t M, int64_t K) {
+    if (M < 1 || M > kMaxM || K <= 0 || K % kQK || K > (1 << 30)) return 0;
+    return tc_operand_total_bytes(M, K);
+}
+
+int iq4xs_quantize_q8_1_tc(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs, void* ds,
+                           void* tc_operand, int64_t stream) {
+    if (!x || !qs || !ds || !tc_operand) return IQ4XS_ERR_ARG;
+    if (M < 1 || M > kMaxM || K <= 0 || K % kQK) return IQ4XS_ERR_SHAPE;
+    if (ldx < K || (ldx * 4) % 16) return IQ4XS_ERR_ARG;
+    if (!aligned(x, 16) || !aligned(qs, 16) || !aligned(ds, 4) || !aligned(tc_operand, 16))
+        return IQ4XS_ERR_ALIGN;
+    DevState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    return from_cuda(launch_quantize_q8_1(x, M, K, ldx, qs, ds, tc_operand,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int64_t iq4xs_weight_bytes(int wtype, int64_t N, int64_t K) {
@@ -158,17 +178,34 @@ int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (path == IQ4XS_PATH_TC)
-        return from_cuda(launch_matmul_tc(w, wtype, N, K, qs, ds, M, y, ldy, st->encode, st->err,
-                                          st->num_sms, g_skip_w_stage.exchange(-1), s));
+        return from_cuda(launch_matmul_tc(w, wtype, N, K, qs, ds, nullptr, M, y, ldy, st->encode,
+                                          st->err, st->num_sms, g_skip_w_stage.exchange(-1), s));
     return from_cuda(launch_matmul_dp4a(w, wtype, N, K, qs, ds, M, y, ldy, st->num_sms, s));
+}
+
+int iq4xs_matmul_tc_operand(const void* w, int wtype, int64_t N, int64_t K, const void* tc_operand,
+                            int64_t M, float* y, int64_t ldy, int64_t stream) {
+    if (!w || !tc_operand || !y) return IQ4XS_ERR_ARG;
+    if (wtype < IQ4XS_WTYPE_IQ4_XS || wtype > IQ4XS_WTYPE_IQ4_NL) return IQ4XS_ERR_ARG;
+    if (M < 1 || M > kMaxM || N < 1 || N > (1 << 30) || K <= 0 || K % kPairK || K > (1 << 30))
+        return IQ4XS_ERR_SHAPE;
+    if (ldy < N) return IQ4XS_ERR_ARG;
+    if (!aligned(w, 16) || !aligned(tc_operand, 16) || !aligned(y, 4)) return IQ4XS_ERR_ALIGN;
+    DevState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    return from_cuda(launch_matmul_tc(w, wtype, N, K, nullptr, nullptr, tc_operand, M, y, ldy,
+                                      st->encode, st->err, st->num_sms, g_skip_w_stage.exchange(-1),
+                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
 namespace {
 inline int64_t align16(int64_t v) { return (v + 15) / 16 * 16; }
 // Workspace of iq4xs_linear: the Q8_1 codes, then (16-byte aligned) the
-// {d, s} pairs -- 1.125 bytes per activation on either path.
+// {d, s} pairs -- `q8` bytes, 1.125 per activation -- and on the
+// tensor-core path the prepared operand after them (`total`).
 struct LinearLayout {
-    int64_t qs, ds, total;
+    int64_t qs, ds, op, q8, total;
     int path;
 };
 bool linear_layout(int64_t M, int64_t N, int64_t K, LinearLayout* L) {
@@ -177,7 +214,9 @@ bool linear_layout(int64_t M, int64_t N, int64_t K, LinearLayout* L) {
     L->path = kernel_path_impl(M, N, K);
     L->qs = 0;
     L->ds = align16(M * K);
-    L->total = L->ds + align16(M * (K / kSub) * 4);
+    L->q8 = L->ds + align16(M * (K / kSub) * 4);
+    L->op = L->q8;
+    L->total = L->q8 + (L->path == IQ4XS_PATH_TC ? tc_operand_total_bytes(M, K) : 0);
     return true;
 }
 }  // namespace
@@ -187,17 +226,27 @@ int64_t iq4xs_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return linear_layout(M, N, K, &L) ? L.total : 0;
 }
 
+int64_t iq4xs_linear_workspace_min_bytes(int64_t M, int64_t N, int64_t K) {
+    LinearLayout L;
+    return linear_layout(M, N, K, &L) ? L.q8 : 0;
+}
+
 int iq4xs_linear(const void* w, int64_t N, int64_t K, const float* x, int64_t M, int64_t ldx,
                  float* y, int64_t ldy, void* workspace, int64_t workspace_bytes,
                  int64_t stream) {
     if (!w || !x || !y || !workspace) return IQ4XS_ERR_ARG;
     LinearLayout L;
     if (!linear_layout(M, N, K, &L)) return IQ4XS_ERR_SHAPE;
-    if (workspace_bytes < L.total) return IQ4XS_ERR_ARG;
+    if (workspace_bytes < L.q8) return IQ4XS_ERR_ARG;
     if (!aligned(workspace, 16)) return IQ4XS_ERR_ALIGN;
     uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
     int8_t* qs = reinterpret_cast<int8_t*>(ws + L.qs);
     void* ds = ws + L.ds;
+    if (L.path == IQ4XS_PATH_TC && workspace_bytes >= L.total) {  // room for the prepared operand
+        int rc = iq4xs_quantize_q8_1_tc(x, M, K, ldx, qs, ds, ws + L.op, stream);
+        if (rc) return rc;
+        return iq4xs_matmul_tc_operand(w, IQ4XS_WTYPE_IQ4_XS, N, K, ws + L.op, M, y, ldy, stream);
+    }
     int rc = iq4xs_quantize_q8_1(x, M, K, ldx, qs, ds, stream);
     if (rc) return rc;
     return iq4xs_matmul(w, N, K, qs, ds, M, y, ldy, L.path, stream);

@@ -130,8 +130,37 @@ __host__ __device__ inline int64_t tc_num_mtiles(int64_t M) {
     int mt = tc_mtile(M);
     return (M + mt - 1) / mt;
 }
-// Activation operand of the tensor-core path, built inside the matmul from
-// the Q8_1 codes: each code q (|q| <= 127) as an exact fp16 integer, in the
+// Prepared tensor-core operand (written by the quantizer on request, for the
+// faster form of the tensor-core matmul): the dequantized activations
+// v = q*d_h (d_h the block's stored fp16 scale), times a power of two 2^-e
+// per row and span of kScaleSpan values, as a pair of fp16 values hi + lo:
+// hi = fp16(v*2^-e), lo = fp16(v*2^-e - hi).  q has 8 significant bits and
+// d_h 11, so v has at most 19 and the pair holds it exactly (lo keeps the low
+// 8 bits) whenever v*2^-e is a multiple of 2^-24.  e is the smallest e >= 0
+// with 127 * max_span(d_h) * 2^-e < 65504: hi never overflows, e = 0 (every
+// value exact) unless the span's values reach the fp16 range, and otherwise
+// only blocks 2^14 times smaller than the span's largest lose low bits.  The
+// matmul scales its fp32 partial sums by 2^e (exact) per span.  With d_x
+// folded into the operand the kernel does no per-CTA conversion and its
+// epilogue one FMA per element (the Q8_1 form: two FP operations and a scale
+// load), for two MMAs more per sub-block.
+//   planes: [mtile][K/32 sub-block][plane hi, lo][4 chunks of 8 K][MT rows][8 fp16]
+//           (16 B per (chunk, row); a sub-block is 8*MT*16 bytes)
+//   then:   [mtile][ceil(K/kScaleSpan) span][MT rows] fp32 2^e
+// K is permuted within every sub-block as in the Q8_1 form (below).
+constexpr int kPlanes = 2;  // hi, lo
+__host__ __device__ inline int64_t tc_qh_bytes(int64_t M, int64_t K) {
+    return tc_num_mtiles(M) * (int64_t)tc_mtile(M) * K * 2 * kPlanes;
+}
+constexpr int kScaleSpan = 1024;                  // values per activation scale span
+constexpr int kSubPerSpan = kScaleSpan / kSub;     // 32 sub-blocks
+__host__ __device__ inline int64_t tc_num_spans(int64_t K) { return (K + kScaleSpan - 1) / kScaleSpan; }
+__host__ __device__ inline int64_t tc_operand_total_bytes(int64_t M, int64_t K) {
+    return tc_qh_bytes(M, K) + tc_num_mtiles(M) * tc_num_spans(K) * (int64_t)tc_mtile(M) * 4;
+}
+
+// Activation operand of the tensor-core path in its Q8_1 form, built inside
+// the matmul from the Q8_1 codes: each code q (|q| <= 127) as an exact fp16 integer, in the
 // K order of the decoded weights.  Within every sub-block K position 2i+h
 // holds element i+16h (one qs byte decodes to elements i and 16+i), so a
 // 16-byte chunk c (K positions 8c..8c+7) holds elements
@@ -838,8 +867,9 @@ __host__ __device__ constexpr uint32_t idesc_f16_m128(int n) {
 // ---------------------------------------------------------------------------
 struct DevCtx;  // per-device state kept by api.cu
 
+// tc_operand: NULL, or where to write the prepared tensor-core operand too.
 cudaError_t launch_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs,
-                                 void* ds, cudaStream_t stream);
+                                 void* ds, void* tc_operand, cudaStream_t stream);
 cudaError_t launch_dequantize(const void* w, int wt, int64_t N, int64_t K, void* out,
                               int out_dtype, cudaStream_t stream);
 // num_sms picks the launch shape (grids of more than two CTAs per SM run
@@ -856,11 +886,13 @@ cudaError_t launch_matmul_dp4a_grouped(const void* w, int64_t expert_stride, int
 // Programmatic dependent launch on (default) or off for every launch.
 bool pdl_enabled();
 // `encode` is the driver's cuTensorMapEncodeTiled; `err` the device error word.
-// qs must be 16-byte aligned (its rows are staged by TMA).  skip_w_stage >= 0
-// leaves that W stage of every CTA unissued (tests of the bounded waits); -1
-// in every ordinary call.
+// Activations: the Q8_1 arrays (qs 16-byte aligned: its rows are staged by
+// TMA) when tc_operand is NULL, else the prepared operand alone (qs, ds
+// unused).  skip_w_stage >= 0 leaves that W stage of every CTA unissued
+// (tests of the bounded waits); -1 in every ordinary call.
 cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,
-                             const void* ds, int64_t M, float* y, int64_t ldy, void* encode,
-                             int* err, int num_sms, int skip_w_stage, cudaStream_t stream);
+                             const void* ds, const void* tc_operand, int64_t M, float* y,
+                             int64_t ldy, void* encode, int* err, int num_sms, int skip_w_stage,
+                             cudaStream_t stream);
 
 }  // namespace iq4xs

@@ -57,16 +57,18 @@ int64_t iq4xs_linear_static_max_bytes(void) { return iq4xs::kStaticScratchBytes;
 int iq4xs_linear_static(const void* w, int64_t N, int64_t K, const float* x, int64_t M,
                         int64_t ldx, float* y, int64_t ldy, int64_t stream) {
     if (!w || !x || !y) return IQ4XS_ERR_ARG;
-    const int64_t need = iq4xs_linear_workspace_bytes(M, N, K);
+    // The Q8_1 codes and scales must fit (the faster prepared tensor-core
+    // operand is used when it fits too); more than the fixed array holds is
+    // refused and nothing is launched.
+    const int64_t need = iq4xs_linear_workspace_min_bytes(M, N, K);
     if (need == 0) return IQ4XS_ERR_SHAPE;
-    // More scratch than the fixed array holds: refused, nothing launched.
     if (need > iq4xs::kStaticScratchBytes) return IQ4XS_ERR_SHAPE;
     void* scratch = nullptr;
     const int rc = iq4xs::scratch_address(&scratch);
     if (rc) return rc;
     // Every byte of the scratch that the matmul reads (the Q8_1 codes and
-    // scales of rows 0..M-1) is written by the quantizer first, so nothing
-    // needs clearing.
+    // scales of rows 0..M-1, or the prepared operand including its padding
+    // rows) is written by the quantizer first, so nothing needs clearing.
     return iq4xs_linear(w, N, K, x, M, ldx, y, ldy, scratch, iq4xs::kStaticScratchBytes, stream);
 }
 

@@ -86,7 +86,13 @@ constexpr int recv_rows_max() {
     return r;
 }
 
-template <int MT, int WT>
+// kPrep selects the activation operand: false -- the Q8_1 arrays, staged by
+// TMA and turned into exact fp16 codes by the MMA warps, d_x applied in the
+// epilogue (two MMAs per sub-block); true -- the prepared operand (each
+// q*d_x as an exact hi / lo pair of fp16, written by the quantizer), loaded
+// by bulk copies, d_x already inside the products (four MMAs per sub-block,
+// one FMA per element in the epilogue, no per-CTA conversion).
+template <int MT, int WT, bool kPrep>
 struct TcCfg {
     static_assert(MT % 16 == 0 && MT >= 16 && MT <= kMaxMTile, "UMMA N for M=128");
     // W stage: 512 weights of each of the 128 rows, as kWBoxes TMA boxes of
@@ -149,47 +155,47 @@ struct TcCfg {
     // byte as bits 8-15), one instruction less per lookup than a shift and
     // add (measured 6-15% faster); larger tiles, whose activation stages
     // leave no room for the 64 KB, keep entries 128 bytes apart.
-    static constexpr bool kWideLut = MT <= 96;
-    static constexpr int kLutStride = kWideLut ? 256 : 128;
+    // Activation stage slot: the staged codes (Q8_1 form: MT rows x 128 B,
+    // swizzled) and the B operand of 4 sub-blocks (kBSubBytes each: one fp16
+    // plane, or hi and lo planes of the prepared form).
+    static constexpr int kQRawBytes = kPrep ? 0 : kQRowBytes * MT;
+    static constexpr int kBSubBytes = (kPrep ? kPlanes : 1) * kChunksPerSub * MT * 16;
+    static constexpr int kBSlotBytes = kQRawBytes + kBStageSubs * kBSubBytes;
+    static constexpr int usage(int nw, int nb, int lut_stride) {
+        const int nx0 = nb + (kNP * kU + kBStageSubs - 1) / kBStageSubs + 1;
+        const int nx = kPrep ? 1 : (nx0 < 8 ? nx0 : 8);
+        return nw * kWStage + 256 * lut_stride + nb * kBSlotBytes + (kPrep ? 0 : nx * kBStageSubs * MT * 4) +
+               8 * (2 * nw + 2 * nb + 2 * nx + 3 * kNP + 2) + 32 + (kPrep ? MT * 4 : 0);
+    }
+    static constexpr int kSmemLimit = 226 * 1024;
+    static constexpr bool kWideLut = MT <= 96 && usage(2, 2, 256) <= kSmemLimit;
+    // Without room for even the 32 KB table (the prepared form at MT = 128)
+    // the decoders use register tables (byte permutes, ~15 integer
+    // instructions per 8 weights).
+    static constexpr bool kLut = kWideLut || usage(2, 2, 128) <= kSmemLimit;
+    static constexpr int kLutStride = kWideLut ? 256 : kLut ? 128 : 0;
     static constexpr int kLutBytes = 256 * kLutStride;
     static constexpr int kNW0 = (MT <= 16) ? 4 : (MT <= 64) ? 3 : 2;  // W stages, before the fit
     static constexpr int kNB0 = (MT <= 32) ? 4 : (MT <= 64) ? 3 : 2;  // activation stages
-    static constexpr int usage(int nw, int nb) {
-        const int np = (kTmemCols / (kU * (MT + kACols + 1)) < 8) ? kTmemCols / (kU * (MT + kACols + 1)) : 8;
-        const int nx0 = nb + (np * kU + kBStageSubs - 1) / kBStageSubs + 1;
-        const int nx = nx0 < 8 ? nx0 : 8;
-        return nw * kWStage + kLutBytes + nb * (kQRowBytes * MT + kBStageSubs * kChunksPerSub * MT * 16) +
-               nx * kBStageSubs * MT * 4 + 8 * (2 * nw + 2 * nb + 2 * nx + 3 * np + 2) + 16;
-    }
-    static constexpr int fit_nb() {
+    static constexpr int fit(bool want_nb) {
         int nw = kNW0, nb = kNB0;
-        while (usage(nw, nb) > 226 * 1024) { if (nb > 2) --nb; else --nw; }
-        return nb;
+        while (usage(nw, nb, kLutStride) > kSmemLimit) { if (nb > 2) --nb; else --nw; }
+        return want_nb ? nb : nw;
     }
-    static constexpr int fit_nw() {
-        int nw = kNW0, nb = kNB0;
-        while (usage(nw, nb) > 226 * 1024) { if (nb > 2) --nb; else --nw; }
-        return nw;
-    }
-    static constexpr int kNW = fit_nw();
-    static constexpr int kNB = fit_nb();
+    static constexpr int kNW = fit(false);
+    static constexpr int kNB = fit(true);
     static_assert(kNW >= 2 && kNB >= 2, "rings of at least two stages");
-    // Activation stage slot: the staged codes (MT rows x 128 B, swizzled)
-    // and the fp16 B operand built from them (4 sub-blocks of kBSubBytes).
-    static constexpr int kQRawBytes = kQRowBytes * MT;
-    static constexpr int kBSubBytes = kChunksPerSub * MT * 16;
-    static constexpr int kBSlotBytes = kQRawBytes + kBStageSubs * kBSubBytes;
     // Activation scales: fp32 [4 sub-blocks][MT] per stage, in a ring the
     // epilogue releases (it runs behind the MMAs by up to kNP units).
     static constexpr int kNX0 = kNB + (kNP * kU + kBStageSubs - 1) / kBStageSubs + 1;
-    static constexpr int kNX = kNX0 < 8 ? kNX0 : 8;
+    static constexpr int kNX = kPrep ? 1 : (kNX0 < 8 ? kNX0 : 8);  // (unused by the prepared form)
     static constexpr int kXStageBytes = kBStageSubs * MT * 4;
     static constexpr int kXItems = (kBStageSubs * MT + 31) / 32;  // scales per lane and stage
     static constexpr int kOffW = 0;
     static constexpr int kOffLut = kOffW + kNW * kWStage;
     static constexpr int kOffB = kOffLut + kLutBytes;
     static constexpr int kOffX = kOffB + kNB * kBSlotBytes;
-    static constexpr int kOffBar = kOffX + kNX * kXStageBytes;
+    static constexpr int kOffBar = kOffX + (kPrep ? 0 : kNX * kXStageBytes);
     // Barriers, in this order: W full / empty, code stage landed, code
     // stage consumed (its MMAs complete), scales built / consumed, and per
     // unit slot A full / MMA done / accumulators free; then drain and
@@ -211,6 +217,7 @@ struct TcCfg {
         return 1;                                    // recv: expect_tx
     }
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base, abort flag
+    static constexpr int kOffSpan = (kOffMisc + 16 + 15) / 16 * 16;  // prepared form: the span's 2^e
     // Split-K reduction.  Each rank stages its partial tile (128 rows of
     // MT fp32, kRedStride apart) in its own activation ring, which is free
     // once its last MMA has completed, and bulk-copies the rows every other
@@ -221,7 +228,8 @@ struct TcCfg {
     static constexpr int kOffRecv = kOffW;
     static_assert(kTileN * kRedStride * 4 <= kNB * kBSlotBytes, "staged partial tile fits the activation ring");
     static_assert(recv_rows_max() * kRedStride * 4 <= kOffB - kOffW, "received slices fit the W ring and table");
-    static constexpr int kUsed = kOffMisc + 16;
+    static constexpr int kUsed = kOffSpan + (kPrep ? MT * 4 : 0);
+    static_assert(kUsed <= usage(kNW, kNB, kLutStride), "the ring fit counts every region");
     static_assert(kUsed <= 226 * 1024, "stages fit shared memory");
     static constexpr int kSmem = (kUsed > kMinSmem) ? kUsed : kMinSmem;
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
@@ -232,15 +240,19 @@ struct TcCfg {
     static_assert(kRegsControl >= 56, "the MMA warps also build the B operand");
 };
 
+constexpr int kEpilogueBarrier = 1;  // named barriers 1, 2: the 4 warps of epilogue group 0, 1
 __device__ volatile int g_never_abort = 0;  // an abort flag that is never set
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
-template <int MT, int WT>
-__global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
+template <int MT, int WT, bool kPrep>
+__global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
     matmul_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                      const __grid_constant__ CUtensorMap tmap_q, const __half* __restrict__ ds,
-                     int64_t M, int N, int K, float* __restrict__ y, int64_t ldy, int* err,
-                     int skip_w_stage) {
-    using C = TcCfg<MT, WT>;
+                     const uint8_t* __restrict__ tc_op, int64_t M, int N, int K,
+                     float* __restrict__ y, int64_t ldy, int* err, int skip_w_stage) {
+    using C = TcCfg<MT, WT, kPrep>;
     constexpr int kDecGroups = C::kDecGroups, kDecWarps = C::kDecWarps;
     constexpr int kMmaWarp0 = C::kMmaWarp0, kMmaWarp1 = C::kMmaWarp1;
     constexpr int kProducerWarp = C::kProducerWarp, kTmemWarp = C::kTmemWarp, kEpiWarp0 = C::kEpiWarp0;
@@ -312,7 +324,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
         if (lane == 0) {
             *abort_flag = 0;
             prefetch_tmap(&tmap_w);
-            prefetch_tmap(&tmap_q);
+            if constexpr (!kPrep) prefetch_tmap(&tmap_q);
             load_w_stage(0, 0);
             // Split-K: this rank's rows arrive from the S - 1 other ranks.
             // Posted now, before any rank can send (sends wait for a cluster
@@ -323,7 +335,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
             }
         }
     }
-    {
+    if constexpr (C::kLut) {
         // Row j of the byte table: 32 copies of entry j (one per bank).
         for (int i = threadIdx.x; i < 256 * 8; i += C::kThreads) {
             const uint32_t e = f16x2_byte_entry<WT>(i >> 3);
@@ -462,7 +474,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
                                 h[u][4 * c + k] = lds_u32(lut + __byte_perm(q[u][c], lane4, 0x5504u | (k << 4)));
-                } else {
+                } else if constexpr (C::kLut) {
                     const uint32_t lut = smem_u32(smem + C::kOffLut) + (uint32_t)lane * 4u;
 #pragma unroll
                     for (int u = 0; u < C::kU; ++u)
@@ -471,6 +483,11 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
                                 h[u][4 * c + k] = lds_u32(lut + (__byte_perm(q[u][c], 0u, 0x4440u + k) << 7));
+                } else {
+#pragma unroll
+                    for (int u = 0; u < C::kU; ++u)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) decode_f16x2<WT>(q[u][c], h[u] + 4 * c);
                 }
             }
             // The stage's bytes are consumed (in registers) once this warp's
@@ -531,7 +548,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                 // 8rb + r8 from code words c and 4 + c: the 32 lanes read 32
                 // distinct banks and store 4 x 128 contiguous bytes.
                 if (ok) ok = mbar_wait(&q_full[bslot], bphase, abort_flag, err, kDevErrTimeoutQ);
-                if (ok) {
+                if (!kPrep && ok) {
                     const uint8_t* raw = smem + C::kOffB + bslot * C::kBSlotBytes;
                     uint8_t* bop = smem + C::kOffB + bslot * C::kBSlotBytes + C::kQRawBytes;
 #pragma unroll 4
@@ -552,14 +569,19 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                 if (elect_one()) {
                     if (ok) {
                         const uint32_t boff = (uint32_t)(bslot * C::kBSlotBytes + lb * C::kBSubBytes);
+                        // per K step of 16: kv*q (Q8_1 form), or kv*hi and kv*lo
+                        constexpr int kPl = kPrep ? kPlanes : 1;
 #pragma unroll
                         for (int u = 0; u < C::kU; ++u)
 #pragma unroll
                             for (int i = 0; i < kMmaPerSub; ++i)
-                                tc_mma_f16_ta(
-                                    tmem + (uint32_t)(C::kColD + (sp * C::kU + u) * MT),
-                                    tmem + (uint32_t)(C::kColA + (sp * C::kU + u) * kACols + i * (kUmmaK / 2)),
-                                    bdesc0 + ((boff + u * C::kBSubBytes + 2 * i * MT * 16) >> 4), idesc, i != 0);
+#pragma unroll
+                                for (int pl = 0; pl < kPl; ++pl)
+                                    tc_mma_f16_ta(
+                                        tmem + (uint32_t)(C::kColD + (sp * C::kU + u) * MT),
+                                        tmem + (uint32_t)(C::kColA + (sp * C::kU + u) * kACols + i * (kUmmaK / 2)),
+                                        bdesc0 + ((boff + u * C::kBSubBytes + (pl * kChunksPerSub + 2 * i) * MT * 16) >> 4),
+                                        idesc, (i | pl) != 0);
                     }
                     // Commits are made even after an abort so that every
                     // waiter's barrier still completes.
@@ -582,9 +604,18 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                 // that at launch, when every CTA requests at once, first
                 // stages are served first.
                 auto load_q_stage = [&](int slot, int bs) {
-                    mbar_arrive_expect_tx(&q_full[slot], C::kQRawBytes);
-                    tma_load_2d(smem + C::kOffB + slot * C::kBSlotBytes, &tmap_q,
-                                (p0 * kSubPerPair + bs * kBStageSubs) * kSub, z * MT, &q_full[slot]);
+                    if constexpr (kPrep) {
+                        // one contiguous bulk copy of the stage's hi / lo planes
+                        const int64_t sub0 = (int64_t)p0 * kSubPerPair + (int64_t)bs * kBStageSubs;
+                        mbar_arrive_expect_tx(&q_full[slot], C::kBSlotBytes);
+                        bulk_load(smem + C::kOffB + slot * C::kBSlotBytes,
+                                  tc_op + ((int64_t)z * (K / kSub) + sub0) * C::kBSubBytes, C::kBSlotBytes,
+                                  &q_full[slot]);
+                    } else {
+                        mbar_arrive_expect_tx(&q_full[slot], C::kQRawBytes);
+                        tma_load_2d(smem + C::kOffB + slot * C::kBSlotBytes, &tmap_q,
+                                    (p0 * kSubPerPair + bs * kBStageSubs) * kSub, z * MT, &q_full[slot]);
+                    }
                 };
                 int issued_w = 1, issued_q = 0;
                 bool ok = true;
@@ -632,7 +663,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                               kDevErrTimeoutDrain);
             }
         } else if (warp == kTmemWarp) {
-            build_scales();
+            if constexpr (!kPrep) build_scales();
             // Every MMA issued has completed before tensor memory is freed
             // (the MMA warps commit this after their loops, abort or not).
             mbar_wait(drain, 0, &g_never_abort, err, kDevErrTimeoutDrain);
@@ -652,17 +683,20 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
         float acc[kMH];
 #pragma unroll
         for (int m = 0; m < kMH; ++m) acc[m] = 0.f;
-        // acc[m0 + i] += (P[i] * d_x[m0 + i]) * sw for i < n, two columns per
-        // instruction; the scales of four columns per shared-memory load
-        // (the same address across the warp: a broadcast).
+        // Scale-in of n columns from m0: Q8_1 form acc += (P * d_x) * sw (the
+        // scales of four columns per shared-memory load, the same address
+        // across the warp: a broadcast); prepared form acc += P * sw (d_x is
+        // inside P).  Two columns per instruction.
         auto scale_in = [&](const uint32_t* r, int n, int m0, float sw, const float* xrow) {
 #pragma unroll
             for (int i = 0; i < n; i += 4) {
-                const float4 d = *reinterpret_cast<const float4*>(xrow + m0 + i);
-                const float2 p0 = __fmul2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
-                                             make_float2(d.x, d.y));
-                const float2 p1 = __fmul2_rn(make_float2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
-                                             make_float2(d.z, d.w));
+                float2 p0 = make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                float2 p1 = make_float2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                if constexpr (!kPrep) {
+                    const float4 d = *reinterpret_cast<const float4*>(xrow + m0 + i);
+                    p0 = __fmul2_rn(p0, make_float2(d.x, d.y));
+                    p1 = __fmul2_rn(p1, make_float2(d.z, d.w));
+                }
                 const float2 a0 = __ffma2_rn(p0, make_float2(sw, sw), make_float2(acc[m0 + i], acc[m0 + i + 1]));
                 const float2 a1 = __ffma2_rn(p1, make_float2(sw, sw), make_float2(acc[m0 + i + 2], acc[m0 + i + 3]));
                 acc[m0 + i] = a0.x;
@@ -671,12 +705,46 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                 acc[m0 + i + 3] = a1.y;
             }
         };
+        // Prepared form: the partial sums are kept in units of the current
+        // span's 2^-e (the operand's per-row power of two, from the preceding
+        // grid) and rescaled by exact powers of two where the span changes
+        // (every 32 sub-blocks); the current span's scales are staged in
+        // shared memory, each group's own entries by that group.
+        const float* span_scale = nullptr;
+        float* s_span = reinterpret_cast<float*>(smem + C::kOffSpan) + c0;
+        int cur_span = (p0 * kSubPerPair) / kSubPerSpan;
+        if constexpr (kPrep) {
+            griddep_wait();
+            span_scale = reinterpret_cast<const float*>(tc_op + tc_qh_bytes(M, K)) +
+                         (int64_t)z * tc_num_spans(K) * MT + c0;
+            if (t < kMH) s_span[t] = span_scale[(int64_t)cur_span * MT + t];
+            named_barrier_sync(kEpilogueBarrier + eg, kTileN);
+        }
         bool ok = true;
         int sp = 0, sphase = 0;
         for (int v = 0; v < nunits; ++v) {
             const int l0 = v * C::kU, bs = l0 / kBStageSubs, jj = l0 % kBStageSubs, xs = bs % C::kNX;
-            if (ok && jj == 0)  // the stage's scales
+            if constexpr (kPrep) {
+                const int span = (p0 * kSubPerPair + l0) / kSubPerSpan;
+                if (span != cur_span) {
+                    const float4* fo = reinterpret_cast<const float4*>(s_span);
+                    const float4* fn = reinterpret_cast<const float4*>(span_scale + (int64_t)span * MT);
+#pragma unroll
+                    for (int m = 0; m < kMH; m += 4) {
+                        const float4 a = fo[m / 4], b = fn[m / 4];
+                        acc[m] *= a.x / b.x;
+                        acc[m + 1] *= a.y / b.y;
+                        acc[m + 2] *= a.z / b.z;
+                        acc[m + 3] *= a.w / b.w;
+                    }
+                    named_barrier_sync(kEpilogueBarrier + eg, kTileN);  // every thread has read the old scales
+                    if (t < kMH) s_span[t] = span_scale[(int64_t)span * MT + t];
+                    named_barrier_sync(kEpilogueBarrier + eg, kTileN);
+                    cur_span = span;
+                }
+            } else if (ok && jj == 0) {  // the stage's scales
                 ok = mbar_wait(&x_full[xs], (bs / C::kNX) & 1, abort_flag, err, kDevErrTimeoutX);
+            }
             if (ok) ok = mbar_wait(&mma_done[sp], sphase, abort_flag, err, kDevErrTimeoutMma);
             tc_fence_after();
             const uint32_t dcol = tmem + lane_off + (uint32_t)(C::kColD + sp * C::kU * MT + c0);
@@ -735,11 +803,22 @@ __global__ void __launch_bounds__(TcCfg<MT, WT>::kThreads, 1)
                     }
                 }
             }
-            if (jj + C::kU >= kBStageSubs) {  // the stage's last unit: its scales are read
+            if (!kPrep && jj + C::kU >= kBStageSubs) {  // the stage's last unit: its scales are read
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&x_empty[xs]);
             }
             if (++sp == C::kNP) { sp = 0; sphase ^= 1; }
+        }
+        if constexpr (kPrep) {  // back to true units: times the last span's 2^e (exact)
+            const float4* f = reinterpret_cast<const float4*>(s_span);
+#pragma unroll
+            for (int m = 0; m < kMH; m += 4) {
+                const float4 a = f[m / 4];
+                acc[m] *= a.x;
+                acc[m + 1] *= a.y;
+                acc[m + 2] *= a.z;
+                acc[m + 3] *= a.w;
+            }
         }
         // Partial tile -> y (one CTA), or staged in this CTA's activation
         // ring (free: every MMA has completed) for the split-K reduction.
@@ -858,11 +937,11 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 // 27.2 -> 18.4 us at 6144 x 5120, M = 16; 96 tiles stay at S = 1.
 // `fallback` (the largest split that fits one wave on the SM count) stands
 // if a query fails.
-template <int MT, int WT>
+template <int MT, int WT, bool kPrep>
 int choose_split(int dev, int fallback, int units, int pairs) {
-    using C = TcCfg<MT, WT>;
+    using C = TcCfg<MT, WT, kPrep>;
     constexpr double kFixed = MT <= 32 ? 1.9 : (MT <= 64 ? 1.1 : 0.66);
-    static int max_clusters[64][kMaxCluster + 1] = {};
+    static int max_clusters[64][kMaxCluster + 1] = {};  // per instantiation
     if (dev < 0 || dev >= 64) return fallback;
     int best = fallback;
     double best_t = 0.0;
@@ -881,7 +960,7 @@ int choose_split(int dev, int fallback, int units, int pairs) {
             q.attrs = a;
             q.numAttrs = 1;
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, matmul_tc_kernel<MT, WT>, &q) != cudaSuccess ||
+            if (cudaOccupancyMaxActiveClusters(&n, matmul_tc_kernel<MT, WT, kPrep>, &q) != cudaSuccess ||
                 n < 1) {
                 cudaGetLastError();
                 n = -1;
@@ -899,21 +978,21 @@ int choose_split(int dev, int fallback, int units, int pairs) {
     return best;
 }
 
-template <int MT, int WT>
-cudaError_t launch_mt(const CUtensorMap& tmap_w, const CUtensorMap& tmap_q, const __half* ds, int64_t M,
-                      int N, int K, float* y, int64_t ldy, int* err, int S, int ntiles, int mtiles,
-                      int skip, cudaStream_t stream) {
-    using C = TcCfg<MT, WT>;
+template <int MT, int WT, bool kPrep>
+cudaError_t launch_mt(const CUtensorMap& tmap_w, const CUtensorMap& tmap_q, const __half* ds,
+                      const uint8_t* op, int64_t M, int N, int K, float* y, int64_t ldy, int* err, int S,
+                      int ntiles, int mtiles, int skip, cudaStream_t stream) {
+    using C = TcCfg<MT, WT, kPrep>;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(matmul_tc_kernel<MT, WT>,
+        cudaError_t e = cudaFuncSetAttribute(matmul_tc_kernel<MT, WT, kPrep>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    S = choose_split<MT, WT>(dev, S, ntiles * mtiles, K / kPairK);
+    S = choose_split<MT, WT, kPrep>(dev, S, ntiles * mtiles, K / kPairK);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ntiles, (unsigned)S, (unsigned)mtiles);
     cfg.blockDim = dim3(C::kThreads);
@@ -928,32 +1007,46 @@ cudaError_t launch_mt(const CUtensorMap& tmap_w, const CUtensorMap& tmap_q, cons
     attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, matmul_tc_kernel<MT, WT>, tmap_w, tmap_q, ds, M, N, K, y, ldy, err,
-                              skip);
+    return cudaLaunchKernelEx(&cfg, matmul_tc_kernel<MT, WT, kPrep>, tmap_w, tmap_q, ds, op, M, N, K, y,
+                              ldy, err, skip);
+}
+
+template <int WT, bool kPrep>
+cudaError_t launch_wt(const CUtensorMap& tw, const CUtensorMap& tq, const __half* ds, const uint8_t* op,
+                      int64_t M, int N, int K, float* y, int64_t ldy, int* err, int S, int ntiles,
+                      int mtiles, int skip, cudaStream_t stream) {
+#define IQ4XS_TC_CASE(mt)                                                                           \
+    case mt:                                                                                        \
+        return launch_mt<mt, WT, kPrep>(tw, tq, ds, op, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, \
+                                        stream);
+    switch (tc_mtile(M)) {
+        IQ4XS_TC_CASE(16)
+        IQ4XS_TC_CASE(32)
+        IQ4XS_TC_CASE(48)
+        IQ4XS_TC_CASE(64)
+        IQ4XS_TC_CASE(80)
+        IQ4XS_TC_CASE(96)
+        IQ4XS_TC_CASE(112)
+        IQ4XS_TC_CASE(128)
+        default: return cudaErrorInvalidValue;
+    }
+#undef IQ4XS_TC_CASE
 }
 
 template <int WT>
-cudaError_t launch_wt(const CUtensorMap& tw, const CUtensorMap& tq, const __half* ds, int64_t M, int N,
-                      int K, float* y, int64_t ldy, int* err, int S, int ntiles, int mtiles, int skip,
-                      cudaStream_t stream) {
-    switch (tc_mtile(M)) {
-        case 16: return launch_mt<16, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
-        case 32: return launch_mt<32, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
-        case 48: return launch_mt<48, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
-        case 64: return launch_mt<64, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
-        case 80: return launch_mt<80, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
-        case 96: return launch_mt<96, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
-        case 112: return launch_mt<112, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
-        case 128: return launch_mt<128, WT>(tw, tq, ds, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
-        default: return cudaErrorInvalidValue;
-    }
+cudaError_t launch_form(const CUtensorMap& tw, const CUtensorMap& tq, const __half* ds, const uint8_t* op,
+                        int64_t M, int N, int K, float* y, int64_t ldy, int* err, int S, int ntiles,
+                        int mtiles, int skip, cudaStream_t stream) {
+    if (op) return launch_wt<WT, true>(tw, tq, ds, op, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
+    return launch_wt<WT, false>(tw, tq, ds, op, M, N, K, y, ldy, err, S, ntiles, mtiles, skip, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,
-                             const void* ds, int64_t M, float* y, int64_t ldy, void* encode,
-                             int* err, int num_sms, int skip_w_stage, cudaStream_t stream) {
+                             const void* ds, const void* tc_operand, int64_t M, float* y,
+                             int64_t ldy, void* encode, int* err, int num_sms, int skip_w_stage,
+                             cudaStream_t stream) {
     if (wt != kWtIQ4XS && wt != kWtQ4_0 && wt != kWtIQ4NL) return cudaErrorInvalidValue;
     const EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(encode);
     const int64_t row_bytes = wt_row_bytes(wt, K);
@@ -972,10 +1065,10 @@ cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const 
     }
     // Q8_1 codes: one TMA box = MT rows x 128 codes (4 sub-blocks), 128-byte
     // swizzle (conflict-free reads when the B operand is built); rows past M
-    // read as 0.
+    // read as 0.  The prepared form does not read them (the W map stands in).
     const int MT = tc_mtile(M);
-    CUtensorMap tmap_q;
-    {
+    CUtensorMap tmap_q = tmap_w;
+    if (!tc_operand) {
         const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
         const cuuint64_t gstride[1] = {(cuuint64_t)K};
         const cuuint32_t box[2] = {(cuuint32_t)kQRowBytes, (cuuint32_t)MT};
@@ -996,11 +1089,15 @@ cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const 
     const __half* dsh = reinterpret_cast<const __half*>(ds);
     const int Ni = (int)N, Ki = (int)K;
     const int skip = skip_w_stage;
+    const uint8_t* op = reinterpret_cast<const uint8_t*>(tc_operand);
     if (wt == kWtQ4_0)
-        return launch_wt<kWtQ4_0>(tmap_w, tmap_q, dsh, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, skip, stream);
+        return launch_form<kWtQ4_0>(tmap_w, tmap_q, dsh, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, skip,
+                                    stream);
     if (wt == kWtIQ4NL)
-        return launch_wt<kWtIQ4NL>(tmap_w, tmap_q, dsh, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, skip, stream);
-    return launch_wt<kWtIQ4XS>(tmap_w, tmap_q, dsh, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, skip, stream);
+        return launch_form<kWtIQ4NL>(tmap_w, tmap_q, dsh, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, skip,
+                                     stream);
+    return launch_form<kWtIQ4XS>(tmap_w, tmap_q, dsh, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, skip,
+                                 stream);
 }
 
 }  // namespace iq4xs

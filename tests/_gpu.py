@@ -27,10 +27,31 @@ def quantize_gpu(x: np.ndarray):
     return qs, ds
 
 
-def matmul_gpu(wd: torch.Tensor, N: int, K: int, qs, ds, M: int, path, ldy: int | None = None):
+def prepare_gpu(x: np.ndarray, qs_ref=None, ds_ref=None):
+    """The prepared tensor-core operand of x (poisoned first); the Q8_1
+    arrays written beside it must equal iq4xs_quantize_q8_1's bit for bit."""
+    M, K = x.shape
+    qs, ds = B.alloc_activations(M, K, "cuda")
+    op = B.alloc_tc_operand(M, K, "cuda")
+    op.fill_(0xFF)  # fp16 NaN pattern / fp32 NaN in the scale part
+    B.iq4xs_quantize_q8_1_tc(dev(x), qs, ds, op)
+    if qs_ref is not None:
+        assert torch.equal(qs, qs_ref) and torch.equal(ds.view(torch.int16), ds_ref.view(torch.int16))
+    return op
+
+
+def matmul_gpu(wd: torch.Tensor, N: int, K: int, qs, ds, M: int, path, ldy: int | None = None,
+               op=None, wtype=0):
+    """y [M, ldy] through the C ABI, NaN-poisoned first.  path "tcp": the
+    tensor-core matmul from the prepared operand `op`."""
     ldy = N if ldy is None else ldy
     y = torch.full((M, ldy), float("nan"), dtype=torch.float32, device="cuda")
-    B.iq4xs_matmul(wd, N, K, qs, ds, M, y, path)
+    if path == "tcp":
+        B.iq4xs_matmul_tc_operand(wd, N, K, op, M, y, wtype)
+    elif wtype:
+        B.iq4xs_matmul_wt(wd, wtype, N, K, qs, ds, M, y, path)
+    else:
+        B.iq4xs_matmul(wd, N, K, qs, ds, M, y, path)
     torch.cuda.synchronize()
     return y.cpu().numpy()
 

@@ -105,6 +105,31 @@ def test_baseline_threshold_is_advice_above_the_tc_range(lib):
     B._install_calibration(lib)
 
 
+def test_tc_operand_bytes(lib):
+    # M rounds up to a multiple of 16 (at most 128 per tile); q*d as an exact
+    # fp16 pair (4 bytes) per padded activation, plus one fp32 power of two
+    # per padded row and span of 1024 values
+    assert B.iq4xs_tc_operand_bytes(1, 1024) == 16 * 1024 * 4 + 16 * 1 * 4
+    assert B.iq4xs_tc_operand_bytes(96, 4096) == 96 * 4096 * 4 + 96 * 4 * 4
+    assert B.iq4xs_tc_operand_bytes(129, 512) == 2 * 128 * 512 * 4 + 2 * 128 * 1 * 4
+    assert B.iq4xs_tc_operand_bytes(0, 1024) == 0
+    assert B.iq4xs_tc_operand_bytes(4, 1000) == 0
+
+
+def test_prepared_form_argument_errors(lib):
+    p = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)
+    assert lib.iq4xs_quantize_q8_1_tc(p, 1, 256, 256, p, p, None, 0) == B.ERR_ARG
+    assert lib.iq4xs_quantize_q8_1_tc(p, 1, 256, 256, p, p, odd, 0) == B.ERR_ALIGN
+    assert lib.iq4xs_quantize_q8_1_tc(p, 1, 300, 300, p, p, p, 0) == B.ERR_SHAPE
+    assert lib.iq4xs_matmul_tc_operand(None, 0, 8, 512, p, 1, p, 8, 0) == B.ERR_ARG
+    assert lib.iq4xs_matmul_tc_operand(p, 0, 8, 512, None, 1, p, 8, 0) == B.ERR_ARG
+    assert lib.iq4xs_matmul_tc_operand(p, 3, 8, 512, p, 1, p, 8, 0) == B.ERR_ARG
+    assert lib.iq4xs_matmul_tc_operand(p, 0, 8, 768, p, 1, p, 8, 0) == B.ERR_SHAPE
+    assert lib.iq4xs_matmul_tc_operand(p, 0, 8, 512, p, 1, p, 4, 0) == B.ERR_ARG
+    assert lib.iq4xs_matmul_tc_operand(p, 0, 8, 512, odd, 1, p, 8, 0) == B.ERR_ALIGN
+
+
 def test_argument_errors_return_before_any_launch(lib):
     p = ctypes.c_void_p(0x10000)      # never dereferenced: validation fails first
     odd = ctypes.c_void_p(0x10008)
@@ -168,14 +193,19 @@ def test_status_strings(lib):
 
 def test_linear_workspace_and_validation(lib):
     B.iq4xs_set_crossover(4)
-    # qs, then ds 16-byte aligned, on either path: 1.125 bytes per activation
+    # the least: qs, then ds 16-byte aligned (1.125 bytes per activation);
+    # the fastest form adds the prepared operand on the tensor-core path
     assert B.iq4xs_linear_workspace_bytes(2, 4096, 4096) == 2 * 4096 + 2 * 128 * 4
-    assert B.iq4xs_linear_workspace_bytes(96, 4096, 4096) == 96 * 4096 + 96 * 128 * 4
-    assert B.iq4xs_linear_workspace_bytes(3, 8, 256) == 3 * 256 + 3 * 8 * 4
+    assert B.iq4xs_linear_workspace_min_bytes(2, 4096, 4096) == 2 * 4096 + 2 * 128 * 4
+    assert B.iq4xs_linear_workspace_min_bytes(96, 4096, 4096) == 96 * 4096 + 96 * 128 * 4
+    assert (B.iq4xs_linear_workspace_bytes(96, 4096, 4096) ==
+            96 * 4096 + 96 * 128 * 4 + B.iq4xs_tc_operand_bytes(96, 4096))
+    assert B.iq4xs_linear_workspace_min_bytes(3, 8, 256) == 3 * 256 + 3 * 8 * 4
     assert B.iq4xs_linear_workspace_bytes(0, 8, 256) == 0
     p = ctypes.c_void_p(0x10000)
     need = B.iq4xs_linear_workspace_bytes(96, 4096, 4096)
-    assert lib.iq4xs_linear(p, 4096, 4096, p, 96, 4096, p, 4096, p, need - 1, 0) == B.ERR_ARG
+    least = B.iq4xs_linear_workspace_min_bytes(96, 4096, 4096)
+    assert lib.iq4xs_linear(p, 4096, 4096, p, 96, 4096, p, 4096, p, least - 1, 0) == B.ERR_ARG
     assert lib.iq4xs_linear(p, 4096, 4096, p, 96, 4096, p, 4096, None, need, 0) == B.ERR_ARG
     assert lib.iq4xs_linear(p, 4096, 300, p, 96, 4096, p, 4096, p, need, 0) == B.ERR_SHAPE
 

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from _gates import gate_independent, gate_parity, gate_written
-from _gpu import dev, oracle_q8, quantize_gpu, sample_rows
+from _gpu import dev, matmul_gpu, oracle_q8, prepare_gpu, quantize_gpu, sample_rows
 from iq4_xs_quantized_gb300 import binding as B
 from iq4_xs_quantized_gb300 import synth
 
@@ -67,9 +67,12 @@ def test_formats_match_oracle_on_every_path(name, wt, N, K):
         qs, ds = quantize_gpu(x[:M])
         qs_o, d_o, _ = oracle_q8(x[:M])
         ref = _oracle_wt(wt, w, N, K, qs_o, d_o)
-        paths = [B.PATH_AUTO, B.PATH_DP4A] + ([B.PATH_TC] if K % 512 == 0 else [])
+        paths = [B.PATH_AUTO, B.PATH_DP4A] + ([B.PATH_TC, "tcp"] if K % 512 == 0 else [])
         for path in paths:
-            y = _matmul_wt(wd, wt, N, K, qs, ds, M, path)
+            if path == "tcp":
+                y = matmul_gpu(wd, N, K, None, None, M, "tcp", op=prepare_gpu(x[:M]), wtype=wt)
+            else:
+                y = _matmul_wt(wd, wt, N, K, qs, ds, M, path)
             assert gate_written(y) is None, (name, M, path)
             r = gate_parity(y, ref)
             assert r is None, (name, N, K, M, path, r)
@@ -136,3 +139,8 @@ def test_iq4nl_equals_iq4xs_with_uniform_scale_bitwise():
             b = _matmul_wt(w_nl, B.WTYPE_IQ4_NL, N, K, qs, ds, M, path)
             assert gate_written(a) is None
             assert np.array_equal(a, b), (M, path)
+        op = prepare_gpu(x[:M])
+        a = matmul_gpu(w_xs, N, K, None, None, M, "tcp", op=op, wtype=B.WTYPE_IQ4_XS)
+        b = matmul_gpu(w_nl, N, K, None, None, M, "tcp", op=op, wtype=B.WTYPE_IQ4_NL)
+        assert gate_written(a) is None
+        assert np.array_equal(a, b), (M, "tcp")

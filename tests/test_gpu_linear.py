@@ -1,12 +1,14 @@
 """iq4xs_linear (quantize + matmul through a caller workspace) on the GPU:
-same result as the two separate calls, within 1e-5 per row of the oracle,
-and the workspace holds the Q8_1 codes and {d, s}, bit-exact."""
+same result as the two separate calls of the form it takes (the prepared
+tensor-core operand when the workspace holds it, else the Q8_1 arrays),
+within 1e-5 per row of the oracle, and the workspace holds the Q8_1 codes
+and {d, s}, bit-exact."""
 import numpy as np
 import pytest
 import torch
 
 from _gates import gate_parity, gate_written
-from _gpu import dev, matmul_gpu, oracle_matmul, oracle_q8, quantize_gpu, sample_rows
+from _gpu import dev, matmul_gpu, oracle_matmul, oracle_q8, prepare_gpu, quantize_gpu, sample_rows
 from iq4_xs_quantized_gb300 import binding as B
 from iq4_xs_quantized_gb300 import synth
 
@@ -40,11 +42,22 @@ def test_linear_matches_two_calls_and_oracle(M):
     assert gate_written(yl) is None
     path = "dp4a" if B.iq4xs_select_path(M, N, K) == B.PATH_DP4A else "tc"
     qs, ds = quantize_gpu(x)
-    y2 = matmul_gpu(wd, N, K, qs, ds, M, path)
+    # the full workspace: the prepared operand on the tensor-core path
+    y2 = matmul_gpu(wd, N, K, qs, ds, M, "tcp" if path == "tc" else path,
+                    op=prepare_gpu(x, qs, ds) if path == "tc" else None)
     assert np.array_equal(yl, y2)
     qs_o, d_o, _ = oracle_q8(x)
     rows = sample_rows(N, 40, seed=M)
     r = gate_parity(yl[:, rows], oracle_matmul(w, N, K, qs_o, d_o, rows))
+    assert r is None, r
+    # the least workspace: the Q8_1 form, the same bits as iq4xs_matmul
+    least = B.iq4xs_linear_workspace_min_bytes(M, N, K)
+    ws2 = torch.full((least,), 0xFF, dtype=torch.uint8, device="cuda")
+    y3 = torch.full((M, N), float("nan"), device="cuda")
+    B.iq4xs_linear(wd, N, K, xd, y3, ws2)
+    torch.cuda.synchronize()
+    assert np.array_equal(y3.cpu().numpy(), matmul_gpu(wd, N, K, qs, ds, M, path))
+    r = gate_parity(y3.cpu().numpy()[:, rows], oracle_matmul(w, N, K, qs_o, d_o, rows))
     assert r is None, r
 
 

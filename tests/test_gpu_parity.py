@@ -13,15 +13,16 @@ import torch
 
 import oracle
 from _gates import gate_independent, gate_parity, gate_written
-from _gpu import (dev, independent_fp32, matmul_gpu, oracle_matmul, oracle_q8, quantize_gpu,
-                  sample_rows)
+from _gpu import (dev, independent_fp32, matmul_gpu, oracle_matmul, oracle_q8, prepare_gpu,
+                  quantize_gpu, sample_rows)
 from _pins import make_block, parse_q8_cases
 from iq4_xs_quantized_gb300 import binding as B
 from iq4_xs_quantized_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
-PATHS = ("dp4a", "tc")
+# dp4a; tcgen05 from the Q8_1 arrays; tcgen05 from the prepared operand
+PATHS = ("dp4a", "tc", "tcp")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -48,7 +49,8 @@ def run_and_gate(w, N, K, x, path, rows=None, ldy=None, independent=True):
     qs, ds = quantize_gpu(x)
     qs_o, d_o = check_q8(x, qs, ds)
     M = x.shape[0]
-    y = matmul_gpu(dev(w), N, K, qs, ds, M, path, ldy=ldy)
+    op = prepare_gpu(x, qs, ds) if path == "tcp" else None
+    y = matmul_gpu(dev(w), N, K, qs, ds, M, path, ldy=ldy, op=op)
     assert gate_written(y[:, :N]) is None, gate_written(y[:, :N])
     if ldy is not None and ldy > N:
         assert np.all(np.isnan(y[:, N:])), "columns beyond N must not be written"
@@ -102,9 +104,10 @@ def test_matmul_tiny_dp4a(M):
 
 
 @pytest.mark.parametrize("M", TINY_MS_TC)
-def test_matmul_tiny_tc(M):
+@pytest.mark.parametrize("form", ("tc", "tcp"))
+def test_matmul_tiny_tc(M, form):
     w, x = synth.TINY.inputs(0, M=M)
-    run_and_gate(w, 256, 1024, x, "tc")
+    run_and_gate(w, 256, 1024, x, form)
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -140,6 +143,9 @@ def test_matmul_k256_dp4a_only():
     y = torch.empty((4, 64), dtype=torch.float32, device="cuda")
     with pytest.raises(B.IQ4XSError) as e:
         B.iq4xs_matmul(dev(w), 64, 256, qs, ds, 4, y, "tc")
+    assert e.value.status == B.ERR_SHAPE
+    with pytest.raises(B.IQ4XSError) as e:
+        B.iq4xs_matmul_tc_operand(dev(w), 64, 256, prepare_gpu(x), 4, y)
     assert e.value.status == B.ERR_SHAPE
 
 
@@ -206,6 +212,7 @@ def test_full_square(M):
     B.iq4xs_set_crossover(4)
     path = "dp4a" if B.iq4xs_select_path(M, 4096, 4096) == B.PATH_DP4A else "tc"
     _full_case("square_4096x4096", 0, M, path)
+    _full_case("square_4096x4096", 0, M, "tcp")
     if M <= 16:
         _full_case("square_4096x4096", 0, M, "tc" if path == "dp4a" else "dp4a")
 
@@ -214,7 +221,7 @@ def test_full_square(M):
 def test_full_decoder_shapes(shape_index):
     # dp4a at M = 1 and 2 meets all three launch shapes across these grids
     # (1024 rows: 64 CTAs; 5120-6144: 320-384; 10240-34816: 640-2176)
-    for M, path in ((1, "dp4a"), (2, "dp4a"), (16, "tc"), (64, "tc")):
+    for M, path in ((1, "dp4a"), (2, "dp4a"), (16, "tc"), (64, "tc"), (16, "tcp"), (64, "tcp")):
         _full_case("decoder27b_9proj", shape_index, M, path, nrows=24)
 
 
@@ -222,6 +229,7 @@ def test_full_decoder_shapes(shape_index):
 @pytest.mark.parametrize("shape_index", (0, 1))
 def test_full_prefill(shape_index, M):
     _full_case("prefill_sweep", shape_index, M, "tc", nrows=16)
+    _full_case("prefill_sweep", shape_index, M, "tcp", nrows=16)
 
 
 # ------------------------------------------------------------------- dequantize
@@ -266,7 +274,7 @@ def test_gate_fires_on_one_corrupted_weight_byte(path):
     w, x = synth.TINY.inputs(0, M=4)
     qs, ds = quantize_gpu(x)
     qs_o, d_o, _ = oracle_q8(x)
-    y = matmul_gpu(dev(w), 256, 1024, qs, ds, 4, path)
+    y = matmul_gpu(dev(w), 256, 1024, qs, ds, 4, path, op=prepare_gpu(x) if path == "tcp" else None)
     bad = w.copy()
     bad[17, 136 * 2 + 8 + 40] ^= 0x5A
     assert gate_parity(y, oracle_matmul(w, 256, 1024, qs_o, d_o)) is None
