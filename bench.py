@@ -339,6 +339,7 @@ def run_ours(args, world, rank, local):
     wcopies = [wd0] + [wd0.clone() for _ in range(N_COPIES - 1)]
     xs = {M: torch.from_numpy(np.ascontiguousarray(x_np[:M])).to(dev) for M in ms}
     acts = {M: B.alloc_activations(M, K, dev) for M in ms}
+    ops = {M: B.alloc_tc_operand(M, K, dev) for M in ms}
     ys = {M: torch.empty((M, N), dtype=torch.float32, device=dev) for M in ms}
     paths = {M: kernel_path(B, M, N, K) for M in ms}
     variants = N_COPIES // len(ms)
@@ -347,8 +348,13 @@ def run_ours(args, world, rank, local):
     def launch_step(v):
         for i, M in enumerate(ms):
             qs, ds = acts[M]
-            B.iq4xs_quantize_q8_1(xs[M], qs, ds, stream)
-            B.iq4xs_matmul(wcopies[v * len(ms) + i], N, K, qs, ds, M, ys[M], paths[M], stream)
+            w = wcopies[v * len(ms) + i]
+            if paths[M] == B.PATH_TC:  # the faster, prepared form (as iq4xs_linear takes it)
+                B.iq4xs_quantize_q8_1_tc(xs[M], qs, ds, ops[M], stream)
+                B.iq4xs_matmul_tc_operand(w, N, K, ops[M], M, ys[M], stream=stream)
+            else:
+                B.iq4xs_quantize_q8_1(xs[M], qs, ds, stream)
+                B.iq4xs_matmul(w, N, K, qs, ds, M, ys[M], paths[M], stream)
 
     # Eager warm-up (also performs the library's one-time device set-up).
     with torch.cuda.stream(stream):
@@ -392,16 +398,22 @@ def run_ours(args, world, rank, local):
     # Per-matmul device time: graphs of back-to-back matmul launches over the
     # rotating weight copies, CUDA events on the launching stream.
     per_m = []
-    mm_us = matmul_only_times(torch, B, stream, ms, N, K, wcopies, acts, ys, paths)
+    mm_us = matmul_only_times(torch, B, stream, ms, N, K, wcopies, acts, ys, paths, ops)
+    q8_us = matmul_only_times(torch, B, stream, [M for M in ms if paths[M] == B.PATH_TC], N, K,
+                              wcopies, acts, ys, paths)
     mm_timing = ("CUDA events around graph replays of 45 back-to-back matmul launches "
                  "(rotating weight copies) on the launching stream, per M")
     peak, peak_kind = hbm_peak_gbs()
     for M in ms:
         us = mm_us[M]
         gbs = matmul_bytes(M, N, K) / (us * 1e-6) / 1e9
-        per_m.append({"M": M, "path": {1: "dp4a", 2: "tc"}[paths[M]], "matmul_us": round(us, 3),
-                      "GBps": round(gbs, 1), "TOPS": round(2 * M * N * K / (us * 1e-6) / 1e12, 3),
-                      "hbm_frac": round(gbs / peak, 4)})
+        row = {"M": M, "path": {1: "dp4a", 2: "tc (prepared operand)"}[paths[M]],
+               "matmul_us": round(us, 3), "GBps": round(gbs, 1),
+               "TOPS": round(2 * M * N * K / (us * 1e-6) / 1e12, 3), "hbm_frac": round(gbs / peak, 4)}
+        if M in q8_us:
+            row["q8_form_us"] = round(q8_us[M], 3)
+            row["q8_form_GBps"] = round(matmul_bytes(M, N, K) / (q8_us[M] * 1e-6) / 1e9, 1)
+        per_m.append(row)
     # Dominant kernel: the tcgen05 matmul (M above the dispatcher's crossover).
     tc_ms = [M for M in ms if paths[M] == B.PATH_TC] or list(ms)
     tc_bytes = sum(matmul_bytes(M, N, K) for M in tc_ms)
@@ -488,8 +500,8 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "traffic_algorithmic": tc_bytes / len(tc_ms),
-                         "kernel": f"matmul_tc_kernel (tcgen05), M in {tc_ms}: algorithmic "
-                                   "bytes per launch / mean launch time",
+                         "kernel": f"matmul_tc_kernel (tcgen05, prepared-operand form), M in {tc_ms}: "
+                                   "algorithmic bytes per launch / mean launch time",
                          "peak_kind": peak_kind, "timing": mm_timing,
                          "tensor": tensor, "alu": issue, "binding": binding,
                          "binding_rule": "the roofline with the largest fraction"},
@@ -507,6 +519,17 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def projection(B, w, N, K, x, qs, ds, op, M, y, path, stream):
+    """quantize + matmul as iq4xs_linear runs them with its full workspace:
+    the prepared tensor-core operand on the TC path, the Q8_1 arrays on dp4a."""
+    if path == B.PATH_TC:
+        B.iq4xs_quantize_q8_1_tc(x, qs, ds, op, stream)
+        B.iq4xs_matmul_tc_operand(w, N, K, op, M, y, stream=stream)
+    else:
+        B.iq4xs_quantize_q8_1(x, qs, ds, stream)
+        B.iq4xs_matmul(w, N, K, qs, ds, M, y, path, stream)
+
+
 def kernel_path(B, M, N, K):
     """The library kernel the dispatcher's choice runs on: its BASELINE advice
     (dequantize + a dense GEMM in the caller's BLAS) maps to the tcgen05
@@ -516,16 +539,20 @@ def kernel_path(B, M, N, K):
     return B.PATH_TC if p == B.PATH_BASELINE else p
 
 
-def matmul_only_times(torch, B, stream, ms, N, K, wcopies, acts, ys, paths, reps=20):
+def matmul_only_times(torch, B, stream, ms, N, K, wcopies, acts, ys, paths, ops=None, reps=20):
     """Average device time per matmul launch (us) from graphs of back-to-back
-    matmuls over the rotating weight copies."""
+    matmuls over the rotating weight copies (tensor-core M from the prepared
+    operands `ops` when given, else from the Q8_1 arrays)."""
     out = {}
     for M in ms:
         qs, ds = acts[M]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for w in wcopies:
-                B.iq4xs_matmul(w, N, K, qs, ds, M, ys[M], paths[M], stream)
+                if ops is not None and paths[M] == B.PATH_TC:
+                    B.iq4xs_matmul_tc_operand(w, N, K, ops[M], M, ys[M], stream=stream)
+                else:
+                    B.iq4xs_matmul(w, N, K, qs, ds, M, ys[M], paths[M], stream)
         with torch.cuda.stream(stream):
             g.replay()
             t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -592,12 +619,13 @@ def decode_stream(torch, B, dev, reps=5):
                 x = torch.randn((M, K), device=dev, generator=g)
                 qs, ds = B.alloc_activations(M, K, dev)
                 y = torch.empty((M, N), dtype=torch.float32, device=dev)
-                calls.append((layers[l][i], N, K, x, qs, ds, y, kernel_path(B, M, N, K)))
+                path = kernel_path(B, M, N, K)
+                op = B.alloc_tc_operand(M, K, dev) if path == B.PATH_TC else None
+                calls.append((layers[l][i], N, K, x, qs, ds, op, y, path))
 
         def step():
-            for (w, N, K, x, qs, ds, y, path) in calls:
-                B.iq4xs_quantize_q8_1(x, qs, ds, stream)
-                B.iq4xs_matmul(w, N, K, qs, ds, M, y, path, stream)
+            for (w, N, K, x, qs, ds, op, y, path) in calls:
+                projection(B, w, N, K, x, qs, ds, op, M, y, path, stream)
         with torch.cuda.stream(stream):
             step()
         torch.cuda.synchronize()
@@ -774,16 +802,27 @@ def decoder_shapes(torch, B, dev, stream, reps=10):
             path = kernel_path(B, M, N, K)
             x = torch.from_numpy(np.ascontiguousarray(x_np[:M])).to(dev)
             qs, ds = B.alloc_activations(M, K, dev)
-            B.iq4xs_quantize_q8_1(x, qs, ds, stream)
+            op = B.alloc_tc_operand(M, K, dev)
+            B.iq4xs_quantize_q8_1_tc(x, qs, ds, op, stream)
 
             def mm():
                 for w in ws:
-                    B.iq4xs_matmul(w, N, K, qs, ds, M, y, path, stream)
+                    if path == B.PATH_TC:
+                        B.iq4xs_matmul_tc_operand(w, N, K, op, M, y, stream=stream)
+                    else:
+                        B.iq4xs_matmul(w, N, K, qs, ds, M, y, path, stream)
+
+            def mm_q8():
+                for w in ws:
+                    B.iq4xs_matmul(w, N, K, qs, ds, M, y, B.PATH_TC, stream)
             us = _graph_us(torch, stream, mm, len(ws), reps)
             gbs = matmul_bytes(M, N, K) / (us * 1e-6) / 1e9
-            res.append({"N": N, "K": K, "M": M, "path": "dp4a" if path == B.PATH_DP4A else "tc",
-                        "us": round(us, 3), "GBps": round(gbs, 1),
-                        "TOPS": round(2 * M * N * K / (us * 1e-6) / 1e12, 2)})
+            row = {"N": N, "K": K, "M": M, "path": "dp4a" if path == B.PATH_DP4A else "tc (prepared)",
+                   "us": round(us, 3), "GBps": round(gbs, 1),
+                   "TOPS": round(2 * M * N * K / (us * 1e-6) / 1e12, 2)}
+            if path == B.PATH_TC:
+                row["q8_form_us"] = round(_graph_us(torch, stream, mm_q8, len(ws), reps), 3)
+            res.append(row)
         del ws
         torch.cuda.empty_cache()
     return res
@@ -805,12 +844,12 @@ def prefill_sweep(torch, B, dev, stream, reps=3):
             x = torch.from_numpy(np.ascontiguousarray(x_np[:M])).to(dev)
             xb = x.to(torch.bfloat16)
             qs, ds = B.alloc_activations(M, K, dev)
+            op = B.alloc_tc_operand(M, K, dev)
             y = torch.empty((M, N), dtype=torch.float32, device=dev)
 
             def tc():
                 for w in ws:
-                    B.iq4xs_quantize_q8_1(x, qs, ds, stream)
-                    B.iq4xs_matmul(w, N, K, qs, ds, M, y, B.PATH_TC, stream)
+                    projection(B, w, N, K, x, qs, ds, op, M, y, B.PATH_TC, stream)
 
             def base():
                 for w in ws:

@@ -32,19 +32,27 @@ L2_BYTES = 129 * 2**20
 
 
 def time_path(B, torch, wcopies, N, K, M, path, reps=20):
+    """us per matmul on `path`; the tensor-core path in its prepared-operand
+    form (the one iq4xs_linear takes with its full workspace)."""
     qs, ds = B.alloc_activations(M, K, "cuda")
+    op = B.alloc_tc_operand(M, K, "cuda")
     x = torch.randn(M, K, device="cuda")
     y = torch.empty(M, N, device="cuda")
-    B.iq4xs_quantize_q8_1(x, qs, ds)
+    B.iq4xs_quantize_q8_1_tc(x, qs, ds, op)
     s = torch.cuda.Stream()
-    with torch.cuda.stream(s):
+
+    def run():
         for w in wcopies:
-            B.iq4xs_matmul(w, N, K, qs, ds, M, y, path, s)
+            if path == B.PATH_TC:
+                B.iq4xs_matmul_tc_operand(w, N, K, op, M, y, stream=s)
+            else:
+                B.iq4xs_matmul(w, N, K, qs, ds, M, y, path, s)
+    with torch.cuda.stream(s):
+        run()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        for w in wcopies:
-            B.iq4xs_matmul(w, N, K, qs, ds, M, y, path, s)
+        run()
     with torch.cuda.stream(s):
         g.replay()
     torch.cuda.synchronize()
@@ -176,12 +184,13 @@ def calibrate_baseline(shapes=BASE_SHAPES, ms=BASE_MS, verbose=True):
         for M in ms:
             x = torch.randn(M, K, device="cuda")
             qs, ds = B.alloc_activations(M, K, "cuda")
+            op = B.alloc_tc_operand(M, K, "cuda")
             y = torch.empty(M, N, device="cuda")
 
             def tc(s):
                 for ww in wcopies:
-                    B.iq4xs_quantize_q8_1(x, qs, ds, s)
-                    B.iq4xs_matmul(ww, N, K, qs, ds, M, y, B.PATH_TC, s)
+                    B.iq4xs_quantize_q8_1_tc(x, qs, ds, op, s)
+                    B.iq4xs_matmul_tc_operand(ww, N, K, op, M, y, stream=s)
 
             def base(s):
                 for ww in wcopies:
