@@ -1,8 +1,9 @@
-"""Correctness gates for the CUDA path (engine page lessons, V100TPS engine:
-"poison the output buffer and assert a nonzero error against an independent
-implementation; add a roofline check because a kernel that did no work is
-impossibly fast"; and the later passage on replacing an absolute threshold by
-a per-row relative one with fixed seeds).
+"""Correctness gates for the CUDA path, after the lessons the V100TPS engine
+page draws from its broken batched route: the output buffer is poisoned
+before every call and its error against an independent implementation must be
+nonzero (an exact match means the same code or memory was compared with
+itself), a call faster than its bytes allow did no work (the roofline gate),
+and absolute thresholds give way to per-row relative ones on fixed seeds.
 
 Each gate returns None when it passes and a short reason string when it fails,
 so the negative-control tests can assert that a gate fires.

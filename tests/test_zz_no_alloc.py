@@ -37,7 +37,7 @@ def test_static_scratch_matches_workspace_entry_point_twice():
     # second call: dp4a path on a small projection
     for workload, M in ((synth.SQUARE, 96), (synth.TINY, 3)):
         N, K = workload.shapes[0]
-        assert B.iq4xs_linear_workspace_bytes(M, N, K) <= B.iq4xs_linear_static_max_bytes()
+        assert B.iq4xs_linear_workspace_bytes(M, N, K) <= B.iq4xs_linear_static_max_bytes()  # prepared form
         wd, xd = _inputs(workload, M)
         y_static = torch.full((M, N), float("nan"), device="cuda")
         B.iq4xs_linear_static(wd, N, K, xd, y_static)
@@ -63,7 +63,7 @@ def test_static_scratch_matches_workspace_entry_point_twice():
 def _largest_m(N, K):
     cap = B.iq4xs_linear_static_max_bytes()
     m = 1
-    while B.iq4xs_linear_workspace_bytes(m + 1, N, K) <= cap:
+    while B.iq4xs_linear_workspace_min_bytes(m + 1, N, K) <= cap:
         m += 1
     return m
 
@@ -97,7 +97,7 @@ def test_static_scratch_size_limit_boundary():
 
 def test_static_scratch_rejects_requests_beyond_its_size():
     N, K, M = 17408, 5120, 2048
-    assert B.iq4xs_linear_workspace_bytes(M, N, K) > B.iq4xs_linear_static_max_bytes()
+    assert B.iq4xs_linear_workspace_min_bytes(M, N, K) > B.iq4xs_linear_static_max_bytes()
     w = torch.zeros((N, K // 256 * 136), dtype=torch.uint8, device="cuda")
     x = torch.zeros((M, K), device="cuda")
     y = torch.full((M, N), float("nan"), device="cuda")
