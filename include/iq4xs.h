@@ -85,7 +85,7 @@ typedef enum {
                               the requested path cannot take */
     IQ4XS_ERR_DEVICE = 4,  /* no CUDA device, or the current device is not sm_103 */
     IQ4XS_ERR_CUDA = 5,    /* a CUDA runtime/driver call or a launch failed */
-    IQ4XS_ERR_TIMEOUT = 6  /* a bounded device wait ran out (device error word) */
+    IQ4XS_ERR_TIMEOUT = 6  /* a bounded device wait ran out (iq4xs_last_device_error) */
 } iq4xs_status;
 
 typedef enum {
@@ -346,10 +346,12 @@ int iq4xs_set_pdl(int enable);
 
 /*
  * Read and clear the current device's error word, written by kernels whose
- * bounded waits (2 s each) ran out.  Synchronizes the current device.
- * Returns IQ4XS_OK with *code_out = 0 when clean, IQ4XS_ERR_TIMEOUT with
- * *code_out = the code of the last wait that ran out, in the tensor-core
- * matmul:
+ * bounded waits ran out (2 s for a copy to land, 4 s for a hand-off between
+ * the kernel's roles, 6 s for the final drains, so that the wait at the root
+ * of a stall runs out first).  Synchronizes the current device.  Returns
+ * IQ4XS_OK with *code_out = 0 when clean, IQ4XS_ERR_TIMEOUT with *code_out =
+ * the code of the first wait that ran out since the last read, in the
+ * tensor-core matmul:
  *   0x101 a W stage      0x102 an activation stage   0x103 a decoded unit
  *   0x104 a unit's MMAs  0x105 a free unit slot      0x106 the final drain
  *   0x107 the split-K slices of the other cluster ranks
@@ -363,7 +365,7 @@ int iq4xs_last_device_error(int* code_out);
  * next tensor-core matmul launched after this call (on any thread) leaves W
  * stage `stage` (0-based, in units of 512 weights of each CTA's K range) of
  * every CTA unissued, so that the decoders' wait for it runs out after its
- * 2 s limit.  That call's output is then undefined, every CTA still drains
+ * 2 s limit (the other roles' waits, longer, end on the abort it raises).  That call's output is then undefined, every CTA still drains
  * its copies and frees its tensor memory, and iq4xs_last_device_error
  * reports IQ4XS_ERR_TIMEOUT with code 0x101.  -1 disarms.  Host only.
  */

@@ -209,7 +209,16 @@ enum DeviceError : int {
     kDevErrTimeoutX = 0x109,
     kDevErrLayout = 0x10A,  // dynamic shared memory not 1024-byte aligned
 };
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: waits for a copy to land
+// Limits by what is awaited, so that the wait at the root of a stall runs out
+// first and its code is the one recorded: a copy landing (W or code stage)
+// 2 s, a hand-off from another role 4 s, the final drains and the split-K
+// slices 6 s.
+__host__ __device__ constexpr unsigned long long wait_limit_ns(int code) {
+    return (code == kDevErrTimeoutW || code == kDevErrTimeoutQ) ? kWaitLimitNs
+           : (code == kDevErrTimeoutDrain || code == kDevErrTimeoutRecv) ? 3 * kWaitLimitNs
+                                                                          : 2 * kWaitLimitNs;
+}
 
 // ---------------------------------------------------------------------------
 // Nibble decoders (prmt.b32: 8 source bytes {b,a}; selector nibble bits 0-2
@@ -403,8 +412,10 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 }
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (without waiting further) once the CTA's abort flag is set, or after
-// kWaitLimitNs, in which case it sets the abort flag and the device error word.
-// The first probe returns at once; later ones suspend for up to 0.1 ms.
+// wait_limit_ns(code), in which case it sets the abort flag and records
+// `code` in the device error word unless an earlier code is there (the first
+// wait to run out is the one reported).  The first probe returns at once;
+// later ones suspend for up to 0.1 ms.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* err, int code) {
     const uint32_t a = smem_u32(bar);
@@ -413,9 +424,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     for (;;) {
         if (mbar_try_wait_sleep(a, parity, 100000u)) return true;
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > wait_limit_ns(code)) {
             *abort_flag = 1;
-            atomicExch(err, code);
+            atomicCAS(err, 0, code);
             return false;
         }
     }
