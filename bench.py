@@ -279,6 +279,34 @@ def oracle_sample(rows: int, threads: int, min_seconds: float = 0.0):
     return nbytes / dt / 1e9, dt, desc
 
 
+def oracle_per_config(min_seconds: float = 2.0):
+    """The oracle single-threaded on the tiny configuration (all of it: 256 x
+    1024, M = 1, 4, 8) and on a 64-row sample of the square one (every M),
+    as GB/s of each workload's algorithmic bytes."""
+    import oracle
+    from iq4_xs_quantized_gb300 import synth
+    orc = oracle.get()
+    out = []
+    for W, rows in ((synth.TINY, None), (synth.SQUARE, 64)):
+        N, K = W.shapes[0]
+        w, x = W.inputs(0)
+        n = N if rows is None else rows
+        wr = np.ascontiguousarray(w[:n])
+        passes, t0 = 0, time.perf_counter()
+        while True:
+            for M in W.ms:
+                qs, d_h, _ = orc.quantize_q8_1(x[:M])
+                orc.matmul(wr, n, K, qs, d_h, nthreads=1)
+            passes += 1
+            dt = time.perf_counter() - t0
+            if dt >= min_seconds:
+                break
+        out.append({"workload": W.name, "rows": n, "of_rows": N, "ms": list(W.ms), "threads": 1,
+                    "GBps": round(passes * step_bytes(W.ms, n, K) / dt / 1e9, 4),
+                    "seconds": round(dt, 2)})
+    return out
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -308,6 +336,8 @@ def run_reference(args, world, rank):
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "same_config": ("the square 4096 x 4096 sweep on a 256-row sample of W (the oracle's "
+                        "rate per byte; the GPU arm runs all 4096 rows)"),
     }
     print(json.dumps(line), flush=True)
 
@@ -480,7 +510,7 @@ def run_ours(args, world, rank, local):
         threads = oracle.threads_available()
         v, dt, desc = oracle_sample(4096, threads, min_seconds=10.0)
         cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
-               "seconds": round(dt, 2)}
+               "seconds": round(dt, 2), "single_thread": oracle_per_config()}
 
     if rank == 0:
         line = {
