@@ -150,11 +150,12 @@ struct TcCfg {
     // Byte-table decode: each qs byte (two nibbles) is looked up in shared
     // memory as the fp16x2 word of the A operand.  32 copies of each of the
     // 256 entries, copy l in bank l, so a warp's 32 lookups never conflict.
-    // Up to MT = 96 entry j starts at byte 256 j: one byte permute of the qs
+    // At MT = 16 entry j starts at byte 256 j: one byte permute of the qs
     // word and the lane's offset 4l builds the whole lookup address (the
     // byte as bits 8-15), one instruction less per lookup than a shift and
-    // add (measured 6-15% faster); larger tiles, whose activation stages
-    // leave no room for the 64 KB, keep entries 128 bytes apart.
+    // add (measured 6-15% faster).  Larger tiles keep entries 128 bytes
+    // apart and give the 32 KB saved to a deeper activation ring (measured
+    // as fast or faster from MT = 32 on).
     // Activation stage slot: the staged codes (Q8_1 form: MT rows x 128 B,
     // swizzled) and the B operand of 4 sub-blocks (kBSubBytes each: one fp16
     // plane, or hi and lo planes of the prepared form).
@@ -165,18 +166,23 @@ struct TcCfg {
         const int nx0 = nb + (kNP * kU + kBStageSubs - 1) / kBStageSubs + 1;
         const int nx = kPrep ? 1 : (nx0 < 8 ? nx0 : 8);
         return nw * kWStage + 256 * lut_stride + nb * kBSlotBytes + (kPrep ? 0 : nx * kBStageSubs * MT * 4) +
-               8 * (2 * nw + 2 * nb + 2 * nx + 3 * kNP + 2) + 32 + (kPrep ? MT * 4 : 0);
+               8 * (2 * nw + 2 * nb + 2 * nx + 3 * kNP + 2) + 32 + (kPrep ? 4 * MT * 4 : 0);
     }
     static constexpr int kSmemLimit = 226 * 1024;
-    static constexpr bool kWideLut = MT <= 96 && usage(2, 2, 256) <= kSmemLimit;
+    static constexpr bool kWideLut = MT <= 16 && usage(2, 2, 256) <= kSmemLimit;
     // Without room for even the 32 KB table (the prepared form at MT = 128)
     // the decoders use register tables (byte permutes, ~15 integer
     // instructions per 8 weights).
     static constexpr bool kLut = kWideLut || usage(2, 2, 128) <= kSmemLimit;
     static constexpr int kLutStride = kWideLut ? 256 : kLut ? 128 : 0;
     static constexpr int kLutBytes = 256 * kLutStride;
-    static constexpr int kNW0 = (MT <= 16) ? 4 : (MT <= 64) ? 3 : 2;  // W stages, before the fit
-    static constexpr int kNB0 = (MT <= 32) ? 4 : (MT <= 64) ? 3 : 2;  // activation stages
+    // Ring depths before the fit.  An activation stage's slot stays busy
+    // until the MMAs of its units complete, a unit or two behind the
+    // decoders, so the activation ring is the deep one: 6 stages instead of
+    // 3 at MT = 16 measured 11-12% faster on K ranges of 5120 and more.  A W
+    // stage holds 8 units of work, so three (two from MT = 64) suffice.
+    static constexpr int kNW0 = (MT <= 48) ? 3 : 2;
+    static constexpr int kNB0 = (MT <= 16) ? 6 : (MT <= 32) ? 5 : (MT <= 64) ? 4 : 3;
     static constexpr int fit(bool want_nb) {
         int nw = kNW0, nb = kNB0;
         while (usage(nw, nb, kLutStride) > kSmemLimit) { if (nb > 2) --nb; else --nw; }
@@ -228,7 +234,7 @@ struct TcCfg {
     static constexpr int kOffRecv = kOffW;
     static_assert(kTileN * kRedStride * 4 <= kNB * kBSlotBytes, "staged partial tile fits the activation ring");
     static_assert(recv_rows_max() * kRedStride * 4 <= kOffB - kOffW, "received slices fit the W ring and table");
-    static constexpr int kUsed = kOffSpan + (kPrep ? MT * 4 : 0);
+    static constexpr int kUsed = kOffSpan + (kPrep ? 4 * MT * 4 : 0);
     static_assert(kUsed <= usage(kNW, kNB, kLutStride), "the ring fit counts every region");
     static_assert(kUsed <= 226 * 1024, "stages fit shared memory");
     static constexpr int kSmem = (kUsed > kMinSmem) ? kUsed : kMinSmem;
@@ -617,11 +623,16 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
                                     (p0 * kSubPerPair + bs * kBStageSubs) * kSub, z * MT, &q_full[slot]);
                     }
                 };
+                // At most three activation stages go out before the W stages
+                // after the first (when every CTA requests at once, the first
+                // units' operands are served first); the rest follow in the
+                // loop, into slots that need no wait.
+                constexpr int kFirstQ = (C::kNB < 3) ? C::kNB : 3;
                 int issued_w = 1, issued_q = 0;
                 bool ok = true;
                 const int pre = (C::kNW < (p1 - p0)) ? C::kNW : (p1 - p0);
                 griddep_wait();  // the codes come from the preceding grid
-                for (int bs = 0; bs < C::kNB && bs < nbst; ++bs) {
+                for (int bs = 0; bs < kFirstQ && bs < nbst; ++bs) {
                     load_q_stage(bs, bs);
                     ++issued_q;
                 }
@@ -711,13 +722,22 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
         // (every 32 sub-blocks); the current span's scales are staged in
         // shared memory, each group's own entries by that group.
         const float* span_scale = nullptr;
+        // [2][MT] the current span's 2^e (two buffers), then [2][MT] the
+        // ratios old / new 2^e of a switch (two buffers)
         float* s_span = reinterpret_cast<float*>(smem + C::kOffSpan) + c0;
         int cur_span = (p0 * kSubPerPair) / kSubPerSpan;
+        const int last_span = (p1 * kSubPerPair - 1) / kSubPerSpan;
+        float cur_e = 1.f, next_e = 1.f;  // thread t < kMH: its column's 2^e, this span and the next
+        int nswitch = 0;
         if constexpr (kPrep) {
             griddep_wait();
             span_scale = reinterpret_cast<const float*>(tc_op + tc_qh_bytes(M, K)) +
                          (int64_t)z * tc_num_spans(K) * MT + c0;
-            if (t < kMH) s_span[t] = span_scale[(int64_t)cur_span * MT + t];
+            if (t < kMH) {
+                cur_e = span_scale[(int64_t)cur_span * MT + t];
+                if (cur_span < last_span) next_e = span_scale[(int64_t)(cur_span + 1) * MT + t];
+                s_span[t] = cur_e;
+            }
             named_barrier_sync(kEpilogueBarrier + eg, kTileN);
         }
         bool ok = true;
@@ -726,20 +746,33 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
             const int l0 = v * C::kU, bs = l0 / kBStageSubs, jj = l0 % kBStageSubs, xs = bs % C::kNX;
             if constexpr (kPrep) {
                 const int span = (p0 * kSubPerPair + l0) / kSubPerSpan;
-                if (span != cur_span) {
-                    const float4* fo = reinterpret_cast<const float4*>(s_span);
-                    const float4* fn = reinterpret_cast<const float4*>(span_scale + (int64_t)span * MT);
+                if (span != cur_span) {  // span == cur_span + 1
+                    // The new span's 2^e was loaded a span ahead (a load at
+                    // the switch itself stalled the epilogue ~1,700 cycles,
+                    // measured).  Thread t publishes its column's ratio, an
+                    // exact power of two, and the new 2^e, each in the
+                    // buffer of this switch's parity: a thread reads switch
+                    // k's buffers between barriers k and k + 1, and the
+                    // buffers are rewritten at switch k + 2, so one barrier
+                    // per switch suffices.
+                    float* ratio = s_span + (2 + (nswitch & 1)) * MT;
+                    if (t < kMH) {
+                        ratio[t] = cur_e / next_e;
+                        cur_e = next_e;
+                        s_span[((nswitch + 1) & 1) * MT + t] = cur_e;
+                        if (span < last_span) next_e = span_scale[(int64_t)(span + 1) * MT + t];
+                    }
+                    named_barrier_sync(kEpilogueBarrier + eg, kTileN);
+                    const float4* f = reinterpret_cast<const float4*>(ratio);
 #pragma unroll
                     for (int m = 0; m < kMH; m += 4) {
-                        const float4 a = fo[m / 4], b = fn[m / 4];
-                        acc[m] *= a.x / b.x;
-                        acc[m + 1] *= a.y / b.y;
-                        acc[m + 2] *= a.z / b.z;
-                        acc[m + 3] *= a.w / b.w;
+                        const float4 a = f[m / 4];
+                        acc[m] *= a.x;
+                        acc[m + 1] *= a.y;
+                        acc[m + 2] *= a.z;
+                        acc[m + 3] *= a.w;
                     }
-                    named_barrier_sync(kEpilogueBarrier + eg, kTileN);  // every thread has read the old scales
-                    if (t < kMH) s_span[t] = span_scale[(int64_t)span * MT + t];
-                    named_barrier_sync(kEpilogueBarrier + eg, kTileN);
+                    ++nswitch;
                     cur_span = span;
                 }
             } else if (ok && jj == 0) {  // the stage's scales
@@ -810,7 +843,8 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
             if (++sp == C::kNP) { sp = 0; sphase ^= 1; }
         }
         if constexpr (kPrep) {  // back to true units: times the last span's 2^e (exact)
-            const float4* f = reinterpret_cast<const float4*>(s_span);
+            // (written before the last barrier this thread passed)
+            const float4* f = reinterpret_cast<const float4*>(s_span + (nswitch & 1) * MT);
 #pragma unroll
             for (int m = 0; m < kMH; m += 4) {
                 const float4 a = f[m / 4];
