@@ -44,9 +44,16 @@ UNIT = "GB/s"
 N_COPIES = 45
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "matmul_square4096_traffic.txt")
-# Sources of the kernel whose DRAM traffic is recorded (the tcgen05 matmul).
-KERNEL_SOURCES = ("iq4_xs_quantized_gb300/csrc/matmul_tc.cu",
-                  "iq4_xs_quantized_gb300/csrc/internal.cuh")
+# Sources of the kernels whose DRAM traffic is recorded, per kernel path
+# (2 = tcgen05, 4 = warp-level MMA).
+KERNEL_SOURCES = {
+    2: ("iq4_xs_quantized_gb300/csrc/matmul_tc.cu", "iq4_xs_quantized_gb300/csrc/internal.cuh"),
+    4: ("iq4_xs_quantized_gb300/csrc/matmul_mma.cu", "iq4_xs_quantized_gb300/csrc/internal.cuh"),
+}
+TRAFFIC_PREFIX = {2: "", 4: "mma."}  # key prefix of each kernel's entries in TRAFFIC_FILE
+PATH_NAMES = {1: "dp4a", 2: "tc (prepared operand)", 4: "mma (warp-level tensor cores)"}
+KERNEL_NAMES = {1: "matmul_dp4a_kernel (CUDA cores)", 2: "matmul_tc_kernel (tcgen05, prepared-operand form)",
+                4: "matmul_mma_kernel (warp-level mma.sync, decode into registers)"}
 
 
 def parse_args():
@@ -118,6 +125,19 @@ def tc_executed_flops(M, N, K):
     return 2 * (-(-N // 128) * 128) * (mtiles * mt) * K
 
 
+def mma_executed_flops(M, N, K):
+    """Floating-point work of one warp-MMA launch: m16n8k16 MMAs over the
+    weight rows (16-row fragments) x activation tiles of 8, 16, 24 or 32
+    rows (M above 32 in tiles of 32)."""
+    mt = min(32, -(-M // 8) * 8)
+    mtiles = -(-M // mt)
+    return 2 * (-(-N // 16) * 16) * (mtiles * mt) * K
+
+
+def executed_flops(path, M, N, K):
+    return mma_executed_flops(M, N, K) if path == 4 else tc_executed_flops(M, N, K)
+
+
 ROOFLINE_SLACK = 1.10
 
 
@@ -134,37 +154,39 @@ def roofline_gate(items, peak_gbs, slack=ROOFLINE_SLACK):
             "ok": not bad}
 
 
-def kernel_source_hash():
+def kernel_source_hash(path=2):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[path]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_counters():
-    """Per tcgen05 matmul launch (mean over the sweep's tcgen05 M) from the
-    committed ncu summary: DRAM bytes and warp instructions executed.  Empty
-    if absent or taken on different kernel sources."""
+def recorded_counters(path=2):
+    """Per matmul launch of the kernel on `path` (mean over the sweep's M on
+    that path) from the committed ncu summary: DRAM bytes and warp
+    instructions executed.  Empty if absent or taken on different kernel
+    sources."""
     try:
+        pre = TRAFFIC_PREFIX[path]
         vals = {}
         with open(TRAFFIC_FILE) as f:
             for line in f:
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     vals[k.strip()] = v.strip()
-        if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        if vals.get(pre + "kernel_source_sha256_16") != kernel_source_hash(path):
             return {}
-        out = {"dram_bytes": float(vals["dram_bytes_per_tc_launch_mean"])}
-        if "inst_executed_per_tc_launch_mean" in vals:
-            out["inst"] = float(vals["inst_executed_per_tc_launch_mean"])
+        out = {"dram_bytes": float(vals[pre + "dram_bytes_per_tc_launch_mean"])}
+        if pre + "inst_executed_per_tc_launch_mean" in vals:
+            out["inst"] = float(vals[pre + "inst_executed_per_tc_launch_mean"])
         return out
     except Exception:
         return {}
 
 
-def recorded_traffic():
-    return recorded_counters().get("dram_bytes")
+def recorded_traffic(path=2):
+    return recorded_counters(path).get("dram_bytes")
 
 
 # ------------------------------------------------------------------------ clocks
@@ -437,19 +459,23 @@ def run_ours(args, world, rank, local):
     for M in ms:
         us = mm_us[M]
         gbs = matmul_bytes(M, N, K) / (us * 1e-6) / 1e9
-        row = {"M": M, "path": {1: "dp4a", 2: "tc (prepared operand)"}[paths[M]],
+        row = {"M": M, "path": PATH_NAMES[paths[M]],
                "matmul_us": round(us, 3), "GBps": round(gbs, 1),
                "TOPS": round(2 * M * N * K / (us * 1e-6) / 1e12, 3), "hbm_frac": round(gbs / peak, 4)}
         if M in q8_us:
             row["q8_form_us"] = round(q8_us[M], 3)
             row["q8_form_GBps"] = round(matmul_bytes(M, N, K) / (q8_us[M] * 1e-6) / 1e9, 1)
         per_m.append(row)
-    # Dominant kernel: the tcgen05 matmul (M above the dispatcher's crossover).
-    tc_ms = [M for M in ms if paths[M] == B.PATH_TC] or list(ms)
+    # Dominant kernel: the path with the largest share of the sweep's matmul time.
+    share = {}
+    for M in ms:
+        share[paths[M]] = share.get(paths[M], 0.0) + mm_us[M]
+    dom = max(share, key=share.get)
+    tc_ms = [M for M in ms if paths[M] == dom]
     tc_bytes = sum(matmul_bytes(M, N, K) for M in tc_ms)
     tc_us = sum(mm_us[M] for M in tc_ms)
     achieved = tc_bytes / (tc_us * 1e-6) / 1e9
-    traffic = recorded_traffic() if not args.shape else None  # recorded for the square shape
+    traffic = recorded_traffic(dom) if (not args.shape and dom in KERNEL_SOURCES) else None
     mm_bytes = sum(matmul_bytes(M, N, K) for M in ms)
     mm_us_total = sum(mm_us.values())
 
@@ -459,14 +485,19 @@ def run_ours(args, world, rank, local):
     # sources) against 4 per SM and cycle at the sampled SM clock.
     tpeak, tpeak_kind = tensor_peak_tflops()
     tc_method = sum(2 * M * N * K for M in tc_ms) / (tc_us * 1e-6) / 1e12
-    tc_exec = sum(tc_executed_flops(M, N, K) for M in tc_ms) / (tc_us * 1e-6) / 1e12
+    tc_exec = (sum(executed_flops(dom, M, N, K) for M in tc_ms) / (tc_us * 1e-6) / 1e12
+               if dom in KERNEL_SOURCES else 0.0)
+    counts = {2: "achieved = executed fp16 MMA flops (128 x MT x 16 MMAs on padded tiles: two per "
+                 "sub-block from the Q8_1 codes, four from the prepared operand, counted as two); "
+                 "method_tops = 2*M*N*K",
+              4: "achieved = executed fp16 MMA flops (m16n8k16 on 8/16/24/32-row activation tiles); "
+                 "method_tops = 2*M*N*K; peak = the dense fp16/bf16 rate of the 5th-generation "
+                 "tensor cores (warp-level MMA issues at a fraction of it)"}.get(dom, "no tensor work")
     tensor = {"achieved": tc_exec, "peak": tpeak, "unit": "TFLOP/s", "frac": tc_exec / tpeak,
               "method_tops": tc_method, "method_frac": tc_method / tpeak,
-              "peak_kind": tpeak_kind,
-              "counts": "achieved = executed fp16 MMA flops (two 128 x MT x 16 MMAs per "
-                        "sub-block, padded tiles); method_tops = 2*M*N*K"}
+              "peak_kind": tpeak_kind, "counts": counts}
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
-    inst = recorded_counters().get("inst") if not args.shape else None
+    inst = recorded_counters(dom).get("inst") if (not args.shape and dom in KERNEL_SOURCES) else None
     issue = None
     if inst and clk.get("sm_mhz"):
         ipeak = nsm * 4 * clk["sm_mhz"] * 1e6 / 1e12  # T warp-instructions / s
@@ -530,15 +561,16 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "traffic_algorithmic": tc_bytes / len(tc_ms),
-                         "kernel": f"matmul_tc_kernel (tcgen05, prepared-operand form), M in {tc_ms}: "
+                         "kernel": f"{KERNEL_NAMES[dom]}, M in {tc_ms}: "
                                    "algorithmic bytes per launch / mean launch time",
+                         "time_share": {PATH_NAMES[p]: round(v / mm_us_total, 3) for p, v in share.items()},
                          "peak_kind": peak_kind, "timing": mm_timing,
                          "tensor": tensor, "alu": issue, "binding": binding,
                          "binding_rule": "the roofline with the largest fraction"},
             "roofline_gate": roofline_gate(gate_items, peak),
             "matmul_all": {"achieved_gbs": mm_bytes / (mm_us_total * 1e-6) / 1e9,
                            "frac": mm_bytes / (mm_us_total * 1e-6) / 1e9 / peak,
-                           "kernels": "dp4a for M <= crossover, tcgen05 above, whole sweep"},
+                           "kernels": "the dispatcher's path per M (dp4a, warp MMA, tcgen05), whole sweep"},
             "per_m": per_m,
             "e2e": e2e,
             **extras,
@@ -842,16 +874,25 @@ def decoder_shapes(torch, B, dev, stream, reps=10):
                     else:
                         B.iq4xs_matmul(w, N, K, qs, ds, M, y, path, stream)
 
-            def mm_q8():
-                for w in ws:
-                    B.iq4xs_matmul(w, N, K, qs, ds, M, y, B.PATH_TC, stream)
+            def mm_path(p):
+                def f():
+                    for w in ws:
+                        if p == "tcp":
+                            B.iq4xs_matmul_tc_operand(w, N, K, op, M, y, stream=stream)
+                        else:
+                            B.iq4xs_matmul(w, N, K, qs, ds, M, y, p, stream)
+                return f
             us = _graph_us(torch, stream, mm, len(ws), reps)
             gbs = matmul_bytes(M, N, K) / (us * 1e-6) / 1e9
-            row = {"N": N, "K": K, "M": M, "path": "dp4a" if path == B.PATH_DP4A else "tc (prepared)",
+            row = {"N": N, "K": K, "M": M, "path": PATH_NAMES[path],
                    "us": round(us, 3), "GBps": round(gbs, 1),
                    "TOPS": round(2 * M * N * K / (us * 1e-6) / 1e12, 2)}
-            if path == B.PATH_TC:
-                row["q8_form_us"] = round(_graph_us(torch, stream, mm_q8, len(ws), reps), 3)
+            # every other kernel path beside the dispatcher's choice
+            alts = {"tc_us": "tcp", "q8_form_us": B.PATH_TC, "mma_us": B.PATH_MMA}
+            if M <= 16:
+                alts["dp4a_us"] = B.PATH_DP4A
+            for key, p in alts.items():
+                row[key] = round(_graph_us(torch, stream, mm_path(p), len(ws), reps), 3)
             res.append(row)
         del ws
         torch.cuda.empty_cache()

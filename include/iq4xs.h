@@ -93,12 +93,17 @@ typedef enum {
     IQ4XS_PATH_DP4A = 1,    /* CUDA-core int8 dot products (small M)             */
     IQ4XS_PATH_TC = 2,      /* tcgen05 tensor cores: exact integer sub-block dots
                                in fp32 tensor memory, fp32 scale-in (larger M)   */
-    IQ4XS_PATH_BASELINE = 3 /* advice from iq4xs_select_path only: above a
+    IQ4XS_PATH_BASELINE = 3,/* advice from iq4xs_select_path only: above a
                                measured M, dequantizing W (iq4xs_dequantize) and
                                a dense bf16 GEMM in the caller's BLAS is faster,
                                at bf16 precision.  The library's own calls never
                                take it: iq4xs_matmul / iq4xs_linear run TC
                                there, and reject it as an explicit path.        */
+    IQ4XS_PATH_MMA = 4      /* warp-level tensor-core MMA (mma.sync m16n8k16):
+                               decoded weights go straight from the byte-table
+                               lookup into the MMA's registers and every
+                               sub-block's exact integer dot is scaled in from
+                               registers (small and medium M; IQ4_XS only)    */
 } iq4xs_path;
 
 /*
@@ -160,13 +165,16 @@ int64_t iq4xs_tc_operand_bytes(int64_t M, int64_t K);
  *   M       activation rows; y fp32 [M][ldy] output, fully overwritten for
  *           columns < N.
  *   path    an iq4xs_path value: AUTO (the choice iq4xs_select_path makes),
- *           DP4A or TC; BASELINE is advice only and returns IQ4XS_ERR_ARG.
- * The TC path needs K % 512 == 0 (super-blocks are staged in pairs so every
- * copy starts on a 16-byte boundary), else IQ4XS_ERR_SHAPE.
- * Result: each sub-block's dot sum_i kv*q is an exact integer on both paths
- * (int32 on DP4A; on TC exact in the tensor core's fp32 accumulator, every
- * partial sum being an integer below 2^24); the scaled sub-block terms are
- * accumulated in fp32, so y differs from the fp64 definition by fp32
+ *           DP4A, TC or MMA; BASELINE is advice only and returns
+ *           IQ4XS_ERR_ARG.
+ * The TC and MMA paths need K % 512 == 0 (they stage W rows by tensor map,
+ * whose row stride must be a multiple of 16 bytes: super-blocks in pairs),
+ * else IQ4XS_ERR_SHAPE; MMA takes IQ4_XS weights only; DP4A takes any
+ * K % 256 == 0.
+ * Result: each sub-block's dot sum_i kv*q is an exact integer on every path
+ * (int32 on DP4A; on TC and MMA exact in the tensor core's fp32 accumulator,
+ * every partial sum being an integer below 2^24); the scaled sub-block terms
+ * are accumulated in fp32, so y differs from the fp64 definition by fp32
  * rounding and summation order only.
  */
 int iq4xs_matmul(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds,
@@ -304,10 +312,14 @@ int iq4xs_dequantize_wt(const void* w, int wtype, int64_t N, int64_t K, void* ou
  * Path choice for (M, N, K) (engine page, mmvq vs dequantize table: the
  * original dispatcher hard-coded its threshold at M=8 while the measured
  * crossover was M~15; the dequantize + GEMM route was the choice above it).
- * Host only, no device access.  Returns DP4A when M <= the calibrated
- * crossover for the matrix's size class (iq4xs_set_crossover_classes) and the
- * DP4A path applies; BASELINE when M >= the calibrated
- * baseline threshold (0 = never); TC otherwise (TC requires K % 512 == 0).
+ * Host only, no device access.  For the matrix's weight-size class (N*K):
+ * DP4A when M <= the calibrated DP4A crossover (iq4xs_set_crossover,
+ * iq4xs_set_crossover_classes); MMA when M <= the calibrated warp-MMA
+ * crossover (iq4xs_set_mma_crossover, iq4xs_set_mma_crossover_classes);
+ * BASELINE when M >= the calibrated baseline threshold (0 = never); TC
+ * otherwise.  K % 512 != 0 always gives DP4A (neither tensor-core path takes
+ * it).  For Q4_0 / IQ4_NL weights (iq4xs_matmul_wt with AUTO) an MMA answer
+ * becomes TC.
  */
 int iq4xs_select_path(int64_t M, int64_t N, int64_t K, int* path_out);
 
@@ -326,6 +338,19 @@ int iq4xs_set_crossover(int64_t m_max_dp4a);
  * nothing changes.  Host only; the arrays are copied.  Thread-safe.
  */
 int iq4xs_set_crossover_classes(const int64_t* min_weights, const int64_t* m_max_dp4a, int count);
+
+/*
+ * Install the measured warp-MMA crossover: above the DP4A range, MMA is
+ * chosen for M <= m_max_mma (default 8 until a calibration sets it), TC
+ * above.  Host only.  Thread-safe.  IQ4XS_ERR_ARG outside 0..32768.
+ */
+int iq4xs_set_mma_crossover(int64_t m_max_mma);
+
+/*
+ * The same per weight-size class, with the rules of
+ * iq4xs_set_crossover_classes (at most 16 entries; count = 0 clears them).
+ */
+int iq4xs_set_mma_crossover_classes(const int64_t* min_weights, const int64_t* m_max_mma, int count);
 
 /*
  * Install the measured upper threshold: iq4xs_select_path answers BASELINE
@@ -355,7 +380,9 @@ int iq4xs_set_pdl(int enable);
  *   0x101 a W stage      0x102 an activation stage   0x103 a decoded unit
  *   0x104 a unit's MMAs  0x105 a free unit slot      0x106 the final drain
  *   0x107 the split-K slices of the other cluster ranks
- *   0x108 a stage of Q8_1 codes  0x109 a stage of activation scales.
+ *   0x108 a stage of Q8_1 codes  0x109 a stage of activation scales;
+ * in the warp-MMA matmul:
+ *   0x10B a stage of weights and codes   0x10C a stage slot being freed.
  * (0x102 is a code stage's MMAs completing, which frees its slot.)
  */
 int iq4xs_last_device_error(int* code_out);
@@ -370,6 +397,18 @@ int iq4xs_last_device_error(int* code_out);
  * reports IQ4XS_ERR_TIMEOUT with code 0x101.  -1 disarms.  Host only.
  */
 int iq4xs_test_skip_w_stage(int64_t stage);
+
+/*
+ * Test hook for the warp-MMA path's launch configuration (no counterpart on
+ * the source pages): later MMA launches use rows_per_cta weight rows per CTA
+ * (a multiple of 32, at most 256; capped at 128 when M > 16) and k_splits
+ * CTAs per cluster along K (1..8, capped at the K range's super-block
+ * pairs) instead of the launch model's choice, so that tests reach every
+ * tile height and split.  0 restores the model's choice for that value.
+ * Host only; applies to every thread's later launches.  IQ4XS_ERR_ARG for
+ * other values.
+ */
+int iq4xs_test_mma_config(int64_t rows_per_cta, int64_t k_splits);
 
 /* Static string for a status code. */
 const char* iq4xs_status_string(int status);

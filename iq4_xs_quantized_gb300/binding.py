@@ -19,8 +19,8 @@ LIB_PATH = os.path.join(_HERE, "libiq4xs.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "iq4xs.h")
 
 OK, ERR_ARG, ERR_ALIGN, ERR_SHAPE, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT = range(7)
-PATH_AUTO, PATH_DP4A, PATH_TC, PATH_BASELINE = 0, 1, 2, 3
-PATHS = {"auto": PATH_AUTO, "dp4a": PATH_DP4A, "tc": PATH_TC}
+PATH_AUTO, PATH_DP4A, PATH_TC, PATH_BASELINE, PATH_MMA = 0, 1, 2, 3, 4
+PATHS = {"auto": PATH_AUTO, "dp4a": PATH_DP4A, "tc": PATH_TC, "mma": PATH_MMA}
 WTYPE_IQ4_XS, WTYPE_Q4_0, WTYPE_IQ4_NL = 0, 1, 2
 WTYPES = {"iq4_xs": WTYPE_IQ4_XS, "q4_0": WTYPE_Q4_0, "iq4_nl": WTYPE_IQ4_NL}
 
@@ -77,6 +77,9 @@ def load(path: str | None = None):
         lib.iq4xs_set_crossover.argtypes = [i64]
         lib.iq4xs_set_baseline_threshold.argtypes = [i64]
         lib.iq4xs_set_crossover_classes.argtypes = [ctypes.POINTER(i64), ctypes.POINTER(i64), ci]
+        lib.iq4xs_set_mma_crossover.argtypes = [i64]
+        lib.iq4xs_test_mma_config.argtypes = [i64, i64]
+        lib.iq4xs_set_mma_crossover_classes.argtypes = [ctypes.POINTER(i64), ctypes.POINTER(i64), ci]
         lib.iq4xs_set_pdl.argtypes = [ci]
         lib.iq4xs_set_pdl.restype = ci
         lib.iq4xs_last_device_error.argtypes = [ctypes.POINTER(ci)]
@@ -87,6 +90,8 @@ def load(path: str | None = None):
                      "iq4xs_dequantize", "iq4xs_linear", "iq4xs_matmul_wt", "iq4xs_dequantize_wt",
                      "iq4xs_select_path", "iq4xs_set_crossover", "iq4xs_set_baseline_threshold",
                      "iq4xs_set_crossover_classes", "iq4xs_test_skip_w_stage",
+                     "iq4xs_set_mma_crossover", "iq4xs_set_mma_crossover_classes",
+                     "iq4xs_test_mma_config",
                      "iq4xs_quantize_q8_1_tc", "iq4xs_matmul_tc_operand",
                      "iq4xs_last_device_error"):
             getattr(lib, name).restype = ci
@@ -107,13 +112,30 @@ def _install_calibration(lib):
         _set_classes(lib, table["crossover_classes"])
     if table and "baseline_m_min" in table:
         lib.iq4xs_set_baseline_threshold(int(table["baseline_m_min"]))
+    if table and "mma_m_max" in table:
+        lib.iq4xs_set_mma_crossover(int(table["mma_m_max"]))
+    if table and "mma_classes" in table:
+        _set_classes(lib, table["mma_classes"], mma=True)
 
 
-def _set_classes(lib, classes):
+def reset_dispatch() -> None:
+    """Dispatcher back to the library defaults (DP4A to M = 4, MMA to M = 8,
+    no classes, no baseline advice), then the calibrated table if present."""
+    lib = load()
+    lib.iq4xs_set_crossover(4)
+    lib.iq4xs_set_mma_crossover(8)
+    _set_classes(lib, [])
+    _set_classes(lib, [], mma=True)
+    lib.iq4xs_set_baseline_threshold(0)
+    _install_calibration(lib)
+
+
+def _set_classes(lib, classes, mma=False):
     n = len(classes)
     mins = (ctypes.c_int64 * max(n, 1))(*[int(c[0]) for c in classes])
     ms = (ctypes.c_int64 * max(n, 1))(*[int(c[1]) for c in classes])
-    return lib.iq4xs_set_crossover_classes(mins, ms, n)
+    fn = lib.iq4xs_set_mma_crossover_classes if mma else lib.iq4xs_set_crossover_classes
+    return fn(mins, ms, n)
 
 
 def _check(fn: str, rc: int):
@@ -265,6 +287,20 @@ def iq4xs_set_crossover(m_max_dp4a: int) -> None:
 def iq4xs_set_crossover_classes(classes) -> None:
     """[(min_weights, m_max_dp4a), ...]: the crossover per weight-size class."""
     _check("iq4xs_set_crossover_classes", _set_classes(load(), list(classes)))
+
+
+def iq4xs_set_mma_crossover(m_max_mma: int) -> None:
+    _check("iq4xs_set_mma_crossover", load().iq4xs_set_mma_crossover(int(m_max_mma)))
+
+
+def iq4xs_set_mma_crossover_classes(classes) -> None:
+    """classes: [(min_weights, m_max_mma), ...]; [] clears them."""
+    _check("iq4xs_set_mma_crossover_classes", _set_classes(load(), list(classes), mma=True))
+
+
+def iq4xs_test_mma_config(rows_per_cta: int = 0, k_splits: int = 0) -> None:
+    """Force the warp-MMA launch configuration (0 = the launch model's choice)."""
+    _check("iq4xs_test_mma_config", load().iq4xs_test_mma_config(int(rows_per_cta), int(k_splits)))
 
 
 def iq4xs_set_baseline_threshold(m_min_baseline: int) -> None:

@@ -1,14 +1,18 @@
-"""Measure the dp4a <-> tcgen05 crossover and store it for the dispatcher.
+"""Measure the path crossovers (dp4a -> warp MMA -> tcgen05) and store them
+for the dispatcher.
 
 The engine page's dispatcher hard-coded its mmvq -> dequantize threshold at
 M=8 while the measured crossover sat near M=15 (V100TPS engine page, mmvq vs
-dequantize table).  Here the crossover is measured: for every M in 1..16 and
-every calibration shape, both kernel paths are timed from CUDA-graph replays
-over rotating weight copies (inputs larger than L2); the dispatcher's
-threshold becomes the largest M at which the dp4a path costs less summed over
-the shapes, each shape's times taken relative to the faster path there (so
-that every shape counts alike, not the one with the most bytes).  The result is written to ``dispatch_table.json`` beside this file
-and installed with ``iq4xs_set_crossover`` whenever the binding loads.
+dequantize table).  Here every crossover is measured: for each calibration
+shape and M, the three kernel paths are timed from CUDA-graph replays over
+rotating weight copies (inputs larger than L2), the tensor-core path in the
+prepared form iq4xs_linear runs.  Per shape, the DP4A range ends at the
+first M at which another path is faster, the MMA range at the first M above
+it at which tcgen05 is faster; each shape's thresholds apply to its
+weight-size class (from the geometric mean of its weight count and the next
+smaller shape's), the smallest shape's to everything below.  The result is
+written to ``dispatch_table.json`` beside this file and installed whenever
+the binding loads.
 
 Run on the GPU:  python -m iq4_xs_quantized_gb300.calibrate
 """
@@ -22,7 +26,8 @@ import numpy as np
 
 TABLE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "dispatch_table.json")
 SHAPES = ((4096, 4096), (5120, 5120), (12288, 5120), (5120, 17408), (34816, 5120))
-MS = tuple(range(1, 17))
+MS = tuple(range(1, 17)) + (20, 24, 28, 32, 40, 48, 64)
+DP4A_MS = tuple(range(1, 17))  # dp4a is timed up to here (its cost grows with M)
 # Upper threshold: the tcgen05 route (quantize + matmul) against dequantize
 # to bf16 + a dense bf16 GEMM, on the square and the two prefill shapes.
 BASE_SHAPES = ((4096, 4096), (17408, 5120), (5120, 17408))
@@ -79,69 +84,69 @@ def calibrate(shapes=SHAPES, ms=MS, verbose=True):
         wcopies = [w] + [w.clone() for _ in range(ncopy - 1)]
         rows = {}
         for M in ms:
-            t_dp = time_path(B, torch, wcopies, N, K, M, B.PATH_DP4A)
-            t_tc = time_path(B, torch, wcopies, N, K, M, B.PATH_TC)
-            rows[M] = {"dp4a_us": round(t_dp, 3), "tc_us": round(t_tc, 3)}
+            r = {}
+            if M in DP4A_MS:
+                r["dp4a_us"] = round(time_path(B, torch, wcopies, N, K, M, B.PATH_DP4A), 3)
+            r["mma_us"] = round(time_path(B, torch, wcopies, N, K, M, B.PATH_MMA), 3)
+            r["tc_us"] = round(time_path(B, torch, wcopies, N, K, M, B.PATH_TC), 3)
+            rows[M] = r
             if verbose:
-                print(f"N={N} K={K} M={M}: dp4a {t_dp:.2f} us  tc {t_tc:.2f} us", flush=True)
+                print(f"N={N} K={K} M={M}: " + "  ".join(f"{k[:-3]} {v:.2f} us" for k, v in r.items()),
+                      flush=True)
         per_shape[f"{N}x{K}"] = rows
         del wcopies, w
         torch.cuda.empty_cache()
-    table = {"crossover_m_max_dp4a": crossover_from(per_shape, ms), "gpu": torch.cuda.get_device_name(),
-             "crossover_classes": class_crossovers(per_shape, ms),
+    dp4a_cls, mma_cls, dflt = class_crossovers(per_shape, ms)
+    table = {"crossover_m_max_dp4a": dflt[0], "mma_m_max": dflt[1], "gpu": torch.cuda.get_device_name(),
+             "crossover_classes": dp4a_cls, "mma_classes": mma_cls,
              "shapes": per_shape, "rule": CROSSOVER_RULE, "class_rule": CLASS_RULE}
     return table
 
 
-CROSSOVER_RULE = ("largest M (scanning up from 1) at which the dp4a path costs less than the "
-                  "tcgen05 path summed over the calibration shapes, each shape's time relative "
-                  "to the faster path at that shape and M")
+CROSSOVER_RULE = ("per shape: DP4A up to the last M (scanning up from 1) at which it is the fastest of "
+                  "the three paths; MMA from there up to the last M at which it is faster than the "
+                  "tcgen05 path (prepared form); tcgen05 above")
+CLASS_RULE = ("a calibration shape's thresholds apply from the geometric mean of its weight count "
+              "and the next smaller shape's; the smallest shape's thresholds are the defaults")
 
 
-def crossover_from(per_shape, ms):
-    """The dispatcher threshold from per-shape timings {shape: {M: {"dp4a_us", "tc_us"}}}."""
-    crossover = 0
+def _row(rows, M):
+    return rows.get(M, rows.get(str(M)))
+
+
+def shape_thresholds(rows, ms):
+    """(m_max_dp4a, m_max_mma) of one shape from {M: {"dp4a_us", "mma_us", "tc_us"}}."""
+    m_dp4a = 0
     for M in ms:
-        rel = {"dp4a": 0.0, "tc": 0.0}
-        for rows in per_shape.values():
-            r = rows.get(M, rows.get(str(M)))
-            best = min(r["dp4a_us"], r["tc_us"])
-            rel["dp4a"] += r["dp4a_us"] / best
-            rel["tc"] += r["tc_us"] / best
-        if rel["dp4a"] < rel["tc"]:
-            crossover = M
+        r = _row(rows, M)
+        if "dp4a_us" in r and r["dp4a_us"] < min(r["mma_us"], r["tc_us"]):
+            m_dp4a = M
         else:
             break
-    return crossover
-
-
-CLASS_RULE = ("per weight-size class: each calibration shape's own crossover (largest M, "
-              "scanning up from 1, at which dp4a is faster on that shape); a shape's class "
-              "starts at the geometric mean of its weight count and the next smaller shape's")
-
-
-def shape_crossover(rows, ms):
-    """Largest M (scanning up from 1) at which dp4a beats tcgen05 on one shape."""
-    crossover = 0
+    m_mma = m_dp4a
     for M in ms:
-        r = rows.get(M, rows.get(str(M)))
-        if r["dp4a_us"] < r["tc_us"]:
-            crossover = M
+        if M <= m_dp4a:
+            continue
+        r = _row(rows, M)
+        if r["mma_us"] < r["tc_us"]:
+            m_mma = M
         else:
             break
-    return crossover
+    return m_dp4a, m_mma
 
 
 def class_crossovers(per_shape, ms):
-    """[[min_weights, m_max_dp4a], ...] ascending, one class per calibration
-    shape above the smallest (the smallest shape's crossover is the default
-    for everything below the first class)."""
+    """([[min_weights, m_max_dp4a], ...], [[min_weights, m_max_mma], ...],
+    (default dp4a, default mma)): one class per calibration shape above the
+    smallest, whose thresholds are the defaults."""
     sizes = sorted((int(k.split("x")[0]) * int(k.split("x")[1]), k) for k in per_shape)
-    out = []
+    th = [shape_thresholds(per_shape[k], ms) for _, k in sizes]
+    dp4a, mma = [], []
     for i in range(1, len(sizes)):
         lo = int(round((sizes[i - 1][0] * sizes[i][0]) ** 0.5))
-        out.append([lo, shape_crossover(per_shape[sizes[i][1]], ms)])
-    return out
+        dp4a.append([lo, th[i][0]])
+        mma.append([lo, th[i][1]])
+    return dp4a, mma, th[0]
 
 
 def _graph_time(torch, fn, reps=10):
@@ -234,7 +239,8 @@ def main():
                               "over the shapes (0 = never)")
     with open(TABLE, "w") as f:
         json.dump(table, f, indent=1)
-    print(json.dumps({"crossover_m_max_dp4a": table["crossover_m_max_dp4a"],
+    print(json.dumps({"crossover_m_max_dp4a": table["crossover_m_max_dp4a"], "mma_m_max": table["mma_m_max"],
+                      "crossover_classes": table["crossover_classes"], "mma_classes": table["mma_classes"],
                       "baseline_m_min": table["baseline_m_min"]}))
 
 

@@ -34,26 +34,46 @@ std::atomic<int64_t> g_baseline_min{0};  // 0 = never advise the dequantize + GE
 std::atomic<int> g_pdl{1};
 std::atomic<int> g_skip_w_stage{-1};  // armed by iq4xs_test_skip_w_stage, one launch
 
-// Measured crossover per weight-size class: entry i applies to matrices of
-// at least g_class_min[i] weights (N*K), the largest such entry winning;
-// matrices below every entry use g_crossover.
-constexpr int kMaxClasses = 16;
-std::mutex g_class_mu;
-int g_nclass = 0;
-int64_t g_class_min[kMaxClasses];
-int64_t g_class_m[kMaxClasses];
+std::atomic<int64_t> g_mma_max{8};      // the warp-MMA path up to this M (above the DP4A range)
 
-int64_t crossover_for(int64_t N, int64_t K) {
-    const int64_t nk = N * K;
-    std::lock_guard<std::mutex> lock(g_class_mu);
-    int64_t m = g_crossover.load();
-    int64_t best = -1;
-    for (int i = 0; i < g_nclass; ++i)
-        if (g_class_min[i] <= nk && g_class_min[i] > best) {
-            best = g_class_min[i];
-            m = g_class_m[i];
-        }
-    return m;
+// Measured crossovers per weight-size class: entry i applies to matrices of
+// at least min[i] weights (N*K), the largest such entry winning; matrices
+// below every entry use the global value.  One table for the DP4A range and
+// one for the warp-MMA range.
+constexpr int kMaxClasses = 16;
+struct ClassTable {
+    std::mutex mu;
+    int n = 0;
+    int64_t min[kMaxClasses];
+    int64_t m[kMaxClasses];
+    int64_t lookup(int64_t nk, int64_t dflt) {
+        std::lock_guard<std::mutex> lock(mu);
+        int64_t r = dflt, best = -1;
+        for (int i = 0; i < n; ++i)
+            if (min[i] <= nk && min[i] > best) {
+                best = min[i];
+                r = m[i];
+            }
+        return r;
+    }
+};
+ClassTable g_dp4a_classes, g_mma_classes;
+
+int64_t crossover_for(int64_t N, int64_t K) { return g_dp4a_classes.lookup(N * K, g_crossover.load()); }
+int64_t mma_max_for(int64_t N, int64_t K) { return g_mma_classes.lookup(N * K, g_mma_max.load()); }
+
+int set_classes(ClassTable& tab, const int64_t* min_weights, const int64_t* m_max, int count) {
+    if (count < 0 || count > kMaxClasses) return IQ4XS_ERR_ARG;
+    if (count > 0 && (!min_weights || !m_max)) return IQ4XS_ERR_ARG;
+    for (int i = 0; i < count; ++i)
+        if (min_weights[i] < 1 || m_max[i] < 0 || m_max[i] > kMaxM) return IQ4XS_ERR_ARG;
+    std::lock_guard<std::mutex> lock(tab.mu);
+    for (int i = 0; i < count; ++i) {
+        tab.min[i] = min_weights[i];
+        tab.m[i] = m_max[i];
+    }
+    tab.n = count;
+    return IQ4XS_OK;
 }
 
 // One-time per-device set-up, done with that device current.
@@ -97,10 +117,15 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 
 inline int from_cuda(cudaError_t e) { return e == cudaSuccess ? IQ4XS_OK : IQ4XS_ERR_CUDA; }
 
-// The path this library's own kernels take (DP4A or TC).
-int kernel_path_impl(int64_t M, int64_t N, int64_t K) {
-    if (K % kPairK != 0) return IQ4XS_PATH_DP4A;  // TC stages super-blocks in pairs
-    return (M <= crossover_for(N, K)) ? IQ4XS_PATH_DP4A : IQ4XS_PATH_TC;
+// The path this library's own kernels take: DP4A up to the matrix class's
+// DP4A crossover, the warp-MMA path (IQ4_XS only) up to its MMA crossover,
+// TC above.  Both tensor-core paths stage W rows with a tensor map, whose
+// row stride must be a multiple of 16 bytes: K % 512 == 0 (136-byte
+// super-blocks in pairs); other K run DP4A.
+int kernel_path_impl(int64_t M, int64_t N, int64_t K, int wtype = IQ4XS_WTYPE_IQ4_XS) {
+    if (K % kPairK != 0 || M <= crossover_for(N, K)) return IQ4XS_PATH_DP4A;
+    if (wtype == IQ4XS_WTYPE_IQ4_XS && M <= mma_max_for(N, K)) return IQ4XS_PATH_MMA;
+    return IQ4XS_PATH_TC;
 }
 // The advised path: the kernel path, or BASELINE above the measured threshold.
 int select_path_impl(int64_t M, int64_t N, int64_t K) {
@@ -166,17 +191,20 @@ int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t
                     const void* ds, int64_t M, float* y, int64_t ldy, int path, int64_t stream) {
     if (!w || !qs || !ds || !y) return IQ4XS_ERR_ARG;
     if (wtype < IQ4XS_WTYPE_IQ4_XS || wtype > IQ4XS_WTYPE_IQ4_NL) return IQ4XS_ERR_ARG;
-    if (path < IQ4XS_PATH_AUTO || path > IQ4XS_PATH_TC) return IQ4XS_ERR_ARG;
+    if (path < IQ4XS_PATH_AUTO || path > IQ4XS_PATH_MMA || path == IQ4XS_PATH_BASELINE) return IQ4XS_ERR_ARG;
     if (M < 1 || M > kMaxM || N < 1 || N > (1 << 30) || K <= 0 || K % kQK || K > (1 << 30))
         return IQ4XS_ERR_SHAPE;
     if (ldy < N) return IQ4XS_ERR_ARG;
     if (!aligned(w, 16) || !aligned(qs, 16) || !aligned(ds, 4) || !aligned(y, 4)) return IQ4XS_ERR_ALIGN;
-    if (path == IQ4XS_PATH_AUTO) path = kernel_path_impl(M, N, K);
-    if (path == IQ4XS_PATH_TC && K % kPairK) return IQ4XS_ERR_SHAPE;
+    if (path == IQ4XS_PATH_AUTO) path = kernel_path_impl(M, N, K, wtype);
+    if ((path == IQ4XS_PATH_TC || path == IQ4XS_PATH_MMA) && K % kPairK) return IQ4XS_ERR_SHAPE;
+    if (path == IQ4XS_PATH_MMA && wtype != IQ4XS_WTYPE_IQ4_XS) return IQ4XS_ERR_SHAPE;
     DevState* st;
     int rc = device_state(&st);
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (path == IQ4XS_PATH_MMA)
+        return from_cuda(launch_matmul_mma(w, N, K, qs, ds, M, y, ldy, st->encode, st->err, st->num_sms, s));
     if (path == IQ4XS_PATH_TC)
         return from_cuda(launch_matmul_tc(w, wtype, N, K, qs, ds, nullptr, M, y, ldy, st->encode,
                                           st->err, st->num_sms, g_skip_w_stage.exchange(-1), s));
@@ -304,17 +332,17 @@ int iq4xs_set_crossover(int64_t m_max_dp4a) {
 }
 
 int iq4xs_set_crossover_classes(const int64_t* min_weights, const int64_t* m_max_dp4a, int count) {
-    if (count < 0 || count > kMaxClasses) return IQ4XS_ERR_ARG;
-    if (count > 0 && (!min_weights || !m_max_dp4a)) return IQ4XS_ERR_ARG;
-    for (int i = 0; i < count; ++i)
-        if (min_weights[i] < 1 || m_max_dp4a[i] < 0 || m_max_dp4a[i] > kMaxM) return IQ4XS_ERR_ARG;
-    std::lock_guard<std::mutex> lock(g_class_mu);
-    for (int i = 0; i < count; ++i) {
-        g_class_min[i] = min_weights[i];
-        g_class_m[i] = m_max_dp4a[i];
-    }
-    g_nclass = count;
+    return set_classes(g_dp4a_classes, min_weights, m_max_dp4a, count);
+}
+
+int iq4xs_set_mma_crossover(int64_t m_max_mma) {
+    if (m_max_mma < 0 || m_max_mma > kMaxM) return IQ4XS_ERR_ARG;
+    g_mma_max.store(m_max_mma);
     return IQ4XS_OK;
+}
+
+int iq4xs_set_mma_crossover_classes(const int64_t* min_weights, const int64_t* m_max_mma, int count) {
+    return set_classes(g_mma_classes, min_weights, m_max_mma, count);
 }
 
 int iq4xs_set_baseline_threshold(int64_t m_min_baseline) {
@@ -338,13 +366,23 @@ int iq4xs_last_device_error(int* code_out) {
     if (cudaMemcpyFromSymbol(code_out, g_device_error, sizeof(int)) != cudaSuccess ||
         cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess)
         return IQ4XS_ERR_CUDA;
-    return (*code_out >= kDevErrTimeoutW && *code_out <= kDevErrTimeoutX) ? IQ4XS_ERR_TIMEOUT
-                                                                           : IQ4XS_OK;
+    const int c = *code_out;
+    return ((c >= kDevErrTimeoutW && c <= kDevErrTimeoutX) || c == kDevErrTimeoutMmaStage ||
+            c == kDevErrTimeoutMmaSlot)
+               ? IQ4XS_ERR_TIMEOUT
+               : IQ4XS_OK;
 }
 
 int iq4xs_test_skip_w_stage(int64_t stage) {
     if (stage < -1 || stage > (1 << 20)) return IQ4XS_ERR_ARG;
     g_skip_w_stage.store((int)stage);
+    return IQ4XS_OK;
+}
+
+int iq4xs_test_mma_config(int64_t rows_per_cta, int64_t k_splits) {
+    if (rows_per_cta < 0 || rows_per_cta > 256 || rows_per_cta % 32 || k_splits < 0 || k_splits > 8)
+        return IQ4XS_ERR_ARG;
+    mma_force_config((int)(rows_per_cta / 32), (int)k_splits);
     return IQ4XS_OK;
 }
 

@@ -208,6 +208,8 @@ enum DeviceError : int {
     kDevErrTimeoutQ = 0x108,
     kDevErrTimeoutX = 0x109,
     kDevErrLayout = 0x10A,  // dynamic shared memory not 1024-byte aligned
+    kDevErrTimeoutMmaStage = 0x10B,  // warp-MMA matmul: a stage (W and codes) never landed
+    kDevErrTimeoutMmaSlot = 0x10C,   // warp-MMA matmul: a stage slot was never freed
 };
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: waits for a copy to land
 // Limits by what is awaited, so that the wait at the root of a stall runs out
@@ -215,7 +217,7 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: waits for a 
 // 2 s, a hand-off from another role 4 s, the final drains and the split-K
 // slices 6 s.
 __host__ __device__ constexpr unsigned long long wait_limit_ns(int code) {
-    return (code == kDevErrTimeoutW || code == kDevErrTimeoutQ) ? kWaitLimitNs
+    return (code == kDevErrTimeoutW || code == kDevErrTimeoutQ || code == kDevErrTimeoutMmaStage) ? kWaitLimitNs
            : (code == kDevErrTimeoutDrain || code == kDevErrTimeoutRecv) ? 3 * kWaitLimitNs
                                                                           : 2 * kWaitLimitNs;
 }
@@ -901,6 +903,15 @@ bool pdl_enabled();
 // TMA) when tc_operand is NULL, else the prepared operand alone (qs, ds
 // unused).  skip_w_stage >= 0 leaves that W stage of every CTA unissued
 // (tests of the bounded waits); -1 in every ordinary call.
+// Warp-level MMA path (IQ4_XS only): activation tiles of mma_tile_rows(M)
+// rows (8, 16, 24 or 32); any K % 256 == 0; qs 16-byte aligned (staged by
+// TMA), ds read directly.
+int mma_tile_rows(int64_t M);
+// Test override of the warp-MMA launch: 16-row weight fragments per consumer
+// warp (rows per CTA = 32 x that) and K splits; 0 = the launch model's choice.
+void mma_force_config(int frags_per_warp, int k_splits);
+cudaError_t launch_matmul_mma(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds, int64_t M,
+                              float* y, int64_t ldy, void* encode, int* err, int num_sms, cudaStream_t stream);
 cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,
                              const void* ds, const void* tc_operand, int64_t M, float* y,
                              int64_t ldy, void* encode, int* err, int num_sms, int skip_w_stage,

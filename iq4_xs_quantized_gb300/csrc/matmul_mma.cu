@@ -1,0 +1,606 @@
+// matmul_mma.cu -- IQ4_XS x Q8_1 matmul for small and medium batches on the
+// warp-level tensor-core MMA (mma.sync m16n8k16, fp16 operands, fp32
+// accumulators held in registers).
+//
+// Method (V100TPS engine page, new-kernel table and the tile-geometry
+// passage after it): per 32-weight sub-block an integer dot product of the
+// decoded codebook values with the Q8_1 codes, scaled by d_w*(ls-32)*d_x into
+// fp32.  As on the tcgen05 path both operands are small integers held
+// exactly in fp16 (codebook values |kv| <= 127, codes |q| <= 127), so a
+// sub-block's two k16 MMAs leave its exact integer dot P in the fp32
+// accumulator (every product and partial sum is an integer below 2^24).
+//
+// Why a warp-level MMA in the memory-bound range.  For M <= 32 the weight
+// bytes bound the call; what limits a kernel is how many instructions and
+// shared-memory wavefronts it spends per weight.  Here the decoded weights go
+// from the byte-table lookup straight into the A fragment registers and every
+// sub-block's accumulator comes back in registers for its scale-in, so no
+// weight tile is stored anywhere, no accumulator is read back from tensor
+// memory and no hand-off between warp roles is needed per sub-block.
+//
+// Tiles.  A CTA owns R weight rows (R a multiple of 16 up to 256, chosen per
+// call so that the row tiles times the K split fill the SMs) and an
+// activation tile of 8*NT rows (MMA N = 8 per fragment, NT fragments).
+// Weights are the A operand (MMA M = 16 rows per fragment).  A stage is 512
+// weights of every row (two super-blocks, one R x 272 B TMA box) plus the
+// matching Q8_1 codes; the 8 consumer warps split it as kRG row groups x
+// kSG sub-block groups: warp (rg, sg) takes fragments rg, rg + kRG, ...
+// (at most kTMax) and kSPW consecutive sub-blocks of one super-block.  K is
+// split over a thread-block cluster of S CTAs whose partial tiles are summed
+// in rank order through distributed shared memory.
+//
+// K order inside a sub-block.  MMA k pair p of k16 step s (k = 2p, 2p+1)
+// holds qs byte b = 4*(p % 4) + 2*s + (p / 4), i.e. sub-block elements b
+// (low nibble) and 16 + b (high nibble).  Lane (g, t) of the warp (g = lane /
+// 4, t = lane % 4) then needs bytes 4t..4t+3 of its two weight rows g and
+// g+8 -- one 32-bit word each -- and Q8_1 codes 4t..4t+3 and 16+4t..16+4t+3
+// of activation row g, two words.  One shared-memory lookup per qs byte
+// returns the fp16x2 (kv[low nibble], kv[high nibble]) that is exactly one A
+// register.
+//
+// Roles: warps 0-7 consume stages; warp 8 lane 0 is the TMA producer (W
+// boxes before the wait for the preceding grid, Q8_1 code boxes after it).
+// Each consumer warp first turns the stage's block headers into its row
+// scales d_w*(ls-32) and the activation scales d_x into fp32, in tables of
+// its own kept in the unused half of every 256-byte row of the byte table.
+// Every mbarrier wait is bounded; a wait that runs out records its code in
+// the device error word, raises the CTA's abort flag, and the CTA drains its
+// copies and leaves y unwritten.
+#include <cuda.h>
+
+#include <atomic>
+
+#include "internal.cuh"
+
+namespace iq4xs {
+namespace {
+
+constexpr int kMmaConsumers = 8;              // consumer warps
+constexpr int kMmaProducerWarp = kMmaConsumers;
+constexpr int kMmaThreads = 32 * (kMmaConsumers + 1);
+constexpr int kMmaMaxCluster = 8;
+constexpr int kMmaMaxRows = 256;              // TMA box height
+constexpr int kMmaMaxStages = 4;
+constexpr int kWideLutBytes = 256 * 256;      // byte table: entry j at 256 j, copy l at 4 l (bytes 0..127)
+constexpr int kGapBytes = kWideLutBytes / 2;  // bytes 128..255 of every table row
+constexpr int kQBoxK = 128;                   // Q8_1 codes per box row (one 128-byte swizzle row)
+constexpr int kQBoxesPerStage = kPairK / kQBoxK;  // 4
+constexpr int kMmaSmemLimit = 227 * 1024;
+constexpr int kOffRingMma = kWideLutBytes;
+constexpr int kMmaBarBytes = 128;             // full[4], empty[4], abort flag
+constexpr int kMmaRingBytes = kMmaSmemLimit - kOffRingMma - kMmaBarBytes;
+__device__ volatile int g_never_abort_mma = 0;  // an abort flag that is never set
+
+// Physical address (bytes from the table start) of byte o of the gap space.
+__host__ __device__ constexpr uint32_t gap_addr(uint32_t o) { return ((o >> 7) << 8) + 128u + (o & 127u); }
+
+// NT: 8-row activation fragments per tile; T: 16-row weight fragments per
+// consumer warp.  The 8 consumer warps are 2 row groups x 4 sub-block
+// groups, so a CTA owns R = 32 T weight rows and a warp takes fragments
+// rg, rg + 2, ..., rg + 2 (T - 1) and 4 consecutive sub-blocks of a stage.
+template <int NT, int T>
+struct MmaCfg {
+    static_assert(NT >= 1 && NT <= 4, "1..4 fragments of 8 activation rows");
+    static_assert(T >= 1 && T * NT <= 16, "accumulators: T x NT x 4 registers per lane");
+    static constexpr int kMt = 8 * NT;                    // activation rows per tile
+    static constexpr int kRG = 2;                         // row groups
+    static constexpr int kSG = kMmaConsumers / kRG;       // sub-block groups
+    static constexpr int kSPW = kSubPerPair / kSG;        // sub-blocks per warp and stage (4)
+    static constexpr int kR = 16 * kRG * T;               // weight rows per CTA
+    static_assert(kR <= kMmaMaxRows, "TMA box height");
+    static_assert(kSubPerBlock % kSPW == 0, "a warp's sub-blocks lie in one super-block");
+    static constexpr int kQBox = kMt * kQBoxK;            // one code box (a multiple of 1024 B)
+    static constexpr int kQStage = kQBoxesPerStage * kQBox;
+    static constexpr int kWBytes = (kR * kPairBytes + 1023) / 1024 * 1024;
+    static constexpr int kStage = kWBytes + kQStage;
+    static constexpr int kNS = kMmaRingBytes / kStage < kMmaMaxStages ? kMmaRingBytes / kStage : kMmaMaxStages;
+    static_assert(kNS >= 2, "two stages in flight");
+    static constexpr int kSmem = kOffRingMma + kNS * kStage + kMmaBarBytes;
+    // Per-warp tables (gap space): row scales [k][s][g][h] (rows
+    // 16 f + g + 8 h of fragment f = rg + 2 k), then d_x [s][m].
+    static constexpr int kSwFloats = kSPW * T * 16;
+    static constexpr int kDxFloats = kSPW * kMt;
+    static constexpr int kWarpTab = ((kSwFloats + kDxFloats) * 4 + 127) / 128 * 128;
+    static_assert(kMmaConsumers * kWarpTab <= kGapBytes, "tables fit the byte table's gaps");
+    static constexpr int kXItems = (kDxFloats + 31) / 32;  // d_x loads per lane and stage
+    static constexpr int kCombos = T * 8;                  // (fragment, g) pairs of a warp
+    static constexpr int kRedStride = kMt + 4;             // fp32 per row of a partial tile
+    static_assert(kSG * kR * kRedStride * 4 <= kNS * kStage, "partials fit the ring");
+    static_assert(kR * kRedStride * 4 <= kWideLutBytes, "CTA tile fits the byte table");
+};
+
+__device__ __forceinline__ void mma_f16_16816(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1,
+                                              const float c[4]) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%10, %11, %12, %13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+          "f"(c[3]));
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
+    uint32_t a;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local_addr), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kMmaConsumers) : "memory");
+}
+
+template <int NT, int T>
+__global__ void __launch_bounds__(kMmaThreads, 1)
+    matmul_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_q,
+                      const __half* __restrict__ ds, int64_t M, int N, int K, float* __restrict__ y, int64_t ldy,
+                      int* err) {
+    using C = MmaCfg<NT, T>;
+    constexpr int kTMax = T, kMt = C::kMt, kSPW = C::kSPW, kRG = C::kRG, R = C::kR, NS = C::kNS;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {  // the 128-byte-swizzled code boxes need 1024-byte alignment
+        if (threadIdx.x == 0) atomicExch(err, kDevErrLayout);
+        return;
+    }
+    constexpr int stage_b = C::kStage, wbytes = C::kWBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffRingMma + NS * stage_b);
+    uint64_t* empty = full + kMmaMaxStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kMmaMaxStages);
+    const uint32_t sbase = smem_u32(smem);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = gridDim.y;
+    const uint32_t rank = (S > 1) ? cluster_ctarank() : 0;
+    const int n0 = blockIdx.x * R;
+    const int z = blockIdx.z;
+    const int pairs = (K + kPairK - 1) / kPairK;
+    const int p0 = (int)((int64_t)pairs * rank / S);
+    const int p1 = (int)((int64_t)pairs * (rank + 1) / S);
+    const int nst = p1 - p0;
+
+    if (warp == kMmaProducerWarp && lane == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kMmaConsumers);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    // Byte table: row j = 32 copies (one per bank) of the fp16x2 word
+    // (kv[j & 15], kv[j >> 4]) in its first 128 bytes.
+    for (int i = threadIdx.x; i < 256 * 8; i += kMmaThreads) {
+        const uint32_t e = f16x2_byte_entry<kWtIQ4XS>(i >> 3);
+        *reinterpret_cast<uint4*>(smem + (i >> 3) * 256 + (i & 7) * 16) = make_uint4(e, e, e, e);
+    }
+    __syncthreads();
+    griddep_launch_dependents();
+
+    bool ok = true;
+    if (warp == kMmaProducerWarp) {
+        if (lane == 0) {
+            prefetch_tmap(&tmap_w);
+            prefetch_tmap(&tmap_q);
+            auto load_w = [&](int ps) {
+                const int slot = ps % NS;
+                mbar_arrive_expect_tx(&full[slot], (uint32_t)(R * kPairBytes + C::kQStage));
+                tma_load_2d(smem + kOffRingMma + slot * stage_b, &tmap_w, (p0 + ps) * (kPairBytes / 4), n0,
+                            &full[slot]);
+            };
+            auto load_q = [&](int ps) {
+                const int slot = ps % NS;
+#pragma unroll
+                for (int b = 0; b < kQBoxesPerStage; ++b)
+                    tma_load_2d(smem + kOffRingMma + slot * stage_b + wbytes + b * C::kQBox, &tmap_q,
+                                (p0 + ps) * kPairK + b * kQBoxK, z * kMt, &full[slot]);
+            };
+            // W (model state) streams before the preceding grid, which
+            // writes the codes, has finished.
+            const int pre = nst < NS ? nst : NS;
+            for (int ps = 0; ps < pre; ++ps) load_w(ps);
+            griddep_wait();
+            for (int ps = 0; ps < pre; ++ps) load_q(ps);
+            int issued = pre;
+            for (int ps = NS; ps < nst && ok; ++ps) {
+                const int slot = ps % NS;
+                ok = mbar_wait(&empty[slot], ((ps / NS) - 1) & 1, abort_flag, err, kDevErrTimeoutMmaSlot);
+                if (!ok) break;
+                load_w(ps);
+                load_q(ps);
+                ++issued;
+            }
+            // Drain: the last stage issued into each slot has landed (the
+            // earlier ones were consumed before their slot was reused).  Not
+            // stopped by an abort: no copy may land after the CTA exits.
+            for (int ps = (issued > NS ? issued - NS : 0); ps < issued; ++ps)
+                mbar_wait(&full[ps % NS], (ps / NS) & 1, &g_never_abort_mma, err, kDevErrTimeoutDrain);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- consumers
+        const int g = lane >> 2, t = lane & 3;
+        const int rg = warp / C::kSG, sg = warp % C::kSG;
+        const int sub_w = sg * kSPW;             // first sub-block of the stage this warp takes
+        const int super_w = sub_w / kSubPerBlock;
+        const int jj0 = sub_w % kSubPerBlock;
+        const uint32_t lane4 = (uint32_t)lane * 4u;
+        const uint32_t tab = (uint32_t)(warp * C::kWarpTab);   // this warp's tables, gap space
+        const uint32_t* ds32 = reinterpret_cast<const uint32_t*>(ds);
+        const int64_t K32 = (K + kSub - 1) / kSub;
+        float acc[kTMax][NT][4];
+#pragma unroll
+        for (int i = 0; i < kTMax; ++i)
+#pragma unroll
+            for (int f = 0; f < NT; ++f)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[i][f][e] = 0.f;
+
+        // Activation scales of stage ps for this warp's sub-blocks: item e =
+        // (row m = e / kSPW, sub-block e % kSPW), fp16 d in ds.
+        uint32_t dxv[C::kXItems];
+        auto load_dx = [&](int ps) {
+#pragma unroll
+            for (int k = 0; k < C::kXItems; ++k) {
+                const int e = lane + 32 * k;
+                const int64_t m = (int64_t)z * kMt + e / kSPW;
+                const int64_t sub = (int64_t)(p0 + ps) * kSubPerPair + sub_w + e % kSPW;
+                dxv[k] = (e < C::kDxFloats && m < M && sub < K32) ? __ldg(ds32 + m * K32 + sub) : 0u;
+            }
+        };
+        griddep_wait();  // ds comes from the preceding grid
+        if (nst > 0) load_dx(0);
+        // Row-scale work of this lane: (fragment slot k, g) pairs c = lane +
+        // 32 i, rows 16 f + g and 16 f + g + 8, all kSPW sub-blocks.
+        const int wrow_lane = 16 * rg + g;       // row of fragment slot 0 for this lane (+ 16 kRG k)
+
+        for (int ps = 0; ps < nst && ok; ++ps) {
+            const int slot = ps % NS;
+            ok = mbar_wait(&full[slot], (ps / NS) & 1, abort_flag, err, kDevErrTimeoutMmaStage);
+            if (!ok) break;
+            // Plain loads from here on: ordered after the barrier wait (an
+            // asm statement with a memory clobber) and free to be scheduled
+            // among themselves.
+            const uint8_t* wst = smem + kOffRingMma + slot * stage_b;
+            const uint8_t* qst = wst + wbytes;
+            // ---- per-stage tables: row scales and activation scales
+#pragma unroll
+            for (int c = lane; c < C::kCombos; c += 32) {
+                const int k = c >> 3, gg = c & 7;
+                const int f = rg + kRG * k;
+                {
+                    const int r = 16 * f + gg;
+                    const uint2 h0 = *reinterpret_cast<const uint2*>(wst + r * kPairBytes + super_w * kBlockBytes);
+                    const uint2 h1 =
+                        *reinterpret_cast<const uint2*>(wst + (r + 8) * kPairBytes + super_w * kBlockBytes);
+#pragma unroll
+                    for (int s2 = 0; s2 < kSPW; ++s2) {
+                        const float2 v = make_float2(iq4xs_scale(h0.x, h0.y, jj0 + s2), iq4xs_scale(h1.x, h1.y, jj0 + s2));
+                        *reinterpret_cast<float2*>(smem + gap_addr(tab + (uint32_t)((((k * kSPW + s2) * 8 + gg) * 2) * 4))) = v;
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < C::kXItems; ++k) {
+                const int e = lane + 32 * k;
+                if (e < C::kDxFloats)
+                    *reinterpret_cast<float*>(smem + gap_addr(tab + (uint32_t)((C::kSwFloats + (e % kSPW) * kMt + e / kSPW) * 4))) =
+                        __half2float(__ushort_as_half((unsigned short)(dxv[k] & 0xFFFFu)));
+            }
+            __syncwarp();
+            if (ps + 1 < nst) load_dx(ps + 1);  // in flight during this stage
+#pragma unroll 1
+            for (int s = 0; s < kSPW; ++s) {
+                const int j = sub_w + s;                 // sub-block within the stage
+                const int jj = j % kSubPerBlock;
+                const int box = j / 4, jq = j % 4;
+                // B fragments: activation row 8 f + g, Q8_1 codes 4t..4t+3 and
+                // 16+4t..16+4t+3 of the sub-block (128-byte swizzle: 16-byte
+                // chunk c of box row r sits at chunk c ^ (r % 8)).
+                uint32_t bfr[NT][4];
+                float2 dx[NT];
+#pragma unroll
+                for (int f = 0; f < NT; ++f) {
+                    const uint8_t* rowa = qst + box * C::kQBox + (8 * f + g) * kQBoxK + 4 * t;
+                    const uint32_t lo4 = *reinterpret_cast<const uint32_t*>(rowa + (((2 * jq) ^ g) << 4));
+                    const uint32_t hi4 = *reinterpret_cast<const uint32_t*>(rowa + (((2 * jq + 1) ^ g) << 4));
+                    const uint4 v = q8x8_to_f16(lo4, hi4);
+                    bfr[f][0] = v.x; bfr[f][1] = v.y; bfr[f][2] = v.z; bfr[f][3] = v.w;
+                    dx[f] = *reinterpret_cast<const float2*>(
+                        smem + gap_addr(tab + (uint32_t)((C::kSwFloats + s * kMt + 8 * f + 2 * t) * 4)));
+                }
+                // row scales of sub-block s: block (k, s) of 64 bytes at gap
+                // offset 64 (k kSPW + s), the lane's pair (rows g, g+8) at +8 g;
+                // kSPW = 4 blocks are two whole 128-byte gap chunks, so block
+                // (k, s) sits 512 k physical bytes after block (0, s).
+                static_assert(kSPW == 4, "two gap chunks per fragment slot");
+                const uint8_t* swp = smem + gap_addr(tab + (uint32_t)(64 * s)) + 8 * g;
+                const uint8_t* wl = wst + wrow_lane * kPairBytes + super_w * kBlockBytes + 8 + 16 * jj + 4 * t;
+#pragma unroll
+                for (int k = 0; k < kTMax; ++k) {
+                    {
+                        const uint8_t* wk = wl + 16 * kRG * k * kPairBytes;
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(wk);
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(wk + 8 * kPairBytes);
+                        // A fragments of k16 steps 0 and 1: bytes (0, 1) and
+                        // (2, 3) of the two rows' words; table byte offset =
+                        // (byte << 8) | 4 lane.
+                        uint32_t a0[4], a1[4];
+                        a0[0] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w0, lane4, 0x5504u));
+                        a0[1] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w1, lane4, 0x5504u));
+                        a0[2] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w0, lane4, 0x5514u));
+                        a0[3] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w1, lane4, 0x5514u));
+                        a1[0] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w0, lane4, 0x5524u));
+                        a1[1] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w1, lane4, 0x5524u));
+                        a1[2] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w0, lane4, 0x5534u));
+                        a1[3] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w1, lane4, 0x5534u));
+                        const float2 sw = *reinterpret_cast<const float2*>(swp + 512 * k);
+                        const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int f = 0; f < NT; ++f) {
+                            float p[4];
+                            mma_f16_16816(p, a0, bfr[f][0], bfr[f][1], zero);
+                            mma_f16_16816(p, a1, bfr[f][2], bfr[f][3], p);
+                            // acc += (P * d_x) * d_w*(ls-32): rows g (p0, p1) and g+8 (p2, p3)
+                            const float2 q01 = __fmul2_rn(make_float2(p[0], p[1]), dx[f]);
+                            const float2 q23 = __fmul2_rn(make_float2(p[2], p[3]), dx[f]);
+                            const float2 r01 =
+                                __ffma2_rn(q01, make_float2(sw.x, sw.x), make_float2(acc[k][f][0], acc[k][f][1]));
+                            const float2 r23 =
+                                __ffma2_rn(q23, make_float2(sw.y, sw.y), make_float2(acc[k][f][2], acc[k][f][3]));
+                            acc[k][f][0] = r01.x; acc[k][f][1] = r01.y;
+                            acc[k][f][2] = r23.x; acc[k][f][3] = r23.y;
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+        if (!ok) {
+            // Wake the producer if it waits on a slot this warp will never free.
+            if (lane == 0) *abort_flag = 1;
+        }
+        // ---- end of the K range: partial tiles of the sub-block groups
+        consumers_sync();  // every consumer is done with the ring
+        if (!*abort_flag) {
+            float* red = reinterpret_cast<float*>(smem + kOffRingMma) + sg * R * C::kRedStride;
+#pragma unroll
+            for (int k = 0; k < kTMax; ++k) {
+                {
+#pragma unroll
+                    for (int f = 0; f < NT; ++f) {
+                        const int r = 16 * (rg + kRG * k) + g, c = 8 * f + 2 * t;
+                        *reinterpret_cast<float2*>(red + r * C::kRedStride + c) =
+                            make_float2(acc[k][f][0], acc[k][f][1]);
+                        *reinterpret_cast<float2*>(red + (r + 8) * C::kRedStride + c) =
+                            make_float2(acc[k][f][2], acc[k][f][3]);
+                    }
+                }
+            }
+        }
+        consumers_sync();
+        if (!*abort_flag) {
+            const float* red = reinterpret_cast<const float*>(smem + kOffRingMma);
+            float* tile = reinterpret_cast<float*>(smem);
+            const int64_t mrows = M - (int64_t)z * kMt;
+            for (int e = threadIdx.x; e < R * kMt; e += 32 * kMmaConsumers) {
+                const int r = e % R, m = e / R;
+                float v = red[r * C::kRedStride + m];
+#pragma unroll
+                for (int q = 1; q < C::kSG; ++q) v += red[(q * R + r) * C::kRedStride + m];
+                if (S == 1) {
+                    if (m < mrows && n0 + r < N) y[((int64_t)z * kMt + m) * ldy + n0 + r] = v;
+                } else {
+                    tile[r * C::kRedStride + m] = v;
+                }
+            }
+        }
+    }
+
+    if (S > 1) {
+        // Split-K: rank r sums rows [R r / S, R (r + 1) / S) of every rank's
+        // tile in rank order (deterministic).  Every thread of every CTA
+        // passes both cluster barriers, aborted or not; after an abort the
+        // output is undefined and the tiles are not summed.
+        __syncwarp();
+        cluster_arrive_release();
+        cluster_wait();
+        if (warp < kMmaConsumers && !*abort_flag) {
+            const int r0 = R * (int)rank / S, r1 = R * ((int)rank + 1) / S;
+            const int64_t mrows = M - (int64_t)z * kMt;
+            for (int e = threadIdx.x; e < (r1 - r0) * kMt; e += 32 * kMmaConsumers) {
+                const int r = r0 + e % (r1 - r0), m = e / (r1 - r0);
+                const uint32_t off = sbase + (uint32_t)((r * C::kRedStride + m) * 4);
+                float v = 0.f;
+                for (int q = 0; q < S; ++q) v += ld_cluster_f32(off, (uint32_t)q);
+                if (m < mrows && n0 + r < N) y[((int64_t)z * kMt + m) * ldy + n0 + r] = v;
+            }
+        }
+        __syncwarp();
+        cluster_arrive_release();
+        cluster_wait();  // no rank exits while another reads its tile
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Cached per device: clusters of S (1..8) the device runs at once for the
+// kernel <NT, T> (cudaOccupancyMaxActiveClusters, queried once).
+template <int NT, int T>
+int mma_max_clusters(int dev, int s, int num_sms) {
+    using C = MmaCfg<NT, T>;
+    static int cache[64][kMmaMaxCluster + 1] = {};
+    int mc = (dev >= 0 && dev < 64) ? cache[dev][s] : 0;
+    if (mc > 0) return mc;
+    static bool attr_done[64] = {};
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        if (cudaFuncSetAttribute(matmul_mma_kernel<NT, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
+            cudaSuccess)
+            cudaGetLastError();
+        attr_done[dev] = true;
+    }
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(1, (unsigned)s, 1);
+    q.blockDim = dim3(kMmaThreads);
+    q.dynamicSmemBytes = C::kSmem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = (unsigned)s;
+    at[0].val.clusterDim.z = 1;
+    q.attrs = at;
+    q.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, matmul_mma_kernel<NT, T>, &q) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = num_sms / s;
+    }
+    mc = n > 0 ? n : 1;
+    if (dev >= 0 && dev < 64) cache[dev][s] = mc;
+    return mc;
+}
+
+template <int NT, int T>
+cudaError_t launch_nt(const void* w, int64_t row_bytes, EncodeTiledFn enc, const CUtensorMap& tq, const __half* ds,
+                      int64_t M, int N, int K, int S, float* y, int64_t ldy, int* err, cudaStream_t stream) {
+    using C = MmaCfg<NT, T>;
+    // W: one box = R rows x one super-block pair (272 B; K % 512 == 0, so
+    // rows are 16-byte strided); rows past N read as zeros (d = 0).
+    CUtensorMap tw;
+    {
+        const cuuint64_t gdim[2] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)N};
+        const cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
+        const cuuint32_t box[2] = {(cuuint32_t)(kPairBytes / 4), (cuuint32_t)C::kR};
+        const cuuint32_t estride[2] = {1, 1};
+        if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(w), gdim, gstride, box, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const int ntiles = (N + C::kR - 1) / C::kR;
+    const int mtiles = (int)((M + C::kMt - 1) / C::kMt);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ntiles, (unsigned)S, (unsigned)mtiles);
+    cfg.blockDim = dim3(kMmaThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)S;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, matmul_mma_kernel<NT, T>, tw, tq, ds, M, N, K, y, ldy, err);
+}
+
+// Fragments per warp T (R = 32 T rows per CTA) and K split S (= cluster
+// size) with the least modelled time  waves x (F + R / 128 x ceil(pairs /
+// S))  in units of one 128-row stage's streaming time, over T = 1..kTMax and
+// S = 1..8 (at most the K pairs); waves from the clusters of S the device
+// runs at once.  F, a CTA's fixed cost (launch, first stage, reduction), is
+// about two stages.  Ties keep the larger R and the smaller S.
+// Test override of the launch configuration (0 = the model's choice).
+std::atomic<int> g_force_t{0}, g_force_s{0};
+
+template <int NT, int kTMax>
+cudaError_t launch_best(const void* w, int64_t row_bytes, EncodeTiledFn enc, const CUtensorMap& tq,
+                        const __half* ds, int64_t M, int N, int K, float* y, int64_t ldy, int* err, int num_sms,
+                        cudaStream_t stream) {
+    constexpr double kFixed = 2.0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int mtiles = (int)((M + 8 * NT - 1) / (8 * NT));
+    const int pairs = (K + kPairK - 1) / kPairK;
+    int best_t = kTMax, best_s = 1;
+    double best = 1e30;
+    for (int tt = kTMax; tt >= 1; --tt) {
+        const int R = 32 * tt;
+        const int units = (N + R - 1) / R * mtiles;
+        for (int s = 1; s <= kMmaMaxCluster && s <= pairs; ++s) {
+            int mc = 0;
+            switch (tt) {
+                case 1: mc = mma_max_clusters<NT, 1>(dev, s, num_sms); break;
+                case 2: mc = mma_max_clusters<NT, 2>(dev, s, num_sms); break;
+                case 3: mc = mma_max_clusters<NT, 3>(dev, s, num_sms); break;
+                case 4: mc = mma_max_clusters<NT, 4>(dev, s, num_sms); break;
+                case 5: mc = mma_max_clusters<NT, (kTMax >= 5 ? 5 : 1)>(dev, s, num_sms); break;
+                case 6: mc = mma_max_clusters<NT, (kTMax >= 6 ? 6 : 1)>(dev, s, num_sms); break;
+                case 7: mc = mma_max_clusters<NT, (kTMax >= 7 ? 7 : 1)>(dev, s, num_sms); break;
+                default: mc = mma_max_clusters<NT, (kTMax >= 8 ? 8 : 1)>(dev, s, num_sms); break;
+            }
+            const int waves = (units * s + mc * s - 1) / (mc * s);
+            const double tm = waves * (kFixed + (double)R / 128.0 * (double)((pairs + s - 1) / s));
+            if (tm < best * 0.999) {
+                best = tm;
+                best_t = tt;
+                best_s = s;
+            }
+        }
+    }
+    {
+        const int ft = g_force_t.load(), fs = g_force_s.load();
+        if (ft > 0) best_t = ft < kTMax ? ft : kTMax;
+        if (fs > 0) best_s = fs < pairs ? fs : pairs;
+    }
+#define IQ4XS_MMA_T(tv)                                                                                        \
+    case tv:                                                                                                   \
+        return launch_nt<NT, (kTMax >= tv ? tv : 1)>(w, row_bytes, enc, tq, ds, M, N, K, best_s, y, ldy, err, \
+                                                     stream);
+    switch (best_t) {
+        IQ4XS_MMA_T(1)
+        IQ4XS_MMA_T(2)
+        IQ4XS_MMA_T(3)
+        IQ4XS_MMA_T(4)
+        IQ4XS_MMA_T(5)
+        IQ4XS_MMA_T(6)
+        IQ4XS_MMA_T(7)
+        IQ4XS_MMA_T(8)
+        default: return cudaErrorInvalidValue;
+    }
+#undef IQ4XS_MMA_T
+}
+
+}  // namespace
+
+void mma_force_config(int frags_per_warp, int k_splits) {
+    g_force_t.store(frags_per_warp);
+    g_force_s.store(k_splits);
+}
+
+int mma_tile_rows(int64_t M) {
+    const int64_t nt = (M + 7) / 8;
+    return 8 * (int)(nt < 4 ? nt : 4);
+}
+
+cudaError_t launch_matmul_mma(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds, int64_t M,
+                              float* y, int64_t ldy, void* encode, int* err, int num_sms, cudaStream_t stream) {
+    const EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(encode);
+    const int64_t row_bytes = wt_row_bytes(kWtIQ4XS, K);
+    const int mt = mma_tile_rows(M);
+    CUtensorMap tq;
+    {
+        // Q8_1 codes: one box = mt rows x 128 codes, 128-byte swizzle; rows
+        // past M read as zeros.
+        const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
+        const cuuint64_t gstride[1] = {(cuuint64_t)K};
+        const cuuint32_t box[2] = {(cuuint32_t)kQBoxK, (cuuint32_t)mt};
+        const cuuint32_t estride[2] = {1, 1};
+        if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qs), gdim, gstride, box, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const __half* dsh = reinterpret_cast<const __half*>(ds);
+    const int Ni = (int)N, Ki = (int)K;
+    switch (mt) {
+        case 8: return launch_best<1, 8>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
+        case 16: return launch_best<2, 8>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
+        case 24: return launch_best<3, 4>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
+        default: return launch_best<4, 4>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
+    }
+}
+
+}  // namespace iq4xs

@@ -62,29 +62,61 @@ def test_library_exports_every_declared_symbol(lib):
         assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
 
 
+def _dispatch(dp4a, mma, baseline=0):
+    B.iq4xs_set_crossover_classes([])
+    B.iq4xs_set_mma_crossover_classes([])
+    B.iq4xs_set_crossover(dp4a)
+    B.iq4xs_set_mma_crossover(mma)
+    B.iq4xs_set_baseline_threshold(baseline)
+
+
 def test_select_path_and_crossover(lib):
-    B.iq4xs_set_crossover(4)
-    B.iq4xs_set_baseline_threshold(0)  # the dp4a/tcgen05 choice alone
-    assert B.iq4xs_select_path(1, 4096, 4096) == B.PATH_DP4A
-    assert B.iq4xs_select_path(4, 4096, 4096) == B.PATH_DP4A
-    assert B.iq4xs_select_path(5, 4096, 4096) == B.PATH_TC
-    assert B.iq4xs_select_path(96, 4096, 4096) == B.PATH_TC
-    # K % 512 != 0 cannot take the tensor-core path
-    assert B.iq4xs_select_path(96, 4096, 256 * 3) == B.PATH_DP4A
-    B.iq4xs_set_crossover(0)
-    assert B.iq4xs_select_path(1, 4096, 4096) == B.PATH_TC
-    B.iq4xs_set_crossover(4)
-    out = ctypes.c_int()
-    assert lib.iq4xs_select_path(0, 1, 256, ctypes.byref(out)) == B.ERR_SHAPE
-    assert lib.iq4xs_select_path(1, 1, 100, ctypes.byref(out)) == B.ERR_SHAPE
-    assert lib.iq4xs_select_path(1, 1, 256, None) == B.ERR_ARG
-    assert lib.iq4xs_set_crossover(-1) == B.ERR_ARG
-    B._install_calibration(lib)
+    try:
+        _dispatch(4, 8)  # DP4A to M = 4, MMA to M = 8, TC above
+        sel = B.iq4xs_select_path
+        assert [sel(m, 4096, 4096) for m in (1, 4, 5, 8, 9, 96)] == [
+            B.PATH_DP4A, B.PATH_DP4A, B.PATH_MMA, B.PATH_MMA, B.PATH_TC, B.PATH_TC]
+        # K % 512 != 0: neither tensor-core path (W rows not 16-byte strided)
+        assert sel(2, 4096, 256 * 3) == B.PATH_DP4A
+        assert sel(96, 4096, 256 * 3) == B.PATH_DP4A
+        B.iq4xs_set_mma_crossover(0)  # no MMA range
+        assert sel(5, 4096, 4096) == B.PATH_TC
+        B.iq4xs_set_crossover(0)
+        assert sel(1, 4096, 4096) == B.PATH_TC
+        # per weight-size class: the largest class at or below N*K applies
+        _dispatch(4, 8)
+        B.iq4xs_set_mma_crossover_classes([(20_000_000, 16), (100_000_000, 4)])
+        B.iq4xs_set_crossover_classes([(20_000_000, 2)])
+        assert sel(12, 12288, 5120) == B.PATH_MMA   # 63M weights: MMA to 16
+        assert sel(3, 12288, 5120) == B.PATH_MMA    # dp4a only to 2 there
+        assert sel(12, 4096, 4096) == B.PATH_TC     # 16.8M: the defaults
+        assert sel(3, 4096, 4096) == B.PATH_DP4A
+        assert sel(8, 34816, 5120) == B.PATH_TC     # 178M: MMA only to 4
+        out = ctypes.c_int()
+        assert lib.iq4xs_select_path(0, 1, 256, ctypes.byref(out)) == B.ERR_SHAPE
+        assert lib.iq4xs_select_path(1, 1, 100, ctypes.byref(out)) == B.ERR_SHAPE
+        assert lib.iq4xs_select_path(1, 1, 256, None) == B.ERR_ARG
+        assert lib.iq4xs_set_crossover(-1) == B.ERR_ARG
+        assert lib.iq4xs_set_mma_crossover(-1) == B.ERR_ARG
+        assert lib.iq4xs_set_mma_crossover(40000) == B.ERR_ARG
+        bad = (ctypes.c_int64 * 1)(0)
+        ok = (ctypes.c_int64 * 1)(4)
+        assert lib.iq4xs_set_mma_crossover_classes(bad, ok, 1) == B.ERR_ARG
+        assert lib.iq4xs_set_mma_crossover_classes(ok, ok, 17) == B.ERR_ARG
+    finally:
+        B.reset_dispatch()
+
+
+def test_mma_config_hook_validation(lib):
+    assert lib.iq4xs_test_mma_config(0, 0) == B.OK
+    for rows, splits in ((16, 1), (288, 1), (-32, 1), (64, 9), (64, -1)):
+        assert lib.iq4xs_test_mma_config(rows, splits) == B.ERR_ARG
+    assert lib.iq4xs_test_mma_config(256, 8) == B.OK
+    assert lib.iq4xs_test_mma_config(0, 0) == B.OK
 
 
 def test_baseline_threshold_is_advice_above_the_tc_range(lib):
-    B.iq4xs_set_crossover(4)
-    B.iq4xs_set_baseline_threshold(0)  # never
+    _dispatch(4, 0)  # no MMA range; baseline never
     assert B.iq4xs_select_path(512, 5120, 17408) == B.PATH_TC
     B.iq4xs_set_baseline_threshold(128)
     assert B.iq4xs_select_path(96, 5120, 17408) == B.PATH_TC
@@ -94,7 +126,7 @@ def test_baseline_threshold_is_advice_above_the_tc_range(lib):
     B.iq4xs_set_baseline_threshold(1)
     assert B.iq4xs_select_path(2, 4096, 4096) == B.PATH_DP4A
     assert B.iq4xs_select_path(8, 4096, 4096) == B.PATH_BASELINE
-    # shapes the tensor-core path cannot take keep dp4a
+    # shapes the tensor-core paths cannot take keep dp4a
     assert B.iq4xs_select_path(256, 4096, 256 * 3) == B.PATH_DP4A
     assert lib.iq4xs_set_baseline_threshold(-1) == B.ERR_ARG
     # the library's own calls never take the advice as an explicit path
@@ -102,7 +134,7 @@ def test_baseline_threshold_is_advice_above_the_tc_range(lib):
     rc = lib.iq4xs_matmul(ctypes.c_void_p(16), 256, 512, ctypes.c_void_p(16), ctypes.c_void_p(16),
                           8, ctypes.c_void_p(16), 256, B.PATH_BASELINE, 0)
     assert rc == B.ERR_ARG, rc
-    B._install_calibration(lib)
+    B.reset_dispatch()
 
 
 def test_tc_operand_bytes(lib):
@@ -192,7 +224,7 @@ def test_status_strings(lib):
 
 
 def test_linear_workspace_and_validation(lib):
-    B.iq4xs_set_crossover(4)
+    _dispatch(4, 8)
     # the least: qs, then ds 16-byte aligned (1.125 bytes per activation);
     # the fastest form adds the prepared operand on the tensor-core path
     assert B.iq4xs_linear_workspace_bytes(2, 4096, 4096) == 2 * 4096 + 2 * 128 * 4
@@ -208,6 +240,7 @@ def test_linear_workspace_and_validation(lib):
     assert lib.iq4xs_linear(p, 4096, 4096, p, 96, 4096, p, 4096, p, least - 1, 0) == B.ERR_ARG
     assert lib.iq4xs_linear(p, 4096, 4096, p, 96, 4096, p, 4096, None, need, 0) == B.ERR_ARG
     assert lib.iq4xs_linear(p, 4096, 300, p, 96, 4096, p, 4096, p, need, 0) == B.ERR_SHAPE
+    B.reset_dispatch()
 
 
 def test_grouped_argument_errors_return_before_any_launch(lib):
@@ -227,8 +260,7 @@ def test_grouped_argument_errors_return_before_any_launch(lib):
 
 
 def test_crossover_classes(lib):
-    B.iq4xs_set_crossover(4)
-    B.iq4xs_set_baseline_threshold(0)
+    _dispatch(4, 0)  # the DP4A / TC choice alone
     try:
         B.iq4xs_set_crossover_classes([(50_000_000, 2), (150_000_000, 6)])
         assert B.iq4xs_select_path(4, 4096, 4096) == B.PATH_DP4A      # below every class: 4
@@ -245,4 +277,4 @@ def test_crossover_classes(lib):
         B.iq4xs_set_crossover_classes([])
         assert B.iq4xs_select_path(4, 12288, 5120) == B.PATH_DP4A
     finally:
-        B._install_calibration(lib)
+        B.reset_dispatch()

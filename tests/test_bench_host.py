@@ -81,33 +81,33 @@ def test_traffic_record_is_ignored_when_kernels_change(tmp_path, monkeypatch):
     assert bench.recorded_traffic() == 123.0
 
 
-def test_crossover_rule_weighs_shapes_alike():
-    """The dispatcher threshold: the largest M (scanning up from 1) at which
-    dp4a costs less summed over shapes, each shape's time relative to the
-    faster path there.  A shape with many bytes must not outvote the others
-    by its absolute microseconds."""
+def test_calibration_thresholds():
+    """Per shape the DP4A range ends at the first M at which another path is
+    faster, the MMA range at the first M above it at which tcgen05 is faster
+    (later wins do not reopen a range); each shape's thresholds apply to its
+    weight-size class, the smallest shape's are the defaults."""
     from iq4_xs_quantized_gb300 import calibrate
-    def row(dp, tc):
-        return {"dp4a_us": dp, "tc_us": tc}
-    per_shape = {
-        # small shape: dp4a clearly faster through M = 4
-        "small": {1: row(3.5, 7.4), 2: row(4.4, 7.4), 3: row(5.7, 7.4), 4: row(5.8, 7.4), 5: row(12.0, 7.4)},
-        # large shape: tcgen05 ahead from M = 3 by more absolute microseconds
-        # than dp4a gains on the small one
-        "large": {1: row(20.8, 27.5), 2: row(25.4, 27.5), 3: row(30.2, 27.5), 4: row(30.9, 27.5),
-                  5: row(71.4, 27.5)},
-        "mid": {1: row(12.6, 21.9), 2: row(15.4, 21.9), 3: row(19.7, 22.0), 4: row(20.3, 22.0),
-                5: row(35.0, 22.0)},
-    }
-    assert calibrate.crossover_from(per_shape, range(1, 6)) == 4
-    # absolute sums would have stopped at M = 3 (dp4a 55.6 vs tcgen05 56.9 us; at M = 4 57.0 vs 56.9)
-    total = {M: [sum(v[M][k] for v in per_shape.values()) for k in ("dp4a_us", "tc_us")] for M in range(1, 6)}
-    assert total[4][0] > total[4][1] and total[3][0] < total[3][1]
-    # string keys (as read back from the JSON table) work the same way
-    as_json = {k: {str(m): r for m, r in v.items()} for k, v in per_shape.items()}
-    assert calibrate.crossover_from(as_json, range(1, 6)) == 4
-    # dp4a never faster -> 0
-    assert calibrate.crossover_from({"s": {1: row(9.0, 7.0)}}, range(1, 2)) == 0
+
+    def row(dp, mma, tc):
+        r = {"mma_us": mma, "tc_us": tc}
+        if dp is not None:
+            r["dp4a_us"] = dp
+        return r
+    ms = (1, 2, 3, 4, 8, 16, 32)
+    a = {1: row(3.5, 7.5, 7.4), 2: row(4.4, 7.5, 7.4), 3: row(8.0, 7.6, 7.4), 4: row(9.0, 7.0, 7.4),
+         8: row(None, 7.3, 7.4), 16: row(None, 10.0, 7.4), 32: row(None, 7.0, 8.0)}
+    assert calibrate.shape_thresholds(a, ms) == (2, 2)     # MMA loses at M = 3: no MMA range
+    b = dict(a)
+    b[3] = row(8.0, 7.2, 7.4)
+    assert calibrate.shape_thresholds(b, ms) == (2, 8)     # MMA through M = 8, tcgen05 from 16
+    c = {m: row(None if m > 16 else 1.0, 2.0, 3.0) for m in ms}
+    assert calibrate.shape_thresholds(c, ms) == (16, 32)   # dp4a untimed above 16
+    as_json = {str(m): r for m, r in b.items()}            # JSON keys are strings
+    assert calibrate.shape_thresholds(as_json, ms) == (2, 8)
+    dp4a_cls, mma_cls, dflt = calibrate.class_crossovers({"64x64": a, "128x128": b, "256x256": c}, ms)
+    assert dflt == (2, 2)
+    assert dp4a_cls == [[int(round((64 * 64 * 128 * 128) ** 0.5)), 2], [int(round((128 * 128 * 256 * 256) ** 0.5)), 16]]
+    assert [m for _, m in mma_cls] == [8, 32]
 
 
 def test_tensor_work_and_roofline_gate():

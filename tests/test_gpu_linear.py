@@ -26,9 +26,22 @@ def _lib():
     assert B.iq4xs_last_device_error() == 0
 
 
-@pytest.mark.parametrize("M", (1, 3, 8, 33, 96, 200))
+@pytest.fixture(autouse=True)
+def _fixed_dispatch():
+    """DP4A to M = 4, warp MMA to M = 8, tcgen05 above, whatever the
+    calibrated table says; the table is restored afterwards."""
+    B.iq4xs_set_crossover_classes([])
+    B.iq4xs_set_mma_crossover_classes([])
+    B.iq4xs_set_mma_crossover(8)
+    yield
+    B.reset_dispatch()
+
+
+NAMES = {B.PATH_DP4A: "dp4a", B.PATH_MMA: "mma", B.PATH_TC: "tc", B.PATH_BASELINE: "tc"}  # linear runs TC on the advice
+
+
+@pytest.mark.parametrize("M", (1, 3, 6, 8, 33, 96, 200))
 def test_linear_matches_two_calls_and_oracle(M):
-    B.iq4xs_set_crossover(4)
     W = synth.SQUARE
     N, K = W.shapes[0]
     w, x = W.inputs(0, M=M)
@@ -40,7 +53,7 @@ def test_linear_matches_two_calls_and_oracle(M):
     torch.cuda.synchronize()
     yl = y.cpu().numpy()
     assert gate_written(yl) is None
-    path = "dp4a" if B.iq4xs_select_path(M, N, K) == B.PATH_DP4A else "tc"
+    path = NAMES[B.iq4xs_select_path(M, N, K)]
     qs, ds = quantize_gpu(x)
     # the full workspace: the prepared operand on the tensor-core path
     y2 = matmul_gpu(wd, N, K, qs, ds, M, "tcp" if path == "tc" else path,
@@ -66,7 +79,6 @@ def test_linear_matches_two_calls_and_oracle(M):
 def test_linear_small_m_bitwise_and_workspace_q8(M, N, K):
     """CUDA-core path across its launch shapes (two, three, four CTAs per
     SM), a ragged N and a long K."""
-    B.iq4xs_set_crossover(4)
     rng = np.random.default_rng([51, M, N, K])
     w = synth.iq4xs_weights(rng, N, K, 1e-3)
     x = synth.activations(rng, M, K, outlier_frac=0.01)
@@ -112,7 +124,6 @@ def test_linear_baseline_route_only_when_asked():
     qs_o, d_o, _ = oracle_q8(x)
     rows = sample_rows(N, 32, seed=5)
     ref = oracle_matmul(w, N, K, qs_o, d_o, rows)
-    B.iq4xs_set_crossover(4)
     B.iq4xs_set_baseline_threshold(64)
     try:
         assert B.iq4xs_select_path(M, N, K) == B.PATH_BASELINE
@@ -134,7 +145,6 @@ def test_linear_on_pinned_host_buffers_is_bitwise_device(M):
     """x read from and y written to page-locked host memory by the kernels
     (the e2e form of the benchmark): bit-identical to device buffers, on
     both paths, with a ragged N tail and split K."""
-    B.iq4xs_set_crossover(4)
     N, K = 1000, 4096
     rng = np.random.default_rng([77, M])
     w = dev(synth.iq4xs_weights(rng, N, K, 1e-3))

@@ -21,8 +21,9 @@ from iq4_xs_quantized_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
-# dp4a; tcgen05 from the Q8_1 arrays; tcgen05 from the prepared operand
-PATHS = ("dp4a", "tc", "tcp")
+# dp4a; tcgen05 from the Q8_1 arrays; tcgen05 from the prepared operand;
+# warp-level MMA
+PATHS = ("dp4a", "tc", "tcp", "mma")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -110,6 +111,34 @@ def test_matmul_tiny_tc(M, form):
     run_and_gate(w, 256, 1024, x, form)
 
 
+TINY_MS_MMA = (1, 2, 3, 4, 7, 8, 9, 15, 16, 17, 24, 25, 32, 33, 40, 64, 96)
+
+
+@pytest.mark.parametrize("M", TINY_MS_MMA)
+def test_matmul_tiny_mma(M):
+    w, x = synth.TINY.inputs(0, M=M)
+    run_and_gate(w, 256, 1024, x, "mma")
+
+
+# Every tile height (32..256 weight rows per CTA: 1..8 fragments per warp,
+# odd and even) and K split of the warp-MMA path, for every activation tile
+# width (8, 16, 24, 32 rows), on a ragged N; K = 4608 is 9 super-block pairs,
+# so the splits take unequal shares.
+@pytest.mark.parametrize("rows", (32, 96, 128, 160, 224, 256))
+@pytest.mark.parametrize("splits", (1, 3, 8))
+def test_matmul_mma_configs(rows, splits):
+    rng = np.random.default_rng([rows, splits])
+    N, K = 300, 4608
+    w = synth.iq4xs_weights(rng, N, K, 1e-3)
+    B.iq4xs_test_mma_config(rows, splits)
+    try:
+        for M in (5, 13, 21, 32):
+            x = synth.activations(rng, M, K, outlier_frac=0.01)
+            run_and_gate(w, N, K, x, "mma")
+    finally:
+        B.iq4xs_test_mma_config(0, 0)
+
+
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("N", (1, 7, 130, 200, 383))
 def test_matmul_ragged_n(path, N):
@@ -139,6 +168,16 @@ def test_matmul_k256_dp4a_only():
     w = synth.iq4xs_weights(rng, 64, 256, 2e-3)
     x = synth.activations(rng, 4, 256)
     run_and_gate(w, 64, 256, x, "dp4a")
+    for K in (768, 1280):  # an odd number of super-blocks: rows not 16-byte strided
+        w2 = synth.iq4xs_weights(rng, 200, K, 2e-3)
+        for M in (3, 20):
+            run_and_gate(w2, 200, K, synth.activations(rng, M, K), "auto")
+            assert B.iq4xs_select_path(M, 200, K) == B.PATH_DP4A
+    qs, ds = quantize_gpu(x)
+    y = torch.empty((4, 64), dtype=torch.float32, device="cuda")
+    with pytest.raises(B.IQ4XSError) as e:
+        B.iq4xs_matmul(dev(w), 64, 256, qs, ds, 4, y, "mma")
+    assert e.value.status == B.ERR_SHAPE
     qs, ds = quantize_gpu(x)
     y = torch.empty((4, 64), dtype=torch.float32, device="cuda")
     with pytest.raises(B.IQ4XSError) as e:
@@ -209,19 +248,20 @@ def _full_case(wl, shape_index, M, path, nrows=48):
 
 @pytest.mark.parametrize("M", synth.SQUARE.ms)
 def test_full_square(M):
-    B.iq4xs_set_crossover(4)
-    path = "dp4a" if B.iq4xs_select_path(M, 4096, 4096) == B.PATH_DP4A else "tc"
-    _full_case("square_4096x4096", 0, M, path)
+    _full_case("square_4096x4096", 0, M, "auto")  # the dispatcher's choice, as the benchmark runs it
     _full_case("square_4096x4096", 0, M, "tcp")
+    _full_case("square_4096x4096", 0, M, "mma")
+    _full_case("square_4096x4096", 0, M, "tc")
     if M <= 16:
-        _full_case("square_4096x4096", 0, M, "tc" if path == "dp4a" else "dp4a")
+        _full_case("square_4096x4096", 0, M, "dp4a")
 
 
 @pytest.mark.parametrize("shape_index", range(9))
 def test_full_decoder_shapes(shape_index):
     # dp4a at M = 1 and 2 meets all three launch shapes across these grids
     # (1024 rows: 64 CTAs; 5120-6144: 320-384; 10240-34816: 640-2176)
-    for M, path in ((1, "dp4a"), (2, "dp4a"), (16, "tc"), (64, "tc"), (16, "tcp"), (64, "tcp")):
+    for M, path in ((1, "dp4a"), (2, "dp4a"), (16, "tc"), (64, "tc"), (16, "tcp"), (64, "tcp"),
+                    (1, "mma"), (4, "mma"), (8, "mma"), (16, "mma"), (32, "mma")):
         _full_case("decoder27b_9proj", shape_index, M, path, nrows=24)
 
 
@@ -249,16 +289,28 @@ def test_dequantize_bit_exact():
 
 # --------------------------------------------------------------------- dispatch
 def test_auto_matches_explicit_path():
+    """AUTO runs exactly the kernel the installed crossovers name (outputs
+    bit-identical to the explicit path's), classes overriding the defaults."""
     w, x = synth.TINY.inputs(0, M=8)
     qs, ds = quantize_gpu(x)
     wd = dev(w)
-    for cross in (2, 8):
-        B.iq4xs_set_crossover(cross)
-        expect = "dp4a" if 8 <= cross else "tc"
-        ya = matmul_gpu(wd, 256, 1024, qs, ds, 8, "auto")
-        ye = matmul_gpu(wd, 256, 1024, qs, ds, 8, expect)
-        assert np.array_equal(ya, ye)
-    B.iq4xs_set_crossover(4)
+    try:
+        B.iq4xs_set_crossover_classes([])
+        B.iq4xs_set_mma_crossover_classes([])
+        for cross, mma, expect in ((8, 8, "dp4a"), (2, 8, "mma"), (2, 4, "tc"), (9, 2, "dp4a")):
+            B.iq4xs_set_crossover(cross)
+            B.iq4xs_set_mma_crossover(mma)
+            assert B.iq4xs_select_path(8, 256, 1024) == B.PATHS[expect]
+            ya = matmul_gpu(wd, 256, 1024, qs, ds, 8, "auto")
+            ye = matmul_gpu(wd, 256, 1024, qs, ds, 8, expect)
+            assert np.array_equal(ya, ye), expect
+        B.iq4xs_set_crossover(2)
+        B.iq4xs_set_mma_crossover(4)
+        B.iq4xs_set_mma_crossover_classes([(256 * 1024, 16)])  # this matrix's class: MMA to M = 16
+        assert B.iq4xs_select_path(8, 256, 1024) == B.PATH_MMA
+        assert B.iq4xs_select_path(8, 128, 1024) == B.PATH_TC  # below the class: the default
+    finally:
+        B.reset_dispatch()  # defaults, then the calibrated table
 
 
 # ------------------------------------------------------------ negative controls

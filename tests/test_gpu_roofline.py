@@ -72,7 +72,7 @@ def matmul_bytes(wbytes, M, N, K):
 
 @pytest.mark.parametrize("N,K", [(4096, 4096), (12288, 5120)])
 @pytest.mark.parametrize("path,M", [("dp4a", 1), ("dp4a", 4), ("tc", 8), ("tc", 16), ("tc", 64),
-                                    ("tc", 96)])
+                                    ("tc", 96), ("mma", 1), ("mma", 8), ("mma", 16), ("mma", 32)])
 def test_matmul_within_hbm_roofline(N, K, path, M):
     rng = np.random.default_rng([N, K, M])
     w = torch.from_numpy(synth.iq4xs_weights(rng, N, K, 1e-3)).cuda()
