@@ -401,14 +401,17 @@ int iq4xs_test_skip_w_stage(int64_t stage);
 /*
  * Test hook for the warp-MMA path's launch configuration (no counterpart on
  * the source pages): later MMA launches use rows_per_cta weight rows per CTA
- * (a multiple of 32, at most 256; capped at 128 when M > 16) and k_splits
- * CTAs per cluster along K (1..8, capped at the K range's super-block
- * pairs) instead of the launch model's choice, so that tests reach every
- * tile height and split.  0 restores the model's choice for that value.
- * Host only; applies to every thread's later launches.  IQ4XS_ERR_ARG for
- * other values.
+ * (a multiple of 32, at most 256), k_splits CTAs per cluster along K (1..8,
+ * capped at the K range's super-block pairs) and ctas_per_sm (1, or 2: the
+ * half-shared-memory tiles) instead of the launch model's choice, so that
+ * tests reach every configuration; a combination the activation tile cannot
+ * take falls back to the nearest smaller tile height (at least 32 rows, at
+ * most 128 from 24 activation rows on; two CTAs per SM only up to 64 rows at
+ * 8 activation rows, 32 at 16 and 24, none above).  0 restores the model's
+ * choice for that value.  Host only; applies to every thread's later
+ * launches.  IQ4XS_ERR_ARG for other values.
  */
-int iq4xs_test_mma_config(int64_t rows_per_cta, int64_t k_splits);
+int iq4xs_test_mma_config(int64_t rows_per_cta, int64_t k_splits, int64_t ctas_per_sm);
 
 /* Static string for a status code. */
 const char* iq4xs_status_string(int status);

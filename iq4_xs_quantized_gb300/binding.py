@@ -78,7 +78,7 @@ def load(path: str | None = None):
         lib.iq4xs_set_baseline_threshold.argtypes = [i64]
         lib.iq4xs_set_crossover_classes.argtypes = [ctypes.POINTER(i64), ctypes.POINTER(i64), ci]
         lib.iq4xs_set_mma_crossover.argtypes = [i64]
-        lib.iq4xs_test_mma_config.argtypes = [i64, i64]
+        lib.iq4xs_test_mma_config.argtypes = [i64, i64, i64]
         lib.iq4xs_set_mma_crossover_classes.argtypes = [ctypes.POINTER(i64), ctypes.POINTER(i64), ci]
         lib.iq4xs_set_pdl.argtypes = [ci]
         lib.iq4xs_set_pdl.restype = ci
@@ -298,9 +298,10 @@ def iq4xs_set_mma_crossover_classes(classes) -> None:
     _check("iq4xs_set_mma_crossover_classes", _set_classes(load(), list(classes), mma=True))
 
 
-def iq4xs_test_mma_config(rows_per_cta: int = 0, k_splits: int = 0) -> None:
+def iq4xs_test_mma_config(rows_per_cta: int = 0, k_splits: int = 0, ctas_per_sm: int = 0) -> None:
     """Force the warp-MMA launch configuration (0 = the launch model's choice)."""
-    _check("iq4xs_test_mma_config", load().iq4xs_test_mma_config(int(rows_per_cta), int(k_splits)))
+    _check("iq4xs_test_mma_config",
+           load().iq4xs_test_mma_config(int(rows_per_cta), int(k_splits), int(ctas_per_sm)))
 
 
 def iq4xs_set_baseline_threshold(m_min_baseline: int) -> None:

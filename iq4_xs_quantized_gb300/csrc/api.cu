@@ -379,10 +379,11 @@ int iq4xs_test_skip_w_stage(int64_t stage) {
     return IQ4XS_OK;
 }
 
-int iq4xs_test_mma_config(int64_t rows_per_cta, int64_t k_splits) {
-    if (rows_per_cta < 0 || rows_per_cta > 256 || rows_per_cta % 32 || k_splits < 0 || k_splits > 8)
+int iq4xs_test_mma_config(int64_t rows_per_cta, int64_t k_splits, int64_t ctas_per_sm) {
+    if (rows_per_cta < 0 || rows_per_cta > 256 || rows_per_cta % 32 || k_splits < 0 || k_splits > 8 ||
+        ctas_per_sm < 0 || ctas_per_sm > 2)
         return IQ4XS_ERR_ARG;
-    mma_force_config((int)(rows_per_cta / 32), (int)k_splits);
+    mma_force_config((int)(rows_per_cta / 32), (int)k_splits, (int)ctas_per_sm);
     return IQ4XS_OK;
 }
 

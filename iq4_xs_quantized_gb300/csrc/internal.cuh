@@ -908,8 +908,9 @@ bool pdl_enabled();
 // TMA), ds read directly.
 int mma_tile_rows(int64_t M);
 // Test override of the warp-MMA launch: 16-row weight fragments per consumer
-// warp (rows per CTA = 32 x that) and K splits; 0 = the launch model's choice.
-void mma_force_config(int frags_per_warp, int k_splits);
+// warp (rows per CTA = 32 x that), K splits and CTAs per SM (1, 2); 0 = the
+// launch model's choice.
+void mma_force_config(int frags_per_warp, int k_splits, int ctas_per_sm);
 cudaError_t launch_matmul_mma(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds, int64_t M,
                               float* y, int64_t ldy, void* encode, int* err, int num_sms, cudaStream_t stream);
 cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,

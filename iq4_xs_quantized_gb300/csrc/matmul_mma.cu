@@ -68,7 +68,7 @@ constexpr int kQBoxesPerStage = kPairK / kQBoxK;  // 4
 constexpr int kMmaSmemLimit = 227 * 1024;
 constexpr int kOffRingMma = kWideLutBytes;
 constexpr int kMmaBarBytes = 128;             // full[4], empty[4], abort flag
-constexpr int kMmaRingBytes = kMmaSmemLimit - kOffRingMma - kMmaBarBytes;
+constexpr int kMmaSmemLimit2 = 113 * 1024;   // per CTA with two CTAs per SM
 __device__ volatile int g_never_abort_mma = 0;  // an abort flag that is never set
 
 // Physical address (bytes from the table start) of byte o of the gap space.
@@ -78,7 +78,7 @@ __host__ __device__ constexpr uint32_t gap_addr(uint32_t o) { return ((o >> 7) <
 // consumer warp.  The 8 consumer warps are 2 row groups x 4 sub-block
 // groups, so a CTA owns R = 32 T weight rows and a warp takes fragments
 // rg, rg + 2, ..., rg + 2 (T - 1) and 4 consecutive sub-blocks of a stage.
-template <int NT, int T>
+template <int NT, int T, int kOcc = 1>
 struct MmaCfg {
     static_assert(NT >= 1 && NT <= 4, "1..4 fragments of 8 activation rows");
     static_assert(T >= 1 && T * NT <= 16, "accumulators: T x NT x 4 registers per lane");
@@ -93,7 +93,12 @@ struct MmaCfg {
     static constexpr int kQStage = kQBoxesPerStage * kQBox;
     static constexpr int kWBytes = (kR * kPairBytes + 1023) / 1024 * 1024;
     static constexpr int kStage = kWBytes + kQStage;
-    static constexpr int kNS = kMmaRingBytes / kStage < kMmaMaxStages ? kMmaRingBytes / kStage : kMmaMaxStages;
+    // kOcc CTAs per SM: the whole shared memory (227 KB) for one, or half
+    // of it (113 KB) for two -- then a launch's CTAs can start beside the
+    // preceding launch's last ones.
+    static_assert(kOcc == 1 || kOcc == 2, "one or two CTAs per SM");
+    static constexpr int kRing = (kOcc == 1 ? kMmaSmemLimit : kMmaSmemLimit2) - kOffRingMma - kMmaBarBytes;
+    static constexpr int kNS = kRing / kStage < kMmaMaxStages ? kRing / kStage : kMmaMaxStages;
     static_assert(kNS >= 2, "two stages in flight");
     static constexpr int kSmem = kOffRingMma + kNS * kStage + kMmaBarBytes;
     // Per-warp tables (gap space): row scales [k][s][g][h] (rows
@@ -106,6 +111,7 @@ struct MmaCfg {
     static constexpr int kCombos = T * 8;                  // (fragment, g) pairs of a warp
     static constexpr int kRedStride = kMt + 4;             // fp32 per row of a partial tile
     static_assert(kSG * kR * kRedStride * 4 <= kNS * kStage, "partials fit the ring");
+    static_assert(kSmem <= (kOcc == 1 ? kMmaSmemLimit : kMmaSmemLimit2), "shared memory per CTA");
     static_assert(kR * kRedStride * 4 <= kWideLutBytes, "CTA tile fits the byte table");
 };
 
@@ -128,12 +134,12 @@ __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kMmaConsumers) : "memory");
 }
 
-template <int NT, int T>
-__global__ void __launch_bounds__(kMmaThreads, 1)
+template <int NT, int T, int kOcc>
+__global__ void __launch_bounds__(kMmaThreads, kOcc)
     matmul_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_q,
                       const __half* __restrict__ ds, int64_t M, int N, int K, float* __restrict__ y, int64_t ldy,
                       int* err) {
-    using C = MmaCfg<NT, T>;
+    using C = MmaCfg<NT, T, kOcc>;
     constexpr int kTMax = T, kMt = C::kMt, kSPW = C::kSPW, kRG = C::kRG, R = C::kR, NS = C::kNS;
     extern __shared__ __align__(1024) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {  // the 128-byte-swizzled code boxes need 1024-byte alignment
@@ -156,6 +162,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int p1 = (int)((int64_t)pairs * (rank + 1) / S);
     const int nst = p1 - p0;
 
+    auto load_w = [&](int ps) {
+        const int slot = ps % NS;
+        mbar_arrive_expect_tx(&full[slot], (uint32_t)(R * kPairBytes + C::kQStage));
+        tma_load_2d(smem + kOffRingMma + slot * stage_b, &tmap_w, (p0 + ps) * (kPairBytes / 4), n0, &full[slot]);
+    };
+    auto load_q = [&](int ps) {
+        const int slot = ps % NS;
+#pragma unroll
+        for (int b = 0; b < kQBoxesPerStage; ++b)
+            tma_load_2d(smem + kOffRingMma + slot * stage_b + wbytes + b * C::kQBox, &tmap_q,
+                        (p0 + ps) * kPairK + b * kQBoxK, z * kMt, &full[slot]);
+    };
+    const int pre = nst < NS ? nst : NS;
     if (warp == kMmaProducerWarp && lane == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&full[i], 1);
@@ -164,6 +183,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
+        // The first W stages (model state) go out at once, before the byte
+        // table is built and before the preceding grid (which writes the
+        // codes) has finished.
+        prefetch_tmap(&tmap_w);
+        prefetch_tmap(&tmap_q);
+        for (int ps = 0; ps < pre; ++ps) load_w(ps);
     }
     // Byte table: row j = 32 copies (one per bank) of the fp16x2 word
     // (kv[j & 15], kv[j >> 4]) in its first 128 bytes.
@@ -177,25 +202,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     bool ok = true;
     if (warp == kMmaProducerWarp) {
         if (lane == 0) {
-            prefetch_tmap(&tmap_w);
-            prefetch_tmap(&tmap_q);
-            auto load_w = [&](int ps) {
-                const int slot = ps % NS;
-                mbar_arrive_expect_tx(&full[slot], (uint32_t)(R * kPairBytes + C::kQStage));
-                tma_load_2d(smem + kOffRingMma + slot * stage_b, &tmap_w, (p0 + ps) * (kPairBytes / 4), n0,
-                            &full[slot]);
-            };
-            auto load_q = [&](int ps) {
-                const int slot = ps % NS;
-#pragma unroll
-                for (int b = 0; b < kQBoxesPerStage; ++b)
-                    tma_load_2d(smem + kOffRingMma + slot * stage_b + wbytes + b * C::kQBox, &tmap_q,
-                                (p0 + ps) * kPairK + b * kQBoxK, z * kMt, &full[slot]);
-            };
-            // W (model state) streams before the preceding grid, which
-            // writes the codes, has finished.
-            const int pre = nst < NS ? nst : NS;
-            for (int ps = 0; ps < pre; ++ps) load_w(ps);
             griddep_wait();
             for (int ps = 0; ps < pre; ++ps) load_q(ps);
             int issued = pre;
@@ -339,6 +345,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                             mma_f16_16816(p, a0, bfr[f][0], bfr[f][1], zero);
                             mma_f16_16816(p, a1, bfr[f][2], bfr[f][3], p);
                             // acc += (P * d_x) * d_w*(ls-32): rows g (p0, p1) and g+8 (p2, p3)
+#ifdef IQ4XS_MMA_SCALAR_FP
+                            acc[k][f][0] = __fmaf_rn(__fmul_rn(p[0], dx[f].x), sw.x, acc[k][f][0]);
+                            acc[k][f][1] = __fmaf_rn(__fmul_rn(p[1], dx[f].y), sw.x, acc[k][f][1]);
+                            acc[k][f][2] = __fmaf_rn(__fmul_rn(p[2], dx[f].x), sw.y, acc[k][f][2]);
+                            acc[k][f][3] = __fmaf_rn(__fmul_rn(p[3], dx[f].y), sw.y, acc[k][f][3]);
+#else
                             const float2 q01 = __fmul2_rn(make_float2(p[0], p[1]), dx[f]);
                             const float2 q23 = __fmul2_rn(make_float2(p[2], p[3]), dx[f]);
                             const float2 r01 =
@@ -347,6 +359,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                                 __ffma2_rn(q23, make_float2(sw.y, sw.y), make_float2(acc[k][f][2], acc[k][f][3]));
                             acc[k][f][0] = r01.x; acc[k][f][1] = r01.y;
                             acc[k][f][2] = r23.x; acc[k][f][3] = r23.y;
+#endif
                         }
                     }
                 }
@@ -426,15 +439,15 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 
 // Cached per device: clusters of S (1..8) the device runs at once for the
 // kernel <NT, T> (cudaOccupancyMaxActiveClusters, queried once).
-template <int NT, int T>
+template <int NT, int T, int kOcc>
 int mma_max_clusters(int dev, int s, int num_sms) {
-    using C = MmaCfg<NT, T>;
+    using C = MmaCfg<NT, T, kOcc>;
     static int cache[64][kMmaMaxCluster + 1] = {};
     int mc = (dev >= 0 && dev < 64) ? cache[dev][s] : 0;
     if (mc > 0) return mc;
     static bool attr_done[64] = {};
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(matmul_mma_kernel<NT, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
+        if (cudaFuncSetAttribute(matmul_mma_kernel<NT, T, kOcc>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
             cudaSuccess)
             cudaGetLastError();
         attr_done[dev] = true;
@@ -451,19 +464,19 @@ int mma_max_clusters(int dev, int s, int num_sms) {
     q.attrs = at;
     q.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, matmul_mma_kernel<NT, T>, &q) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, matmul_mma_kernel<NT, T, kOcc>, &q) != cudaSuccess || n < 1) {
         cudaGetLastError();
-        n = num_sms / s;
+        n = kOcc * num_sms / s;
     }
     mc = n > 0 ? n : 1;
     if (dev >= 0 && dev < 64) cache[dev][s] = mc;
     return mc;
 }
 
-template <int NT, int T>
+template <int NT, int T, int kOcc>
 cudaError_t launch_nt(const void* w, int64_t row_bytes, EncodeTiledFn enc, const CUtensorMap& tq, const __half* ds,
                       int64_t M, int N, int K, int S, float* y, int64_t ldy, int* err, cudaStream_t stream) {
-    using C = MmaCfg<NT, T>;
+    using C = MmaCfg<NT, T, kOcc>;
     // W: one box = R rows x one super-block pair (272 B; K % 512 == 0, so
     // rows are 16-byte strided); rows past N read as zeros (d = 0).
     CUtensorMap tw;
@@ -493,7 +506,7 @@ cudaError_t launch_nt(const void* w, int64_t row_bytes, EncodeTiledFn enc, const
     attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, matmul_mma_kernel<NT, T>, tw, tq, ds, M, N, K, y, ldy, err);
+    return cudaLaunchKernelEx(&cfg, matmul_mma_kernel<NT, T, kOcc>, tw, tq, ds, M, N, K, y, ldy, err);
 }
 
 // Fragments per warp T (R = 32 T rows per CTA) and K split S (= cluster
@@ -503,9 +516,58 @@ cudaError_t launch_nt(const void* w, int64_t row_bytes, EncodeTiledFn enc, const
 // runs at once.  F, a CTA's fixed cost (launch, first stage, reduction), is
 // about two stages.  Ties keep the larger R and the smaller S.
 // Test override of the launch configuration (0 = the model's choice).
-std::atomic<int> g_force_t{0}, g_force_s{0};
+std::atomic<int> g_force_t{0}, g_force_s{0}, g_force_occ{0};
 
-template <int NT, int kTMax>
+// One launch configuration: fragments per warp T (R = 32 T rows per CTA)
+// and CTAs per SM, with its cluster-occupancy query and its launcher.
+struct MmaConfig {
+    int T, occ;
+    int (*max_clusters)(int dev, int s, int num_sms);
+    cudaError_t (*launch)(const void*, int64_t, EncodeTiledFn, const CUtensorMap&, const __half*, int64_t, int,
+                          int, int, float*, int64_t, int*, cudaStream_t);
+};
+template <int NT, int T, int kOcc>
+constexpr MmaConfig cfg_of() {
+    return {T, kOcc, &mma_max_clusters<NT, T, kOcc>, &launch_nt<NT, T, kOcc>};
+}
+// Per activation-tile width: T = 1..8 (4 from 24 activation rows on, the
+// accumulators' registers) at one CTA per SM, and the tiles that leave room
+// for two CTAs per SM (113 KB each, two stages: up to 64 rows at 8
+// activation rows, 32 at 16 and 24).
+template <int NT>
+struct MmaConfigs;
+template <>
+struct MmaConfigs<1> {
+    static constexpr MmaConfig list[] = {cfg_of<1, 8, 1>(), cfg_of<1, 7, 1>(), cfg_of<1, 6, 1>(), cfg_of<1, 5, 1>(),
+                                         cfg_of<1, 4, 1>(), cfg_of<1, 3, 1>(), cfg_of<1, 2, 1>(), cfg_of<1, 1, 1>(),
+                                         cfg_of<1, 2, 2>(), cfg_of<1, 1, 2>()};
+};
+template <>
+struct MmaConfigs<2> {
+    static constexpr MmaConfig list[] = {cfg_of<2, 8, 1>(), cfg_of<2, 7, 1>(), cfg_of<2, 6, 1>(), cfg_of<2, 5, 1>(),
+                                         cfg_of<2, 4, 1>(), cfg_of<2, 3, 1>(), cfg_of<2, 2, 1>(), cfg_of<2, 1, 1>(),
+                                         cfg_of<2, 1, 2>()};
+};
+template <>
+struct MmaConfigs<3> {
+    static constexpr MmaConfig list[] = {cfg_of<3, 4, 1>(), cfg_of<3, 3, 1>(), cfg_of<3, 2, 1>(), cfg_of<3, 1, 1>(),
+                                         cfg_of<3, 1, 2>()};
+};
+template <>
+struct MmaConfigs<4> {
+    static constexpr MmaConfig list[] = {cfg_of<4, 4, 1>(), cfg_of<4, 3, 1>(), cfg_of<4, 2, 1>(),
+                                         cfg_of<4, 1, 1>()};
+};
+
+// The configuration (T, CTAs per SM) and K split S (= cluster size) with the
+// least modelled time  waves x (F + c x R / 128 x ceil(pairs / S))  in units
+// of one 128-row stage's streaming time per SM, over every configuration of
+// the activation-tile width and S = 1..8 (at most the K pairs); waves from
+// the clusters of S the device runs at once for that configuration; c = the
+// CTAs sharing an SM.  F, a CTA's fixed cost (launch, first stage,
+// reduction), is about two stages.  Ties keep the earlier configuration
+// (larger R, one CTA per SM) and the smaller S.
+template <int NT>
 cudaError_t launch_best(const void* w, int64_t row_bytes, EncodeTiledFn enc, const CUtensorMap& tq,
                         const __half* ds, int64_t M, int N, int K, float* y, int64_t ldy, int* err, int num_sms,
                         cudaStream_t stream) {
@@ -514,60 +576,46 @@ cudaError_t launch_best(const void* w, int64_t row_bytes, EncodeTiledFn enc, con
     cudaGetDevice(&dev);
     const int mtiles = (int)((M + 8 * NT - 1) / (8 * NT));
     const int pairs = (K + kPairK - 1) / kPairK;
-    int best_t = kTMax, best_s = 1;
+    const auto& list = MmaConfigs<NT>::list;
+    constexpr int kCount = (int)(sizeof(list) / sizeof(list[0]));
+    int best_c = 0, best_s = 1;
     double best = 1e30;
-    for (int tt = kTMax; tt >= 1; --tt) {
-        const int R = 32 * tt;
+    for (int ci = 0; ci < kCount; ++ci) {
+        const MmaConfig& c = list[ci];
+        const int R = 32 * c.T;
         const int units = (N + R - 1) / R * mtiles;
         for (int s = 1; s <= kMmaMaxCluster && s <= pairs; ++s) {
-            int mc = 0;
-            switch (tt) {
-                case 1: mc = mma_max_clusters<NT, 1>(dev, s, num_sms); break;
-                case 2: mc = mma_max_clusters<NT, 2>(dev, s, num_sms); break;
-                case 3: mc = mma_max_clusters<NT, 3>(dev, s, num_sms); break;
-                case 4: mc = mma_max_clusters<NT, 4>(dev, s, num_sms); break;
-                case 5: mc = mma_max_clusters<NT, (kTMax >= 5 ? 5 : 1)>(dev, s, num_sms); break;
-                case 6: mc = mma_max_clusters<NT, (kTMax >= 6 ? 6 : 1)>(dev, s, num_sms); break;
-                case 7: mc = mma_max_clusters<NT, (kTMax >= 7 ? 7 : 1)>(dev, s, num_sms); break;
-                default: mc = mma_max_clusters<NT, (kTMax >= 8 ? 8 : 1)>(dev, s, num_sms); break;
-            }
-            const int waves = (units * s + mc * s - 1) / (mc * s);
-            const double tm = waves * (kFixed + (double)R / 128.0 * (double)((pairs + s - 1) / s));
+            const int mc = c.max_clusters(dev, s, num_sms);
+            const int waves = (units + mc - 1) / mc;
+            const double tm = waves * (kFixed + c.occ * (double)R / 128.0 * (double)((pairs + s - 1) / s));
             if (tm < best * 0.999) {
                 best = tm;
-                best_t = tt;
+                best_c = ci;
                 best_s = s;
             }
         }
     }
-    {
-        const int ft = g_force_t.load(), fs = g_force_s.load();
-        if (ft > 0) best_t = ft < kTMax ? ft : kTMax;
-        if (fs > 0) best_s = fs < pairs ? fs : pairs;
+    const int ft = g_force_t.load(), fs = g_force_s.load(), fo = g_force_occ.load();
+    if (ft > 0 || fo > 0) {  // the forced configuration, or the nearest one the list holds
+        const int want_t = ft > 0 ? ft : list[best_c].T, want_o = fo > 0 ? fo : list[best_c].occ;
+        int pick = -1;
+        for (int ci = 0; ci < kCount; ++ci)
+            if (list[ci].occ == want_o && list[ci].T <= want_t && (pick < 0 || list[ci].T > list[pick].T)) pick = ci;
+        if (pick < 0)
+            for (int ci = 0; ci < kCount; ++ci)
+                if (list[ci].T <= want_t && (pick < 0 || list[ci].T > list[pick].T)) pick = ci;
+        best_c = pick < 0 ? kCount - 1 : pick;
     }
-#define IQ4XS_MMA_T(tv)                                                                                        \
-    case tv:                                                                                                   \
-        return launch_nt<NT, (kTMax >= tv ? tv : 1)>(w, row_bytes, enc, tq, ds, M, N, K, best_s, y, ldy, err, \
-                                                     stream);
-    switch (best_t) {
-        IQ4XS_MMA_T(1)
-        IQ4XS_MMA_T(2)
-        IQ4XS_MMA_T(3)
-        IQ4XS_MMA_T(4)
-        IQ4XS_MMA_T(5)
-        IQ4XS_MMA_T(6)
-        IQ4XS_MMA_T(7)
-        IQ4XS_MMA_T(8)
-        default: return cudaErrorInvalidValue;
-    }
-#undef IQ4XS_MMA_T
+    if (fs > 0) best_s = fs < pairs ? fs : pairs;
+    return list[best_c].launch(w, row_bytes, enc, tq, ds, M, N, K, best_s, y, ldy, err, stream);
 }
 
 }  // namespace
 
-void mma_force_config(int frags_per_warp, int k_splits) {
+void mma_force_config(int frags_per_warp, int k_splits, int ctas_per_sm) {
     g_force_t.store(frags_per_warp);
     g_force_s.store(k_splits);
+    g_force_occ.store(ctas_per_sm);
 }
 
 int mma_tile_rows(int64_t M) {
@@ -596,10 +644,10 @@ cudaError_t launch_matmul_mma(const void* w, int64_t N, int64_t K, const int8_t*
     const __half* dsh = reinterpret_cast<const __half*>(ds);
     const int Ni = (int)N, Ki = (int)K;
     switch (mt) {
-        case 8: return launch_best<1, 8>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
-        case 16: return launch_best<2, 8>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
-        case 24: return launch_best<3, 4>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
-        default: return launch_best<4, 4>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
+        case 8: return launch_best<1>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
+        case 16: return launch_best<2>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
+        case 24: return launch_best<3>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
+        default: return launch_best<4>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
     }
 }
 

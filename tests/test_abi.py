@@ -108,11 +108,12 @@ def test_select_path_and_crossover(lib):
 
 
 def test_mma_config_hook_validation(lib):
-    assert lib.iq4xs_test_mma_config(0, 0) == B.OK
-    for rows, splits in ((16, 1), (288, 1), (-32, 1), (64, 9), (64, -1)):
-        assert lib.iq4xs_test_mma_config(rows, splits) == B.ERR_ARG
-    assert lib.iq4xs_test_mma_config(256, 8) == B.OK
-    assert lib.iq4xs_test_mma_config(0, 0) == B.OK
+    assert lib.iq4xs_test_mma_config(0, 0, 0) == B.OK
+    for rows, splits, occ in ((16, 1, 0), (288, 1, 0), (-32, 1, 0), (64, 9, 0), (64, -1, 0), (64, 1, 3),
+                              (64, 1, -1)):
+        assert lib.iq4xs_test_mma_config(rows, splits, occ) == B.ERR_ARG
+    assert lib.iq4xs_test_mma_config(256, 8, 2) == B.OK
+    assert lib.iq4xs_test_mma_config(0, 0, 0) == B.OK
 
 
 def test_baseline_threshold_is_advice_above_the_tc_range(lib):

@@ -130,13 +130,29 @@ def test_matmul_mma_configs(rows, splits):
     rng = np.random.default_rng([rows, splits])
     N, K = 300, 4608
     w = synth.iq4xs_weights(rng, N, K, 1e-3)
-    B.iq4xs_test_mma_config(rows, splits)
+    B.iq4xs_test_mma_config(rows, splits, 1)
     try:
         for M in (5, 13, 21, 32):
             x = synth.activations(rng, M, K, outlier_frac=0.01)
             run_and_gate(w, N, K, x, "mma")
     finally:
-        B.iq4xs_test_mma_config(0, 0)
+        B.iq4xs_test_mma_config(0, 0, 0)
+
+
+# The half-shared-memory tiles (two CTAs per SM): 32 and 64 rows at 8
+# activation rows, 32 at 16 and 24 (M = 32 falls back to one CTA per SM).
+@pytest.mark.parametrize("rows,splits", [(32, 1), (64, 2), (64, 5), (32, 8)])
+def test_matmul_mma_two_ctas_per_sm(rows, splits):
+    rng = np.random.default_rng([rows, splits, 2])
+    N, K = 1000, 5120
+    w = synth.iq4xs_weights(rng, N, K, 1e-3)
+    B.iq4xs_test_mma_config(rows, splits, 2)
+    try:
+        for M in (1, 8, 9, 16, 24, 32):
+            x = synth.activations(rng, M, K, outlier_frac=0.01)
+            run_and_gate(w, N, K, x, "mma")
+    finally:
+        B.iq4xs_test_mma_config(0, 0, 0)
 
 
 @pytest.mark.parametrize("path", PATHS)
