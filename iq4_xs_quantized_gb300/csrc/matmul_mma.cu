@@ -267,21 +267,36 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
             const uint8_t* wst = smem + kOffRingMma + slot * stage_b;
             const uint8_t* qst = wst + wbytes;
             // ---- per-stage tables: row scales and activation scales
+            // Row scales of this warp's kSPW = 4 consecutive sub-blocks
+            // jj0..jj0+3 of one super-block: from the header's 16 bits of
+            // low nibbles and 8 bits of high pairs shifted once, each
+            // ls - 32 comes out exact through the float 2^23 + ls.
+            static_assert(kSPW == 4, "four sub-blocks per header read");
 #pragma unroll
             for (int c = lane; c < C::kCombos; c += 32) {
                 const int k = c >> 3, gg = c & 7;
-                const int f = rg + kRG * k;
-                {
-                    const int r = 16 * f + gg;
-                    const uint2 h0 = *reinterpret_cast<const uint2*>(wst + r * kPairBytes + super_w * kBlockBytes);
-                    const uint2 h1 =
-                        *reinterpret_cast<const uint2*>(wst + (r + 8) * kPairBytes + super_w * kBlockBytes);
+                const int r = 16 * (rg + kRG * k) + gg;
+                float sw[2][4];
 #pragma unroll
-                    for (int s2 = 0; s2 < kSPW; ++s2) {
-                        const float2 v = make_float2(iq4xs_scale(h0.x, h0.y, jj0 + s2), iq4xs_scale(h1.x, h1.y, jj0 + s2));
-                        *reinterpret_cast<float2*>(smem + gap_addr(tab + (uint32_t)((((k * kSPW + s2) * 8 + gg) * 2) * 4))) = v;
+                for (int h = 0; h < 2; ++h) {
+                    const uint2 hd =
+                        *reinterpret_cast<const uint2*>(wst + (r + 8 * h) * kPairBytes + super_w * kBlockBytes);
+                    const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
+                    const uint32_t lo16 = hd.y >> (4 * jj0);          // ls low nibbles of jj0..jj0+3
+                    const uint32_t hi8 = hd.x >> (16 + 2 * jj0);      // ls high bit pairs
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t ls = ((lo16 >> (4 * u)) & 0xFu) | (((hi8 >> (2 * u)) & 3u) << 4);
+                        const float l = __uint_as_float(0x4B000000u | ls) - 8388640.0f;  // ls - 32, exact
+                        sw[h][u] = d * l;
                     }
                 }
+                // block (k, s2) of 64 bytes at gap offset 64 (4 k + s2): two
+                // 128-byte chunks per k, entries (rows r, r + 8) at +8 gg
+                uint8_t* tk = smem + gap_addr(tab + (uint32_t)(256 * k)) + 8 * gg;
+#pragma unroll
+                for (int s2 = 0; s2 < 4; ++s2)
+                    *reinterpret_cast<float2*>(tk + 256 * (s2 >> 1) + 64 * (s2 & 1)) = make_float2(sw[0][s2], sw[1][s2]);
             }
 #pragma unroll
             for (int k = 0; k < C::kXItems; ++k) {
