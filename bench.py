@@ -711,13 +711,15 @@ def decode_stream(torch, B, dev, reps=5):
     return res
 
 
-def moe_grouped(torch, B, dev, layers=12, reps=5):
+def moe_grouped(torch, B, dev, layers=12, reps=5, tokens=(1, 4, 16, 64, 256)):
     """Routed-expert layer (128 experts of 1536 x 2048, top-8): per token
     count T, one layer call = quantize the T*8 routed rows + the grouped
-    matmul in one launch, against the same layer with one dp4a launch per
-    routed expert.  `layers` copies of the expert set (2.6 GB) rotate so the
-    touched experts' bytes exceed L2.  GB/s counts the touched experts'
-    weights plus activations and outputs."""
+    matmul in one launch (the dispatcher's form, and the CUDA-core and
+    warp-MMA forms forced), against the same layer with one launch per
+    routed expert (each on the dispatcher's path for its rows).  `layers`
+    copies of the expert set (2.6 GB) rotate so the touched experts' bytes
+    exceed L2.  GB/s counts the touched experts' weights plus activations
+    and outputs."""
     from iq4_xs_quantized_gb300 import synth
     W = synth.MOE_DECODE
     w0 = torch.from_numpy(W.weights().reshape(W.G, -1)).to(dev)
@@ -725,7 +727,7 @@ def moe_grouped(torch, B, dev, layers=12, reps=5):
     ws = [w0] + [w0.clone() for _ in range(layers - 1)]
     stream = torch.cuda.Stream(device=dev)
     res = []
-    for T in W.tokens:
+    for T in tokens:
         _, rows, offsets = W.inputs(T)
         M = rows.shape[0]
         xr = torch.from_numpy(rows).to(dev)
@@ -734,10 +736,12 @@ def moe_grouped(torch, B, dev, layers=12, reps=5):
         y = torch.empty((M, W.N), dtype=torch.float32, device=dev)
         touched = [g for g in range(W.G) if offsets[g + 1] > offsets[g]]
 
-        def grouped(s):
-            for w in ws:
-                B.iq4xs_quantize_q8_1(xr, qs, ds, s)
-                B.iq4xs_matmul_grouped(w, stride, W.G, W.N, W.K, qs, ds, off, y, s)
+        def grouped(path):
+            def fn(s):
+                for w in ws:
+                    B.iq4xs_quantize_q8_1(xr, qs, ds, s)
+                    B.iq4xs_matmul_grouped(w, stride, W.G, W.N, W.K, qs, ds, off, y, s, path=path)
+            return fn
 
         def per_expert(s):
             for w in ws:
@@ -745,10 +749,11 @@ def moe_grouped(torch, B, dev, layers=12, reps=5):
                 for g in touched:
                     r0, r1 = int(offsets[g]), int(offsets[g + 1])
                     B.iq4xs_matmul(w[g], W.N, W.K, qs[r0:r1], ds[r0:r1], r1 - r0, y[r0:r1],
-                                   B.PATH_DP4A, s)
+                                   B.PATH_AUTO, s)
 
         times = {}
-        for name, fn in (("grouped", grouped), ("per_expert", per_expert)):
+        for name, fn in (("grouped", grouped("auto")), ("grouped_dp4a", grouped("dp4a")),
+                         ("grouped_mma", grouped("mma")), ("per_expert", per_expert)):
             with torch.cuda.stream(stream):
                 fn(stream)
             torch.cuda.synchronize()
@@ -767,8 +772,12 @@ def moe_grouped(torch, B, dev, layers=12, reps=5):
             del g
         nbytes = (len(touched) * W.N * (W.K // 256) * 136 + M * W.K + M * (W.K // 32) * 4
                   + 4 * M * W.N + quantize_bytes(M, W.K))
-        res.append({"tokens": T, "rows": M, "experts_touched": len(touched),
+        mean = -(-M // min(W.G, M))
+        auto = "mma" if M >= W.G or B.iq4xs_select_path(mean, W.N, W.K) != B.PATH_DP4A else "dp4a"
+        res.append({"tokens": T, "rows": M, "experts_touched": len(touched), "auto_form": auto,
                     "grouped_us_per_layer": round(times["grouped"], 3),
+                    "grouped_dp4a_us": round(times["grouped_dp4a"], 3),
+                    "grouped_mma_us": round(times["grouped_mma"], 3),
                     "per_expert_launches_us_per_layer": round(times["per_expert"], 3),
                     "grouped_GBps": round(nbytes / (times["grouped"] * 1e-6) / 1e9, 1)})
     del ws

@@ -85,7 +85,9 @@ typedef enum {
                               the requested path cannot take */
     IQ4XS_ERR_DEVICE = 4,  /* no CUDA device, or the current device is not sm_103 */
     IQ4XS_ERR_CUDA = 5,    /* a CUDA runtime/driver call or a launch failed */
-    IQ4XS_ERR_TIMEOUT = 6  /* a bounded device wait ran out (iq4xs_last_device_error) */
+    IQ4XS_ERR_TIMEOUT = 6, /* a bounded device wait ran out (iq4xs_last_device_error) */
+    IQ4XS_ERR_BOUNDS = 7   /* bounds-checked build only: a checked device access
+                              missed its buffer (iq4xs_last_device_error) */
 } iq4xs_status;
 
 typedef enum {
@@ -227,13 +229,28 @@ int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t
  *                 that many expert slots, each taking the next non-empty
  *                 expert, so empty experts cost nothing.
  *   y             fp32 [rows][ldy]; the rows of every expert are written.
- * Each expert is computed with the batch width its own row count selects,
- * so the result per expert is bit-identical to iq4xs_matmul on the DP4A
- * path over the same rows.
+ * Path: the CUDA-core (DP4A) kernel, each expert computed with the batch
+ * width its own row count selects, so the result per expert is
+ * bit-identical to iq4xs_matmul on the DP4A path over the same rows; or,
+ * when K % 512 == 0 and either total_rows >= G (at least one row per expert
+ * on average) or the mean rows per expert that has rows (total_rows /
+ * min(G, total_rows)) exceeds the DP4A crossover of one expert's matrix
+ * size, the warp-level MMA kernel in its grouped form (one CTA per (row
+ * tile, expert), the expert's rows in activation tiles of up to 32; each
+ * sub-block's dot is exact as on the MMA path of iq4xs_matmul).
  */
 int iq4xs_matmul_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
                          const int8_t* qs, const void* ds, const int32_t* row_offsets,
                          int64_t total_rows, float* y, int64_t ldy, int64_t stream);
+
+/*
+ * iq4xs_matmul_grouped with the path chosen by the caller: IQ4XS_PATH_AUTO
+ * (the rule above), IQ4XS_PATH_DP4A or IQ4XS_PATH_MMA (K % 512 == 0, else
+ * IQ4XS_ERR_SHAPE; qs 16-byte aligned); other values IQ4XS_ERR_ARG.
+ */
+int iq4xs_matmul_grouped_path(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
+                              const int8_t* qs, const void* ds, const int32_t* row_offsets,
+                              int64_t total_rows, float* y, int64_t ldy, int path, int64_t stream);
 
 /*
  * The projection as one call: y = Q8_1(x) . W^T from fp32 activations
@@ -386,6 +403,40 @@ int iq4xs_set_pdl(int enable);
  * (0x102 is a code stage's MMAs completing, which frees its slot.)
  */
 int iq4xs_last_device_error(int* code_out);
+
+/*
+ * Bounds-checked debug build (no counterpart on the source pages; stands in
+ * for a memory checker).  The same sources compiled with IQ4XS_BOUNDS_CHECK
+ * defined give libiq4xs_bounds.so, with the same entry points.  There every
+ * plain global load and store of every kernel, every TMA box origin and
+ * every shared-memory range the kernels compute at run time is checked
+ * against the extent the kernel derives from its own arguments (the sizes
+ * this header states for each buffer).  A miss skips the access (a load
+ * yields zero) and records code 0x200 + site in the device error word, so
+ * iq4xs_last_device_error returns IQ4XS_ERR_BOUNDS.  The site number says
+ * which access missed: 0x01-0x05 the quantizer (x, qs, ds, the prepared
+ * operand, its span scales); 0x10-0x11 the dequantizer (W, out); 0x20-0x25
+ * the dp4a matmul (W, qs, ds, y, row_offsets, an expert's rows outside y);
+ * 0x30-0x39 the warp-MMA matmul (W box, W box alignment, code box, code box
+ * alignment, ds, y, row_offsets, an expert's rows, shared-memory size,
+ * split-K tile); 0x40-0x49 the tcgen05 matmul (W box, W box alignment,
+ * code box, code box alignment, prepared operand, ds, y, span scales,
+ * shared-memory size, split-K slices).  A TMA box reaching past its tensor
+ * is recorded but still copied (the copy unit fills the rest); a box origin
+ * off the 16-byte grid is recorded and not copied, and that stage's bounded
+ * wait then runs out.  Results are those of the normal build whenever
+ * nothing is recorded.
+ *
+ * iq4xs_bounds_checked: *out = 1 in the checked build, 0 otherwise.
+ * iq4xs_test_bounds_margin: checked build only (IQ4XS_ERR_ARG otherwise):
+ * later launches treat the last `bytes` bytes of every global buffer as
+ * outside it (copies the kernels wait for are still made), so a test can
+ * see the checks fire on in-range accesses near a buffer's end without any
+ * access leaving its buffer.  0 restores the exact extents.  Synchronizes
+ * the current device.
+ */
+int iq4xs_bounds_checked(int* out);
+int iq4xs_test_bounds_margin(int64_t bytes);
 
 /*
  * Test hook for the bounded waits (no counterpart on the source pages): the

@@ -16,9 +16,10 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libiq4xs.so")
+BOUNDS_LIB_PATH = os.path.join(_HERE, "libiq4xs_bounds.so")  # the bounds-checked debug build
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "iq4xs.h")
 
-OK, ERR_ARG, ERR_ALIGN, ERR_SHAPE, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT = range(7)
+OK, ERR_ARG, ERR_ALIGN, ERR_SHAPE, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_BOUNDS = range(8)
 PATH_AUTO, PATH_DP4A, PATH_TC, PATH_BASELINE, PATH_MMA = 0, 1, 2, 3, 4
 PATHS = {"auto": PATH_AUTO, "dp4a": PATH_DP4A, "tc": PATH_TC, "mma": PATH_MMA}
 WTYPE_IQ4_XS, WTYPE_Q4_0, WTYPE_IQ4_NL = 0, 1, 2
@@ -66,6 +67,7 @@ def load(path: str | None = None):
         lib.iq4xs_weight_bytes.argtypes = [ci, i64, i64]
         lib.iq4xs_weight_bytes.restype = i64
         lib.iq4xs_matmul_grouped.argtypes = [vp, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, i64]
+        lib.iq4xs_matmul_grouped_path.argtypes = [vp, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, ci, i64]
         lib.iq4xs_linear.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, i64]
         lib.iq4xs_linear_workspace_bytes.argtypes = [i64, i64, i64]
         lib.iq4xs_linear_workspace_bytes.restype = i64
@@ -84,21 +86,34 @@ def load(path: str | None = None):
         lib.iq4xs_set_pdl.restype = ci
         lib.iq4xs_last_device_error.argtypes = [ctypes.POINTER(ci)]
         lib.iq4xs_test_skip_w_stage.argtypes = [i64]
+        lib.iq4xs_bounds_checked.argtypes = [ctypes.POINTER(ci)]
+        lib.iq4xs_test_bounds_margin.argtypes = [i64]
         lib.iq4xs_status_string.argtypes = [ci]
         lib.iq4xs_status_string.restype = ctypes.c_char_p
-        for name in ("iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_matmul_grouped",
+        for name in ("iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_matmul_grouped", "iq4xs_matmul_grouped_path",
                      "iq4xs_dequantize", "iq4xs_linear", "iq4xs_matmul_wt", "iq4xs_dequantize_wt",
                      "iq4xs_select_path", "iq4xs_set_crossover", "iq4xs_set_baseline_threshold",
                      "iq4xs_set_crossover_classes", "iq4xs_test_skip_w_stage",
                      "iq4xs_set_mma_crossover", "iq4xs_set_mma_crossover_classes",
                      "iq4xs_test_mma_config",
                      "iq4xs_quantize_q8_1_tc", "iq4xs_matmul_tc_operand",
-                     "iq4xs_last_device_error"):
+                     "iq4xs_last_device_error", "iq4xs_bounds_checked", "iq4xs_test_bounds_margin"):
             getattr(lib, name).restype = ci
         if path is None:
             _lib = lib
             _install_calibration(lib)
         return lib
+
+
+def use(path: str | None = None):
+    """Route every call of this module through the library at ``path`` (None:
+    the default build), e.g. the bounds-checked build; returns it."""
+    global _lib
+    lib = load(path or LIB_PATH)
+    with _lock:
+        _lib = lib
+    _install_calibration(lib)
+    return lib
 
 
 def _install_calibration(lib):
@@ -247,17 +262,20 @@ def iq4xs_linear_static_max_bytes() -> int:
 
 
 def iq4xs_matmul_grouped(w, expert_stride: int, G: int, N: int, K: int, qs, ds, row_offsets, y,
-                         stream=None) -> None:
+                         stream=None, path=PATH_AUTO) -> None:
     """Mixture-of-experts matmul in one launch: expert g (W at byte
     g * expert_stride of w) over the Q8_1 rows [row_offsets[g],
     row_offsets[g+1]) (row_offsets: int32 device tensor [G+1]); y holds
-    every row (its row count bounds the number of non-empty experts)."""
+    every row (its row count bounds the number of non-empty experts).
+    path: AUTO, DP4A or MMA (iq4xs_matmul_grouped_path)."""
     if row_offsets.dtype != torch.int32:
         raise TypeError("row_offsets must be int32")
-    rc = load().iq4xs_matmul_grouped(_ptr(w), int(expert_stride), G, N, K, _ptr(qs), _ptr(ds),
-                                     _ptr(row_offsets), y.shape[0], _ptr(y), y.stride(0),
-                                     _stream(stream))
-    _check("iq4xs_matmul_grouped", rc)
+    if isinstance(path, str):
+        path = PATHS[path]
+    rc = load().iq4xs_matmul_grouped_path(_ptr(w), int(expert_stride), G, N, K, _ptr(qs), _ptr(ds),
+                                          _ptr(row_offsets), y.shape[0], _ptr(y), y.stride(0), int(path),
+                                          _stream(stream))
+    _check("iq4xs_matmul_grouped_path", rc)
 
 
 def iq4xs_dequantize(w, N: int, K: int, out, stream=None) -> None:
@@ -313,13 +331,24 @@ def iq4xs_set_pdl(enable: bool) -> None:
 
 
 def iq4xs_last_device_error() -> int:
-    """The device error word (0 = clean), read and cleared; a timeout code
-    (status IQ4XS_ERR_TIMEOUT) is returned, not raised."""
+    """The device error word (0 = clean), read and cleared; a timeout or
+    bounds code (status IQ4XS_ERR_TIMEOUT / IQ4XS_ERR_BOUNDS) is returned,
+    not raised."""
     out = ctypes.c_int(-1)
     rc = load().iq4xs_last_device_error(ctypes.byref(out))
-    if rc != ERR_TIMEOUT:
+    if rc not in (ERR_TIMEOUT, ERR_BOUNDS):
         _check("iq4xs_last_device_error", rc)
     return out.value
+
+
+def iq4xs_bounds_checked() -> bool:
+    out = ctypes.c_int(-1)
+    _check("iq4xs_bounds_checked", load().iq4xs_bounds_checked(ctypes.byref(out)))
+    return out.value == 1
+
+
+def iq4xs_test_bounds_margin(nbytes: int) -> None:
+    _check("iq4xs_test_bounds_margin", load().iq4xs_test_bounds_margin(int(nbytes)))
 
 
 def iq4xs_test_skip_w_stage(stage: int) -> None:

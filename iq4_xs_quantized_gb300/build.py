@@ -4,6 +4,12 @@ Each translation unit under ``csrc/`` is compiled in parallel with
 ``-gencode arch=compute_103a,code=sm_103a -lineinfo -O3`` and linked into
 ``iq4_xs_quantized_gb300/libiq4xs.so`` against the shared CUDA runtime.  The
 library is rebuilt only when a source or header is newer than it.
+
+``build(bounds_check=True)`` compiles the same sources with
+``-DIQ4XS_BOUNDS_CHECK`` into ``libiq4xs_bounds.so`` (objects under
+``_build_bounds/``): the debug build whose kernels check every global access,
+TMA box origin and computed shared-memory range against its buffer and record
+misses in the device error word.
 """
 from __future__ import annotations
 
@@ -19,6 +25,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libiq4xs.so")
+BOUNDS_LIB = os.path.join(PKG, "libiq4xs_bounds.so")
+BOUNDS_BUILD = os.path.join(PKG, "_build_bounds")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fPIC", "-Xptxas", "-warn-spills"]
@@ -40,15 +48,15 @@ def _deps():
         os.path.join(ROOT, "include", "iq4xs.h"), os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def _compile(src: str, extra) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, extra, build_dir: str) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     cmd = [nvcc_path(), *ARCH, *NVCC_FLAGS, *extra, "-I", os.path.join(ROOT, "include"),
            "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -59,23 +67,28 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile and link the library; return its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, bounds_check: bool = False) -> str:
+    """Compile and link the library (the bounds-checked one with
+    ``bounds_check``); return its path."""
+    lib, build_dir = (BOUNDS_LIB, BOUNDS_BUILD) if bounds_check else (LIB, BUILD)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    if bounds_check:
+        extra += ["-DIQ4XS_BOUNDS_CHECK"]
     srcs = sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, build_dir), srcs))
+    tmp = lib + ".tmp"
     cmd = [nvcc_path(), *ARCH, "-shared", "-cudart", "shared", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv,
+                bounds_check="--bounds" in sys.argv))

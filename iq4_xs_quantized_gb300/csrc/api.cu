@@ -11,8 +11,10 @@
 
 namespace iq4xs {
 
-// Device error word: kernels whose bounded waits run out record a code here.
-__device__ int g_device_error = 0;
+// Device error word: kernels whose bounded waits run out (and, in the
+// bounds-checked build, checked accesses that miss their buffer) record a
+// code in word 0; words 2-3 hold the bounds-checked build's test margin.
+__device__ __align__(16) int g_device_error[kErrWords] = {0, 0, 0, 0};
 
 namespace {
 
@@ -23,7 +25,7 @@ struct DevState {
     bool ready = false;
     int status = IQ4XS_OK;
     int num_sms = 0;
-    int* err = nullptr;       // device address of g_device_error
+    int* err = nullptr;       // device address of g_device_error (kErrWords ints)
     void* encode = nullptr;   // cuTensorMapEncodeTiled
 };
 
@@ -154,7 +156,7 @@ int iq4xs_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx, int8_
     int rc = device_state(&st);
     if (rc) return rc;
     return from_cuda(
-        launch_quantize_q8_1(x, M, K, ldx, qs, ds, nullptr, reinterpret_cast<cudaStream_t>(stream)));
+        launch_quantize_q8_1(x, M, K, ldx, qs, ds, nullptr, st->err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int64_t iq4xs_tc_operand_bytes(int64_t M, int64_t K) {
@@ -172,7 +174,7 @@ int iq4xs_quantize_q8_1_tc(const float* x, int64_t M, int64_t K, int64_t ldx, in
     DevState* st;
     int rc = device_state(&st);
     if (rc) return rc;
-    return from_cuda(launch_quantize_q8_1(x, M, K, ldx, qs, ds, tc_operand,
+    return from_cuda(launch_quantize_q8_1(x, M, K, ldx, qs, ds, tc_operand, st->err,
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -208,7 +210,7 @@ int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t
     if (path == IQ4XS_PATH_TC)
         return from_cuda(launch_matmul_tc(w, wtype, N, K, qs, ds, nullptr, M, y, ldy, st->encode,
                                           st->err, st->num_sms, g_skip_w_stage.exchange(-1), s));
-    return from_cuda(launch_matmul_dp4a(w, wtype, N, K, qs, ds, M, y, ldy, st->num_sms, s));
+    return from_cuda(launch_matmul_dp4a(w, wtype, N, K, qs, ds, M, y, ldy, st->err, st->num_sms, s));
 }
 
 int iq4xs_matmul_tc_operand(const void* w, int wtype, int64_t N, int64_t K, const void* tc_operand,
@@ -283,7 +285,15 @@ int iq4xs_linear(const void* w, int64_t N, int64_t K, const float* x, int64_t M,
 int iq4xs_matmul_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
                          const int8_t* qs, const void* ds, const int32_t* row_offsets,
                          int64_t total_rows, float* y, int64_t ldy, int64_t stream) {
+    return iq4xs_matmul_grouped_path(w, expert_stride, G, N, K, qs, ds, row_offsets, total_rows, y, ldy,
+                                     IQ4XS_PATH_AUTO, stream);
+}
+
+int iq4xs_matmul_grouped_path(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
+                              const int8_t* qs, const void* ds, const int32_t* row_offsets,
+                              int64_t total_rows, float* y, int64_t ldy, int path, int64_t stream) {
     if (!w || !qs || !ds || !row_offsets || !y) return IQ4XS_ERR_ARG;
+    if (path != IQ4XS_PATH_AUTO && path != IQ4XS_PATH_DP4A && path != IQ4XS_PATH_MMA) return IQ4XS_ERR_ARG;
     if (G < 1 || G > 65535 || N < 1 || N > (1 << 30) || K <= 0 || K % kQK || K > (1 << 30))
         return IQ4XS_ERR_SHAPE;
     if (ldy < N || total_rows < 1) return IQ4XS_ERR_ARG;
@@ -291,12 +301,26 @@ int iq4xs_matmul_grouped(const void* w, int64_t expert_stride, int64_t G, int64_
     if (!aligned(w, 16) || !aligned(qs, 16) || !aligned(ds, 4) || !aligned(row_offsets, 4) ||
         !aligned(y, 4))
         return IQ4XS_ERR_ALIGN;
+    if (path == IQ4XS_PATH_AUTO) {
+        // The warp-MMA form once there are at least as many rows as experts
+        // (measured on a 128 x 1536 x 2048 layer: from 128 rows on; at 512
+        // rows it takes half the time of the CUDA-core form), or once the
+        // mean rows of an expert slot leave one expert matrix's DP4A range.
+        const int64_t slots = G < total_rows ? G : total_rows;
+        const int64_t mean = (total_rows + slots - 1) / slots;
+        path = (K % kPairK == 0 && (total_rows >= G || mean > crossover_for(N, K))) ? IQ4XS_PATH_MMA
+                                                                                   : IQ4XS_PATH_DP4A;
+    }
+    if (path == IQ4XS_PATH_MMA && K % kPairK) return IQ4XS_ERR_SHAPE;
     DevState* st;
     int rc = device_state(&st);
     if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (path == IQ4XS_PATH_MMA)
+        return from_cuda(launch_matmul_mma_grouped(w, expert_stride, G, N, K, qs, ds, row_offsets, total_rows,
+                                                   y, ldy, st->encode, st->err, st->num_sms, s));
     return from_cuda(launch_matmul_dp4a_grouped(w, expert_stride, G, N, K, qs, ds, row_offsets,
-                                                total_rows, y, ldy,
-                                                reinterpret_cast<cudaStream_t>(stream)));
+                                                total_rows, y, ldy, st->err, s));
 }
 
 int iq4xs_dequantize(const void* w, int64_t N, int64_t K, void* out, int out_dtype,
@@ -314,7 +338,7 @@ int iq4xs_dequantize_wt(const void* w, int wtype, int64_t N, int64_t K, void* ou
     DevState* st;
     int rc = device_state(&st);
     if (rc) return rc;
-    return from_cuda(launch_dequantize(w, wtype, N, K, out, out_dtype,
+    return from_cuda(launch_dequantize(w, wtype, N, K, out, out_dtype, st->err,
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -367,10 +391,27 @@ int iq4xs_last_device_error(int* code_out) {
         cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess)
         return IQ4XS_ERR_CUDA;
     const int c = *code_out;
+    if (c >= kDevErrBounds && c < kDevErrBounds + 0x100) return IQ4XS_ERR_BOUNDS;
     return ((c >= kDevErrTimeoutW && c <= kDevErrTimeoutX) || c == kDevErrTimeoutMmaStage ||
             c == kDevErrTimeoutMmaSlot)
                ? IQ4XS_ERR_TIMEOUT
                : IQ4XS_OK;
+}
+
+int iq4xs_bounds_checked(int* out) {
+    if (!out) return IQ4XS_ERR_ARG;
+    *out = kBoundsCheck ? 1 : 0;
+    return IQ4XS_OK;
+}
+
+int iq4xs_test_bounds_margin(int64_t bytes) {
+    if (!kBoundsCheck || bytes < 0 || bytes > (int64_t(1) << 40)) return IQ4XS_ERR_ARG;
+    DevState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    if (cudaDeviceSynchronize() != cudaSuccess) return IQ4XS_ERR_CUDA;
+    const long long v = bytes;
+    return from_cuda(cudaMemcpyToSymbol(g_device_error, &v, sizeof(v), 2 * sizeof(int)));
 }
 
 int iq4xs_test_skip_w_stage(int64_t stage) {
@@ -383,7 +424,7 @@ int iq4xs_test_mma_config(int64_t rows_per_cta, int64_t k_splits, int64_t ctas_p
     if (rows_per_cta < 0 || rows_per_cta > 256 || rows_per_cta % 32 || k_splits < 0 || k_splits > 8 ||
         ctas_per_sm < 0 || ctas_per_sm > 2)
         return IQ4XS_ERR_ARG;
-    mma_force_config((int)(rows_per_cta / 32), (int)k_splits, (int)ctas_per_sm);
+    mma_force_config((int)rows_per_cta, (int)k_splits, (int)ctas_per_sm);
     return IQ4XS_OK;
 }
 
@@ -396,6 +437,7 @@ const char* iq4xs_status_string(int status) {
         case IQ4XS_ERR_DEVICE: return "no sm_103 device";
         case IQ4XS_ERR_CUDA: return "CUDA error";
         case IQ4XS_ERR_TIMEOUT: return "device wait timed out";
+        case IQ4XS_ERR_BOUNDS: return "checked device access out of bounds";
         default: return "unknown status";
     }
 }

@@ -210,7 +210,109 @@ enum DeviceError : int {
     kDevErrLayout = 0x10A,  // dynamic shared memory not 1024-byte aligned
     kDevErrTimeoutMmaStage = 0x10B,  // warp-MMA matmul: a stage (W and codes) never landed
     kDevErrTimeoutMmaSlot = 0x10C,   // warp-MMA matmul: a stage slot was never freed
+    kDevErrBounds = 0x200,           // + BoundsSite: a checked access missed its buffer
 };
+
+// ---------------------------------------------------------------------------
+// Bounds-checked debug build (compiled with -DIQ4XS_BOUNDS_CHECK into a
+// library of its own).  Every plain global access of a kernel, every TMA box
+// origin and every computed shared-memory offset is checked against the
+// extent the kernel derives from its own arguments.  A miss records
+// kDevErrBounds + site in the device error word (the first code recorded
+// sticks) and skips the access: a load yields zero, a store is dropped.  A
+// TMA box origin outside its tensor is recorded only (the copy unit fills
+// such boxes itself); an innermost coordinate off the 16-byte grid is
+// recorded and its copy skipped (the stage's bounded wait then runs out
+// instead of the copy faulting).  The 8 bytes at word 2 of the error array
+// hold a margin subtracted from every global extent, so that in-range
+// accesses within that many bytes of a buffer's end are reported although no
+// access leaves the buffer.  In the normal build every check is the constant
+// true and compiles away.
+// ---------------------------------------------------------------------------
+enum BoundsSite : int {
+    kBcQuantX = 1, kBcQuantQs, kBcQuantDs, kBcQuantOp, kBcQuantSpan,
+    kBcDqW = 0x10, kBcDqOut,
+    kBcDp4aW = 0x20, kBcDp4aQs, kBcDp4aDs, kBcDp4aY, kBcDp4aOffsets, kBcDp4aRows,
+    kBcMmaW = 0x30, kBcMmaWAlign, kBcMmaQ, kBcMmaQAlign, kBcMmaDs, kBcMmaY, kBcMmaOffsets,
+    kBcMmaRows, kBcMmaSmem, kBcMmaSplit,
+    kBcTcW = 0x40, kBcTcWAlign, kBcTcQ, kBcTcQAlign, kBcTcOp, kBcTcDs, kBcTcY, kBcTcSpan,
+    kBcTcSmem, kBcTcRecv,
+};
+#ifdef IQ4XS_BOUNDS_CHECK
+constexpr bool kBoundsCheck = true;
+#else
+constexpr bool kBoundsCheck = false;
+#endif
+constexpr int kErrWords = 4;  // error code, spare, 64-bit margin (bounds-checked build)
+
+struct Bc {
+    int* err;
+    int64_t margin;
+};
+__device__ __forceinline__ Bc bc_open(int* err) {
+    if constexpr (kBoundsCheck) {
+        return {err, err ? (int64_t)*reinterpret_cast<const volatile long long*>(err + 2) : 0};
+    } else {
+        return {nullptr, 0};
+    }
+}
+__device__ __forceinline__ bool bc_fail(const Bc& bc, int site) {
+    if (bc.err) atomicCAS(bc.err, 0, kDevErrBounds + site);
+    return false;
+}
+// [p, p + n) inside [base, base + extent - margin).
+__device__ __forceinline__ bool bc_global(const Bc& bc, const void* p, int64_t n, const void* base,
+                                          int64_t extent, int site) {
+    if constexpr (!kBoundsCheck) {
+        return true;
+    } else {
+        const int64_t off = reinterpret_cast<const char*>(p) - reinterpret_cast<const char*>(base);
+        return (off >= 0 && n >= 0 && off + n <= extent - bc.margin) ? true : bc_fail(bc, site);
+    }
+}
+// A global range an asynchronous copy reads (a bulk copy the kernel then
+// waits for): false (skip the copy) only if it leaves the buffer itself; a
+// range inside the buffer but within the margin of its end is recorded and
+// still copied, so that no wait depends on the margin.
+__device__ __forceinline__ bool bc_global_async(const Bc& bc, const void* p, int64_t n, const void* base,
+                                                int64_t extent, int site) {
+    if constexpr (!kBoundsCheck) {
+        return true;
+    } else {
+        const int64_t off = reinterpret_cast<const char*>(p) - reinterpret_cast<const char*>(base);
+        if (off < 0 || n < 0 || off + n > extent) return bc_fail(bc, site);
+        if (off + n > extent - bc.margin) bc_fail(bc, site);
+        return true;
+    }
+}
+// A TMA box origin: its innermost coordinate x (elements of `elem` bytes)
+// on the 16-byte grid (false: skip the copy), and the box [x, x + box_x) x
+// rows [y, y + 1) inside the tensor's [0, dim_x) x [0, dim_y) (recorded only:
+// the copy unit fills what lies outside).
+__device__ __forceinline__ bool bc_tma(const Bc& bc, int64_t x, int elem, int64_t box_x, int64_t dim_x,
+                                       int64_t y, int64_t dim_y, int site_align, int site_range) {
+    if constexpr (!kBoundsCheck) {
+        return true;
+    } else {
+        if ((x * elem) % 16 != 0) return bc_fail(bc, site_align);
+        if (x < 0 || x + box_x > dim_x || y < 0 || y >= dim_y) bc_fail(bc, site_range);
+        return true;
+    }
+}
+// 0 <= i and i + n <= limit (offsets in shared memory, tensor coordinates).
+__device__ __forceinline__ bool bc_range(const Bc& bc, int64_t i, int64_t n, int64_t limit, int site) {
+    if constexpr (!kBoundsCheck) {
+        return true;
+    } else {
+        return (i >= 0 && n >= 0 && i + n <= limit) ? true : bc_fail(bc, site);
+    }
+}
+// Bytes of dynamic shared memory this CTA was launched with.
+__device__ __forceinline__ uint32_t dyn_smem_bytes() {
+    uint32_t v;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
+    return v;
+}
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: waits for a copy to land
 // Limits by what is awaited, so that the wait at the root of a stall runs out
 // first and its code is the one recorded: a copy landing (W or code stage)
@@ -352,6 +454,20 @@ __device__ __forceinline__ void wt_load_sub(const uint8_t* row, int64_t s, uint3
 #pragma unroll
         for (int k = 0; k < 5; ++k) raw[k] = __ldg(a + k);
         raw[5] = 0;
+    }
+}
+// Bounds-checked build: the bytes wt_load_sub reads for sub-block s of
+// `row` lie inside the weight buffer [base, base + extent).
+template <int WT>
+__device__ __forceinline__ bool wt_sub_in_bounds(const Bc& bc, const uint8_t* row, int64_t s,
+                                                 const void* base, int64_t extent, int site) {
+    if constexpr (WT == kWtIQ4XS) {
+        const uint8_t* blk = row + (s / kSubPerBlock) * kBlockBytes;
+        const int j = (int)(s % kSubPerBlock);
+        return bc_global(bc, blk, 8, base, extent, site) &&
+               bc_global(bc, blk + 8 + 16 * j, 16, base, extent, site);
+    } else {
+        return bc_global(bc, row + kB18Bytes * s - 2 * (s & 1), 20, base, extent, site);
     }
 }
 template <int WT>
@@ -881,21 +997,23 @@ __host__ __device__ constexpr uint32_t idesc_f16_m128(int n) {
 struct DevCtx;  // per-device state kept by api.cu
 
 // tc_operand: NULL, or where to write the prepared tensor-core operand too.
+// err: the device error word (kErrWords ints); kernels of the bounds-checked
+// build record misses there.
 cudaError_t launch_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs,
-                                 void* ds, void* tc_operand, cudaStream_t stream);
+                                 void* ds, void* tc_operand, int* err, cudaStream_t stream);
 cudaError_t launch_dequantize(const void* w, int wt, int64_t N, int64_t K, void* out,
-                              int out_dtype, cudaStream_t stream);
+                              int out_dtype, int* err, cudaStream_t stream);
 // num_sms picks the launch shape (grids of more than two CTAs per SM run
 // with more resident CTAs).
 cudaError_t launch_matmul_dp4a(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,
-                               const void* ds, int64_t M, float* y, int64_t ldy, int num_sms,
-                               cudaStream_t stream);
+                               const void* ds, int64_t M, float* y, int64_t ldy, int* err,
+                               int num_sms, cudaStream_t stream);
 // G experts in one launch: expert g has W at w + g * expert_stride and the
 // Q8_1 / output rows [row_offsets[g], row_offsets[g+1]) (device array).
 cudaError_t launch_matmul_dp4a_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N,
                                        int64_t K, const int8_t* qs, const void* ds,
                                        const int32_t* row_offsets, int64_t total_rows, float* y,
-                                       int64_t ldy, cudaStream_t stream);
+                                       int64_t ldy, int* err, cudaStream_t stream);
 // Programmatic dependent launch on (default) or off for every launch.
 bool pdl_enabled();
 // `encode` is the driver's cuTensorMapEncodeTiled; `err` the device error word.
@@ -907,10 +1025,16 @@ bool pdl_enabled();
 // rows (8, 16, 24 or 32); any K % 256 == 0; qs 16-byte aligned (staged by
 // TMA), ds read directly.
 int mma_tile_rows(int64_t M);
-// Test override of the warp-MMA launch: 16-row weight fragments per consumer
-// warp (rows per CTA = 32 x that), K splits and CTAs per SM (1, 2); 0 = the
-// launch model's choice.
-void mma_force_config(int frags_per_warp, int k_splits, int ctas_per_sm);
+// The grouped (mixture-of-experts) form of the warp-MMA path: expert g's W at
+// w + g * expert_stride (a multiple of 16), its rows [row_offsets[g],
+// row_offsets[g+1]) of qs / ds / y; K % 512 == 0.
+cudaError_t launch_matmul_mma_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
+                                      const int8_t* qs, const void* ds, const int32_t* row_offsets,
+                                      int64_t total_rows, float* y, int64_t ldy, void* encode, int* err,
+                                      int num_sms, cudaStream_t stream);
+// Test override of the warp-MMA launch: weight rows per CTA, K splits and
+// CTAs per SM (1, 2); 0 = the launch model's choice.
+void mma_force_config(int rows_per_cta, int k_splits, int ctas_per_sm);
 cudaError_t launch_matmul_mma(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds, int64_t M,
                               float* y, int64_t ldy, void* encode, int* err, int num_sms, cudaStream_t stream);
 cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,

@@ -46,15 +46,18 @@ __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
 
 // Rows [0, M) of x against the warp's kRows weight rows n0.. of W (format
 // WT), MC activation rows per pass.  `waited`: the wait for the preceding
-// grid (which wrote the activations) has been done already.
+// grid (which wrote the activations) has been done already.  The buffers'
+// extents (checked in the bounds-checked build) follow from N, K, M, ldy.
 template <int MC, int WT, int kIters>
 __device__ __forceinline__ void dp4a_rows(const uint8_t* __restrict__ w, int64_t N, int64_t K,
                                           const int8_t* __restrict__ qs,
                                           const __half2* __restrict__ ds, int64_t M,
                                           float* __restrict__ y, int64_t ldy, int64_t n0, int lane,
-                                          bool waited) {
+                                          bool waited, const Bc& bc) {
     const int64_t nsub = K / kSub;
     const int64_t row_bytes = wt_row_bytes(WT, K);
+    const int64_t w_ext = N * row_bytes, qs_ext = M * K, ds_ext = M * nsub * 4;
+    const int64_t y_ext = ((M - 1) * ldy + N) * 4;
     for (int64_t m0 = 0; m0 < M; m0 += MC) {
         float acc[kRows][MC];
 #pragma unroll
@@ -70,7 +73,8 @@ __device__ __forceinline__ void dp4a_rows(const uint8_t* __restrict__ w, int64_t
                 const int64_t s = sb + lane + 32 * it;
 #pragma unroll
                 for (int r = 0; r < kRows; ++r) {
-                    if (s < nsub && n0 + r < N) {
+                    if (s < nsub && n0 + r < N &&
+                        wt_sub_in_bounds<WT>(bc, w + (n0 + r) * row_bytes, s, w, w_ext, kBcDp4aW)) {
                         wt_load_sub<WT>(w + (n0 + r) * row_bytes, s, raw[it][r]);
                     } else {
 #pragma unroll
@@ -92,7 +96,9 @@ __device__ __forceinline__ void dp4a_rows(const uint8_t* __restrict__ w, int64_t
                 const int64_t s = sb + lane + 32 * it;
 #pragma unroll
                 for (int mi = 0; mi < MC; ++mi) {
-                    if (s < nsub && m0 + mi < M) {
+                    if (s < nsub && m0 + mi < M &&
+                        bc_global(bc, qs + (m0 + mi) * K + s * kSub, kSub, qs, qs_ext, kBcDp4aQs) &&
+                        bc_global(bc, ds + (m0 + mi) * nsub + s, 4, ds, ds_ext, kBcDp4aDs)) {
                         const uint4* qp = reinterpret_cast<const uint4*>(qs + (m0 + mi) * K + s * kSub);
                         qa[mi][0] = __ldg(qp);
                         qa[mi][1] = __ldg(qp + 1);
@@ -152,7 +158,8 @@ __device__ __forceinline__ void dp4a_rows(const uint8_t* __restrict__ w, int64_t
         for (int r = 0; r < kRows; ++r)
 #pragma unroll
             for (int mi = 0; mi < MC; ++mi)
-                if (lane == r * MC + mi && n0 + r < N && m0 + mi < M)
+                if (lane == r * MC + mi && n0 + r < N && m0 + mi < M &&
+                    bc_global(bc, y + (m0 + mi) * ldy + n0 + r, 4, y, y_ext, kBcDp4aY))
                     y[(m0 + mi) * ldy + n0 + r] = acc[r][mi];
     }
 }
@@ -161,12 +168,13 @@ template <int MC, int WT, int S>  // activation rows per pass, weight format, la
 __global__ void __launch_bounds__(kDp4aThreads, ctas_per_sm<MC, S>())
     matmul_dp4a_kernel(const uint8_t* __restrict__ w, int64_t N, int64_t K,
                        const int8_t* __restrict__ qs, const __half2* __restrict__ ds, int64_t M,
-                       float* __restrict__ y, int64_t ldy) {
+                       float* __restrict__ y, int64_t ldy, int* err) {
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t n0 = ((int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)) * kRows;
     if (n0 >= N) return;  // whole warp
-    dp4a_rows<MC, WT, iters_for<MC, S>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, false);
+    const Bc bc = bc_open(err);
+    dp4a_rows<MC, WT, iters_for<MC, S>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, false, bc);
 }
 
 // Grouped (mixture-of-experts) form: G experts, expert g with its own W at
@@ -187,11 +195,12 @@ __global__ void __launch_bounds__(kDp4aThreads, kNarrow ? 3 : 2)
     matmul_dp4a_grouped_kernel(const uint8_t* __restrict__ w, int64_t expert_stride, int64_t G,
                                int64_t N, int64_t K, const int8_t* __restrict__ qs,
                                const __half2* __restrict__ ds, const int32_t* __restrict__ row_offsets,
-                               float* __restrict__ y, int64_t ldy) {
+                               int64_t total_rows, float* __restrict__ y, int64_t ldy, int* err) {
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t n0 = ((int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)) * kRows;
     if (n0 >= N) return;  // whole warp
+    const Bc bc = bc_open(err);
     griddep_wait();
     // The k-th non-empty expert: the offsets of 128 experts are loaded at
     // once (independent loads), then a ballot per 32 of them.
@@ -202,8 +211,9 @@ __global__ void __launch_bounds__(kDp4aThreads, kNarrow ? 3 : 2)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int64_t e = base + 32 * j + lane;
-            lo[j] = e < G ? __ldg(row_offsets + e) : 0;
-            hi[j] = e < G ? __ldg(row_offsets + e + 1) : 0;
+            const bool in = e < G && bc_global(bc, row_offsets + e, 8, row_offsets, (G + 1) * 4, kBcDp4aOffsets);
+            lo[j] = in ? __ldg(row_offsets + e) : 0;
+            hi[j] = in ? __ldg(row_offsets + e + 1) : 0;
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -217,19 +227,20 @@ __global__ void __launch_bounds__(kDp4aThreads, kNarrow ? 3 : 2)
     }
     if (g < 0) return;  // fewer non-empty experts than slots (whole warp)
     const int64_t r0 = row_offsets[g], M = row_offsets[g + 1] - r0;
+    if (!bc_range(bc, r0, M, total_rows, kBcDp4aRows)) return;  // offsets outside the rows of y
     w += g * expert_stride;
     qs += r0 * K;
     ds += r0 * (K / kSub);
     y += r0 * ldy;
     constexpr int X = kWtIQ4XS;
     if constexpr (kNarrow) {
-        if (M == 1) dp4a_rows<1, X, iters_for<1, 1>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
-        else dp4a_rows<2, X, iters_for<2, 1>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+        if (M == 1) dp4a_rows<1, X, iters_for<1, 1>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true, bc);
+        else dp4a_rows<2, X, iters_for<2, 1>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true, bc);
     } else {
-        if (M == 1) dp4a_rows<1, X, iters_for<1, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
-        else if (M == 2) dp4a_rows<2, X, iters_for<2, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
-        else if (M <= 4) dp4a_rows<4, X, iters_for<4, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
-        else dp4a_rows<8, X, iters_for<8, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true);
+        if (M == 1) dp4a_rows<1, X, iters_for<1, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true, bc);
+        else if (M == 2) dp4a_rows<2, X, iters_for<2, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true, bc);
+        else if (M <= 4) dp4a_rows<4, X, iters_for<4, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true, bc);
+        else dp4a_rows<8, X, iters_for<8, 0>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true, bc);
     }
 }
 
@@ -249,7 +260,7 @@ cudaLaunchConfig_t dp4a_config(int64_t N, unsigned slots, cudaStream_t stream,
 
 template <int MC, int WT>
 cudaError_t launch_mc(const uint8_t* w, int64_t N, int64_t K, const int8_t* qs, const __half2* ds,
-                      int64_t M, float* y, int64_t ldy, int num_sms, cudaStream_t stream) {
+                      int64_t M, float* y, int64_t ldy, int* err, int num_sms, cudaStream_t stream) {
     static_assert(kRows * MC <= 32, "one output per lane");
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = dp4a_config(N, 1, stream, attr);
@@ -257,33 +268,33 @@ cudaError_t launch_mc(const uint8_t* w, int64_t N, int64_t K, const int8_t* qs, 
     const int shape = G <= 2 * sms ? 0 : (G <= 3 * sms ? 1 : 2);
     if constexpr (max_shape<MC>() >= 2)
         if (shape >= 2)
-            return cudaLaunchKernelEx(&cfg, matmul_dp4a_kernel<MC, WT, 2>, w, N, K, qs, ds, M, y, ldy);
+            return cudaLaunchKernelEx(&cfg, matmul_dp4a_kernel<MC, WT, 2>, w, N, K, qs, ds, M, y, ldy, err);
     if constexpr (max_shape<MC>() >= 1)
         if (shape >= 1)
-            return cudaLaunchKernelEx(&cfg, matmul_dp4a_kernel<MC, WT, 1>, w, N, K, qs, ds, M, y, ldy);
-    return cudaLaunchKernelEx(&cfg, matmul_dp4a_kernel<MC, WT, 0>, w, N, K, qs, ds, M, y, ldy);
+            return cudaLaunchKernelEx(&cfg, matmul_dp4a_kernel<MC, WT, 1>, w, N, K, qs, ds, M, y, ldy, err);
+    return cudaLaunchKernelEx(&cfg, matmul_dp4a_kernel<MC, WT, 0>, w, N, K, qs, ds, M, y, ldy, err);
 }
 
 template <int WT>
 cudaError_t launch_wt(const uint8_t* w, int64_t N, int64_t K, const int8_t* qs, const __half2* ds,
-                      int64_t M, float* y, int64_t ldy, int num_sms, cudaStream_t stream) {
-    if (M == 1) return launch_mc<1, WT>(w, N, K, qs, ds, M, y, ldy, num_sms, stream);
-    if (M == 2) return launch_mc<2, WT>(w, N, K, qs, ds, M, y, ldy, num_sms, stream);
-    if (M <= 4) return launch_mc<4, WT>(w, N, K, qs, ds, M, y, ldy, num_sms, stream);
-    return launch_mc<8, WT>(w, N, K, qs, ds, M, y, ldy, num_sms, stream);
+                      int64_t M, float* y, int64_t ldy, int* err, int num_sms, cudaStream_t stream) {
+    if (M == 1) return launch_mc<1, WT>(w, N, K, qs, ds, M, y, ldy, err, num_sms, stream);
+    if (M == 2) return launch_mc<2, WT>(w, N, K, qs, ds, M, y, ldy, err, num_sms, stream);
+    if (M <= 4) return launch_mc<4, WT>(w, N, K, qs, ds, M, y, ldy, err, num_sms, stream);
+    return launch_mc<8, WT>(w, N, K, qs, ds, M, y, ldy, err, num_sms, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_matmul_dp4a(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,
-                               const void* ds, int64_t M, float* y, int64_t ldy, int num_sms,
-                               cudaStream_t stream) {
+                               const void* ds, int64_t M, float* y, int64_t ldy, int* err,
+                               int num_sms, cudaStream_t stream) {
     const uint8_t* wb = reinterpret_cast<const uint8_t*>(w);
     const __half2* d2 = reinterpret_cast<const __half2*>(ds);
     switch (wt) {
-        case kWtIQ4XS: return launch_wt<kWtIQ4XS>(wb, N, K, qs, d2, M, y, ldy, num_sms, stream);
-        case kWtQ4_0: return launch_wt<kWtQ4_0>(wb, N, K, qs, d2, M, y, ldy, num_sms, stream);
-        case kWtIQ4NL: return launch_wt<kWtIQ4NL>(wb, N, K, qs, d2, M, y, ldy, num_sms, stream);
+        case kWtIQ4XS: return launch_wt<kWtIQ4XS>(wb, N, K, qs, d2, M, y, ldy, err, num_sms, stream);
+        case kWtQ4_0: return launch_wt<kWtQ4_0>(wb, N, K, qs, d2, M, y, ldy, err, num_sms, stream);
+        case kWtIQ4NL: return launch_wt<kWtIQ4NL>(wb, N, K, qs, d2, M, y, ldy, err, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -291,7 +302,7 @@ cudaError_t launch_matmul_dp4a(const void* w, int wt, int64_t N, int64_t K, cons
 cudaError_t launch_matmul_dp4a_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N,
                                        int64_t K, const int8_t* qs, const void* ds,
                                        const int32_t* row_offsets, int64_t total_rows, float* y,
-                                       int64_t ldy, cudaStream_t stream) {
+                                       int64_t ldy, int* err, cudaStream_t stream) {
     // at most min(G, total rows) experts have rows
     const unsigned slots = (unsigned)(G < total_rows ? G : total_rows);
     cudaLaunchAttribute attr[1];
@@ -300,9 +311,9 @@ cudaError_t launch_matmul_dp4a_grouped(const void* w, int64_t expert_stride, int
     const __half2* d2 = reinterpret_cast<const __half2*>(ds);
     if (total_rows <= 2 * (int64_t)slots)  // at most two rows per routed expert on average
         return cudaLaunchKernelEx(&cfg, matmul_dp4a_grouped_kernel<true>, wb, expert_stride, G, N, K,
-                                  qs, d2, row_offsets, y, ldy);
+                                  qs, d2, row_offsets, total_rows, y, ldy, err);
     return cudaLaunchKernelEx(&cfg, matmul_dp4a_grouped_kernel<false>, wb, expert_stride, G, N, K, qs,
-                              d2, row_offsets, y, ldy);
+                              d2, row_offsets, total_rows, y, ldy, err);
 }
 
 }  // namespace iq4xs

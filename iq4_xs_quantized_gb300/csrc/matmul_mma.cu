@@ -58,6 +58,7 @@ namespace {
 constexpr int kMmaConsumers = 8;              // consumer warps
 constexpr int kMmaProducerWarp = kMmaConsumers;
 constexpr int kMmaThreads = 32 * (kMmaConsumers + 1);
+
 constexpr int kMmaMaxCluster = 8;
 constexpr int kMmaMaxRows = 256;              // TMA box height
 constexpr int kMmaMaxStages = 4;
@@ -133,12 +134,28 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t ra
 __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kMmaConsumers) : "memory");
 }
+// Consumers and producer between two activation tiles of one CTA.
+__device__ __forceinline__ void tile_sync() { asm volatile("bar.sync 2, %0;" ::"n"(kMmaThreads) : "memory"); }
+// 3D tiled TMA load (coordinates x, y, z) into this CTA's shared memory.
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, int x, int yc, int zc, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(x), "r"(yc), "r"(zc), "r"(smem_u32(bar))
+        : "memory");
+}
 
-template <int NT, int T, int kOcc>
+// kGrouped: mixture-of-experts form.  Expert slot z (grid z) takes the z-th
+// expert that has rows (row_offsets, a device array read after the wait for
+// the preceding grid); W is that expert's matrix (a 3D tensor map over the
+// experts) and its rows [r0, r1) of the activations are covered in tiles of
+// kMt, one pass over K per tile; no K split.  Otherwise grid z is the
+// activation tile of rows [z kMt, (z + 1) kMt).
+template <int NT, int T, int kOcc, bool kGrouped>
 __global__ void __launch_bounds__(kMmaThreads, kOcc)
     matmul_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_q,
                       const __half* __restrict__ ds, int64_t M, int N, int K, float* __restrict__ y, int64_t ldy,
-                      int* err) {
+                      int* err, const int32_t* __restrict__ row_offsets, int G) {
     using C = MmaCfg<NT, T, kOcc>;
     constexpr int kTMax = T, kMt = C::kMt, kSPW = C::kSPW, kRG = C::kRG, R = C::kR, NS = C::kNS;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -147,9 +164,12 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
         return;
     }
     constexpr int stage_b = C::kStage, wbytes = C::kWBytes;
+    const Bc bc = bc_open(err);
+    if (!bc_range(bc, 0, C::kSmem, dyn_smem_bytes(), kBcMmaSmem)) return;  // every CTA alike
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffRingMma + NS * stage_b);
     uint64_t* empty = full + kMmaMaxStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kMmaMaxStages);
+    int* grp = reinterpret_cast<int*>(empty + kMmaMaxStages) + 2;  // grouped: expert, first row, end row
     const uint32_t sbase = smem_u32(smem);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,19 +182,81 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
     const int p1 = (int)((int64_t)pairs * (rank + 1) / S);
     const int nst = p1 - p0;
 
-    auto load_w = [&](int ps) {
-        const int slot = ps % NS;
-        mbar_arrive_expect_tx(&full[slot], (uint32_t)(R * kPairBytes + C::kQStage));
-        tma_load_2d(smem + kOffRingMma + slot * stage_b, &tmap_w, (p0 + ps) * (kPairBytes / 4), n0, &full[slot]);
-    };
-    auto load_q = [&](int ps) {
-        const int slot = ps % NS;
+    // Activation rows this CTA covers: [row_lo, row_hi) in mtiles tiles.
+    int gexp = 0;
+    int64_t row_lo = (int64_t)z * kMt, row_hi = (row_lo + kMt < M) ? row_lo + kMt : M;
+    if constexpr (kGrouped) {
+        if (warp == 0) {
+            griddep_wait();  // the offsets may come from the preceding grid
+            // The z-th expert with rows: offsets of 128 experts per step
+            // (independent loads), one ballot per 32.
+            int ge = -1;
+            uint32_t k = (uint32_t)z;
+            for (int base = 0; base < G && ge < 0; base += 4 * 32) {
+                int32_t lo[4], hi[4];
 #pragma unroll
-        for (int b = 0; b < kQBoxesPerStage; ++b)
-            tma_load_2d(smem + kOffRingMma + slot * stage_b + wbytes + b * C::kQBox, &tmap_q,
-                        (p0 + ps) * kPairK + b * kQBoxK, z * kMt, &full[slot]);
+                for (int j = 0; j < 4; ++j) {
+                    const int e = base + 32 * j + lane;
+                    const bool in =
+                        e < G && bc_global(bc, row_offsets + e, 8, row_offsets, (int64_t)(G + 1) * 4, kBcMmaOffsets);
+                    lo[j] = in ? __ldg(row_offsets + e) : 0;
+                    hi[j] = in ? __ldg(row_offsets + e + 1) : 0;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t mask = __ballot_sync(0xffffffffu, hi[j] > lo[j]);
+                    const uint32_t cnt = __popc(mask);
+                    if (ge < 0) {
+                        if (k < cnt) ge = base + 32 * j + (int)__fns(mask, 0, (int)k + 1);
+                        else k -= cnt;
+                    }
+                }
+            }
+            if (lane == 0) {
+                grp[0] = ge;
+                grp[1] = ge >= 0 ? row_offsets[ge] : 0;
+                grp[2] = ge >= 0 ? row_offsets[ge + 1] : 0;
+                // offsets outside the rows of y: the expert is skipped
+                if (ge >= 0 && !bc_range(bc, grp[1], (int64_t)grp[2] - grp[1], M, kBcMmaRows)) grp[0] = -1;
+            }
+        }
+        __syncthreads();
+        gexp = grp[0];
+        if (gexp < 0) return;  // fewer experts with rows than slots (whole CTA; no cluster)
+        row_lo = grp[1];
+        row_hi = grp[2];
+    }
+    // one activation tile per CTA unless it covers an expert's rows
+    const int mtiles = kGrouped ? (int)((row_hi - row_lo + kMt - 1) / kMt) : 1;
+    const int total = mtiles * nst;  // stages over all activation tiles
+
+    // Stage gs = activation tile gs / nst, K pair p0 + gs % nst.
+    auto tile_of = [&](int gs) { return kGrouped ? gs / nst : 0; };
+    auto pair_of = [&](int gs) { return p0 + (kGrouped ? gs % nst : gs); };
+    auto load_w = [&](int gs) {
+        const int slot = gs % NS;
+        const int x = pair_of(gs) * (kPairBytes / 4);
+        if (!bc_tma(bc, x, 4, kPairBytes / 4, (int64_t)(K / kQK) * (kBlockBytes / 4), n0, N, kBcMmaWAlign,
+                    kBcMmaW))
+            return;
+        if constexpr (kGrouped) bc_range(bc, gexp, 1, G, kBcMmaW);
+        mbar_arrive_expect_tx(&full[slot], (uint32_t)(R * kPairBytes + C::kQStage));
+        if constexpr (kGrouped)
+            tma_load_3d(smem + kOffRingMma + slot * stage_b, &tmap_w, x, n0, gexp, &full[slot]);
+        else
+            tma_load_2d(smem + kOffRingMma + slot * stage_b, &tmap_w, x, n0, &full[slot]);
     };
-    const int pre = nst < NS ? nst : NS;
+    auto load_q = [&](int gs) {
+        const int slot = gs % NS;
+        const int rq = (int)(row_lo + (int64_t)tile_of(gs) * kMt);
+#pragma unroll
+        for (int b = 0; b < kQBoxesPerStage; ++b) {
+            const int x = pair_of(gs) * kPairK + b * kQBoxK;
+            if (bc_tma(bc, x, 1, kQBoxK, K, rq, M, kBcMmaQAlign, kBcMmaQ))
+                tma_load_2d(smem + kOffRingMma + slot * stage_b + wbytes + b * C::kQBox, &tmap_q, x, rq, &full[slot]);
+        }
+    };
+    const int pre = nst < NS ? nst : NS;  // stages of the first activation tile issued at set-up
     if (warp == kMmaProducerWarp && lane == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&full[i], 1);
@@ -201,23 +283,39 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
 
     bool ok = true;
     if (warp == kMmaProducerWarp) {
-        if (lane == 0) {
-            griddep_wait();
-            for (int ps = 0; ps < pre; ++ps) load_q(ps);
-            int issued = pre;
-            for (int ps = NS; ps < nst && ok; ++ps) {
-                const int slot = ps % NS;
-                ok = mbar_wait(&empty[slot], ((ps / NS) - 1) & 1, abort_flag, err, kDevErrTimeoutMmaSlot);
-                if (!ok) break;
-                load_w(ps);
-                load_q(ps);
-                ++issued;
+        int issued = 0;
+        for (int mt = 0; mt < mtiles; ++mt) {
+            // The next tile's stages wait until the consumers have summed
+            // the current tile's partials, which they keep in the ring.
+            if (mt > 0) tile_sync();
+            if (lane == 0) {
+                const int gs0 = mt * nst;
+                int first = 0;
+                if (mt == 0) {
+                    griddep_wait();  // the codes come from the preceding grid
+                    for (int ps = 0; ps < pre; ++ps) load_q(ps);
+                    first = pre;
+                    issued = pre;
+                }
+                for (int ps = first; ps < nst && ok; ++ps) {
+                    const int gs = gs0 + ps, slot = gs % NS;
+                    if (gs >= NS) {
+                        ok = mbar_wait(&empty[slot], ((gs / NS) - 1) & 1, abort_flag, err, kDevErrTimeoutMmaSlot);
+                        if (!ok) break;
+                    }
+                    load_w(gs);
+                    load_q(gs);
+                    ++issued;
+                }
             }
+            __syncwarp();
+        }
+        if (lane == 0) {
             // Drain: the last stage issued into each slot has landed (the
             // earlier ones were consumed before their slot was reused).  Not
             // stopped by an abort: no copy may land after the CTA exits.
-            for (int ps = (issued > NS ? issued - NS : 0); ps < issued; ++ps)
-                mbar_wait(&full[ps % NS], (ps / NS) & 1, &g_never_abort_mma, err, kDevErrTimeoutDrain);
+            for (int gs = (issued > NS ? issued - NS : 0); gs < issued; ++gs)
+                mbar_wait(&full[gs % NS], (gs / NS) & 1, &g_never_abort_mma, err, kDevErrTimeoutDrain);
         }
         __syncwarp();
     } else {
@@ -232,34 +330,40 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
         const uint32_t* ds32 = reinterpret_cast<const uint32_t*>(ds);
         const int64_t K32 = (K + kSub - 1) / kSub;
         float acc[kTMax][NT][4];
+        // Activation scales of stage gs for this warp's sub-blocks: item e =
+        // (row m = e / kSPW of the stage's tile, sub-block e % kSPW), fp16 d
+        // in ds; rows outside the CTA's range read as 0.
+        uint32_t dxv[C::kXItems];
+        auto load_dx = [&](int gs) {
+            const int64_t rb = row_lo + (int64_t)tile_of(gs) * kMt;
+#pragma unroll
+            for (int k = 0; k < C::kXItems; ++k) {
+                const int e = lane + 32 * k;
+                const int64_t m = rb + e / kSPW;
+                const int64_t sub = (int64_t)pair_of(gs) * kSubPerPair + sub_w + e % kSPW;
+                dxv[k] = (e < C::kDxFloats && m < row_hi && sub < K32 &&
+                          bc_global(bc, ds32 + m * K32 + sub, 4, ds, M * K32 * 4, kBcMmaDs))
+                             ? __ldg(ds32 + m * K32 + sub)
+                             : 0u;
+            }
+        };
+        griddep_wait();  // ds comes from the preceding grid
+        if (total > 0) load_dx(0);
+        // Row-scale work of this lane: (fragment slot k, g) pairs c = lane +
+        // 32 i, rows 16 f + g and 16 f + g + 8, all kSPW sub-blocks.
+        const int wrow_lane = 16 * rg + g;       // row of fragment slot 0 for this lane (+ 16 kRG k)
+
+        for (int mt = 0; mt < mtiles; ++mt) {
+        const int64_t row_base = row_lo + (int64_t)mt * kMt;
 #pragma unroll
         for (int i = 0; i < kTMax; ++i)
 #pragma unroll
             for (int f = 0; f < NT; ++f)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[i][f][e] = 0.f;
-
-        // Activation scales of stage ps for this warp's sub-blocks: item e =
-        // (row m = e / kSPW, sub-block e % kSPW), fp16 d in ds.
-        uint32_t dxv[C::kXItems];
-        auto load_dx = [&](int ps) {
-#pragma unroll
-            for (int k = 0; k < C::kXItems; ++k) {
-                const int e = lane + 32 * k;
-                const int64_t m = (int64_t)z * kMt + e / kSPW;
-                const int64_t sub = (int64_t)(p0 + ps) * kSubPerPair + sub_w + e % kSPW;
-                dxv[k] = (e < C::kDxFloats && m < M && sub < K32) ? __ldg(ds32 + m * K32 + sub) : 0u;
-            }
-        };
-        griddep_wait();  // ds comes from the preceding grid
-        if (nst > 0) load_dx(0);
-        // Row-scale work of this lane: (fragment slot k, g) pairs c = lane +
-        // 32 i, rows 16 f + g and 16 f + g + 8, all kSPW sub-blocks.
-        const int wrow_lane = 16 * rg + g;       // row of fragment slot 0 for this lane (+ 16 kRG k)
-
         for (int ps = 0; ps < nst && ok; ++ps) {
-            const int slot = ps % NS;
-            ok = mbar_wait(&full[slot], (ps / NS) & 1, abort_flag, err, kDevErrTimeoutMmaStage);
+            const int gs = mt * nst + ps, slot = gs % NS;
+            ok = mbar_wait(&full[slot], (gs / NS) & 1, abort_flag, err, kDevErrTimeoutMmaStage);
             if (!ok) break;
             // Plain loads from here on: ordered after the barrier wait (an
             // asm statement with a memory clobber) and free to be scheduled
@@ -306,7 +410,7 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
                         __half2float(__ushort_as_half((unsigned short)(dxv[k] & 0xFFFFu)));
             }
             __syncwarp();
-            if (ps + 1 < nst) load_dx(ps + 1);  // in flight during this stage
+            if (gs + 1 < total) load_dx(gs + 1);  // in flight during this stage
 #pragma unroll 1
             for (int s = 0; s < kSPW; ++s) {
                 const int j = sub_w + s;                 // sub-block within the stage
@@ -386,7 +490,7 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
             // Wake the producer if it waits on a slot this warp will never free.
             if (lane == 0) *abort_flag = 1;
         }
-        // ---- end of the K range: partial tiles of the sub-block groups
+        // ---- end of the K range of this tile: partial tiles of the sub-block groups
         consumers_sync();  // every consumer is done with the ring
         if (!*abort_flag) {
             float* red = reinterpret_cast<float*>(smem + kOffRingMma) + sg * R * C::kRedStride;
@@ -408,19 +512,23 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
         if (!*abort_flag) {
             const float* red = reinterpret_cast<const float*>(smem + kOffRingMma);
             float* tile = reinterpret_cast<float*>(smem);
-            const int64_t mrows = M - (int64_t)z * kMt;
+            const int64_t mrows = row_hi - row_base;
             for (int e = threadIdx.x; e < R * kMt; e += 32 * kMmaConsumers) {
                 const int r = e % R, m = e / R;
                 float v = red[r * C::kRedStride + m];
 #pragma unroll
                 for (int q = 1; q < C::kSG; ++q) v += red[(q * R + r) * C::kRedStride + m];
                 if (S == 1) {
-                    if (m < mrows && n0 + r < N) y[((int64_t)z * kMt + m) * ldy + n0 + r] = v;
+                    if (m < mrows && n0 + r < N &&
+                        bc_global(bc, y + (row_base + m) * ldy + n0 + r, 4, y, ((M - 1) * ldy + N) * 4, kBcMmaY))
+                        y[(row_base + m) * ldy + n0 + r] = v;
                 } else {
                     tile[r * C::kRedStride + m] = v;
                 }
             }
         }
+        if (mt + 1 < mtiles) tile_sync();  // the ring may take the next tile's stages
+        }  // activation tiles
     }
 
     if (S > 1) {
@@ -433,13 +541,16 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
         cluster_wait();
         if (warp < kMmaConsumers && !*abort_flag) {
             const int r0 = R * (int)rank / S, r1 = R * ((int)rank + 1) / S;
-            const int64_t mrows = M - (int64_t)z * kMt;
+            const int64_t mrows = row_hi - row_lo;  // one tile (K splits only without experts)
             for (int e = threadIdx.x; e < (r1 - r0) * kMt; e += 32 * kMmaConsumers) {
                 const int r = r0 + e % (r1 - r0), m = e / (r1 - r0);
                 const uint32_t off = sbase + (uint32_t)((r * C::kRedStride + m) * 4);
                 float v = 0.f;
-                for (int q = 0; q < S; ++q) v += ld_cluster_f32(off, (uint32_t)q);
-                if (m < mrows && n0 + r < N) y[((int64_t)z * kMt + m) * ldy + n0 + r] = v;
+                if (bc_range(bc, (r * C::kRedStride + m) * 4, 4, R * C::kRedStride * 4, kBcMmaSplit))
+                    for (int q = 0; q < S; ++q) v += ld_cluster_f32(off, (uint32_t)q);
+                if (m < mrows && n0 + r < N &&
+                    bc_global(bc, y + (row_lo + m) * ldy + n0 + r, 4, y, ((M - 1) * ldy + N) * 4, kBcMmaY))
+                    y[(row_lo + m) * ldy + n0 + r] = v;
             }
         }
         __syncwarp();
@@ -452,21 +563,27 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The kernel's dynamic shared-memory limit, raised once per device.
+template <int NT, int T, int kOcc, bool kGrouped>
+cudaError_t mma_smem_attr(int dev) {
+    static bool done[64] = {};
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(matmul_mma_kernel<NT, T, kOcc, kGrouped>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               MmaCfg<NT, T, kOcc>::kSmem);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    return e;
+}
+
 // Cached per device: clusters of S (1..8) the device runs at once for the
-// kernel <NT, T> (cudaOccupancyMaxActiveClusters, queried once).
+// kernel <NT, T, kOcc> (cudaOccupancyMaxActiveClusters, queried once).
 template <int NT, int T, int kOcc>
 int mma_max_clusters(int dev, int s, int num_sms) {
     using C = MmaCfg<NT, T, kOcc>;
     static int cache[64][kMmaMaxCluster + 1] = {};
     int mc = (dev >= 0 && dev < 64) ? cache[dev][s] : 0;
     if (mc > 0) return mc;
-    static bool attr_done[64] = {};
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(matmul_mma_kernel<NT, T, kOcc>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
-            cudaSuccess)
-            cudaGetLastError();
-        attr_done[dev] = true;
-    }
+    if (mma_smem_attr<NT, T, kOcc, false>(dev) != cudaSuccess) cudaGetLastError();
     cudaLaunchConfig_t q = {};
     q.gridDim = dim3(1, (unsigned)s, 1);
     q.blockDim = dim3(kMmaThreads);
@@ -479,7 +596,7 @@ int mma_max_clusters(int dev, int s, int num_sms) {
     q.attrs = at;
     q.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, matmul_mma_kernel<NT, T, kOcc>, &q) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, matmul_mma_kernel<NT, T, kOcc, false>, &q) != cudaSuccess || n < 1) {
         cudaGetLastError();
         n = kOcc * num_sms / s;
     }
@@ -492,6 +609,10 @@ template <int NT, int T, int kOcc>
 cudaError_t launch_nt(const void* w, int64_t row_bytes, EncodeTiledFn enc, const CUtensorMap& tq, const __half* ds,
                       int64_t M, int N, int K, int S, float* y, int64_t ldy, int* err, cudaStream_t stream) {
     using C = MmaCfg<NT, T, kOcc>;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const cudaError_t ea = mma_smem_attr<NT, T, kOcc, false>(dev);
+    if (ea != cudaSuccess) return ea;
     // W: one box = R rows x one super-block pair (272 B; K % 512 == 0, so
     // rows are 16-byte strided); rows past N read as zeros (d = 0).
     CUtensorMap tw;
@@ -521,29 +642,62 @@ cudaError_t launch_nt(const void* w, int64_t row_bytes, EncodeTiledFn enc, const
     attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, matmul_mma_kernel<NT, T, kOcc>, tw, tq, ds, M, N, K, y, ldy, err);
+    return cudaLaunchKernelEx(&cfg, matmul_mma_kernel<NT, T, kOcc, false>, tw, tq, ds, M, N, K, y, ldy, err,
+                              static_cast<const int32_t*>(nullptr), 0);
 }
 
-// Fragments per warp T (R = 32 T rows per CTA) and K split S (= cluster
-// size) with the least modelled time  waves x (F + R / 128 x ceil(pairs /
-// S))  in units of one 128-row stage's streaming time, over T = 1..kTMax and
-// S = 1..8 (at most the K pairs); waves from the clusters of S the device
-// runs at once.  F, a CTA's fixed cost (launch, first stage, reduction), is
-// about two stages.  Ties keep the larger R and the smaller S.
-// Test override of the launch configuration (0 = the model's choice).
-std::atomic<int> g_force_t{0}, g_force_s{0}, g_force_occ{0};
+// Grouped (mixture-of-experts) launch of the <NT, T> kernel: W of expert g
+// through a 3D tensor map (row words x rows x experts, expert_stride bytes
+// apart), grid (row tiles, 1, expert slots).
+template <int NT, int T>
+cudaError_t launch_grouped_nt(const void* w, int64_t expert_stride, int G, int64_t row_bytes, EncodeTiledFn enc,
+                              const CUtensorMap& tq, const __half* ds, const int32_t* row_offsets, int64_t rows,
+                              int slots, int N, int K, float* y, int64_t ldy, int* err, int num_sms,
+                              cudaStream_t stream) {
+    using C = MmaCfg<NT, T, 1>;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const cudaError_t ea = mma_smem_attr<NT, T, 1, true>(dev);
+    if (ea != cudaSuccess) return ea;
+    CUtensorMap tw;
+    {
+        const cuuint64_t gdim[3] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)N, (cuuint64_t)G};
+        const cuuint64_t gstride[2] = {(cuuint64_t)row_bytes, (cuuint64_t)expert_stride};
+        const cuuint32_t box[3] = {(cuuint32_t)(kPairBytes / 4), (cuuint32_t)C::kR, 1};
+        const cuuint32_t estride[3] = {1, 1, 1};
+        if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(w), gdim, gstride, box, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((N + C::kR - 1) / C::kR), 1, (unsigned)slots);
+    cfg.blockDim = dim3(kMmaThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, matmul_mma_kernel<NT, T, 1, true>, tw, tq, ds, rows, N, K, y, ldy, err,
+                              row_offsets, G);
+}
 
-// One launch configuration: fragments per warp T (R = 32 T rows per CTA)
-// and CTAs per SM, with its cluster-occupancy query and its launcher.
+// Test override of the launch configuration (0 = the model's choice).
+std::atomic<int> g_force_rows{0}, g_force_s{0}, g_force_occ{0};
+
+// One launch configuration: R weight rows per CTA and CTAs per SM, with its
+// cluster-occupancy query and its launcher.
 struct MmaConfig {
-    int T, occ;
+    int R, occ;
     int (*max_clusters)(int dev, int s, int num_sms);
     cudaError_t (*launch)(const void*, int64_t, EncodeTiledFn, const CUtensorMap&, const __half*, int64_t, int,
                           int, int, float*, int64_t, int*, cudaStream_t);
 };
 template <int NT, int T, int kOcc>
 constexpr MmaConfig cfg_of() {
-    return {T, kOcc, &mma_max_clusters<NT, T, kOcc>, &launch_nt<NT, T, kOcc>};
+    return {MmaCfg<NT, T, kOcc>::kR, kOcc, &mma_max_clusters<NT, T, kOcc>, &launch_nt<NT, T, kOcc>};
 }
 // Per activation-tile width: T = 1..8 (4 from 24 activation rows on, the
 // accumulators' registers) at one CTA per SM, and the tiles that leave room
@@ -574,7 +728,7 @@ struct MmaConfigs<4> {
                                          cfg_of<4, 1, 1>()};
 };
 
-// The configuration (T, CTAs per SM) and K split S (= cluster size) with the
+// The configuration (R, CTAs per SM) and K split S (= cluster size) with the
 // least modelled time  waves x (F + c x R / 128 x ceil(pairs / S))  in units
 // of one 128-row stage's streaming time per SM, over every configuration of
 // the activation-tile width and S = 1..8 (at most the K pairs); waves from
@@ -597,12 +751,11 @@ cudaError_t launch_best(const void* w, int64_t row_bytes, EncodeTiledFn enc, con
     double best = 1e30;
     for (int ci = 0; ci < kCount; ++ci) {
         const MmaConfig& c = list[ci];
-        const int R = 32 * c.T;
-        const int units = (N + R - 1) / R * mtiles;
+        const int units = (N + c.R - 1) / c.R * mtiles;
         for (int s = 1; s <= kMmaMaxCluster && s <= pairs; ++s) {
             const int mc = c.max_clusters(dev, s, num_sms);
             const int waves = (units + mc - 1) / mc;
-            const double tm = waves * (kFixed + c.occ * (double)R / 128.0 * (double)((pairs + s - 1) / s));
+            const double tm = waves * (kFixed + c.occ * (double)c.R / 128.0 * (double)((pairs + s - 1) / s));
             if (tm < best * 0.999) {
                 best = tm;
                 best_c = ci;
@@ -610,15 +763,19 @@ cudaError_t launch_best(const void* w, int64_t row_bytes, EncodeTiledFn enc, con
             }
         }
     }
-    const int ft = g_force_t.load(), fs = g_force_s.load(), fo = g_force_occ.load();
-    if (ft > 0 || fo > 0) {  // the forced configuration, or the nearest one the list holds
-        const int want_t = ft > 0 ? ft : list[best_c].T, want_o = fo > 0 ? fo : list[best_c].occ;
+    const int fr = g_force_rows.load(), fs = g_force_s.load(), fo = g_force_occ.load();
+    if (fr > 0 || fo > 0) {
+        // the forced configuration, or the nearest one the list holds: the
+        // largest R up to the one wanted with the wanted CTAs per SM, else
+        // with any
+        const int want_r = fr > 0 ? fr : list[best_c].R, want_o = fo > 0 ? fo : list[best_c].occ;
         int pick = -1;
-        for (int ci = 0; ci < kCount; ++ci)
-            if (list[ci].occ == want_o && list[ci].T <= want_t && (pick < 0 || list[ci].T > list[pick].T)) pick = ci;
-        if (pick < 0)
-            for (int ci = 0; ci < kCount; ++ci)
-                if (list[ci].T <= want_t && (pick < 0 || list[ci].T > list[pick].T)) pick = ci;
+        for (int pass = 0; pass < 2 && pick < 0; ++pass)
+            for (int ci = 0; ci < kCount; ++ci) {
+                const MmaConfig& c = list[ci];
+                if (c.R > want_r || (pass < 1 && c.occ != want_o)) continue;
+                if (pick < 0 || c.R > list[pick].R) pick = ci;
+            }
         best_c = pick < 0 ? kCount - 1 : pick;
     }
     if (fs > 0) best_s = fs < pairs ? fs : pairs;
@@ -627,10 +784,58 @@ cudaError_t launch_best(const void* w, int64_t row_bytes, EncodeTiledFn enc, con
 
 }  // namespace
 
-void mma_force_config(int frags_per_warp, int k_splits, int ctas_per_sm) {
-    g_force_t.store(frags_per_warp);
+void mma_force_config(int rows_per_cta, int k_splits, int ctas_per_sm) {
+    g_force_rows.store(rows_per_cta);
     g_force_s.store(k_splits);
     g_force_occ.store(ctas_per_sm);
+}
+
+cudaError_t launch_matmul_mma_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
+                                      const int8_t* qs, const void* ds, const int32_t* row_offsets,
+                                      int64_t total_rows, float* y, int64_t ldy, void* encode, int* err,
+                                      int num_sms, cudaStream_t stream) {
+    const EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(encode);
+    const int64_t row_bytes = wt_row_bytes(kWtIQ4XS, K);
+    // at most min(G, rows) experts have rows; the activation tile from the
+    // mean rows per such expert (larger experts take several tiles)
+    const int slots = (int)(G < total_rows ? G : total_rows);
+    const int64_t mean = (total_rows + slots - 1) / slots;
+    const int mt = mma_tile_rows(mean);
+    CUtensorMap tq;
+    {
+        const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)total_rows};
+        const cuuint64_t gstride[1] = {(cuuint64_t)K};
+        const cuuint32_t box[2] = {(cuuint32_t)kQBoxK, (cuuint32_t)mt};
+        const cuuint32_t estride[2] = {1, 1};
+        if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qs), gdim, gstride, box, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const __half* dsh = reinterpret_cast<const __half*>(ds);
+    // 128-row tiles, or 64 / 32 when the experts' row tiles alone do not
+    // give every SM a CTA.
+    const int Ni = (int)N, Ki = (int)K, Gi = (int)G;
+    const int64_t ctas128 = (N + 127) / 128 * slots;
+    const int rows_cta = ctas128 >= num_sms ? 128 : ((N + 63) / 64 * slots >= num_sms ? 64 : 32);
+#define IQ4XS_MMA_G(nt)                                                                                         \
+    case 8 * nt:                                                                                               \
+        if (rows_cta == 128)                                                                                   \
+            return launch_grouped_nt<nt, 4>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets,        \
+                                            total_rows, slots, Ni, Ki, y, ldy, err, num_sms, stream);          \
+        if (rows_cta == 64)                                                                                    \
+            return launch_grouped_nt<nt, 2>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets,        \
+                                            total_rows, slots, Ni, Ki, y, ldy, err, num_sms, stream);          \
+        return launch_grouped_nt<nt, 1>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets, total_rows, \
+                                        slots, Ni, Ki, y, ldy, err, num_sms, stream);
+    switch (mt) {
+        IQ4XS_MMA_G(1)
+        IQ4XS_MMA_G(2)
+        IQ4XS_MMA_G(3)
+        IQ4XS_MMA_G(4)
+        default: return cudaErrorInvalidValue;
+    }
+#undef IQ4XS_MMA_G
 }
 
 int mma_tile_rows(int64_t M) {

@@ -270,6 +270,8 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
         if (threadIdx.x == 0) atomicExch(err, kDevErrLayout);
         return;
     }
+    const Bc bc = bc_open(err);
+    if (!bc_range(bc, 0, C::kSmem, dyn_smem_bytes(), kBcTcSmem)) return;  // every CTA alike
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint64_t* w_full = bars;
     uint64_t* w_empty = w_full + C::kNW;
@@ -311,10 +313,12 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
         if (ps == skip_w_stage) return;
         mbar_arrive_expect_tx(&w_full[slot], C::kWStage);
 #pragma unroll
-        for (int b = 0; b < C::kWBoxes; ++b)
-            tma_load_2d(smem + C::kOffW + slot * C::kWStage + b * (kTileN * C::kWBoxBytes), &tmap_w,
-                        (p0 + ps) * (C::kWRowBytes / 4) + b * (C::kWBoxBytes / 4), n0,
-                        &w_full[slot]);
+        for (int b = 0; b < C::kWBoxes; ++b) {
+            const int x = (p0 + ps) * (C::kWRowBytes / 4) + b * (C::kWBoxBytes / 4);
+            if (bc_tma(bc, x, 4, C::kWBoxBytes / 4, wt_row_bytes(WT, K) / 4, n0, N, kBcTcWAlign, kBcTcW))
+                tma_load_2d(smem + C::kOffW + slot * C::kWStage + b * (kTileN * C::kWBoxBytes), &tmap_w, x, n0,
+                            &w_full[slot]);
+        }
     };
     if (warp == kProducerWarp) {
         // Lane i initialises barriers i, i + 32, i + 64; lane 0 then starts
@@ -382,7 +386,10 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
             for (int k = 0; k < C::kXItems; ++k) {
                 const int e = lane + 32 * k;
                 const int64_t row = (int64_t)z * MT + e / kBStageSubs;
-                dsv[k] = (e < kBStageSubs * MT && row < M) ? __ldg(ds32 + row * K32 + sub0 + e % kBStageSubs) : 0u;
+                const uint32_t* dp = ds32 + row * K32 + sub0 + e % kBStageSubs;
+                dsv[k] = (e < kBStageSubs * MT && row < M && bc_global(bc, dp, 4, ds, M * K32 * 4, kBcTcDs))
+                             ? __ldg(dp)
+                             : 0u;
             }
             if (ok && bs >= C::kNX)
                 ok = mbar_wait(&x_empty[xs], ((bs / C::kNX) - 1) & 1, abort_flag, err, kDevErrTimeoutX);
@@ -613,14 +620,15 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
                     if constexpr (kPrep) {
                         // one contiguous bulk copy of the stage's hi / lo planes
                         const int64_t sub0 = (int64_t)p0 * kSubPerPair + (int64_t)bs * kBStageSubs;
+                        const uint8_t* src = tc_op + ((int64_t)z * (K / kSub) + sub0) * C::kBSubBytes;
                         mbar_arrive_expect_tx(&q_full[slot], C::kBSlotBytes);
-                        bulk_load(smem + C::kOffB + slot * C::kBSlotBytes,
-                                  tc_op + ((int64_t)z * (K / kSub) + sub0) * C::kBSubBytes, C::kBSlotBytes,
-                                  &q_full[slot]);
+                        if (bc_global_async(bc, src, C::kBSlotBytes, tc_op, tc_qh_bytes(M, K), kBcTcOp))
+                            bulk_load(smem + C::kOffB + slot * C::kBSlotBytes, src, C::kBSlotBytes, &q_full[slot]);
                     } else {
+                        const int x = (p0 * kSubPerPair + bs * kBStageSubs) * kSub;
                         mbar_arrive_expect_tx(&q_full[slot], C::kQRawBytes);
-                        tma_load_2d(smem + C::kOffB + slot * C::kBSlotBytes, &tmap_q,
-                                    (p0 * kSubPerPair + bs * kBStageSubs) * kSub, z * MT, &q_full[slot]);
+                        if (bc_tma(bc, x, 1, kBStageSubs * kSub, K, (int64_t)z * MT, M, kBcTcQAlign, kBcTcQ))
+                            tma_load_2d(smem + C::kOffB + slot * C::kBSlotBytes, &tmap_q, x, z * MT, &q_full[slot]);
                     }
                 };
                 // At most three activation stages go out before the W stages
@@ -734,8 +742,11 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
             span_scale = reinterpret_cast<const float*>(tc_op + tc_qh_bytes(M, K)) +
                          (int64_t)z * tc_num_spans(K) * MT + c0;
             if (t < kMH) {
-                cur_e = span_scale[(int64_t)cur_span * MT + t];
-                if (cur_span < last_span) next_e = span_scale[(int64_t)(cur_span + 1) * MT + t];
+                const void* sbase = tc_op + tc_qh_bytes(M, K);
+                const int64_t sext = tc_operand_total_bytes(M, K) - tc_qh_bytes(M, K);
+                const float* sp0 = span_scale + (int64_t)cur_span * MT + t;
+                if (bc_global(bc, sp0, 4, sbase, sext, kBcTcSpan)) cur_e = *sp0;
+                if (cur_span < last_span && bc_global(bc, sp0 + MT, 4, sbase, sext, kBcTcSpan)) next_e = sp0[MT];
                 s_span[t] = cur_e;
             }
             named_barrier_sync(kEpilogueBarrier + eg, kTileN);
@@ -861,7 +872,10 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
             griddep_wait();
 #pragma unroll
             for (int m = 0; m < kMH; ++m)
-                if (c0 + m < mrows && n0 + t < N) y[((int64_t)z * MT + c0 + m) * ldy + n0 + t] = acc[m];
+                if (c0 + m < mrows && n0 + t < N &&
+                    bc_global(bc, y + ((int64_t)z * MT + c0 + m) * ldy + n0 + t, 4, y, ((M - 1) * ldy + N) * 4,
+                              kBcTcY))
+                    y[((int64_t)z * MT + c0 + m) * ldy + n0 + t] = acc[m];
         } else {
             float* st = reinterpret_cast<float*>(smem + C::kOffStage) + t * C::kRedStride + c0;
 #pragma unroll
@@ -891,6 +905,11 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
                 if (q == (int)rank) continue;
                 const int q0 = kTileN * q / S, q1 = kTileN * (q + 1) / S;
                 const int slot = slot_base < q ? slot_base : slot_base - 1;
+                // the slice inside this CTA's staging area and the owner's receive area
+                if (!bc_range(bc, (int64_t)q1 * C::kRedStride * 4, 0, (int64_t)C::kNB * C::kBSlotBytes, kBcTcRecv) ||
+                    !bc_range(bc, (int64_t)slot * cap * C::kRedStride * 4, (int64_t)(q1 - q0) * C::kRedStride * 4,
+                              (int64_t)(C::kOffB - C::kOffRecv), kBcTcRecv))
+                    continue;
                 bulk_copy_to_rank(recv0 + (uint32_t)(slot * cap * C::kRedStride * 4),
                                   stage0 + (uint32_t)(q0 * C::kRedStride * 4),
                                   (uint32_t)((q1 - q0) * C::kRedStride * 4), smem_u32(recv_bar), (uint32_t)q);
@@ -930,7 +949,11 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
                     }
                 }
                 const int row = r0 + lr;
-                if (n0 + row < N) {
+                // rows m .. last of y (the checked build checks the first and the last)
+                const int64_t y_ext = ((M - 1) * ldy + N) * 4, last = (m + 3 < mrows) ? m + 3 : mrows - 1;
+                if (n0 + row < N && m < mrows &&
+                    bc_global(bc, y + ((int64_t)z * MT + m) * ldy + n0 + row, 4, y, y_ext, kBcTcY) &&
+                    bc_global(bc, y + ((int64_t)z * MT + last) * ldy + n0 + row, 4, y, y_ext, kBcTcY)) {
                     float* yp = y + ((int64_t)z * MT + m) * ldy + n0 + row;
                     if (m < mrows) yp[0] = sum.x;
                     if (m + 1 < mrows) yp[ldy] = sum.y;

@@ -28,7 +28,7 @@ template <bool kTc>
 __global__ void __launch_bounds__(kQuantThreads)
     quantize_q8_1_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
                          int8_t* __restrict__ qs, __half2* __restrict__ ds,
-                         uint4* __restrict__ qh, float* __restrict__ spanscale, int MT) {
+                         uint4* __restrict__ qh, float* __restrict__ spanscale, int MT, int* err) {
     // x may come from the preceding grid, and qs/ds/the operand may still be
     // read by it: wait for it, then let the next grid start launching.
     griddep_wait();
@@ -38,9 +38,12 @@ __global__ void __launch_bounds__(kQuantThreads)
     const bool live = e0 < K;  // whole warps (see above)
     const int lane = threadIdx.x & 31;
     const int l8 = lane & 7;  // position of this thread inside its Q8_1 block
+    const Bc bc = bc_open(err);
+    const int64_t nsub = K / kSub;
 
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (live && m < M) v = __ldg(reinterpret_cast<const float4*>(x + m * ldx + e0));
+    if (live && m < M && bc_global(bc, x + m * ldx + e0, 16, x, ((M - 1) * ldx + K) * 4, kBcQuantX))
+        v = __ldg(reinterpret_cast<const float4*>(x + m * ldx + e0));
 
     float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
@@ -64,8 +67,10 @@ __global__ void __launch_bounds__(kQuantThreads)
     if (live && m < M) {
         const uint32_t packed = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
                                 ((uint32_t)(q[2] & 0xFF) << 16) | ((uint32_t)(q[3] & 0xFF) << 24);
-        *reinterpret_cast<uint32_t*>(qs + m * K + e0) = packed;
-        if (l8 == 0) ds[m * (K / kSub) + blk] = __halves2half2(d_h, __float2half_rn(d * (float)sum));
+        if (bc_global(bc, qs + m * K + e0, 4, qs, M * K, kBcQuantQs))
+            *reinterpret_cast<uint32_t*>(qs + m * K + e0) = packed;
+        if (l8 == 0 && bc_global(bc, ds + m * nsub + blk, 4, ds, M * nsub * 4, kBcQuantDs))
+            ds[m * nsub + blk] = __halves2half2(d_h, __float2half_rn(d * (float)sum));
     }
 
     if constexpr (kTc) {
@@ -88,8 +93,10 @@ __global__ void __launch_bounds__(kQuantThreads)
         }
         const int64_t mt = m / MT;
         const int64_t r = m % MT;
-        if (threadIdx.x == 0)
-            spanscale[(mt * tc_num_spans(K) + blockIdx.x) * MT + r] = ldexpf(1.0f, e);
+        const int64_t span_i = (mt * tc_num_spans(K) + blockIdx.x) * MT + r;
+        if (threadIdx.x == 0 && bc_global(bc, spanscale + span_i, 4, spanscale,
+                                          tc_operand_total_bytes(M, K) - tc_qh_bytes(M, K), kBcQuantSpan))
+            spanscale[span_i] = ldexpf(1.0f, e);
         // Element e of the block goes to K position 2*(e % 16) + e / 16.  The
         // thread holding e = 4*l8 .. 4*l8+3 (l8 < 4) pairs with lane ^ 4,
         // which holds e + 16, and writes one 16-byte chunk (8 positions) of
@@ -107,9 +114,12 @@ __global__ void __launch_bounds__(kQuantThreads)
                 hi[k] = __float2half_rn(val);
                 lo[k] = __float2half_rn(val - __half2float(hi[k]));
             }
-            uint4* sub = qh + (mt * (K / kSub) + blk) * (kPlanes * kChunksPerSub * MT);
-            sub[l8 * MT + r] = *reinterpret_cast<const uint4*>(hi);
-            sub[(kChunksPerSub + l8) * MT + r] = *reinterpret_cast<const uint4*>(lo);
+            uint4* sub = qh + (mt * nsub + blk) * (kPlanes * kChunksPerSub * MT);
+            const int64_t op_bytes = tc_qh_bytes(M, K);
+            if (bc_global(bc, sub + l8 * MT + r, 16, qh, op_bytes, kBcQuantOp))
+                sub[l8 * MT + r] = *reinterpret_cast<const uint4*>(hi);
+            if (bc_global(bc, sub + (kChunksPerSub + l8) * MT + r, 16, qh, op_bytes, kBcQuantOp))
+                sub[(kChunksPerSub + l8) * MT + r] = *reinterpret_cast<const uint4*>(lo);
         }
     }
 }
@@ -117,7 +127,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 }  // namespace
 
 cudaError_t launch_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qs,
-                                 void* ds, void* tc_operand, cudaStream_t stream) {
+                                 void* ds, void* tc_operand, int* err, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kQuantThreads);
     cfg.stream = stream;
@@ -131,14 +141,14 @@ cudaError_t launch_quantize_q8_1(const float* x, int64_t M, int64_t K, int64_t l
     if (tc_operand == nullptr) {
         cfg.gridDim = dim3(spans, (unsigned)M);
         return cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<false>, x, M, K, ldx, qs, d2,
-                                  (uint4*)nullptr, (float*)nullptr, 0);
+                                  (uint4*)nullptr, (float*)nullptr, 0, err);
     }
     const int MT = tc_mtile(M);
     cfg.gridDim = dim3(spans, (unsigned)(tc_num_mtiles(M) * MT));  // padding rows written as zeros
     uint8_t* op = reinterpret_cast<uint8_t*>(tc_operand);
     return cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<true>, x, M, K, ldx, qs, d2,
                               reinterpret_cast<uint4*>(op),
-                              reinterpret_cast<float*>(op + tc_qh_bytes(M, K)), MT);
+                              reinterpret_cast<float*>(op + tc_qh_bytes(M, K)), MT, err);
 }
 
 }  // namespace iq4xs

@@ -220,8 +220,23 @@ def test_valid_call_without_gpu_reports_device_error(lib):
 
 
 def test_status_strings(lib):
-    for s in range(7):
-        assert B.iq4xs_status_string(s)
+    for s in range(8):
+        assert B.iq4xs_status_string(s) != "unknown status"
+
+
+def test_bounds_checked_build_exports_and_flags(lib):
+    """The debug build with bounds checks builds from the same sources,
+    exports every declared function and says which build it is; the margin
+    hook is refused by the normal build."""
+    blib = B.load(build.build(bounds_check=True))
+    for name in B.header_functions():
+        assert hasattr(blib, name), name
+    out = ctypes.c_int(-1)
+    assert blib.iq4xs_bounds_checked(ctypes.byref(out)) == B.OK and out.value == 1
+    assert lib.iq4xs_bounds_checked(ctypes.byref(out)) == B.OK and out.value == 0
+    assert lib.iq4xs_bounds_checked(None) == B.ERR_ARG
+    assert lib.iq4xs_test_bounds_margin(16) == B.ERR_ARG
+    assert blib.iq4xs_test_bounds_margin(-1) == B.ERR_ARG
 
 
 def test_linear_workspace_and_validation(lib):

@@ -1,8 +1,10 @@
 """Grouped (mixture-of-experts) matmul on the GPU: one launch over G experts
-with per-expert rows read from a device array.  Each expert's rows match the
-oracle (within 1e-5 per row) and, bit for bit, the single-expert dp4a call
+with per-expert rows read from a device array, on the CUDA-core (dp4a) form
+and the warp-level MMA form.  Each expert's rows match the oracle (within
+1e-5 per row); on dp4a they also match, bit for bit, the single-expert call
 on the same rows; empty experts, an expert holding every row and experts
-with more rows than the kernel's batch width are covered."""
+with more rows than a kernel's batch width (several activation tiles on the
+MMA form) are covered."""
 import numpy as np
 import pytest
 import torch
@@ -26,7 +28,7 @@ def _lib():
     assert B.iq4xs_last_device_error() == 0
 
 
-def _run_grouped(W, rows_x, offsets):
+def _run_grouped(W, rows_x, offsets, path="auto"):
     G, N, K = W.G, W.N, W.K
     w = W.weights()
     stride = w.shape[1] * w.shape[2]
@@ -35,9 +37,20 @@ def _run_grouped(W, rows_x, offsets):
     off_d = dev(offsets.astype(np.int32))
     M = rows_x.shape[0]
     y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
-    B.iq4xs_matmul_grouped(wd, stride, G, N, K, qs, ds, off_d, y)
+    B.iq4xs_matmul_grouped(wd, stride, G, N, K, qs, ds, off_d, y, path=path)
     torch.cuda.synchronize()
     return w, wd, qs, ds, y.cpu().numpy()
+
+
+def _check_experts(W, w, rows_x, offsets, y):
+    assert gate_written(y) is None
+    qs_o, d_o, _ = oracle_q8(rows_x)
+    for g in range(W.G):
+        r0, r1 = int(offsets[g]), int(offsets[g + 1])
+        if r1 > r0:
+            r = gate_parity(y[r0:r1], oracle_matmul(w[g], W.N, W.K, qs_o[r0:r1], d_o[r0:r1]))
+            assert r is None, (g, r)
+    return qs_o, d_o
 
 
 @pytest.mark.parametrize("T,topk", [(20, 4), (40, 6), (3, 2), (9, 3)])
@@ -45,7 +58,7 @@ def test_grouped_matches_oracle_and_single_expert_calls(T, topk):
     W = synth.MoEWorkload("moe_small", seed=7, G=8, N=256, K=1024, topk=topk, tokens=(T,),
                           d_scale=2e-3)
     x, rows_x, offsets = W.inputs(T)
-    w, wd, qs, ds, y = _run_grouped(W, rows_x, offsets)
+    w, wd, qs, ds, y = _run_grouped(W, rows_x, offsets, "dp4a")
     assert gate_written(y) is None
     qs_o, d_o, _ = oracle_q8(rows_x)
     for g in range(W.G):
@@ -68,29 +81,54 @@ def test_grouped_matches_oracle_and_single_expert_calls(T, topk):
     assert gate_independent(y, ind_own) is None
 
 
+@pytest.mark.parametrize("T,topk", [(20, 4), (40, 6), (9, 3), (64, 8)])
+def test_grouped_mma_matches_oracle(T, topk):
+    """The warp-MMA form over larger per-expert batches (ragged N)."""
+    W = synth.MoEWorkload("moe_mma", seed=17, G=8, N=200, K=1024, topk=topk, tokens=(T,),
+                          d_scale=2e-3)
+    _, rows_x, offsets = W.inputs(T)
+    w, wd, qs, ds, y = _run_grouped(W, rows_x, offsets, "mma")
+    qs_o, d_o = _check_experts(W, w, rows_x, offsets, y)
+    ind = independent_fp32(np.concatenate([w[g] for g in range(W.G)]), W.G * W.N, W.K, qs_o, d_o)
+    ind_own = np.full_like(y, np.nan)
+    for g in range(W.G):
+        r0, r1 = int(offsets[g]), int(offsets[g + 1])
+        ind_own[r0:r1] = ind[r0:r1, g * W.N:(g + 1) * W.N]
+    assert gate_independent(y, ind_own) is None
+    # AUTO: the MMA form from as many rows as experts on, or once the mean
+    # rows of an expert slot leave one expert's dp4a range, else dp4a (same
+    # bits as the explicit call either way)
+    M = rows_x.shape[0]
+    slots = min(W.G, M)
+    mean = -(-M // slots)
+    auto = "mma" if M >= W.G or B.iq4xs_select_path(mean, W.N, W.K) != B.PATH_DP4A else "dp4a"
+    y_auto = _run_grouped(W, rows_x, offsets)[-1]
+    y_expl = y if auto == "mma" else _run_grouped(W, rows_x, offsets, "dp4a")[-1]
+    assert np.array_equal(y_auto, y_expl), auto
+
+
+@pytest.mark.parametrize("path", ("dp4a", "mma"))
 @pytest.mark.parametrize("G,T,topk", [(70, 5, 2), (100, 40, 3)])
-def test_grouped_many_experts_compacted_slots(G, T, topk):
+def test_grouped_many_experts_compacted_slots(G, T, topk, path):
     # more experts than a warp's ballot covers; fewer (and more) rows than experts
     W = synth.MoEWorkload("moe_wide", seed=13, G=G, N=128, K=512, topk=topk, tokens=(T,),
                           d_scale=2e-3)
     _, rows_x, offsets = W.inputs(T)
-    w, wd, qs, ds, y = _run_grouped(W, rows_x, offsets)
-    assert gate_written(y) is None
-    qs_o, d_o, _ = oracle_q8(rows_x)
-    for g in range(W.G):
-        r0, r1 = int(offsets[g]), int(offsets[g + 1])
-        if r1 > r0:
-            r = gate_parity(y[r0:r1], oracle_matmul(w[g], W.N, W.K, qs_o[r0:r1], d_o[r0:r1]))
-            assert r is None, (g, r)
+    w, wd, qs, ds, y = _run_grouped(W, rows_x, offsets, path)
+    _check_experts(W, w, rows_x, offsets, y)
 
 
-def test_grouped_empty_experts_and_one_expert_with_every_row():
-    W = synth.MoEWorkload("moe_edge", seed=9, G=6, N=128, K=512, topk=1, tokens=(11,),
+@pytest.mark.parametrize("path", ("dp4a", "mma"))
+@pytest.mark.parametrize("rows", (11, 80))
+def test_grouped_empty_experts_and_one_expert_with_every_row(path, rows):
+    """80 rows on one expert: five activation tiles of 16 rows in one CTA on
+    the MMA form (the tile from the mean rows of the six expert slots)."""
+    W = synth.MoEWorkload("moe_edge", seed=9, G=6, N=128, K=512, topk=1, tokens=(rows,),
                           d_scale=2e-3)
     rng = np.random.default_rng(11)
-    rows_x = synth.activations(rng, 11, W.K)
-    offsets = np.array([0, 0, 0, 11, 11, 11, 11], dtype=np.int32)  # all rows on expert 2
-    w, wd, qs, ds, y = _run_grouped(W, rows_x, offsets)
+    rows_x = synth.activations(rng, rows, W.K)
+    offsets = np.array([0, 0, 0, rows, rows, rows, rows], dtype=np.int32)  # all rows on expert 2
+    w, wd, qs, ds, y = _run_grouped(W, rows_x, offsets, path)
     assert gate_written(y) is None
     qs_o, d_o, _ = oracle_q8(rows_x)
     assert gate_parity(y, oracle_matmul(w[2], W.N, W.K, qs_o, d_o)) is None
@@ -108,4 +146,13 @@ def test_grouped_rejects_bad_arguments():
     assert e.value.status == B.ERR_ARG
     with pytest.raises(B.IQ4XSError) as e:
         B.iq4xs_matmul_grouped(w, stride, 0, W.N, W.K, qs, ds, off, y)
+    assert e.value.status == B.ERR_SHAPE
+    with pytest.raises(B.IQ4XSError) as e:
+        B.iq4xs_matmul_grouped(w, stride, 2, W.N, W.K, qs, ds, off, y, path=B.PATH_TC)
+    assert e.value.status == B.ERR_ARG
+    W3 = synth.MoEWorkload("moe_k768", seed=1, G=2, N=128, K=768, topk=1, tokens=(2,), d_scale=2e-3)
+    w3 = dev(W3.weights().reshape(2, -1))
+    qs3, ds3 = B.alloc_activations(2, 768, "cuda")
+    with pytest.raises(B.IQ4XSError) as e:  # the MMA form needs K % 512 == 0
+        B.iq4xs_matmul_grouped(w3, w3.shape[1], 2, W3.N, 768, qs3, ds3, off, y, path="mma")
     assert e.value.status == B.ERR_SHAPE

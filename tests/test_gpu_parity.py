@@ -13,8 +13,8 @@ import torch
 
 import oracle
 from _gates import gate_independent, gate_parity, gate_written
-from _gpu import (dev, independent_fp32, matmul_gpu, oracle_matmul, oracle_q8, prepare_gpu,
-                  quantize_gpu, sample_rows)
+from _gpu import (check_q8, dev, independent_fp32, matmul_gpu, oracle_matmul, oracle_q8, prepare_gpu,
+                  quantize_gpu, run_and_gate, sample_rows)
 from _pins import make_block, parse_q8_cases
 from iq4_xs_quantized_gb300 import binding as B
 from iq4_xs_quantized_gb300 import synth
@@ -35,38 +35,6 @@ def _lib():
     B.load()
     yield
     assert B.iq4xs_last_device_error() == 0
-
-
-def check_q8(x, qs, ds):
-    qs_o, d_o, s_o = oracle_q8(x)
-    assert np.array_equal(qs.cpu().numpy(), qs_o)
-    dsn = ds.cpu().numpy().view(np.uint16)
-    assert np.array_equal(dsn[..., 0], d_o)
-    assert np.array_equal(dsn[..., 1], s_o)
-    return qs_o, d_o
-
-
-def run_and_gate(w, N, K, x, path, rows=None, ldy=None, independent=True):
-    qs, ds = quantize_gpu(x)
-    qs_o, d_o = check_q8(x, qs, ds)
-    M = x.shape[0]
-    op = prepare_gpu(x, qs, ds) if path == "tcp" else None
-    y = matmul_gpu(dev(w), N, K, qs, ds, M, path, ldy=ldy, op=op)
-    assert gate_written(y[:, :N]) is None, gate_written(y[:, :N])
-    if ldy is not None and ldy > N:
-        assert np.all(np.isnan(y[:, N:])), "columns beyond N must not be written"
-    y = y[:, :N]
-    ys = y if rows is None else y[:, rows]
-    yo = oracle_matmul(w, N, K, qs_o, d_o, rows)
-    r = gate_parity(ys, yo)
-    assert r is None, r
-    if independent:
-        yi = independent_fp32(w, N, K, qs_o, d_o, rows)
-        # A handful of outputs can agree with the independent path exactly by
-        # chance; the nonzero-error rule is applied to outputs of >= 256 values.
-        r = gate_independent(ys, yi, require_nonzero=ys.size >= 256)
-        assert r is None, r
-    return y, yo
 
 
 # --------------------------------------------------------------------------- Q8_1

@@ -112,8 +112,8 @@ def test_weight_formats_within_hbm_roofline(wtype, M):
     assert r is None, f"{wtype} M={M}: {r}"
 
 
-@pytest.mark.parametrize("T", (1, 16))
-def test_grouped_within_hbm_roofline(T):
+@pytest.mark.parametrize("T,path", [(1, "auto"), (16, "auto"), (64, "mma"), (128, "mma")])
+def test_grouped_within_hbm_roofline(T, path):
     W = synth.MOE_DECODE
     _, rows, offsets = W.inputs(T)
     M = rows.shape[0]
@@ -129,9 +129,9 @@ def test_grouped_within_hbm_roofline(T):
 
     def launch(s):
         for wc in ws:
-            B.iq4xs_matmul_grouped(wc, stride, W.G, W.N, W.K, qs, ds, off, y, s)
+            B.iq4xs_matmul_grouped(wc, stride, W.G, W.N, W.K, qs, ds, off, y, s, path=path)
 
     t = time_calls(launch, len(ws))
     # only the experts that have rows are read
     r = gate_roofline(matmul_bytes(touched * W.N * (W.K // 256) * 136, M, W.N, W.K), t, hbm_peak())
-    assert r is None, f"grouped T={T}: {r}"
+    assert r is None, f"grouped T={T} {path}: {r}"
