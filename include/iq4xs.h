@@ -464,6 +464,17 @@ int iq4xs_test_skip_w_stage(int64_t stage);
  */
 int iq4xs_test_mma_config(int64_t rows_per_cta, int64_t k_splits, int64_t ctas_per_sm);
 
+/*
+ * The launch the warp-MMA path makes for (M, N, K) on the current device
+ * (no counterpart on the source pages; for tests and tuning): weight rows
+ * per CTA, CTAs per cluster along K, and CTAs per SM, as the launch model
+ * chooses them (or as iq4xs_test_mma_config forces them) for activation
+ * tiles of min(32, M rounded up to 8) rows.  Host only; queries the device's
+ * cluster occupancy once per configuration.  IQ4XS_ERR_SHAPE unless K %
+ * 512 == 0 and the sizes are in range; IQ4XS_ERR_ARG for null outputs.
+ */
+int iq4xs_mma_launch_config(int64_t M, int64_t N, int64_t K, int* rows_per_cta, int* k_splits, int* ctas_per_sm);
+
 /* Static string for a status code. */
 const char* iq4xs_status_string(int status);
 

@@ -87,6 +87,8 @@ def load(path: str | None = None):
         lib.iq4xs_last_device_error.argtypes = [ctypes.POINTER(ci)]
         lib.iq4xs_test_skip_w_stage.argtypes = [i64]
         lib.iq4xs_bounds_checked.argtypes = [ctypes.POINTER(ci)]
+        lib.iq4xs_mma_launch_config.argtypes = [i64, i64, i64, ctypes.POINTER(ci), ctypes.POINTER(ci),
+                                                ctypes.POINTER(ci)]
         lib.iq4xs_test_bounds_margin.argtypes = [i64]
         lib.iq4xs_status_string.argtypes = [ci]
         lib.iq4xs_status_string.restype = ctypes.c_char_p
@@ -97,7 +99,8 @@ def load(path: str | None = None):
                      "iq4xs_set_mma_crossover", "iq4xs_set_mma_crossover_classes",
                      "iq4xs_test_mma_config",
                      "iq4xs_quantize_q8_1_tc", "iq4xs_matmul_tc_operand",
-                     "iq4xs_last_device_error", "iq4xs_bounds_checked", "iq4xs_test_bounds_margin"):
+                     "iq4xs_last_device_error", "iq4xs_bounds_checked", "iq4xs_test_bounds_margin",
+                     "iq4xs_mma_launch_config"):
             getattr(lib, name).restype = ci
         if path is None:
             _lib = lib
@@ -320,6 +323,14 @@ def iq4xs_test_mma_config(rows_per_cta: int = 0, k_splits: int = 0, ctas_per_sm:
     """Force the warp-MMA launch configuration (0 = the launch model's choice)."""
     _check("iq4xs_test_mma_config",
            load().iq4xs_test_mma_config(int(rows_per_cta), int(k_splits), int(ctas_per_sm)))
+
+
+def iq4xs_mma_launch_config(M: int, N: int, K: int) -> tuple[int, int, int]:
+    """(rows per CTA, K splits, CTAs per SM) of the warp-MMA launch for (M, N, K)."""
+    r, s, o = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check("iq4xs_mma_launch_config",
+           load().iq4xs_mma_launch_config(M, N, K, ctypes.byref(r), ctypes.byref(s), ctypes.byref(o)))
+    return r.value, s.value, o.value
 
 
 def iq4xs_set_baseline_threshold(m_min_baseline: int) -> None:

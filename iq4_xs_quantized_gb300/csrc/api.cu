@@ -428,6 +428,21 @@ int iq4xs_test_mma_config(int64_t rows_per_cta, int64_t k_splits, int64_t ctas_p
     return IQ4XS_OK;
 }
 
+int iq4xs_mma_launch_config(int64_t M, int64_t N, int64_t K, int* rows_per_cta, int* k_splits, int* ctas_per_sm) {
+    if (!rows_per_cta || !k_splits || !ctas_per_sm) return IQ4XS_ERR_ARG;
+    if (M < 1 || M > kMaxM || N < 1 || N > (1 << 30) || K <= 0 || K % kPairK || K > (1 << 30))
+        return IQ4XS_ERR_SHAPE;
+    DevState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    int r = 0, s = 0, o = 0;
+    mma_launch_config(M, N, K, st->num_sms, &r, &s, &o);
+    *rows_per_cta = r;
+    *k_splits = s;
+    *ctas_per_sm = o;
+    return IQ4XS_OK;
+}
+
 const char* iq4xs_status_string(int status) {
     switch (status) {
         case IQ4XS_OK: return "ok";

@@ -1035,6 +1035,10 @@ cudaError_t launch_matmul_mma_grouped(const void* w, int64_t expert_stride, int6
 // Test override of the warp-MMA launch: weight rows per CTA, K splits and
 // CTAs per SM (1, 2); 0 = the launch model's choice.
 void mma_force_config(int rows_per_cta, int k_splits, int ctas_per_sm);
+// The warp-MMA launch the path takes for (M, N, K): weight rows per CTA, K
+// splits (cluster size) and CTAs per SM (the launch model's choice, or the
+// forced one).
+void mma_launch_config(int64_t M, int64_t N, int64_t K, int num_sms, int* rows, int* splits, int* ctas_per_sm);
 cudaError_t launch_matmul_mma(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds, int64_t M,
                               float* y, int64_t ldy, void* encode, int* err, int num_sms, cudaStream_t stream);
 cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,

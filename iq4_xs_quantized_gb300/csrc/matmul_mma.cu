@@ -737,9 +737,7 @@ struct MmaConfigs<4> {
 // reduction), is about two stages.  Ties keep the earlier configuration
 // (larger R, one CTA per SM) and the smaller S.
 template <int NT>
-cudaError_t launch_best(const void* w, int64_t row_bytes, EncodeTiledFn enc, const CUtensorMap& tq,
-                        const __half* ds, int64_t M, int N, int K, float* y, int64_t ldy, int* err, int num_sms,
-                        cudaStream_t stream) {
+void choose_config(int64_t M, int N, int K, int num_sms, int* best_c, int* best_s) {
     constexpr double kFixed = 2.0;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -747,7 +745,8 @@ cudaError_t launch_best(const void* w, int64_t row_bytes, EncodeTiledFn enc, con
     const int pairs = (K + kPairK - 1) / kPairK;
     const auto& list = MmaConfigs<NT>::list;
     constexpr int kCount = (int)(sizeof(list) / sizeof(list[0]));
-    int best_c = 0, best_s = 1;
+    *best_c = 0;
+    *best_s = 1;
     double best = 1e30;
     for (int ci = 0; ci < kCount; ++ci) {
         const MmaConfig& c = list[ci];
@@ -758,8 +757,8 @@ cudaError_t launch_best(const void* w, int64_t row_bytes, EncodeTiledFn enc, con
             const double tm = waves * (kFixed + c.occ * (double)c.R / 128.0 * (double)((pairs + s - 1) / s));
             if (tm < best * 0.999) {
                 best = tm;
-                best_c = ci;
-                best_s = s;
+                *best_c = ci;
+                *best_s = s;
             }
         }
     }
@@ -768,7 +767,7 @@ cudaError_t launch_best(const void* w, int64_t row_bytes, EncodeTiledFn enc, con
         // the forced configuration, or the nearest one the list holds: the
         // largest R up to the one wanted with the wanted CTAs per SM, else
         // with any
-        const int want_r = fr > 0 ? fr : list[best_c].R, want_o = fo > 0 ? fo : list[best_c].occ;
+        const int want_r = fr > 0 ? fr : list[*best_c].R, want_o = fo > 0 ? fo : list[*best_c].occ;
         int pick = -1;
         for (int pass = 0; pass < 2 && pick < 0; ++pass)
             for (int ci = 0; ci < kCount; ++ci) {
@@ -776,13 +775,40 @@ cudaError_t launch_best(const void* w, int64_t row_bytes, EncodeTiledFn enc, con
                 if (c.R > want_r || (pass < 1 && c.occ != want_o)) continue;
                 if (pick < 0 || c.R > list[pick].R) pick = ci;
             }
-        best_c = pick < 0 ? kCount - 1 : pick;
+        *best_c = pick < 0 ? kCount - 1 : pick;
     }
-    if (fs > 0) best_s = fs < pairs ? fs : pairs;
-    return list[best_c].launch(w, row_bytes, enc, tq, ds, M, N, K, best_s, y, ldy, err, stream);
+    if (fs > 0) *best_s = fs < pairs ? fs : pairs;
+}
+
+template <int NT>
+cudaError_t launch_best(const void* w, int64_t row_bytes, EncodeTiledFn enc, const CUtensorMap& tq,
+                        const __half* ds, int64_t M, int N, int K, float* y, int64_t ldy, int* err, int num_sms,
+                        cudaStream_t stream) {
+    int ci = 0, s = 1;
+    choose_config<NT>(M, N, K, num_sms, &ci, &s);
+    return MmaConfigs<NT>::list[ci].launch(w, row_bytes, enc, tq, ds, M, N, K, s, y, ldy, err, stream);
+}
+
+template <int NT>
+void report_config(int64_t M, int N, int K, int num_sms, int* rows, int* splits, int* ctas_per_sm) {
+    int ci = 0, s = 1;
+    choose_config<NT>(M, N, K, num_sms, &ci, &s);
+    *rows = MmaConfigs<NT>::list[ci].R;
+    *splits = s;
+    *ctas_per_sm = MmaConfigs<NT>::list[ci].occ;
 }
 
 }  // namespace
+
+void mma_launch_config(int64_t M, int64_t N, int64_t K, int num_sms, int* rows, int* splits, int* ctas_per_sm) {
+    const int Ni = (int)N, Ki = (int)K;
+    switch (mma_tile_rows(M)) {
+        case 8: return report_config<1>(M, Ni, Ki, num_sms, rows, splits, ctas_per_sm);
+        case 16: return report_config<2>(M, Ni, Ki, num_sms, rows, splits, ctas_per_sm);
+        case 24: return report_config<3>(M, Ni, Ki, num_sms, rows, splits, ctas_per_sm);
+        default: return report_config<4>(M, Ni, Ki, num_sms, rows, splits, ctas_per_sm);
+    }
+}
 
 void mma_force_config(int rows_per_cta, int k_splits, int ctas_per_sm) {
     g_force_rows.store(rows_per_cta);

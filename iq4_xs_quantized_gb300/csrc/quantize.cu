@@ -29,10 +29,15 @@ __global__ void __launch_bounds__(kQuantThreads)
     quantize_q8_1_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
                          int8_t* __restrict__ qs, __half2* __restrict__ ds,
                          uint4* __restrict__ qh, float* __restrict__ spanscale, int MT, int* err) {
-    // x may come from the preceding grid, and qs/ds/the operand may still be
-    // read by it: wait for it, then let the next grid start launching.
-    griddep_wait();
+    // The next grid (the matmul) may launch at once: it reads qs/ds only
+    // after its own wait for this grid, and this grid completes only after
+    // the preceding one (whose CTAs are all resident by now: this grid
+    // launched when each had started).  The matmul's CTAs take SMs as the
+    // preceding grid's leave and stream their weights meanwhile.  x may come
+    // from the preceding grid, and qs/ds/the operand may still be read by it:
+    // wait for it before reading or writing anything.
     griddep_launch_dependents();
+    griddep_wait();
     const int64_t m = blockIdx.y;
     const int64_t e0 = (int64_t)blockIdx.x * kElemsPerCta + threadIdx.x * kElemsPerThread;
     const bool live = e0 < K;  // whole warps (see above)

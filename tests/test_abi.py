@@ -219,6 +219,14 @@ def test_valid_call_without_gpu_reports_device_error(lib):
     assert lib.iq4xs_matmul(p, 8, 256, p, p, 1, p, 8, 1, 0) == B.ERR_DEVICE
 
 
+def test_mma_launch_config_validation(lib):
+    r, sp, o = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    assert lib.iq4xs_mma_launch_config(8, 4096, 4096, None, ctypes.byref(sp), ctypes.byref(o)) == B.ERR_ARG
+    for M, N, K in ((0, 4096, 4096), (8, 0, 4096), (8, 4096, 768), (8, 4096, 0), (40000, 4096, 4096)):
+        assert lib.iq4xs_mma_launch_config(M, N, K, ctypes.byref(r), ctypes.byref(sp),
+                                           ctypes.byref(o)) == B.ERR_SHAPE, (M, N, K)
+
+
 def test_status_strings(lib):
     for s in range(8):
         assert B.iq4xs_status_string(s) != "unknown status"

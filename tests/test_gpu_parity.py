@@ -107,6 +107,20 @@ def test_matmul_mma_configs(rows, splits):
         B.iq4xs_test_mma_config(0, 0, 0)
 
 
+def test_mma_launch_config_reports_the_launch():
+    """The reported launch is the forced one when forced, and the model's
+    own choice covers N with at most 256 rows per CTA and at most 8 splits."""
+    for c in ((96, 3, 1), (64, 2, 2), (256, 1, 1)):
+        B.iq4xs_test_mma_config(*c)
+        try:
+            assert B.iq4xs_mma_launch_config(8, 4096, 4608) == c
+        finally:
+            B.iq4xs_test_mma_config(0, 0, 0)
+    for M, N, K in ((1, 4096, 4096), (16, 34816, 5120), (32, 5120, 17408), (8, 300, 512)):
+        r, sp, o = B.iq4xs_mma_launch_config(M, N, K)
+        assert r % 32 == 0 and 32 <= r <= 256 and 1 <= sp <= min(8, K // 512) and o in (1, 2)
+
+
 # The half-shared-memory tiles (two CTAs per SM): 32 and 64 rows at 8
 # activation rows, 32 at 16 and 24 (M = 32 falls back to one CTA per SM).
 @pytest.mark.parametrize("rows,splits", [(32, 1), (64, 2), (64, 5), (32, 8)])
