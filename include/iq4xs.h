@@ -465,11 +465,26 @@ int iq4xs_test_skip_w_stage(int64_t stage);
 int iq4xs_test_mma_config(int64_t rows_per_cta, int64_t k_splits, int64_t ctas_per_sm);
 
 /*
+ * Measured launches of the warp-MMA path (no counterpart on the source
+ * pages; written by the calibration, which times every configuration on
+ * its shapes): `count` entries of six int64 each -- N, K, the activation
+ * tile's rows (8, 16, 24 or 32), weight rows per CTA (a multiple of 32 up
+ * to 256), CTAs per cluster along K (1..8) and CTAs per SM (1, 2).  A call
+ * whose N, K and tile height match an entry launches that configuration
+ * (when the tile width's configurations hold it and the K split fits K);
+ * other calls use the launch model.  count = 0 clears the table; at most
+ * 256 entries.  Replaces the whole table; IQ4XS_ERR_ARG (nothing
+ * installed) for a value out of range.  Host only.
+ */
+int iq4xs_set_mma_launch_table(const int64_t* entries, int count);
+
+/*
  * The launch the warp-MMA path makes for (M, N, K) on the current device
  * (no counterpart on the source pages; for tests and tuning): weight rows
- * per CTA, CTAs per cluster along K, and CTAs per SM, as the launch model
- * chooses them (or as iq4xs_test_mma_config forces them) for activation
- * tiles of min(32, M rounded up to 8) rows.  Host only; queries the device's
+ * per CTA, CTAs per cluster along K, and CTAs per SM, as the call would
+ * take them (forced by iq4xs_test_mma_config, else from the measured
+ * launch table, else from the launch model) for activation tiles of
+ * min(32, M rounded up to 8) rows.  Host only; queries the device's
  * cluster occupancy once per configuration.  IQ4XS_ERR_SHAPE unless K %
  * 512 == 0 and the sizes are in range; IQ4XS_ERR_ARG for null outputs.
  */

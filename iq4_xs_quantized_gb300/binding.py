@@ -89,6 +89,7 @@ def load(path: str | None = None):
         lib.iq4xs_bounds_checked.argtypes = [ctypes.POINTER(ci)]
         lib.iq4xs_mma_launch_config.argtypes = [i64, i64, i64, ctypes.POINTER(ci), ctypes.POINTER(ci),
                                                 ctypes.POINTER(ci)]
+        lib.iq4xs_set_mma_launch_table.argtypes = [ctypes.POINTER(i64), ci]
         lib.iq4xs_test_bounds_margin.argtypes = [i64]
         lib.iq4xs_status_string.argtypes = [ci]
         lib.iq4xs_status_string.restype = ctypes.c_char_p
@@ -100,7 +101,7 @@ def load(path: str | None = None):
                      "iq4xs_test_mma_config",
                      "iq4xs_quantize_q8_1_tc", "iq4xs_matmul_tc_operand",
                      "iq4xs_last_device_error", "iq4xs_bounds_checked", "iq4xs_test_bounds_margin",
-                     "iq4xs_mma_launch_config"):
+                     "iq4xs_mma_launch_config", "iq4xs_set_mma_launch_table"):
             getattr(lib, name).restype = ci
         if path is None:
             _lib = lib
@@ -134,16 +135,31 @@ def _install_calibration(lib):
         lib.iq4xs_set_mma_crossover(int(table["mma_m_max"]))
     if table and "mma_classes" in table:
         _set_classes(lib, table["mma_classes"], mma=True)
+    if table and "mma_launch" in table:
+        _set_launch_table(lib, table["mma_launch"])
+
+
+def _set_launch_table(lib, entries):
+    flat = [int(v) for e in entries for v in e]
+    arr = (ctypes.c_int64 * max(1, len(flat)))(*flat)
+    _check("iq4xs_set_mma_launch_table", lib.iq4xs_set_mma_launch_table(arr, len(entries)))
+
+
+def iq4xs_set_mma_launch_table(entries) -> None:
+    """Install measured warp-MMA launches: [(N, K, tile_rows, rows_per_cta, k_splits, ctas_per_sm), ...]."""
+    _set_launch_table(load(), entries)
 
 
 def reset_dispatch() -> None:
     """Dispatcher back to the library defaults (DP4A to M = 4, MMA to M = 8,
-    no classes, no baseline advice), then the calibrated table if present."""
+    no classes, no baseline advice, no measured launches), then the
+    calibrated table if present."""
     lib = load()
     lib.iq4xs_set_crossover(4)
     lib.iq4xs_set_mma_crossover(8)
     _set_classes(lib, [])
     _set_classes(lib, [], mma=True)
+    _set_launch_table(lib, [])
     lib.iq4xs_set_baseline_threshold(0)
     _install_calibration(lib)
 

@@ -14,6 +14,13 @@ smaller shape's), the smallest shape's to everything below.  The result is
 written to ``dispatch_table.json`` beside this file and installed whenever
 the binding loads.
 
+Before the crossovers, the warp-MMA launches are tuned: on the shapes the
+benchmark runs (the square 4096 projection and the nine projections of a
+~27B decoder layer), for each activation-tile height (8, 16, 24, 32 rows),
+every launch configuration the kernel holds (rows per CTA, K split, CTAs
+per SM) is timed and the fastest goes into the table's ``mma_launch``
+entries; other shapes use the kernel's launch model.
+
 Run on the GPU:  python -m iq4_xs_quantized_gb300.calibrate
 """
 from __future__ import annotations
@@ -34,6 +41,10 @@ BASE_SHAPES = ((4096, 4096), (17408, 5120), (5120, 17408))
 BASE_MS = (32, 48, 64, 80, 96, 128, 192, 256, 512)
 L2_MULTIPLE = 3
 L2_BYTES = 129 * 2**20
+# Shapes whose warp-MMA launches are tuned, and the activation-tile heights.
+LAUNCH_SHAPES = ((4096, 4096), (5120, 5120), (6144, 5120), (1024, 5120), (10240, 5120), (12288, 5120),
+                 (5120, 6144), (17408, 5120), (34816, 5120), (5120, 17408))
+LAUNCH_TILES = (8, 16, 24, 32)
 
 
 def time_path(B, torch, wcopies, N, K, M, path, reps=20):
@@ -221,6 +232,63 @@ def calibrate_baseline(shapes=BASE_SHAPES, ms=BASE_MS, verbose=True):
     return threshold, per_shape
 
 
+def launch_candidates(K, tile_rows):
+    """Every (rows per CTA, K split, CTAs per SM) the warp-MMA kernel may hold
+    for this tile height (the kernel reports which it does)."""
+    pairs = K // 512
+    rmax = 256 if tile_rows <= 16 else 128
+    out = [(r, s, 1) for r in range(32, rmax + 1, 32) for s in range(1, 9) if s <= pairs]
+    out += [(r, s, 2) for r in (32, 64) for s in (1, 2, 3, 4) if s <= pairs]
+    return out
+
+
+def calibrate_launches(shapes=LAUNCH_SHAPES, tiles=LAUNCH_TILES, verbose=True):
+    """[[N, K, tile_rows, rows, splits, ctas_per_sm], ...] of the fastest
+    warp-MMA launch per shape and tile height, and the timings behind them
+    (the launch model's own choice beside the best)."""
+    import torch
+
+    from . import binding as B
+    from . import synth
+    B.iq4xs_set_mma_launch_table([])  # time the model's choices, not an older table's
+    rng = np.random.default_rng(77)
+    entries, detail = [], {}
+    for N, K in shapes:
+        w = torch.from_numpy(synth.iq4xs_weights(rng, N, K, 1e-3)).cuda()
+        ncopy = max(2, int(np.ceil(L2_MULTIPLE * L2_BYTES / w.numel())))
+        wcopies = [w] + [w.clone() for _ in range(ncopy - 1)]
+        for mt in tiles:
+            M = mt
+            qs, ds = B.alloc_activations(M, K, "cuda")
+            B.iq4xs_quantize_q8_1(torch.randn(M, K, device="cuda"), qs, ds)
+            y = torch.empty(M, N, device="cuda")
+
+            def run(s):
+                for ww in wcopies:
+                    B.iq4xs_matmul(ww, N, K, qs, ds, M, y, B.PATH_MMA, s)
+
+            model = B.iq4xs_mma_launch_config(M, N, K)
+            times = {}
+            try:
+                for c in launch_candidates(K, mt):
+                    B.iq4xs_test_mma_config(*c)
+                    if B.iq4xs_mma_launch_config(M, N, K) != c:
+                        continue  # not one the kernel holds
+                    times[c] = _graph_time(torch, run, reps=5) / len(wcopies)
+            finally:
+                B.iq4xs_test_mma_config(0, 0, 0)
+            best = min(times, key=times.get)
+            entries.append([N, K, mt, *best])
+            detail[f"{N}x{K}/{mt}"] = {"best": list(best), "best_us": round(times[best], 3),
+                                       "model": list(model), "model_us": round(times.get(model, -1.0), 3)}
+            if verbose:
+                print(f"N={N} K={K} tile {mt}: best {best} {times[best]:.2f} us, model {model} "
+                      f"{times.get(model, float('nan')):.2f} us", flush=True)
+        del wcopies, w
+        torch.cuda.empty_cache()
+    return entries, detail
+
+
 def load_table():
     try:
         with open(TABLE) as f:
@@ -230,7 +298,12 @@ def load_table():
 
 
 def main():
+    from . import binding as B
+    launches, launch_detail = calibrate_launches()
+    B.iq4xs_set_mma_launch_table(launches)  # the crossovers below see the tuned launches
     table = calibrate()
+    table["mma_launch"] = launches
+    table["mma_launch_detail"] = launch_detail
     thr, per_shape = calibrate_baseline()
     table["baseline_m_min"] = thr
     table["baseline_shapes"] = per_shape

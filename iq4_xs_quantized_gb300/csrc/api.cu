@@ -428,6 +428,10 @@ int iq4xs_test_mma_config(int64_t rows_per_cta, int64_t k_splits, int64_t ctas_p
     return IQ4XS_OK;
 }
 
+int iq4xs_set_mma_launch_table(const int64_t* entries, int count) {
+    return mma_set_launch_table(entries, count) == 0 ? IQ4XS_OK : IQ4XS_ERR_ARG;
+}
+
 int iq4xs_mma_launch_config(int64_t M, int64_t N, int64_t K, int* rows_per_cta, int* k_splits, int* ctas_per_sm) {
     if (!rows_per_cta || !k_splits || !ctas_per_sm) return IQ4XS_ERR_ARG;
     if (M < 1 || M > kMaxM || N < 1 || N > (1 << 30) || K <= 0 || K % kPairK || K > (1 << 30))

@@ -1039,6 +1039,10 @@ void mma_force_config(int rows_per_cta, int k_splits, int ctas_per_sm);
 // splits (cluster size) and CTAs per SM (the launch model's choice, or the
 // forced one).
 void mma_launch_config(int64_t M, int64_t N, int64_t K, int num_sms, int* rows, int* splits, int* ctas_per_sm);
+// Measured warp-MMA launches: count entries of 6 int64 (N, K, activation-tile
+// rows 8/16/24/32, rows per CTA, K splits, CTAs per SM); 0 clears.  -1 on a
+// value out of range (nothing installed).
+int mma_set_launch_table(const int64_t* entries, int count);
 cudaError_t launch_matmul_mma(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds, int64_t M,
                               float* y, int64_t ldy, void* encode, int* err, int num_sms, cudaStream_t stream);
 cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,

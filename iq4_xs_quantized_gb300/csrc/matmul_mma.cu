@@ -49,6 +49,7 @@
 #include <cuda.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "internal.cuh"
 
@@ -411,7 +412,11 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
             }
             __syncwarp();
             if (gs + 1 < total) load_dx(gs + 1);  // in flight during this stage
-#pragma unroll 1
+            // The four sub-blocks unrolled at one activation fragment (loads of
+            // the next sub-block's words overlap this one's lookups and MMAs:
+            // 5-6 % faster at 8 rows); one at a time at more (registers).
+            constexpr int kUnrollS = (NT == 1) ? kSPW : 1;
+#pragma unroll kUnrollS
             for (int s = 0; s < kSPW; ++s) {
                 const int j = sub_w + s;                 // sub-block within the stage
                 const int jj = j % kSubPerBlock;
@@ -687,6 +692,28 @@ cudaError_t launch_grouped_nt(const void* w, int64_t expert_stride, int G, int64
 // Test override of the launch configuration (0 = the model's choice).
 std::atomic<int> g_force_rows{0}, g_force_s{0}, g_force_occ{0};
 
+// Measured launches (installed from the calibration): for a weight shape
+// and activation-tile height, the rows per CTA, K split and CTAs per SM
+// that timed fastest.
+struct LaunchEntry {
+    int64_t N, K;
+    int mt, R, S, occ;
+};
+constexpr int kMaxLaunchEntries = 256;
+std::mutex g_launch_mu;
+LaunchEntry g_launch[kMaxLaunchEntries];
+int g_launch_n = 0;
+
+bool measured_launch(int64_t N, int64_t K, int mt, LaunchEntry* out) {
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    for (int i = 0; i < g_launch_n; ++i)
+        if (g_launch[i].N == N && g_launch[i].K == K && g_launch[i].mt == mt) {
+            *out = g_launch[i];
+            return true;
+        }
+    return false;
+}
+
 // One launch configuration: R weight rows per CTA and CTAs per SM, with its
 // cluster-occupancy query and its launcher.
 struct MmaConfig {
@@ -728,17 +755,31 @@ struct MmaConfigs<4> {
                                          cfg_of<4, 1, 1>()};
 };
 
-// The configuration (R, CTAs per SM) and K split S (= cluster size) with the
-// least modelled time  waves x (F + c x R / 128 x ceil(pairs / S))  in units
-// of one 128-row stage's streaming time per SM, over every configuration of
-// the activation-tile width and S = 1..8 (at most the K pairs); waves from
-// the clusters of S the device runs at once for that configuration; c = the
-// CTAs sharing an SM.  F, a CTA's fixed cost (launch, first stage,
-// reduction), is about two stages.  Ties keep the earlier configuration
-// (larger R, one CTA per SM) and the smaller S.
+// Launch cost model, per activation-tile width: a wave of CTAs costs F, plus
+// a per 128-row stage of one CTA (times the CTAs sharing an SM) and d per
+// stage whatever its rows; every CTA beyond the first in a cluster adds c
+// (the split-K reduction and the cluster's scheduling).  In microseconds,
+// fitted by least squares to about 1,700 timed launches of every
+// configuration on ten weight shapes (4096 x 4096 and the nine projections
+// of a ~27B decoder layer) at 8, 16, 24 and 32 activation rows.
+struct LaunchCost {
+    double F, a, d, c;
+};
+constexpr LaunchCost kLaunchCost[4] = {
+    {3.66, 1.21, 0.29, 0.71}, {4.20, 1.89, 0.11, 1.35}, {4.64, 3.14, 0.10, 1.06}, {4.64, 3.14, 0.10, 1.06}};
+
+// The configuration (R, CTAs per SM) and K split S (= cluster size) for a
+// call: the forced one (tests), else the measured one for this shape and
+// tile height if the calibration installed it, else the least modelled time
+// waves x (F + a x occ x R / 128 x st + d x st) + c x (S - 1), st =
+// ceil(pairs / S) stages per CTA, over every configuration of the
+// activation-tile width and S = 1..8 (at most the K pairs), with waves from
+// the clusters of S the device runs at once for that configuration.  Ties
+// keep the earlier configuration (larger R, one CTA per SM) and the
+// smaller S.
 template <int NT>
 void choose_config(int64_t M, int N, int K, int num_sms, int* best_c, int* best_s) {
-    constexpr double kFixed = 2.0;
+    constexpr LaunchCost kC = kLaunchCost[NT - 1];
     int dev = 0;
     cudaGetDevice(&dev);
     const int mtiles = (int)((M + 8 * NT - 1) / (8 * NT));
@@ -754,7 +795,8 @@ void choose_config(int64_t M, int N, int K, int num_sms, int* best_c, int* best_
         for (int s = 1; s <= kMmaMaxCluster && s <= pairs; ++s) {
             const int mc = c.max_clusters(dev, s, num_sms);
             const int waves = (units + mc - 1) / mc;
-            const double tm = waves * (kFixed + c.occ * (double)c.R / 128.0 * (double)((pairs + s - 1) / s));
+            const double st = (double)((pairs + s - 1) / s);
+            const double tm = waves * (kC.F + kC.a * c.occ * (double)c.R / 128.0 * st + kC.d * st) + kC.c * (s - 1);
             if (tm < best * 0.999) {
                 best = tm;
                 *best_c = ci;
@@ -763,6 +805,15 @@ void choose_config(int64_t M, int N, int K, int num_sms, int* best_c, int* best_
         }
     }
     const int fr = g_force_rows.load(), fs = g_force_s.load(), fo = g_force_occ.load();
+    LaunchEntry e;
+    if (fr <= 0 && fs <= 0 && fo <= 0 && measured_launch(N, K, 8 * NT, &e)) {
+        for (int ci = 0; ci < kCount; ++ci)
+            if (list[ci].R == e.R && list[ci].occ == e.occ && e.S >= 1 && e.S <= kMmaMaxCluster && e.S <= pairs) {
+                *best_c = ci;
+                *best_s = e.S;
+                return;
+            }
+    }
     if (fr > 0 || fo > 0) {
         // the forced configuration, or the nearest one the list holds: the
         // largest R up to the one wanted with the wanted CTAs per SM, else
@@ -808,6 +859,24 @@ void mma_launch_config(int64_t M, int64_t N, int64_t K, int num_sms, int* rows, 
         case 24: return report_config<3>(M, Ni, Ki, num_sms, rows, splits, ctas_per_sm);
         default: return report_config<4>(M, Ni, Ki, num_sms, rows, splits, ctas_per_sm);
     }
+}
+
+int mma_set_launch_table(const int64_t* entries, int count) {
+    if (count < 0 || count > kMaxLaunchEntries || (count > 0 && !entries)) return -1;
+    for (int i = 0; i < count; ++i) {
+        const int64_t* v = entries + 6 * i;
+        if (v[0] < 1 || v[1] < kPairK || v[1] % kPairK || (v[2] != 8 && v[2] != 16 && v[2] != 24 && v[2] != 32) ||
+            v[3] < 32 || v[3] > kMmaMaxRows || v[3] % 32 || v[4] < 1 || v[4] > kMmaMaxCluster || v[5] < 1 ||
+            v[5] > 2)
+            return -1;
+    }
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    for (int i = 0; i < count; ++i) {
+        const int64_t* v = entries + 6 * i;
+        g_launch[i] = {v[0], v[1], (int)v[2], (int)v[3], (int)v[4], (int)v[5]};
+    }
+    g_launch_n = count;
+    return 0;
 }
 
 void mma_force_config(int rows_per_cta, int k_splits, int ctas_per_sm) {

@@ -219,6 +219,23 @@ def test_valid_call_without_gpu_reports_device_error(lib):
     assert lib.iq4xs_matmul(p, 8, 256, p, p, 1, p, 8, 1, 0) == B.ERR_DEVICE
 
 
+def test_mma_launch_table_validation(lib):
+    def put(entries):
+        flat = [v for e in entries for v in e]
+        arr = (ctypes.c_int64 * max(1, len(flat)))(*flat)
+        return lib.iq4xs_set_mma_launch_table(arr, len(entries))
+    good = (4096, 4096, 8, 128, 4, 1)
+    assert put([good]) == B.OK
+    for bad in ((0, 4096, 8, 128, 4, 1), (4096, 768, 8, 128, 4, 1), (4096, 4096, 12, 128, 4, 1),
+                (4096, 4096, 8, 48, 4, 1), (4096, 4096, 8, 288, 4, 1), (4096, 4096, 8, 128, 9, 1),
+                (4096, 4096, 8, 128, 0, 1), (4096, 4096, 8, 128, 4, 3)):
+        assert put([good, bad]) == B.ERR_ARG, bad
+    assert lib.iq4xs_set_mma_launch_table(None, 1) == B.ERR_ARG
+    assert put([good] * 257) == B.ERR_ARG
+    assert put([]) == B.OK
+    B.reset_dispatch()
+
+
 def test_mma_launch_config_validation(lib):
     r, sp, o = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     assert lib.iq4xs_mma_launch_config(8, 4096, 4096, None, ctypes.byref(sp), ctypes.byref(o)) == B.ERR_ARG

@@ -107,6 +107,22 @@ def test_matmul_mma_configs(rows, splits):
         B.iq4xs_test_mma_config(0, 0, 0)
 
 
+def test_mma_measured_launch_is_taken():
+    """An installed launch-table entry decides the launch for its exact shape
+    and tile height (and only there); the result still matches the oracle."""
+    rng = np.random.default_rng(31)
+    N, K = 600, 4608
+    w = synth.iq4xs_weights(rng, N, K, 1e-3)
+    try:
+        B.iq4xs_set_mma_launch_table([(N, K, 16, 96, 3, 1), (N, K, 8, 64, 2, 2)])
+        assert B.iq4xs_mma_launch_config(12, N, K) == (96, 3, 1)
+        assert B.iq4xs_mma_launch_config(5, N, K) == (64, 2, 2)
+        for M in (5, 12):
+            run_and_gate(w, N, K, synth.activations(rng, M, K), "mma")
+    finally:
+        B.reset_dispatch()
+
+
 def test_mma_launch_config_reports_the_launch():
     """The reported launch is the forced one when forced, and the model's
     own choice covers N with at most 256 rows per CTA and at most 8 splits."""
