@@ -412,10 +412,13 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
             }
             __syncwarp();
             if (gs + 1 < total) load_dx(gs + 1);  // in flight during this stage
-            // The four sub-blocks unrolled at one activation fragment (loads of
-            // the next sub-block's words overlap this one's lookups and MMAs:
-            // 5-6 % faster at 8 rows); one at a time at more (registers).
-            constexpr int kUnrollS = (NT == 1) ? kSPW : 1;
+            // The four sub-blocks unrolled (loads of the next sub-block's words
+            // overlap this one's lookups and MMAs: 5-6 % faster at 8 rows,
+            // 6-14 % at 16) where the registers allow it: one activation
+            // fragment, or two with at most four weight fragments per warp
+            // (not in the grouped form, which spills there); one at a time
+            // otherwise.
+            constexpr int kUnrollS = (NT == 1 || (NT == 2 && T <= 4 && !kGrouped)) ? kSPW : 1;
 #pragma unroll kUnrollS
             for (int s = 0; s < kSPW; ++s) {
                 const int j = sub_w + s;                 // sub-block within the stage
