@@ -120,3 +120,24 @@ def test_tensor_work_and_roofline_gate():
     g = bench.roofline_gate([("fast", 9.25e6, 0.5e-6), ("ok", 9.25e6, 2.0e-6)], 6800.0)
     assert not g["ok"] and [v["call"] for v in g["violations"]] == ["fast"]
     assert bench.roofline_gate([("ok", 9.25e6, 2.0e-6)], 6800.0)["ok"]
+
+
+def test_stored_launch_table_is_well_formed():
+    """The calibration's warp-MMA launches: six integers each, a tile height
+    of 8-32 rows, rows per CTA a multiple of 32 up to 256 (128 from 24
+    activation rows on), a K split the K range holds, one or two CTAs per SM;
+    at most one entry per (N, K, tile height)."""
+    from iq4_xs_quantized_gb300 import calibrate
+    table = calibrate.load_table()
+    if not table or "mma_launch" not in table:
+        pytest.skip("no calibrated table")
+    seen = set()
+    for e in table["mma_launch"]:
+        assert len(e) == 6 and all(isinstance(v, int) for v in e), e
+        N, K, mt, R, S, occ = e
+        assert N >= 1 and K % 512 == 0 and mt in (8, 16, 24, 32), e
+        assert R % 32 == 0 and 32 <= R <= (256 if mt <= 16 else 128), e
+        assert 1 <= S <= min(8, K // 512) and occ in (1, 2), e
+        assert (N, K, mt) not in seen, e
+        seen.add((N, K, mt))
+

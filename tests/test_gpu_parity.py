@@ -123,6 +123,17 @@ def test_mma_measured_launch_is_taken():
         B.reset_dispatch()
 
 
+def test_calibrated_launch_table_is_taken():
+    """Every measured launch the calibration stored is one the kernel holds,
+    and the call for that shape and tile height takes it."""
+    from iq4_xs_quantized_gb300 import calibrate
+    table = calibrate.load_table() or {}
+    entries = table.get("mma_launch", [])
+    B.reset_dispatch()
+    for N, K, mt, R, S, occ in entries:
+        assert B.iq4xs_mma_launch_config(mt, N, K) == (R, S, occ), (N, K, mt)
+
+
 def test_mma_launch_config_reports_the_launch():
     """The reported launch is the forced one when forced, and the model's
     own choice covers N with at most 256 rows per CTA and at most 8 splits."""
