@@ -125,11 +125,14 @@ __device__ __forceinline__ void mma_f16_16816(float d[4], const uint32_t a[4], u
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
           "f"(c[3]));
 }
-__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t local_addr, uint32_t rank) {
     uint32_t a;
-    float v;
+    float4 v;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local_addr), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a)
+                 : "memory");
     return v;
 }
 __device__ __forceinline__ void consumers_sync() {
@@ -548,17 +551,34 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
         cluster_arrive_release();
         cluster_wait();
         if (warp < kMmaConsumers && !*abort_flag) {
+            // Four activation rows of one weight row per item: the S ranks'
+            // 16-byte slices are all requested before any is summed.
             const int r0 = R * (int)rank / S, r1 = R * ((int)rank + 1) / S;
             const int64_t mrows = row_hi - row_lo;  // one tile (K splits only without experts)
-            for (int e = threadIdx.x; e < (r1 - r0) * kMt; e += 32 * kMmaConsumers) {
-                const int r = r0 + e % (r1 - r0), m = e / (r1 - r0);
+            for (int e = threadIdx.x; e < (r1 - r0) * (kMt / 4); e += 32 * kMmaConsumers) {
+                const int r = r0 + e % (r1 - r0), m = 4 * (e / (r1 - r0));
                 const uint32_t off = sbase + (uint32_t)((r * C::kRedStride + m) * 4);
-                float v = 0.f;
-                if (bc_range(bc, (r * C::kRedStride + m) * 4, 4, R * C::kRedStride * 4, kBcMmaSplit))
-                    for (int q = 0; q < S; ++q) v += ld_cluster_f32(off, (uint32_t)q);
-                if (m < mrows && n0 + r < N &&
-                    bc_global(bc, y + (row_lo + m) * ldy + n0 + r, 4, y, ((M - 1) * ldy + N) * 4, kBcMmaY))
-                    y[(row_lo + m) * ldy + n0 + r] = v;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (bc_range(bc, (r * C::kRedStride + m) * 4, 16, R * C::kRedStride * 4, kBcMmaSplit)) {
+                    float4 part[kMmaMaxCluster];
+#pragma unroll
+                    for (int q = 0; q < kMmaMaxCluster; ++q)
+                        if (q < S) part[q] = ld_cluster_f32x4(off, (uint32_t)q);
+#pragma unroll
+                    for (int q = 0; q < kMmaMaxCluster; ++q)
+                        if (q < S) {
+                            v.x += part[q].x;
+                            v.y += part[q].y;
+                            v.z += part[q].z;
+                            v.w += part[q].w;
+                        }
+                }
+                const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (m + i < mrows && n0 + r < N &&
+                        bc_global(bc, y + (row_lo + m + i) * ldy + n0 + r, 4, y, ((M - 1) * ldy + N) * 4, kBcMmaY))
+                        y[(row_lo + m + i) * ldy + n0 + r] = vv[i];
             }
         }
         __syncwarp();
