@@ -714,8 +714,8 @@ def decode_stream(torch, B, dev, reps=5):
 def moe_grouped(torch, B, dev, layers=12, reps=5, tokens=(1, 4, 16, 64, 256)):
     """Routed-expert layer (128 experts of 1536 x 2048, top-8): per token
     count T, one layer call = quantize the T*8 routed rows + the grouped
-    matmul in one launch (the dispatcher's form, and the CUDA-core and
-    warp-MMA forms forced), against the same layer with one launch per
+    matmul in one launch (the dispatcher's form, and the CUDA-core,
+    warp-MMA and tcgen05 forms forced), against the same layer with one launch per
     routed expert (each on the dispatcher's path for its rows).  `layers`
     copies of the expert set (2.6 GB) rotate so the touched experts' bytes
     exceed L2.  GB/s counts the touched experts' weights plus activations
@@ -753,7 +753,8 @@ def moe_grouped(torch, B, dev, layers=12, reps=5, tokens=(1, 4, 16, 64, 256)):
 
         times = {}
         for name, fn in (("grouped", grouped("auto")), ("grouped_dp4a", grouped("dp4a")),
-                         ("grouped_mma", grouped("mma")), ("per_expert", per_expert)):
+                         ("grouped_mma", grouped("mma")), ("grouped_tc", grouped("tc")),
+                         ("per_expert", per_expert)):
             with torch.cuda.stream(stream):
                 fn(stream)
             torch.cuda.synchronize()
@@ -773,11 +774,13 @@ def moe_grouped(torch, B, dev, layers=12, reps=5, tokens=(1, 4, 16, 64, 256)):
         nbytes = (len(touched) * W.N * (W.K // 256) * 136 + M * W.K + M * (W.K // 32) * 4
                   + 4 * M * W.N + quantize_bytes(M, W.K))
         mean = -(-M // min(W.G, M))
-        auto = "mma" if M >= W.G or B.iq4xs_select_path(mean, W.N, W.K) != B.PATH_DP4A else "dp4a"
+        auto = ("tc" if mean > 96 else "mma") if M >= W.G or B.iq4xs_select_path(mean, W.N, W.K) != B.PATH_DP4A \
+            else "dp4a"
         res.append({"tokens": T, "rows": M, "experts_touched": len(touched), "auto_form": auto,
                     "grouped_us_per_layer": round(times["grouped"], 3),
                     "grouped_dp4a_us": round(times["grouped_dp4a"], 3),
                     "grouped_mma_us": round(times["grouped_mma"], 3),
+                    "grouped_tc_us": round(times["grouped_tc"], 3),
                     "per_expert_launches_us_per_layer": round(times["per_expert"], 3),
                     "grouped_GBps": round(nbytes / (times["grouped"] * 1e-6) / 1e9, 1)})
     del ws

@@ -235,9 +235,11 @@ int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t
  * when K % 512 == 0 and either total_rows >= G (at least one row per expert
  * on average) or the mean rows per expert that has rows (total_rows /
  * min(G, total_rows)) exceeds the DP4A crossover of one expert's matrix
- * size, the warp-level MMA kernel in its grouped form (one CTA per (row
- * tile, expert), the expert's rows in activation tiles of up to 32; each
- * sub-block's dot is exact as on the MMA path of iq4xs_matmul).
+ * size, a tensor-core form: the warp-level MMA kernel in its grouped form
+ * (one CTA per (row tile, expert), the expert's rows in activation tiles
+ * of up to 32) up to 96 mean rows per expert slot, the tcgen05 kernel's
+ * grouped form above; each sub-block's dot is exact as on those paths of
+ * iq4xs_matmul.
  */
 int iq4xs_matmul_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
                          const int8_t* qs, const void* ds, const int32_t* row_offsets,
@@ -245,8 +247,13 @@ int iq4xs_matmul_grouped(const void* w, int64_t expert_stride, int64_t G, int64_
 
 /*
  * iq4xs_matmul_grouped with the path chosen by the caller: IQ4XS_PATH_AUTO
- * (the rule above), IQ4XS_PATH_DP4A or IQ4XS_PATH_MMA (K % 512 == 0, else
- * IQ4XS_ERR_SHAPE; qs 16-byte aligned); other values IQ4XS_ERR_ARG.
+ * (the rule above), IQ4XS_PATH_DP4A, IQ4XS_PATH_MMA or IQ4XS_PATH_TC (the
+ * last two need K % 512 == 0, else IQ4XS_ERR_SHAPE; qs 16-byte aligned);
+ * other values IQ4XS_ERR_ARG.  IQ4XS_PATH_TC is the tcgen05 kernel in its
+ * Q8_1 form: the layer's activation tiles (tc tile height from the mean
+ * rows per expert slot, 16..128) each one CTA per 128 weight rows of its
+ * expert, no K split; each sub-block's dot is exact as on that path of
+ * iq4xs_matmul.
  */
 int iq4xs_matmul_grouped_path(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
                               const int8_t* qs, const void* ds, const int32_t* row_offsets,
@@ -419,9 +426,10 @@ int iq4xs_last_device_error(int* code_out);
  * the dp4a matmul (W, qs, ds, y, row_offsets, an expert's rows outside y);
  * 0x30-0x39 the warp-MMA matmul (W box, W box alignment, code box, code box
  * alignment, ds, y, row_offsets, an expert's rows, shared-memory size,
- * split-K tile); 0x40-0x49 the tcgen05 matmul (W box, W box alignment,
+ * split-K tile); 0x40-0x4A the tcgen05 matmul (W box, W box alignment,
  * code box, code box alignment, prepared operand, ds, y, span scales,
- * shared-memory size, split-K slices).  A TMA box reaching past its tensor
+ * shared-memory size, split-K slices, grouped row_offsets or an expert's
+ * rows).  A TMA box reaching past its tensor
  * is recorded but still copied (the copy unit fills the rest); a box origin
  * off the 16-byte grid is recorded and not copied, and that stage's bounded
  * wait then runs out.  Results are those of the normal build whenever

@@ -286,7 +286,7 @@ def iq4xs_matmul_grouped(w, expert_stride: int, G: int, N: int, K: int, qs, ds, 
     g * expert_stride of w) over the Q8_1 rows [row_offsets[g],
     row_offsets[g+1]) (row_offsets: int32 device tensor [G+1]); y holds
     every row (its row count bounds the number of non-empty experts).
-    path: AUTO, DP4A or MMA (iq4xs_matmul_grouped_path)."""
+    path: AUTO, DP4A, MMA or TC (iq4xs_matmul_grouped_path)."""
     if row_offsets.dtype != torch.int32:
         raise TypeError("row_offsets must be int32")
     if isinstance(path, str):

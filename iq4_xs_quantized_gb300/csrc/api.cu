@@ -19,6 +19,7 @@ __device__ __align__(16) int g_device_error[kErrWords] = {0, 0, 0, 0};
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int64_t kGroupedTcMinRows = 96;  // grouped: tcgen05 above this mean rows per expert slot
 constexpr int64_t kMaxM = 32768;
 
 struct DevState {
@@ -293,7 +294,8 @@ int iq4xs_matmul_grouped_path(const void* w, int64_t expert_stride, int64_t G, i
                               const int8_t* qs, const void* ds, const int32_t* row_offsets,
                               int64_t total_rows, float* y, int64_t ldy, int path, int64_t stream) {
     if (!w || !qs || !ds || !row_offsets || !y) return IQ4XS_ERR_ARG;
-    if (path != IQ4XS_PATH_AUTO && path != IQ4XS_PATH_DP4A && path != IQ4XS_PATH_MMA) return IQ4XS_ERR_ARG;
+    if (path != IQ4XS_PATH_AUTO && path != IQ4XS_PATH_DP4A && path != IQ4XS_PATH_MMA && path != IQ4XS_PATH_TC)
+        return IQ4XS_ERR_ARG;
     if (G < 1 || G > 65535 || N < 1 || N > (1 << 30) || K <= 0 || K % kQK || K > (1 << 30))
         return IQ4XS_ERR_SHAPE;
     if (ldy < N || total_rows < 1) return IQ4XS_ERR_ARG;
@@ -305,17 +307,24 @@ int iq4xs_matmul_grouped_path(const void* w, int64_t expert_stride, int64_t G, i
         // The warp-MMA form once there are at least as many rows as experts
         // (measured on a 128 x 1536 x 2048 layer: from 128 rows on; at 512
         // rows it takes half the time of the CUDA-core form), or once the
-        // mean rows of an expert slot leave one expert matrix's DP4A range.
+        // mean rows of an expert slot leave one expert matrix's DP4A range;
+        // the tcgen05 form above 96 mean rows per expert slot (the same
+        // layer: equal at 64, 17 % faster at 256).
         const int64_t slots = G < total_rows ? G : total_rows;
         const int64_t mean = (total_rows + slots - 1) / slots;
-        path = (K % kPairK == 0 && (total_rows >= G || mean > crossover_for(N, K))) ? IQ4XS_PATH_MMA
-                                                                                   : IQ4XS_PATH_DP4A;
+        if (K % kPairK == 0 && (total_rows >= G || mean > crossover_for(N, K)))
+            path = mean > kGroupedTcMinRows ? IQ4XS_PATH_TC : IQ4XS_PATH_MMA;
+        else
+            path = IQ4XS_PATH_DP4A;
     }
-    if (path == IQ4XS_PATH_MMA && K % kPairK) return IQ4XS_ERR_SHAPE;
+    if ((path == IQ4XS_PATH_MMA || path == IQ4XS_PATH_TC) && K % kPairK) return IQ4XS_ERR_SHAPE;
     DevState* st;
     int rc = device_state(&st);
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (path == IQ4XS_PATH_TC)
+        return from_cuda(launch_matmul_tc_grouped(w, expert_stride, G, N, K, qs, ds, row_offsets, total_rows, y,
+                                                  ldy, st->encode, st->err, s));
     if (path == IQ4XS_PATH_MMA)
         return from_cuda(launch_matmul_mma_grouped(w, expert_stride, G, N, K, qs, ds, row_offsets, total_rows,
                                                    y, ldy, st->encode, st->err, st->num_sms, s));

@@ -236,7 +236,7 @@ enum BoundsSite : int {
     kBcMmaW = 0x30, kBcMmaWAlign, kBcMmaQ, kBcMmaQAlign, kBcMmaDs, kBcMmaY, kBcMmaOffsets,
     kBcMmaRows, kBcMmaSmem, kBcMmaSplit,
     kBcTcW = 0x40, kBcTcWAlign, kBcTcQ, kBcTcQAlign, kBcTcOp, kBcTcDs, kBcTcY, kBcTcSpan,
-    kBcTcSmem, kBcTcRecv,
+    kBcTcSmem, kBcTcRecv, kBcTcRows,
 };
 #ifdef IQ4XS_BOUNDS_CHECK
 constexpr bool kBoundsCheck = true;
@@ -562,6 +562,15 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, in
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
         "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+// 3D tiled TMA load (coordinates x, y, z) into this CTA's shared memory,
+// completing on `bar` (the experts of a grouped launch: z = expert).
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, int x, int yc, int zc, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(x), "r"(yc), "r"(zc), "r"(smem_u32(bar))
         : "memory");
 }
 // Contiguous bulk copy global -> this CTA's shared memory (16-byte aligned
@@ -1032,6 +1041,13 @@ cudaError_t launch_matmul_mma_grouped(const void* w, int64_t expert_stride, int6
                                       const int8_t* qs, const void* ds, const int32_t* row_offsets,
                                       int64_t total_rows, float* y, int64_t ldy, void* encode, int* err,
                                       int num_sms, cudaStream_t stream);
+// Grouped (mixture-of-experts) matmul on the tcgen05 kernel (Q8_1 form,
+// IQ4_XS, K % 512 == 0): activation tiles of tc_mtile(mean rows per expert
+// slot) rows, one CTA per (row tile, expert tile), no K split.
+cudaError_t launch_matmul_tc_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
+                                     const int8_t* qs, const void* ds, const int32_t* row_offsets,
+                                     int64_t total_rows, float* y, int64_t ldy, void* encode, int* err,
+                                     cudaStream_t stream);
 // Test override of the warp-MMA launch: weight rows per CTA, K splits and
 // CTAs per SM (1, 2); 0 = the launch model's choice.
 void mma_force_config(int rows_per_cta, int k_splits, int ctas_per_sm);

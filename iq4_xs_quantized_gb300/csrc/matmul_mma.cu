@@ -140,15 +140,6 @@ __device__ __forceinline__ void consumers_sync() {
 }
 // Consumers and producer between two activation tiles of one CTA.
 __device__ __forceinline__ void tile_sync() { asm volatile("bar.sync 2, %0;" ::"n"(kMmaThreads) : "memory"); }
-// 3D tiled TMA load (coordinates x, y, z) into this CTA's shared memory.
-__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, int x, int yc, int zc, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
-        "l"(tmap), "r"(x), "r"(yc), "r"(zc), "r"(smem_u32(bar))
-        : "memory");
-}
-
 // kGrouped: mixture-of-experts form.  Expert slot z (grid z) takes the z-th
 // expert that has rows (row_offsets, a device array read after the wait for
 // the preceding grid); W is that expert's matrix (a 3D tensor map over the

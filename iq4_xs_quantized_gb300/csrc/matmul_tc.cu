@@ -54,6 +54,8 @@
 // and frees its tensor memory, and the call's output is undefined.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "internal.cuh"
 
 namespace iq4xs {
@@ -252,12 +254,13 @@ __device__ __forceinline__ void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-template <int MT, int WT, bool kPrep>
+template <int MT, int WT, bool kPrep, bool kGrouped = false>
 __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
     matmul_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                      const __grid_constant__ CUtensorMap tmap_q, const __half* __restrict__ ds,
                      const uint8_t* __restrict__ tc_op, int64_t M, int N, int K,
-                     float* __restrict__ y, int64_t ldy, int* err, int skip_w_stage) {
+                     float* __restrict__ y, int64_t ldy, int* err, int skip_w_stage,
+                     const int32_t* __restrict__ row_offsets, int G) {
     using C = TcCfg<MT, WT, kPrep>;
     constexpr int kDecGroups = C::kDecGroups, kDecWarps = C::kDecWarps;
     constexpr int kMmaWarp0 = C::kMmaWarp0, kMmaWarp1 = C::kMmaWarp1;
@@ -299,6 +302,55 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
     const uint32_t rank = (S > 1) ? cluster_ctarank() : 0;
     const int n0 = blockIdx.x * kTileN;
     const int z = blockIdx.z;  // activation tile
+    // Activation rows [row_lo, row_hi) of this CTA's tile (the tile holds
+    // the first MT of them).  Grouped form (kGrouped, mixture of experts, the
+    // Q8_1 form, no K split): tile z of the layer is tile t of expert g, the
+    // experts with rows taken in order and each covering ceil(rows / MT)
+    // tiles; W is expert g's matrix (a 3D tensor map), the rows its own.
+    // CTAs past the last tile return before any set-up.
+    static_assert(!kGrouped || (!kPrep && WT == kWtIQ4XS), "grouped: IQ4_XS codes in the Q8_1 form");
+    int gexp = 0;
+    using RowT = typename std::conditional<kGrouped, int, int64_t>::type;  // M <= 32768 rows
+    RowT row_lo = (RowT)z * MT, row_hi = (RowT)M;
+    if constexpr (kGrouped) {
+        int* grp = reinterpret_cast<int*>(smem + C::kOffMisc + 8);
+        if (warp == 0) {
+            griddep_wait();  // the offsets may come from the preceding grid
+            int found = -1, found_t = 0, before = 0;  // tiles of the experts already passed
+            for (int e0 = 0; e0 < G && found < 0; e0 += 32) {
+                const int e = e0 + lane;
+                int tiles = 0;
+                if (e < G && bc_global(bc, row_offsets + e, 8, row_offsets, (int64_t)(G + 1) * 4, kBcTcRows)) {
+                    const int lo = __ldg(row_offsets + e), hi = __ldg(row_offsets + e + 1);
+                    tiles = hi > lo ? (hi - lo + MT - 1) / MT : 0;
+                }
+                int incl = tiles;  // inclusive prefix sum over the 32 experts
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                const int zz = z - before;
+                const uint32_t mask = __ballot_sync(0xffffffffu, tiles > 0 && zz >= incl - tiles && zz < incl);
+                if (mask) {
+                    const int src = __ffs(mask) - 1;
+                    found = e0 + src;
+                    found_t = __shfl_sync(0xffffffffu, zz - (incl - tiles), src);
+                }
+                before += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) {
+                grp[0] = found;
+                grp[1] = found_t;
+            }
+        }
+        __syncthreads();
+        gexp = grp[0];
+        if (gexp < 0) return;  // past the layer's last tile (whole CTA; no cluster)
+        row_lo = __ldg(row_offsets + gexp) + grp[1] * MT;
+        row_hi = __ldg(row_offsets + gexp + 1);
+        if (!bc_range(bc, row_lo, row_hi - row_lo, M, kBcTcRows)) return;  // offsets outside the rows of y
+    }
     const int pairs = K / kPairK;
     const int p0 = (int)((int64_t)pairs * rank / S);
     const int p1 = (int)((int64_t)pairs * (rank + 1) / S);
@@ -315,7 +367,11 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
 #pragma unroll
         for (int b = 0; b < C::kWBoxes; ++b) {
             const int x = (p0 + ps) * (C::kWRowBytes / 4) + b * (C::kWBoxBytes / 4);
-            if (bc_tma(bc, x, 4, C::kWBoxBytes / 4, wt_row_bytes(WT, K) / 4, n0, N, kBcTcWAlign, kBcTcW))
+            if (!bc_tma(bc, x, 4, C::kWBoxBytes / 4, wt_row_bytes(WT, K) / 4, n0, N, kBcTcWAlign, kBcTcW)) continue;
+            if constexpr (kGrouped)
+                tma_load_3d(smem + C::kOffW + slot * C::kWStage + b * (kTileN * C::kWBoxBytes), &tmap_w, x, n0, gexp,
+                            &w_full[slot]);
+            else
                 tma_load_2d(smem + C::kOffW + slot * C::kWStage + b * (kTileN * C::kWBoxBytes), &tmap_w, x, n0,
                             &w_full[slot]);
         }
@@ -385,9 +441,9 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
 #pragma unroll
             for (int k = 0; k < C::kXItems; ++k) {
                 const int e = lane + 32 * k;
-                const int64_t row = (int64_t)z * MT + e / kBStageSubs;
+                const int64_t row = row_lo + e / kBStageSubs;
                 const uint32_t* dp = ds32 + row * K32 + sub0 + e % kBStageSubs;
-                dsv[k] = (e < kBStageSubs * MT && row < M && bc_global(bc, dp, 4, ds, M * K32 * 4, kBcTcDs))
+                dsv[k] = (e < kBStageSubs * MT && row < row_hi && bc_global(bc, dp, 4, ds, M * K32 * 4, kBcTcDs))
                              ? __ldg(dp)
                              : 0u;
             }
@@ -627,8 +683,9 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
                     } else {
                         const int x = (p0 * kSubPerPair + bs * kBStageSubs) * kSub;
                         mbar_arrive_expect_tx(&q_full[slot], C::kQRawBytes);
-                        if (bc_tma(bc, x, 1, kBStageSubs * kSub, K, (int64_t)z * MT, M, kBcTcQAlign, kBcTcQ))
-                            tma_load_2d(smem + C::kOffB + slot * C::kBSlotBytes, &tmap_q, x, z * MT, &q_full[slot]);
+                        if (bc_tma(bc, x, 1, kBStageSubs * kSub, K, row_lo, M, kBcTcQAlign, kBcTcQ))
+                            tma_load_2d(smem + C::kOffB + slot * C::kBSlotBytes, &tmap_q, x, (int)row_lo,
+                                        &q_full[slot]);
                     }
                 };
                 // At most three activation stages go out before the W stages
@@ -867,15 +924,14 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
         }
         // Partial tile -> y (one CTA), or staged in this CTA's activation
         // ring (free: every MMA has completed) for the split-K reduction.
-        const int64_t mrows = M - (int64_t)z * MT;
+        const int64_t mrows = row_hi - row_lo;
         if (S == 1) {
             griddep_wait();
 #pragma unroll
             for (int m = 0; m < kMH; ++m)
                 if (c0 + m < mrows && n0 + t < N &&
-                    bc_global(bc, y + ((int64_t)z * MT + c0 + m) * ldy + n0 + t, 4, y, ((M - 1) * ldy + N) * 4,
-                              kBcTcY))
-                    y[((int64_t)z * MT + c0 + m) * ldy + n0 + t] = acc[m];
+                    bc_global(bc, y + (row_lo + c0 + m) * ldy + n0 + t, 4, y, ((M - 1) * ldy + N) * 4, kBcTcY))
+                    y[(row_lo + c0 + m) * ldy + n0 + t] = acc[m];
         } else {
             float* st = reinterpret_cast<float*>(smem + C::kOffStage) + t * C::kRedStride + c0;
 #pragma unroll
@@ -924,7 +980,7 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
         if (warp < kDecWarps || warp >= kEpiWarp0) {
             griddep_wait();
             const int idx = (warp < kDecWarps) ? threadIdx.x : threadIdx.x - (kEpiWarp0 - kDecWarps) * 32;
-            const int64_t mrows = M - (int64_t)z * MT;
+            const int64_t mrows = row_hi - row_lo;
             const float* stg = reinterpret_cast<const float*>(smem + C::kOffStage);
             const float* recv = reinterpret_cast<const float*>(smem + C::kOffRecv);
             const int r0 = (int)(kTileN * rank / S), r1 = (int)(kTileN * (rank + 1) / S);
@@ -952,9 +1008,9 @@ __global__ void __launch_bounds__(TcCfg<MT, WT, kPrep>::kThreads, 1)
                 // rows m .. last of y (the checked build checks the first and the last)
                 const int64_t y_ext = ((M - 1) * ldy + N) * 4, last = (m + 3 < mrows) ? m + 3 : mrows - 1;
                 if (n0 + row < N && m < mrows &&
-                    bc_global(bc, y + ((int64_t)z * MT + m) * ldy + n0 + row, 4, y, y_ext, kBcTcY) &&
-                    bc_global(bc, y + ((int64_t)z * MT + last) * ldy + n0 + row, 4, y, y_ext, kBcTcY)) {
-                    float* yp = y + ((int64_t)z * MT + m) * ldy + n0 + row;
+                    bc_global(bc, y + (row_lo + m) * ldy + n0 + row, 4, y, y_ext, kBcTcY) &&
+                    bc_global(bc, y + (row_lo + last) * ldy + n0 + row, 4, y, y_ext, kBcTcY)) {
+                    float* yp = y + (row_lo + m) * ldy + n0 + row;
                     if (m < mrows) yp[0] = sum.x;
                     if (m + 1 < mrows) yp[ldy] = sum.y;
                     if (m + 2 < mrows) yp[2 * ldy] = sum.z;
@@ -1035,6 +1091,37 @@ int choose_split(int dev, int fallback, int units, int pairs) {
     return best;
 }
 
+// Grouped launch of the <MT> Q8_1-form kernel: grid (row tiles, 1, tiles)
+// with `tiles` an upper bound of the layer's expert tiles.
+template <int MT>
+cudaError_t launch_grouped_mt(const CUtensorMap& tmap_w, const CUtensorMap& tmap_q, const __half* ds,
+                              const int32_t* row_offsets, int G, int64_t total_rows, int N, int K, float* y,
+                              int64_t ldy, int* err, int ntiles, int tiles, cudaStream_t stream) {
+    using C = TcCfg<MT, kWtIQ4XS, false>;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(matmul_tc_kernel<MT, kWtIQ4XS, false, true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ntiles, 1, (unsigned)tiles);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, matmul_tc_kernel<MT, kWtIQ4XS, false, true>, tmap_w, tmap_q, ds,
+                              static_cast<const uint8_t*>(nullptr), total_rows, N, K, y, ldy, err, -1, row_offsets,
+                              G);
+}
+
 template <int MT, int WT, bool kPrep>
 cudaError_t launch_mt(const CUtensorMap& tmap_w, const CUtensorMap& tmap_q, const __half* ds,
                       const uint8_t* op, int64_t M, int N, int K, float* y, int64_t ldy, int* err, int S,
@@ -1065,7 +1152,7 @@ cudaError_t launch_mt(const CUtensorMap& tmap_w, const CUtensorMap& tmap_q, cons
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, matmul_tc_kernel<MT, WT, kPrep>, tmap_w, tmap_q, ds, op, M, N, K, y,
-                              ldy, err, skip);
+                              ldy, err, skip, static_cast<const int32_t*>(nullptr), 0);
 }
 
 template <int WT, bool kPrep>
@@ -1155,6 +1242,65 @@ cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const 
                                      stream);
     return launch_form<kWtIQ4XS>(tmap_w, tmap_q, dsh, op, M, Ni, Ki, y, ldy, err, S, ntiles, mtiles, skip,
                                  stream);
+}
+
+cudaError_t launch_matmul_tc_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
+                                     const int8_t* qs, const void* ds, const int32_t* row_offsets,
+                                     int64_t total_rows, float* y, int64_t ldy, void* encode, int* err,
+                                     cudaStream_t stream) {
+    const EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(encode);
+    const int64_t row_bytes = wt_row_bytes(kWtIQ4XS, K);
+    // W of expert g: a 3D map (row words x rows x experts, expert_stride
+    // bytes apart), one box = 128 rows x one super-block pair of one expert.
+    CUtensorMap tmap_w;
+    {
+        const cuuint64_t gdim[3] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)N, (cuuint64_t)G};
+        const cuuint64_t gstride[2] = {(cuuint64_t)row_bytes, (cuuint64_t)expert_stride};
+        const cuuint32_t box[3] = {(cuuint32_t)(kPairBytes / 4), (cuuint32_t)kTileN, 1};
+        const cuuint32_t estride[3] = {1, 1, 1};
+        if (enc(&tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(w), gdim, gstride, box, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    // at most min(G, rows) experts have rows; the tile height from the mean
+    // rows per such expert
+    const int64_t slots = G < total_rows ? G : total_rows;
+    const int64_t mean = (total_rows + slots - 1) / slots;
+    const int MT = tc_mtile(mean);
+    CUtensorMap tmap_q;
+    {
+        const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)total_rows};
+        const cuuint64_t gstride[1] = {(cuuint64_t)K};
+        const cuuint32_t box[2] = {(cuuint32_t)kQRowBytes, (cuuint32_t)MT};
+        const cuuint32_t estride[2] = {1, 1};
+        if (enc(&tmap_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qs), gdim, gstride, box, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    // an expert with r rows takes ceil(r / MT) <= r / MT + 1 tiles
+    const int64_t tiles = (total_rows + MT - 1) / MT + slots;
+    if (tiles > 65535) return cudaErrorInvalidValue;
+    const int ntiles = (int)((N + kTileN - 1) / kTileN);
+    const __half* dsh = reinterpret_cast<const __half*>(ds);
+    const int Ni = (int)N, Ki = (int)K, Gi = (int)G, Ti = (int)tiles;
+#define IQ4XS_TC_G(mt)                                                                                     \
+    case mt:                                                                                              \
+        return launch_grouped_mt<mt>(tmap_w, tmap_q, dsh, row_offsets, Gi, total_rows, Ni, Ki, y, ldy, err, \
+                                     ntiles, Ti, stream);
+    switch (MT) {
+        IQ4XS_TC_G(16)
+        IQ4XS_TC_G(32)
+        IQ4XS_TC_G(48)
+        IQ4XS_TC_G(64)
+        IQ4XS_TC_G(80)
+        IQ4XS_TC_G(96)
+        IQ4XS_TC_G(112)
+        IQ4XS_TC_G(128)
+        default: return cudaErrorInvalidValue;
+    }
+#undef IQ4XS_TC_G
 }
 
 }  // namespace iq4xs

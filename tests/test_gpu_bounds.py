@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 
 # site ranges of the kernels (code = 0x200 + site)
 SITES = {"quantize": (0x01, 0x05), "dequantize": (0x10, 0x11), "dp4a": (0x20, 0x25),
-         "mma": (0x30, 0x39), "tc": (0x40, 0x49)}
+         "mma": (0x30, 0x39), "tc": (0x40, 0x4A)}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -137,7 +137,7 @@ def test_block32_formats_clean(wt):
             _clean()
 
 
-@pytest.mark.parametrize("path", ("dp4a", "mma"))
+@pytest.mark.parametrize("path", ("dp4a", "mma", "tc"))
 @pytest.mark.parametrize("T,topk,G", [(20, 4, 8), (3, 2, 70), (64, 8, 8)])
 def test_grouped_clean(path, T, topk, G):
     W = synth.MoEWorkload("moe_bounds", seed=19, G=G, N=136, K=1024, topk=topk, tokens=(T,), d_scale=2e-3)
@@ -216,6 +216,6 @@ def test_margin_reports_every_kernel():
     offsets = dev(np.array([0, 5, 5, M], dtype=np.int32))
     stride = N * (K // 256) * 136
     wg = dev(np.concatenate([w] * 3))
-    for path in ("dp4a", "mma"):
+    for path in ("dp4a", "mma", "tc"):
         _under_margin(lambda: B.iq4xs_matmul_grouped(wg, stride, 3, N, K, qs, ds, offsets, y, path=path), path)
     _clean()

@@ -101,13 +101,35 @@ def test_grouped_mma_matches_oracle(T, topk):
     M = rows_x.shape[0]
     slots = min(W.G, M)
     mean = -(-M // slots)
-    auto = "mma" if M >= W.G or B.iq4xs_select_path(mean, W.N, W.K) != B.PATH_DP4A else "dp4a"
+    auto = ("tc" if mean > 96 else "mma") if M >= W.G or B.iq4xs_select_path(mean, W.N, W.K) != B.PATH_DP4A \
+        else "dp4a"
     y_auto = _run_grouped(W, rows_x, offsets)[-1]
-    y_expl = y if auto == "mma" else _run_grouped(W, rows_x, offsets, "dp4a")[-1]
+    y_expl = y if auto == "mma" else _run_grouped(W, rows_x, offsets, auto)[-1]
     assert np.array_equal(y_auto, y_expl), auto
 
 
-@pytest.mark.parametrize("path", ("dp4a", "mma"))
+@pytest.mark.parametrize("T,topk,G", [(64, 8, 8), (256, 8, 16), (1024, 4, 8), (40, 6, 8)])
+def test_grouped_tc_matches_oracle(T, topk, G):
+    """The tcgen05 form over per-expert batches from a few rows to several
+    128-row tiles (ragged N; tiles of the layer mapped to experts in-kernel),
+    against the oracle and an independent fp32 product."""
+    W = synth.MoEWorkload("moe_tc", seed=23, G=G, N=200, K=1024, topk=topk, tokens=(T,), d_scale=2e-3)
+    _, rows_x, offsets = W.inputs(T)
+    w, wd, qs, ds, y = _run_grouped(W, rows_x, offsets, "tc")
+    qs_o, d_o = _check_experts(W, w, rows_x, offsets, y)
+    ind = independent_fp32(np.concatenate([w[g] for g in range(W.G)]), W.G * W.N, W.K, qs_o, d_o)
+    ind_own = np.full_like(y, np.nan)
+    for g in range(W.G):
+        r0, r1 = int(offsets[g]), int(offsets[g + 1])
+        ind_own[r0:r1] = ind[r0:r1, g * W.N:(g + 1) * W.N]
+    assert gate_independent(y, ind_own) is None
+    # AUTO takes the tcgen05 form above 96 mean rows per expert slot
+    M = rows_x.shape[0]
+    if -(-M // min(W.G, M)) > 96:
+        assert np.array_equal(_run_grouped(W, rows_x, offsets)[-1], y)
+
+
+@pytest.mark.parametrize("path", ("dp4a", "mma", "tc"))
 @pytest.mark.parametrize("G,T,topk", [(70, 5, 2), (100, 40, 3)])
 def test_grouped_many_experts_compacted_slots(G, T, topk, path):
     # more experts than a warp's ballot covers; fewer (and more) rows than experts
@@ -118,8 +140,8 @@ def test_grouped_many_experts_compacted_slots(G, T, topk, path):
     _check_experts(W, w, rows_x, offsets, y)
 
 
-@pytest.mark.parametrize("path", ("dp4a", "mma"))
-@pytest.mark.parametrize("rows", (11, 80))
+@pytest.mark.parametrize("path", ("dp4a", "mma", "tc"))
+@pytest.mark.parametrize("rows", (11, 80, 300))
 def test_grouped_empty_experts_and_one_expert_with_every_row(path, rows):
     """80 rows on one expert: five activation tiles of 16 rows in one CTA on
     the MMA form (the tile from the mean rows of the six expert slots)."""
@@ -148,11 +170,12 @@ def test_grouped_rejects_bad_arguments():
         B.iq4xs_matmul_grouped(w, stride, 0, W.N, W.K, qs, ds, off, y)
     assert e.value.status == B.ERR_SHAPE
     with pytest.raises(B.IQ4XSError) as e:
-        B.iq4xs_matmul_grouped(w, stride, 2, W.N, W.K, qs, ds, off, y, path=B.PATH_TC)
+        B.iq4xs_matmul_grouped(w, stride, 2, W.N, W.K, qs, ds, off, y, path=B.PATH_BASELINE)
     assert e.value.status == B.ERR_ARG
     W3 = synth.MoEWorkload("moe_k768", seed=1, G=2, N=128, K=768, topk=1, tokens=(2,), d_scale=2e-3)
     w3 = dev(W3.weights().reshape(2, -1))
     qs3, ds3 = B.alloc_activations(2, 768, "cuda")
-    with pytest.raises(B.IQ4XSError) as e:  # the MMA form needs K % 512 == 0
-        B.iq4xs_matmul_grouped(w3, w3.shape[1], 2, W3.N, 768, qs3, ds3, off, y, path="mma")
-    assert e.value.status == B.ERR_SHAPE
+    for p in ("mma", "tc"):  # the tensor-core forms need K % 512 == 0
+        with pytest.raises(B.IQ4XSError) as e:
+            B.iq4xs_matmul_grouped(w3, w3.shape[1], 2, W3.N, 768, qs3, ds3, off, y, path=p)
+        assert e.value.status == B.ERR_SHAPE
