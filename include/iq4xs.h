@@ -224,7 +224,7 @@ int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t
  *                 [row_offsets[g], row_offsets[g+1]); non-decreasing, read
  *                 by the kernel after the preceding grid completes (so it may
  *                 come from a routing kernel).
- *   total_rows    the number of rows (row_offsets[G] <= total_rows); at most
+ *   total_rows    the number of rows, 1..32768 (row_offsets[G] <= total_rows); at most
  *                 min(G, total_rows) experts have rows, and the launch has
  *                 that many expert slots, each taking the next non-empty
  *                 expert, so empty experts cost nothing.

@@ -299,6 +299,7 @@ int iq4xs_matmul_grouped_path(const void* w, int64_t expert_stride, int64_t G, i
     if (G < 1 || G > 65535 || N < 1 || N > (1 << 30) || K <= 0 || K % kQK || K > (1 << 30))
         return IQ4XS_ERR_SHAPE;
     if (ldy < N || total_rows < 1) return IQ4XS_ERR_ARG;
+    if (total_rows > kMaxM) return IQ4XS_ERR_SHAPE;  // the rows one quantize call takes
     if (expert_stride < N * (K / kQK) * kBlockBytes || expert_stride % 16) return IQ4XS_ERR_ARG;
     if (!aligned(w, 16) || !aligned(qs, 16) || !aligned(ds, 4) || !aligned(row_offsets, 4) ||
         !aligned(y, 4))

@@ -244,6 +244,17 @@ def test_mma_launch_config_validation(lib):
                                            ctypes.byref(o)) == B.ERR_SHAPE, (M, N, K)
 
 
+def test_largest_m_is_32768(lib):
+    p = ctypes.c_void_p(0x10000)
+    out = ctypes.c_int(-1)
+    assert lib.iq4xs_select_path(32769, 8, 256, ctypes.byref(out)) == B.ERR_SHAPE
+    assert lib.iq4xs_matmul(p, 8, 256, p, p, 32769, p, 8, 0, 0) == B.ERR_SHAPE
+    assert lib.iq4xs_quantize_q8_1(p, 32769, 256, 256, p, p, 0) == B.ERR_SHAPE
+    assert lib.iq4xs_quantize_q8_1_tc(p, 32769, 256, 256, p, p, p, 0) == B.ERR_SHAPE
+    assert lib.iq4xs_matmul_grouped(p, 16 * 136, 2, 8, 512, p, p, p, 32769, p, 8, 0) == B.ERR_SHAPE
+    assert lib.iq4xs_select_path(32768, 8, 256, ctypes.byref(out)) == B.OK
+
+
 def test_status_strings(lib):
     for s in range(8):
         assert B.iq4xs_status_string(s) != "unknown status"

@@ -298,6 +298,25 @@ def test_full_prefill(shape_index, M):
 
 
 # ------------------------------------------------------------------- dequantize
+def test_matmul_max_m_every_path():
+    """The largest M the boundary takes (32768 rows: 1024 warp-MMA activation
+    tiles, 256 tcgen05 tiles, 4096 dp4a passes) on a ragged N, every output
+    against the oracle."""
+    rng = np.random.default_rng(32768)
+    M, N, K = 32768, 135, 512
+    w = synth.iq4xs_weights(rng, N, K, 2e-3)
+    x = synth.activations(rng, M, K)
+    qs, ds = quantize_gpu(x)
+    qs_o, d_o = check_q8(x, qs, ds)
+    yo = oracle_matmul(w, N, K, qs_o, d_o)
+    op = prepare_gpu(x, qs, ds)
+    for path in PATHS:
+        y = matmul_gpu(dev(w), N, K, qs, ds, M, path, op=op if path == "tcp" else None)
+        assert gate_written(y) is None, path
+        r = gate_parity(y, yo)
+        assert r is None, (path, r)
+
+
 def test_dequantize_bit_exact():
     rng = np.random.default_rng(21)
     N, K = 300, 2048
