@@ -156,6 +156,28 @@ def test_grouped_empty_experts_and_one_expert_with_every_row(path, rows):
     assert gate_parity(y, oracle_matmul(w[2], W.N, W.K, qs_o, d_o)) is None
 
 
+@pytest.mark.parametrize("path", ("dp4a", "mma", "tc"))
+def test_grouped_padded_expert_stride_and_ldy(path):
+    """Experts 512 bytes apart beyond their matrices and y rows wider than N:
+    every form reads only its expert's rows and writes only columns < N."""
+    W = synth.MoEWorkload("moe_pad", seed=29, G=5, N=136, K=1024, topk=2, tokens=(150,), d_scale=2e-3)
+    _, rows_x, offsets = W.inputs(150)
+    w = W.weights()
+    G, N, K = W.G, W.N, W.K
+    mat = w.shape[1] * w.shape[2]
+    stride = mat + 512
+    buf = np.full((G, stride), 0xA5, dtype=np.uint8)  # the padding holds garbage blocks
+    buf[:, :mat] = w.reshape(G, -1)
+    qs, ds = quantize_gpu(rows_x)
+    M, ldy = rows_x.shape[0], N + 7
+    y = torch.full((M, ldy), float("nan"), dtype=torch.float32, device="cuda")
+    B.iq4xs_matmul_grouped(dev(buf), stride, G, N, K, qs, ds, dev(offsets.astype(np.int32)), y, path=path)
+    torch.cuda.synchronize()
+    yn = y.cpu().numpy()
+    assert np.all(np.isnan(yn[:, N:])), "columns beyond N must not be written"
+    _check_experts(W, w, rows_x, offsets, np.ascontiguousarray(yn[:, :N]))
+
+
 def test_grouped_rejects_bad_arguments():
     W = synth.MoEWorkload("moe_arg", seed=1, G=2, N=128, K=512, topk=1, tokens=(2,), d_scale=2e-3)
     w = dev(W.weights().reshape(2, -1))
