@@ -794,7 +794,9 @@ def weight_formats(torch, B, dev, stream, iq4xs_us, N=4096, K=4096, copies=48, r
     (18-byte blocks of 32, 0.5625 B/weight) on the dispatcher's path:
     device time per launch from graphs of back-to-back launches over
     `copies` rotating weight copies (452 MB, larger than L2), beside the
-    IQ4_XS time of the main sweep.  GB/s counts the format's weight bytes
+    IQ4_XS time of the main sweep.  Where the path is the tcgen05 kernel,
+    `us` is its prepared-operand form (as in the main sweep) and
+    `q8_form_us` the Q8_1 form.  GB/s counts the format's weight bytes
     plus the Q8_1 activations and fp32 outputs."""
     from iq4_xs_quantized_gb300 import synth
     res = []
@@ -810,24 +812,37 @@ def weight_formats(torch, B, dev, stream, iq4xs_us, N=4096, K=4096, copies=48, r
             qs, ds = B.alloc_activations(M, K, dev)
             B.iq4xs_quantize_q8_1(x, qs, ds, stream)
             y = torch.empty((M, N), dtype=torch.float32, device=dev)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for w in ws:
-                    B.iq4xs_matmul_wt(w, wt, N, K, qs, ds, M, y, B.PATH_AUTO, stream)
-            with torch.cuda.stream(stream):
-                g.replay()
-                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                t0.record(stream)
-                for _ in range(reps):
+            # above the dp4a range the 32-weight formats run the tcgen05 kernel
+            tc = B.iq4xs_select_path(M, N, K) != B.PATH_DP4A
+            op = None
+            if tc:
+                op = B.alloc_tc_operand(M, K, dev)
+                B.iq4xs_quantize_q8_1_tc(x, qs, ds, op, stream)
+
+            def timed(fn):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for w in ws:
+                        fn(w)
+                with torch.cuda.stream(stream):
                     g.replay()
-                t1.record(stream)
-            torch.cuda.synchronize()
-            us = t0.elapsed_time(t1) * 1e3 / (reps * copies)
+                    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    t0.record(stream)
+                    for _ in range(reps):
+                        g.replay()
+                    t1.record(stream)
+                torch.cuda.synchronize()
+                return t0.elapsed_time(t1) * 1e3 / (reps * copies)
+
+            q8_us = timed(lambda w: B.iq4xs_matmul_wt(w, wt, N, K, qs, ds, M, y, B.PATH_AUTO, stream))
+            us = timed(lambda w: B.iq4xs_matmul_tc_operand(w, N, K, op, M, y, wt, stream=stream)) if tc else q8_us
             nbytes = wbytes + M * K + M * (K // 32) * 4 + 4 * M * N
-            res.append({"format": name, "M": M, "us": round(us, 3),
-                        "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
-                        "iq4_xs_us": round(iq4xs_us[M], 3) if M in iq4xs_us else None})
-            del g
+            row = {"format": name, "M": M, "us": round(us, 3),
+                   "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                   "iq4_xs_us": round(iq4xs_us[M], 3) if M in iq4xs_us else None}
+            if tc:
+                row["q8_form_us"] = round(q8_us, 3)
+            res.append(row)
         del ws, w0
         torch.cuda.empty_cache()
     return res

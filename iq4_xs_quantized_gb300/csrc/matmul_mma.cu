@@ -466,12 +466,6 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
                             mma_f16_16816(p, a0, bfr[f][0], bfr[f][1], zero);
                             mma_f16_16816(p, a1, bfr[f][2], bfr[f][3], p);
                             // acc += (P * d_x) * d_w*(ls-32): rows g (p0, p1) and g+8 (p2, p3)
-#ifdef IQ4XS_MMA_SCALAR_FP
-                            acc[k][f][0] = __fmaf_rn(__fmul_rn(p[0], dx[f].x), sw.x, acc[k][f][0]);
-                            acc[k][f][1] = __fmaf_rn(__fmul_rn(p[1], dx[f].y), sw.x, acc[k][f][1]);
-                            acc[k][f][2] = __fmaf_rn(__fmul_rn(p[2], dx[f].x), sw.y, acc[k][f][2]);
-                            acc[k][f][3] = __fmaf_rn(__fmul_rn(p[3], dx[f].y), sw.y, acc[k][f][3]);
-#else
                             const float2 q01 = __fmul2_rn(make_float2(p[0], p[1]), dx[f]);
                             const float2 q23 = __fmul2_rn(make_float2(p[2], p[3]), dx[f]);
                             const float2 r01 =
@@ -480,7 +474,6 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
                                 __ffma2_rn(q23, make_float2(sw.y, sw.y), make_float2(acc[k][f][2], acc[k][f][3]));
                             acc[k][f][0] = r01.x; acc[k][f][1] = r01.y;
                             acc[k][f][2] = r23.x; acc[k][f][3] = r23.y;
-#endif
                         }
                     }
                 }
