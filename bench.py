@@ -794,10 +794,11 @@ def weight_formats(torch, B, dev, stream, iq4xs_us, N=4096, K=4096, copies=48, r
     (18-byte blocks of 32, 0.5625 B/weight) on the dispatcher's path:
     device time per launch from graphs of back-to-back launches over
     `copies` rotating weight copies (452 MB, larger than L2), beside the
-    IQ4_XS time of the main sweep.  Where the path is the tcgen05 kernel,
-    `us` is its prepared-operand form (as in the main sweep) and
-    `q8_form_us` the Q8_1 form.  GB/s counts the format's weight bytes
-    plus the Q8_1 activations and fp32 outputs."""
+    IQ4_XS time of the main sweep; `path` names the kernel (dp4a, mma,
+    tc).  Where the path is the tcgen05 kernel, `us` is its
+    prepared-operand form (as in the main sweep) and `q8_form_us` the Q8_1
+    form.  GB/s counts the format's weight bytes plus the Q8_1 activations
+    and fp32 outputs."""
     from iq4_xs_quantized_gb300 import synth
     res = []
     for name in ("q4_0", "iq4_nl"):
@@ -812,8 +813,9 @@ def weight_formats(torch, B, dev, stream, iq4xs_us, N=4096, K=4096, copies=48, r
             qs, ds = B.alloc_activations(M, K, dev)
             B.iq4xs_quantize_q8_1(x, qs, ds, stream)
             y = torch.empty((M, N), dtype=torch.float32, device=dev)
-            # above the dp4a range the 32-weight formats run the tcgen05 kernel
-            tc = B.iq4xs_select_path(M, N, K) != B.PATH_DP4A
+            # the 32-weight formats take the dispatcher's path for the shape
+            path = B.iq4xs_select_path(M, N, K)
+            tc = path in (B.PATH_TC, B.PATH_BASELINE)
             op = None
             if tc:
                 op = B.alloc_tc_operand(M, K, dev)
@@ -837,7 +839,8 @@ def weight_formats(torch, B, dev, stream, iq4xs_us, N=4096, K=4096, copies=48, r
             q8_us = timed(lambda w: B.iq4xs_matmul_wt(w, wt, N, K, qs, ds, M, y, B.PATH_AUTO, stream))
             us = timed(lambda w: B.iq4xs_matmul_tc_operand(w, N, K, op, M, y, wt, stream=stream)) if tc else q8_us
             nbytes = wbytes + M * K + M * (K // 32) * 4 + 4 * M * N
-            row = {"format": name, "M": M, "us": round(us, 3),
+            row = {"format": name, "M": M, "path": "tc" if tc else ("mma" if path == B.PATH_MMA else "dp4a"),
+                   "us": round(us, 3),
                    "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
                    "iq4_xs_us": round(iq4xs_us[M], 3) if M in iq4xs_us else None}
             if tc:

@@ -105,7 +105,8 @@ typedef enum {
                                decoded weights go straight from the byte-table
                                lookup into the MMA's registers and every
                                sub-block's exact integer dot is scaled in from
-                               registers (small and medium M; IQ4_XS only)    */
+                               registers (small and medium M; every weight
+                               format)                                        */
 } iq4xs_path;
 
 /*
@@ -171,8 +172,8 @@ int64_t iq4xs_tc_operand_bytes(int64_t M, int64_t K);
  *           IQ4XS_ERR_ARG.
  * The TC and MMA paths need K % 512 == 0 (they stage W rows by tensor map,
  * whose row stride must be a multiple of 16 bytes: super-blocks in pairs),
- * else IQ4XS_ERR_SHAPE; MMA takes IQ4_XS weights only; DP4A takes any
- * K % 256 == 0.
+ * else IQ4XS_ERR_SHAPE; DP4A takes any K % 256 == 0.  Every path takes
+ * every weight format.
  * Result: each sub-block's dot sum_i kv*q is an exact integer on every path
  * (int32 on DP4A; on TC and MMA exact in the tensor core's fp32 accumulator,
  * every partial sum being an integer below 2^24); the scaled sub-block terms
@@ -342,8 +343,8 @@ int iq4xs_dequantize_wt(const void* w, int wtype, int64_t N, int64_t K, void* ou
  * crossover (iq4xs_set_mma_crossover, iq4xs_set_mma_crossover_classes);
  * BASELINE when M >= the calibrated baseline threshold (0 = never); TC
  * otherwise.  K % 512 != 0 always gives DP4A (neither tensor-core path takes
- * it).  For Q4_0 / IQ4_NL weights (iq4xs_matmul_wt with AUTO) an MMA answer
- * becomes TC.
+ * it).  Q4_0 / IQ4_NL weights (iq4xs_matmul_wt with AUTO) take the same
+ * path as IQ4_XS weights of the same shape.
  */
 int iq4xs_select_path(int64_t M, int64_t N, int64_t K, int* path_out);
 
@@ -492,7 +493,9 @@ int iq4xs_set_mma_launch_table(const int64_t* entries, int count);
  * per CTA, CTAs per cluster along K, and CTAs per SM, as the call would
  * take them (forced by iq4xs_test_mma_config, else from the measured
  * launch table, else from the launch model) for activation tiles of
- * min(32, M rounded up to 8) rows.  Host only; queries the device's
+ * min(32, M rounded up to 8) rows, for IQ4_XS weights (Q4_0 / IQ4_NL
+ * launches choose among a subset of the configurations by the same model,
+ * with no measured table).  Host only; queries the device's
  * cluster occupancy once per configuration.  IQ4XS_ERR_SHAPE unless K %
  * 512 == 0 and the sizes are in range; IQ4XS_ERR_ARG for null outputs.
  */

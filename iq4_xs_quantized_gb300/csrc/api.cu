@@ -121,13 +121,14 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 inline int from_cuda(cudaError_t e) { return e == cudaSuccess ? IQ4XS_OK : IQ4XS_ERR_CUDA; }
 
 // The path this library's own kernels take: DP4A up to the matrix class's
-// DP4A crossover, the warp-MMA path (IQ4_XS only) up to its MMA crossover,
-// TC above.  Both tensor-core paths stage W rows with a tensor map, whose
-// row stride must be a multiple of 16 bytes: K % 512 == 0 (136-byte
-// super-blocks in pairs); other K run DP4A.
-int kernel_path_impl(int64_t M, int64_t N, int64_t K, int wtype = IQ4XS_WTYPE_IQ4_XS) {
+// DP4A crossover, the warp-MMA path up to its MMA crossover, TC above (the
+// crossovers measured on IQ4_XS serve the 18-byte-block formats too: their
+// kernels are the same but for the weight layout).  Both tensor-core paths
+// stage W rows with a tensor map, whose row stride must be a multiple of 16
+// bytes: K % 512 == 0 (136-byte super-blocks in pairs); other K run DP4A.
+int kernel_path_impl(int64_t M, int64_t N, int64_t K) {
     if (K % kPairK != 0 || M <= crossover_for(N, K)) return IQ4XS_PATH_DP4A;
-    if (wtype == IQ4XS_WTYPE_IQ4_XS && M <= mma_max_for(N, K)) return IQ4XS_PATH_MMA;
+    if (M <= mma_max_for(N, K)) return IQ4XS_PATH_MMA;
     return IQ4XS_PATH_TC;
 }
 // The advised path: the kernel path, or BASELINE above the measured threshold.
@@ -199,15 +200,15 @@ int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t
         return IQ4XS_ERR_SHAPE;
     if (ldy < N) return IQ4XS_ERR_ARG;
     if (!aligned(w, 16) || !aligned(qs, 16) || !aligned(ds, 4) || !aligned(y, 4)) return IQ4XS_ERR_ALIGN;
-    if (path == IQ4XS_PATH_AUTO) path = kernel_path_impl(M, N, K, wtype);
+    if (path == IQ4XS_PATH_AUTO) path = kernel_path_impl(M, N, K);
     if ((path == IQ4XS_PATH_TC || path == IQ4XS_PATH_MMA) && K % kPairK) return IQ4XS_ERR_SHAPE;
-    if (path == IQ4XS_PATH_MMA && wtype != IQ4XS_WTYPE_IQ4_XS) return IQ4XS_ERR_SHAPE;
     DevState* st;
     int rc = device_state(&st);
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (path == IQ4XS_PATH_MMA)
-        return from_cuda(launch_matmul_mma(w, N, K, qs, ds, M, y, ldy, st->encode, st->err, st->num_sms, s));
+        return from_cuda(
+            launch_matmul_mma(w, wtype, N, K, qs, ds, M, y, ldy, st->encode, st->err, st->num_sms, s));
     if (path == IQ4XS_PATH_TC)
         return from_cuda(launch_matmul_tc(w, wtype, N, K, qs, ds, nullptr, M, y, ldy, st->encode,
                                           st->err, st->num_sms, g_skip_w_stage.exchange(-1), s));

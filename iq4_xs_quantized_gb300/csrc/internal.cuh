@@ -1030,9 +1030,9 @@ bool pdl_enabled();
 // TMA) when tc_operand is NULL, else the prepared operand alone (qs, ds
 // unused).  skip_w_stage >= 0 leaves that W stage of every CTA unissued
 // (tests of the bounded waits); -1 in every ordinary call.
-// Warp-level MMA path (IQ4_XS only): activation tiles of mma_tile_rows(M)
-// rows (8, 16, 24 or 32); any K % 256 == 0; qs 16-byte aligned (staged by
-// TMA), ds read directly.
+// Warp-level MMA path (every weight format wt): activation tiles of
+// mma_tile_rows(M) rows (8, 16, 24 or 32); K % 512 == 0; qs 16-byte aligned
+// (staged by TMA), ds read directly.
 int mma_tile_rows(int64_t M);
 // The grouped (mixture-of-experts) form of the warp-MMA path: expert g's W at
 // w + g * expert_stride (a multiple of 16), its rows [row_offsets[g],
@@ -1059,8 +1059,9 @@ void mma_launch_config(int64_t M, int64_t N, int64_t K, int num_sms, int* rows, 
 // rows 8/16/24/32, rows per CTA, K splits, CTAs per SM); 0 clears.  -1 on a
 // value out of range (nothing installed).
 int mma_set_launch_table(const int64_t* entries, int count);
-cudaError_t launch_matmul_mma(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds, int64_t M,
-                              float* y, int64_t ldy, void* encode, int* err, int num_sms, cudaStream_t stream);
+cudaError_t launch_matmul_mma(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs, const void* ds,
+                              int64_t M, float* y, int64_t ldy, void* encode, int* err, int num_sms,
+                              cudaStream_t stream);
 cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,
                              const void* ds, const void* tc_operand, int64_t M, float* y,
                              int64_t ldy, void* encode, int* err, int num_sms, int skip_w_stage,

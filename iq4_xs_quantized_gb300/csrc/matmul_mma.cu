@@ -1,662 +1,15 @@
-// matmul_mma.cu -- IQ4_XS x Q8_1 matmul for small and medium batches on the
-// warp-level tensor-core MMA (mma.sync m16n8k16, fp16 operands, fp32
-// accumulators held in registers).
-//
-// Method (V100TPS engine page, new-kernel table and the tile-geometry
-// passage after it): per 32-weight sub-block an integer dot product of the
-// decoded codebook values with the Q8_1 codes, scaled by d_w*(ls-32)*d_x into
-// fp32.  As on the tcgen05 path both operands are small integers held
-// exactly in fp16 (codebook values |kv| <= 127, codes |q| <= 127), so a
-// sub-block's two k16 MMAs leave its exact integer dot P in the fp32
-// accumulator (every product and partial sum is an integer below 2^24).
-//
-// Why a warp-level MMA in the memory-bound range.  For M <= 32 the weight
-// bytes bound the call; what limits a kernel is how many instructions and
-// shared-memory wavefronts it spends per weight.  Here the decoded weights go
-// from the byte-table lookup straight into the A fragment registers and every
-// sub-block's accumulator comes back in registers for its scale-in, so no
-// weight tile is stored anywhere, no accumulator is read back from tensor
-// memory and no hand-off between warp roles is needed per sub-block.
-//
-// Tiles.  A CTA owns R weight rows (R a multiple of 16 up to 256, chosen per
-// call so that the row tiles times the K split fill the SMs) and an
-// activation tile of 8*NT rows (MMA N = 8 per fragment, NT fragments).
-// Weights are the A operand (MMA M = 16 rows per fragment).  A stage is 512
-// weights of every row (two super-blocks, one R x 272 B TMA box) plus the
-// matching Q8_1 codes; the 8 consumer warps split it as kRG row groups x
-// kSG sub-block groups: warp (rg, sg) takes fragments rg, rg + kRG, ...
-// (at most kTMax) and kSPW consecutive sub-blocks of one super-block.  K is
-// split over a thread-block cluster of S CTAs whose partial tiles are summed
-// in rank order through distributed shared memory.
-//
-// K order inside a sub-block.  MMA k pair p of k16 step s (k = 2p, 2p+1)
-// holds qs byte b = 4*(p % 4) + 2*s + (p / 4), i.e. sub-block elements b
-// (low nibble) and 16 + b (high nibble).  Lane (g, t) of the warp (g = lane /
-// 4, t = lane % 4) then needs bytes 4t..4t+3 of its two weight rows g and
-// g+8 -- one 32-bit word each -- and Q8_1 codes 4t..4t+3 and 16+4t..16+4t+3
-// of activation row g, two words.  One shared-memory lookup per qs byte
-// returns the fp16x2 (kv[low nibble], kv[high nibble]) that is exactly one A
-// register.
-//
-// Roles: warps 0-7 consume stages; warp 8 lane 0 is the TMA producer (W
-// boxes before the wait for the preceding grid, Q8_1 code boxes after it).
-// Each consumer warp first turns the stage's block headers into its row
-// scales d_w*(ls-32) and the activation scales d_x into fp32, in tables of
-// its own kept in the unused half of every 256-byte row of the byte table.
-// Every mbarrier wait is bounded; a wait that runs out records its code in
-// the device error word, raises the CTA's abort flag, and the CTA drains its
-// copies and leaves y unwritten.
-#include <cuda.h>
-
+// matmul_mma.cu -- IQ4_XS launches of the warp-level MMA matmul (the kernel
+// and its launch model are in mma_kernel.cuh): the launch configurations
+// per activation-tile width, the measured launch table and the forced test
+// configuration, the grouped (mixture-of-experts) form, and the path's
+// entry points (other weight formats go on to matmul_mma_b18.cu).
 #include <atomic>
 #include <mutex>
 
-#include "internal.cuh"
+#include "mma_kernel.cuh"
 
 namespace iq4xs {
 namespace {
-
-constexpr int kMmaConsumers = 8;              // consumer warps
-constexpr int kMmaProducerWarp = kMmaConsumers;
-constexpr int kMmaThreads = 32 * (kMmaConsumers + 1);
-
-constexpr int kMmaMaxCluster = 8;
-constexpr int kMmaMaxRows = 256;              // TMA box height
-constexpr int kMmaMaxStages = 4;
-constexpr int kWideLutBytes = 256 * 256;      // byte table: entry j at 256 j, copy l at 4 l (bytes 0..127)
-constexpr int kGapBytes = kWideLutBytes / 2;  // bytes 128..255 of every table row
-constexpr int kQBoxK = 128;                   // Q8_1 codes per box row (one 128-byte swizzle row)
-constexpr int kQBoxesPerStage = kPairK / kQBoxK;  // 4
-constexpr int kMmaSmemLimit = 227 * 1024;
-constexpr int kOffRingMma = kWideLutBytes;
-constexpr int kMmaBarBytes = 128;             // full[4], empty[4], abort flag
-constexpr int kMmaSmemLimit2 = 113 * 1024;   // per CTA with two CTAs per SM
-__device__ volatile int g_never_abort_mma = 0;  // an abort flag that is never set
-
-// Physical address (bytes from the table start) of byte o of the gap space.
-__host__ __device__ constexpr uint32_t gap_addr(uint32_t o) { return ((o >> 7) << 8) + 128u + (o & 127u); }
-
-// NT: 8-row activation fragments per tile; T: 16-row weight fragments per
-// consumer warp.  The 8 consumer warps are 2 row groups x 4 sub-block
-// groups, so a CTA owns R = 32 T weight rows and a warp takes fragments
-// rg, rg + 2, ..., rg + 2 (T - 1) and 4 consecutive sub-blocks of a stage.
-template <int NT, int T, int kOcc = 1>
-struct MmaCfg {
-    static_assert(NT >= 1 && NT <= 4, "1..4 fragments of 8 activation rows");
-    static_assert(T >= 1 && T * NT <= 16, "accumulators: T x NT x 4 registers per lane");
-    static constexpr int kMt = 8 * NT;                    // activation rows per tile
-    static constexpr int kRG = 2;                         // row groups
-    static constexpr int kSG = kMmaConsumers / kRG;       // sub-block groups
-    static constexpr int kSPW = kSubPerPair / kSG;        // sub-blocks per warp and stage (4)
-    static constexpr int kR = 16 * kRG * T;               // weight rows per CTA
-    static_assert(kR <= kMmaMaxRows, "TMA box height");
-    static_assert(kSubPerBlock % kSPW == 0, "a warp's sub-blocks lie in one super-block");
-    static constexpr int kQBox = kMt * kQBoxK;            // one code box (a multiple of 1024 B)
-    static constexpr int kQStage = kQBoxesPerStage * kQBox;
-    static constexpr int kWBytes = (kR * kPairBytes + 1023) / 1024 * 1024;
-    static constexpr int kStage = kWBytes + kQStage;
-    // kOcc CTAs per SM: the whole shared memory (227 KB) for one, or half
-    // of it (113 KB) for two -- then a launch's CTAs can start beside the
-    // preceding launch's last ones.
-    static_assert(kOcc == 1 || kOcc == 2, "one or two CTAs per SM");
-    static constexpr int kRing = (kOcc == 1 ? kMmaSmemLimit : kMmaSmemLimit2) - kOffRingMma - kMmaBarBytes;
-    static constexpr int kNS = kRing / kStage < kMmaMaxStages ? kRing / kStage : kMmaMaxStages;
-    static_assert(kNS >= 2, "two stages in flight");
-    static constexpr int kSmem = kOffRingMma + kNS * kStage + kMmaBarBytes;
-    // Per-warp tables (gap space): row scales [k][s][g][h] (rows
-    // 16 f + g + 8 h of fragment f = rg + 2 k), then d_x [s][m].
-    static constexpr int kSwFloats = kSPW * T * 16;
-    static constexpr int kDxFloats = kSPW * kMt;
-    static constexpr int kWarpTab = ((kSwFloats + kDxFloats) * 4 + 127) / 128 * 128;
-    static_assert(kMmaConsumers * kWarpTab <= kGapBytes, "tables fit the byte table's gaps");
-    static constexpr int kXItems = (kDxFloats + 31) / 32;  // d_x loads per lane and stage
-    static constexpr int kCombos = T * 8;                  // (fragment, g) pairs of a warp
-    static constexpr int kRedStride = kMt + 4;             // fp32 per row of a partial tile
-    static_assert(kSG * kR * kRedStride * 4 <= kNS * kStage, "partials fit the ring");
-    static_assert(kSmem <= (kOcc == 1 ? kMmaSmemLimit : kMmaSmemLimit2), "shared memory per CTA");
-    static_assert(kR * kRedStride * 4 <= kWideLutBytes, "CTA tile fits the byte table");
-};
-
-__device__ __forceinline__ void mma_f16_16816(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1,
-                                              const float c[4]) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%10, %11, %12, %13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
-          "f"(c[3]));
-}
-__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t local_addr, uint32_t rank) {
-    uint32_t a;
-    float4 v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local_addr), "r"(rank));
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(a)
-                 : "memory");
-    return v;
-}
-__device__ __forceinline__ void consumers_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kMmaConsumers) : "memory");
-}
-// Consumers and producer between two activation tiles of one CTA.
-__device__ __forceinline__ void tile_sync() { asm volatile("bar.sync 2, %0;" ::"n"(kMmaThreads) : "memory"); }
-// kGrouped: mixture-of-experts form.  Expert slot z (grid z) takes the z-th
-// expert that has rows (row_offsets, a device array read after the wait for
-// the preceding grid); W is that expert's matrix (a 3D tensor map over the
-// experts) and its rows [r0, r1) of the activations are covered in tiles of
-// kMt, one pass over K per tile; no K split.  Otherwise grid z is the
-// activation tile of rows [z kMt, (z + 1) kMt).
-template <int NT, int T, int kOcc, bool kGrouped>
-__global__ void __launch_bounds__(kMmaThreads, kOcc)
-    matmul_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_q,
-                      const __half* __restrict__ ds, int64_t M, int N, int K, float* __restrict__ y, int64_t ldy,
-                      int* err, const int32_t* __restrict__ row_offsets, int G) {
-    using C = MmaCfg<NT, T, kOcc>;
-    constexpr int kTMax = T, kMt = C::kMt, kSPW = C::kSPW, kRG = C::kRG, R = C::kR, NS = C::kNS;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    if (smem_u32(smem) & 1023u) {  // the 128-byte-swizzled code boxes need 1024-byte alignment
-        if (threadIdx.x == 0) atomicExch(err, kDevErrLayout);
-        return;
-    }
-    constexpr int stage_b = C::kStage, wbytes = C::kWBytes;
-    const Bc bc = bc_open(err);
-    if (!bc_range(bc, 0, C::kSmem, dyn_smem_bytes(), kBcMmaSmem)) return;  // every CTA alike
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffRingMma + NS * stage_b);
-    uint64_t* empty = full + kMmaMaxStages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kMmaMaxStages);
-    int* grp = reinterpret_cast<int*>(empty + kMmaMaxStages) + 2;  // grouped: expert, first row, end row
-    const uint32_t sbase = smem_u32(smem);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int S = gridDim.y;
-    const uint32_t rank = (S > 1) ? cluster_ctarank() : 0;
-    const int n0 = blockIdx.x * R;
-    const int z = blockIdx.z;
-    const int pairs = (K + kPairK - 1) / kPairK;
-    const int p0 = (int)((int64_t)pairs * rank / S);
-    const int p1 = (int)((int64_t)pairs * (rank + 1) / S);
-    const int nst = p1 - p0;
-
-    // Activation rows this CTA covers: [row_lo, row_hi) in mtiles tiles.
-    int gexp = 0;
-    int64_t row_lo = (int64_t)z * kMt, row_hi = (row_lo + kMt < M) ? row_lo + kMt : M;
-    if constexpr (kGrouped) {
-        if (warp == 0) {
-            griddep_wait();  // the offsets may come from the preceding grid
-            // The z-th expert with rows: offsets of 128 experts per step
-            // (independent loads), one ballot per 32.
-            int ge = -1;
-            uint32_t k = (uint32_t)z;
-            for (int base = 0; base < G && ge < 0; base += 4 * 32) {
-                int32_t lo[4], hi[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int e = base + 32 * j + lane;
-                    const bool in =
-                        e < G && bc_global(bc, row_offsets + e, 8, row_offsets, (int64_t)(G + 1) * 4, kBcMmaOffsets);
-                    lo[j] = in ? __ldg(row_offsets + e) : 0;
-                    hi[j] = in ? __ldg(row_offsets + e + 1) : 0;
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t mask = __ballot_sync(0xffffffffu, hi[j] > lo[j]);
-                    const uint32_t cnt = __popc(mask);
-                    if (ge < 0) {
-                        if (k < cnt) ge = base + 32 * j + (int)__fns(mask, 0, (int)k + 1);
-                        else k -= cnt;
-                    }
-                }
-            }
-            if (lane == 0) {
-                grp[0] = ge;
-                grp[1] = ge >= 0 ? row_offsets[ge] : 0;
-                grp[2] = ge >= 0 ? row_offsets[ge + 1] : 0;
-                // offsets outside the rows of y: the expert is skipped
-                if (ge >= 0 && !bc_range(bc, grp[1], (int64_t)grp[2] - grp[1], M, kBcMmaRows)) grp[0] = -1;
-            }
-        }
-        __syncthreads();
-        gexp = grp[0];
-        if (gexp < 0) return;  // fewer experts with rows than slots (whole CTA; no cluster)
-        row_lo = grp[1];
-        row_hi = grp[2];
-    }
-    // one activation tile per CTA unless it covers an expert's rows
-    const int mtiles = kGrouped ? (int)((row_hi - row_lo + kMt - 1) / kMt) : 1;
-    const int total = mtiles * nst;  // stages over all activation tiles
-
-    // Stage gs = activation tile gs / nst, K pair p0 + gs % nst.
-    auto tile_of = [&](int gs) { return kGrouped ? gs / nst : 0; };
-    auto pair_of = [&](int gs) { return p0 + (kGrouped ? gs % nst : gs); };
-    auto load_w = [&](int gs) {
-        const int slot = gs % NS;
-        const int x = pair_of(gs) * (kPairBytes / 4);
-        if (!bc_tma(bc, x, 4, kPairBytes / 4, (int64_t)(K / kQK) * (kBlockBytes / 4), n0, N, kBcMmaWAlign,
-                    kBcMmaW))
-            return;
-        if constexpr (kGrouped) bc_range(bc, gexp, 1, G, kBcMmaW);
-        mbar_arrive_expect_tx(&full[slot], (uint32_t)(R * kPairBytes + C::kQStage));
-        if constexpr (kGrouped)
-            tma_load_3d(smem + kOffRingMma + slot * stage_b, &tmap_w, x, n0, gexp, &full[slot]);
-        else
-            tma_load_2d(smem + kOffRingMma + slot * stage_b, &tmap_w, x, n0, &full[slot]);
-    };
-    auto load_q = [&](int gs) {
-        const int slot = gs % NS;
-        const int rq = (int)(row_lo + (int64_t)tile_of(gs) * kMt);
-#pragma unroll
-        for (int b = 0; b < kQBoxesPerStage; ++b) {
-            const int x = pair_of(gs) * kPairK + b * kQBoxK;
-            if (bc_tma(bc, x, 1, kQBoxK, K, rq, M, kBcMmaQAlign, kBcMmaQ))
-                tma_load_2d(smem + kOffRingMma + slot * stage_b + wbytes + b * C::kQBox, &tmap_q, x, rq, &full[slot]);
-        }
-    };
-    const int pre = nst < NS ? nst : NS;  // stages of the first activation tile issued at set-up
-    if (warp == kMmaProducerWarp && lane == 0) {
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kMmaConsumers);
-        }
-        *abort_flag = 0;
-        fence_barrier_init();
-        fence_proxy_async_smem();
-        // The first W stages (model state) go out at once, before the byte
-        // table is built and before the preceding grid (which writes the
-        // codes) has finished.
-        prefetch_tmap(&tmap_w);
-        prefetch_tmap(&tmap_q);
-        for (int ps = 0; ps < pre; ++ps) load_w(ps);
-    }
-    // Byte table: row j = 32 copies (one per bank) of the fp16x2 word
-    // (kv[j & 15], kv[j >> 4]) in its first 128 bytes.
-    for (int i = threadIdx.x; i < 256 * 8; i += kMmaThreads) {
-        const uint32_t e = f16x2_byte_entry<kWtIQ4XS>(i >> 3);
-        *reinterpret_cast<uint4*>(smem + (i >> 3) * 256 + (i & 7) * 16) = make_uint4(e, e, e, e);
-    }
-    __syncthreads();
-    griddep_launch_dependents();
-
-    bool ok = true;
-    if (warp == kMmaProducerWarp) {
-        int issued = 0;
-        for (int mt = 0; mt < mtiles; ++mt) {
-            // The next tile's stages wait until the consumers have summed
-            // the current tile's partials, which they keep in the ring.
-            if (mt > 0) tile_sync();
-            if (lane == 0) {
-                const int gs0 = mt * nst;
-                int first = 0;
-                if (mt == 0) {
-                    griddep_wait();  // the codes come from the preceding grid
-                    for (int ps = 0; ps < pre; ++ps) load_q(ps);
-                    first = pre;
-                    issued = pre;
-                }
-                for (int ps = first; ps < nst && ok; ++ps) {
-                    const int gs = gs0 + ps, slot = gs % NS;
-                    if (gs >= NS) {
-                        ok = mbar_wait(&empty[slot], ((gs / NS) - 1) & 1, abort_flag, err, kDevErrTimeoutMmaSlot);
-                        if (!ok) break;
-                    }
-                    load_w(gs);
-                    load_q(gs);
-                    ++issued;
-                }
-            }
-            __syncwarp();
-        }
-        if (lane == 0) {
-            // Drain: the last stage issued into each slot has landed (the
-            // earlier ones were consumed before their slot was reused).  Not
-            // stopped by an abort: no copy may land after the CTA exits.
-            for (int gs = (issued > NS ? issued - NS : 0); gs < issued; ++gs)
-                mbar_wait(&full[gs % NS], (gs / NS) & 1, &g_never_abort_mma, err, kDevErrTimeoutDrain);
-        }
-        __syncwarp();
-    } else {
-        // ---------------------------------------------------------- consumers
-        const int g = lane >> 2, t = lane & 3;
-        const int rg = warp / C::kSG, sg = warp % C::kSG;
-        const int sub_w = sg * kSPW;             // first sub-block of the stage this warp takes
-        const int super_w = sub_w / kSubPerBlock;
-        const int jj0 = sub_w % kSubPerBlock;
-        const uint32_t lane4 = (uint32_t)lane * 4u;
-        const uint32_t tab = (uint32_t)(warp * C::kWarpTab);   // this warp's tables, gap space
-        const uint32_t* ds32 = reinterpret_cast<const uint32_t*>(ds);
-        const int64_t K32 = (K + kSub - 1) / kSub;
-        float acc[kTMax][NT][4];
-        // Activation scales of stage gs for this warp's sub-blocks: item e =
-        // (row m = e / kSPW of the stage's tile, sub-block e % kSPW), fp16 d
-        // in ds; rows outside the CTA's range read as 0.
-        uint32_t dxv[C::kXItems];
-        auto load_dx = [&](int gs) {
-            const int64_t rb = row_lo + (int64_t)tile_of(gs) * kMt;
-#pragma unroll
-            for (int k = 0; k < C::kXItems; ++k) {
-                const int e = lane + 32 * k;
-                const int64_t m = rb + e / kSPW;
-                const int64_t sub = (int64_t)pair_of(gs) * kSubPerPair + sub_w + e % kSPW;
-                dxv[k] = (e < C::kDxFloats && m < row_hi && sub < K32 &&
-                          bc_global(bc, ds32 + m * K32 + sub, 4, ds, M * K32 * 4, kBcMmaDs))
-                             ? __ldg(ds32 + m * K32 + sub)
-                             : 0u;
-            }
-        };
-        griddep_wait();  // ds comes from the preceding grid
-        if (total > 0) load_dx(0);
-        // Row-scale work of this lane: (fragment slot k, g) pairs c = lane +
-        // 32 i, rows 16 f + g and 16 f + g + 8, all kSPW sub-blocks.
-        const int wrow_lane = 16 * rg + g;       // row of fragment slot 0 for this lane (+ 16 kRG k)
-
-        for (int mt = 0; mt < mtiles; ++mt) {
-        const int64_t row_base = row_lo + (int64_t)mt * kMt;
-#pragma unroll
-        for (int i = 0; i < kTMax; ++i)
-#pragma unroll
-            for (int f = 0; f < NT; ++f)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[i][f][e] = 0.f;
-        for (int ps = 0; ps < nst && ok; ++ps) {
-            const int gs = mt * nst + ps, slot = gs % NS;
-            ok = mbar_wait(&full[slot], (gs / NS) & 1, abort_flag, err, kDevErrTimeoutMmaStage);
-            if (!ok) break;
-            // Plain loads from here on: ordered after the barrier wait (an
-            // asm statement with a memory clobber) and free to be scheduled
-            // among themselves.
-            const uint8_t* wst = smem + kOffRingMma + slot * stage_b;
-            const uint8_t* qst = wst + wbytes;
-            // ---- per-stage tables: row scales and activation scales
-            // Row scales of this warp's kSPW = 4 consecutive sub-blocks
-            // jj0..jj0+3 of one super-block: from the header's 16 bits of
-            // low nibbles and 8 bits of high pairs shifted once, each
-            // ls - 32 comes out exact through the float 2^23 + ls.
-            static_assert(kSPW == 4, "four sub-blocks per header read");
-#pragma unroll
-            for (int c = lane; c < C::kCombos; c += 32) {
-                const int k = c >> 3, gg = c & 7;
-                const int r = 16 * (rg + kRG * k) + gg;
-                float sw[2][4];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint2 hd =
-                        *reinterpret_cast<const uint2*>(wst + (r + 8 * h) * kPairBytes + super_w * kBlockBytes);
-                    const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
-                    const uint32_t lo16 = hd.y >> (4 * jj0);          // ls low nibbles of jj0..jj0+3
-                    const uint32_t hi8 = hd.x >> (16 + 2 * jj0);      // ls high bit pairs
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const uint32_t ls = ((lo16 >> (4 * u)) & 0xFu) | (((hi8 >> (2 * u)) & 3u) << 4);
-                        const float l = __uint_as_float(0x4B000000u | ls) - 8388640.0f;  // ls - 32, exact
-                        sw[h][u] = d * l;
-                    }
-                }
-                // block (k, s2) of 64 bytes at gap offset 64 (4 k + s2): two
-                // 128-byte chunks per k, entries (rows r, r + 8) at +8 gg
-                uint8_t* tk = smem + gap_addr(tab + (uint32_t)(256 * k)) + 8 * gg;
-#pragma unroll
-                for (int s2 = 0; s2 < 4; ++s2)
-                    *reinterpret_cast<float2*>(tk + 256 * (s2 >> 1) + 64 * (s2 & 1)) = make_float2(sw[0][s2], sw[1][s2]);
-            }
-#pragma unroll
-            for (int k = 0; k < C::kXItems; ++k) {
-                const int e = lane + 32 * k;
-                if (e < C::kDxFloats)
-                    *reinterpret_cast<float*>(smem + gap_addr(tab + (uint32_t)((C::kSwFloats + (e % kSPW) * kMt + e / kSPW) * 4))) =
-                        __half2float(__ushort_as_half((unsigned short)(dxv[k] & 0xFFFFu)));
-            }
-            __syncwarp();
-            if (gs + 1 < total) load_dx(gs + 1);  // in flight during this stage
-            // The four sub-blocks unrolled (loads of the next sub-block's words
-            // overlap this one's lookups and MMAs: 5-6 % faster at 8 rows,
-            // 6-14 % at 16) where the registers allow it: one activation
-            // fragment, or two with at most four weight fragments per warp
-            // (not in the grouped form, which spills there); one at a time
-            // otherwise.
-            constexpr int kUnrollS = (NT == 1 || (NT == 2 && T <= 4 && !kGrouped)) ? kSPW : 1;
-#pragma unroll kUnrollS
-            for (int s = 0; s < kSPW; ++s) {
-                const int j = sub_w + s;                 // sub-block within the stage
-                const int jj = j % kSubPerBlock;
-                const int box = j / 4, jq = j % 4;
-                // B fragments: activation row 8 f + g, Q8_1 codes 4t..4t+3 and
-                // 16+4t..16+4t+3 of the sub-block (128-byte swizzle: 16-byte
-                // chunk c of box row r sits at chunk c ^ (r % 8)).
-                uint32_t bfr[NT][4];
-                float2 dx[NT];
-#pragma unroll
-                for (int f = 0; f < NT; ++f) {
-                    const uint8_t* rowa = qst + box * C::kQBox + (8 * f + g) * kQBoxK + 4 * t;
-                    const uint32_t lo4 = *reinterpret_cast<const uint32_t*>(rowa + (((2 * jq) ^ g) << 4));
-                    const uint32_t hi4 = *reinterpret_cast<const uint32_t*>(rowa + (((2 * jq + 1) ^ g) << 4));
-                    const uint4 v = q8x8_to_f16(lo4, hi4);
-                    bfr[f][0] = v.x; bfr[f][1] = v.y; bfr[f][2] = v.z; bfr[f][3] = v.w;
-                    dx[f] = *reinterpret_cast<const float2*>(
-                        smem + gap_addr(tab + (uint32_t)((C::kSwFloats + s * kMt + 8 * f + 2 * t) * 4)));
-                }
-                // row scales of sub-block s: block (k, s) of 64 bytes at gap
-                // offset 64 (k kSPW + s), the lane's pair (rows g, g+8) at +8 g;
-                // kSPW = 4 blocks are two whole 128-byte gap chunks, so block
-                // (k, s) sits 512 k physical bytes after block (0, s).
-                static_assert(kSPW == 4, "two gap chunks per fragment slot");
-                const uint8_t* swp = smem + gap_addr(tab + (uint32_t)(64 * s)) + 8 * g;
-                const uint8_t* wl = wst + wrow_lane * kPairBytes + super_w * kBlockBytes + 8 + 16 * jj + 4 * t;
-#pragma unroll
-                for (int k = 0; k < kTMax; ++k) {
-                    {
-                        const uint8_t* wk = wl + 16 * kRG * k * kPairBytes;
-                        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(wk);
-                        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(wk + 8 * kPairBytes);
-                        // A fragments of k16 steps 0 and 1: bytes (0, 1) and
-                        // (2, 3) of the two rows' words; table byte offset =
-                        // (byte << 8) | 4 lane.
-                        uint32_t a0[4], a1[4];
-                        a0[0] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w0, lane4, 0x5504u));
-                        a0[1] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w1, lane4, 0x5504u));
-                        a0[2] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w0, lane4, 0x5514u));
-                        a0[3] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w1, lane4, 0x5514u));
-                        a1[0] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w0, lane4, 0x5524u));
-                        a1[1] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w1, lane4, 0x5524u));
-                        a1[2] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w0, lane4, 0x5534u));
-                        a1[3] = *reinterpret_cast<const uint32_t*>(smem + __byte_perm(w1, lane4, 0x5534u));
-                        const float2 sw = *reinterpret_cast<const float2*>(swp + 512 * k);
-                        const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int f = 0; f < NT; ++f) {
-                            float p[4];
-                            mma_f16_16816(p, a0, bfr[f][0], bfr[f][1], zero);
-                            mma_f16_16816(p, a1, bfr[f][2], bfr[f][3], p);
-                            // acc += (P * d_x) * d_w*(ls-32): rows g (p0, p1) and g+8 (p2, p3)
-                            const float2 q01 = __fmul2_rn(make_float2(p[0], p[1]), dx[f]);
-                            const float2 q23 = __fmul2_rn(make_float2(p[2], p[3]), dx[f]);
-                            const float2 r01 =
-                                __ffma2_rn(q01, make_float2(sw.x, sw.x), make_float2(acc[k][f][0], acc[k][f][1]));
-                            const float2 r23 =
-                                __ffma2_rn(q23, make_float2(sw.y, sw.y), make_float2(acc[k][f][2], acc[k][f][3]));
-                            acc[k][f][0] = r01.x; acc[k][f][1] = r01.y;
-                            acc[k][f][2] = r23.x; acc[k][f][3] = r23.y;
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-        }
-        if (!ok) {
-            // Wake the producer if it waits on a slot this warp will never free.
-            if (lane == 0) *abort_flag = 1;
-        }
-        // ---- end of the K range of this tile: partial tiles of the sub-block groups
-        consumers_sync();  // every consumer is done with the ring
-        if (!*abort_flag) {
-            float* red = reinterpret_cast<float*>(smem + kOffRingMma) + sg * R * C::kRedStride;
-#pragma unroll
-            for (int k = 0; k < kTMax; ++k) {
-                {
-#pragma unroll
-                    for (int f = 0; f < NT; ++f) {
-                        const int r = 16 * (rg + kRG * k) + g, c = 8 * f + 2 * t;
-                        *reinterpret_cast<float2*>(red + r * C::kRedStride + c) =
-                            make_float2(acc[k][f][0], acc[k][f][1]);
-                        *reinterpret_cast<float2*>(red + (r + 8) * C::kRedStride + c) =
-                            make_float2(acc[k][f][2], acc[k][f][3]);
-                    }
-                }
-            }
-        }
-        consumers_sync();
-        if (!*abort_flag) {
-            const float* red = reinterpret_cast<const float*>(smem + kOffRingMma);
-            float* tile = reinterpret_cast<float*>(smem);
-            const int64_t mrows = row_hi - row_base;
-            for (int e = threadIdx.x; e < R * kMt; e += 32 * kMmaConsumers) {
-                const int r = e % R, m = e / R;
-                float v = red[r * C::kRedStride + m];
-#pragma unroll
-                for (int q = 1; q < C::kSG; ++q) v += red[(q * R + r) * C::kRedStride + m];
-                if (S == 1) {
-                    if (m < mrows && n0 + r < N &&
-                        bc_global(bc, y + (row_base + m) * ldy + n0 + r, 4, y, ((M - 1) * ldy + N) * 4, kBcMmaY))
-                        y[(row_base + m) * ldy + n0 + r] = v;
-                } else {
-                    tile[r * C::kRedStride + m] = v;
-                }
-            }
-        }
-        if (mt + 1 < mtiles) tile_sync();  // the ring may take the next tile's stages
-        }  // activation tiles
-    }
-
-    if (S > 1) {
-        // Split-K: rank r sums rows [R r / S, R (r + 1) / S) of every rank's
-        // tile in rank order (deterministic).  Every thread of every CTA
-        // passes both cluster barriers, aborted or not; after an abort the
-        // output is undefined and the tiles are not summed.
-        __syncwarp();
-        cluster_arrive_release();
-        cluster_wait();
-        if (warp < kMmaConsumers && !*abort_flag) {
-            // Four activation rows of one weight row per item: the S ranks'
-            // 16-byte slices are all requested before any is summed.
-            const int r0 = R * (int)rank / S, r1 = R * ((int)rank + 1) / S;
-            const int64_t mrows = row_hi - row_lo;  // one tile (K splits only without experts)
-            for (int e = threadIdx.x; e < (r1 - r0) * (kMt / 4); e += 32 * kMmaConsumers) {
-                const int r = r0 + e % (r1 - r0), m = 4 * (e / (r1 - r0));
-                const uint32_t off = sbase + (uint32_t)((r * C::kRedStride + m) * 4);
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (bc_range(bc, (r * C::kRedStride + m) * 4, 16, R * C::kRedStride * 4, kBcMmaSplit)) {
-                    float4 part[kMmaMaxCluster];
-#pragma unroll
-                    for (int q = 0; q < kMmaMaxCluster; ++q)
-                        if (q < S) part[q] = ld_cluster_f32x4(off, (uint32_t)q);
-#pragma unroll
-                    for (int q = 0; q < kMmaMaxCluster; ++q)
-                        if (q < S) {
-                            v.x += part[q].x;
-                            v.y += part[q].y;
-                            v.z += part[q].z;
-                            v.w += part[q].w;
-                        }
-                }
-                const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (m + i < mrows && n0 + r < N &&
-                        bc_global(bc, y + (row_lo + m + i) * ldy + n0 + r, 4, y, ((M - 1) * ldy + N) * 4, kBcMmaY))
-                        y[(row_lo + m + i) * ldy + n0 + r] = vv[i];
-            }
-        }
-        __syncwarp();
-        cluster_arrive_release();
-        cluster_wait();  // no rank exits while another reads its tile
-    }
-}
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// The kernel's dynamic shared-memory limit, raised once per device.
-template <int NT, int T, int kOcc, bool kGrouped>
-cudaError_t mma_smem_attr(int dev) {
-    static bool done[64] = {};
-    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(matmul_mma_kernel<NT, T, kOcc, kGrouped>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               MmaCfg<NT, T, kOcc>::kSmem);
-    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
-    return e;
-}
-
-// Cached per device: clusters of S (1..8) the device runs at once for the
-// kernel <NT, T, kOcc> (cudaOccupancyMaxActiveClusters, queried once).
-template <int NT, int T, int kOcc>
-int mma_max_clusters(int dev, int s, int num_sms) {
-    using C = MmaCfg<NT, T, kOcc>;
-    static int cache[64][kMmaMaxCluster + 1] = {};
-    int mc = (dev >= 0 && dev < 64) ? cache[dev][s] : 0;
-    if (mc > 0) return mc;
-    if (mma_smem_attr<NT, T, kOcc, false>(dev) != cudaSuccess) cudaGetLastError();
-    cudaLaunchConfig_t q = {};
-    q.gridDim = dim3(1, (unsigned)s, 1);
-    q.blockDim = dim3(kMmaThreads);
-    q.dynamicSmemBytes = C::kSmem;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 1;
-    at[0].val.clusterDim.y = (unsigned)s;
-    at[0].val.clusterDim.z = 1;
-    q.attrs = at;
-    q.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, matmul_mma_kernel<NT, T, kOcc, false>, &q) != cudaSuccess || n < 1) {
-        cudaGetLastError();
-        n = kOcc * num_sms / s;
-    }
-    mc = n > 0 ? n : 1;
-    if (dev >= 0 && dev < 64) cache[dev][s] = mc;
-    return mc;
-}
-
-template <int NT, int T, int kOcc>
-cudaError_t launch_nt(const void* w, int64_t row_bytes, EncodeTiledFn enc, const CUtensorMap& tq, const __half* ds,
-                      int64_t M, int N, int K, int S, float* y, int64_t ldy, int* err, cudaStream_t stream) {
-    using C = MmaCfg<NT, T, kOcc>;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const cudaError_t ea = mma_smem_attr<NT, T, kOcc, false>(dev);
-    if (ea != cudaSuccess) return ea;
-    // W: one box = R rows x one super-block pair (272 B; K % 512 == 0, so
-    // rows are 16-byte strided); rows past N read as zeros (d = 0).
-    CUtensorMap tw;
-    {
-        const cuuint64_t gdim[2] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)N};
-        const cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
-        const cuuint32_t box[2] = {(cuuint32_t)(kPairBytes / 4), (cuuint32_t)C::kR};
-        const cuuint32_t estride[2] = {1, 1};
-        if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(w), gdim, gstride, box, estride,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    const int ntiles = (N + C::kR - 1) / C::kR;
-    const int mtiles = (int)((M + C::kMt - 1) / C::kMt);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)ntiles, (unsigned)S, (unsigned)mtiles);
-    cfg.blockDim = dim3(kMmaThreads);
-    cfg.dynamicSmemBytes = C::kSmem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = (unsigned)S;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, matmul_mma_kernel<NT, T, kOcc, false>, tw, tq, ds, M, N, K, y, ldy, err,
-                              static_cast<const int32_t*>(nullptr), 0);
-}
 
 // Grouped (mixture-of-experts) launch of the <NT, T> kernel: W of expert g
 // through a 3D tensor map (row words x rows x experts, expert_stride bytes
@@ -693,7 +46,7 @@ cudaError_t launch_grouped_nt(const void* w, int64_t expert_stride, int G, int64
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, matmul_mma_kernel<NT, T, 1, true>, tw, tq, ds, rows, N, K, y, ldy, err,
-                              row_offsets, G);
+                              row_offsets, G, 0);
 }
 
 // Test override of the launch configuration (0 = the model's choice).
@@ -721,18 +74,6 @@ bool measured_launch(int64_t N, int64_t K, int mt, LaunchEntry* out) {
     return false;
 }
 
-// One launch configuration: R weight rows per CTA and CTAs per SM, with its
-// cluster-occupancy query and its launcher.
-struct MmaConfig {
-    int R, occ;
-    int (*max_clusters)(int dev, int s, int num_sms);
-    cudaError_t (*launch)(const void*, int64_t, EncodeTiledFn, const CUtensorMap&, const __half*, int64_t, int,
-                          int, int, float*, int64_t, int*, cudaStream_t);
-};
-template <int NT, int T, int kOcc>
-constexpr MmaConfig cfg_of() {
-    return {MmaCfg<NT, T, kOcc>::kR, kOcc, &mma_max_clusters<NT, T, kOcc>, &launch_nt<NT, T, kOcc>};
-}
 // Per activation-tile width: T = 1..8 (4 from 24 activation rows on, the
 // accumulators' registers) at one CTA per SM, and the tiles that leave room
 // for two CTAs per SM (113 KB each, two stages: up to 64 rows at 8
@@ -762,101 +103,32 @@ struct MmaConfigs<4> {
                                          cfg_of<4, 1, 1>()};
 };
 
-// Launch cost model, per activation-tile width: a wave of CTAs costs F, plus
-// a per 128-row stage of one CTA (times the CTAs sharing an SM) and d per
-// stage whatever its rows; every CTA beyond the first in a cluster adds c
-// (the split-K reduction and the cluster's scheduling).  In microseconds,
-// fitted by least squares to about 1,700 timed launches of every
-// configuration on ten weight shapes (4096 x 4096 and the nine projections
-// of a ~27B decoder layer) at 8, 16, 24 and 32 activation rows.
-struct LaunchCost {
-    double F, a, d, c;
-};
-constexpr LaunchCost kLaunchCost[4] = {
-    {3.66, 1.21, 0.29, 0.71}, {4.20, 1.89, 0.11, 1.35}, {4.64, 3.14, 0.10, 1.06}, {4.64, 3.14, 0.10, 1.06}};
-
-// The configuration (R, CTAs per SM) and K split S (= cluster size) for a
-// call: the forced one (tests), else the measured one for this shape and
-// tile height if the calibration installed it, else the least modelled time
-// waves x (F + a x occ x R / 128 x st + d x st) + c x (S - 1), st =
-// ceil(pairs / S) stages per CTA, over every configuration of the
-// activation-tile width and S = 1..8 (at most the K pairs), with waves from
-// the clusters of S the device runs at once for that configuration.  Ties
-// keep the earlier configuration (larger R, one CTA per SM) and the
-// smaller S.
-template <int NT>
-void choose_config(int64_t M, int N, int K, int num_sms, int* best_c, int* best_s) {
-    constexpr LaunchCost kC = kLaunchCost[NT - 1];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const int mtiles = (int)((M + 8 * NT - 1) / (8 * NT));
-    const int pairs = (K + kPairK - 1) / kPairK;
-    const auto& list = MmaConfigs<NT>::list;
-    constexpr int kCount = (int)(sizeof(list) / sizeof(list[0]));
-    *best_c = 0;
-    *best_s = 1;
-    double best = 1e30;
-    for (int ci = 0; ci < kCount; ++ci) {
-        const MmaConfig& c = list[ci];
-        const int units = (N + c.R - 1) / c.R * mtiles;
-        for (int s = 1; s <= kMmaMaxCluster && s <= pairs; ++s) {
-            const int mc = c.max_clusters(dev, s, num_sms);
-            const int waves = (units + mc - 1) / mc;
-            const double st = (double)((pairs + s - 1) / s);
-            const double tm = waves * (kC.F + kC.a * c.occ * (double)c.R / 128.0 * st + kC.d * st) + kC.c * (s - 1);
-            if (tm < best * 0.999) {
-                best = tm;
-                *best_c = ci;
-                *best_s = s;
-            }
-        }
-    }
-    const int fr = g_force_rows.load(), fs = g_force_s.load(), fo = g_force_occ.load();
-    LaunchEntry e;
-    if (fr <= 0 && fs <= 0 && fo <= 0 && measured_launch(N, K, 8 * NT, &e)) {
-        for (int ci = 0; ci < kCount; ++ci)
-            if (list[ci].R == e.R && list[ci].occ == e.occ && e.S >= 1 && e.S <= kMmaMaxCluster && e.S <= pairs) {
-                *best_c = ci;
-                *best_s = e.S;
-                return;
-            }
-    }
-    if (fr > 0 || fo > 0) {
-        // the forced configuration, or the nearest one the list holds: the
-        // largest R up to the one wanted with the wanted CTAs per SM, else
-        // with any
-        const int want_r = fr > 0 ? fr : list[*best_c].R, want_o = fo > 0 ? fo : list[*best_c].occ;
-        int pick = -1;
-        for (int pass = 0; pass < 2 && pick < 0; ++pass)
-            for (int ci = 0; ci < kCount; ++ci) {
-                const MmaConfig& c = list[ci];
-                if (c.R > want_r || (pass < 1 && c.occ != want_o)) continue;
-                if (pick < 0 || c.R > list[pick].R) pick = ci;
-            }
-        *best_c = pick < 0 ? kCount - 1 : pick;
-    }
-    if (fs > 0) *best_s = fs < pairs ? fs : pairs;
-}
-
-template <int NT>
-cudaError_t launch_best(const void* w, int64_t row_bytes, EncodeTiledFn enc, const CUtensorMap& tq,
-                        const __half* ds, int64_t M, int N, int K, float* y, int64_t ldy, int* err, int num_sms,
-                        cudaStream_t stream) {
-    int ci = 0, s = 1;
-    choose_config<NT>(M, N, K, num_sms, &ci, &s);
-    return MmaConfigs<NT>::list[ci].launch(w, row_bytes, enc, tq, ds, M, N, K, s, y, ldy, err, stream);
-}
-
 template <int NT>
 void report_config(int64_t M, int N, int K, int num_sms, int* rows, int* splits, int* ctas_per_sm) {
+    const auto& list = MmaConfigs<NT>::list;
     int ci = 0, s = 1;
-    choose_config<NT>(M, N, K, num_sms, &ci, &s);
-    *rows = MmaConfigs<NT>::list[ci].R;
+    choose_config<NT, false>(list, (int)(sizeof(list) / sizeof(list[0])), M, N, K, num_sms, &ci, &s);
+    *rows = list[ci].R;
     *splits = s;
-    *ctas_per_sm = MmaConfigs<NT>::list[ci].occ;
+    *ctas_per_sm = list[ci].occ;
 }
 
 }  // namespace
+
+void mma_forced_config(int* rows, int* splits, int* ctas_per_sm) {
+    *rows = g_force_rows.load();
+    *splits = g_force_s.load();
+    *ctas_per_sm = g_force_occ.load();
+}
+
+bool mma_measured_launch(int64_t N, int64_t K, int mt, int* rows, int* splits, int* ctas_per_sm) {
+    LaunchEntry e;
+    if (!measured_launch(N, K, mt, &e)) return false;
+    *rows = e.R;
+    *splits = e.S;
+    *ctas_per_sm = e.occ;
+    return true;
+}
 
 void mma_launch_config(int64_t M, int64_t N, int64_t K, int num_sms, int* rows, int* splits, int* ctas_per_sm) {
     const int Ni = (int)N, Ki = (int)K;
@@ -904,16 +176,8 @@ cudaError_t launch_matmul_mma_grouped(const void* w, int64_t expert_stride, int6
     const int64_t mean = (total_rows + slots - 1) / slots;
     const int mt = mma_tile_rows(mean);
     CUtensorMap tq;
-    {
-        const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)total_rows};
-        const cuuint64_t gstride[1] = {(cuuint64_t)K};
-        const cuuint32_t box[2] = {(cuuint32_t)kQBoxK, (cuuint32_t)mt};
-        const cuuint32_t estride[2] = {1, 1};
-        if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qs), gdim, gstride, box, estride,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
+    const cudaError_t eq = encode_q_map(enc, qs, K, total_rows, mt, &tq);
+    if (eq != cudaSuccess) return eq;
     const __half* dsh = reinterpret_cast<const __half*>(ds);
     // 128-row tiles, or 64 / 32 when the experts' row tiles alone do not
     // give every SM a CTA.
@@ -945,32 +209,27 @@ int mma_tile_rows(int64_t M) {
     return 8 * (int)(nt < 4 ? nt : 4);
 }
 
-cudaError_t launch_matmul_mma(const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds, int64_t M,
-                              float* y, int64_t ldy, void* encode, int* err, int num_sms, cudaStream_t stream) {
+cudaError_t launch_matmul_mma(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs, const void* ds,
+                              int64_t M, float* y, int64_t ldy, void* encode, int* err, int num_sms,
+                              cudaStream_t stream) {
+    if (wt != kWtIQ4XS) return launch_matmul_mma_b18(wt, w, N, K, qs, ds, M, y, ldy, encode, err, num_sms, stream);
     const EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(encode);
     const int64_t row_bytes = wt_row_bytes(kWtIQ4XS, K);
     const int mt = mma_tile_rows(M);
     CUtensorMap tq;
-    {
-        // Q8_1 codes: one box = mt rows x 128 codes, 128-byte swizzle; rows
-        // past M read as zeros.
-        const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
-        const cuuint64_t gstride[1] = {(cuuint64_t)K};
-        const cuuint32_t box[2] = {(cuuint32_t)kQBoxK, (cuuint32_t)mt};
-        const cuuint32_t estride[2] = {1, 1};
-        if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qs), gdim, gstride, box, estride,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
+    const cudaError_t eq = encode_q_map(enc, qs, K, M, mt, &tq);
+    if (eq != cudaSuccess) return eq;
     const __half* dsh = reinterpret_cast<const __half*>(ds);
     const int Ni = (int)N, Ki = (int)K;
+#define IQ4XS_MMA_BEST(nt) \
+    launch_best<nt, false>(MmaConfigs<nt>::list, w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, kWtIQ4XS, num_sms, stream)
     switch (mt) {
-        case 8: return launch_best<1>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
-        case 16: return launch_best<2>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
-        case 24: return launch_best<3>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
-        default: return launch_best<4>(w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, num_sms, stream);
+        case 8: return IQ4XS_MMA_BEST(1);
+        case 16: return IQ4XS_MMA_BEST(2);
+        case 24: return IQ4XS_MMA_BEST(3);
+        default: return IQ4XS_MMA_BEST(4);
     }
+#undef IQ4XS_MMA_BEST
 }
 
 }  // namespace iq4xs

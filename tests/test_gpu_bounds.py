@@ -129,7 +129,7 @@ def test_block32_formats_clean(wt):
         qs, ds = quantize_gpu(x)
         qs_o, d_o, _ = oracle_q8(x)
         ref = oracle.get().matmul_wt(wt, w, N, K, qs_o, d_o)
-        for path in (B.PATH_DP4A, B.PATH_TC):
+        for path in (B.PATH_DP4A, B.PATH_TC, B.PATH_MMA):
             y = torch.full((M, N), float("nan"), device="cuda")
             B.iq4xs_matmul_wt(dev(w), wt, N, K, qs, ds, M, y, path)
             torch.cuda.synchronize()
@@ -218,4 +218,7 @@ def test_margin_reports_every_kernel():
     wg = dev(np.concatenate([w] * 3))
     for path in ("dp4a", "mma", "tc"):
         _under_margin(lambda: B.iq4xs_matmul_grouped(wg, stride, 3, N, K, qs, ds, offsets, y, path=path), path)
+    w18 = dev(synth.block32_weights(rng, N, K, 2e-3))
+    for path, kernel in ((B.PATH_DP4A, "dp4a"), (B.PATH_MMA, "mma"), (B.PATH_TC, "tc")):
+        _under_margin(lambda: B.iq4xs_matmul_wt(w18, B.WTYPE_Q4_0, N, K, qs, ds, M, y, path), kernel)
     _clean()

@@ -1,6 +1,7 @@
 """Q4_0 and IQ4_NL weights (32-weight blocks of 18 bytes) on the GPU through
-the C ABI, against the oracle: both paths, ragged N tails, several M tiles,
-split K, full-size sampled rows; dequantization bit-exact; and the
+the C ABI, against the oracle: every path (DP4A, warp MMA, tcgen05 in both
+forms), ragged N tails, several M tiles, split K, every warp-MMA launch
+configuration, full-size sampled rows; dequantization bit-exact; and the
 IQ4_NL / IQ4_XS identity (uniform sub-block scale) bit for bit."""
 import numpy as np
 import pytest
@@ -67,7 +68,7 @@ def test_formats_match_oracle_on_every_path(name, wt, N, K):
         qs, ds = quantize_gpu(x[:M])
         qs_o, d_o, _ = oracle_q8(x[:M])
         ref = _oracle_wt(wt, w, N, K, qs_o, d_o)
-        paths = [B.PATH_AUTO, B.PATH_DP4A] + ([B.PATH_TC, "tcp"] if K % 512 == 0 else [])
+        paths = [B.PATH_AUTO, B.PATH_DP4A] + ([B.PATH_TC, "tcp", B.PATH_MMA] if K % 512 == 0 else [])
         for path in paths:
             if path == "tcp":
                 y = matmul_gpu(wd, N, K, None, None, M, "tcp", op=prepare_gpu(x[:M]), wtype=wt)
@@ -90,9 +91,35 @@ def test_formats_full_size_sampled_rows(name, wt, N, K):
         x = synth.activations(rng, M, K)
         qs, ds = quantize_gpu(x)
         qs_o, d_o, _ = oracle_q8(x)
-        y = _matmul_wt(wd, wt, N, K, qs, ds, M, B.PATH_AUTO)
-        assert gate_written(y) is None
-        assert gate_parity(y[:, rows], _oracle_wt(wt, w, N, K, qs_o, d_o, rows)) is None, (name, M)
+        ref = _oracle_wt(wt, w, N, K, qs_o, d_o, rows)
+        for path in (B.PATH_AUTO, B.PATH_MMA) if M <= 32 else (B.PATH_AUTO,):
+            y = _matmul_wt(wd, wt, N, K, qs, ds, M, path)
+            assert gate_written(y) is None
+            assert gate_parity(y[:, rows], ref) is None, (name, M, path)
+
+
+@pytest.mark.parametrize("name,wt", FORMATS)
+@pytest.mark.parametrize("rows,splits,occ", [(32, 1, 0), (64, 3, 0), (128, 8, 0), (256, 2, 0), (32, 4, 2),
+                                             (64, 1, 2)])
+def test_formats_mma_launch_configs(name, wt, rows, splits, occ):
+    """Every warp-MMA launch the 18-byte formats can take (rows per CTA,
+    K split over a cluster, one or two CTAs per SM), with ragged row tiles
+    and activation tiles of 8 to 32 rows."""
+    rng = np.random.default_rng([45, wt, rows, splits])
+    N, K = 300, 4608
+    w = synth.block32_weights(rng, N, K, 2e-3)
+    wd = dev(w)
+    B.iq4xs_test_mma_config(rows, splits, occ)
+    try:
+        for M in (1, 8, 13, 24, 40):
+            x = synth.activations(rng, M, K, outlier_frac=0.01)
+            qs, ds = quantize_gpu(x)
+            qs_o, d_o, _ = oracle_q8(x)
+            y = _matmul_wt(wd, wt, N, K, qs, ds, M, B.PATH_MMA)
+            assert gate_written(y) is None
+            assert gate_parity(y, _oracle_wt(wt, w, N, K, qs_o, d_o)) is None, (name, rows, splits, occ, M)
+    finally:
+        B.iq4xs_test_mma_config(0, 0, 0)
 
 
 @pytest.mark.parametrize("name,wt", FORMATS + [("iq4_xs", B.WTYPE_IQ4_XS)])
@@ -134,7 +161,7 @@ def test_iq4nl_equals_iq4xs_with_uniform_scale_bitwise():
     x = synth.activations(rng, 40, K)
     for M in (1, 3, 40):
         qs, ds = quantize_gpu(x[:M])
-        for path in (B.PATH_DP4A, B.PATH_TC):
+        for path in (B.PATH_DP4A, B.PATH_TC, B.PATH_MMA):
             a = _matmul_wt(w_xs, B.WTYPE_IQ4_XS, N, K, qs, ds, M, path)
             b = _matmul_wt(w_nl, B.WTYPE_IQ4_NL, N, K, qs, ds, M, path)
             assert gate_written(a) is None
