@@ -494,8 +494,9 @@ int iq4xs_set_mma_launch_table(const int64_t* entries, int count);
  * take them (forced by iq4xs_test_mma_config, else from the measured
  * launch table, else from the launch model) for activation tiles of
  * min(32, M rounded up to 8) rows, for IQ4_XS weights (Q4_0 / IQ4_NL
- * launches choose among a subset of the configurations by the same model,
- * with no measured table).  Host only; queries the device's
+ * launches take the same measured launch where the table holds the shape;
+ * the model alone weighs their 6 % larger stages).  Host only; queries the
+ * device's
  * cluster occupancy once per configuration.  IQ4XS_ERR_SHAPE unless K %
  * 512 == 0 and the sizes are in range; IQ4XS_ERR_ARG for null outputs.
  */

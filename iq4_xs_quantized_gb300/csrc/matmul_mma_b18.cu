@@ -9,9 +9,11 @@
 //
 // The kernel is the IQ4_XS one with the 18-byte layout (its stage row is 288
 // bytes in two 144-byte boxes, the row scale is the block's d) and the
-// format's values in the byte table.  The launch list is a subset of the
-// IQ4_XS one (fewer instantiations to compile; the cost model weighs the
-// larger stage rows); no calibrated launch table applies to these formats.
+// format's values in the byte table.  The launch list is the IQ4_XS one, and
+// the launch is chosen the same way: the measured IQ4_XS launch for the
+// shape and tile height if the calibration installed one (the kernels differ
+// only in the decode and 6 % more weight bytes), else the cost model with
+// the larger stage rows weighed in.
 #include "mma_kernel.cuh"
 
 namespace iq4xs {
@@ -21,22 +23,26 @@ template <int NT>
 struct MmaConfigsB18;
 template <>
 struct MmaConfigsB18<1> {
-    static constexpr MmaConfig list[] = {cfg_of<1, 8, 1, true>(), cfg_of<1, 4, 1, true>(), cfg_of<1, 2, 1, true>(),
-                                         cfg_of<1, 1, 1, true>(), cfg_of<1, 2, 2, true>(), cfg_of<1, 1, 2, true>()};
+    static constexpr MmaConfig list[] = {cfg_of<1, 8, 1, true>(), cfg_of<1, 7, 1, true>(), cfg_of<1, 6, 1, true>(),
+                                         cfg_of<1, 5, 1, true>(), cfg_of<1, 4, 1, true>(), cfg_of<1, 3, 1, true>(),
+                                         cfg_of<1, 2, 1, true>(), cfg_of<1, 1, 1, true>(), cfg_of<1, 2, 2, true>(),
+                                         cfg_of<1, 1, 2, true>()};
 };
 template <>
 struct MmaConfigsB18<2> {
-    static constexpr MmaConfig list[] = {cfg_of<2, 8, 1, true>(), cfg_of<2, 4, 1, true>(), cfg_of<2, 2, 1, true>(),
-                                         cfg_of<2, 1, 1, true>(), cfg_of<2, 1, 2, true>()};
+    static constexpr MmaConfig list[] = {cfg_of<2, 8, 1, true>(), cfg_of<2, 7, 1, true>(), cfg_of<2, 6, 1, true>(),
+                                         cfg_of<2, 5, 1, true>(), cfg_of<2, 4, 1, true>(), cfg_of<2, 3, 1, true>(),
+                                         cfg_of<2, 2, 1, true>(), cfg_of<2, 1, 1, true>(), cfg_of<2, 1, 2, true>()};
 };
 template <>
 struct MmaConfigsB18<3> {
-    static constexpr MmaConfig list[] = {cfg_of<3, 4, 1, true>(), cfg_of<3, 2, 1, true>(), cfg_of<3, 1, 1, true>(),
-                                         cfg_of<3, 1, 2, true>()};
+    static constexpr MmaConfig list[] = {cfg_of<3, 4, 1, true>(), cfg_of<3, 3, 1, true>(), cfg_of<3, 2, 1, true>(),
+                                         cfg_of<3, 1, 1, true>(), cfg_of<3, 1, 2, true>()};
 };
 template <>
 struct MmaConfigsB18<4> {
-    static constexpr MmaConfig list[] = {cfg_of<4, 4, 1, true>(), cfg_of<4, 2, 1, true>(), cfg_of<4, 1, 1, true>()};
+    static constexpr MmaConfig list[] = {cfg_of<4, 4, 1, true>(), cfg_of<4, 3, 1, true>(), cfg_of<4, 2, 1, true>(),
+                                         cfg_of<4, 1, 1, true>()};
 };
 
 }  // namespace

@@ -62,8 +62,8 @@
 namespace iq4xs {
 
 // Launch choices kept once (matmul_mma.cu) for both translation units: the
-// forced test configuration (0 = none), and the measured launch for an
-// IQ4_XS shape and activation-tile height, if the calibration installed one.
+// forced test configuration (0 = none), and the measured launch for a shape
+// and activation-tile height, if the calibration installed one.
 void mma_forced_config(int* rows, int* splits, int* ctas_per_sm);
 bool mma_measured_launch(int64_t N, int64_t K, int mt, int* rows, int* splits, int* ctas_per_sm);
 // Q4_0 / IQ4_NL weights (wt) on the warp-MMA path (matmul_mma_b18.cu).
@@ -744,7 +744,8 @@ constexpr LaunchCost kLaunchCost[4] = {
 
 // The configuration (R, CTAs per SM) and K split S (= cluster size) for a
 // call: the forced one (tests), else the measured one for this shape and
-// tile height if the calibration installed it (IQ4_XS), else the least
+// tile height if the calibration installed it (measured on IQ4_XS weights,
+// taken for every format), else the least
 // modelled time waves x (F + a x occ x R / 128 x st x b + d x st) +
 // c x (S - 1), st = ceil(pairs / S) stages per CTA and b = the stage row's
 // bytes / 272, over the list's configurations and S = 1..8 (at most the K
@@ -782,7 +783,7 @@ void choose_config(const MmaConfig* list, int count, int64_t M, int N, int K, in
     int fr = 0, fs = 0, fo = 0;
     mma_forced_config(&fr, &fs, &fo);
     int mr = 0, ms = 0, mo = 0;
-    if (!kB18 && fr <= 0 && fs <= 0 && fo <= 0 && mma_measured_launch(N, K, 8 * NT, &mr, &ms, &mo)) {
+    if (fr <= 0 && fs <= 0 && fo <= 0 && mma_measured_launch(N, K, 8 * NT, &mr, &ms, &mo)) {
         for (int ci = 0; ci < count; ++ci)
             if (list[ci].R == mr && list[ci].occ == mo && ms >= 1 && ms <= kMmaMaxCluster && ms <= pairs) {
                 *best_c = ci;

@@ -99,8 +99,8 @@ def test_formats_full_size_sampled_rows(name, wt, N, K):
 
 
 @pytest.mark.parametrize("name,wt", FORMATS)
-@pytest.mark.parametrize("rows,splits,occ", [(32, 1, 0), (64, 3, 0), (128, 8, 0), (256, 2, 0), (32, 4, 2),
-                                             (64, 1, 2)])
+@pytest.mark.parametrize("rows,splits,occ", [(32, 1, 0), (64, 3, 0), (96, 5, 0), (128, 8, 0), (192, 1, 0),
+                                             (256, 2, 0), (32, 4, 2), (64, 1, 2)])
 def test_formats_mma_launch_configs(name, wt, rows, splits, occ):
     """Every warp-MMA launch the 18-byte formats can take (rows per CTA,
     K split over a cluster, one or two CTAs per SM), with ragged row tiles
