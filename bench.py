@@ -789,7 +789,7 @@ def moe_grouped(torch, B, dev, layers=12, reps=5, tokens=(1, 4, 16, 64, 256)):
 
 
 def weight_formats(torch, B, dev, stream, iq4xs_us, N=4096, K=4096, copies=48, reps=10,
-                   ms=(1, 4, 16, 64, 96)):
+                   ms=(1, 4, 8, 16, 64, 96)):
     """The same square 4096 x 4096 matmul with Q4_0 and IQ4_NL weights
     (18-byte blocks of 32, 0.5625 B/weight) on the dispatcher's path:
     device time per launch from graphs of back-to-back launches over

@@ -35,12 +35,15 @@ __global__ void __launch_bounds__(kQuantThreads)
     // launched when each had started).  The matmul's CTAs take SMs as the
     // preceding grid's leave and stream their weights meanwhile.  x may come
     // from the preceding grid, and qs/ds/the operand may still be read by it:
-    // wait for it before reading or writing anything.
+    // wait for it before reading or writing anything.  Its lines are only
+    // requested into L2 before the wait: a prefetch is a hint that reads no
+    // value, and L2 is where the preceding grid's writes land.
     griddep_launch_dependents();
-    griddep_wait();
     const int64_t m = blockIdx.y;
     const int64_t e0 = (int64_t)blockIdx.x * kElemsPerCta + threadIdx.x * kElemsPerThread;
     const bool live = e0 < K;  // whole warps (see above)
+    if (live && m < M) asm volatile("prefetch.global.L2 [%0];" ::"l"(x + m * ldx + e0));
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int l8 = lane & 7;  // position of this thread inside its Q8_1 block
     const Bc bc = bc_open(err);
