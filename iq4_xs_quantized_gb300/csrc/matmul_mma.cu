@@ -11,15 +11,17 @@
 namespace iq4xs {
 namespace {
 
-// Grouped (mixture-of-experts) launch of the <NT, T> kernel: W of expert g
-// through a 3D tensor map (row words x rows x experts, expert_stride bytes
-// apart), grid (row tiles, 1, expert slots).
+// Grouped (mixture-of-experts) launch of the persistent <NT, T> kernel: W
+// of expert g through a 3D tensor map (row words x rows x experts,
+// expert_stride bytes apart); one CTA per SM, or fewer when the layer has
+// fewer work items (at most row tiles x (activation tiles of all rows +
+// experts with rows)).
 template <int NT, int T>
 cudaError_t launch_grouped_nt(const void* w, int64_t expert_stride, int G, int64_t row_bytes, EncodeTiledFn enc,
                               const CUtensorMap& tq, const __half* ds, const int32_t* row_offsets, int64_t rows,
                               int slots, int N, int K, float* y, int64_t ldy, int* err, int num_sms,
                               cudaStream_t stream) {
-    using C = MmaCfg<NT, T, 1>;
+    using C = MmaCfg<NT, T, 1, false, true>;
     int dev = 0;
     cudaGetDevice(&dev);
     const cudaError_t ea = mma_smem_attr<NT, T, 1, true>(dev);
@@ -36,7 +38,8 @@ cudaError_t launch_grouped_nt(const void* w, int64_t expert_stride, int G, int64
             return cudaErrorInvalidValue;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + C::kR - 1) / C::kR), 1, (unsigned)slots);
+    const int64_t items = (N + C::kR - 1) / C::kR * ((rows + C::kMt - 1) / C::kMt + slots);
+    cfg.gridDim = dim3((unsigned)(items < num_sms ? items : num_sms), 1, 1);
     cfg.blockDim = dim3(kMmaThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
@@ -180,7 +183,7 @@ cudaError_t launch_matmul_mma_grouped(const void* w, int64_t expert_stride, int6
     if (eq != cudaSuccess) return eq;
     const __half* dsh = reinterpret_cast<const __half*>(ds);
     // 128-row tiles, or 64 / 32 when the experts' row tiles alone do not
-    // give every SM a CTA.
+    // give every SM a work item.
     const int Ni = (int)N, Ki = (int)K, Gi = (int)G;
     const int64_t ctas128 = (N + 127) / 128 * slots;
     const int rows_cta = ctas128 >= num_sms ? 128 : ((N + 63) / 64 * slots >= num_sms ? 64 : 32);
@@ -198,7 +201,12 @@ cudaError_t launch_matmul_mma_grouped(const void* w, int64_t expert_stride, int6
         IQ4XS_MMA_G(1)
         IQ4XS_MMA_G(2)
         IQ4XS_MMA_G(3)
-        IQ4XS_MMA_G(4)
+        case 32:  // 64-row tiles at most: the partial tiles of 128 would leave one stage
+            if (rows_cta >= 64)
+                return launch_grouped_nt<4, 2>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets,
+                                               total_rows, slots, Ni, Ki, y, ldy, err, num_sms, stream);
+            return launch_grouped_nt<4, 1>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets, total_rows,
+                                           slots, Ni, Ki, y, ldy, err, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 #undef IQ4XS_MMA_G

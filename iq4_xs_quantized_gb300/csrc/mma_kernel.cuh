@@ -101,7 +101,9 @@ __host__ __device__ constexpr uint32_t gap_addr(uint32_t o) { return ((o >> 7) <
 // kB18: weights in 18-byte blocks of 32 (Q4_0, IQ4_NL) instead of 136-byte
 // super-blocks of 256; a stage is 512 weights of a row either way (272 or
 // 288 bytes).
-template <int NT, int T, int kOcc = 1, bool kB18 = false>
+// kPersist (the grouped form): the partial tiles and the item descriptors
+// get a region of their own after the ring.
+template <int NT, int T, int kOcc = 1, bool kB18 = false, bool kPersist = false>
 struct MmaCfg {
     static_assert(NT >= 1 && NT <= 4, "1..4 fragments of 8 activation rows");
     static_assert(T >= 1 && T * NT <= 16, "accumulators: T x NT x 4 registers per lane");
@@ -117,14 +119,18 @@ struct MmaCfg {
     static constexpr int kRowB = kB18 ? 2 * kB18GroupBytes : kPairBytes;  // W bytes of a row per stage
     static constexpr int kWBytes = (kR * kRowB + 1023) / 1024 * 1024;
     static constexpr int kStage = kWBytes + kQStage;
+    static constexpr int kRedStride = kMt + 4;             // fp32 per row of a partial tile
+    static constexpr int kRedBytes = kPersist ? kMmaConsumers / 2 * kR * kRedStride * 4 : 0;
+    static constexpr int kExtra = kPersist ? kRedBytes + kMmaMaxStages * 16 : 0;
     // kOcc CTAs per SM: the whole shared memory (227 KB) for one, or half
     // of it (113 KB) for two -- then a launch's CTAs can start beside the
     // preceding launch's last ones.
     static_assert(kOcc == 1 || kOcc == 2, "one or two CTAs per SM");
-    static constexpr int kRing = (kOcc == 1 ? kMmaSmemLimit : kMmaSmemLimit2) - kOffRingMma - kMmaBarBytes;
+    static constexpr int kRing =
+        (kOcc == 1 ? kMmaSmemLimit : kMmaSmemLimit2) - kOffRingMma - kMmaBarBytes - kExtra;
     static constexpr int kNS = kRing / kStage < kMmaMaxStages ? kRing / kStage : kMmaMaxStages;
     static_assert(kNS >= 2, "two stages in flight");
-    static constexpr int kSmem = kOffRingMma + kNS * kStage + kMmaBarBytes;
+    static constexpr int kSmem = kOffRingMma + kNS * kStage + kExtra + kMmaBarBytes;
     // Per-warp tables (gap space): row scales [k][s][g][h] (rows
     // 16 f + g + 8 h of fragment f = rg + 2 k), then d_x [s][m].
     static constexpr int kSwFloats = kSPW * T * 16;
@@ -133,8 +139,8 @@ struct MmaCfg {
     static_assert(kMmaConsumers * kWarpTab <= kGapBytes, "tables fit the byte table's gaps");
     static constexpr int kXItems = (kDxFloats + 31) / 32;  // d_x loads per lane and stage
     static constexpr int kCombos = T * 8;                  // (fragment, g) pairs of a warp
-    static constexpr int kRedStride = kMt + 4;             // fp32 per row of a partial tile
-    static_assert(kSG * kR * kRedStride * 4 <= kNS * kStage, "partials fit the ring");
+    static_assert(kPersist || kSG * kR * kRedStride * 4 <= kNS * kStage, "partials fit the ring");
+    static_assert(!kPersist || kRedBytes == kSG * kR * kRedStride * 4, "a partial tile per sub-block group");
     static_assert(kSmem <= (kOcc == 1 ? kMmaSmemLimit : kMmaSmemLimit2), "shared memory per CTA");
     static_assert(kR * kRedStride * 4 <= kWideLutBytes, "CTA tile fits the byte table");
 };
@@ -160,20 +166,37 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t local_addr, uint32_t
 __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kMmaConsumers) : "memory");
 }
-// Consumers and producer between two activation tiles of one CTA.
-__device__ __forceinline__ void tile_sync() { asm volatile("bar.sync 2, %0;" ::"n"(kMmaThreads) : "memory"); }
-// kGrouped: mixture-of-experts form.  Expert slot z (grid z) takes the z-th
-// expert that has rows (row_offsets, a device array read after the wait for
-// the preceding grid); W is that expert's matrix (a 3D tensor map over the
-// experts) and its rows [r0, r1) of the activations are covered in tiles of
-// kMt, one pass over K per tile; no K split.  Otherwise grid z is the
-// activation tile of rows [z kMt, (z + 1) kMt).
+// consumers_sync that also returns whether v held in any consumer thread.
+__device__ __forceinline__ bool consumers_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, 1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(32 * kMmaConsumers)
+        : "memory");
+    return r != 0;
+}
+// kGrouped: mixture-of-experts form, persistent.  The layer's work items
+// are, for each expert with rows (in expert order; rows from row_offsets, a
+// device array read after the wait for the preceding grid), each R-row tile
+// of its W and each kMt-row tile of its activation rows (the activation
+// tile varying fastest, so that CTAs working at once share a W tile in L2);
+// CTA c takes items c, c + gridDim.x, ...  One pass over K per item, no K
+// split.  The producer warp walks the experts once, 32 at a time, and runs
+// ahead across items: each item's descriptor goes into a small ring in
+// shared memory before its first stage is issued, and an empty stage after
+// the last item tells the consumers to stop.  The partial tiles of the
+// sub-block groups have a region of their own, so the next item's stages
+// stream in while the consumers sum the current one.  Otherwise grid z is
+// the activation tile of rows [z kMt, (z + 1) kMt) and grid (x, y) the
+// weight-row tile and the K range.
 template <int NT, int T, int kOcc, bool kGrouped, bool kB18 = false>
 __global__ void __launch_bounds__(kMmaThreads, kOcc)
     matmul_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_q,
                       const __half* __restrict__ ds, int64_t M, int N, int K, float* __restrict__ y, int64_t ldy,
                       int* err, const int32_t* __restrict__ row_offsets, int G, int wt) {
-    using C = MmaCfg<NT, T, kOcc, kB18>;
+    using C = MmaCfg<NT, T, kOcc, kB18, kGrouped>;
     static_assert(!(kGrouped && kB18), "the grouped form takes IQ4_XS");
     constexpr int kTMax = T, kMt = C::kMt, kSPW = C::kSPW, kRG = C::kRG, R = C::kR, NS = C::kNS;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -184,104 +207,59 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
     constexpr int stage_b = C::kStage, wbytes = C::kWBytes;
     const Bc bc = bc_open(err);
     if (!bc_range(bc, 0, C::kSmem, dyn_smem_bytes(), kBcMmaSmem)) return;  // every CTA alike
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffRingMma + NS * stage_b);
+    uint8_t* extra = smem + kOffRingMma + NS * stage_b;  // grouped: partial tiles, then descriptors
+    uint64_t* full = reinterpret_cast<uint64_t*>(extra + C::kExtra);
     uint64_t* empty = full + kMmaMaxStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kMmaMaxStages);
-    int* grp = reinterpret_cast<int*>(empty + kMmaMaxStages) + 2;  // grouped: expert, first row, end row
+    int4* desc = reinterpret_cast<int4*>(extra + C::kRedBytes);  // grouped: {expert, n0, first row, end row}
     const uint32_t sbase = smem_u32(smem);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = gridDim.y;
     const uint32_t rank = (S > 1) ? cluster_ctarank() : 0;
-    const int n0 = blockIdx.x * R;
+    const int n0 = blockIdx.x * R;  // dense form
     const int z = blockIdx.z;
     const int pairs = (K + kPairK - 1) / kPairK;
     const int p0 = (int)((int64_t)pairs * rank / S);
     const int p1 = (int)((int64_t)pairs * (rank + 1) / S);
     const int nst = p1 - p0;
+    // dense form: activation rows [row_lo, row_hi)
+    const int64_t row_lo = (int64_t)z * kMt, row_hi = (row_lo + kMt < M) ? row_lo + kMt : M;
 
-    // Activation rows this CTA covers: [row_lo, row_hi) in mtiles tiles.
-    int gexp = 0;
-    int64_t row_lo = (int64_t)z * kMt, row_hi = (row_lo + kMt < M) ? row_lo + kMt : M;
-    if constexpr (kGrouped) {
-        if (warp == 0) {
-            griddep_wait();  // the offsets may come from the preceding grid
-            // The z-th expert with rows: offsets of 128 experts per step
-            // (independent loads), one ballot per 32.
-            int ge = -1;
-            uint32_t k = (uint32_t)z;
-            for (int base = 0; base < G && ge < 0; base += 4 * 32) {
-                int32_t lo[4], hi[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int e = base + 32 * j + lane;
-                    const bool in =
-                        e < G && bc_global(bc, row_offsets + e, 8, row_offsets, (int64_t)(G + 1) * 4, kBcMmaOffsets);
-                    lo[j] = in ? __ldg(row_offsets + e) : 0;
-                    hi[j] = in ? __ldg(row_offsets + e + 1) : 0;
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t mask = __ballot_sync(0xffffffffu, hi[j] > lo[j]);
-                    const uint32_t cnt = __popc(mask);
-                    if (ge < 0) {
-                        if (k < cnt) ge = base + 32 * j + (int)__fns(mask, 0, (int)k + 1);
-                        else k -= cnt;
-                    }
-                }
-            }
-            if (lane == 0) {
-                grp[0] = ge;
-                grp[1] = ge >= 0 ? row_offsets[ge] : 0;
-                grp[2] = ge >= 0 ? row_offsets[ge + 1] : 0;
-                // offsets outside the rows of y: the expert is skipped
-                if (ge >= 0 && !bc_range(bc, grp[1], (int64_t)grp[2] - grp[1], M, kBcMmaRows)) grp[0] = -1;
-            }
-        }
-        __syncthreads();
-        gexp = grp[0];
-        if (gexp < 0) return;  // fewer experts with rows than slots (whole CTA; no cluster)
-        row_lo = grp[1];
-        row_hi = grp[2];
-    }
-    // one activation tile per CTA unless it covers an expert's rows
-    const int mtiles = kGrouped ? (int)((row_hi - row_lo + kMt - 1) / kMt) : 1;
-    const int total = mtiles * nst;  // stages over all activation tiles
-
-    // Stage gs = activation tile gs / nst, K pair p0 + gs % nst.
-    auto tile_of = [&](int gs) { return kGrouped ? gs / nst : 0; };
-    auto pair_of = [&](int gs) { return p0 + (kGrouped ? gs % nst : gs); };
-    auto load_w = [&](int gs) {
+    // Stage gs of the current item: K pair p0 + gs % nst (grouped: items of
+    // nst stages one after the other), weight rows from n0w, activation rows
+    // from rq, expert e.
+    auto load_w = [&](int gs, int n0w, int e) {
         const int slot = gs % NS;
         uint8_t* dst = smem + kOffRingMma + slot * stage_b;
-        const int x = pair_of(gs) * (C::kRowB / 4);
-        if (!bc_tma(bc, x, 4, C::kRowB / 4, (int64_t)(K / kPairK) * (C::kRowB / 4), n0, N, kBcMmaWAlign, kBcMmaW))
+        const int x = (p0 + gs % nst) * (C::kRowB / 4);
+        if (!bc_tma(bc, x, 4, C::kRowB / 4, (int64_t)(K / kPairK) * (C::kRowB / 4), n0w, N, kBcMmaWAlign, kBcMmaW))
             return;
-        if constexpr (kGrouped) bc_range(bc, gexp, 1, G, kBcMmaW);
+        if constexpr (kGrouped) bc_range(bc, e, 1, G, kBcMmaW);
         mbar_arrive_expect_tx(&full[slot], (uint32_t)(R * C::kRowB + C::kQStage));
         if constexpr (kGrouped) {
-            tma_load_3d(dst, &tmap_w, x, n0, gexp, &full[slot]);
+            tma_load_3d(dst, &tmap_w, x, n0w, e, &full[slot]);
         } else if constexpr (kB18) {
             // two boxes of R rows x 144 B (eight 18-byte blocks each), one
             // after the other: 144-byte rows put the 8 rows a warp reads at
             // once on distinct banks, where 288-byte rows would not
-            tma_load_2d(dst, &tmap_w, x, n0, &full[slot]);
-            tma_load_2d(dst + R * kB18GroupBytes, &tmap_w, x + kB18GroupBytes / 4, n0, &full[slot]);
+            tma_load_2d(dst, &tmap_w, x, n0w, &full[slot]);
+            tma_load_2d(dst + R * kB18GroupBytes, &tmap_w, x + kB18GroupBytes / 4, n0w, &full[slot]);
         } else {
-            tma_load_2d(dst, &tmap_w, x, n0, &full[slot]);
+            tma_load_2d(dst, &tmap_w, x, n0w, &full[slot]);
         }
     };
-    auto load_q = [&](int gs) {
+    auto load_q = [&](int gs, int64_t rq64) {
         const int slot = gs % NS;
-        const int rq = (int)(row_lo + (int64_t)tile_of(gs) * kMt);
+        const int rq = (int)rq64;
 #pragma unroll
         for (int b = 0; b < kQBoxesPerStage; ++b) {
-            const int x = pair_of(gs) * kPairK + b * kQBoxK;
+            const int x = (p0 + gs % nst) * kPairK + b * kQBoxK;
             if (bc_tma(bc, x, 1, kQBoxK, K, rq, M, kBcMmaQAlign, kBcMmaQ))
                 tma_load_2d(smem + kOffRingMma + slot * stage_b + wbytes + b * C::kQBox, &tmap_q, x, rq, &full[slot]);
         }
     };
-    const int pre = nst < NS ? nst : NS;  // stages of the first activation tile issued at set-up
+    const int pre = nst < NS ? nst : NS;  // dense form: stages issued at set-up
     if (warp == kMmaProducerWarp && lane == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&full[i], 1);
@@ -290,12 +268,13 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
-        // The first W stages (model state) go out at once, before the byte
-        // table is built and before the preceding grid (which writes the
-        // codes) has finished.
         prefetch_tmap(&tmap_w);
         prefetch_tmap(&tmap_q);
-        for (int ps = 0; ps < pre; ++ps) load_w(ps);
+        // Dense form: the first W stages (model state) go out at once, before
+        // the byte table is built and before the preceding grid (which
+        // writes the codes) has finished.
+        if constexpr (!kGrouped)
+            for (int ps = 0; ps < pre; ++ps) load_w(ps, n0, 0);
     }
     // Byte table: row j = 32 copies (one per bank) of the fp16x2 word
     // (kv[j & 15], kv[j >> 4]) in its first 128 bytes.
@@ -310,37 +289,108 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
     bool ok = true;
     if (warp == kMmaProducerWarp) {
         int issued = 0;
-        for (int mt = 0; mt < mtiles; ++mt) {
-            // The next tile's stages wait until the consumers have summed
-            // the current tile's partials, which they keep in the ring.
-            if (mt > 0) tile_sync();
+        bool ended = false;  // grouped: the empty stage after the last item was posted
+        if constexpr (!kGrouped) {
             if (lane == 0) {
-                const int gs0 = mt * nst;
-                int first = 0;
-                if (mt == 0) {
-                    griddep_wait();  // the codes come from the preceding grid
-                    for (int ps = 0; ps < pre; ++ps) load_q(ps);
-                    first = pre;
-                    issued = pre;
-                }
-                for (int ps = first; ps < nst && ok; ++ps) {
-                    const int gs = gs0 + ps, slot = gs % NS;
+                griddep_wait();  // the codes come from the preceding grid
+                for (int ps = 0; ps < pre; ++ps) load_q(ps, row_lo);
+                issued = pre;
+                for (int gs = pre; gs < nst && ok; ++gs) {
+                    const int slot = gs % NS;
                     if (gs >= NS) {
                         ok = mbar_wait(&empty[slot], ((gs / NS) - 1) & 1, abort_flag, err, kDevErrTimeoutMmaSlot);
                         if (!ok) break;
                     }
-                    load_w(gs);
-                    load_q(gs);
+                    load_w(gs, n0, 0);
+                    load_q(gs, row_lo);
                     ++issued;
                 }
             }
             __syncwarp();
+        } else {
+            griddep_wait();  // the offsets and the codes come from the preceding grid
+            const int64_t ntx = (N + R - 1) / R;
+            // The expert cursor: experts [e0, e0 + 32) held one per lane (rows
+            // [lo, hi), items cnt, inclusive prefix incl within the 32), base =
+            // items of the experts before e0.
+            int e0 = 0, lo = 0, hi = 0;
+            int64_t base = 0, cnt = 0, incl = 0, tot = 0;
+            bool have = false;
+            int64_t item = blockIdx.x;
+            for (int k = 0;; ++k, item += gridDim.x) {
+                bool done = false;
+                for (;;) {
+                    if (!have) {
+                        if (e0 >= G) {
+                            done = true;
+                            break;
+                        }
+                        const int e = e0 + lane;
+                        const bool in = e < G && bc_global(bc, row_offsets + e, 8, row_offsets,
+                                                           (int64_t)(G + 1) * 4, kBcMmaOffsets);
+                        lo = in ? __ldg(row_offsets + e) : 0;
+                        hi = in ? __ldg(row_offsets + e + 1) : 0;
+                        // offsets outside the rows of y: the expert is skipped
+                        if (hi > lo && !bc_range(bc, lo, (int64_t)hi - lo, M, kBcMmaRows)) hi = lo;
+                        cnt = hi > lo ? ntx * ((hi - lo + kMt - 1) / kMt) : 0;
+                        incl = cnt;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+                            if (lane >= o) incl += v;
+                        }
+                        tot = __shfl_sync(0xffffffffu, incl, 31);
+                        have = true;
+                    }
+                    if (item < base + tot) break;
+                    base += tot;
+                    e0 += 32;
+                    have = false;
+                }
+                int4 d = make_int4(-1, 0, 0, 0);
+                if (!done) {
+                    const int f = __ffs(__ballot_sync(0xffffffffu, base + incl > item)) - 1;
+                    const int lo_f = __shfl_sync(0xffffffffu, lo, f), hi_f = __shfl_sync(0xffffffffu, hi, f);
+                    const int64_t j = item - base - __shfl_sync(0xffffffffu, incl - cnt, f);
+                    const int64_t tiles = (hi_f - lo_f + kMt - 1) / kMt;
+                    const int tr = (int)(j % tiles);
+                    const int r0 = lo_f + kMt * tr;
+                    d = make_int4(e0 + f, (int)(j / tiles) * R, r0, r0 + kMt < hi_f ? r0 + kMt : hi_f);
+                }
+                if (lane == 0) {
+                    // Item k's stages are gs0 .. gs0 + nst - 1.  Its descriptor
+                    // slot was last read when the consumers started item
+                    // k - kMmaMaxStages, before they released stage gs0 - NS.
+                    const int gs0 = k * nst;
+                    for (int ps = 0; ps < nst && ok; ++ps) {
+                        const int gs = gs0 + ps, slot = gs % NS;
+                        if (gs >= NS) {
+                            ok = mbar_wait(&empty[slot], ((gs / NS) - 1) & 1, abort_flag, err,
+                                           kDevErrTimeoutMmaSlot);
+                            if (!ok) break;
+                        }
+                        if (ps == 0) desc[k % kMmaMaxStages] = d;  // published by the stage's arrival
+                        if (d.x < 0) {
+                            mbar_arrive(&full[slot]);  // no more items: an empty stage
+                            ended = true;
+                            break;
+                        }
+                        load_w(gs, d.y, d.x);
+                        load_q(gs, d.z);
+                        ++issued;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+                if (done || !ok) break;
+            }
         }
         if (lane == 0) {
             // Drain: the last stage issued into each slot has landed (the
-            // earlier ones were consumed before their slot was reused).  Not
+            // earlier ones were consumed before their slot was reused; so
+            // was stage issued - NS once the empty stage took its slot).  Not
             // stopped by an abort: no copy may land after the CTA exits.
-            for (int gs = (issued > NS ? issued - NS : 0); gs < issued; ++gs)
+            const int first = issued - NS + (ended ? 1 : 0);
+            for (int gs = (first > 0 ? first : 0); gs < issued; ++gs)
                 mbar_wait(&full[gs % NS], (gs / NS) & 1, &g_never_abort_mma, err, kDevErrTimeoutDrain);
         }
         __syncwarp();
@@ -356,41 +406,39 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
         const uint32_t* ds32 = reinterpret_cast<const uint32_t*>(ds);
         const int64_t K32 = (K + kSub - 1) / kSub;
         float acc[kTMax][NT][4];
-        // Activation scales of stage gs for this warp's sub-blocks: item e =
-        // (row m = e / kSPW of the stage's tile, sub-block e % kSPW), fp16 d
-        // in ds; rows outside the CTA's range read as 0.
+        // Activation scales of K pair `pair` for this warp's sub-blocks: item
+        // e = (row m = rb + e / kSPW, sub-block e % kSPW), fp16 d in ds; rows
+        // from rhi on read as 0.
         uint32_t dxv[C::kXItems];
-        auto load_dx = [&](int gs) {
-            const int64_t rb = row_lo + (int64_t)tile_of(gs) * kMt;
+        auto load_dx = [&](int64_t rb, int64_t rhi, int pair) {
 #pragma unroll
             for (int k = 0; k < C::kXItems; ++k) {
                 const int e = lane + 32 * k;
                 const int64_t m = rb + e / kSPW;
-                const int64_t sub = (int64_t)pair_of(gs) * kSubPerPair + sub_w + e % kSPW;
-                dxv[k] = (e < C::kDxFloats && m < row_hi && sub < K32 &&
+                const int64_t sub = (int64_t)pair * kSubPerPair + sub_w + e % kSPW;
+                dxv[k] = (e < C::kDxFloats && m < rhi && sub < K32 &&
                           bc_global(bc, ds32 + m * K32 + sub, 4, ds, M * K32 * 4, kBcMmaDs))
                              ? __ldg(ds32 + m * K32 + sub)
                              : 0u;
             }
         };
         griddep_wait();  // ds comes from the preceding grid
-        if (total > 0) load_dx(0);
         // Row-scale work of this lane: (fragment slot k, g) pairs c = lane +
         // 32 i, rows 16 f + g and 16 f + g + 8, all kSPW sub-blocks.
         const int wrow_lane = 16 * rg + g;       // row of fragment slot 0 for this lane (+ 16 kRG k)
-
-        for (int mt = 0; mt < mtiles; ++mt) {
-        const int64_t row_base = row_lo + (int64_t)mt * kMt;
+        auto zero_acc = [&]() {
 #pragma unroll
-        for (int i = 0; i < kTMax; ++i)
+            for (int i = 0; i < kTMax; ++i)
 #pragma unroll
-            for (int f = 0; f < NT; ++f)
+                for (int f = 0; f < NT; ++f)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[i][f][e] = 0.f;
-        for (int ps = 0; ps < nst && ok; ++ps) {
-            const int gs = mt * nst + ps, slot = gs % NS;
-            ok = mbar_wait(&full[slot], (gs / NS) & 1, abort_flag, err, kDevErrTimeoutMmaStage);
-            if (!ok) break;
+                    for (int e = 0; e < 4; ++e) acc[i][f][e] = 0.f;
+        };
+        // Stage gs (landed) of an item with activation rows [rb, rhi): this
+        // warp's tables, then its MMAs; the activation scales of K pair
+        // next_pair of the same item (if >= 0) are requested meanwhile.
+        auto consume = [&](int gs, int64_t rb, int64_t rhi, int next_pair) {
+            const int slot = gs % NS;
             // Plain loads from here on: ordered after the barrier wait (an
             // asm statement with a memory clobber) and free to be scheduled
             // among themselves.
@@ -447,7 +495,7 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
                         __half2float(__ushort_as_half((unsigned short)(dxv[k] & 0xFFFFu)));
             }
             __syncwarp();
-            if (gs + 1 < total) load_dx(gs + 1);  // in flight during this stage
+            if (next_pair >= 0) load_dx(rb, rhi, next_pair);  // in flight during this stage
             // The four sub-blocks unrolled (loads of the next sub-block's words
             // overlap this one's lookups and MMAs: 5-6 % faster at 8 rows,
             // 6-14 % at 16) where the registers allow it: one activation
@@ -536,50 +584,87 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
-        }
-        if (!ok) {
-            // Wake the producer if it waits on a slot this warp will never free.
-            if (lane == 0) *abort_flag = 1;
-        }
-        // ---- end of the K range of this tile: partial tiles of the sub-block groups
-        consumers_sync();  // every consumer is done with the ring
-        if (!*abort_flag) {
-            float* red = reinterpret_cast<float*>(smem + kOffRingMma) + sg * R * C::kRedStride;
+        };
+        // The partial tiles of the sub-block groups into red, then (after a
+        // barrier) their sum into y rows [rb, rhi), columns n0i.. (or, with a
+        // K split, into this CTA's tile for the cluster's reduction).
+        auto store_partials = [&](float* red) {
+            red += sg * R * C::kRedStride;
 #pragma unroll
             for (int k = 0; k < kTMax; ++k) {
-                {
 #pragma unroll
-                    for (int f = 0; f < NT; ++f) {
-                        const int r = 16 * (rg + kRG * k) + g, c = 8 * f + 2 * t;
-                        *reinterpret_cast<float2*>(red + r * C::kRedStride + c) =
-                            make_float2(acc[k][f][0], acc[k][f][1]);
-                        *reinterpret_cast<float2*>(red + (r + 8) * C::kRedStride + c) =
-                            make_float2(acc[k][f][2], acc[k][f][3]);
-                    }
+                for (int f = 0; f < NT; ++f) {
+                    const int r = 16 * (rg + kRG * k) + g, c = 8 * f + 2 * t;
+                    *reinterpret_cast<float2*>(red + r * C::kRedStride + c) = make_float2(acc[k][f][0], acc[k][f][1]);
+                    *reinterpret_cast<float2*>(red + (r + 8) * C::kRedStride + c) =
+                        make_float2(acc[k][f][2], acc[k][f][3]);
                 }
             }
-        }
-        consumers_sync();
-        if (!*abort_flag) {
-            const float* red = reinterpret_cast<const float*>(smem + kOffRingMma);
+        };
+        auto sum_partials = [&](const float* red, int64_t rb, int64_t rhi, int n0i) {
             float* tile = reinterpret_cast<float*>(smem);
-            const int64_t mrows = row_hi - row_base;
+            const int64_t mrows = rhi - rb;
             for (int e = threadIdx.x; e < R * kMt; e += 32 * kMmaConsumers) {
                 const int r = e % R, m = e / R;
                 float v = red[r * C::kRedStride + m];
 #pragma unroll
                 for (int q = 1; q < C::kSG; ++q) v += red[(q * R + r) * C::kRedStride + m];
                 if (S == 1) {
-                    if (m < mrows && n0 + r < N &&
-                        bc_global(bc, y + (row_base + m) * ldy + n0 + r, 4, y, ((M - 1) * ldy + N) * 4, kBcMmaY))
-                        y[(row_base + m) * ldy + n0 + r] = v;
+                    if (m < mrows && n0i + r < N &&
+                        bc_global(bc, y + (rb + m) * ldy + n0i + r, 4, y, ((M - 1) * ldy + N) * 4, kBcMmaY))
+                        y[(rb + m) * ldy + n0i + r] = v;
                 } else {
                     tile[r * C::kRedStride + m] = v;
                 }
             }
+        };
+        if constexpr (!kGrouped) {
+            if (nst > 0) load_dx(row_lo, row_hi, p0);
+            zero_acc();
+            for (int ps = 0; ps < nst && ok; ++ps) {
+                ok = mbar_wait(&full[ps % NS], (ps / NS) & 1, abort_flag, err, kDevErrTimeoutMmaStage);
+                if (!ok) break;
+                consume(ps, row_lo, row_hi, ps + 1 < nst ? p0 + ps + 1 : -1);
+            }
+            if (!ok) {
+                // Wake the producer if it waits on a slot this warp will never free.
+                if (lane == 0) *abort_flag = 1;
+            }
+            // ---- end of the K range: partial tiles of the sub-block groups
+            float* red = reinterpret_cast<float*>(smem + kOffRingMma);
+            consumers_sync();  // every consumer is done with the ring
+            if (!*abort_flag) store_partials(red);
+            consumers_sync();
+            if (!*abort_flag) sum_partials(red, row_lo, row_hi, n0);
+        } else {
+            float* red = reinterpret_cast<float*>(extra);
+            bool failed = false;
+            for (int k = 0;; ++k) {
+                const int gs0 = k * nst;
+                ok = mbar_wait(&full[gs0 % NS], (gs0 / NS) & 1, abort_flag, err, kDevErrTimeoutMmaStage);
+                const int4 d = ok ? desc[k % kMmaMaxStages] : make_int4(-1, 0, 0, 0);
+                // Every consumer warp leaves together: after the last item, or
+                // when a wait of any of them ran out.
+                failed = consumers_any(!ok);
+                if (failed || d.x < 0) break;
+                load_dx(d.z, d.w, p0);
+                zero_acc();
+                for (int ps = 0; ps < nst && ok; ++ps) {
+                    const int gs = gs0 + ps;
+                    if (ps > 0) {
+                        ok = mbar_wait(&full[gs % NS], (gs / NS) & 1, abort_flag, err, kDevErrTimeoutMmaStage);
+                        if (!ok) break;
+                    }
+                    consume(gs, d.z, d.w, ps + 1 < nst ? p0 + ps + 1 : -1);
+                }
+                failed = consumers_any(!ok);  // and every consumer is done with this item's stages
+                if (failed) break;
+                store_partials(red);
+                consumers_sync();
+                sum_partials(red, d.z, d.w, d.y);
+            }
+            if (failed && threadIdx.x == 0) *abort_flag = 1;  // the producer stops issuing
         }
-        if (mt + 1 < mtiles) tile_sync();  // the ring may take the next tile's stages
-        }  // activation tiles
     }
 
     if (S > 1) {
@@ -638,7 +723,7 @@ cudaError_t mma_smem_attr(int dev) {
     if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
     const cudaError_t e = cudaFuncSetAttribute(matmul_mma_kernel<NT, T, kOcc, kGrouped, kB18>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               MmaCfg<NT, T, kOcc, kB18>::kSmem);
+                                               MmaCfg<NT, T, kOcc, kB18, kGrouped>::kSmem);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     return e;
 }
