@@ -73,6 +73,9 @@ def parse_args():
                     help="launch without programmatic dependent launch (for serialised profilers)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the dequantize+GEMM baseline and the decode-stream workload")
+    ap.add_argument("--moe-tokens", type=int, default=None,
+                    help="profiling runs only: time the grouped MoE layer at this many tokens, "
+                         "print its line and stop")
     return ap.parse_args()
 
 
@@ -376,6 +379,11 @@ def run_ours(args, world, rank, local):
     B.iq4xs_set_pdl(not args.no_pdl)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.moe_tokens:
+        res = moe_grouped(torch, B, dev, layers=2, reps=2, tokens=(args.moe_tokens,))
+        if rank == 0:
+            print(json.dumps({"moe_grouped": res}), flush=True)
+        return
     W = synth.SQUARE
     N, K = W.shapes[0]
     ms = list(W.ms) if not args.ms else [int(v) for v in args.ms.split(",")]
@@ -774,8 +782,8 @@ def moe_grouped(torch, B, dev, layers=12, reps=5, tokens=(1, 4, 16, 64, 256)):
         nbytes = (len(touched) * W.N * (W.K // 256) * 136 + M * W.K + M * (W.K // 32) * 4
                   + 4 * M * W.N + quantize_bytes(M, W.K))
         mean = -(-M // min(W.G, M))
-        auto = ("tc" if mean > 96 else "mma") if M >= W.G or B.iq4xs_select_path(mean, W.N, W.K) != B.PATH_DP4A \
-            else "dp4a"
+        auto = ("tc" if mean >= 32 else "mma") \
+            if M >= min(W.G, 24) or B.iq4xs_select_path(mean, W.N, W.K) != B.PATH_DP4A else "dp4a"
         res.append({"tokens": T, "rows": M, "experts_touched": len(touched), "auto_form": auto,
                     "grouped_us_per_layer": round(times["grouped"], 3),
                     "grouped_dp4a_us": round(times["grouped_dp4a"], 3),

@@ -233,14 +233,14 @@ int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t
  * Path: the CUDA-core (DP4A) kernel, each expert computed with the batch
  * width its own row count selects, so the result per expert is
  * bit-identical to iq4xs_matmul on the DP4A path over the same rows; or,
- * when K % 512 == 0 and either total_rows >= G (at least one row per expert
- * on average) or the mean rows per expert that has rows (total_rows /
- * min(G, total_rows)) exceeds the DP4A crossover of one expert's matrix
- * size, a tensor-core form: the warp-level MMA kernel in its grouped form
- * (one CTA per (row tile, expert), the expert's rows in activation tiles
- * of up to 32) up to 96 mean rows per expert slot, the tcgen05 kernel's
- * grouped form above; each sub-block's dot is exact as on those paths of
- * iq4xs_matmul.
+ * when K % 512 == 0 and either total_rows >= min(G, 24) or the mean rows
+ * per expert that has rows (total_rows / min(G, total_rows)) exceeds the
+ * DP4A crossover of one expert's matrix size, a tensor-core form: the
+ * warp-level MMA kernel in its grouped form (persistent: one CTA per SM
+ * walks the layer's (expert, weight-row tile, activation tile) items, the
+ * expert's rows in activation tiles of up to 32) below 32 mean rows per
+ * expert slot, the tcgen05 kernel's grouped form from 32 on; each
+ * sub-block's dot is exact as on those paths of iq4xs_matmul.
  */
 int iq4xs_matmul_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
                          const int8_t* qs, const void* ds, const int32_t* row_offsets,

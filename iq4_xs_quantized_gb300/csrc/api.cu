@@ -19,7 +19,8 @@ __device__ __align__(16) int g_device_error[kErrWords] = {0, 0, 0, 0};
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int64_t kGroupedTcMinRows = 96;  // grouped: tcgen05 above this mean rows per expert slot
+constexpr int64_t kGroupedTcMinRows = 32;   // grouped: tcgen05 from this mean rows per expert slot on
+constexpr int64_t kGroupedMmaMinRows = 24;  // grouped: warp MMA from this many rows on (at most G)
 constexpr int64_t kMaxM = 32768;
 
 struct DevState {
@@ -306,16 +307,18 @@ int iq4xs_matmul_grouped_path(const void* w, int64_t expert_stride, int64_t G, i
         !aligned(y, 4))
         return IQ4XS_ERR_ALIGN;
     if (path == IQ4XS_PATH_AUTO) {
-        // The warp-MMA form once there are at least as many rows as experts
-        // (measured on a 128 x 1536 x 2048 layer: from 128 rows on; at 512
-        // rows it takes half the time of the CUDA-core form), or once the
-        // mean rows of an expert slot leave one expert matrix's DP4A range;
-        // the tcgen05 form above 96 mean rows per expert slot (the same
-        // layer: equal at 64, 17 % faster at 256).
+        // The warp-MMA form from 24 rows on (as many as the experts, if
+        // fewer), or once the mean rows of an expert slot leave one expert
+        // matrix's DP4A range (measured on a 128 x 1536 x 2048 layer: the
+        // CUDA-core form is 6 % faster at 16 rows, 19 % slower at 24 and
+        // 30 % at 64); the tcgen05 form from 32 mean rows per expert slot on
+        // (the same layer: 15 % slower at 24, 2 % faster at 32, 8 % at 64,
+        // 24 % at 256).
         const int64_t slots = G < total_rows ? G : total_rows;
         const int64_t mean = (total_rows + slots - 1) / slots;
-        if (K % kPairK == 0 && (total_rows >= G || mean > crossover_for(N, K)))
-            path = mean > kGroupedTcMinRows ? IQ4XS_PATH_TC : IQ4XS_PATH_MMA;
+        const int64_t mma_min = G < kGroupedMmaMinRows ? G : kGroupedMmaMinRows;
+        if (K % kPairK == 0 && (total_rows >= mma_min || mean > crossover_for(N, K)))
+            path = mean >= kGroupedTcMinRows ? IQ4XS_PATH_TC : IQ4XS_PATH_MMA;
         else
             path = IQ4XS_PATH_DP4A;
     }

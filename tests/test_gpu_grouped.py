@@ -95,14 +95,14 @@ def test_grouped_mma_matches_oracle(T, topk):
         r0, r1 = int(offsets[g]), int(offsets[g + 1])
         ind_own[r0:r1] = ind[r0:r1, g * W.N:(g + 1) * W.N]
     assert gate_independent(y, ind_own) is None
-    # AUTO: the MMA form from as many rows as experts on, or once the mean
-    # rows of an expert slot leave one expert's dp4a range, else dp4a (same
-    # bits as the explicit call either way)
+    # AUTO: the MMA form from min(G, 24) rows on, or once the mean rows of
+    # an expert slot leave one expert's dp4a range, else dp4a; tcgen05 from
+    # 32 mean rows per expert slot on (same bits as the explicit call)
     M = rows_x.shape[0]
     slots = min(W.G, M)
     mean = -(-M // slots)
-    auto = ("tc" if mean > 96 else "mma") if M >= W.G or B.iq4xs_select_path(mean, W.N, W.K) != B.PATH_DP4A \
-        else "dp4a"
+    auto = ("tc" if mean >= 32 else "mma") \
+        if M >= min(W.G, 24) or B.iq4xs_select_path(mean, W.N, W.K) != B.PATH_DP4A else "dp4a"
     y_auto = _run_grouped(W, rows_x, offsets)[-1]
     y_expl = y if auto == "mma" else _run_grouped(W, rows_x, offsets, auto)[-1]
     assert np.array_equal(y_auto, y_expl), auto
@@ -123,9 +123,9 @@ def test_grouped_tc_matches_oracle(T, topk, G):
         r0, r1 = int(offsets[g]), int(offsets[g + 1])
         ind_own[r0:r1] = ind[r0:r1, g * W.N:(g + 1) * W.N]
     assert gate_independent(y, ind_own) is None
-    # AUTO takes the tcgen05 form above 96 mean rows per expert slot
+    # AUTO takes the tcgen05 form from 32 mean rows per expert slot on
     M = rows_x.shape[0]
-    if -(-M // min(W.G, M)) > 96:
+    if -(-M // min(W.G, M)) >= 32:
         assert np.array_equal(_run_grouped(W, rows_x, offsets)[-1], y)
 
 
