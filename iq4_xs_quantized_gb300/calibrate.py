@@ -32,7 +32,9 @@ import sys
 import numpy as np
 
 TABLE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "dispatch_table.json")
-SHAPES = ((4096, 4096), (5120, 5120), (12288, 5120), (5120, 17408), (34816, 5120))
+# Crossover shapes, one per weight-size class (classes are keyed by N*K
+# alone, so no two shapes share a weight count).
+SHAPES = ((1024, 5120), (4096, 4096), (5120, 5120), (6144, 5120), (12288, 5120), (5120, 17408), (34816, 5120))
 MS = tuple(range(1, 17)) + (20, 24, 28, 32, 40, 48, 64)
 DP4A_MS = tuple(range(1, 17))  # dp4a is timed up to here (its cost grows with M)
 # Upper threshold: the tcgen05 route (quantize + matmul) against dequantize
