@@ -77,8 +77,10 @@ def test_linear_matches_two_calls_and_oracle(M):
 @pytest.mark.parametrize("M,N,K", [(1, 5120, 5120), (2, 12288, 5120), (3, 300, 1536),
                                    (4, 1024, 17408), (4, 256, 25600), (1, 34816, 5120)])
 def test_linear_small_m_bitwise_and_workspace_q8(M, N, K):
-    """CUDA-core path across its launch shapes (two, three, four CTAs per
-    SM), a ragged N and a long K."""
+    """The dispatcher's small-M path (the CUDA-core kernel across its launch
+    shapes, or the warp-MMA kernel where the calibration measured it
+    faster), a ragged N and a long K: bitwise the two separate calls, and
+    the workspace holds the Q8_1 arrays."""
     rng = np.random.default_rng([51, M, N, K])
     w = synth.iq4xs_weights(rng, N, K, 1e-3)
     x = synth.activations(rng, M, K, outlier_frac=0.01)
@@ -91,7 +93,9 @@ def test_linear_small_m_bitwise_and_workspace_q8(M, N, K):
     yl = y.cpu().numpy()
     assert gate_written(yl) is None
     qs, ds = quantize_gpu(x)
-    assert np.array_equal(yl, matmul_gpu(wd, N, K, qs, ds, M, "dp4a"))
+    path = NAMES[B.iq4xs_select_path(M, N, K)]
+    assert path in ("dp4a", "mma"), path
+    assert np.array_equal(yl, matmul_gpu(wd, N, K, qs, ds, M, path))
     qs_o, d_o, s_o = oracle_q8(x)
     wsh = ws.cpu().numpy()
     assert np.array_equal(wsh[:M * K].view(np.int8).reshape(M, K), qs_o)
