@@ -449,12 +449,16 @@ int iq4xs_test_bounds_margin(int64_t bytes);
 
 /*
  * Test hook for the bounded waits (no counterpart on the source pages): the
- * next tensor-core matmul launched after this call (on any thread) leaves W
- * stage `stage` (0-based, in units of 512 weights of each CTA's K range) of
- * every CTA unissued, so that the decoders' wait for it runs out after its
- * 2 s limit (the other roles' waits, longer, end on the abort it raises).  That call's output is then undefined, every CTA still drains
- * its copies and frees its tensor memory, and iq4xs_last_device_error
- * reports IQ4XS_ERR_TIMEOUT with code 0x101.  -1 disarms.  Host only.
+ * next tensor-core matmul launched after this call (on any thread; tcgen05
+ * or warp MMA, dense or grouped) leaves W stage `stage` of every CTA
+ * unissued (0-based: in units of 512 weights of each CTA's K range; in the
+ * persistent grouped warp-MMA form, counted over the CTA's items one after
+ * the other), so that the consumers' wait for it runs out after its 2 s
+ * limit (the other roles' waits, longer, end on the abort it raises).  That
+ * call's output is then undefined, every CTA still drains its copies (and,
+ * on tcgen05, frees its tensor memory), and iq4xs_last_device_error
+ * reports IQ4XS_ERR_TIMEOUT with code 0x101 (tcgen05) or 0x10B (warp MMA).
+ * -1 disarms.  Host only.
  */
 int iq4xs_test_skip_w_stage(int64_t stage);
 

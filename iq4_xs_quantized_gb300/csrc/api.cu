@@ -209,7 +209,8 @@ int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (path == IQ4XS_PATH_MMA)
         return from_cuda(
-            launch_matmul_mma(w, wtype, N, K, qs, ds, M, y, ldy, st->encode, st->err, st->num_sms, s));
+            launch_matmul_mma(w, wtype, N, K, qs, ds, M, y, ldy, st->encode, st->err, st->num_sms,
+                              g_skip_w_stage.exchange(-1), s));
     if (path == IQ4XS_PATH_TC)
         return from_cuda(launch_matmul_tc(w, wtype, N, K, qs, ds, nullptr, M, y, ldy, st->encode,
                                           st->err, st->num_sms, g_skip_w_stage.exchange(-1), s));
@@ -332,7 +333,8 @@ int iq4xs_matmul_grouped_path(const void* w, int64_t expert_stride, int64_t G, i
                                                   ldy, st->encode, st->err, s));
     if (path == IQ4XS_PATH_MMA)
         return from_cuda(launch_matmul_mma_grouped(w, expert_stride, G, N, K, qs, ds, row_offsets, total_rows,
-                                                   y, ldy, st->encode, st->err, st->num_sms, s));
+                                                   y, ldy, st->encode, st->err, st->num_sms,
+                                                   g_skip_w_stage.exchange(-1), s));
     return from_cuda(launch_matmul_dp4a_grouped(w, expert_stride, G, N, K, qs, ds, row_offsets,
                                                 total_rows, y, ldy, st->err, s));
 }

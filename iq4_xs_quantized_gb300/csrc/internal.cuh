@@ -1040,7 +1040,7 @@ int mma_tile_rows(int64_t M);
 cudaError_t launch_matmul_mma_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
                                       const int8_t* qs, const void* ds, const int32_t* row_offsets,
                                       int64_t total_rows, float* y, int64_t ldy, void* encode, int* err,
-                                      int num_sms, cudaStream_t stream);
+                                      int num_sms, int skip_w_stage, cudaStream_t stream);
 // Grouped (mixture-of-experts) matmul on the tcgen05 kernel (Q8_1 form,
 // IQ4_XS, K % 512 == 0): activation tiles of tc_mtile(mean rows per expert
 // slot) rows, one CTA per (row tile, expert tile), no K split.
@@ -1061,7 +1061,7 @@ void mma_launch_config(int64_t M, int64_t N, int64_t K, int num_sms, int* rows, 
 int mma_set_launch_table(const int64_t* entries, int count);
 cudaError_t launch_matmul_mma(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs, const void* ds,
                               int64_t M, float* y, int64_t ldy, void* encode, int* err, int num_sms,
-                              cudaStream_t stream);
+                              int skip_w_stage, cudaStream_t stream);
 cudaError_t launch_matmul_tc(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,
                              const void* ds, const void* tc_operand, int64_t M, float* y,
                              int64_t ldy, void* encode, int* err, int num_sms, int skip_w_stage,

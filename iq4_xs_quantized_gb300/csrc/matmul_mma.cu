@@ -20,7 +20,7 @@ template <int NT, int T>
 cudaError_t launch_grouped_nt(const void* w, int64_t expert_stride, int G, int64_t row_bytes, EncodeTiledFn enc,
                               const CUtensorMap& tq, const __half* ds, const int32_t* row_offsets, int64_t rows,
                               int slots, int N, int K, float* y, int64_t ldy, int* err, int num_sms,
-                              cudaStream_t stream) {
+                              int skip_w_stage, cudaStream_t stream) {
     using C = MmaCfg<NT, T, 1, false, true>;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -49,7 +49,7 @@ cudaError_t launch_grouped_nt(const void* w, int64_t expert_stride, int G, int64
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, matmul_mma_kernel<NT, T, 1, true>, tw, tq, ds, rows, N, K, y, ldy, err,
-                              row_offsets, G, 0);
+                              row_offsets, G, 0, skip_w_stage);
 }
 
 // Test override of the launch configuration (0 = the model's choice).
@@ -170,7 +170,7 @@ void mma_force_config(int rows_per_cta, int k_splits, int ctas_per_sm) {
 cudaError_t launch_matmul_mma_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
                                       const int8_t* qs, const void* ds, const int32_t* row_offsets,
                                       int64_t total_rows, float* y, int64_t ldy, void* encode, int* err,
-                                      int num_sms, cudaStream_t stream) {
+                                      int num_sms, int skip_w_stage, cudaStream_t stream) {
     const EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(encode);
     const int64_t row_bytes = wt_row_bytes(kWtIQ4XS, K);
     // at most min(G, rows) experts have rows; the activation tile from the
@@ -191,12 +191,12 @@ cudaError_t launch_matmul_mma_grouped(const void* w, int64_t expert_stride, int6
     case 8 * nt:                                                                                               \
         if (rows_cta == 128)                                                                                   \
             return launch_grouped_nt<nt, 4>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets,        \
-                                            total_rows, slots, Ni, Ki, y, ldy, err, num_sms, stream);          \
+                                            total_rows, slots, Ni, Ki, y, ldy, err, num_sms, skip_w_stage, stream);          \
         if (rows_cta == 64)                                                                                    \
             return launch_grouped_nt<nt, 2>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets,        \
-                                            total_rows, slots, Ni, Ki, y, ldy, err, num_sms, stream);          \
+                                            total_rows, slots, Ni, Ki, y, ldy, err, num_sms, skip_w_stage, stream);          \
         return launch_grouped_nt<nt, 1>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets, total_rows, \
-                                        slots, Ni, Ki, y, ldy, err, num_sms, stream);
+                                        slots, Ni, Ki, y, ldy, err, num_sms, skip_w_stage, stream);
     switch (mt) {
         IQ4XS_MMA_G(1)
         IQ4XS_MMA_G(2)
@@ -204,9 +204,9 @@ cudaError_t launch_matmul_mma_grouped(const void* w, int64_t expert_stride, int6
         case 32:  // 64-row tiles at most: the partial tiles of 128 would leave one stage
             if (rows_cta >= 64)
                 return launch_grouped_nt<4, 2>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets,
-                                               total_rows, slots, Ni, Ki, y, ldy, err, num_sms, stream);
+                                               total_rows, slots, Ni, Ki, y, ldy, err, num_sms, skip_w_stage, stream);
             return launch_grouped_nt<4, 1>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets, total_rows,
-                                           slots, Ni, Ki, y, ldy, err, num_sms, stream);
+                                           slots, Ni, Ki, y, ldy, err, num_sms, skip_w_stage, stream);
         default: return cudaErrorInvalidValue;
     }
 #undef IQ4XS_MMA_G
@@ -219,8 +219,9 @@ int mma_tile_rows(int64_t M) {
 
 cudaError_t launch_matmul_mma(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs, const void* ds,
                               int64_t M, float* y, int64_t ldy, void* encode, int* err, int num_sms,
-                              cudaStream_t stream) {
-    if (wt != kWtIQ4XS) return launch_matmul_mma_b18(wt, w, N, K, qs, ds, M, y, ldy, encode, err, num_sms, stream);
+                              int skip_w_stage, cudaStream_t stream) {
+    if (wt != kWtIQ4XS)
+        return launch_matmul_mma_b18(wt, w, N, K, qs, ds, M, y, ldy, encode, err, num_sms, skip_w_stage, stream);
     const EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(encode);
     const int64_t row_bytes = wt_row_bytes(kWtIQ4XS, K);
     const int mt = mma_tile_rows(M);
@@ -230,7 +231,8 @@ cudaError_t launch_matmul_mma(const void* w, int wt, int64_t N, int64_t K, const
     const __half* dsh = reinterpret_cast<const __half*>(ds);
     const int Ni = (int)N, Ki = (int)K;
 #define IQ4XS_MMA_BEST(nt) \
-    launch_best<nt, false>(MmaConfigs<nt>::list, w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, kWtIQ4XS, num_sms, stream)
+    launch_best<nt, false>(MmaConfigs<nt>::list, w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, kWtIQ4XS, \
+                           skip_w_stage, num_sms, stream)
     switch (mt) {
         case 8: return IQ4XS_MMA_BEST(1);
         case 16: return IQ4XS_MMA_BEST(2);

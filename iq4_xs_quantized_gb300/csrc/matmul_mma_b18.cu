@@ -49,7 +49,7 @@ struct MmaConfigsB18<4> {
 
 cudaError_t launch_matmul_mma_b18(int wt, const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds,
                                   int64_t M, float* y, int64_t ldy, void* encode, int* err, int num_sms,
-                                  cudaStream_t stream) {
+                                  int skip_w_stage, cudaStream_t stream) {
     if (wt != kWtQ4_0 && wt != kWtIQ4NL) return cudaErrorInvalidValue;
     const EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(encode);
     const int64_t row_bytes = wt_row_bytes(wt, K);
@@ -60,7 +60,8 @@ cudaError_t launch_matmul_mma_b18(int wt, const void* w, int64_t N, int64_t K, c
     const __half* dsh = reinterpret_cast<const __half*>(ds);
     const int Ni = (int)N, Ki = (int)K;
 #define IQ4XS_MMA_BEST(nt) \
-    launch_best<nt, true>(MmaConfigsB18<nt>::list, w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, wt, num_sms, stream)
+    launch_best<nt, true>(MmaConfigsB18<nt>::list, w, row_bytes, enc, tq, dsh, M, Ni, Ki, y, ldy, err, wt, \
+                          skip_w_stage, num_sms, stream)
     switch (mt) {
         case 8: return IQ4XS_MMA_BEST(1);
         case 16: return IQ4XS_MMA_BEST(2);

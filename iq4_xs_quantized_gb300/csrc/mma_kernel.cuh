@@ -69,7 +69,7 @@ bool mma_measured_launch(int64_t N, int64_t K, int mt, int* rows, int* splits, i
 // Q4_0 / IQ4_NL weights (wt) on the warp-MMA path (matmul_mma_b18.cu).
 cudaError_t launch_matmul_mma_b18(int wt, const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds,
                                   int64_t M, float* y, int64_t ldy, void* encode, int* err, int num_sms,
-                                  cudaStream_t stream);
+                                  int skip_w_stage, cudaStream_t stream);
 
 namespace {
 
@@ -195,7 +195,7 @@ template <int NT, int T, int kOcc, bool kGrouped, bool kB18 = false>
 __global__ void __launch_bounds__(kMmaThreads, kOcc)
     matmul_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_q,
                       const __half* __restrict__ ds, int64_t M, int N, int K, float* __restrict__ y, int64_t ldy,
-                      int* err, const int32_t* __restrict__ row_offsets, int G, int wt) {
+                      int* err, const int32_t* __restrict__ row_offsets, int G, int wt, int skip_stage) {
     using C = MmaCfg<NT, T, kOcc, kB18, kGrouped>;
     static_assert(!(kGrouped && kB18), "the grouped form takes IQ4_XS");
     constexpr int kTMax = T, kMt = C::kMt, kSPW = C::kSPW, kRG = C::kRG, R = C::kR, NS = C::kNS;
@@ -228,8 +228,10 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
 
     // Stage gs of the current item: K pair p0 + gs % nst (grouped: items of
     // nst stages one after the other), weight rows from n0w, activation rows
-    // from rq, expert e.
+    // from rq, expert e.  Stage skip_stage (a test of the bounded waits; -1
+    // in every ordinary call) is not issued: its barrier never completes.
     auto load_w = [&](int gs, int n0w, int e) {
+        if (gs == skip_stage) return;
         const int slot = gs % NS;
         uint8_t* dst = smem + kOffRingMma + slot * stage_b;
         const int x = (p0 + gs % nst) * (C::kRowB / 4);
@@ -250,6 +252,7 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
         }
     };
     auto load_q = [&](int gs, int64_t rq64) {
+        if (gs == skip_stage) return;
         const int slot = gs % NS;
         const int rq = (int)rq64;
 #pragma unroll
@@ -391,7 +394,8 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
             // stopped by an abort: no copy may land after the CTA exits.
             const int first = issued - NS + (ended ? 1 : 0);
             for (int gs = (first > 0 ? first : 0); gs < issued; ++gs)
-                mbar_wait(&full[gs % NS], (gs / NS) & 1, &g_never_abort_mma, err, kDevErrTimeoutDrain);
+                if (gs != skip_stage)
+                    mbar_wait(&full[gs % NS], (gs / NS) & 1, &g_never_abort_mma, err, kDevErrTimeoutDrain);
         }
         __syncwarp();
     } else {
@@ -761,7 +765,8 @@ int mma_max_clusters(int dev, int s, int num_sms) {
 
 template <int NT, int T, int kOcc, bool kB18 = false>
 cudaError_t launch_nt(const void* w, int64_t row_bytes, EncodeTiledFn enc, const CUtensorMap& tq, const __half* ds,
-                      int64_t M, int N, int K, int S, float* y, int64_t ldy, int* err, int wt, cudaStream_t stream) {
+                      int64_t M, int N, int K, int S, float* y, int64_t ldy, int* err, int wt, int skip_stage,
+                      cudaStream_t stream) {
     using C = MmaCfg<NT, T, kOcc, kB18>;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -798,7 +803,7 @@ cudaError_t launch_nt(const void* w, int64_t row_bytes, EncodeTiledFn enc, const
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, matmul_mma_kernel<NT, T, kOcc, false, kB18>, tw, tq, ds, M, N, K, y, ldy, err,
-                              static_cast<const int32_t*>(nullptr), 0, wt);
+                              static_cast<const int32_t*>(nullptr), 0, wt, skip_stage);
 }
 
 // One launch configuration: R weight rows per CTA and CTAs per SM, with its
@@ -807,7 +812,7 @@ struct MmaConfig {
     int R, occ;
     int (*max_clusters)(int dev, int s, int num_sms);
     cudaError_t (*launch)(const void*, int64_t, EncodeTiledFn, const CUtensorMap&, const __half*, int64_t, int,
-                          int, int, float*, int64_t, int*, int, cudaStream_t);
+                          int, int, float*, int64_t, int*, int, int, cudaStream_t);
 };
 template <int NT, int T, int kOcc, bool kB18 = false>
 constexpr MmaConfig cfg_of() {
@@ -896,10 +901,10 @@ void choose_config(const MmaConfig* list, int count, int64_t M, int N, int K, in
 template <int NT, bool kB18, int kCount>
 cudaError_t launch_best(const MmaConfig (&list)[kCount], const void* w, int64_t row_bytes, EncodeTiledFn enc,
                         const CUtensorMap& tq, const __half* ds, int64_t M, int N, int K, float* y, int64_t ldy,
-                        int* err, int wt, int num_sms, cudaStream_t stream) {
+                        int* err, int wt, int skip_stage, int num_sms, cudaStream_t stream) {
     int ci = 0, s = 1;
     choose_config<NT, kB18>(list, kCount, M, N, K, num_sms, &ci, &s);
-    return list[ci].launch(w, row_bytes, enc, tq, ds, M, N, K, s, y, ldy, err, wt, stream);
+    return list[ci].launch(w, row_bytes, enc, tq, ds, M, N, K, s, y, ldy, err, wt, skip_stage, stream);
 }
 
 // Q8_1 codes: one box = mt rows x 128 codes, 128-byte swizzle; rows past
