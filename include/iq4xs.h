@@ -226,9 +226,9 @@ int iq4xs_matmul_wt(const void* w, int wtype, int64_t N, int64_t K, const int8_t
  *                 by the kernel after the preceding grid completes (so it may
  *                 come from a routing kernel).
  *   total_rows    the number of rows, 1..32768 (row_offsets[G] <= total_rows); at most
- *                 min(G, total_rows) experts have rows, and the launch has
- *                 that many expert slots, each taking the next non-empty
- *                 expert, so empty experts cost nothing.
+ *                 min(G, total_rows) experts have rows, and the launch is
+ *                 sized for that many (the kernels find the non-empty
+ *                 experts themselves), so empty experts cost nothing.
  *   y             fp32 [rows][ldy]; the rows of every expert are written.
  * Path: the CUDA-core (DP4A) kernel, each expert computed with the batch
  * width its own row count selects, so the result per expert is
