@@ -261,6 +261,19 @@ int iq4xs_matmul_grouped_path(const void* w, int64_t expert_stride, int64_t G, i
                               int64_t total_rows, float* y, int64_t ldy, int path, int64_t stream);
 
 /*
+ * iq4xs_matmul_grouped_path for experts in weight format wtype (an
+ * iq4xs_wtype: every expert's N x K matrix in that format, expert_stride >=
+ * iq4xs_weight_bytes(wtype, N, K)).  Q4_0 / IQ4_NL experts run on the DP4A
+ * and warp-MMA forms (AUTO takes the warp-MMA form wherever it would take
+ * the tcgen05 one for IQ4_XS; an explicit IQ4XS_PATH_TC returns
+ * IQ4XS_ERR_SHAPE); each expert's result is that of iq4xs_matmul_wt on the
+ * same path over its rows.  IQ4XS_ERR_ARG for an unknown format.
+ */
+int iq4xs_matmul_grouped_wt(const void* w, int wtype, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
+                            const int8_t* qs, const void* ds, const int32_t* row_offsets, int64_t total_rows,
+                            float* y, int64_t ldy, int path, int64_t stream);
+
+/*
  * The projection as one call: y = Q8_1(x) . W^T from fp32 activations
  * (engine page, kernel table at M=64: the projection op quantizes its
  * activations with quantize_q8_1 and runs the batched matmul).  Launches the

@@ -68,6 +68,7 @@ def load(path: str | None = None):
         lib.iq4xs_weight_bytes.restype = i64
         lib.iq4xs_matmul_grouped.argtypes = [vp, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, i64]
         lib.iq4xs_matmul_grouped_path.argtypes = [vp, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, ci, i64]
+        lib.iq4xs_matmul_grouped_wt.argtypes = [vp, ci, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, ci, i64]
         lib.iq4xs_linear.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, i64]
         lib.iq4xs_linear_workspace_bytes.argtypes = [i64, i64, i64]
         lib.iq4xs_linear_workspace_bytes.restype = i64
@@ -94,6 +95,7 @@ def load(path: str | None = None):
         lib.iq4xs_status_string.argtypes = [ci]
         lib.iq4xs_status_string.restype = ctypes.c_char_p
         for name in ("iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_matmul_grouped", "iq4xs_matmul_grouped_path",
+                     "iq4xs_matmul_grouped_wt",
                      "iq4xs_dequantize", "iq4xs_linear", "iq4xs_matmul_wt", "iq4xs_dequantize_wt",
                      "iq4xs_select_path", "iq4xs_set_crossover", "iq4xs_set_baseline_threshold",
                      "iq4xs_set_crossover_classes", "iq4xs_test_skip_w_stage",
@@ -281,20 +283,20 @@ def iq4xs_linear_static_max_bytes() -> int:
 
 
 def iq4xs_matmul_grouped(w, expert_stride: int, G: int, N: int, K: int, qs, ds, row_offsets, y,
-                         stream=None, path=PATH_AUTO) -> None:
+                         stream=None, path=PATH_AUTO, wtype=WTYPE_IQ4_XS) -> None:
     """Mixture-of-experts matmul in one launch: expert g (W at byte
-    g * expert_stride of w) over the Q8_1 rows [row_offsets[g],
-    row_offsets[g+1]) (row_offsets: int32 device tensor [G+1]); y holds
-    every row (its row count bounds the number of non-empty experts).
-    path: AUTO, DP4A, MMA or TC (iq4xs_matmul_grouped_path)."""
+    g * expert_stride of w, format ``wtype``) over the Q8_1 rows
+    [row_offsets[g], row_offsets[g+1]) (row_offsets: int32 device tensor
+    [G+1]); y holds every row (its row count bounds the number of non-empty
+    experts).  path: AUTO, DP4A, MMA or TC (iq4xs_matmul_grouped_wt)."""
     if row_offsets.dtype != torch.int32:
         raise TypeError("row_offsets must be int32")
     if isinstance(path, str):
         path = PATHS[path]
-    rc = load().iq4xs_matmul_grouped_path(_ptr(w), int(expert_stride), G, N, K, _ptr(qs), _ptr(ds),
-                                          _ptr(row_offsets), y.shape[0], _ptr(y), y.stride(0), int(path),
-                                          _stream(stream))
-    _check("iq4xs_matmul_grouped_path", rc)
+    rc = load().iq4xs_matmul_grouped_wt(_ptr(w), _wtype(wtype), int(expert_stride), G, N, K, _ptr(qs), _ptr(ds),
+                                        _ptr(row_offsets), y.shape[0], _ptr(y), y.stride(0), int(path),
+                                        _stream(stream))
+    _check("iq4xs_matmul_grouped_wt", rc)
 
 
 def iq4xs_dequantize(w, N: int, K: int, out, stream=None) -> None:

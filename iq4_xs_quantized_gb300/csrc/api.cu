@@ -296,14 +296,22 @@ int iq4xs_matmul_grouped(const void* w, int64_t expert_stride, int64_t G, int64_
 int iq4xs_matmul_grouped_path(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
                               const int8_t* qs, const void* ds, const int32_t* row_offsets,
                               int64_t total_rows, float* y, int64_t ldy, int path, int64_t stream) {
+    return iq4xs_matmul_grouped_wt(w, IQ4XS_WTYPE_IQ4_XS, expert_stride, G, N, K, qs, ds, row_offsets, total_rows,
+                                   y, ldy, path, stream);
+}
+
+int iq4xs_matmul_grouped_wt(const void* w, int wtype, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
+                            const int8_t* qs, const void* ds, const int32_t* row_offsets, int64_t total_rows,
+                            float* y, int64_t ldy, int path, int64_t stream) {
     if (!w || !qs || !ds || !row_offsets || !y) return IQ4XS_ERR_ARG;
+    if (wtype < IQ4XS_WTYPE_IQ4_XS || wtype > IQ4XS_WTYPE_IQ4_NL) return IQ4XS_ERR_ARG;
     if (path != IQ4XS_PATH_AUTO && path != IQ4XS_PATH_DP4A && path != IQ4XS_PATH_MMA && path != IQ4XS_PATH_TC)
         return IQ4XS_ERR_ARG;
     if (G < 1 || G > 65535 || N < 1 || N > (1 << 30) || K <= 0 || K % kQK || K > (1 << 30))
         return IQ4XS_ERR_SHAPE;
     if (ldy < N || total_rows < 1) return IQ4XS_ERR_ARG;
     if (total_rows > kMaxM) return IQ4XS_ERR_SHAPE;  // the rows one quantize call takes
-    if (expert_stride < N * (K / kQK) * kBlockBytes || expert_stride % 16) return IQ4XS_ERR_ARG;
+    if (expert_stride < N * wt_row_bytes(wtype, K) || expert_stride % 16) return IQ4XS_ERR_ARG;
     if (!aligned(w, 16) || !aligned(qs, 16) || !aligned(ds, 4) || !aligned(row_offsets, 4) ||
         !aligned(y, 4))
         return IQ4XS_ERR_ALIGN;
@@ -314,16 +322,18 @@ int iq4xs_matmul_grouped_path(const void* w, int64_t expert_stride, int64_t G, i
         // CUDA-core form is 6 % faster at 16 rows, 19 % slower at 24 and
         // 30 % at 64); the tcgen05 form from 32 mean rows per expert slot on
         // (the same layer: 15 % slower at 24, 2 % faster at 32, 8 % at 64,
-        // 24 % at 256).
+        // 24 % at 256), for IQ4_XS weights (the other formats stay on the
+        // warp-MMA form).
         const int64_t slots = G < total_rows ? G : total_rows;
         const int64_t mean = (total_rows + slots - 1) / slots;
         const int64_t mma_min = G < kGroupedMmaMinRows ? G : kGroupedMmaMinRows;
         if (K % kPairK == 0 && (total_rows >= mma_min || mean > crossover_for(N, K)))
-            path = mean >= kGroupedTcMinRows ? IQ4XS_PATH_TC : IQ4XS_PATH_MMA;
+            path = (mean >= kGroupedTcMinRows && wtype == IQ4XS_WTYPE_IQ4_XS) ? IQ4XS_PATH_TC : IQ4XS_PATH_MMA;
         else
             path = IQ4XS_PATH_DP4A;
     }
     if ((path == IQ4XS_PATH_MMA || path == IQ4XS_PATH_TC) && K % kPairK) return IQ4XS_ERR_SHAPE;
+    if (path == IQ4XS_PATH_TC && wtype != IQ4XS_WTYPE_IQ4_XS) return IQ4XS_ERR_SHAPE;
     DevState* st;
     int rc = device_state(&st);
     if (rc) return rc;
@@ -332,10 +342,10 @@ int iq4xs_matmul_grouped_path(const void* w, int64_t expert_stride, int64_t G, i
         return from_cuda(launch_matmul_tc_grouped(w, expert_stride, G, N, K, qs, ds, row_offsets, total_rows, y,
                                                   ldy, st->encode, st->err, s));
     if (path == IQ4XS_PATH_MMA)
-        return from_cuda(launch_matmul_mma_grouped(w, expert_stride, G, N, K, qs, ds, row_offsets, total_rows,
-                                                   y, ldy, st->encode, st->err, st->num_sms,
+        return from_cuda(launch_matmul_mma_grouped(w, wtype, expert_stride, G, N, K, qs, ds, row_offsets,
+                                                   total_rows, y, ldy, st->encode, st->err, st->num_sms,
                                                    g_skip_w_stage.exchange(-1), s));
-    return from_cuda(launch_matmul_dp4a_grouped(w, expert_stride, G, N, K, qs, ds, row_offsets,
+    return from_cuda(launch_matmul_dp4a_grouped(w, wtype, expert_stride, G, N, K, qs, ds, row_offsets,
                                                 total_rows, y, ldy, st->err, s));
 }
 

@@ -1017,9 +1017,10 @@ cudaError_t launch_dequantize(const void* w, int wt, int64_t N, int64_t K, void*
 cudaError_t launch_matmul_dp4a(const void* w, int wt, int64_t N, int64_t K, const int8_t* qs,
                                const void* ds, int64_t M, float* y, int64_t ldy, int* err,
                                int num_sms, cudaStream_t stream);
-// G experts in one launch: expert g has W at w + g * expert_stride and the
-// Q8_1 / output rows [row_offsets[g], row_offsets[g+1]) (device array).
-cudaError_t launch_matmul_dp4a_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N,
+// G experts in one launch: expert g has W (format wt) at w + g *
+// expert_stride and the Q8_1 / output rows [row_offsets[g], row_offsets[g+1])
+// (device array).
+cudaError_t launch_matmul_dp4a_grouped(const void* w, int wt, int64_t expert_stride, int64_t G, int64_t N,
                                        int64_t K, const int8_t* qs, const void* ds,
                                        const int32_t* row_offsets, int64_t total_rows, float* y,
                                        int64_t ldy, int* err, cudaStream_t stream);
@@ -1034,11 +1035,11 @@ bool pdl_enabled();
 // mma_tile_rows(M) rows (8, 16, 24 or 32); K % 512 == 0; qs 16-byte aligned
 // (staged by TMA), ds read directly.
 int mma_tile_rows(int64_t M);
-// The grouped (mixture-of-experts) form of the warp-MMA path: expert g's W at
-// w + g * expert_stride (a multiple of 16), its rows [row_offsets[g],
-// row_offsets[g+1]) of qs / ds / y; K % 512 == 0.
-cudaError_t launch_matmul_mma_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
-                                      const int8_t* qs, const void* ds, const int32_t* row_offsets,
+// The grouped (mixture-of-experts) form of the warp-MMA path: expert g's W
+// (format wt) at w + g * expert_stride (a multiple of 16), its rows
+// [row_offsets[g], row_offsets[g+1]) of qs / ds / y; K % 512 == 0.
+cudaError_t launch_matmul_mma_grouped(const void* w, int wt, int64_t expert_stride, int64_t G, int64_t N,
+                                      int64_t K, const int8_t* qs, const void* ds, const int32_t* row_offsets,
                                       int64_t total_rows, float* y, int64_t ldy, void* encode, int* err,
                                       int num_sms, int skip_w_stage, cudaStream_t stream);
 // Grouped (mixture-of-experts) matmul on the tcgen05 kernel (Q8_1 form,

@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kDp4aThreads, ctas_per_sm<MC, S>())
 // shape that keeps the next wave streaming on these many-wave grids.  A row's
 // result does not depend on the batch width (each lane sums its sub-blocks
 // in the same order), so both forms give the same bits.
-template <bool kNarrow>
+template <bool kNarrow, int WT>
 __global__ void __launch_bounds__(kDp4aThreads, kNarrow ? 3 : 2)
     matmul_dp4a_grouped_kernel(const uint8_t* __restrict__ w, int64_t expert_stride, int64_t G,
                                int64_t N, int64_t K, const int8_t* __restrict__ qs,
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kDp4aThreads, kNarrow ? 3 : 2)
     qs += r0 * K;
     ds += r0 * (K / kSub);
     y += r0 * ldy;
-    constexpr int X = kWtIQ4XS;
+    constexpr int X = WT;
     if constexpr (kNarrow) {
         if (M == 1) dp4a_rows<1, X, iters_for<1, 1>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true, bc);
         else dp4a_rows<2, X, iters_for<2, 1>()>(w, N, K, qs, ds, M, y, ldy, n0, lane, true, bc);
@@ -299,21 +299,43 @@ cudaError_t launch_matmul_dp4a(const void* w, int wt, int64_t N, int64_t K, cons
     }
 }
 
-cudaError_t launch_matmul_dp4a_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N,
-                                       int64_t K, const int8_t* qs, const void* ds,
-                                       const int32_t* row_offsets, int64_t total_rows, float* y,
-                                       int64_t ldy, int* err, cudaStream_t stream) {
+namespace {
+
+template <int WT>
+cudaError_t launch_grouped_wt(const uint8_t* wb, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
+                              const int8_t* qs, const __half2* d2, const int32_t* row_offsets, int64_t total_rows,
+                              float* y, int64_t ldy, int* err, cudaStream_t stream) {
     // at most min(G, total rows) experts have rows
     const unsigned slots = (unsigned)(G < total_rows ? G : total_rows);
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = dp4a_config(N, slots, stream, attr);
+    if (total_rows <= 2 * (int64_t)slots)  // at most two rows per routed expert on average
+        return cudaLaunchKernelEx(&cfg, matmul_dp4a_grouped_kernel<true, WT>, wb, expert_stride, G, N, K, qs, d2,
+                                  row_offsets, total_rows, y, ldy, err);
+    return cudaLaunchKernelEx(&cfg, matmul_dp4a_grouped_kernel<false, WT>, wb, expert_stride, G, N, K, qs, d2,
+                              row_offsets, total_rows, y, ldy, err);
+}
+
+}  // namespace
+
+cudaError_t launch_matmul_dp4a_grouped(const void* w, int wt, int64_t expert_stride, int64_t G, int64_t N,
+                                       int64_t K, const int8_t* qs, const void* ds,
+                                       const int32_t* row_offsets, int64_t total_rows, float* y,
+                                       int64_t ldy, int* err, cudaStream_t stream) {
     const uint8_t* wb = reinterpret_cast<const uint8_t*>(w);
     const __half2* d2 = reinterpret_cast<const __half2*>(ds);
-    if (total_rows <= 2 * (int64_t)slots)  // at most two rows per routed expert on average
-        return cudaLaunchKernelEx(&cfg, matmul_dp4a_grouped_kernel<true>, wb, expert_stride, G, N, K,
-                                  qs, d2, row_offsets, total_rows, y, ldy, err);
-    return cudaLaunchKernelEx(&cfg, matmul_dp4a_grouped_kernel<false>, wb, expert_stride, G, N, K, qs,
-                              d2, row_offsets, total_rows, y, ldy, err);
+    switch (wt) {
+        case kWtIQ4XS:
+            return launch_grouped_wt<kWtIQ4XS>(wb, expert_stride, G, N, K, qs, d2, row_offsets, total_rows, y, ldy,
+                                               err, stream);
+        case kWtQ4_0:
+            return launch_grouped_wt<kWtQ4_0>(wb, expert_stride, G, N, K, qs, d2, row_offsets, total_rows, y, ldy,
+                                              err, stream);
+        case kWtIQ4NL:
+            return launch_grouped_wt<kWtIQ4NL>(wb, expert_stride, G, N, K, qs, d2, row_offsets, total_rows, y, ldy,
+                                               err, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace iq4xs

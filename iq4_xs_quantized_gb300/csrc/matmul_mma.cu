@@ -1,8 +1,8 @@
 // matmul_mma.cu -- IQ4_XS launches of the warp-level MMA matmul (the kernel
 // and its launch model are in mma_kernel.cuh): the launch configurations
 // per activation-tile width, the measured launch table and the forced test
-// configuration, the grouped (mixture-of-experts) form, and the path's
-// entry points (other weight formats go on to matmul_mma_b18.cu).
+// configuration, and the path's entry points, dense and grouped (other
+// weight formats go on to matmul_mma_b18.cu).
 #include <atomic>
 #include <mutex>
 
@@ -10,47 +10,6 @@
 
 namespace iq4xs {
 namespace {
-
-// Grouped (mixture-of-experts) launch of the persistent <NT, T> kernel: W
-// of expert g through a 3D tensor map (row words x rows x experts,
-// expert_stride bytes apart); one CTA per SM, or fewer when the layer has
-// fewer work items (at most row tiles x (activation tiles of all rows +
-// experts with rows)).
-template <int NT, int T>
-cudaError_t launch_grouped_nt(const void* w, int64_t expert_stride, int G, int64_t row_bytes, EncodeTiledFn enc,
-                              const CUtensorMap& tq, const __half* ds, const int32_t* row_offsets, int64_t rows,
-                              int slots, int N, int K, float* y, int64_t ldy, int* err, int num_sms,
-                              int skip_w_stage, cudaStream_t stream) {
-    using C = MmaCfg<NT, T, 1, false, true>;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const cudaError_t ea = mma_smem_attr<NT, T, 1, true>(dev);
-    if (ea != cudaSuccess) return ea;
-    CUtensorMap tw;
-    {
-        const cuuint64_t gdim[3] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)N, (cuuint64_t)G};
-        const cuuint64_t gstride[2] = {(cuuint64_t)row_bytes, (cuuint64_t)expert_stride};
-        const cuuint32_t box[3] = {(cuuint32_t)(kPairBytes / 4), (cuuint32_t)C::kR, 1};
-        const cuuint32_t estride[3] = {1, 1, 1};
-        if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(w), gdim, gstride, box, estride,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    cudaLaunchConfig_t cfg = {};
-    const int64_t items = (N + C::kR - 1) / C::kR * ((rows + C::kMt - 1) / C::kMt + slots);
-    cfg.gridDim = dim3((unsigned)(items < num_sms ? items : num_sms), 1, 1);
-    cfg.blockDim = dim3(kMmaThreads);
-    cfg.dynamicSmemBytes = C::kSmem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, matmul_mma_kernel<NT, T, 1, true>, tw, tq, ds, rows, N, K, y, ldy, err,
-                              row_offsets, G, 0, skip_w_stage);
-}
 
 // Test override of the launch configuration (0 = the model's choice).
 std::atomic<int> g_force_rows{0}, g_force_s{0}, g_force_occ{0};
@@ -167,49 +126,15 @@ void mma_force_config(int rows_per_cta, int k_splits, int ctas_per_sm) {
     g_force_occ.store(ctas_per_sm);
 }
 
-cudaError_t launch_matmul_mma_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
-                                      const int8_t* qs, const void* ds, const int32_t* row_offsets,
+cudaError_t launch_matmul_mma_grouped(const void* w, int wt, int64_t expert_stride, int64_t G, int64_t N,
+                                      int64_t K, const int8_t* qs, const void* ds, const int32_t* row_offsets,
                                       int64_t total_rows, float* y, int64_t ldy, void* encode, int* err,
                                       int num_sms, int skip_w_stage, cudaStream_t stream) {
-    const EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(encode);
-    const int64_t row_bytes = wt_row_bytes(kWtIQ4XS, K);
-    // at most min(G, rows) experts have rows; the activation tile from the
-    // mean rows per such expert (larger experts take several tiles)
-    const int slots = (int)(G < total_rows ? G : total_rows);
-    const int64_t mean = (total_rows + slots - 1) / slots;
-    const int mt = mma_tile_rows(mean);
-    CUtensorMap tq;
-    const cudaError_t eq = encode_q_map(enc, qs, K, total_rows, mt, &tq);
-    if (eq != cudaSuccess) return eq;
-    const __half* dsh = reinterpret_cast<const __half*>(ds);
-    // 128-row tiles, or 64 / 32 when the experts' row tiles alone do not
-    // give every SM a work item.
-    const int Ni = (int)N, Ki = (int)K, Gi = (int)G;
-    const int64_t ctas128 = (N + 127) / 128 * slots;
-    const int rows_cta = ctas128 >= num_sms ? 128 : ((N + 63) / 64 * slots >= num_sms ? 64 : 32);
-#define IQ4XS_MMA_G(nt)                                                                                         \
-    case 8 * nt:                                                                                               \
-        if (rows_cta == 128)                                                                                   \
-            return launch_grouped_nt<nt, 4>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets,        \
-                                            total_rows, slots, Ni, Ki, y, ldy, err, num_sms, skip_w_stage, stream);          \
-        if (rows_cta == 64)                                                                                    \
-            return launch_grouped_nt<nt, 2>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets,        \
-                                            total_rows, slots, Ni, Ki, y, ldy, err, num_sms, skip_w_stage, stream);          \
-        return launch_grouped_nt<nt, 1>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets, total_rows, \
-                                        slots, Ni, Ki, y, ldy, err, num_sms, skip_w_stage, stream);
-    switch (mt) {
-        IQ4XS_MMA_G(1)
-        IQ4XS_MMA_G(2)
-        IQ4XS_MMA_G(3)
-        case 32:  // 64-row tiles at most: the partial tiles of 128 would leave one stage
-            if (rows_cta >= 64)
-                return launch_grouped_nt<4, 2>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets,
-                                               total_rows, slots, Ni, Ki, y, ldy, err, num_sms, skip_w_stage, stream);
-            return launch_grouped_nt<4, 1>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets, total_rows,
-                                           slots, Ni, Ki, y, ldy, err, num_sms, skip_w_stage, stream);
-        default: return cudaErrorInvalidValue;
-    }
-#undef IQ4XS_MMA_G
+    if (wt != kWtIQ4XS)
+        return launch_matmul_mma_grouped_b18(wt, w, expert_stride, G, N, K, qs, ds, row_offsets, total_rows, y, ldy,
+                                             encode, err, num_sms, skip_w_stage, stream);
+    return launch_grouped<false>(wt, w, expert_stride, G, N, K, qs, ds, row_offsets, total_rows, y, ldy, encode,
+                                 err, num_sms, skip_w_stage, stream);
 }
 
 int mma_tile_rows(int64_t M) {

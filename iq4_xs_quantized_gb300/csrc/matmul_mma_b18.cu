@@ -1,5 +1,6 @@
 // matmul_mma_b18.cu -- Q4_0 and IQ4_NL weights (18-byte blocks of 32: fp16 d,
-// then 16 bytes of nibbles) on the warp-level MMA matmul of mma_kernel.cuh.
+// then 16 bytes of nibbles) on the warp-level MMA matmul of mma_kernel.cuh,
+// dense and grouped (mixture of experts).
 //
 // The formats' definitions are the same as on the CUDA-core and tcgen05
 // paths: a block's weight i is d * value[nibble i], value = nibble - 8 for
@@ -69,6 +70,15 @@ cudaError_t launch_matmul_mma_b18(int wt, const void* w, int64_t N, int64_t K, c
         default: return IQ4XS_MMA_BEST(4);
     }
 #undef IQ4XS_MMA_BEST
+}
+
+cudaError_t launch_matmul_mma_grouped_b18(int wt, const void* w, int64_t expert_stride, int64_t G, int64_t N,
+                                          int64_t K, const int8_t* qs, const void* ds, const int32_t* row_offsets,
+                                          int64_t total_rows, float* y, int64_t ldy, void* encode, int* err,
+                                          int num_sms, int skip_w_stage, cudaStream_t stream) {
+    if (wt != kWtQ4_0 && wt != kWtIQ4NL) return cudaErrorInvalidValue;
+    return launch_grouped<true>(wt, w, expert_stride, G, N, K, qs, ds, row_offsets, total_rows, y, ldy, encode,
+                                err, num_sms, skip_w_stage, stream);
 }
 
 }  // namespace iq4xs

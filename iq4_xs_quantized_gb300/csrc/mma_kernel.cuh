@@ -66,10 +66,15 @@ namespace iq4xs {
 // and activation-tile height, if the calibration installed one.
 void mma_forced_config(int* rows, int* splits, int* ctas_per_sm);
 bool mma_measured_launch(int64_t N, int64_t K, int mt, int* rows, int* splits, int* ctas_per_sm);
-// Q4_0 / IQ4_NL weights (wt) on the warp-MMA path (matmul_mma_b18.cu).
+// Q4_0 / IQ4_NL weights (wt) on the warp-MMA path, dense and grouped
+// (matmul_mma_b18.cu).
 cudaError_t launch_matmul_mma_b18(int wt, const void* w, int64_t N, int64_t K, const int8_t* qs, const void* ds,
                                   int64_t M, float* y, int64_t ldy, void* encode, int* err, int num_sms,
                                   int skip_w_stage, cudaStream_t stream);
+cudaError_t launch_matmul_mma_grouped_b18(int wt, const void* w, int64_t expert_stride, int64_t G, int64_t N,
+                                          int64_t K, const int8_t* qs, const void* ds, const int32_t* row_offsets,
+                                          int64_t total_rows, float* y, int64_t ldy, void* encode, int* err,
+                                          int num_sms, int skip_w_stage, cudaStream_t stream);
 
 namespace {
 
@@ -197,7 +202,6 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
                       const __half* __restrict__ ds, int64_t M, int N, int K, float* __restrict__ y, int64_t ldy,
                       int* err, const int32_t* __restrict__ row_offsets, int G, int wt, int skip_stage) {
     using C = MmaCfg<NT, T, kOcc, kB18, kGrouped>;
-    static_assert(!(kGrouped && kB18), "the grouped form takes IQ4_XS");
     constexpr int kTMax = T, kMt = C::kMt, kSPW = C::kSPW, kRG = C::kRG, R = C::kR, NS = C::kNS;
     extern __shared__ __align__(1024) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {  // the 128-byte-swizzled code boxes need 1024-byte alignment
@@ -239,7 +243,10 @@ __global__ void __launch_bounds__(kMmaThreads, kOcc)
             return;
         if constexpr (kGrouped) bc_range(bc, e, 1, G, kBcMmaW);
         mbar_arrive_expect_tx(&full[slot], (uint32_t)(R * C::kRowB + C::kQStage));
-        if constexpr (kGrouped) {
+        if constexpr (kGrouped && kB18) {
+            tma_load_3d(dst, &tmap_w, x, n0w, e, &full[slot]);
+            tma_load_3d(dst + R * kB18GroupBytes, &tmap_w, x + kB18GroupBytes / 4, n0w, e, &full[slot]);
+        } else if constexpr (kGrouped) {
             tma_load_3d(dst, &tmap_w, x, n0w, e, &full[slot]);
         } else if constexpr (kB18) {
             // two boxes of R rows x 144 B (eight 18-byte blocks each), one
@@ -920,6 +927,90 @@ inline cudaError_t encode_q_map(EncodeTiledFn enc, const int8_t* qs, int64_t K, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
                ? cudaSuccess
                : cudaErrorInvalidValue;
+}
+
+
+// Grouped (mixture-of-experts) launch of the persistent <NT, T> kernel for
+// weights of layout kB18 (format wt): W of expert g through a 3D tensor map
+// (row words x rows x experts, expert_stride bytes apart); one CTA per SM,
+// or fewer when the layer has fewer work items (at most row tiles x
+// (activation tiles of all rows + experts with rows)).
+template <int NT, int T, bool kB18>
+cudaError_t launch_grouped_nt(const void* w, int64_t expert_stride, int G, int64_t row_bytes, EncodeTiledFn enc,
+                              const CUtensorMap& tq, const __half* ds, const int32_t* row_offsets, int64_t rows,
+                              int slots, int N, int K, float* y, int64_t ldy, int* err, int wt, int num_sms,
+                              int skip_w_stage, cudaStream_t stream) {
+    using C = MmaCfg<NT, T, 1, kB18, true>;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const cudaError_t ea = mma_smem_attr<NT, T, 1, true, kB18>(dev);
+    if (ea != cudaSuccess) return ea;
+    CUtensorMap tw;
+    {
+        const cuuint64_t gdim[3] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)N, (cuuint64_t)G};
+        const cuuint64_t gstride[2] = {(cuuint64_t)row_bytes, (cuuint64_t)expert_stride};
+        const cuuint32_t box[3] = {(cuuint32_t)((kB18 ? kB18GroupBytes : kPairBytes) / 4), (cuuint32_t)C::kR, 1};
+        const cuuint32_t estride[3] = {1, 1, 1};
+        if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(w), gdim, gstride, box, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    cudaLaunchConfig_t cfg = {};
+    const int64_t items = (N + C::kR - 1) / C::kR * ((rows + C::kMt - 1) / C::kMt + slots);
+    cfg.gridDim = dim3((unsigned)(items < num_sms ? items : num_sms), 1, 1);
+    cfg.blockDim = dim3(kMmaThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, matmul_mma_kernel<NT, T, 1, true, kB18>, tw, tq, ds, rows, N, K, y, ldy, err,
+                              row_offsets, G, wt, skip_w_stage);
+}
+
+// The grouped form's launch: activation tiles of mma_tile_rows(mean rows per
+// expert with rows) rows (larger experts take several tiles); 128-row
+// weight tiles, or 64 / 32 when the experts' row tiles alone do not give
+// every SM a work item; at 32 activation rows 64 at most (the partial tiles
+// of 128 rows would leave one stage).
+template <bool kB18>
+cudaError_t launch_grouped(int wt, const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,
+                           const int8_t* qs, const void* ds, const int32_t* row_offsets, int64_t total_rows, float* y,
+                           int64_t ldy, void* encode, int* err, int num_sms, int skip_w_stage, cudaStream_t stream) {
+    const EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(encode);
+    const int64_t row_bytes = wt_row_bytes(wt, K);
+    const int slots = (int)(G < total_rows ? G : total_rows);  // experts that can have rows
+    const int64_t mean = (total_rows + slots - 1) / slots;
+    const int mt = mma_tile_rows(mean);
+    CUtensorMap tq;
+    const cudaError_t eq = encode_q_map(enc, qs, K, total_rows, mt, &tq);
+    if (eq != cudaSuccess) return eq;
+    const __half* dsh = reinterpret_cast<const __half*>(ds);
+    const int Ni = (int)N, Ki = (int)K, Gi = (int)G;
+    const int64_t ctas128 = (N + 127) / 128 * slots;
+    int rows_cta = ctas128 >= num_sms ? 128 : ((N + 63) / 64 * slots >= num_sms ? 64 : 32);
+    if (mt == 32 && rows_cta > 64) rows_cta = 64;
+#define IQ4XS_MMA_G(nt, t)                                                                                      \
+    launch_grouped_nt<nt, t, kB18>(w, expert_stride, Gi, row_bytes, enc, tq, dsh, row_offsets, total_rows, slots, \
+                                   Ni, Ki, y, ldy, err, wt, num_sms, skip_w_stage, stream)
+    switch (mt * 1000 + rows_cta) {
+        case 8128: return IQ4XS_MMA_G(1, 4);
+        case 8064: return IQ4XS_MMA_G(1, 2);
+        case 8032: return IQ4XS_MMA_G(1, 1);
+        case 16128: return IQ4XS_MMA_G(2, 4);
+        case 16064: return IQ4XS_MMA_G(2, 2);
+        case 16032: return IQ4XS_MMA_G(2, 1);
+        case 24128: return IQ4XS_MMA_G(3, 4);
+        case 24064: return IQ4XS_MMA_G(3, 2);
+        case 24032: return IQ4XS_MMA_G(3, 1);
+        case 32064: return IQ4XS_MMA_G(4, 2);
+        case 32032: return IQ4XS_MMA_G(4, 1);
+        default: return cudaErrorInvalidValue;
+    }
+#undef IQ4XS_MMA_G
 }
 
 }  // namespace

@@ -158,6 +158,28 @@ def test_grouped_clean(path, T, topk, G):
     _clean()
 
 
+@pytest.mark.parametrize("path", ("dp4a", "mma"))
+@pytest.mark.parametrize("wt", (B.WTYPE_Q4_0, B.WTYPE_IQ4_NL))
+def test_grouped_formats_clean(path, wt):
+    G, T, topk = 8, 20, 4
+    W = synth.MoEWorkload("moe_bounds_b18", seed=37, G=G, N=136, K=1024, topk=topk, tokens=(T,), d_scale=2e-3)
+    _, rows_x, offsets = W.inputs(T)
+    w = np.stack([synth.block32_weights(np.random.default_rng([37, wt, g]), W.N, W.K, 2e-3) for g in range(G)])
+    qs, ds = quantize_gpu(rows_x)
+    y = torch.full((rows_x.shape[0], W.N), float("nan"), device="cuda")
+    B.iq4xs_matmul_grouped(dev(w.reshape(G, -1)), w.shape[1] * w.shape[2], G, W.N, W.K, qs, ds,
+                           dev(offsets.astype(np.int32)), y, path=path, wtype=wt)
+    torch.cuda.synchronize()
+    yn = y.cpu().numpy()
+    assert gate_written(yn) is None
+    qs_o, d_o, _ = oracle_q8(rows_x)
+    for g in range(G):
+        r0, r1 = int(offsets[g]), int(offsets[g + 1])
+        if r1 > r0:
+            assert gate_parity(yn[r0:r1], oracle.get().matmul_wt(wt, w[g], W.N, W.K, qs_o[r0:r1], d_o[r0:r1])) is None
+    _clean()
+
+
 @pytest.mark.parametrize("M", (2, 40))
 def test_linear_entry_points_clean(M):
     N, K = 256, 1024

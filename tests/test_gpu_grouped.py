@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from _gates import gate_independent, gate_parity, gate_written
 from _gpu import dev, independent_fp32, oracle_matmul, oracle_q8, quantize_gpu
 from iq4_xs_quantized_gb300 import binding as B
@@ -201,3 +202,54 @@ def test_grouped_rejects_bad_arguments():
         with pytest.raises(B.IQ4XSError) as e:
             B.iq4xs_matmul_grouped(w3, w3.shape[1], 2, W3.N, 768, qs3, ds3, off, y, path=p)
         assert e.value.status == B.ERR_SHAPE
+
+
+@pytest.mark.parametrize("wt", (B.WTYPE_Q4_0, B.WTYPE_IQ4_NL))
+@pytest.mark.parametrize("path", ("dp4a", "mma", "auto"))
+@pytest.mark.parametrize("T,topk,G", [(20, 4, 8), (3, 2, 70), (64, 8, 16)])
+def test_grouped_formats_match_oracle(wt, path, T, topk, G):
+    """Q4_0 / IQ4_NL experts on the CUDA-core and persistent warp-MMA forms
+    (and AUTO, which keeps them off the tcgen05 form): every expert's rows
+    against the oracle's matmul of that format, and bitwise against
+    iq4xs_matmul_wt on the same path over the expert's rows."""
+    W = synth.MoEWorkload("moe_formats", seed=31, G=G, N=200, K=1024, topk=topk, tokens=(T,), d_scale=2e-3)
+    _, rows_x, offsets = W.inputs(T)
+    N, K = W.N, W.K
+    w = np.stack([synth.block32_weights(np.random.default_rng([31, wt, g]), N, K, 2e-3) for g in range(G)])
+    stride = w.shape[1] * w.shape[2]
+    wd = dev(w.reshape(G, -1))
+    qs, ds = quantize_gpu(rows_x)
+    off_d = dev(offsets.astype(np.int32))
+    M = rows_x.shape[0]
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    B.iq4xs_matmul_grouped(wd, stride, G, N, K, qs, ds, off_d, y, path=path, wtype=wt)
+    torch.cuda.synchronize()
+    yn = y.cpu().numpy()
+    assert gate_written(yn) is None
+    qs_o, d_o, _ = oracle_q8(rows_x)
+    orc = oracle.get()
+    slots = min(G, M)
+    mean = -(-M // slots)
+    form = path if path != "auto" else (
+        "mma" if M >= min(G, 24) or B.iq4xs_select_path(mean, N, K) != B.PATH_DP4A else "dp4a")
+    for g in range(G):
+        r0, r1 = int(offsets[g]), int(offsets[g + 1])
+        if r1 > r0:
+            r = gate_parity(yn[r0:r1], orc.matmul_wt(wt, w[g], N, K, qs_o[r0:r1], d_o[r0:r1]))
+            assert r is None, (g, r)
+            if form == "dp4a":  # the CUDA-core form: each expert with its own batch width
+                ys = torch.full((r1 - r0, N), float("nan"), dtype=torch.float32, device="cuda")
+                B.iq4xs_matmul_wt(wd[g], wt, N, K, qs[r0:r1], ds[r0:r1], r1 - r0, ys, B.PATH_DP4A)
+                torch.cuda.synchronize()
+                assert np.array_equal(ys.cpu().numpy(), yn[r0:r1]), g
+
+
+def test_grouped_formats_reject_the_tcgen05_form():
+    G, N, K = 4, 128, 512
+    w = torch.zeros((G, N * (K // 32) * 18), dtype=torch.uint8, device="cuda")
+    qs, ds = B.alloc_activations(8, K, "cuda")
+    off = torch.tensor([0, 2, 4, 6, 8], dtype=torch.int32, device="cuda")
+    y = torch.empty((8, N), device="cuda")
+    with pytest.raises(B.IQ4XSError) as e:
+        B.iq4xs_matmul_grouped(w, w.shape[1], G, N, K, qs, ds, off, y, path="tc", wtype=B.WTYPE_Q4_0)
+    assert e.value.status == B.ERR_SHAPE
