@@ -533,6 +533,7 @@ def run_ours(args, world, rank, local):
         torch.cuda.empty_cache()
         extras["decode_stream"] = decode_stream(torch, B, dev)
         extras["moe_grouped"] = moe_grouped(torch, B, dev)
+        extras["moe_grouped_q4_0"] = moe_grouped(torch, B, dev, tokens=(4, 16, 64), wtype=B.WTYPE_Q4_0)
         extras["weight_formats"] = weight_formats(torch, B, dev, stream, mm_us)
         extras["decoder_shapes"] = decoder_shapes(torch, B, dev, stream)
         extras["prefill_sweep"] = prefill_sweep(torch, B, dev, stream)
@@ -719,8 +720,9 @@ def decode_stream(torch, B, dev, reps=5):
     return res
 
 
-def moe_grouped(torch, B, dev, layers=12, reps=5, tokens=(1, 4, 16, 64, 256)):
-    """Routed-expert layer (128 experts of 1536 x 2048, top-8): per token
+def moe_grouped(torch, B, dev, layers=12, reps=5, tokens=(1, 4, 16, 64, 256), wtype=0):
+    """Routed-expert layer (128 experts of 1536 x 2048, top-8; IQ4_XS experts,
+    or Q4_0 / IQ4_NL ones with ``wtype``, which have no tcgen05 form): per token
     count T, one layer call = quantize the T*8 routed rows + the grouped
     matmul in one launch (the dispatcher's form, and the CUDA-core,
     warp-MMA and tcgen05 forms forced), against the same layer with one launch per
@@ -730,7 +732,11 @@ def moe_grouped(torch, B, dev, layers=12, reps=5, tokens=(1, 4, 16, 64, 256)):
     and outputs."""
     from iq4_xs_quantized_gb300 import synth
     W = synth.MOE_DECODE
-    w0 = torch.from_numpy(W.weights().reshape(W.G, -1)).to(dev)
+    if wtype == B.WTYPE_IQ4_XS:
+        w0 = torch.from_numpy(W.weights().reshape(W.G, -1)).to(dev)
+    else:
+        w0 = torch.from_numpy(np.stack([synth.block32_weights(np.random.default_rng([W.seed, wtype, g]), W.N, W.K,
+                                                              W.d_scale) for g in range(W.G)]).reshape(W.G, -1)).to(dev)
     stride = w0.shape[1]
     ws = [w0] + [w0.clone() for _ in range(layers - 1)]
     stream = torch.cuda.Stream(device=dev)
@@ -748,7 +754,7 @@ def moe_grouped(torch, B, dev, layers=12, reps=5, tokens=(1, 4, 16, 64, 256)):
             def fn(s):
                 for w in ws:
                     B.iq4xs_quantize_q8_1(xr, qs, ds, s)
-                    B.iq4xs_matmul_grouped(w, stride, W.G, W.N, W.K, qs, ds, off, y, s, path=path)
+                    B.iq4xs_matmul_grouped(w, stride, W.G, W.N, W.K, qs, ds, off, y, s, path=path, wtype=wtype)
             return fn
 
         def per_expert(s):
@@ -756,13 +762,14 @@ def moe_grouped(torch, B, dev, layers=12, reps=5, tokens=(1, 4, 16, 64, 256)):
                 B.iq4xs_quantize_q8_1(xr, qs, ds, s)
                 for g in touched:
                     r0, r1 = int(offsets[g]), int(offsets[g + 1])
-                    B.iq4xs_matmul(w[g], W.N, W.K, qs[r0:r1], ds[r0:r1], r1 - r0, y[r0:r1],
-                                   B.PATH_AUTO, s)
+                    B.iq4xs_matmul_wt(w[g], wtype, W.N, W.K, qs[r0:r1], ds[r0:r1], r1 - r0, y[r0:r1],
+                                      B.PATH_AUTO, s)
 
         times = {}
-        for name, fn in (("grouped", grouped("auto")), ("grouped_dp4a", grouped("dp4a")),
-                         ("grouped_mma", grouped("mma")), ("grouped_tc", grouped("tc")),
-                         ("per_expert", per_expert)):
+        forms = [("grouped", grouped("auto")), ("grouped_dp4a", grouped("dp4a")), ("grouped_mma", grouped("mma"))]
+        if wtype == B.WTYPE_IQ4_XS:
+            forms.append(("grouped_tc", grouped("tc")))
+        for name, fn in forms + [("per_expert", per_expert)]:
             with torch.cuda.stream(stream):
                 fn(stream)
             torch.cuda.synchronize()
@@ -779,16 +786,16 @@ def moe_grouped(torch, B, dev, layers=12, reps=5, tokens=(1, 4, 16, 64, 256)):
             torch.cuda.synchronize()
             times[name] = t0.elapsed_time(t1) * 1e3 / (reps * layers)
             del g
-        nbytes = (len(touched) * W.N * (W.K // 256) * 136 + M * W.K + M * (W.K // 32) * 4
+        nbytes = (len(touched) * B.iq4xs_weight_bytes(wtype, W.N, W.K) + M * W.K + M * (W.K // 32) * 4
                   + 4 * M * W.N + quantize_bytes(M, W.K))
         mean = -(-M // min(W.G, M))
-        auto = ("tc" if mean >= 32 else "mma") \
+        auto = ("tc" if mean >= 32 and wtype == B.WTYPE_IQ4_XS else "mma") \
             if M >= min(W.G, 24) or B.iq4xs_select_path(mean, W.N, W.K) != B.PATH_DP4A else "dp4a"
         res.append({"tokens": T, "rows": M, "experts_touched": len(touched), "auto_form": auto,
                     "grouped_us_per_layer": round(times["grouped"], 3),
                     "grouped_dp4a_us": round(times["grouped_dp4a"], 3),
                     "grouped_mma_us": round(times["grouped_mma"], 3),
-                    "grouped_tc_us": round(times["grouped_tc"], 3),
+                    "grouped_tc_us": round(times["grouped_tc"], 3) if "grouped_tc" in times else None,
                     "per_expert_launches_us_per_layer": round(times["per_expert"], 3),
                     "grouped_GBps": round(nbytes / (times["grouped"] * 1e-6) / 1e9, 1)})
     del ws
