@@ -297,6 +297,16 @@ int iq4xs_linear(const void* w, int64_t N, int64_t K, const float* x, int64_t M,
                  float* y, int64_t ldy, void* workspace, int64_t workspace_bytes,
                  int64_t stream);
 
+/*
+ * iq4xs_linear for weights in format wtype (an iq4xs_wtype: W of
+ * iq4xs_weight_bytes(wtype, N, K) bytes): the same workspace, path and
+ * forms, the matmul that of iq4xs_matmul_wt (or, with the prepared operand,
+ * iq4xs_matmul_tc_operand) for that format.  IQ4XS_ERR_ARG for an unknown
+ * format.
+ */
+int iq4xs_linear_wt(const void* w, int wtype, int64_t N, int64_t K, const float* x, int64_t M, int64_t ldx,
+                    float* y, int64_t ldy, void* workspace, int64_t workspace_bytes, int64_t stream);
+
 /* Workspace bytes for iq4xs_linear's fastest form at (M, N, K), and the
  * least it accepts (the Q8_1 codes and scales); 0 if the shape is invalid. */
 int64_t iq4xs_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);

@@ -70,6 +70,7 @@ def load(path: str | None = None):
         lib.iq4xs_matmul_grouped_path.argtypes = [vp, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, ci, i64]
         lib.iq4xs_matmul_grouped_wt.argtypes = [vp, ci, i64, i64, i64, i64, vp, vp, vp, i64, vp, i64, ci, i64]
         lib.iq4xs_linear.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, i64]
+        lib.iq4xs_linear_wt.argtypes = [vp, ci, i64, i64, vp, i64, i64, vp, i64, vp, i64, i64]
         lib.iq4xs_linear_workspace_bytes.argtypes = [i64, i64, i64]
         lib.iq4xs_linear_workspace_bytes.restype = i64
         lib.iq4xs_linear_static.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, i64]
@@ -95,7 +96,7 @@ def load(path: str | None = None):
         lib.iq4xs_status_string.argtypes = [ci]
         lib.iq4xs_status_string.restype = ctypes.c_char_p
         for name in ("iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_matmul_grouped", "iq4xs_matmul_grouped_path",
-                     "iq4xs_matmul_grouped_wt",
+                     "iq4xs_matmul_grouped_wt", "iq4xs_linear_wt",
                      "iq4xs_dequantize", "iq4xs_linear", "iq4xs_matmul_wt", "iq4xs_dequantize_wt",
                      "iq4xs_select_path", "iq4xs_set_crossover", "iq4xs_set_baseline_threshold",
                      "iq4xs_set_crossover_classes", "iq4xs_test_skip_w_stage",
@@ -259,14 +260,15 @@ def iq4xs_linear_workspace_min_bytes(M: int, N: int, K: int) -> int:
     return int(load().iq4xs_linear_workspace_min_bytes(M, N, K))
 
 
-def iq4xs_linear(w, N: int, K: int, x, y, workspace, stream=None) -> None:
-    """y fp32 [M, ldy] = Q8_1(x) . W^T in one call; workspace: uint8 device
-    tensor of at least iq4xs_linear_workspace_bytes(M, N, K) bytes."""
+def iq4xs_linear(w, N: int, K: int, x, y, workspace, stream=None, wtype=WTYPE_IQ4_XS) -> None:
+    """y fp32 [M, ldy] = Q8_1(x) . W^T in one call (W in format ``wtype``);
+    workspace: uint8 device tensor of at least
+    iq4xs_linear_workspace_bytes(M, N, K) bytes."""
     M = x.shape[0]
-    rc = load().iq4xs_linear(_ptr(w), N, K, _ptr(x), M, x.stride(0), _ptr(y), y.stride(0),
-                             _ptr(workspace), workspace.numel() * workspace.element_size(),
-                             _stream(stream))
-    _check("iq4xs_linear", rc)
+    rc = load().iq4xs_linear_wt(_ptr(w), _wtype(wtype), N, K, _ptr(x), M, x.stride(0), _ptr(y), y.stride(0),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _stream(stream))
+    _check("iq4xs_linear_wt", rc)
 
 
 def iq4xs_linear_static(w, N: int, K: int, x, y, stream=None) -> None:

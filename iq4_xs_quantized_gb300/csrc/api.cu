@@ -268,7 +268,13 @@ int64_t iq4xs_linear_workspace_min_bytes(int64_t M, int64_t N, int64_t K) {
 int iq4xs_linear(const void* w, int64_t N, int64_t K, const float* x, int64_t M, int64_t ldx,
                  float* y, int64_t ldy, void* workspace, int64_t workspace_bytes,
                  int64_t stream) {
+    return iq4xs_linear_wt(w, IQ4XS_WTYPE_IQ4_XS, N, K, x, M, ldx, y, ldy, workspace, workspace_bytes, stream);
+}
+
+int iq4xs_linear_wt(const void* w, int wtype, int64_t N, int64_t K, const float* x, int64_t M, int64_t ldx,
+                    float* y, int64_t ldy, void* workspace, int64_t workspace_bytes, int64_t stream) {
     if (!w || !x || !y || !workspace) return IQ4XS_ERR_ARG;
+    if (wtype < IQ4XS_WTYPE_IQ4_XS || wtype > IQ4XS_WTYPE_IQ4_NL) return IQ4XS_ERR_ARG;
     LinearLayout L;
     if (!linear_layout(M, N, K, &L)) return IQ4XS_ERR_SHAPE;
     if (workspace_bytes < L.q8) return IQ4XS_ERR_ARG;
@@ -279,11 +285,11 @@ int iq4xs_linear(const void* w, int64_t N, int64_t K, const float* x, int64_t M,
     if (L.path == IQ4XS_PATH_TC && workspace_bytes >= L.total) {  // room for the prepared operand
         int rc = iq4xs_quantize_q8_1_tc(x, M, K, ldx, qs, ds, ws + L.op, stream);
         if (rc) return rc;
-        return iq4xs_matmul_tc_operand(w, IQ4XS_WTYPE_IQ4_XS, N, K, ws + L.op, M, y, ldy, stream);
+        return iq4xs_matmul_tc_operand(w, wtype, N, K, ws + L.op, M, y, ldy, stream);
     }
     int rc = iq4xs_quantize_q8_1(x, M, K, ldx, qs, ds, stream);
     if (rc) return rc;
-    return iq4xs_matmul(w, N, K, qs, ds, M, y, ldy, L.path, stream);
+    return iq4xs_matmul_wt(w, wtype, N, K, qs, ds, M, y, ldy, L.path, stream);
 }
 
 int iq4xs_matmul_grouped(const void* w, int64_t expert_stride, int64_t G, int64_t N, int64_t K,

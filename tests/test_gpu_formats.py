@@ -171,3 +171,33 @@ def test_iq4nl_equals_iq4xs_with_uniform_scale_bitwise():
         b = matmul_gpu(w_nl, N, K, None, None, M, "tcp", op=op, wtype=B.WTYPE_IQ4_NL)
         assert gate_written(a) is None
         assert np.array_equal(a, b), (M, "tcp")
+
+
+@pytest.mark.parametrize("name,wt", FORMATS)
+def test_formats_linear_one_call(name, wt):
+    """iq4xs_linear for Q4_0 / IQ4_NL weights on the dispatcher's path per M
+    (CUDA cores, warp MMA, tcgen05 with the prepared operand): against the
+    oracle, and bitwise the separate quantize + matmul calls."""
+    rng = np.random.default_rng([47, wt])
+    N, K = 300, 2048
+    w = synth.block32_weights(rng, N, K, 2e-3)
+    wd = dev(w)
+    names = {B.PATH_DP4A: "dp4a", B.PATH_MMA: "mma", B.PATH_TC: "tcp", B.PATH_BASELINE: "tcp"}
+    for M in (1, 3, 8, 16, 40):
+        x = synth.activations(rng, M, K, outlier_frac=0.01)
+        xd = dev(x)
+        ws = torch.full((B.iq4xs_linear_workspace_bytes(M, N, K),), 0xFF, dtype=torch.uint8, device="cuda")
+        y = torch.full((M, N), float("nan"), device="cuda")
+        B.iq4xs_linear(wd, N, K, xd, y, ws, wtype=wt)
+        torch.cuda.synchronize()
+        yl = y.cpu().numpy()
+        assert gate_written(yl) is None
+        qs_o, d_o, _ = oracle_q8(x)
+        assert gate_parity(yl, _oracle_wt(wt, w, N, K, qs_o, d_o)) is None, (name, M)
+        path = names[B.iq4xs_select_path(M, N, K)]
+        qs, ds = quantize_gpu(x)
+        if path == "tcp":
+            y2 = matmul_gpu(wd, N, K, None, None, M, "tcp", op=prepare_gpu(x), wtype=wt)
+        else:
+            y2 = _matmul_wt(wd, wt, N, K, qs, ds, M, {"dp4a": B.PATH_DP4A, "mma": B.PATH_MMA}[path])
+        assert np.array_equal(yl, y2), (name, M, path)
