@@ -788,9 +788,8 @@ def moe_grouped(torch, B, dev, layers=12, reps=5, tokens=(1, 4, 16, 64, 256), wt
             del g
         nbytes = (len(touched) * B.iq4xs_weight_bytes(wtype, W.N, W.K) + M * W.K + M * (W.K // 32) * 4
                   + 4 * M * W.N + quantize_bytes(M, W.K))
-        mean = -(-M // min(W.G, M))
-        auto = ("tc" if mean >= 32 and wtype == B.WTYPE_IQ4_XS else "mma") \
-            if M >= min(W.G, 24) or B.iq4xs_select_path(mean, W.N, W.K) != B.PATH_DP4A else "dp4a"
+        auto = {B.PATH_DP4A: "dp4a", B.PATH_MMA: "mma", B.PATH_TC: "tc"}[
+            B.iq4xs_select_grouped_path(W.G, W.N, W.K, M, wtype)]
         res.append({"tokens": T, "rows": M, "experts_touched": len(touched), "auto_form": auto,
                     "grouped_us_per_layer": round(times["grouped"], 3),
                     "grouped_dp4a_us": round(times["grouped_dp4a"], 3),

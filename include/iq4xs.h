@@ -372,6 +372,16 @@ int iq4xs_dequantize_wt(const void* w, int wtype, int64_t N, int64_t K, void* ou
 int iq4xs_select_path(int64_t M, int64_t N, int64_t K, int* path_out);
 
 /*
+ * The form iq4xs_matmul_grouped_wt takes with IQ4XS_PATH_AUTO for G experts
+ * of N x K weights in format wtype over total_rows rows (the rule given
+ * with iq4xs_matmul_grouped): IQ4XS_PATH_DP4A, IQ4XS_PATH_MMA or
+ * IQ4XS_PATH_TC.  Host only, no device access.  IQ4XS_ERR_SHAPE for sizes
+ * out of the call's range, IQ4XS_ERR_ARG for a null output or an unknown
+ * format.
+ */
+int iq4xs_select_grouped_path(int64_t G, int64_t N, int64_t K, int64_t total_rows, int wtype, int* path_out);
+
+/*
  * Install the measured crossover: DP4A is chosen for M <= m_max_dp4a.
  * Host only.  Defaults to 4 until a calibration sets it.  Thread-safe.
  */

@@ -78,6 +78,7 @@ def load(path: str | None = None):
         lib.iq4xs_linear_static_max_bytes.argtypes = []
         lib.iq4xs_linear_static_max_bytes.restype = i64
         lib.iq4xs_select_path.argtypes = [i64, i64, i64, ctypes.POINTER(ci)]
+        lib.iq4xs_select_grouped_path.argtypes = [i64, i64, i64, i64, ci, ctypes.POINTER(ci)]
         lib.iq4xs_set_crossover.argtypes = [i64]
         lib.iq4xs_set_baseline_threshold.argtypes = [i64]
         lib.iq4xs_set_crossover_classes.argtypes = [ctypes.POINTER(i64), ctypes.POINTER(i64), ci]
@@ -98,7 +99,8 @@ def load(path: str | None = None):
         for name in ("iq4xs_quantize_q8_1", "iq4xs_matmul", "iq4xs_matmul_grouped", "iq4xs_matmul_grouped_path",
                      "iq4xs_matmul_grouped_wt", "iq4xs_linear_wt",
                      "iq4xs_dequantize", "iq4xs_linear", "iq4xs_matmul_wt", "iq4xs_dequantize_wt",
-                     "iq4xs_select_path", "iq4xs_set_crossover", "iq4xs_set_baseline_threshold",
+                     "iq4xs_select_path", "iq4xs_select_grouped_path", "iq4xs_set_crossover",
+                     "iq4xs_set_baseline_threshold",
                      "iq4xs_set_crossover_classes", "iq4xs_test_skip_w_stage",
                      "iq4xs_set_mma_crossover", "iq4xs_set_mma_crossover_classes",
                      "iq4xs_test_mma_config",
@@ -318,6 +320,14 @@ def iq4xs_dequantize_wt(w, wtype, N: int, K: int, out, stream=None) -> None:
 def iq4xs_select_path(M: int, N: int, K: int) -> int:
     out = ctypes.c_int(-1)
     _check("iq4xs_select_path", load().iq4xs_select_path(M, N, K, ctypes.byref(out)))
+    return out.value
+
+
+def iq4xs_select_grouped_path(G: int, N: int, K: int, total_rows: int, wtype=WTYPE_IQ4_XS) -> int:
+    """The form the grouped call takes with AUTO (PATH_DP4A, PATH_MMA or PATH_TC)."""
+    out = ctypes.c_int(-1)
+    _check("iq4xs_select_grouped_path",
+           load().iq4xs_select_grouped_path(G, N, K, total_rows, _wtype(wtype), ctypes.byref(out)))
     return out.value
 
 

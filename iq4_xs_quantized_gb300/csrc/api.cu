@@ -132,6 +132,21 @@ int kernel_path_impl(int64_t M, int64_t N, int64_t K) {
     if (M <= mma_max_for(N, K)) return IQ4XS_PATH_MMA;
     return IQ4XS_PATH_TC;
 }
+// The grouped form: the warp-MMA form from 24 rows on (as many as the
+// experts, if fewer), or once the mean rows of an expert slot leave one
+// expert matrix's DP4A range (measured on a 128 x 1536 x 2048 layer: the
+// CUDA-core form is 6 % faster at 16 rows, 19 % slower at 24 and 30 % at
+// 64); the tcgen05 form from 32 mean rows per expert slot on (the same
+// layer: 15 % slower at 24, 2 % faster at 32, 8 % at 64, 24 % at 256), for
+// IQ4_XS weights (the other formats stay on the warp-MMA form); DP4A
+// otherwise, and whenever K % 512 != 0.
+int grouped_path_impl(int64_t G, int64_t N, int64_t K, int64_t total_rows, int wtype) {
+    const int64_t slots = G < total_rows ? G : total_rows;
+    const int64_t mean = (total_rows + slots - 1) / slots;
+    const int64_t mma_min = G < kGroupedMmaMinRows ? G : kGroupedMmaMinRows;
+    if (K % kPairK != 0 || (total_rows < mma_min && mean <= crossover_for(N, K))) return IQ4XS_PATH_DP4A;
+    return (mean >= kGroupedTcMinRows && wtype == IQ4XS_WTYPE_IQ4_XS) ? IQ4XS_PATH_TC : IQ4XS_PATH_MMA;
+}
 // The advised path: the kernel path, or BASELINE above the measured threshold.
 int select_path_impl(int64_t M, int64_t N, int64_t K) {
     const int p = kernel_path_impl(M, N, K);
@@ -321,23 +336,7 @@ int iq4xs_matmul_grouped_wt(const void* w, int wtype, int64_t expert_stride, int
     if (!aligned(w, 16) || !aligned(qs, 16) || !aligned(ds, 4) || !aligned(row_offsets, 4) ||
         !aligned(y, 4))
         return IQ4XS_ERR_ALIGN;
-    if (path == IQ4XS_PATH_AUTO) {
-        // The warp-MMA form from 24 rows on (as many as the experts, if
-        // fewer), or once the mean rows of an expert slot leave one expert
-        // matrix's DP4A range (measured on a 128 x 1536 x 2048 layer: the
-        // CUDA-core form is 6 % faster at 16 rows, 19 % slower at 24 and
-        // 30 % at 64); the tcgen05 form from 32 mean rows per expert slot on
-        // (the same layer: 15 % slower at 24, 2 % faster at 32, 8 % at 64,
-        // 24 % at 256), for IQ4_XS weights (the other formats stay on the
-        // warp-MMA form).
-        const int64_t slots = G < total_rows ? G : total_rows;
-        const int64_t mean = (total_rows + slots - 1) / slots;
-        const int64_t mma_min = G < kGroupedMmaMinRows ? G : kGroupedMmaMinRows;
-        if (K % kPairK == 0 && (total_rows >= mma_min || mean > crossover_for(N, K)))
-            path = (mean >= kGroupedTcMinRows && wtype == IQ4XS_WTYPE_IQ4_XS) ? IQ4XS_PATH_TC : IQ4XS_PATH_MMA;
-        else
-            path = IQ4XS_PATH_DP4A;
-    }
+    if (path == IQ4XS_PATH_AUTO) path = grouped_path_impl(G, N, K, total_rows, wtype);
     if ((path == IQ4XS_PATH_MMA || path == IQ4XS_PATH_TC) && K % kPairK) return IQ4XS_ERR_SHAPE;
     if (path == IQ4XS_PATH_TC && wtype != IQ4XS_WTYPE_IQ4_XS) return IQ4XS_ERR_SHAPE;
     DevState* st;
@@ -378,6 +377,16 @@ int iq4xs_select_path(int64_t M, int64_t N, int64_t K, int* path_out) {
     if (!path_out) return IQ4XS_ERR_ARG;
     if (M < 1 || M > kMaxM || N < 1 || K <= 0 || K % kQK) return IQ4XS_ERR_SHAPE;
     *path_out = select_path_impl(M, N, K);
+    return IQ4XS_OK;
+}
+
+int iq4xs_select_grouped_path(int64_t G, int64_t N, int64_t K, int64_t total_rows, int wtype, int* path_out) {
+    if (!path_out) return IQ4XS_ERR_ARG;
+    if (wtype < IQ4XS_WTYPE_IQ4_XS || wtype > IQ4XS_WTYPE_IQ4_NL) return IQ4XS_ERR_ARG;
+    if (G < 1 || G > 65535 || N < 1 || N > (1 << 30) || K <= 0 || K % kQK || K > (1 << 30) || total_rows < 1 ||
+        total_rows > kMaxM)
+        return IQ4XS_ERR_SHAPE;
+    *path_out = grouped_path_impl(G, N, K, total_rows, wtype);
     return IQ4XS_OK;
 }
 

@@ -107,6 +107,38 @@ def test_select_path_and_crossover(lib):
         B.reset_dispatch()
 
 
+def test_select_grouped_path_rule(lib):
+    """The grouped AUTO rule (host only): the CUDA-core form below min(G, 24)
+    rows unless the mean rows per expert leave the DP4A range, the warp-MMA
+    form from there, tcgen05 from 32 mean rows per expert slot on (IQ4_XS
+    only), and the CUDA-core form whenever K % 512 != 0."""
+    try:
+        _dispatch(1, 8)
+        sel = B.iq4xs_select_grouped_path
+        G, N, K = 128, 1536, 2048
+        assert [sel(G, N, K, r) for r in (1, 16, 23, 24, 128, 3968, 3969, 32768)] == [
+            B.PATH_DP4A, B.PATH_DP4A, B.PATH_DP4A, B.PATH_MMA, B.PATH_MMA, B.PATH_MMA, B.PATH_TC, B.PATH_TC]
+        for wt in (B.WTYPE_Q4_0, B.WTYPE_IQ4_NL):
+            assert sel(G, N, K, 4096, wt) == B.PATH_MMA  # no tcgen05 grouped form for these formats
+            assert sel(G, N, K, 16, wt) == B.PATH_DP4A
+        assert sel(8, N, K, 7) == B.PATH_DP4A      # fewer rows than the 8 experts: mean 1 row
+        assert sel(8, N, K, 8) == B.PATH_MMA       # min(G, 24) = 8 rows
+        assert sel(8, N, K, 248) == B.PATH_MMA     # mean 31 rows (rounded up)
+        assert sel(8, N, K, 249) == B.PATH_TC      # mean 32 rows
+        assert sel(G, N, 1280, 4096) == B.PATH_DP4A  # K % 512 != 0
+        assert sel(32, N, K, 20) == B.PATH_DP4A    # 20 rows < min(32, 24)
+        B.iq4xs_set_crossover(0)  # a matrix size without a DP4A range: one row already leaves it
+        assert sel(G, N, K, 1) == B.PATH_MMA
+        out = ctypes.c_int()
+        assert lib.iq4xs_select_grouped_path(0, N, K, 8, 0, ctypes.byref(out)) == B.ERR_SHAPE
+        assert lib.iq4xs_select_grouped_path(G, N, K, 0, 0, ctypes.byref(out)) == B.ERR_SHAPE
+        assert lib.iq4xs_select_grouped_path(G, N, K, 32769, 0, ctypes.byref(out)) == B.ERR_SHAPE
+        assert lib.iq4xs_select_grouped_path(G, N, K, 8, 3, ctypes.byref(out)) == B.ERR_ARG
+        assert lib.iq4xs_select_grouped_path(G, N, K, 8, 0, None) == B.ERR_ARG
+    finally:
+        B.reset_dispatch()
+
+
 def test_mma_config_hook_validation(lib):
     assert lib.iq4xs_test_mma_config(0, 0, 0) == B.OK
     for rows, splits, occ in ((16, 1, 0), (288, 1, 0), (-32, 1, 0), (64, 9, 0), (64, -1, 0), (64, 1, 3),

@@ -29,6 +29,9 @@ def _lib():
     assert B.iq4xs_last_device_error() == 0
 
 
+FORMS = {B.PATH_DP4A: "dp4a", B.PATH_MMA: "mma", B.PATH_TC: "tc"}
+
+
 def _run_grouped(W, rows_x, offsets, path="auto"):
     G, N, K = W.G, W.N, W.K
     w = W.weights()
@@ -96,14 +99,10 @@ def test_grouped_mma_matches_oracle(T, topk):
         r0, r1 = int(offsets[g]), int(offsets[g + 1])
         ind_own[r0:r1] = ind[r0:r1, g * W.N:(g + 1) * W.N]
     assert gate_independent(y, ind_own) is None
-    # AUTO: the MMA form from min(G, 24) rows on, or once the mean rows of
-    # an expert slot leave one expert's dp4a range, else dp4a; tcgen05 from
-    # 32 mean rows per expert slot on (same bits as the explicit call)
+    # AUTO takes the form the host query names (its rule is pinned on the
+    # CPU); same bits as the explicit call
     M = rows_x.shape[0]
-    slots = min(W.G, M)
-    mean = -(-M // slots)
-    auto = ("tc" if mean >= 32 else "mma") \
-        if M >= min(W.G, 24) or B.iq4xs_select_path(mean, W.N, W.K) != B.PATH_DP4A else "dp4a"
+    auto = FORMS[B.iq4xs_select_grouped_path(W.G, W.N, W.K, M)]
     y_auto = _run_grouped(W, rows_x, offsets)[-1]
     y_expl = y if auto == "mma" else _run_grouped(W, rows_x, offsets, auto)[-1]
     assert np.array_equal(y_auto, y_expl), auto
@@ -126,7 +125,7 @@ def test_grouped_tc_matches_oracle(T, topk, G):
     assert gate_independent(y, ind_own) is None
     # AUTO takes the tcgen05 form from 32 mean rows per expert slot on
     M = rows_x.shape[0]
-    if -(-M // min(W.G, M)) >= 32:
+    if B.iq4xs_select_grouped_path(W.G, W.N, W.K, M) == B.PATH_TC:
         assert np.array_equal(_run_grouped(W, rows_x, offsets)[-1], y)
 
 
@@ -228,10 +227,8 @@ def test_grouped_formats_match_oracle(wt, path, T, topk, G):
     assert gate_written(yn) is None
     qs_o, d_o, _ = oracle_q8(rows_x)
     orc = oracle.get()
-    slots = min(G, M)
-    mean = -(-M // slots)
-    form = path if path != "auto" else (
-        "mma" if M >= min(G, 24) or B.iq4xs_select_path(mean, N, K) != B.PATH_DP4A else "dp4a")
+    form = path if path != "auto" else FORMS[B.iq4xs_select_grouped_path(G, N, K, M, wt)]
+    assert form != "tc"
     for g in range(G):
         r0, r1 = int(offsets[g]), int(offsets[g + 1])
         if r1 > r0:
