@@ -73,6 +73,9 @@ def parse_args():
                     help="launch without programmatic dependent launch (for serialised profilers)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the dequantize+GEMM baseline and the decode-stream workload")
+    ap.add_argument("--formats-only", action="store_true",
+                    help="profiling runs only: time the Q4_0 / IQ4_NL matmuls (square, or --shape; --ms), "
+                         "print their line and stop")
     ap.add_argument("--moe-tokens", type=int, default=None,
                     help="profiling runs only: time the grouped MoE layer at this many tokens, "
                          "print its line and stop")
@@ -383,6 +386,13 @@ def run_ours(args, world, rank, local):
         res = moe_grouped(torch, B, dev, layers=2, reps=2, tokens=(args.moe_tokens,))
         if rank == 0:
             print(json.dumps({"moe_grouped": res}), flush=True)
+        return
+    if args.formats_only:
+        fN, fK = (int(v) for v in args.shape.split(",")) if args.shape else (4096, 4096)
+        fms = tuple(int(v) for v in args.ms.split(",")) if args.ms else (1, 4, 8, 16, 64, 96)
+        res = weight_formats(torch, B, dev, torch.cuda.Stream(device=dev), {}, N=fN, K=fK, ms=fms)
+        if rank == 0:
+            print(json.dumps({"weight_formats": res}), flush=True)
         return
     W = synth.SQUARE
     N, K = W.shapes[0]
@@ -802,13 +812,13 @@ def moe_grouped(torch, B, dev, layers=12, reps=5, tokens=(1, 4, 16, 64, 256), wt
     return res
 
 
-def weight_formats(torch, B, dev, stream, iq4xs_us, N=4096, K=4096, copies=48, reps=10,
+def weight_formats(torch, B, dev, stream, iq4xs_us, N=4096, K=4096, copies=None, reps=10,
                    ms=(1, 4, 8, 16, 64, 96)):
-    """The same square 4096 x 4096 matmul with Q4_0 and IQ4_NL weights
-    (18-byte blocks of 32, 0.5625 B/weight) on the dispatcher's path:
-    device time per launch from graphs of back-to-back launches over
-    `copies` rotating weight copies (452 MB, larger than L2), beside the
-    IQ4_XS time of the main sweep; `path` names the kernel (dp4a, mma,
+    """The same square 4096 x 4096 matmul (or N x K) with Q4_0 and IQ4_NL
+    weights (18-byte blocks of 32, 0.5625 B/weight) on the dispatcher's
+    path: device time per launch from graphs of back-to-back launches over
+    rotating weight copies (three times L2 unless `copies` is given),
+    beside the IQ4_XS time of the main sweep; `path` names the kernel (dp4a, mma,
     tc).  Where the path is the tcgen05 kernel, `us` is its
     prepared-operand form (as in the main sweep) and `q8_form_us` the Q8_1
     form.  GB/s counts the format's weight bytes plus the Q8_1 activations
@@ -819,8 +829,9 @@ def weight_formats(torch, B, dev, stream, iq4xs_us, N=4096, K=4096, copies=48, r
         wt = B.WTYPES[name]
         w0 = torch.from_numpy(synth.block32_weights(np.random.default_rng([7, wt]), N, K,
                                                     1e-3)).to(dev)
-        ws = [w0] + [w0.clone() for _ in range(copies - 1)]
         wbytes = B.iq4xs_weight_bytes(wt, N, K)
+        ncopy = copies if copies else max(2, -(-3 * 129 * 2**20 // wbytes))  # three times L2
+        ws = [w0] + [w0.clone() for _ in range(ncopy - 1)]
         rng = np.random.default_rng(8)
         for M in ms:
             x = torch.from_numpy(synth.activations(rng, M, K)).to(dev)
@@ -848,7 +859,7 @@ def weight_formats(torch, B, dev, stream, iq4xs_us, N=4096, K=4096, copies=48, r
                         g.replay()
                     t1.record(stream)
                 torch.cuda.synchronize()
-                return t0.elapsed_time(t1) * 1e3 / (reps * copies)
+                return t0.elapsed_time(t1) * 1e3 / (reps * ncopy)
 
             q8_us = timed(lambda w: B.iq4xs_matmul_wt(w, wt, N, K, qs, ds, M, y, B.PATH_AUTO, stream))
             us = timed(lambda w: B.iq4xs_matmul_tc_operand(w, N, K, op, M, y, wt, stream=stream)) if tc else q8_us
